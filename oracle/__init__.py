@@ -1,0 +1,187 @@
+"""CPU oracle for the weight-only quantized decode GEMV (fp64, plain C).
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and
+the CPU-baseline leg of ``bench.py`` may import this package.  It shares no
+code with the CUDA library (``bit_weight_only_gb300``), and it never imports
+it.  The arithmetic lives in ``oracle.c``; this module only marshals numpy
+arrays into it.
+
+What it computes:  y[m][n] = sum_k x[m][k] * w[n][k] with w the exact fp64
+decode of the canonical packed bytes, plus the per-output bound
+B[m][n] = sum_k |x[m][k] * w[n][k]| used by the GEMV tolerance
+|y - y_ref| <= 1e-3 * B + 1e-6.  See ``oracle.c`` for the formats, the pages
+they come from and the readings taken where the pages are silent.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+Q4_0, CBK4, CBK8, PQ2_0, AQLM_2X8 = 1, 2, 3, 4, 5
+FORMATS = {"q4_0": Q4_0, "cbk4": CBK4, "cbk8": CBK8, "pq2_0": PQ2_0,
+           "aqlm_2x8": AQLM_2X8}
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        # A test may point the loader at a deliberately broken build of the
+        # same source (mutation checks of the pins); normally it is built here.
+        path = os.environ.get("ORACLE_LIB_OVERRIDE") or _build.build()
+        lib = ctypes.CDLL(path)
+        i64, c_int, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
+        lib.oracle_half_to_double.argtypes = [ctypes.c_uint16]
+        lib.oracle_half_to_double.restype = ctypes.c_double
+        lib.oracle_float_to_half.argtypes = [ctypes.c_float]
+        lib.oracle_float_to_half.restype = ctypes.c_uint16
+        lib.oracle_packed_bytes.argtypes = [c_int, i64, i64]
+        lib.oracle_packed_bytes.restype = i64
+        lib.oracle_scales_count.argtypes = [c_int, i64, i64]
+        lib.oracle_scales_count.restype = i64
+        lib.oracle_codebook_count.argtypes = [c_int]
+        lib.oracle_codebook_count.restype = i64
+        lib.oracle_dequant_row.argtypes = [c_int, i64, i64, vp, vp, vp, i64, vp]
+        lib.oracle_dequant_row.restype = c_int
+        lib.oracle_dequant.argtypes = [c_int, i64, i64, vp, vp, vp, vp]
+        lib.oracle_dequant.restype = c_int
+        lib.oracle_gemv.argtypes = [c_int, i64, i64, vp, vp, vp, vp, i64, vp, i64,
+                                    vp, vp, c_int]
+        lib.oracle_gemv.restype = c_int
+        lib.oracle_quantize_q4_0.argtypes = [vp, i64, i64, vp]
+        lib.oracle_quantize_q4_0.restype = c_int
+        _lib = lib
+    return _lib
+
+
+def _fmt(fmt) -> int:
+    return FORMATS[fmt] if isinstance(fmt, str) else int(fmt)
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _u8(a):
+    return None if a is None else np.ascontiguousarray(a).view(np.uint8).reshape(-1)
+
+
+def _u16(a):
+    if a is None:
+        return None
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.float16:
+        a = a.view(np.uint16)
+    return a.reshape(-1)
+
+
+def packed_bytes(fmt, N: int, K: int) -> int:
+    """Size in bytes of the canonical packed weights (0 if (N, K) is invalid)."""
+    return int(_load().oracle_packed_bytes(_fmt(fmt), N, K))
+
+
+def scales_count(fmt, N: int, K: int) -> int:
+    return int(_load().oracle_scales_count(_fmt(fmt), N, K))
+
+
+def codebook_count(fmt) -> int:
+    return int(_load().oracle_codebook_count(_fmt(fmt)))
+
+
+def half_to_double(bits: int) -> float:
+    return float(_load().oracle_half_to_double(int(bits) & 0xFFFF))
+
+
+def float_to_half(value: float) -> int:
+    return int(_load().oracle_float_to_half(float(value)))
+
+
+def _check(fmt, N, K, packed, scales, codebooks):
+    f = _fmt(fmt)
+    nbytes = packed_bytes(f, N, K)
+    if nbytes == 0:
+        raise ValueError(f"invalid (format, N, K) = ({fmt}, {N}, {K})")
+    p = _u8(packed)
+    if p.size != nbytes:
+        raise ValueError(f"packed has {p.size} bytes, expected {nbytes}")
+    s = _u16(scales)
+    if scales_count(f, N, K) and (s is None or s.size != scales_count(f, N, K)):
+        raise ValueError("scales missing or of the wrong size")
+    c = _u16(codebooks)
+    if codebook_count(f) and (c is None or c.size != codebook_count(f)):
+        raise ValueError("codebooks missing or of the wrong size")
+    return f, p, s, c
+
+
+def dequant(fmt, N: int, K: int, packed, scales=None, codebooks=None) -> np.ndarray:
+    """Exact fp64 decode of the whole matrix, shape [N, K]."""
+    f, p, s, c = _check(fmt, N, K, packed, scales, codebooks)
+    w = np.empty((N, K), dtype=np.float64)
+    rc = _load().oracle_dequant(f, N, K, _ptr(p), _ptr(s), _ptr(c), _ptr(w))
+    if rc:
+        raise RuntimeError(f"oracle_dequant failed ({rc})")
+    return w
+
+
+def dequant_rows(fmt, N: int, K: int, packed, scales, codebooks, rows) -> np.ndarray:
+    """Exact fp64 decode of the listed rows, shape [len(rows), K]."""
+    f, p, s, c = _check(fmt, N, K, packed, scales, codebooks)
+    rows = np.asarray(rows, dtype=np.int64)
+    out = np.empty((rows.size, K), dtype=np.float64)
+    lib = _load()
+    for i, n in enumerate(rows):
+        rc = lib.oracle_dequant_row(f, N, K, _ptr(p), _ptr(s), _ptr(c), int(n),
+                                    _ptr(out[i]))
+        if rc:
+            raise RuntimeError(f"oracle_dequant_row failed ({rc})")
+    return out
+
+
+def gemv(fmt, N: int, K: int, packed, scales, codebooks, x, rows=None,
+         nthreads: int | None = None):
+    """Reference GEMV.  x: fp16 [M, K].  Returns (y, bound), fp64 [M, len(rows)]
+    (all N rows when ``rows`` is None)."""
+    f, p, s, c = _check(fmt, N, K, packed, scales, codebooks)
+    x = np.ascontiguousarray(x, dtype=np.float16)
+    if x.ndim != 2 or x.shape[1] != K:
+        raise ValueError("x must be fp16 [M, K]")
+    M = x.shape[0]
+    if rows is None:
+        nrows, r = N, None
+    else:
+        r = np.ascontiguousarray(rows, dtype=np.int64)
+        if r.size and (r.min() < 0 or r.max() >= N):
+            raise ValueError("row index out of range")
+        nrows = r.size
+    y = np.empty((M, nrows), dtype=np.float64)
+    b = np.empty((M, nrows), dtype=np.float64)
+    if nthreads is None:
+        nthreads = os.cpu_count() or 1
+    rc = _load().oracle_gemv(f, N, K, _ptr(p), _ptr(s), _ptr(c), _ptr(_u16(x)), M,
+                             _ptr(r), nrows, _ptr(y), _ptr(b), int(nthreads))
+    if rc:
+        raise RuntimeError(f"oracle_gemv failed ({rc})")
+    return y, b
+
+
+def quantize_q4_0(w, N: int, K: int) -> np.ndarray:
+    """Q4_0 quantizer: fp32 [N, K] -> canonical blocks (uint8, N*K/32*18 bytes)."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    if w.shape != (N, K):
+        raise ValueError("w must be fp32 [N, K]")
+    out = np.empty(packed_bytes(Q4_0, N, K), dtype=np.uint8)
+    rc = _load().oracle_quantize_q4_0(_ptr(w), N, K, _ptr(out))
+    if rc:
+        raise RuntimeError(f"oracle_quantize_q4_0 failed ({rc})")
+    return out
+
+
+def within_tolerance(y, y_ref, bound, rel: float = 1e-3, abs_: float = 1e-6):
+    """Elementwise GEMV acceptance: |y - y_ref| <= rel * bound + abs."""
+    y = np.asarray(y, dtype=np.float64)
+    return np.abs(y - y_ref) <= rel * bound + abs_

@@ -1,0 +1,315 @@
+/*
+ * oracle.c -- plain, slow, fp64 CPU reference for the weight-only quantized
+ * decode GEMV
+ *
+ *     y[m][n] = sum_k x[m][k] * w[n][k],      w = dequant(packed weights)
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may link, load or
+ * call this file; only the tests, the smoke check and the CPU-baseline leg of
+ * the benchmark do.  It shares no code, header, table or constant with the
+ * CUDA library: the formats are decoded here again, from the pages' text.
+ *
+ * Every weight is decoded to an exact fp64 value, and each output is a naive
+ * left-to-right fp64 sum.  Every product x*w is exact in fp64 (an fp16 times
+ * a value with at most 24 significant bits), so the only rounding is the fp64
+ * summation itself, far below the GEMV tolerance.
+ *
+ * Sources (page title, section):
+ *   Q4_0      -- "Model quantization, read carefully" (localai blog),
+ *                sections "The ladder, with corrected numbers" and
+ *                "Anatomy of a block": blocks of 32 weights, one fp16 scale,
+ *                4.5 bits per weight, decode = stored integer times scale.
+ *                Value (q-8)*d and the quantizer d = signed-max/-8,
+ *                q = clamp(round(w/d)+8, 0..15) follow the ggml convention.
+ *   CBK4/CBK8 -- "Trapetum benchmarks", sections "Kernel microbenchmarks"
+ *                (4-bit index into K = 16 centroids, uint8 index into 256) and
+ *                "Model-level results"; one codebook per projection.
+ *   PQ2_0     -- "Making a ternary reasoning model fast in vLLM", section
+ *                "Anatomy of a PQ2_0 block": {half d; uint8 qs[32]}, 34 bytes
+ *                per 128 weights, codes 0/1/2/3 -> -1/0/+1/+2, two-bit fields
+ *                read from the low end of each byte.
+ *   AQLM 2x8  -- "Trapetum benchmarks", sections "Additive vector-quantization
+ *                GEMV" and "Llama-2-70B in 2 bits": per group of 8 weights
+ *                two uint8 codes into two 256x8 fp16 codebooks, summed, and a
+ *                per-output-row scale.
+ *
+ * Readings where the pages are silent (each also listed in the design notes):
+ *   R1 Q4_0 nibble order: byte i of a block holds element i in its low nibble
+ *      and element i+16 in its high nibble (the ggml convention).
+ *   R2 Q4_0 quantizer: w/d is an IEEE fp32 division, round() is round half
+ *      away from zero, q uses the fp32 d, and d is stored as fp16 (ties to
+ *      even).  An all-zero block (d = 0) stores q = 8 everywhere.
+ *   R3 CBK4 index layout: row-major [N][K/2]; byte j of row n holds k = 2j in
+ *      its low nibble and k = 2j+1 in its high nibble.  CBK8: [N][K], one byte
+ *      per weight.
+ *   R4 PQ2_0: byte j of a block holds elements 4j..4j+3, lowest bits first.
+ *   R5 AQLM 2x8: codes [N][K/8][2] (codebook 0 first), codebooks [2][256][8]
+ *      fp16, one fp16 scale per output row multiplying the summed vector.
+ *   All multi-byte values are little-endian.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_Q4_0 1
+#define ORACLE_CBK4 2
+#define ORACLE_CBK8 3
+#define ORACLE_PQ2_0 4
+#define ORACLE_AQLM_2X8 5
+
+#define ORACLE_OK 0
+#define ORACLE_ERR_ARG 1
+#define ORACLE_ERR_NOMEM 2
+
+/* ---------------------------------------------------------------- fp16 ---- */
+
+/* IEEE 754 binary16 -> double, straight from the definition:
+ *   exponent 0     : (-1)^s * mant * 2^-24            (subnormal / zero)
+ *   exponent 1..30 : (-1)^s * (1024 + mant) * 2^(e-25)
+ *   exponent 31    : infinity (mant == 0) or NaN.                           */
+double oracle_half_to_double(uint16_t h) {
+  int s = (h >> 15) & 1;
+  int e = (h >> 10) & 0x1f;
+  int mant = h & 0x3ff;
+  double v;
+  if (e == 0)
+    v = ldexp((double)mant, -24);
+  else if (e == 31)
+    v = mant ? NAN : INFINITY;
+  else
+    v = ldexp((double)(1024 + mant), e - 25);
+  return s ? -v : v;
+}
+
+/* float -> nearest binary16, ties to even, from the definition.  The float is
+ * exact in double; its binary16 significand is computed by scaling and
+ * rint() (which rounds to nearest even in the default rounding mode).       */
+uint16_t oracle_float_to_half(float f) {
+  double a = fabs((double)f);
+  uint16_t sign = signbit(f) ? 0x8000 : 0;
+  if (isnan(f)) return (uint16_t)(sign | 0x7e00);
+  if (isinf(f)) return (uint16_t)(sign | 0x7c00);
+  if (a == 0.0) return sign;
+  int ex;
+  frexp(a, &ex);            /* a = fr * 2^ex, fr in [0.5, 1) */
+  int E = ex - 1;           /* a = 1.xxx * 2^E               */
+  if (E < -14) {            /* subnormal range: multiples of 2^-24 */
+    double S = rint(ldexp(a, 24));
+    /* S == 1024 is the smallest normal, whose bit pattern is 0x0400 too */
+    return (uint16_t)(sign | (uint16_t)S);
+  }
+  double S = rint(ldexp(a, 10 - E)); /* 1024 <= S <= 2048 */
+  if (S >= 2048.0) {
+    S = 1024.0;
+    E += 1;
+  }
+  if (E > 15) return (uint16_t)(sign | 0x7c00);
+  return (uint16_t)(sign | (uint16_t)((E + 15) << 10) | (uint16_t)(S - 1024.0));
+}
+
+static uint16_t rd16(const uint8_t* p) { return (uint16_t)(p[0] | (p[1] << 8)); }
+
+/* ---------------------------------------------------------- byte sizes ---- */
+
+/* Bytes of the canonical inputs; returns 0 for an invalid (fmt, N, K). */
+int64_t oracle_packed_bytes(int fmt, int64_t N, int64_t K) {
+  if (N <= 0 || K <= 0) return 0;
+  switch (fmt) {
+    case ORACLE_Q4_0: return (K % 32) ? 0 : N * (K / 32) * 18;
+    case ORACLE_CBK4: return (K % 2) ? 0 : N * (K / 2);
+    case ORACLE_CBK8: return N * K;
+    case ORACLE_PQ2_0: return (K % 128) ? 0 : N * (K / 128) * 34;
+    case ORACLE_AQLM_2X8: return (K % 8) ? 0 : N * (K / 8) * 2;
+  }
+  return 0;
+}
+
+/* Number of fp16 values in the `scales` input. */
+int64_t oracle_scales_count(int fmt, int64_t N, int64_t K) {
+  (void)K;
+  return fmt == ORACLE_AQLM_2X8 ? N : 0;
+}
+
+/* Number of fp16 values in the `codebooks` input. */
+int64_t oracle_codebook_count(int fmt) {
+  switch (fmt) {
+    case ORACLE_CBK4: return 16;
+    case ORACLE_CBK8: return 256;
+    case ORACLE_AQLM_2X8: return 2 * 256 * 8;
+  }
+  return 0;
+}
+
+/* ------------------------------------------------------------- dequant ---- */
+
+/* Decode output row n (K weights) into w[0..K-1], exactly, in fp64. */
+int oracle_dequant_row(int fmt, int64_t N, int64_t K, const uint8_t* packed,
+                       const uint16_t* scales, const uint16_t* codebooks,
+                       int64_t n, double* w) {
+  if (oracle_packed_bytes(fmt, N, K) == 0 || n < 0 || n >= N || !packed || !w)
+    return ORACLE_ERR_ARG;
+  if ((fmt == ORACLE_CBK4 || fmt == ORACLE_CBK8 || fmt == ORACLE_AQLM_2X8) && !codebooks)
+    return ORACLE_ERR_ARG;
+  if (fmt == ORACLE_AQLM_2X8 && !scales) return ORACLE_ERR_ARG;
+
+  if (fmt == ORACLE_Q4_0) {
+    /* block = { fp16 d ; uint8 qs[16] }, 18 bytes, 32 weights; value (q-8)*d */
+    int64_t nb = K / 32;
+    for (int64_t b = 0; b < nb; ++b) {
+      const uint8_t* blk = packed + (n * nb + b) * 18;
+      double d = oracle_half_to_double(rd16(blk));
+      const uint8_t* qs = blk + 2;
+      for (int i = 0; i < 16; ++i) {
+        int lo = qs[i] & 0x0f; /* element i      (reading R1) */
+        int hi = qs[i] >> 4;   /* element i + 16 (reading R1) */
+        w[b * 32 + i] = (double)(lo - 8) * d;
+        w[b * 32 + i + 16] = (double)(hi - 8) * d;
+      }
+    }
+  } else if (fmt == ORACLE_CBK4) {
+    /* 4-bit index into 16 centroids, two indices per byte (reading R3) */
+    const uint8_t* row = packed + n * (K / 2);
+    for (int64_t j = 0; j < K / 2; ++j) {
+      w[2 * j] = oracle_half_to_double(codebooks[row[j] & 0x0f]);
+      w[2 * j + 1] = oracle_half_to_double(codebooks[row[j] >> 4]);
+    }
+  } else if (fmt == ORACLE_CBK8) {
+    /* 8-bit index into 256 centroids */
+    const uint8_t* row = packed + n * K;
+    for (int64_t k = 0; k < K; ++k) w[k] = oracle_half_to_double(codebooks[row[k]]);
+  } else if (fmt == ORACLE_PQ2_0) {
+    /* block = { fp16 d ; uint8 qs[32] }, 34 bytes, 128 weights;
+     * code c = 2-bit field, value (c - 1) * d: 0,1,2,3 -> -1,0,+1,+2      */
+    int64_t nb = K / 128;
+    for (int64_t b = 0; b < nb; ++b) {
+      const uint8_t* blk = packed + (n * nb + b) * 34;
+      double d = oracle_half_to_double(rd16(blk));
+      const uint8_t* qs = blk + 2;
+      for (int e = 0; e < 128; ++e) {
+        int c = (qs[e / 4] >> (2 * (e % 4))) & 3; /* reading R4 */
+        w[b * 128 + e] = (double)(c - 1) * d;
+      }
+    }
+  } else { /* ORACLE_AQLM_2X8 */
+    /* w[n][8g+j] = s_n * (C0[code0][j] + C1[code1][j])   (reading R5)     */
+    int64_t ng = K / 8;
+    double s = oracle_half_to_double(scales[n]);
+    for (int64_t g = 0; g < ng; ++g) {
+      int a = packed[(n * ng + g) * 2 + 0];
+      int b = packed[(n * ng + g) * 2 + 1];
+      for (int j = 0; j < 8; ++j) {
+        double c0 = oracle_half_to_double(codebooks[(0 * 256 + a) * 8 + j]);
+        double c1 = oracle_half_to_double(codebooks[(1 * 256 + b) * 8 + j]);
+        w[g * 8 + j] = s * (c0 + c1);
+      }
+    }
+  }
+  return ORACLE_OK;
+}
+
+/* Decode the whole matrix: w is [N][K] row-major. */
+int oracle_dequant(int fmt, int64_t N, int64_t K, const uint8_t* packed,
+                   const uint16_t* scales, const uint16_t* codebooks, double* w) {
+  for (int64_t n = 0; n < N; ++n) {
+    int rc = oracle_dequant_row(fmt, N, K, packed, scales, codebooks, n, w + n * K);
+    if (rc) return rc;
+  }
+  return ORACLE_OK;
+}
+
+/* ---------------------------------------------------------------- GEMV ---- */
+
+/* y[m][r] = sum_k x[m][k] * w[rows[r]][k]  and  bound[m][r] = sum_k |x*w|,
+ * for the `nrows` output rows listed in `rows` (all N rows when rows == NULL,
+ * in which case nrows must equal N).  x is fp16 [M][K] row-major; y and bound
+ * are fp64 [M][nrows].  nthreads > 1 spreads the rows over OpenMP threads;
+ * each output is still one left-to-right sum.                               */
+int oracle_gemv(int fmt, int64_t N, int64_t K, const uint8_t* packed,
+                const uint16_t* scales, const uint16_t* codebooks,
+                const uint16_t* x, int64_t M, const int64_t* rows, int64_t nrows,
+                double* y, double* bound, int nthreads) {
+  if (oracle_packed_bytes(fmt, N, K) == 0 || M <= 0 || !x || !y) return ORACLE_ERR_ARG;
+  if (!rows && nrows != N) return ORACLE_ERR_ARG;
+  double* xd = (double*)malloc(sizeof(double) * (size_t)(M * K));
+  if (!xd) return ORACLE_ERR_NOMEM;
+  for (int64_t i = 0; i < M * K; ++i) xd[i] = oracle_half_to_double(x[i]);
+
+  int rc_all = ORACLE_OK;
+#if defined(_OPENMP)
+#pragma omp parallel num_threads(nthreads > 0 ? nthreads : 1)
+#endif
+  {
+    double* w = (double*)malloc(sizeof(double) * (size_t)K);
+#if defined(_OPENMP)
+#pragma omp for schedule(dynamic, 4)
+#endif
+    for (int64_t r = 0; r < nrows; ++r) {
+      int64_t n = rows ? rows[r] : r;
+      int rc = w ? oracle_dequant_row(fmt, N, K, packed, scales, codebooks, n, w)
+                 : ORACLE_ERR_NOMEM;
+      if (rc) {
+#if defined(_OPENMP)
+#pragma omp critical
+#endif
+        rc_all = rc;
+        continue;
+      }
+      for (int64_t m = 0; m < M; ++m) {
+        double s = 0.0, b = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+          double t = xd[m * K + k] * w[k];
+          s += t;
+          b += fabs(t);
+        }
+        y[m * nrows + r] = s;
+        if (bound) bound[m * nrows + r] = b;
+      }
+    }
+    free(w);
+  }
+  free(xd);
+  return rc_all;
+}
+
+/* ----------------------------------------------------------- quantizer ---- */
+
+/* Q4_0 quantizer (reading R2), fp32 weights [N][K] -> canonical blocks.
+ * Per block of 32 weights along K:
+ *   amax = the weight of largest magnitude, with its sign (first one on ties)
+ *   d    = amax / -8                       (fp32)
+ *   q_i  = clamp(round(w_i / d) + 8, 0, 15) (fp32 division, half away from 0)
+ *   store fp16(d) little-endian, then qs[i] = q_i | q_(i+16) << 4.         */
+int oracle_quantize_q4_0(const float* wf, int64_t N, int64_t K, uint8_t* out) {
+  if (!wf || !out || N <= 0 || K <= 0 || K % 32) return ORACLE_ERR_ARG;
+  int64_t nb = K / 32;
+  for (int64_t n = 0; n < N; ++n) {
+    for (int64_t b = 0; b < nb; ++b) {
+      const float* v = wf + n * K + b * 32;
+      float amax = 0.0f, absmax = 0.0f;
+      for (int i = 0; i < 32; ++i) {
+        if (fabsf(v[i]) > absmax) {
+          absmax = fabsf(v[i]);
+          amax = v[i];
+        }
+      }
+      float d = amax / -8.0f;
+      int q[32];
+      for (int i = 0; i < 32; ++i) {
+        if (d == 0.0f) {
+          q[i] = 8;
+        } else {
+          float r = roundf(v[i] / d);
+          int qi = (int)r + 8;
+          q[i] = qi < 0 ? 0 : (qi > 15 ? 15 : qi);
+        }
+      }
+      uint8_t* blk = out + (n * nb + b) * 18;
+      uint16_t h = oracle_float_to_half(d);
+      blk[0] = (uint8_t)(h & 0xff);
+      blk[1] = (uint8_t)(h >> 8);
+      for (int i = 0; i < 16; ++i) blk[2 + i] = (uint8_t)(q[i] | (q[i + 16] << 4));
+    }
+  }
+  return ORACLE_OK;
+}
