@@ -1,0 +1,483 @@
+"""Benchmark of the weight-only quantized decode GEMV on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--m M]
+
+One JSON line on rank 0 (stdout); everything else goes to stderr.
+
+Default workload ("cbk4_7b_stack"): the projection stack of a 32-layer 7B
+decoder -- per layer q/k/v/o 4096x4096, gate/up 11008x4096, down 4096x11008
+(224 projections, 4-bit scalar codebook, 16 fp16 centroids each) plus a
+32000x4096 LM head with an 8-bit codebook (256 centroids) -- at M = 1.  One
+step is one token: all 225 GEMVs, replayed as CUDA graphs.  The stack is
+3.37 GB of packed weights, far larger than L2, so no flush is needed.
+Inputs are synthetic and seeded (see bit_weight_only_gb300/inputs.py).
+
+The metric is the achieved weight-stream bandwidth: algorithmic bytes
+(packed weights + codebooks/scales + x + y) per step / device time per step.
+
+--impl reference times the CPU oracle (fp64, plain C, this repository's
+test reference) on a bounded sample of the same workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Quantized decode GEMV achieved HBM GB/s & % of GB300 peak, M=1..16"
+UNIT = "GB/s"
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def measured_peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except Exception:
+        return None
+
+
+def hbm_peak():
+    p = measured_peaks()
+    if p and p.get("hbm_gbs"):
+        return float(p["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "bit_weight_only_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(f.encode())
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+# ----------------------------------------------------------- workloads ----
+
+LLAMA7B = [("q", 4096, 4096), ("k", 4096, 4096), ("v", 4096, 4096), ("o", 4096, 4096),
+           ("gate", 11008, 4096), ("up", 11008, 4096), ("down", 4096, 11008)]
+
+
+def cbk4_stack_specs(layers=32):
+    specs = []
+    for layer in range(layers):
+        for name, N, K in LLAMA7B:
+            specs.append(("cbk4", f"L{layer}.{name}", N, K))
+    specs.append(("cbk8", "lm_head", 32000, 4096))
+    return specs
+
+
+WORKLOADS = {
+    # name: (specs, dominant format, description)
+    "cbk4_7b_stack": (lambda: cbk4_stack_specs(), "cbk4",
+                      "7B decoder projection stack, 224 x CBK4 + CBK8 LM head 32000x4096"),
+    "q4_0_4096": (lambda: [("q4_0", "q4_0", 4096, 4096)], "q4_0", "Q4_0 GEMV 4096x4096"),
+    "q4_0_down": (lambda: [("q4_0", "down", 8192, 28672)], "q4_0", "Q4_0 down 8192x28672"),
+    "pq2_5120": (lambda: [("pq2_0", "gate_up", 34816, 5120), ("pq2_0", "down", 5120, 17408)],
+                 "pq2_0", "PQ2_0 gate+up 34816x5120 and down 5120x17408"),
+    "pq2_down": (lambda: [("pq2_0", "down", 8192, 28672)], "pq2_0", "PQ2_0 down 8192x28672"),
+    "cbk4_down": (lambda: [("cbk4", "down", 8192, 28672)], "cbk4", "CBK4 down 8192x28672"),
+    "cbk8_head": (lambda: [("cbk8", "lm_head", 32000, 4096)], "cbk8", "CBK8 LM head 32000x4096"),
+}
+
+
+def canonical_extra_bytes(fmt, N):
+    return {"q4_0": 0, "pq2_0": 0, "cbk4": 32, "cbk8": 512, "aqlm_2x8": 2 * N + 8192}[fmt]
+
+
+def build_handles(specs, M, device, seed=0):
+    """Create one handle per projection from device-drawn canonical inputs."""
+    import torch
+    from bit_weight_only_gb300 import inputs, qgemv
+    ops = []
+    # all activations in one buffer and all outputs in another, so the end to
+    # end run moves one input copy and one output copy per step
+    x_all = torch.empty(sum(M * K for _, _, _, K in specs), dtype=torch.float16, device=device)
+    y_all = torch.empty(sum(M * N for _, _, N, _ in specs), dtype=torch.float32, device=device)
+    xo = yo = 0
+    c16 = inputs.cbk_centroids(16)
+    c256 = inputs.cbk_centroids(256)
+    p16, p256 = inputs.cbk_cell_probs(c16), inputs.cbk_cell_probs(c256)
+    for fmt, name, N, K in specs:
+        tag = f"bench/{name}"
+        scales = cb = None
+        if fmt == "cbk4":
+            packed = inputs.cbk_packed_cuda(tag, N, K, 4, p16, device, seed)
+            cb = c16
+        elif fmt == "cbk8":
+            packed = inputs.cbk_packed_cuda(tag, N, K, 8, p256, device, seed)
+            cb = c256
+        elif fmt == "pq2_0":
+            packed = inputs.pq2_packed_cuda(tag, N, K, device=device, seed=seed)
+        elif fmt == "q4_0":
+            w = inputs.w_fp32_cuda(tag, N, K, device=device, seed=seed)
+            packed = qgemv.quantize_q4_0(w)
+            del w
+        elif fmt == "aqlm_2x8":
+            packed, scales, cb = inputs.aqlm_inputs_cuda(tag, N, K, device=device, seed=seed)
+        else:
+            raise ValueError(fmt)
+        h = qgemv.QGemv(fmt, N, K, packed, scales, cb)
+        del packed
+        x = x_all[xo:xo + M * K].view(M, K)
+        x.copy_(inputs.x_fp16_cuda(f"{tag}/x", M, K, device=device, seed=seed))
+        y = y_all[yo:yo + M * N].view(M, N)
+        xo += M * K
+        yo += M * N
+        nbytes = qgemv.qgemv_packed_bytes(fmt, N, K) + canonical_extra_bytes(fmt, N) + 2 * M * K + 4 * M * N
+        ops.append({"fmt": fmt, "name": name, "N": N, "K": K, "h": h, "x": x, "y": y,
+                    "bytes": nbytes})
+    torch.cuda.synchronize()
+    return ops, x_all, y_all
+
+
+# ---------------------------------------------------------------- clocks --
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"qgemv_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() in ("active", "0x1", "1"):
+                    reasons.add(nm)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------- our arm ------
+
+def run_ours(args, rank, world, device):
+    import torch
+    from bit_weight_only_gb300 import build, qgemv
+    build.build()            # compiles only if sources changed
+    qgemv.load()             # fails loudly without the library
+
+    specs_fn, dominant, desc = WORKLOADS[args.workload]
+    M = args.m
+    t_setup = time.time()
+    ops, x_all, y_all = build_handles(specs_fn(), M, device)
+    log(f"[bench] rank {rank}: {len(ops)} GEMVs ready in {time.time() - t_setup:.1f}s")
+
+    dom = [o for o in ops if o["fmt"] == dominant]
+    rest = [o for o in ops if o["fmt"] != dominant]
+    step_bytes = sum(o["bytes"] for o in ops)
+    dom_bytes = sum(o["bytes"] for o in dom)
+
+    stream = torch.cuda.Stream(device=device)
+    graphs = []
+    for group in (dom, rest):
+        if not group:
+            graphs.append(None)
+            continue
+        g = torch.cuda.CUDAGraph()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            for o in group:
+                o["h"].run(o["x"], o["y"], stream=torch.cuda.current_stream())
+        graphs.append(g)
+    g_dom, g_rest = graphs
+
+    def step():
+        g_dom.replay()
+        if g_rest is not None:
+            g_rest.replay()
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize()
+    for o in ops:
+        o["h"].status()
+
+    if world > 1:
+        torch.distributed.barrier()
+    sampler = ClockSampler(device.index if device.index is not None else 0)
+    sampler.start()
+    time.sleep(0.3)
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for k in range(K):
+            ev[k][0].record(stream)
+            g_dom.replay()
+            ev[k][1].record(stream)
+            if g_rest is not None:
+                g_rest.replay()
+        end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    total_ms = start.elapsed_time(end)
+    dom_ms = sum(a.elapsed_time(b) for a, b in ev)
+    for o in ops:
+        o["h"].status()
+
+    # End to end: every step copies all activations in from pinned host
+    # memory, runs the same API calls (graph-replayed) and reads the last
+    # GEMV's output (the LM head logits for the stack) back to pinned host
+    # memory, then synchronizes, as a decode loop that needs its logits would.
+    x_host = torch.empty_like(x_all, device="cpu").pin_memory()
+    x_host.copy_(x_all)
+    y_last = ops[-1]["y"]
+    y_host = torch.empty_like(y_last, device="cpu").pin_memory()
+    h2d = x_host.numel() * x_host.element_size()
+    d2h = y_host.numel() * y_host.element_size()
+    K_e2e = max(1, min(K, 500))
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for _ in range(K_e2e):
+            x_all.copy_(x_host, non_blocking=True)
+            step()
+            y_host.copy_(y_last, non_blocking=True)
+            stream.synchronize()
+    e2e_s = time.perf_counter() - t0
+
+    t = torch.tensor([total_ms, dom_ms, e2e_s], dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    total_ms, dom_ms, e2e_s = t.tolist()
+    if rank != 0:
+        return None
+
+    ms_step = total_ms / K
+    value = world * step_bytes / (ms_step * 1e-3) / 1e9
+    peak, peak_kind = hbm_peak()
+    dom_launches = len(dom)
+    dom_achieved = dom_bytes / (dom_ms / K * 1e-3) / 1e9
+    traffic = None
+    prof = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(prof):
+        try:
+            pj = json.load(open(prof))
+            entry = pj.get(args.workload)
+            if entry and entry.get("kernel_source_hash") == kernel_source_hash():
+                traffic = entry.get("dram_bytes_per_launch")
+        except Exception:
+            traffic = None
+    e2e_value = world * step_bytes * K_e2e / e2e_s / 1e9
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "description": desc, "M": M,
+                   "gemvs_per_step": len(ops), "bytes_per_step": step_bytes,
+                   "l2": "weights larger than L2 (no flush needed)" if step_bytes > 4 * 135e6
+                   else "weights rotate through L2 (smaller than 4x L2)",
+                   "parallelism": f"replicas{world}", "peak_hbm_gbs": peak,
+                   "frac_of_peak": round(value / world / peak, 4)},
+        "roofline": {"bound": "hbm", "kernel": f"gemv_kernel<{dominant}, M={M}>",
+                     "achieved": round(dom_achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(dom_achieved / peak, 4), "peak_kind": peak_kind,
+                     "traffic": traffic,
+                     "bytes_per_launch": dom_bytes / max(1, dom_launches),
+                     "avg_launch_us": round(dom_ms / K / max(1, dom_launches) * 1e3, 3)},
+        "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": K_e2e},
+        "gpu_launches": len(ops) * K,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(args.workload, M, budget_s=args.cpu_seconds)
+    return line
+
+
+# ---------------------------------------------------- oracle (CPU) arm ----
+
+def oracle_sample(workload, M, rows, seed=0):
+    """Host inputs for `rows` rows of the workload's first dominant matrix."""
+    from bit_weight_only_gb300 import inputs
+    specs_fn, dominant, _ = WORKLOADS[workload]
+    fmt, name, N, K = next(s for s in specs_fn() if s[0] == dominant)
+    rows = min(rows, N)
+    g = inputs.rng(f"cpu/{name}", seed)
+    scales = cb = None
+    if fmt == "cbk4":
+        cb = inputs.cbk_centroids(16)
+        packed = inputs.cbk_packed(g, rows, K, 4, inputs.cbk_cell_probs(cb))
+    elif fmt == "cbk8":
+        cb = inputs.cbk_centroids(256)
+        packed = inputs.cbk_packed(g, rows, K, 8, inputs.cbk_cell_probs(cb))
+    elif fmt == "pq2_0":
+        packed = inputs.pq2_packed(g, rows, K)
+    elif fmt == "q4_0":
+        packed = inputs.q4_0_random_blocks(g, rows, K)
+    else:
+        packed, scales, cb = inputs.aqlm_inputs(g, rows, K)
+    x = inputs.x_fp16(inputs.rng("cpu/x", seed), M, K)
+    nbytes = (packed.nbytes + (0 if scales is None else scales.nbytes)
+              + (0 if cb is None else cb.nbytes) + x.nbytes + 4 * M * rows)
+    return fmt, name, rows, K, packed, scales, cb, x, nbytes
+
+
+def time_oracle(workload, M, rows, threads, reps=1):
+    import oracle
+    fmt, name, rows, K, packed, scales, cb, x, nbytes = oracle_sample(workload, M, rows)
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle.gemv(fmt, rows, K, packed, scales, cb, x, nthreads=threads)
+    dt = time.perf_counter() - t0
+    return dt, nbytes * reps, f"{reps} x {rows} rows of {name} ({fmt}, K={K}), M={M}"
+
+
+def cpu_baseline(workload, M, budget_s=15.0):
+    """The oracle as it stands on the host cores, on a bounded sample (about
+    budget_s seconds of work: repeated passes over rows of the workload's
+    first matrix)."""
+    threads = os.cpu_count() or 1
+    rows, reps = 256, 1
+    dt, nbytes, desc = time_oracle(workload, M, rows, threads, reps)
+    while dt < budget_s / 2:
+        if rows < 4096:
+            rows *= 4
+        else:
+            reps = max(reps * 2, int(reps * budget_s / max(dt, 1e-3) * 0.6))
+        dt, nbytes, desc = time_oracle(workload, M, rows, threads, reps)
+    return {"value": round(nbytes / dt / 1e9, 4), "unit": UNIT, "cores": threads,
+            "kind": "oracle", "sample": desc, "seconds": round(dt, 3)}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    threads = os.cpu_count() or 1
+    total_budget = args.cpu_seconds * 4
+    per_step = max(0.05, total_budget / max(1, args.steps + args.warmup))
+    rows = 64
+    dt, nbytes, desc = time_oracle(args.workload, args.m, rows, threads)
+    while dt < per_step / 2 and rows < 65536:
+        rows *= 2
+        dt, nbytes, desc = time_oracle(args.workload, args.m, rows, threads)
+    for _ in range(args.warmup):
+        time_oracle(args.workload, args.m, rows, threads)
+    times = []
+    for _ in range(args.steps):
+        dt, nbytes, desc = time_oracle(args.workload, args.m, rows, threads)
+        times.append(dt)
+    tot = sum(times)
+    value = nbytes * len(times) / tot / 1e9
+    specs_fn, dominant, wdesc = WORKLOADS[args.workload]
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(tot / len(times) * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "description": wdesc, "M": args.m,
+                   "parallelism": f"replicas{world}"},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": threads,
+                         "kind": "oracle", "sample": desc},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+# ------------------------------------------------------------------ main --
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="cbk4_7b_stack")
+    ap.add_argument("--m", type=int, default=1)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+
+    import torch
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=device)
+    line = run_ours(args, rank, world, device)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,281 @@
+// fmt_cbk.cuh -- scalar codebook formats: CBK4 (4-bit index into 16 fp16
+// centroids) and CBK8 (8-bit index into 256 fp16 centroids), one codebook
+// per matrix ("Trapetum benchmarks", sections "Kernel microbenchmarks" and
+// "Model-level results"; the 8-bit table is the LM head's).
+//
+// Decode: a table lookup in shared memory per index byte.  The table is
+// replicated once per lane (entry e of lane l at byte e*256 + l*4), so the 32
+// lanes of a warp always hit 32 different banks whatever their indices, and
+// the byte offset of an entry is built from the index byte with one PRMT
+// (index byte -> bits 8..15, lane*4 -> bits 0..7).
+//   CBK4: one byte = two indices (k even in the low nibble, k odd in the
+//         high nibble); the entry is the fp16 pair (c[lo], c[hi]), and the
+//         products with the fp16 activations accumulate in fp32 with the
+//         mixed-precision FMA (f16 x f16 + f32; the product is exact).
+//   CBK8: one byte = one index; the entry is c[idx] as fp32 and pairs of k
+//         accumulate with FFMA2 against fp32 activation pairs.
+#pragma once
+
+#include "gemv_kernel.cuh"
+
+namespace qgemv {
+
+constexpr int kLutBytes = 256 * 256;  // 256 entries x 64 four-byte slots
+
+// byte offset in the lane-replicated table of index byte `bsel` (0..3) of w
+__device__ __forceinline__ uint32_t lut_offset(uint32_t w, uint32_t lane4, int bsel) {
+  // result bytes: [0] = lane4.b0, [1] = w.b(bsel), [2] = [3] = lane4.b1 (= 0)
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(lane4), "r"(w), "r"(0x1100u | ((4u + bsel) << 4)));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t lds32(const uint8_t* base, uint32_t off) {
+  return *reinterpret_cast<const uint32_t*>(base + off);
+}
+
+// d = a.lo * b.lo + (a.hi * b.hi + c)   (f16 x f16 products, f32 accumulation)
+__device__ __forceinline__ float fma2_f16_f32(uint32_t a2, uint32_t b2, float c) {
+  float d;
+  asm("{\n\t.reg .f16 al, ah, bl, bh;\n\t.reg .f32 t;\n\t"
+      "mov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+      "fma.rn.f32.f16 t, ah, bh, %3;\n\t"
+      "fma.rn.f32.f16 %0, al, bl, t;\n\t}"
+      : "=f"(d)
+      : "r"(a2), "r"(b2), "f"(c));
+  return d;
+}
+
+// ------------------------------------------------------------------ CBK4 --
+//
+// Tile: 128 rows x 256 k.  Warp w <-> k slice 32w..32w+31, lane l <-> rows
+// 4l..4l+3.  codes [j][t = w*32 + l][16 B]: the 16 canonical index bytes of
+// row 4l+j for the slice (byte b = k pair b: low nibble k = 2b, high 2b+1).
+// Activations are staged as fp16 pairs: xs word (q * MP + m) = (x[2q][m],
+// x[2q+1][m]).
+struct FmtCBK4 {
+  static constexpr int kKW = 32;
+  static constexpr int kKT = kKW * kSlices;                          // 256
+  static constexpr int kTileBytes = kLaneSlots * kRowsPerLane * 16;  // 16384
+  __host__ __device__ static constexpr int stages(int M) { return M <= 8 ? 6 : 4; }
+  static constexpr int kSharedBytes = kLutBytes;
+  static constexpr float kOutScale = 1.0f;
+  using XRegs = XRegsT<1>;
+
+  __device__ static void init_shared(uint8_t* lut, const GemvParams& p, int tid, int nthreads) {
+    const uint16_t* cb = static_cast<const uint16_t*>(p.aux);
+    for (int i = tid; i < 256 * 32; i += nthreads) {
+      const int e = i >> 5, l = i & 31;
+      const uint32_t v = static_cast<uint32_t>(cb[e & 15]) | (static_cast<uint32_t>(cb[e >> 4]) << 16);
+      *reinterpret_cast<uint32_t*>(lut + e * 256 + l * 4) = v;
+    }
+  }
+
+  template <int M>
+  __device__ static void load_x(XRegs& xr, const GemvParams& p, int kt, int slice, int lane) {
+    load_x_slice<kKW, M, 1>(xr, p, kt, slice, lane);
+  }
+
+  // fp16 pairs, no scaling; no block sums needed
+  template <int M>
+  __device__ static void stage_x(float* xs, float (&)[M], const XRegs& xr, int lane) {
+    constexpr int MP = mpad(M);
+    uint16_t* xh = reinterpret_cast<uint16_t*>(xs);
+#pragma unroll
+    for (int m = 0; m < MP; ++m) xh[((lane >> 1) * MP + m) * 2 + (lane & 1)] = m < M ? xr.v[m][0] : 0;
+  }
+
+  template <int M, int RPW>
+  __device__ static void tile_math(const uint8_t* stage, const float* xs, const float (&)[M],
+                                   RowAcc<M, RPW>& yacc, uint8_t* lut, int slice, int half,
+                                   int lane, uint64_t* empty_bar) {
+    constexpr int MP = mpad(M);
+    const int t = slice * 32 + lane;
+    const int j0 = half * RPW;
+    uint4 cwd[RPW];
+#pragma unroll
+    for (int j = 0; j < RPW; ++j) cwd[j] = lds128(stage + ((j0 + j) * kLaneSlots + t) * 16);
+    release_stage(empty_bar, lane);
+    const uint32_t lane4 = static_cast<uint32_t>(lane) << 2;
+    const uint32_t* xw = reinterpret_cast<const uint32_t*>(xs);
+
+    float acc[RPW][M];
+#pragma unroll
+    for (int j = 0; j < RPW; ++j)
+#pragma unroll
+      for (int m = 0; m < M; ++m) acc[j][m] = 0.f;
+    constexpr int UI = (M > 8) ? 1 : 4;
+#pragma unroll UI
+    for (int i = 0; i < 4; ++i) {     // word i: k pairs 4i..4i+3
+#pragma unroll
+      for (int bp = 0; bp < 4; ++bp) {
+        const int q = 4 * i + bp;
+        uint32_t xp[M];
+        if constexpr (M == 1) {
+          xp[0] = xw[q];
+        } else {
+#pragma unroll
+          for (int m = 0; m < MP; m += 2) {
+            const uint2 v = *reinterpret_cast<const uint2*>(xw + q * MP + m);
+            if (m < M) xp[m] = v.x;
+            if (m + 1 < M) xp[m + 1] = v.y;
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < RPW; ++j) {
+          const uint32_t wv = word_of(cwd[j], i);
+          const uint32_t c2 = lds32(lut, lut_offset(wv, lane4, bp));
+#pragma unroll
+          for (int m = 0; m < M; ++m) acc[j][m] = fma2_f16_f32(c2, xp[m], acc[j][m]);
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < RPW; ++j) yacc.add_row(j, 1.0f, acc[j]);
+  }
+};
+
+// ------------------------------------------------------------------ CBK8 --
+//
+// Tile: 128 rows x 128 k.  Warp w <-> k slice 16w..16w+15 (lanes 0..15 stage
+// one activation each), lane l <-> rows 4l..4l+3.  codes [j][t][16 B]: the 16
+// canonical index bytes of row 4l+j for the slice.  Activations are staged
+// as fp32 pairs (x[2q][m], x[2q+1][m]).
+struct FmtCBK8 {
+  static constexpr int kKW = 16;
+  static constexpr int kKT = kKW * kSlices;                          // 128
+  static constexpr int kTileBytes = kLaneSlots * kRowsPerLane * 16;  // 16384
+  __host__ __device__ static constexpr int stages(int M) { return M <= 8 ? 6 : 4; }
+  static constexpr int kSharedBytes = kLutBytes;
+  static constexpr float kOutScale = 1.0f;
+  using XRegs = XRegsT<1>;
+
+  __device__ static void init_shared(uint8_t* lut, const GemvParams& p, int tid, int nthreads) {
+    const uint16_t* cb = static_cast<const uint16_t*>(p.aux);
+    for (int i = tid; i < 256 * 32; i += nthreads) {
+      const int e = i >> 5, l = i & 31;
+      *reinterpret_cast<float*>(lut + e * 256 + l * 4) = h2f(cb[e]);
+    }
+  }
+
+  template <int M>
+  __device__ static void load_x(XRegs& xr, const GemvParams& p, int kt, int slice, int lane) {
+    const int64_t k = static_cast<int64_t>(kt) * kKT + slice * kKW + lane;
+    const unsigned short* xb = reinterpret_cast<const unsigned short*>(p.x);
+#pragma unroll
+    for (int m = 0; m < M; ++m)
+      xr.v[m][0] = (lane < kKW && k < p.K) ? __ldg(xb + m * p.K + k) : static_cast<unsigned short>(0);
+  }
+
+  template <int M>
+  __device__ static void stage_x(float* xs, float (&)[M], const XRegs& xr, int lane) {
+    constexpr int MP = mpad(M);
+    if (lane < kKW) {
+#pragma unroll
+      for (int m = 0; m < MP; ++m)
+        xs[((lane >> 1) * MP + m) * 2 + (lane & 1)] = m < M ? h2f(xr.v[m][0]) : 0.f;
+    }
+  }
+
+  template <int M, int RPW>
+  __device__ static void tile_math(const uint8_t* stage, const float* xs, const float (&)[M],
+                                   RowAcc<M, RPW>& yacc, uint8_t* lut, int slice, int half,
+                                   int lane, uint64_t* empty_bar) {
+    const int t = slice * 32 + lane;
+    const int j0 = half * RPW;
+    uint4 cwd[RPW];
+#pragma unroll
+    for (int j = 0; j < RPW; ++j) cwd[j] = lds128(stage + ((j0 + j) * kLaneSlots + t) * 16);
+    release_stage(empty_bar, lane);
+    const uint32_t lane4 = static_cast<uint32_t>(lane) << 2;
+
+    float2 acc[RPW][M];
+#pragma unroll
+    for (int j = 0; j < RPW; ++j)
+#pragma unroll
+      for (int m = 0; m < M; ++m) acc[j][m] = make_float2(0.f, 0.f);
+    constexpr int UI = (M > 8) ? 1 : 4;
+#pragma unroll UI
+    for (int i = 0; i < 4; ++i) {       // word i: k = 4i..4i+3 -> pairs 2i, 2i+1
+#pragma unroll
+      for (int pp = 0; pp < 2; ++pp) {
+        float2 xv[M];
+        load_xpairs<M>(xs, 2 * i + pp, xv);
+#pragma unroll
+        for (int j = 0; j < RPW; ++j) {
+          const uint32_t wv = word_of(cwd[j], i);
+          const float2 w2 = make_float2(__uint_as_float(lds32(lut, lut_offset(wv, lane4, 2 * pp))),
+                                        __uint_as_float(lds32(lut, lut_offset(wv, lane4, 2 * pp + 1))));
+#pragma unroll
+          for (int m = 0; m < M; ++m) acc[j][m] = __ffma2_rn(w2, xv[m], acc[j][m]);
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < RPW; ++j) {
+      float a[M];
+#pragma unroll
+      for (int m = 0; m < M; ++m) a[m] = acc[j][m].x + acc[j][m].y;
+      yacc.add_row(j, 1.0f, a);
+    }
+  }
+};
+
+}  // namespace qgemv
+
+namespace qgemv {
+namespace cbk {
+
+// Prepared code chunk (tile, j, t) <- the 16 canonical index bytes of row
+// rt*128 + 4l + j covering the warp's k slice; bytes past the row are 0.
+template <class F, int kBitsPerIndex>
+__global__ void prepare_kernel(const uint8_t* __restrict__ canon, int64_t N, int64_t K, int nKT,
+                               int64_t nchunks, uint8_t* __restrict__ tiles) {
+  const int64_t row_bytes = K * kBitsPerIndex / 8;
+  for (int64_t ci = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; ci < nchunks;
+       ci += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t tile = ci / (kRowsPerLane * kLaneSlots);
+    const int rem = static_cast<int>(ci % (kRowsPerLane * kLaneSlots));
+    const int j = rem / kLaneSlots, t = rem % kLaneSlots;
+    const int cw = t / 32, lane = t % 32;
+    const int64_t n = (tile / nKT) * kTileRows + kRowsPerLane * lane + j;
+    const int64_t b0 = ((tile % nKT) * F::kKT + cw * F::kKW) * kBitsPerIndex / 8;
+    uint32_t w[4] = {0, 0, 0, 0};
+    if (n < N) {
+      for (int i = 0; i < 16; ++i) {
+        const int64_t b = b0 + i;
+        if (b < row_bytes) w[i / 4] |= static_cast<uint32_t>(canon[n * row_bytes + b]) << (8 * (i % 4));
+      }
+    }
+    *reinterpret_cast<uint4*>(tiles + tile * F::kTileBytes + (j * kLaneSlots + t) * 16) =
+        make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+// Exact decode (codebook entry of each index) from the prepared tiles.
+template <class F, int kBitsPerIndex>
+__global__ void dequant_kernel(const uint8_t* __restrict__ tiles, const uint16_t* __restrict__ cb,
+                               int64_t N, int64_t K, int nKT, float* __restrict__ w) {
+  const int64_t total = N * K;
+  for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
+       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t n = e / K, k = e % K;
+    const int r = static_cast<int>(n % kTileRows);
+    const int lane = r / kRowsPerLane, j = r % kRowsPerLane;
+    const int64_t tile = (n / kTileRows) * nKT + k / F::kKT;
+    const int kk = static_cast<int>(k % F::kKT);
+    const int cw = kk / F::kKW, el = kk % F::kKW;
+    const uint8_t byte =
+        tiles[tile * F::kTileBytes + (j * kLaneSlots + cw * 32 + lane) * 16 + el * kBitsPerIndex / 8];
+    const int idx = kBitsPerIndex == 8 ? byte : ((el & 1) ? (byte >> 4) : (byte & 15));
+    w[e] = h2f(cb[idx]);
+  }
+}
+
+inline int grid_for(int64_t items, int threads) {
+  const int64_t g = (items + threads - 1) / threads;
+  return static_cast<int>(g < 1 ? 1 : (g > 65536 ? 65536 : g));
+}
+
+}  // namespace cbk
+}  // namespace qgemv

@@ -1,0 +1,38 @@
+// fmt_cbk4.cu -- CBK4 (4-bit index into 16 fp16 centroids): re-layout,
+// exact decode export and the GEMV launch table for M = 1..16.
+#include "fmt_cbk.cuh"
+#include "formats.h"
+#include "launch_table.cuh"
+
+namespace qgemv {
+namespace {
+
+using F = FmtCBK4;
+
+cudaError_t prepare(const PrepareArgs& a, cudaStream_t s) {
+  const int64_t nchunks = a.nRT * a.nKT * kRowsPerLane * kLaneSlots;
+  cbk::prepare_kernel<F, 4><<<cbk::grid_for(nchunks, 256), 256, 0, s>>>(a.packed, a.N, a.K, a.nKT,
+                                                                       nchunks, a.tiles);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return cudaMemcpyAsync(a.aux, a.codebooks, 16 * sizeof(uint16_t), cudaMemcpyDeviceToDevice, s);
+}
+
+cudaError_t dequant(const uint8_t* tiles, const void* aux, int64_t N, int64_t K, int nKT, float* w,
+                    cudaStream_t s) {
+  cbk::dequant_kernel<F, 4><<<cbk::grid_for(N * K, 256), 256, 0, s>>>(
+      tiles, static_cast<const uint16_t*>(aux), N, K, nKT, w);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+const FormatOps* ops_cbk4() {
+  static const FormatOps ops = {
+      /*format=*/2, F::kKT, F::kTileBytes, /*aux_bytes=*/16 * 2,
+      &LaunchTable<F>::smem_bytes, &LaunchTable<F>::setup, &LaunchTable<F>::launch,
+      &prepare, &dequant};
+  return &ops;
+}
+
+}  // namespace qgemv

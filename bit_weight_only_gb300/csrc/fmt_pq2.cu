@@ -1,0 +1,132 @@
+// fmt_pq2.cu -- PQ2_0: re-layout (prepare), exact decode export and the
+// launch table of the GEMV kernel for M = 1..16.
+//
+// Canonical PQ2_0 ("Making a ternary reasoning model fast in vLLM", section
+// "Anatomy of a PQ2_0 block"): per output row n, K/128 blocks of
+// {fp16 d; uint8 qs[32]} (34 bytes), byte j of qs holding elements
+// 4j..4j+3 as two-bit codes read from the low end; code c decodes to
+// (c - 1) * d, i.e. 0,1,2,3 -> -1,0,+1,+2.  The prepared layout keeps the same
+// bytes, split into a code plane and a scale plane per tile, as the page's
+// "prepared weights" do, so that every code row is 16-byte aligned.
+#include "fmt_fields.cuh"
+#include "formats.h"
+#include "launch_table.cuh"
+
+namespace qgemv {
+namespace {
+
+using F = FmtPQ2;
+constexpr int kBlockBytes = 34;
+
+__device__ __forceinline__ uint32_t canon_code(const uint8_t* qs, int e) {
+  return (qs[e >> 2] >> (2 * (e & 3))) & 3u;
+}
+
+// One thread per 32-bit code word of the prepared stream.
+__global__ void prepare_codes(const uint8_t* __restrict__ canon, int64_t N, int64_t K, int nKT,
+                              int64_t nwords, uint32_t* __restrict__ tiles) {
+  constexpr int kWordsPerTile = F::kTileBytes / 4;
+  constexpr int kCodeWords = F::kCodeBytes / 4;
+  const int64_t nb = K / 128;
+  for (int64_t wi = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; wi < nwords;
+       wi += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t tile = wi / kCodeWords;
+    const int off = static_cast<int>(wi % kCodeWords);
+    const int chunk = off / 4, i = off % 4;
+    const int j = chunk / kLaneSlots, t = chunk % kLaneSlots;
+    const int cw = t / 32, lane = t % 32;
+    const int64_t n = (tile / nKT) * kTileRows + kRowsPerLane * lane + j;
+    const int64_t b = static_cast<int64_t>(tile % nKT) * 4 + (cw >> 1);
+    uint32_t word = 0;
+    if (n < N && b < nb) {
+      const uint8_t* qs = canon + (n * nb + b) * kBlockBytes + 2;
+      const int e0 = 64 * (cw & 1) + 16 * i;
+#pragma unroll
+      for (int jj = 0; jj < 16; ++jj) word |= canon_code(qs, e0 + jj) << (2 * jj);
+    }
+    tiles[tile * kWordsPerTile + off] = word;
+  }
+}
+
+// One thread per (tile, block-in-tile, lane): four fp16 scales.
+__global__ void prepare_scales(const uint8_t* __restrict__ canon, int64_t N, int64_t K, int nKT,
+                               int64_t nitems, uint8_t* __restrict__ tiles) {
+  const int64_t nb = K / 128;
+  for (int64_t it = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; it < nitems;
+       it += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t tile = it / 128;
+    const int blk = static_cast<int>((it % 128) / 32), lane = static_cast<int>(it % 32);
+    const int64_t b = static_cast<int64_t>(tile % nKT) * 4 + blk;
+    uint16_t h[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int64_t n = (tile / nKT) * kTileRows + kRowsPerLane * lane + j;
+      h[j] = 0;
+      if (n < N && b < nb) {
+        const uint8_t* p = canon + (n * nb + b) * kBlockBytes;
+        h[j] = static_cast<uint16_t>(p[0] | (p[1] << 8));
+      }
+    }
+    uint2 v;
+    v.x = h[0] | (static_cast<uint32_t>(h[1]) << 16);
+    v.y = h[2] | (static_cast<uint32_t>(h[3]) << 16);
+    *reinterpret_cast<uint2*>(tiles + tile * F::kTileBytes + F::kCodeBytes + (blk * 32 + lane) * 8) = v;
+  }
+}
+
+__global__ void dequant_kernel(const uint8_t* __restrict__ tiles, int64_t N, int64_t K, int nKT,
+                               float* __restrict__ w) {
+  const int64_t total = N * K;
+  for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
+       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t n = e / K, k = e % K;
+    const int r = static_cast<int>(n % kTileRows);
+    const int lane = r / kRowsPerLane, j = r % kRowsPerLane;
+    const int64_t tile = (n / kTileRows) * nKT + k / F::kKT;
+    const int kk = static_cast<int>(k % F::kKT);
+    const int cw = kk / F::kKW, el = kk % F::kKW;
+    const int t = cw * 32 + lane;
+    const uint8_t* tb = tiles + tile * F::kTileBytes;
+    const uint32_t word =
+        *reinterpret_cast<const uint32_t*>(tb + (j * kLaneSlots + t) * 16 + 4 * (el / 16));
+    const int c = static_cast<int>((word >> (2 * (el % 16))) & 3u);
+    const uint16_t hb = *reinterpret_cast<const uint16_t*>(
+        tb + F::kCodeBytes + ((cw >> 1) * 32 + lane) * 8 + 2 * j);
+    w[e] = static_cast<float>(c - 1) * h2f(hb);  // exact
+  }
+}
+
+int grid_for(int64_t items, int threads) {
+  const int64_t g = (items + threads - 1) / threads;
+  return static_cast<int>(g < 1 ? 1 : (g > 65536 ? 65536 : g));
+}
+
+cudaError_t prepare(const PrepareArgs& a, cudaStream_t s) {
+  const int64_t T = a.nRT * a.nKT;
+  const int64_t nwords = T * (F::kCodeBytes / 4);
+  prepare_codes<<<grid_for(nwords, 256), 256, 0, s>>>(a.packed, a.N, a.K, a.nKT, nwords,
+                                                      reinterpret_cast<uint32_t*>(a.tiles));
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int64_t nitems = T * 128;
+  prepare_scales<<<grid_for(nitems, 256), 256, 0, s>>>(a.packed, a.N, a.K, a.nKT, nitems, a.tiles);
+  return cudaGetLastError();
+}
+
+cudaError_t dequant(const uint8_t* tiles, const void*, int64_t N, int64_t K, int nKT, float* w,
+                    cudaStream_t s) {
+  dequant_kernel<<<grid_for(N * K, 256), 256, 0, s>>>(tiles, N, K, nKT, w);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+const FormatOps* ops_pq2() {
+  static const FormatOps ops = {
+      /*format=*/4, F::kKT, F::kTileBytes, /*aux_bytes=*/0,
+      &LaunchTable<F>::smem_bytes, &LaunchTable<F>::setup, &LaunchTable<F>::launch,
+      &prepare, &dequant};
+  return &ops;
+}
+
+}  // namespace qgemv

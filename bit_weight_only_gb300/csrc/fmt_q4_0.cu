@@ -1,0 +1,174 @@
+// fmt_q4_0.cu -- Q4_0: re-layout (prepare), exact decode export, quantizer,
+// and the launch table of the GEMV kernel for M = 1..16.
+//
+// Canonical Q4_0 ("Model quantization, read carefully", sections "The
+// ladder" and "Anatomy of a block"; value (q - 8) * d and the quantizer
+// d = signed-max / -8, q = clamp(round(w/d) + 8, 0..15) follow the ggml
+// convention): per output row n, K/32 blocks of {fp16 d; uint8 qs[16]},
+// byte i of qs holding element i (low nibble) and element i+16 (high).
+#include <cuda_fp16.h>
+
+#include "fmt_fields.cuh"
+#include "formats.h"
+#include "launch_table.cuh"
+
+namespace qgemv {
+namespace {
+
+using F = FmtQ4_0;
+constexpr int kBlockBytes = 18;
+
+// Nibble q of element e (0..31) of a canonical block's qs[16].
+__device__ __forceinline__ uint32_t canon_q(const uint8_t* qs, int e) {
+  return e < 16 ? (qs[e] & 0xfu) : (qs[e - 16] >> 4);
+}
+
+// One thread per 32-bit code word of the prepared stream.
+__global__ void prepare_codes(const uint8_t* __restrict__ canon, int64_t N, int64_t K, int nKT,
+                              int64_t nwords, uint32_t* __restrict__ tiles) {
+  constexpr int kWordsPerTile = F::kTileBytes / 4;
+  constexpr int kCodeWords = F::kCodeBytes / 4;
+  const int64_t nb = K / 32;
+  for (int64_t wi = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; wi < nwords;
+       wi += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t tile = wi / kCodeWords;
+    const int off = static_cast<int>(wi % kCodeWords);
+    const int chunk = off / 4, i = off % 4;
+    const int j = chunk / kLaneSlots, t = chunk % kLaneSlots;
+    const int cw = t / 32, lane = t % 32;
+    const int64_t n = (tile / nKT) * kTileRows + kRowsPerLane * lane + j;
+    const int64_t b = static_cast<int64_t>(tile % nKT) * kSlices + cw;
+    uint32_t word = 0;
+    if (n < N && b < nb) {
+      const uint8_t* qs = canon + (n * nb + b) * kBlockBytes + 2;
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) word |= canon_q(qs, 8 * i + jj) << (4 * jj);
+    }
+    tiles[tile * kWordsPerTile + off] = word;
+  }
+}
+
+// One thread per (tile, t): the four fp16 scales of rows 4l..4l+3.
+__global__ void prepare_scales(const uint8_t* __restrict__ canon, int64_t N, int64_t K, int nKT,
+                               int64_t nitems, uint8_t* __restrict__ tiles) {
+  const int64_t nb = K / 32;
+  for (int64_t it = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; it < nitems;
+       it += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t tile = it / kLaneSlots;
+    const int t = static_cast<int>(it % kLaneSlots);
+    const int cw = t / 32, lane = t % 32;
+    const int64_t b = static_cast<int64_t>(tile % nKT) * kSlices + cw;
+    uint16_t h[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int64_t n = (tile / nKT) * kTileRows + kRowsPerLane * lane + j;
+      h[j] = 0;
+      if (n < N && b < nb) {
+        const uint8_t* blk = canon + (n * nb + b) * kBlockBytes;
+        h[j] = static_cast<uint16_t>(blk[0] | (blk[1] << 8));
+      }
+    }
+    uint2 v;
+    v.x = h[0] | (static_cast<uint32_t>(h[1]) << 16);
+    v.y = h[2] | (static_cast<uint32_t>(h[3]) << 16);
+    *reinterpret_cast<uint2*>(tiles + tile * F::kTileBytes + F::kCodeBytes + t * 8) = v;
+  }
+}
+
+// Exact decode of every weight from the prepared tiles.
+__global__ void dequant_kernel(const uint8_t* __restrict__ tiles, int64_t N, int64_t K, int nKT,
+                               float* __restrict__ w) {
+  const int64_t total = N * K;
+  for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
+       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t n = e / K, k = e % K;
+    const int r = static_cast<int>(n % kTileRows);
+    const int lane = r / kRowsPerLane, j = r % kRowsPerLane;
+    const int64_t tile = (n / kTileRows) * nKT + k / F::kKT;
+    const int kk = static_cast<int>(k % F::kKT);
+    const int cw = kk / F::kKW, el = kk % F::kKW;
+    const int t = cw * 32 + lane;
+    const uint8_t* tb = tiles + tile * F::kTileBytes;
+    const uint32_t word = *reinterpret_cast<const uint32_t*>(tb + (j * kLaneSlots + t) * 16 + 4 * (el / 8));
+    const int q = static_cast<int>((word >> (4 * (el % 8))) & 0xfu);
+    const uint16_t hb = *reinterpret_cast<const uint16_t*>(tb + F::kCodeBytes + t * 8 + 2 * j);
+    w[e] = static_cast<float>(q - 8) * h2f(hb);  // exact: 4-bit int x fp16 fits fp32
+  }
+}
+
+// One thread per block of 32 weights.
+__global__ void quantize_kernel(const float* __restrict__ w, int64_t nblocks,
+                                uint8_t* __restrict__ out) {
+  for (int64_t b = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; b < nblocks;
+       b += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const float* v = w + b * 32;
+    float amax = 0.f, absmax = 0.f;
+    for (int i = 0; i < 32; ++i) {
+      const float a = fabsf(v[i]);
+      if (a > absmax) {
+        absmax = a;
+        amax = v[i];
+      }
+    }
+    const float d = __fdiv_rn(amax, -8.0f);
+    uint32_t q[32];
+    for (int i = 0; i < 32; ++i) {
+      int qi = 8;
+      if (d != 0.0f) {
+        qi = static_cast<int>(roundf(__fdiv_rn(v[i], d))) + 8;
+        qi = qi < 0 ? 0 : (qi > 15 ? 15 : qi);
+      }
+      q[i] = static_cast<uint32_t>(qi);
+    }
+    // The block starts at an even byte offset: write it as nine 16-bit words
+    // (fp16 d, then qs[2i] | qs[2i+1] << 8 with qs[i] = q_i | q_(i+16) << 4).
+    uint16_t* blk = reinterpret_cast<uint16_t*>(out + b * kBlockBytes);
+    blk[0] = __half_as_ushort(__float2half_rn(d));
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t lo = q[2 * i] | (q[2 * i + 16] << 4);
+      const uint32_t hi = q[2 * i + 1] | (q[2 * i + 17] << 4);
+      blk[1 + i] = static_cast<uint16_t>(lo | (hi << 8));
+    }
+  }
+}
+
+int grid_for(int64_t items, int threads) {
+  const int64_t g = (items + threads - 1) / threads;
+  return static_cast<int>(g < 1 ? 1 : (g > 65536 ? 65536 : g));
+}
+
+cudaError_t prepare(const PrepareArgs& a, cudaStream_t s) {
+  const int64_t T = a.nRT * a.nKT;
+  const int64_t nwords = T * (F::kCodeBytes / 4);
+  prepare_codes<<<grid_for(nwords, 256), 256, 0, s>>>(a.packed, a.N, a.K, a.nKT, nwords,
+                                                      reinterpret_cast<uint32_t*>(a.tiles));
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int64_t nitems = T * kLaneSlots;
+  prepare_scales<<<grid_for(nitems, 256), 256, 0, s>>>(a.packed, a.N, a.K, a.nKT, nitems, a.tiles);
+  return cudaGetLastError();
+}
+
+cudaError_t dequant(const uint8_t* tiles, const void*, int64_t N, int64_t K, int nKT, float* w,
+                    cudaStream_t s) {
+  dequant_kernel<<<grid_for(N * K, 256), 256, 0, s>>>(tiles, N, K, nKT, w);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t quantize_q4_0(const float* w, int64_t N, int64_t K, uint8_t* out, cudaStream_t s) {
+  const int64_t nblocks = N * (K / 32);
+  quantize_kernel<<<grid_for(nblocks, 128), 128, 0, s>>>(w, nblocks, out);
+  return cudaGetLastError();
+}
+
+const FormatOps* ops_q4_0() {
+  static const FormatOps ops = {
+      /*format=*/1, F::kKT, F::kTileBytes, /*aux_bytes=*/0,
+      &LaunchTable<F>::smem_bytes, &LaunchTable<F>::setup, &LaunchTable<F>::launch,
+      &prepare, &dequant};
+  return &ops;
+}
+
+}  // namespace qgemv

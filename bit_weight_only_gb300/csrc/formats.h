@@ -1,0 +1,46 @@
+// formats.h -- internal interface between the C ABI (qgemv_api.cu) and the
+// per-format translation units.  Host-side declarations only.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace qgemv {
+
+struct GemvParams;  // gemv_kernel.cuh
+
+// Canonical inputs already on the device, plus the prepared-layout geometry.
+struct PrepareArgs {
+  const uint8_t* packed;     // canonical packed bytes
+  const uint16_t* scales;    // canonical fp16 scales or nullptr
+  const uint16_t* codebooks; // canonical fp16 codebooks or nullptr
+  int64_t N, K;
+  int64_t nRT;               // row tiles
+  int nKT;                   // k tiles per row tile
+  uint8_t* tiles;            // out: nRT * nKT * tile_bytes
+  void* aux;                 // out: format data (aux_bytes), may be nullptr
+};
+
+struct FormatOps {
+  int format;
+  int kt;          // k per tile
+  int tile_bytes;  // bytes per prepared tile
+  int64_t aux_bytes;
+  int (*smem_bytes)(int M);
+  cudaError_t (*setup)();  // one-time kernel attributes
+  cudaError_t (*launch)(int M, const GemvParams& p, int grid, cudaStream_t s);
+  cudaError_t (*prepare)(const PrepareArgs& a, cudaStream_t s);
+  // w_out[n*K + k] = exact decoded weight, read back from the prepared tiles
+  cudaError_t (*dequant)(const uint8_t* tiles, const void* aux, int64_t N, int64_t K, int nKT,
+                         float* w_out, cudaStream_t s);
+};
+
+const FormatOps* ops_q4_0();
+const FormatOps* ops_pq2();
+const FormatOps* ops_cbk4();
+const FormatOps* ops_cbk8();
+
+// Q4_0 quantizer (canonical output).
+cudaError_t quantize_q4_0(const float* w, int64_t N, int64_t K, uint8_t* out, cudaStream_t s);
+
+}  // namespace qgemv

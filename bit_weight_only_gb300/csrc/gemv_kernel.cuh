@@ -1,0 +1,403 @@
+// gemv_kernel.cuh -- the weight-streaming GEMV kernel shared by all formats.
+//
+//   y[m][n] = sum_k x[m][k] * w[n][k]      (1 <= M <= 16, fp32 accumulation)
+//
+// Design (one persistent CTA per SM):
+//   * The weights were re-laid out at create time into "tiles" of
+//     kTileRows (128) output rows x F::kKT inputs, each tile one contiguous
+//     run of F::kTileBytes bytes, stored in (row tile, k tile) order.  The
+//     whole matrix is therefore one sequential byte stream.  Inside a tile,
+//     the k range is cut into kSlices (8) slices of F::kKW inputs, and the
+//     packed codes of slice s for rows 4l..4l+3 sit at lane slot t = 32s + l
+//     (16 bytes per row), so one 128-bit shared load per row per lane and no
+//     bank conflicts.
+//   * The stream of T tiles is split evenly over the grid ("stream-K"): CTA
+//     c owns tiles [c*T/G, (c+1)*T/G).  A row tile cut by a CTA boundary is
+//     finished by whichever of its contributors arrives last (an integer
+//     counter), which sums all partial results in contributor order: fixed
+//     order, no float atomics, bitwise reproducible.
+//   * One elected thread keeps an F::stages(M) ring of shared-memory stages
+//     filled with TMA bulk copies (cp.async.bulk, evict-first L2 policy),
+//     stages - 1 tiles ahead of the math, signalled through mbarriers.  There
+//     is no separate producer warp.
+//   * WPS warps serve each slice: with WPS = 1 (eight warps) lane l of the
+//     slice's warp owns rows 4l..4l+3; with WPS = 2 (sixteen warps, used for
+//     small M where registers allow it, to hide more latency) the two warps
+//     of a slice split those four rows.  Each lane loads its codes, releases
+//     the stage, then decodes in registers and accumulates in fp32.  The
+//     activations of the slice are staged per tile in a per-warp shared
+//     buffer (prefetched from global one tile ahead), in the pre-scaled form
+//     the format's decode wants.
+//   * At the end of a row tile the eight slices' partial sums are added in
+//     slice order through shared memory and written to y (or to the
+//     stream-K workspace).
+// Every mbarrier wait is bounded; a timeout sets an error word, skips the
+// remaining math and still meets every named barrier, so the kernel always
+// returns.
+#pragma once
+
+#include <cstdint>
+#include <cuda_fp16.h>
+
+#include "device_common.cuh"
+
+namespace qgemv {
+
+constexpr int kSlices = 8;                         // k slices per tile
+constexpr int kLaneSlots = 32 * kSlices;           // 256 (slice, lane) slots
+constexpr int kRowsPerLane = 4;
+constexpr int kTileRows = 32 * kRowsPerLane;       // 128
+constexpr int kMaxM = 16;
+constexpr int kPartialStride = kTileRows * kMaxM;  // floats per partial slot
+
+struct GemvParams {
+  const uint8_t* tiles;  // prepared tiles (device)
+  const __half* x;       // [M][K] fp16
+  float* y;              // [M][N] fp32
+  float* partials;       // [gridDim.x][2][kPartialStride]
+  int* counters;         // [number of row tiles], zero between calls
+  int* err;              // error word (kErr* bits)
+  const void* aux;       // format data (codebooks ...)
+  int64_t N, K;
+  int64_t T;             // tiles in the stream = nRT * nKT
+  int nKT;               // k tiles per row tile
+};
+
+// Warps per slice for a given M: two while the whole accumulator set of a
+// lane fits in 128 registers, one above.
+__host__ __device__ constexpr int wps_for(int M) { return M <= 4 ? 2 : 1; }
+
+// x rows stored per k pair; padded so vector loads stay aligned.
+__host__ __device__ constexpr int mpad(int M) { return M <= 2 ? M : (M + 3) / 4 * 4; }
+
+// Row stride (floats) of the cross-slice reduction buffer.
+__host__ __device__ constexpr int acc_stride(int M) { return M > 8 ? mpad(M) : M; }
+
+// Accumulators of one lane's RPW rows over the k tiles of a row tile.
+// M <= 8: registers.  M > 8: the lane's own rows of the slice's reduction
+// buffer in shared memory, so the registers stay with the inner loop.
+template <int M, int RPW, bool kInSmem = (M > 8)>
+struct RowAcc;
+
+template <int M, int RPW>
+struct RowAcc<M, RPW, false> {
+  float v[RPW][M];
+  __device__ __forceinline__ void init(float*, int, int, int) { reset(); }
+  __device__ __forceinline__ void reset() {
+#pragma unroll
+    for (int j = 0; j < RPW; ++j)
+#pragma unroll
+      for (int m = 0; m < M; ++m) v[j][m] = 0.f;
+  }
+  // row j (of the lane's RPW rows) += d * a
+  __device__ __forceinline__ void add_row(int j, float d, const float (&a)[M]) {
+#pragma unroll
+    for (int m = 0; m < M; ++m) v[j][m] = fmaf(d, a[m], v[j][m]);
+  }
+  __device__ __forceinline__ void flush(float* red, int slice, int half, int lane) {
+#pragma unroll
+    for (int j = 0; j < RPW; ++j)
+#pragma unroll
+      for (int m = 0; m < M; ++m)
+        red[(slice * kTileRows + kRowsPerLane * lane + half * RPW + j) * M + m] = v[j][m];
+  }
+};
+
+template <int M, int RPW>
+struct RowAcc<M, RPW, true> {
+  static constexpr int RS = acc_stride(M);
+  float* rows;
+  __device__ __forceinline__ void init(float* red, int slice, int half, int lane) {
+    rows = red + (slice * kTileRows + kRowsPerLane * lane + half * RPW) * RS;
+    reset();
+  }
+  __device__ __forceinline__ void reset() {
+#pragma unroll
+    for (int i = 0; i < RPW * RS; i += 4)
+      *reinterpret_cast<float4*>(rows + i) = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  __device__ __forceinline__ void add_row(int j, float d, const float (&a)[M]) {
+    float* r = rows + j * RS;
+#pragma unroll
+    for (int m = 0; m < M; m += 4) {
+      float4 o = lds128f(r + m);
+      o.x = fmaf(d, a[m], o.x);
+      if (m + 1 < M) o.y = fmaf(d, a[m + 1], o.y);
+      if (m + 2 < M) o.z = fmaf(d, a[m + 2], o.z);
+      if (m + 3 < M) o.w = fmaf(d, a[m + 3], o.w);
+      *reinterpret_cast<float4*>(r + m) = o;
+    }
+  }
+  __device__ __forceinline__ void flush(float*, int, int, int) {}
+};
+
+// Dynamic shared memory of gemv_kernel<F, M>.
+template <class F, int M>
+__host__ __device__ constexpr int gemv_smem_bytes() {
+  return F::stages(M) * F::kTileBytes                              // tile ring
+         + kSlices * wps_for(M) * (F::kKW / 2) * mpad(M) * 8      // x pairs, per warp
+         + kSlices * kTileRows * acc_stride(M) * 4                 // cross-slice reduction
+         + F::kSharedBytes                                         // format tables
+         + 2 * F::stages(M) * 8;                                   // mbarriers
+}
+
+template <int M>
+__host__ __device__ constexpr int gemv_threads() { return 32 * kSlices * wps_for(M); }
+
+// CTA that owns tile t when T tiles are split over G CTAs.
+__device__ __forceinline__ int64_t cta_of_tile(int64_t t, int64_t T, int64_t G) {
+  return ((t + 1) * G - 1) / T;
+}
+
+template <class F, int M>
+__global__ void __launch_bounds__(gemv_threads<M>(), 1) gemv_kernel(const GemvParams p) {
+  constexpr int NS = F::stages(M);
+  constexpr int TB = F::kTileBytes;
+  constexpr int MP = mpad(M);
+  constexpr int WPS = wps_for(M);
+  constexpr int NT = gemv_threads<M>();
+  constexpr int RPW = kRowsPerLane / WPS;
+  constexpr int XS_FLOATS = (F::kKW / 2) * MP * 2;  // per warp
+  constexpr int RS = acc_stride(M);
+
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* ring = smem;
+  float* xs_all = reinterpret_cast<float*>(smem + NS * TB);
+  float* red = xs_all + kSlices * WPS * XS_FLOATS;
+  uint8_t* fsh = reinterpret_cast<uint8_t*>(red + kSlices * kTileRows * RS);
+  uint64_t* full = reinterpret_cast<uint64_t*>(fsh + F::kSharedBytes);
+  uint64_t* empty = full + NS;
+  __shared__ int s_flag;
+  __shared__ volatile int s_abort;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int slice = warp % kSlices;
+  const int half = warp / kSlices;  // 0 when WPS == 1
+  const int tid = threadIdx.x;
+  const int64_t G = gridDim.x;
+  const int64_t c = blockIdx.x;
+  const int64_t t0 = c * p.T / G;
+  const int64_t t1 = (c + 1) * p.T / G;
+
+  if (tid == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kSlices * WPS);
+    }
+    s_abort = 0;
+    fence_mbarrier_init();
+  }
+  F::init_shared(fsh, p, tid, NT);
+  __syncthreads();
+
+  float* xs = xs_all + warp * XS_FLOATS;
+  RowAcc<M, RPW> acc;
+  acc.init(red, slice, half, lane);
+
+  // The elected thread fills the ring NS - 1 tiles ahead of the math.
+  const int64_t ntiles = t1 - t0;
+  const bool elected = (tid == 0);
+  uint64_t pol = 0;
+  int64_t n_issued = 0;  // meaningful on the elected thread
+  if (elected) {
+    pol = l2_policy_evict_first();
+    for (; n_issued < NS - 1 && n_issued < ntiles; ++n_issued) {
+      mbar_arrive_expect_tx(&full[n_issued], TB);
+      bulk_g2s(ring + n_issued * TB, p.tiles + (t0 + n_issued) * TB, TB, &full[n_issued], pol);
+    }
+  }
+
+  // Position of tile t0 in the stream, advanced incrementally below.
+  int64_t rt = t0 / p.nKT;
+  int kt = static_cast<int>(t0 - rt * p.nKT);
+  typename F::XRegs xr;
+  if (ntiles > 0) F::template load_x<M>(xr, p, kt, slice, lane);
+
+  int s = 0;           // stage of the tile being computed
+  uint32_t ph = 0;     // its fill parity
+  int su = static_cast<int>(n_issued % NS);            // next stage to fill
+  uint32_t phu = static_cast<uint32_t>((n_issued / NS) & 1);
+  for (int64_t i = 0; i < ntiles; ++i) {
+    bool abort = s_abort != 0;
+
+    // Refill: tile u = i + NS - 1 goes to the stage released by tile
+    // u - NS = i - 1, whose codes every warp loaded one iteration ago.
+    if (elected && !abort && n_issued < ntiles) {
+      if (n_issued >= NS && !mbar_wait_bounded(&empty[su], phu ^ 1)) {
+        atomicOr(p.err, kErrTimeoutEmpty);
+        s_abort = 1;
+        abort = true;
+      } else {
+        mbar_arrive_expect_tx(&full[su], TB);
+        bulk_g2s(ring + su * TB, p.tiles + (t0 + n_issued) * TB, TB, &full[su], pol);
+        ++n_issued;
+        if (++su == NS) { su = 0; phu ^= 1; }
+      }
+    }
+
+    // Stage this tile's activations, then prefetch the next tile's.
+    float xsum[M];
+    __syncwarp();
+    F::template stage_x<M>(xs, xsum, xr, lane);
+    __syncwarp();
+    const int kt_next = (kt + 1 == p.nKT) ? 0 : kt + 1;
+    if (i + 1 < ntiles) F::template load_x<M>(xr, p, kt_next, slice, lane);
+
+    const bool ok = !abort && mbar_wait_bounded(&full[s], ph);
+    if (!ok) {
+      if (!abort && lane == 0) atomicOr(p.err, kErrTimeoutFull);
+      s_abort = 1;
+    } else {
+      F::template tile_math<M, RPW>(ring + s * TB, xs, xsum, acc, fsh, slice, half, lane,
+                                    &empty[s]);
+    }
+    if (++s == NS) { s = 0; ph ^= 1; }
+
+    const bool row_end = (kt_next == 0) || (i + 1 == ntiles);
+    const int64_t cur_rt = rt;
+    kt = kt_next;
+    if (kt_next == 0) ++rt;
+    if (!row_end) continue;
+
+    // ---- row-tile epilogue: add the slices' partials in slice order ----
+    acc.flush(red, slice, half, lane);
+    named_bar_sync(1, NT);
+
+    const bool owner = (cur_rt * p.nKT >= t0) && ((cur_rt + 1) * p.nKT <= t1);
+    const int side = (cur_rt == t0 / p.nKT) ? 0 : 1;
+    float* my_part = p.partials + (c * 2 + side) * kPartialStride;
+    for (int o = tid; o < kTileRows * M; o += NT) {
+      const int r = o % kTileRows;
+      const int m = o / kTileRows;
+      float v = 0.f;
+#pragma unroll
+      for (int w = 0; w < kSlices; ++w) v += red[(w * kTileRows + r) * RS + m];
+      if (owner) {
+        const int64_t n = cur_rt * kTileRows + r;
+        if (n < p.N) p.y[m * p.N + n] = v * F::kOutScale;
+      } else {
+        my_part[m * kTileRows + r] = v;
+      }
+    }
+    if (!owner) __threadfence();
+    named_bar_sync(1, NT);
+
+    if (!owner) {
+      const int64_t cf = cta_of_tile(cur_rt * p.nKT, p.T, G);
+      const int64_t cl = cta_of_tile((cur_rt + 1) * p.nKT - 1, p.T, G);
+      if (tid == 0) {
+        const int old = atomicAdd(&p.counters[cur_rt], 1);
+        s_flag = (old == static_cast<int>(cl - cf));
+      }
+      named_bar_sync(1, NT);
+      if (s_flag) {
+        __threadfence();
+        for (int o = tid; o < kTileRows * M; o += NT) {
+          const int r = o % kTileRows;
+          const int m = o / kTileRows;
+          float v = 0.f;
+          for (int64_t cc = cf; cc <= cl; ++cc) {
+            const int64_t cc_first_rt = (cc * p.T / G) / p.nKT;
+            const int sd = (cur_rt == cc_first_rt) ? 0 : 1;
+            v += __ldcg(p.partials + (cc * 2 + sd) * kPartialStride + m * kTileRows + r);
+          }
+          const int64_t n = cur_rt * kTileRows + r;
+          if (n < p.N) p.y[m * p.N + n] = v * F::kOutScale;
+        }
+        if (tid == 0) p.counters[cur_rt] = 0;
+      }
+    }
+    acc.reset();
+  }
+
+  // Never leave while a copy issued by this CTA may still be landing (only
+  // possible after an aborted run; normally every issued tile was consumed).
+  if (elected) {
+    for (int64_t u = (n_issued > NS ? n_issued - NS : 0); u < n_issued; ++u)
+      mbar_wait_bounded(&full[u % NS], static_cast<uint32_t>((u / NS) & 1));
+  }
+}
+
+// ------------------------------------------------- activation staging ----
+//
+// Helpers for formats whose slice is 32 (one k per lane) or 64 (two k per
+// lane) wide.  x is fp16 [M][K]; k >= K reads as 0.  stage_x converts to
+// fp32, multiplies by the format's per-position power of two (exact) and
+// stores pairs (x'[2q][m], x'[2q+1][m]) at xs[(q * MP + m) * 2 + {0,1}];
+// xsum[m] is the plain sum of the slice's x[m][k] (all lanes get it).
+
+template <int LPL>
+struct XRegsT {
+  unsigned short v[kMaxM][LPL];
+};
+
+template <int KW, int M, int LPL>
+__device__ __forceinline__ void load_x_slice(XRegsT<LPL>& xr, const GemvParams& p, int kt,
+                                             int slice, int lane) {
+  const int64_t kbase = static_cast<int64_t>(kt) * (KW * kSlices) + slice * KW + lane * LPL;
+  const unsigned short* xb = reinterpret_cast<const unsigned short*>(p.x);
+#pragma unroll
+  for (int m = 0; m < M; ++m)
+#pragma unroll
+    for (int i = 0; i < LPL; ++i) {
+      const int64_t k = kbase + i;
+      xr.v[m][i] = (k < p.K) ? __ldg(xb + m * p.K + k) : static_cast<unsigned short>(0);
+    }
+}
+
+template <int M, int LPL, class Scale>
+__device__ __forceinline__ void stage_x_slice(float* xs, float (&xsum)[M],
+                                              const XRegsT<LPL>& xr, int lane, Scale scale) {
+  constexpr int MP = mpad(M);
+#pragma unroll
+  for (int m = 0; m < M; ++m) {
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < LPL; ++i) {
+      const int kk = lane * LPL + i;  // position inside the slice
+      const float v = h2f(xr.v[m][i]);
+      s += v;
+      xs[((kk >> 1) * MP + m) * 2 + (kk & 1)] = v * scale(kk);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    xsum[m] = s;
+  }
+  if (MP > M) {  // keep padding lanes of the vector loads finite
+#pragma unroll
+    for (int i = 0; i < LPL; ++i) {
+      const int kk = lane * LPL + i;
+#pragma unroll
+      for (int m = M; m < MP; ++m) xs[((kk >> 1) * MP + m) * 2 + (kk & 1)] = 0.f;
+    }
+  }
+}
+
+// Load the x pairs of pair index q for all m: out[m] = (x'[2q][m], x'[2q+1][m]).
+template <int M>
+__device__ __forceinline__ void load_xpairs(const float* xs, int q, float2 (&out)[M]) {
+  constexpr int MP = mpad(M);
+  const float* b = xs + q * MP * 2;
+  if constexpr (M == 1) {
+    out[0] = *reinterpret_cast<const float2*>(b);
+  } else {
+#pragma unroll
+    for (int m = 0; m < MP; m += 2) {
+      const float4 v = lds128f(b + m * 2);
+      if (m < M) out[m] = make_float2(v.x, v.y);
+      if (m + 1 < M) out[m + 1] = make_float2(v.z, v.w);
+    }
+  }
+}
+
+__device__ __forceinline__ void release_stage(uint64_t* empty_bar, int lane) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(empty_bar);
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
+  return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+}
+
+}  // namespace qgemv

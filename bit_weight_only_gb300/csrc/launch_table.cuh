@@ -1,0 +1,65 @@
+// launch_table.cuh -- compile-time table of gemv_kernel<F, M>, M = 1..16.
+// M is a template parameter so every accumulator lives in registers; the
+// host picks the instantiation per call (no per-M compilation at run time).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "gemv_kernel.cuh"
+
+namespace qgemv {
+
+template <class F>
+struct LaunchTable {
+  template <int M>
+  static cudaError_t launch_m(const GemvParams& p, int grid, cudaStream_t s) {
+    gemv_kernel<F, M><<<grid, gemv_threads<M>(), gemv_smem_bytes<F, M>(), s>>>(p);
+    return cudaGetLastError();
+  }
+
+  template <int M>
+  static cudaError_t setup_m() {
+    return cudaFuncSetAttribute(gemv_kernel<F, M>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                gemv_smem_bytes<F, M>());
+  }
+
+  static int smem_bytes(int M) {
+    switch (M) {
+#define QGEMV_CASE(m) \
+  case m:             \
+    return gemv_smem_bytes<F, m>();
+      QGEMV_CASE(1) QGEMV_CASE(2) QGEMV_CASE(3) QGEMV_CASE(4) QGEMV_CASE(5) QGEMV_CASE(6)
+      QGEMV_CASE(7) QGEMV_CASE(8) QGEMV_CASE(9) QGEMV_CASE(10) QGEMV_CASE(11) QGEMV_CASE(12)
+      QGEMV_CASE(13) QGEMV_CASE(14) QGEMV_CASE(15) QGEMV_CASE(16)
+#undef QGEMV_CASE
+    }
+    return 0;
+  }
+
+  static cudaError_t setup() {
+    cudaError_t e = cudaSuccess;
+#define QGEMV_SETUP(m) \
+  if (e == cudaSuccess) e = setup_m<m>();
+    QGEMV_SETUP(1) QGEMV_SETUP(2) QGEMV_SETUP(3) QGEMV_SETUP(4) QGEMV_SETUP(5) QGEMV_SETUP(6)
+    QGEMV_SETUP(7) QGEMV_SETUP(8) QGEMV_SETUP(9) QGEMV_SETUP(10) QGEMV_SETUP(11) QGEMV_SETUP(12)
+    QGEMV_SETUP(13) QGEMV_SETUP(14) QGEMV_SETUP(15) QGEMV_SETUP(16)
+#undef QGEMV_SETUP
+    return e;
+  }
+
+  static cudaError_t launch(int M, const GemvParams& p, int grid, cudaStream_t s) {
+    switch (M) {
+#define QGEMV_LAUNCH(m) \
+  case m:               \
+    return launch_m<m>(p, grid, s);
+      QGEMV_LAUNCH(1) QGEMV_LAUNCH(2) QGEMV_LAUNCH(3) QGEMV_LAUNCH(4) QGEMV_LAUNCH(5)
+      QGEMV_LAUNCH(6) QGEMV_LAUNCH(7) QGEMV_LAUNCH(8) QGEMV_LAUNCH(9) QGEMV_LAUNCH(10)
+      QGEMV_LAUNCH(11) QGEMV_LAUNCH(12) QGEMV_LAUNCH(13) QGEMV_LAUNCH(14) QGEMV_LAUNCH(15)
+      QGEMV_LAUNCH(16)
+#undef QGEMV_LAUNCH
+    }
+    return cudaErrorInvalidValue;
+  }
+};
+
+}  // namespace qgemv

@@ -1,0 +1,328 @@
+// qgemv_api.cu -- the C ABI declared in include/qgemv.h.
+//
+// Host side only: argument checks, ownership of the device buffers of a
+// handle, the per-format dispatch (format -> FormatOps, M -> kernel
+// instantiation) and error reporting.  No exception crosses the ABI and no
+// call aborts.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include <cuda_runtime.h>
+
+#include "formats.h"
+#include "gemv_kernel.cuh"
+#include "qgemv.h"
+
+namespace {
+
+constexpr uint32_t kMagic = 0x51474d56u;  // "QGMV"
+
+thread_local char g_msg[512] = "";
+thread_local int g_code = QGEMV_OK;
+
+int set_error(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  g_code = code;
+  return code;
+}
+
+int ok() {
+  g_msg[0] = '\0';
+  g_code = QGEMV_OK;
+  return QGEMV_OK;
+}
+
+int cuda_error(cudaError_t e, const char* what) {
+  return set_error(QGEMV_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorString(e), cudaGetErrorName(e));
+}
+
+const qgemv::FormatOps* ops_for(int format) {
+  switch (format) {
+    case QGEMV_Q4_0: return qgemv::ops_q4_0();
+    case QGEMV_PQ2_0: return qgemv::ops_pq2();
+    case QGEMV_CBK4: return qgemv::ops_cbk4();
+    case QGEMV_CBK8: return qgemv::ops_cbk8();
+  }
+  return nullptr;
+}
+
+// K granularity and canonical sizes per format.
+int64_t k_multiple(int format) {
+  switch (format) {
+    case QGEMV_Q4_0: return 32;
+    case QGEMV_CBK4: return 2;
+    case QGEMV_CBK8: return 1;
+    case QGEMV_PQ2_0: return 128;
+    case QGEMV_AQLM_2X8: return 8;
+  }
+  return 0;
+}
+
+int64_t scales_count(int format, int64_t N) { return format == QGEMV_AQLM_2X8 ? N : 0; }
+
+int64_t codebook_count(int format) {
+  switch (format) {
+    case QGEMV_CBK4: return 16;
+    case QGEMV_CBK8: return 256;
+    case QGEMV_AQLM_2X8: return 2 * 256 * 8;
+  }
+  return 0;
+}
+
+bool is_device_pointer(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();  // clear: plain host memory on some setups
+    return false;
+  }
+  return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+}
+
+// Copy `bytes` from a host or device pointer into a fresh device buffer.
+cudaError_t to_device(const void* src, size_t bytes, void** dst) {
+  *dst = nullptr;
+  if (bytes == 0) return cudaSuccess;
+  cudaError_t e = cudaMalloc(dst, bytes);
+  if (e != cudaSuccess) return e;
+  e = cudaMemcpy(*dst, src, bytes, is_device_pointer(src) ? cudaMemcpyDeviceToDevice
+                                                          : cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) {
+    cudaFree(*dst);
+    *dst = nullptr;
+  }
+  return e;
+}
+
+std::once_flag g_setup_once[8];
+cudaError_t g_setup_err[8];
+
+}  // namespace
+
+struct qgemv_ctx {
+  uint32_t magic;
+  int format;
+  int64_t N, K;
+  const qgemv::FormatOps* ops;
+  int64_t nRT;
+  int nKT;
+  int64_t T;
+  int grid;
+  uint8_t* tiles;
+  void* aux;
+  float* partials;
+  int* counters;
+  int* err;
+};
+
+extern "C" {
+
+int64_t qgemv_packed_bytes(int format, int64_t N, int64_t K) {
+  const int64_t km = k_multiple(format);
+  if (km == 0 || N <= 0 || K <= 0 || K % km) return 0;
+  switch (format) {
+    case QGEMV_Q4_0: return N * (K / 32) * 18;
+    case QGEMV_CBK4: return N * (K / 2);
+    case QGEMV_CBK8: return N * K;
+    case QGEMV_PQ2_0: return N * (K / 128) * 34;
+    case QGEMV_AQLM_2X8: return N * (K / 8) * 2;
+  }
+  return 0;
+}
+
+qgemv_handle qgemv_create(int format, int64_t N, int64_t K, const void* packed, const void* scales,
+                          const void* codebooks) {
+  const qgemv::FormatOps* ops = ops_for(format);
+  if (k_multiple(format) == 0) {
+    set_error(QGEMV_ERR_ARG, "unknown format %d", format);
+    return nullptr;
+  }
+  if (!ops) {
+    set_error(QGEMV_ERR_ARG, "format %d is not built into this library", format);
+    return nullptr;
+  }
+  if (N <= 0 || K <= 0 || K % k_multiple(format)) {
+    set_error(QGEMV_ERR_ARG, "invalid shape N=%lld K=%lld for format %d (K must be a positive multiple of %lld)",
+              (long long)N, (long long)K, format, (long long)k_multiple(format));
+    return nullptr;
+  }
+  if (N > (int64_t(1) << 31) || K > (int64_t(1) << 31)) {
+    set_error(QGEMV_ERR_ARG, "N and K must be at most 2^31");
+    return nullptr;
+  }
+  if (!packed) {
+    set_error(QGEMV_ERR_ARG, "packed is NULL");
+    return nullptr;
+  }
+  if ((scales_count(format, N) > 0) != (scales != nullptr)) {
+    set_error(QGEMV_ERR_ARG, scales ? "format %d takes no scales" : "format %d needs scales", format);
+    return nullptr;
+  }
+  if ((codebook_count(format) > 0) != (codebooks != nullptr)) {
+    set_error(QGEMV_ERR_ARG, codebooks ? "format %d takes no codebooks" : "format %d needs codebooks",
+              format);
+    return nullptr;
+  }
+
+  std::call_once(g_setup_once[format], [&] { g_setup_err[format] = ops->setup(); });
+  if (g_setup_err[format] != cudaSuccess) {
+    cuda_error(g_setup_err[format], "kernel setup");
+    return nullptr;
+  }
+
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) {
+    cuda_error(e, "device query");
+    return nullptr;
+  }
+
+  qgemv_ctx* h = new (std::nothrow) qgemv_ctx();
+  if (!h) {
+    set_error(QGEMV_ERR_NOMEM, "host allocation failed");
+    return nullptr;
+  }
+  h->magic = kMagic;
+  h->format = format;
+  h->N = N;
+  h->K = K;
+  h->ops = ops;
+  h->nRT = (N + qgemv::kTileRows - 1) / qgemv::kTileRows;
+  h->nKT = static_cast<int>((K + ops->kt - 1) / ops->kt);
+  h->T = h->nRT * h->nKT;
+  h->grid = static_cast<int>(h->T < sms ? h->T : sms);
+
+  void *d_packed = nullptr, *d_scales = nullptr, *d_cb = nullptr;
+  auto cleanup = [&](int code, const char* what, cudaError_t ce) -> qgemv_handle {
+    if (ce != cudaSuccess) cuda_error(ce, what);
+    else set_error(code, "%s", what);
+    cudaFree(d_packed);
+    cudaFree(d_scales);
+    cudaFree(d_cb);
+    cudaFree(h->tiles);
+    cudaFree(h->aux);
+    cudaFree(h->partials);
+    cudaFree(h->counters);
+    cudaFree(h->err);
+    h->magic = 0;
+    delete h;
+    return nullptr;
+  };
+
+  e = to_device(packed, static_cast<size_t>(qgemv_packed_bytes(format, N, K)), &d_packed);
+  if (e == cudaSuccess) e = to_device(scales, 2 * scales_count(format, N), &d_scales);
+  if (e == cudaSuccess) e = to_device(codebooks, 2 * codebook_count(format), &d_cb);
+  if (e != cudaSuccess) return cleanup(QGEMV_ERR_CUDA, "copying the canonical inputs", e);
+
+  e = cudaMalloc(&h->tiles, static_cast<size_t>(h->T) * ops->tile_bytes);
+  if (e == cudaSuccess && ops->aux_bytes > 0) e = cudaMalloc(&h->aux, ops->aux_bytes);
+  if (e == cudaSuccess)
+    e = cudaMalloc(&h->partials, sizeof(float) * 2 * qgemv::kPartialStride * static_cast<size_t>(h->grid));
+  if (e == cudaSuccess) e = cudaMalloc(&h->counters, sizeof(int) * h->nRT);
+  if (e == cudaSuccess) e = cudaMalloc(&h->err, sizeof(int));
+  if (e == cudaSuccess) e = cudaMemset(h->counters, 0, sizeof(int) * h->nRT);
+  if (e == cudaSuccess) e = cudaMemset(h->err, 0, sizeof(int));
+  if (e != cudaSuccess) return cleanup(QGEMV_ERR_CUDA, "allocating the handle's device buffers", e);
+
+  qgemv::PrepareArgs a;
+  a.packed = static_cast<const uint8_t*>(d_packed);
+  a.scales = static_cast<const uint16_t*>(d_scales);
+  a.codebooks = static_cast<const uint16_t*>(d_cb);
+  a.N = N;
+  a.K = K;
+  a.nRT = h->nRT;
+  a.nKT = h->nKT;
+  a.tiles = h->tiles;
+  a.aux = h->aux;
+  e = ops->prepare(a, 0);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cleanup(QGEMV_ERR_CUDA, "preparing the tiles", e);
+
+  cudaFree(d_packed);
+  cudaFree(d_scales);
+  cudaFree(d_cb);
+  ok();
+  return h;
+}
+
+static bool valid(qgemv_handle h) { return h && h->magic == kMagic; }
+
+int qgemv_run(qgemv_handle h, const void* x, int M, float* y, void* stream) {
+  if (!valid(h)) return set_error(QGEMV_ERR_ARG, "invalid handle");
+  if (M < 1 || M > qgemv::kMaxM) return set_error(QGEMV_ERR_ARG, "M=%d outside [1, 16]", M);
+  if (!x || !y) return set_error(QGEMV_ERR_ARG, "x or y is NULL");
+  if ((reinterpret_cast<uintptr_t>(x) & 3) || (reinterpret_cast<uintptr_t>(y) & 3))
+    return set_error(QGEMV_ERR_ALIGN, "x and y must be 4-byte aligned");
+  qgemv::GemvParams p;
+  p.tiles = h->tiles;
+  p.x = static_cast<const __half*>(x);
+  p.y = y;
+  p.partials = h->partials;
+  p.counters = h->counters;
+  p.err = h->err;
+  p.aux = h->aux;
+  p.N = h->N;
+  p.K = h->K;
+  p.T = h->T;
+  p.nKT = h->nKT;
+  cudaError_t e = h->ops->launch(M, p, h->grid, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_error(e, "launching the GEMV kernel");
+  return ok();
+}
+
+int qgemv_dequant(qgemv_handle h, float* w_out, void* stream) {
+  if (!valid(h)) return set_error(QGEMV_ERR_ARG, "invalid handle");
+  if (!w_out) return set_error(QGEMV_ERR_ARG, "w_out is NULL");
+  cudaError_t e = h->ops->dequant(h->tiles, h->aux, h->N, h->K, h->nKT, w_out,
+                                  static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_error(e, "launching the decode kernel");
+  return ok();
+}
+
+int qgemv_quantize_q4_0(const float* w, int64_t N, int64_t K, void* packed_out, void* stream) {
+  if (!w || !packed_out) return set_error(QGEMV_ERR_ARG, "w or packed_out is NULL");
+  if (N <= 0 || K <= 0 || K % 32) return set_error(QGEMV_ERR_ARG, "K must be a positive multiple of 32");
+  cudaError_t e = qgemv::quantize_q4_0(w, N, K, static_cast<uint8_t*>(packed_out),
+                                       static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_error(e, "launching the quantizer");
+  return ok();
+}
+
+int qgemv_status(qgemv_handle h) {
+  if (!valid(h)) return set_error(QGEMV_ERR_ARG, "invalid handle");
+  cudaError_t e = cudaDeviceSynchronize();
+  int err = 0;
+  if (e == cudaSuccess) e = cudaMemcpy(&err, h->err, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_error(e, "reading the kernel status");
+  if (err) {
+    // A run that gave up may have left stream-K counters half counted.
+    cudaMemset(h->counters, 0, sizeof(int) * h->nRT);
+    cudaMemset(h->err, 0, sizeof(int));
+    return set_error(QGEMV_ERR_TIMEOUT, "a kernel gave up a bounded wait (code %d)", err);
+  }
+  return ok();
+}
+
+void qgemv_destroy(qgemv_handle h) {
+  if (!valid(h)) return;
+  cudaDeviceSynchronize();
+  cudaFree(h->tiles);
+  cudaFree(h->aux);
+  cudaFree(h->partials);
+  cudaFree(h->counters);
+  cudaFree(h->err);
+  h->magic = 0;
+  delete h;
+}
+
+const char* qgemv_last_error(void) { return g_msg; }
+
+int qgemv_last_error_code(void) { return g_code; }
+
+}  // extern "C"

@@ -54,6 +54,18 @@ def w_fp32(g: np.random.Generator, N: int, K: int, sigma: float = 0.02) -> np.nd
     return (g.standard_normal((N, K), dtype=np.float32) * np.float32(sigma))
 
 
+def q4_0_random_blocks(g: np.random.Generator, N: int, K: int,
+                       sigma_d: float = 0.003) -> np.ndarray:
+    """Canonical Q4_0 rows with uniformly random nibbles and a signed fp16
+    scale ~ N(0, sigma_d): every byte pattern of a block is a valid block."""
+    nb = K // 32
+    blocks = np.empty((N, nb, 18), dtype=np.uint8)
+    d = (g.standard_normal((N, nb), dtype=np.float32) * np.float32(sigma_d)).astype(np.float16)
+    blocks[:, :, 0:2] = d.view(np.uint8).reshape(N, nb, 2)
+    blocks[:, :, 2:] = g.integers(0, 256, size=(N, nb, 16), dtype=np.uint8)
+    return blocks.reshape(N, nb * 18)
+
+
 def cbk_centroids(L: int, sigma: float = 0.02) -> np.ndarray:
     """Sorted fp16 mid-rank quantiles of N(0, sigma); strictly increasing."""
     c = (sigma * ndtri((np.arange(L) + 0.5) / L)).astype(np.float16)

@@ -1,0 +1,192 @@
+"""Thin ctypes binding of the C ABI in ``include/qgemv.h``.
+
+The functions keep the C names and only marshal arguments (pointers and
+sizes); every step of the computation runs in ``libqgemv.so``.  The library
+is loaded on first use from ``bit_weight_only_gb300/_build``; if it is
+missing, ``load()`` raises: there is no CPU fallback.
+
+``QGemv`` wraps one handle for torch users: it takes canonical inputs as
+torch tensors or numpy arrays (host or CUDA) and runs on CUDA tensors.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+Q4_0, CBK4, CBK8, PQ2_0, AQLM_2X8 = 1, 2, 3, 4, 5
+FORMATS = {"q4_0": Q4_0, "cbk4": CBK4, "cbk8": CBK8, "pq2_0": PQ2_0, "aqlm_2x8": AQLM_2X8}
+QGEMV_OK, QGEMV_ERR_ARG, QGEMV_ERR_ALIGN, QGEMV_ERR_CUDA, QGEMV_ERR_TIMEOUT, QGEMV_ERR_NOMEM = range(6)
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "libqgemv.so")
+
+# Every exported symbol of include/qgemv.h with its ctypes signature.
+_SIGNATURES = {
+    "qgemv_packed_bytes": (ctypes.c_int64, [ctypes.c_int, ctypes.c_int64, ctypes.c_int64]),
+    "qgemv_create": (ctypes.c_void_p, [ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
+                                       ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
+    "qgemv_run": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                                 ctypes.c_void_p, ctypes.c_void_p]),
+    "qgemv_dequant": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
+    "qgemv_quantize_q4_0": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
+                                           ctypes.c_void_p, ctypes.c_void_p]),
+    "qgemv_status": (ctypes.c_int, [ctypes.c_void_p]),
+    "qgemv_destroy": (None, [ctypes.c_void_p]),
+    "qgemv_last_error": (ctypes.c_char_p, []),
+    "qgemv_last_error_code": (ctypes.c_int, []),
+}
+
+_lib = None
+
+
+class QgemvError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"qgemv error {code}: {msg}")
+        self.code = code
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load libqgemv.so (once) and declare the ABI's signatures."""
+    global _lib
+    if _lib is None:
+        path = path or LIB_PATH
+        if not os.path.exists(path):
+            raise ImportError(f"libqgemv.so not built ({path}); run "
+                              "`python -m bit_weight_only_gb300.build` (needs nvcc)")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def _fmt(fmt) -> int:
+    return FORMATS[fmt] if isinstance(fmt, str) else int(fmt)
+
+
+def _check(rc: int):
+    if rc != QGEMV_OK:
+        raise QgemvError(rc, qgemv_last_error())
+    return rc
+
+
+def _stream_ptr(stream) -> int | None:
+    if stream is None:
+        return None
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream  # torch.cuda.Stream
+
+
+# --------------------------------------------------------- C-ABI mirrors ----
+
+def qgemv_packed_bytes(fmt, N: int, K: int) -> int:
+    return int(load().qgemv_packed_bytes(_fmt(fmt), N, K))
+
+
+def qgemv_create(fmt, N: int, K: int, packed: int, scales: int | None,
+                 codebooks: int | None) -> int:
+    """Pointers are raw addresses (host or device).  Returns the handle."""
+    h = load().qgemv_create(_fmt(fmt), N, K, packed, scales, codebooks)
+    if not h:
+        raise QgemvError(qgemv_last_error_code(), qgemv_last_error())
+    return h
+
+
+def qgemv_run(h: int, x: int, M: int, y: int, stream=None) -> int:
+    return _check(load().qgemv_run(h, x, M, y, _stream_ptr(stream)))
+
+
+def qgemv_dequant(h: int, w_out: int, stream=None) -> int:
+    return _check(load().qgemv_dequant(h, w_out, _stream_ptr(stream)))
+
+
+def qgemv_quantize_q4_0(w: int, N: int, K: int, packed_out: int, stream=None) -> int:
+    return _check(load().qgemv_quantize_q4_0(w, N, K, packed_out, _stream_ptr(stream)))
+
+
+def qgemv_status(h: int) -> int:
+    return _check(load().qgemv_status(h))
+
+
+def qgemv_destroy(h: int) -> None:
+    load().qgemv_destroy(h)
+
+
+def qgemv_last_error() -> str:
+    return (load().qgemv_last_error() or b"").decode()
+
+
+def qgemv_last_error_code() -> int:
+    return int(load().qgemv_last_error_code())
+
+
+# ----------------------------------------------------------- torch helper --
+
+def _addr(a):
+    """(address, keepalive) of a torch tensor / numpy array / None."""
+    if a is None:
+        return None, None
+    if isinstance(a, np.ndarray):
+        a = np.ascontiguousarray(a)
+        return a.ctypes.data, a
+    a = a.contiguous()
+    return a.data_ptr(), a
+
+
+class QGemv:
+    """One packed weight matrix on the GPU.
+
+    ``QGemv(fmt, N, K, packed, scales=None, codebooks=None)`` copies the
+    canonical inputs into the library; ``gemv(x)`` returns y = x . W^T as a
+    new fp32 CUDA tensor, ``run(x, y)`` writes into ``y``."""
+
+    def __init__(self, fmt, N: int, K: int, packed, scales=None, codebooks=None):
+        self.fmt, self.N, self.K = _fmt(fmt), int(N), int(K)
+        p, kp = _addr(packed)
+        s, ks = _addr(scales)
+        c, kc = _addr(codebooks)
+        self.handle = qgemv_create(self.fmt, self.N, self.K, p, s, c)
+        del kp, ks, kc
+
+    def run(self, x, y, stream=None):
+        M = x.shape[0]
+        qgemv_run(self.handle, x.data_ptr(), M, y.data_ptr(), stream)
+        return y
+
+    def gemv(self, x, stream=None):
+        import torch
+        y = torch.empty((x.shape[0], self.N), dtype=torch.float32, device=x.device)
+        return self.run(x.contiguous(), y, stream)
+
+    def dequant(self, stream=None):
+        import torch
+        w = torch.empty((self.N, self.K), dtype=torch.float32, device="cuda")
+        qgemv_dequant(self.handle, w.data_ptr(), stream)
+        return w
+
+    def status(self):
+        return qgemv_status(self.handle)
+
+    def close(self):
+        if getattr(self, "handle", None):
+            qgemv_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def quantize_q4_0(w, stream=None):
+    """Q4_0 quantizer on the GPU: fp32 CUDA tensor [N, K] -> uint8 CUDA tensor."""
+    import torch
+    N, K = w.shape
+    out = torch.empty(qgemv_packed_bytes(Q4_0, N, K), dtype=torch.uint8, device=w.device)
+    qgemv_quantize_q4_0(w.contiguous().data_ptr(), N, K, out.data_ptr(), stream)
+    return out

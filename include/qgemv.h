@@ -1,0 +1,134 @@
+/*
+ * qgemv.h -- C ABI of the weight-only quantized decode GEMV for GB300 (sm_103a)
+ *
+ *     y[M x N] = x[M x K] . dequant(W)^T ,   1 <= M <= 16
+ *
+ * W is an N x K weight matrix (N outputs, K inputs) held in a packed low-bit
+ * format; x holds M fp16 activation rows; y receives M fp32 output rows.  The
+ * packed weights stream from HBM, are decoded in registers and multiplied and
+ * accumulated in fp32 by the library's CUDA kernels.  The problem statement
+ * (M rows, N outputs, K inputs per output) is the one of "Making a ternary
+ * reasoning model fast in vLLM", section "Reading the prompt and writing the
+ * answer"; the formats are listed with their sources below.
+ *
+ * Conventions for every call:
+ *   - Sizes are int64_t element counts; all multi-byte values little-endian.
+ *   - Device pointers are CUDA device (or managed) addresses on the current
+ *     device.  `stream` is a cudaStream_t passed as void* (NULL = the legacy
+ *     default stream).
+ *   - A call returns QGEMV_OK (0) or one of the QGEMV_ERR_* codes; the handle
+ *     constructor returns NULL on error.  qgemv_last_error() then gives a
+ *     thread-local message.  No call aborts the process or throws.
+ *   - Argument errors are found on the host before anything is launched or
+ *     allocated.
+ *   - Calls that launch kernels are asynchronous on `stream` unless stated
+ *     otherwise.
+ */
+#ifndef QGEMV_H
+#define QGEMV_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Weight formats.  "Canonical" is the byte layout the caller passes in. */
+typedef enum {
+  /* ggml-style Q4_0 ("Model quantization, read carefully", sections "The
+   * ladder" and "Anatomy of a block"): blocks of 32 weights along K, each
+   * {fp16 d; uint8 qs[16]} = 18 bytes, 4.5 bits per weight.  Byte i of qs
+   * holds element i in its low nibble and element i+16 in its high nibble;
+   * the weight is (q - 8) * d.  packed = N*K/32 blocks, row-major over rows
+   * n; K % 32 == 0; scales = codebooks = NULL.                              */
+  QGEMV_Q4_0 = 1,
+  /* Scalar 4-bit codebook ("Trapetum benchmarks", "Kernel microbenchmarks":
+   * 4-bit index into K = 16 centroids): packed = uint8 [N][K/2], byte j of a
+   * row holds k = 2j (low nibble) and k = 2j+1 (high nibble); codebooks =
+   * 16 fp16 centroids shared by the whole matrix; K % 2 == 0; scales = NULL. */
+  QGEMV_CBK4 = 2,
+  /* Scalar 8-bit codebook (same page: uint8 index into 256 centroids, the
+   * 8-bit LM head): packed = uint8 [N][K]; codebooks = 256 fp16; any K.    */
+  QGEMV_CBK8 = 3,
+  /* PQ2_0 ternary ("Making a ternary reasoning model fast in vLLM", "Anatomy
+   * of a PQ2_0 block"): blocks of 128 weights along K, {fp16 d; uint8
+   * qs[32]} = 34 bytes; byte j holds elements 4j..4j+3 as two-bit codes from
+   * the low end; codes 0,1,2,3 decode to -1,0,+1,+2 times d.  packed = N*K/128
+   * blocks, one row of blocks per output; K % 128 == 0.                      */
+  QGEMV_PQ2_0 = 4,
+  /* AQLM 2x8 additive codebooks ("Trapetum benchmarks", "Additive
+   * vector-quantization GEMV" and "Llama-2-70B in 2 bits"): per group of 8
+   * weights along K two uint8 codes; w[n][8g+j] = s[n] * (C0[c0][j] +
+   * C1[c1][j]).  packed = codes uint8 [N][K/8][2] (codebook 0 first);
+   * scales = fp16 [N]; codebooks = fp16 [2][256][8]; K % 8 == 0.          */
+  QGEMV_AQLM_2X8 = 5
+} qgemv_format;
+
+/* Status codes. */
+enum {
+  QGEMV_OK = 0,
+  QGEMV_ERR_ARG = 1,     /* bad format, size, M, null pointer or handle     */
+  QGEMV_ERR_ALIGN = 2,   /* x or y not aligned as required                  */
+  QGEMV_ERR_CUDA = 3,    /* a CUDA call failed (message has its error text) */
+  QGEMV_ERR_TIMEOUT = 4, /* a kernel's bounded wait gave up (qgemv_status)  */
+  QGEMV_ERR_NOMEM = 5    /* device or host allocation failed                */
+};
+
+typedef struct qgemv_ctx* qgemv_handle; /* opaque */
+
+/* Bytes of the canonical packed weights for (format, N, K); 0 if invalid. */
+int64_t qgemv_packed_bytes(int format, int64_t N, int64_t K);
+
+/* Create a handle for one weight matrix.
+ *   packed, scales, codebooks: canonical inputs as described per format
+ *     (unused ones must be NULL).  Each may be a host or a device pointer
+ *     (told apart with cudaPointerGetAttributes); the data is copied into
+ *     library-owned device memory and re-laid out there ("prepared" tiles),
+ *     so the caller may free its buffers once this call returns.
+ *   The call allocates the handle's device buffers (prepared weights and a
+ *   small per-handle workspace), runs the re-layout kernel on the legacy
+ *   default stream and synchronizes before returning.
+ * Returns NULL on error (see qgemv_last_error).                              */
+qgemv_handle qgemv_create(int format, int64_t N, int64_t K, const void* packed,
+                          const void* scales, const void* codebooks);
+
+/* y = x . dequant(W)^T for M rows.
+ *   x: device fp16 [M][K] row-major, 4-byte aligned.
+ *   y: device fp32 [M][N] row-major, 4-byte aligned; fully overwritten.
+ *   1 <= M <= 16.
+ * Asynchronous on `stream`; no allocation, no synchronization, so it can be
+ * captured in a CUDA graph.  The handle's workspace is shared by its runs:
+ * one handle must not run on two streams at the same time.  Results are
+ * bitwise reproducible run to run for a given (handle, M).                  */
+int qgemv_run(qgemv_handle h, const void* x, int M, float* y, void* stream);
+
+/* Write the decoded weights, fp32 [N][K] row-major, to device memory w_out
+ * (the exact value of every weight; read back from the prepared tiles, so it
+ * also checks the re-layout).  Asynchronous on `stream`.                     */
+int qgemv_dequant(qgemv_handle h, float* w_out, void* stream);
+
+/* Q4_0 quantizer on the device: fp32 weights [N][K] (device) -> canonical
+ * Q4_0 blocks (device, N*K/32*18 bytes).  Per block: d = (signed value of
+ * largest magnitude, first on ties) / -8 in fp32; q = clamp(round(w/d) + 8,
+ * 0, 15) with an IEEE fp32 division and round half away from zero; d stored
+ * as fp16 (nearest even).  An all-zero block stores q = 8.  Asynchronous.  */
+int qgemv_quantize_q4_0(const float* w, int64_t N, int64_t K, void* packed_out,
+                        void* stream);
+
+/* Synchronize with the handle's last run and return QGEMV_ERR_TIMEOUT if a
+ * kernel of it gave up a bounded wait (then clear that flag), else QGEMV_OK. */
+int qgemv_status(qgemv_handle h);
+
+/* Release the handle's device memory (synchronizes the device first).
+ * NULL is accepted and ignored.                                             */
+void qgemv_destroy(qgemv_handle h);
+
+/* Message and code of the last error on the calling thread ("" / 0 if none). */
+const char* qgemv_last_error(void);
+int qgemv_last_error_code(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QGEMV_H */

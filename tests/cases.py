@@ -1,0 +1,33 @@
+"""Canonical test inputs, drawn only from the seeded generators.
+
+``make_case`` returns the canonical packed bytes, scales and codebooks of one
+format as numpy arrays; both the CUDA path and the oracle are fed from them.
+Q4_0 here uses random (valid) blocks; the end-to-end tests that start from
+fp32 weights let each side run its own quantizer.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from bit_weight_only_gb300 import inputs
+
+MIN_K = {"q4_0": 32, "cbk4": 2, "cbk8": 1, "pq2_0": 128, "aqlm_2x8": 8}
+
+
+def make_case(fmt: str, N: int, K: int, tag: str = "case", seed: int = 0):
+    g = inputs.rng(f"{tag}/{fmt}/{N}x{K}", seed)
+    if fmt == "q4_0":
+        return inputs.q4_0_random_blocks(g, N, K), None, None
+    if fmt in ("cbk4", "cbk8"):
+        L = 16 if fmt == "cbk4" else 256
+        cb = inputs.cbk_centroids(L)
+        return inputs.cbk_packed(g, N, K, 4 if L == 16 else 8, inputs.cbk_cell_probs(cb)), None, cb
+    if fmt == "pq2_0":
+        return inputs.pq2_packed(g, N, K), None, None
+    if fmt == "aqlm_2x8":
+        return inputs.aqlm_inputs(g, N, K)
+    raise ValueError(fmt)
+
+
+def make_x(M: int, K: int, tag: str = "x", seed: int = 0) -> np.ndarray:
+    return inputs.x_fp16(inputs.rng(f"{tag}/{M}x{K}", seed), M, K)

@@ -1,0 +1,89 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds and
+loads, exports every function ``include/qgemv.h`` declares, and rejects bad
+arguments on the host before launching anything."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from bit_weight_only_gb300 import build, qgemv
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return qgemv.load()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "qgemv.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(qgemv_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for f in ("qgemv_create", "qgemv_run", "qgemv_destroy", "qgemv_dequant",
+              "qgemv_last_error", "qgemv_packed_bytes", "qgemv_quantize_q4_0", "qgemv_status"):
+        assert f in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in qgemv.h but not exported"
+    assert set(declared_functions()) <= set(qgemv._SIGNATURES)
+
+
+def test_packed_bytes_matches_formats(lib):
+    assert qgemv.qgemv_packed_bytes("q4_0", 4096, 4096) == 4096 * 128 * 18
+    assert qgemv.qgemv_packed_bytes("pq2_0", 5120, 17408) == 5120 * 136 * 34
+    assert qgemv.qgemv_packed_bytes("aqlm_2x8", 4096, 4096) == 4_194_304
+    assert qgemv.qgemv_packed_bytes("cbk4", 7, 10) == 35
+    assert qgemv.qgemv_packed_bytes("cbk8", 7, 9) == 63
+    assert qgemv.qgemv_packed_bytes("q4_0", 7, 48) == 0
+    assert qgemv.qgemv_packed_bytes(99, 7, 64) == 0
+
+
+@pytest.mark.parametrize("args, fragment", [
+    ((99, 8, 64, 1, None, None), "unknown format"),
+    ((qgemv.Q4_0, 8, 48, 1, None, None), "invalid shape"),
+    ((qgemv.Q4_0, 0, 64, 1, None, None), "invalid shape"),
+    ((qgemv.PQ2_0, 8, 64, 1, None, None), "invalid shape"),
+    ((qgemv.Q4_0, 8, 64, None, None, None), "packed is NULL"),
+    ((qgemv.Q4_0, 8, 64, 1, 1, None), "takes no scales"),
+])
+def test_create_rejects_bad_arguments_on_host(lib, args, fragment):
+    h = lib.qgemv_create(*args)
+    assert not h
+    assert fragment in qgemv.qgemv_last_error()
+    assert qgemv.qgemv_last_error_code() == qgemv.QGEMV_ERR_ARG
+
+
+def test_run_rejects_bad_handle_and_m(lib):
+    assert lib.qgemv_run(None, 16, 1, 16, None) == qgemv.QGEMV_ERR_ARG
+    bogus = ctypes.create_string_buffer(256)  # not a handle: magic check fails
+    assert lib.qgemv_run(ctypes.addressof(bogus), 16, 1, 16, None) == qgemv.QGEMV_ERR_ARG
+    assert lib.qgemv_dequant(None, 16, None) == qgemv.QGEMV_ERR_ARG
+    assert lib.qgemv_status(None) == qgemv.QGEMV_ERR_ARG
+    lib.qgemv_destroy(None)  # NULL is accepted
+
+
+def test_quantizer_rejects_bad_shape(lib):
+    assert lib.qgemv_quantize_q4_0(16, 4, 48, 16, None) == qgemv.QGEMV_ERR_ARG
+    assert lib.qgemv_quantize_q4_0(None, 4, 64, 16, None) == qgemv.QGEMV_ERR_ARG
+
+
+def test_product_path_does_not_reference_the_oracle():
+    """The CUDA package never imports, loads or links the oracle."""
+    pkg = os.path.join(ROOT, "bit_weight_only_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        if "_build" in dirpath:
+            continue
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "liboracle" not in text, f
