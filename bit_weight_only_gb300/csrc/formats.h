@@ -40,6 +40,10 @@ const FormatOps* ops_pq2();
 const FormatOps* ops_cbk4();
 const FormatOps* ops_cbk8();
 
+// Record the calling thread's last error (what qgemv_last_error returns);
+// returns `code`.  QGEMV_OK clears it.
+int report_error(int code, const char* msg);
+
 // Q4_0 quantizer (canonical output).
 cudaError_t quantize_q4_0(const float* w, int64_t N, int64_t K, uint8_t* out, cudaStream_t s);
 

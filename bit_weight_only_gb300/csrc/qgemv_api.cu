@@ -104,6 +104,13 @@ cudaError_t g_setup_err[8];
 
 }  // namespace
 
+namespace qgemv {
+int report_error(int code, const char* msg) {
+  if (code == QGEMV_OK) return ok();
+  return set_error(code, "%s", msg);
+}
+}  // namespace qgemv
+
 struct qgemv_ctx {
   uint32_t magic;
   int format;

@@ -32,6 +32,9 @@ _SIGNATURES = {
     "qgemv_quantize_q4_0": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
                                            ctypes.c_void_p, ctypes.c_void_p]),
     "qgemv_status": (ctypes.c_int, [ctypes.c_void_p]),
+    "qgemv_run_q4_0_noalloc": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
+                                              ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
+                                              ctypes.c_void_p]),
     "qgemv_destroy": (None, [ctypes.c_void_p]),
     "qgemv_last_error": (ctypes.c_char_p, []),
     "qgemv_last_error_code": (ctypes.c_int, []),
@@ -106,6 +109,12 @@ def qgemv_dequant(h: int, w_out: int, stream=None) -> int:
 
 def qgemv_quantize_q4_0(w: int, N: int, K: int, packed_out: int, stream=None) -> int:
     return _check(load().qgemv_quantize_q4_0(w, N, K, packed_out, _stream_ptr(stream)))
+
+
+def qgemv_run_q4_0_noalloc(packed: int, N: int, K: int, x: int, M: int, y: int,
+                           stream=None) -> int:
+    """Allocation-free Q4_0 GEMV on canonical device blocks (no handle)."""
+    return _check(load().qgemv_run_q4_0_noalloc(packed, N, K, x, M, y, _stream_ptr(stream)))
 
 
 def qgemv_status(h: int) -> int:

@@ -123,6 +123,31 @@ int qgemv_status(qgemv_handle h);
  * NULL is accepted and ignored.                                             */
 void qgemv_destroy(qgemv_handle h);
 
+/* Allocation-free Q4_0 GEMV.  No counterpart in the paper: this is a service
+ * for callers that cannot allocate device memory when they need the product,
+ * for instance code running inside a framework whose caching allocator owns
+ * all device memory, or a latency-critical loop that must not pay for (or
+ * synchronize on) cudaMalloc.  It needs no handle: it reads the caller's
+ * canonical Q4_0 blocks directly (same layout as QGEMV_Q4_0 above).
+ *   packed: device, N*K/32 blocks of 18 bytes, 2-byte aligned; K % 32 == 0.
+ *   x: device fp16 [M][K]; y: device fp32 [M][N] (4-byte aligned); 1<=M<=16.
+ * The call allocates nothing: its scratch (split-K partial sums and arrival
+ * counters) lives in one static device array of 8 MiB that every GPU which
+ * loads this library holds until the process exits.  A shape needs
+ * ceil(K/2048) * M * N * 4 bytes of partial sums (none when K <= 2048) plus
+ * 4 bytes per 64 rows of counters; a shape that needs more than 8 MiB is
+ * rejected with QGEMV_ERR_ARG and a message giving both sizes.
+ * All calls share that array and leave in it whatever the last one wrote; the
+ * counters, which must start at zero, are cleared by every call.  Calls whose
+ * executions overlap on the GPU (different streams, or several processes'
+ * worth of work on one context) race on the array: serialize them.
+ * The first call on a device finds the array's device address
+ * (cudaGetSymbolAddress) with that device current and sets the kernel's
+ * shared-memory limit; make that first call before any stream capture.
+ * Asynchronous on `stream`; results are bitwise reproducible call to call.  */
+int qgemv_run_q4_0_noalloc(const void* packed, int64_t N, int64_t K, const void* x, int M,
+                           float* y, void* stream);
+
 /* Message and code of the last error on the calling thread ("" / 0 if none). */
 const char* qgemv_last_error(void);
 int qgemv_last_error_code(void);
