@@ -48,19 +48,20 @@ __device__ __forceinline__ float fma2_f16_f32(uint32_t a2, uint32_t b2, float c)
 
 // ------------------------------------------------------------------ CBK4 --
 //
-// Tile: 128 rows x 256 k.  Warp w <-> k slice 32w..32w+31, lane l <-> rows
-// 4l..4l+3.  codes [j][t = w*32 + l][16 B]: the 16 canonical index bytes of
-// row 4l+j for the slice (byte b = k pair b: low nibble k = 2b, high 2b+1).
-// Activations are staged as fp16 pairs: xs word (q * MP + m) = (x[2q][m],
-// x[2q+1][m]).
+// Tile: 128 rows x 512 k.  Slice s <-> k 64s..64s+63, lane slot t = 32s + l
+// <-> rows 4l..4l+3.  Codes [j][h][t][16 B]: the 32 canonical index bytes of
+// row 4l+j for the slice, 16 per half h (byte b = k pair b: low nibble
+// k = 2b, high nibble k = 2b+1).  Activations are staged as fp16 pairs: xs
+// word (q * MP + m) = (x[2q][m], x[2q+1][m]).
 struct FmtCBK4 {
-  static constexpr int kKW = 32;
-  static constexpr int kKT = kKW * kSlices;                          // 256
-  static constexpr int kTileBytes = kLaneSlots * kRowsPerLane * 16;  // 16384
-  __host__ __device__ static constexpr int stages(int M) { return M <= 8 ? 6 : 4; }
+  static constexpr int kKW = 64;
+  static constexpr int kKT = kKW * kSlices;                              // 512
+  static constexpr int kTileBytes = kLaneSlots * kRowsPerLane * 32;      // 32768
+  __host__ __device__ static constexpr int stages(int M) { return M <= 4 ? 4 : 2; }
   static constexpr int kSharedBytes = kLutBytes;
   static constexpr float kOutScale = 1.0f;
-  using XRegs = XRegsT<1>;
+  static constexpr int kSumGroups = 1;  // unused: codebook values carry no offset
+  using XRegs = XRegsT<2>;
 
   __device__ static void init_shared(uint8_t* lut, const GemvParams& p, int tid, int nthreads) {
     const uint16_t* cb = static_cast<const uint16_t*>(p.aux);
@@ -73,28 +74,40 @@ struct FmtCBK4 {
 
   template <int M>
   __device__ static void load_x(XRegs& xr, const GemvParams& p, int kt, int slice, int lane) {
-    load_x_slice<kKW, M, 1>(xr, p, kt, slice, lane);
+    load_x_slice<kKW, M, 2>(xr, p, kt, slice, lane);
   }
 
-  // fp16 pairs, no scaling; no block sums needed
+  // fp16 pairs, unscaled: lane l holds k pair l of the slice
   template <int M>
-  __device__ static void stage_x(float* xs, float (&)[M], const XRegs& xr, int lane) {
+  __device__ static void stage_x(float* xs, float (&)[kSumGroups][M], const XRegs& xr, int lane) {
     constexpr int MP = mpad(M);
-    uint16_t* xh = reinterpret_cast<uint16_t*>(xs);
+    uint32_t* xw = reinterpret_cast<uint32_t*>(xs);
 #pragma unroll
-    for (int m = 0; m < MP; ++m) xh[((lane >> 1) * MP + m) * 2 + (lane & 1)] = m < M ? xr.v[m][0] : 0;
+    for (int m = 0; m < MP; ++m)
+      xw[lane * MP + m] = m < M ? (static_cast<uint32_t>(xr.v[m][0]) |
+                                   (static_cast<uint32_t>(xr.v[m][1]) << 16)) : 0u;
+  }
+
+  template <int R>
+  __device__ static void load_codes32(const uint8_t* stage, int j0, int t, uint4 (&lo)[R],
+                                      uint4 (&hi)[R]) {
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+      lo[j] = lds128(stage + (((j0 + j) * 2 + 0) * kLaneSlots + t) * 16);
+      hi[j] = lds128(stage + (((j0 + j) * 2 + 1) * kLaneSlots + t) * 16);
+    }
   }
 
   template <int M, int RPW>
-  __device__ static void tile_math(const uint8_t* stage, const float* xs, const float (&)[M],
-                                   RowAcc<M, RPW>& yacc, uint8_t* lut, int slice, int half,
-                                   int lane, uint64_t* empty_bar) {
+  __device__ static void tile_math(const uint8_t* stage, const float* xs,
+                                   const float (&)[kSumGroups][M], RowAcc<M, RPW>& yacc,
+                                   uint8_t* lut, int slice, int half, int lane,
+                                   uint64_t* empty_bar) {
     constexpr int MP = mpad(M);
     const int t = slice * 32 + lane;
     const int j0 = half * RPW;
-    uint4 cwd[RPW];
-#pragma unroll
-    for (int j = 0; j < RPW; ++j) cwd[j] = lds128(stage + ((j0 + j) * kLaneSlots + t) * 16);
+    uint4 clo[RPW], chi[RPW];
+    load_codes32<RPW>(stage, j0, t, clo, chi);
     release_stage(empty_bar, lane);
     const uint32_t lane4 = static_cast<uint32_t>(lane) << 2;
     const uint32_t* xw = reinterpret_cast<const uint32_t*>(xs);
@@ -104,9 +117,9 @@ struct FmtCBK4 {
     for (int j = 0; j < RPW; ++j)
 #pragma unroll
       for (int m = 0; m < M; ++m) acc[j][m] = 0.f;
-    constexpr int UI = (M > 8) ? 1 : 4;
+    constexpr int UI = (M > 8) ? 1 : (M > 4 ? 2 : 8);
 #pragma unroll UI
-    for (int i = 0; i < 4; ++i) {     // word i: k pairs 4i..4i+3
+    for (int i = 0; i < 8; ++i) {     // word i: k pairs 4i..4i+3
 #pragma unroll
       for (int bp = 0; bp < 4; ++bp) {
         const int q = 4 * i + bp;
@@ -123,7 +136,7 @@ struct FmtCBK4 {
         }
 #pragma unroll
         for (int j = 0; j < RPW; ++j) {
-          const uint32_t wv = word_of(cwd[j], i);
+          const uint32_t wv = i < 4 ? word_of(clo[j], i) : word_of(chi[j], i - 4);
           const uint32_t c2 = lds32(lut, lut_offset(wv, lane4, bp));
 #pragma unroll
           for (int m = 0; m < M; ++m) acc[j][m] = fma2_f16_f32(c2, xp[m], acc[j][m]);
@@ -137,17 +150,18 @@ struct FmtCBK4 {
 
 // ------------------------------------------------------------------ CBK8 --
 //
-// Tile: 128 rows x 128 k.  Warp w <-> k slice 16w..16w+15 (lanes 0..15 stage
-// one activation each), lane l <-> rows 4l..4l+3.  codes [j][t][16 B]: the 16
-// canonical index bytes of row 4l+j for the slice.  Activations are staged
-// as fp32 pairs (x[2q][m], x[2q+1][m]).
+// Tile: 128 rows x 256 k.  Slice s <-> k 32s..32s+31, lane slot t = 32s + l
+// <-> rows 4l..4l+3.  Codes [j][h][t][16 B]: the 32 canonical index bytes of
+// row 4l+j for the slice.  Activations are staged as fp32 pairs
+// (x[2q][m], x[2q+1][m]).
 struct FmtCBK8 {
-  static constexpr int kKW = 16;
-  static constexpr int kKT = kKW * kSlices;                          // 128
-  static constexpr int kTileBytes = kLaneSlots * kRowsPerLane * 16;  // 16384
-  __host__ __device__ static constexpr int stages(int M) { return M <= 8 ? 6 : 4; }
+  static constexpr int kKW = 32;
+  static constexpr int kKT = kKW * kSlices;                              // 256
+  static constexpr int kTileBytes = kLaneSlots * kRowsPerLane * 32;      // 32768
+  __host__ __device__ static constexpr int stages(int M) { return M <= 4 ? 4 : 2; }
   static constexpr int kSharedBytes = kLutBytes;
   static constexpr float kOutScale = 1.0f;
+  static constexpr int kSumGroups = 1;  // unused
   using XRegs = XRegsT<1>;
 
   __device__ static void init_shared(uint8_t* lut, const GemvParams& p, int tid, int nthreads) {
@@ -160,32 +174,26 @@ struct FmtCBK8 {
 
   template <int M>
   __device__ static void load_x(XRegs& xr, const GemvParams& p, int kt, int slice, int lane) {
-    const int64_t k = static_cast<int64_t>(kt) * kKT + slice * kKW + lane;
-    const unsigned short* xb = reinterpret_cast<const unsigned short*>(p.x);
-#pragma unroll
-    for (int m = 0; m < M; ++m)
-      xr.v[m][0] = (lane < kKW && k < p.K) ? __ldg(xb + m * p.K + k) : static_cast<unsigned short>(0);
+    load_x_slice<kKW, M, 1>(xr, p, kt, slice, lane);
   }
 
   template <int M>
-  __device__ static void stage_x(float* xs, float (&)[M], const XRegs& xr, int lane) {
+  __device__ static void stage_x(float* xs, float (&)[kSumGroups][M], const XRegs& xr, int lane) {
     constexpr int MP = mpad(M);
-    if (lane < kKW) {
 #pragma unroll
-      for (int m = 0; m < MP; ++m)
-        xs[((lane >> 1) * MP + m) * 2 + (lane & 1)] = m < M ? h2f(xr.v[m][0]) : 0.f;
-    }
+    for (int m = 0; m < MP; ++m)
+      xs[((lane >> 1) * MP + m) * 2 + (lane & 1)] = m < M ? h2f(xr.v[m][0]) : 0.f;
   }
 
   template <int M, int RPW>
-  __device__ static void tile_math(const uint8_t* stage, const float* xs, const float (&)[M],
-                                   RowAcc<M, RPW>& yacc, uint8_t* lut, int slice, int half,
-                                   int lane, uint64_t* empty_bar) {
+  __device__ static void tile_math(const uint8_t* stage, const float* xs,
+                                   const float (&)[kSumGroups][M], RowAcc<M, RPW>& yacc,
+                                   uint8_t* lut, int slice, int half, int lane,
+                                   uint64_t* empty_bar) {
     const int t = slice * 32 + lane;
     const int j0 = half * RPW;
-    uint4 cwd[RPW];
-#pragma unroll
-    for (int j = 0; j < RPW; ++j) cwd[j] = lds128(stage + ((j0 + j) * kLaneSlots + t) * 16);
+    uint4 clo[RPW], chi[RPW];
+    FmtCBK4::load_codes32<RPW>(stage, j0, t, clo, chi);
     release_stage(empty_bar, lane);
     const uint32_t lane4 = static_cast<uint32_t>(lane) << 2;
 
@@ -194,16 +202,16 @@ struct FmtCBK8 {
     for (int j = 0; j < RPW; ++j)
 #pragma unroll
       for (int m = 0; m < M; ++m) acc[j][m] = make_float2(0.f, 0.f);
-    constexpr int UI = (M > 8) ? 1 : 4;
+    constexpr int UI = (M > 8) ? 1 : (M > 4 ? 2 : 8);
 #pragma unroll UI
-    for (int i = 0; i < 4; ++i) {       // word i: k = 4i..4i+3 -> pairs 2i, 2i+1
+    for (int i = 0; i < 8; ++i) {       // word i: k = 4i..4i+3 -> pairs 2i, 2i+1
 #pragma unroll
       for (int pp = 0; pp < 2; ++pp) {
         float2 xv[M];
         load_xpairs<M>(xs, 2 * i + pp, xv);
 #pragma unroll
         for (int j = 0; j < RPW; ++j) {
-          const uint32_t wv = word_of(cwd[j], i);
+          const uint32_t wv = i < 4 ? word_of(clo[j], i) : word_of(chi[j], i - 4);
           const float2 w2 = make_float2(__uint_as_float(lds32(lut, lut_offset(wv, lane4, 2 * pp))),
                                         __uint_as_float(lds32(lut, lut_offset(wv, lane4, 2 * pp + 1))));
 #pragma unroll
@@ -226,20 +234,22 @@ struct FmtCBK8 {
 namespace qgemv {
 namespace cbk {
 
-// Prepared code chunk (tile, j, t) <- the 16 canonical index bytes of row
-// rt*128 + 4l + j covering the warp's k slice; bytes past the row are 0.
+// Prepared code chunk (tile, j, h, t) <- 16 of the 32 canonical index bytes
+// of row rt*128 + 4l + j covering the slice (half h); bytes past the row are 0.
 template <class F, int kBitsPerIndex>
 __global__ void prepare_kernel(const uint8_t* __restrict__ canon, int64_t N, int64_t K, int nKT,
                                int64_t nchunks, uint8_t* __restrict__ tiles) {
   const int64_t row_bytes = K * kBitsPerIndex / 8;
+  constexpr int kChunks = kRowsPerLane * 2 * kLaneSlots;
   for (int64_t ci = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; ci < nchunks;
        ci += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t tile = ci / (kRowsPerLane * kLaneSlots);
-    const int rem = static_cast<int>(ci % (kRowsPerLane * kLaneSlots));
-    const int j = rem / kLaneSlots, t = rem % kLaneSlots;
+    const int64_t tile = ci / kChunks;
+    const int rem = static_cast<int>(ci % kChunks);
+    const int jh = rem / kLaneSlots, t = rem % kLaneSlots;
+    const int j = jh / 2, h = jh % 2;
     const int cw = t / 32, lane = t % 32;
     const int64_t n = (tile / nKT) * kTileRows + kRowsPerLane * lane + j;
-    const int64_t b0 = ((tile % nKT) * F::kKT + cw * F::kKW) * kBitsPerIndex / 8;
+    const int64_t b0 = ((tile % nKT) * F::kKT + cw * F::kKW) * kBitsPerIndex / 8 + 16 * h;
     uint32_t w[4] = {0, 0, 0, 0};
     if (n < N) {
       for (int i = 0; i < 16; ++i) {
@@ -247,7 +257,7 @@ __global__ void prepare_kernel(const uint8_t* __restrict__ canon, int64_t N, int
         if (b < row_bytes) w[i / 4] |= static_cast<uint32_t>(canon[n * row_bytes + b]) << (8 * (i % 4));
       }
     }
-    *reinterpret_cast<uint4*>(tiles + tile * F::kTileBytes + (j * kLaneSlots + t) * 16) =
+    *reinterpret_cast<uint4*>(tiles + tile * F::kTileBytes + (jh * kLaneSlots + t) * 16) =
         make_uint4(w[0], w[1], w[2], w[3]);
   }
 }
@@ -265,8 +275,10 @@ __global__ void dequant_kernel(const uint8_t* __restrict__ tiles, const uint16_t
     const int64_t tile = (n / kTileRows) * nKT + k / F::kKT;
     const int kk = static_cast<int>(k % F::kKT);
     const int cw = kk / F::kKW, el = kk % F::kKW;
-    const uint8_t byte =
-        tiles[tile * F::kTileBytes + (j * kLaneSlots + cw * 32 + lane) * 16 + el * kBitsPerIndex / 8];
+    const int byte_in_row = el * kBitsPerIndex / 8;  // 0..31
+    const int h = byte_in_row / 16;
+    const uint8_t byte = tiles[tile * F::kTileBytes + ((j * 2 + h) * kLaneSlots + cw * 32 + lane) * 16 +
+                               byte_in_row % 16];
     const int idx = kBitsPerIndex == 8 ? byte : ((el & 1) ? (byte >> 4) : (byte & 15));
     w[e] = h2f(cb[idx]);
   }

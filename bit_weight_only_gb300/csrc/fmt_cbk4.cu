@@ -10,7 +10,7 @@ namespace {
 using F = FmtCBK4;
 
 cudaError_t prepare(const PrepareArgs& a, cudaStream_t s) {
-  const int64_t nchunks = a.nRT * a.nKT * kRowsPerLane * kLaneSlots;
+  const int64_t nchunks = a.nRT * a.nKT * kRowsPerLane * 2 * kLaneSlots;
   cbk::prepare_kernel<F, 4><<<cbk::grid_for(nchunks, 256), 256, 0, s>>>(a.packed, a.N, a.K, a.nKT,
                                                                        nchunks, a.tiles);
   cudaError_t e = cudaGetLastError();

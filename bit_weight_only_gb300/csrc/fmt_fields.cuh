@@ -1,7 +1,7 @@
 // fmt_fields.cuh -- Q4_0 and PQ2_0: formats whose weight is an integer code
 // times a per-block fp16 scale.
 //
-// Decode trick ("denormal fields").  In the prepared tiles every 32-bit word
+// Decode trick ("subnormal fields").  In the prepared tiles every 32-bit word
 // holds the codes of consecutive k (8 nibbles for Q4_0, 16 two-bit fields
 // for PQ2_0).  A code sitting at bit p of a word, masked out with one AND,
 // *is* the fp32 bit pattern of the subnormal q * 2^(p - 149), exactly.
@@ -19,6 +19,9 @@
 // "Anatomy of a block": 32 weights, one fp16 scale, (q - 8) * d, 18 bytes.
 // PQ2_0 -- "Making a ternary reasoning model fast in vLLM", "Anatomy of a
 // PQ2_0 block": 128 weights, fp16 d, two-bit codes 0..3 -> -1, 0, +1, +2.
+//
+// Both use 32 code bytes per (row, lane slot) per tile: codes region
+// [j = row 0..3 of the slot][h = 16-byte half][t = lane slot 0..255][16 B].
 #pragma once
 
 #include "gemv_kernel.cuh"
@@ -27,27 +30,43 @@ namespace qgemv {
 
 constexpr int kFieldExp = -40;                       // outputs carry 2^kFieldExp
 constexpr float kFieldOutScale = pow2f(-kFieldExp);  // 2^40
+constexpr int kCodeBytes32 = kRowsPerLane * 2 * kLaneSlots * 16;  // 32 KB of codes per tile
 
 // 2^e as a float (exact for -126 <= e <= 127).
 __device__ __forceinline__ float exp2i(int e) { return __int_as_float((127 + e) << 23); }
 
+// The eight code words of rows j0 .. j0+R-1 of lane slot t.
+template <int R>
+__device__ __forceinline__ void load_codes32(const uint8_t* stage, int j0, int t,
+                                             uint4 (&lo)[R], uint4 (&hi)[R]) {
+#pragma unroll
+  for (int j = 0; j < R; ++j) {
+    lo[j] = lds128(stage + (((j0 + j) * 2 + 0) * kLaneSlots + t) * 16);
+    hi[j] = lds128(stage + (((j0 + j) * 2 + 1) * kLaneSlots + t) * 16);
+  }
+}
+
+__device__ __forceinline__ uint32_t word8(const uint4& lo, const uint4& hi, int i) {
+  return i < 4 ? word_of(lo, i) : word_of(hi, i - 4);
+}
 
 // ------------------------------------------------------------------ Q4_0 --
 //
-// Tile: 128 rows x 256 k.  Slice s <-> Q4_0 block s of the tile (32 k);
-// lane slot t = 32s + l <-> rows 4l..4l+3.
-//   codes  [j = 0..3][t][16 B]  row 4l+j, block s: word i holds k = 8i..8i+7
-//          of the block, nibble jj at bits 4jj.
-//   scales [t][4 x fp16]        d of rows 4l..4l+3, block s.
+// Tile: 128 rows x 512 k.  Slice s <-> Q4_0 blocks 2s, 2s+1 of the tile
+// (64 k); lane slot t = 32s + l <-> rows 4l..4l+3.
+//   codes  word i (0..7) of (row, slot) holds k = 8i..8i+7 of the slice,
+//          nibble jj at bits 4jj; words 0-3 are block 2s, 4-7 block 2s+1.
+//   scales [t][j = 0..3][b = 0..1] fp16: d of row 4l+j, block 2s+b.
 struct FmtQ4_0 {
-  static constexpr int kKW = 32;
-  static constexpr int kKT = kKW * kSlices;                   // 256
-  static constexpr int kCodeBytes = kLaneSlots * kRowsPerLane * 16;
-  static constexpr int kTileBytes = kCodeBytes + kLaneSlots * 8;  // 18432
-  __host__ __device__ static constexpr int stages(int) { return 6; }
+  static constexpr int kKW = 64;
+  static constexpr int kKT = kKW * kSlices;                        // 512
+  static constexpr int kCodeBytes = kCodeBytes32;
+  static constexpr int kTileBytes = kCodeBytes + kLaneSlots * 16;  // 36864
+  __host__ __device__ static constexpr int stages(int M) { return M <= 4 ? 4 : 3; }
   static constexpr int kSharedBytes = 0;
   static constexpr float kOutScale = kFieldOutScale;
-  using XRegs = XRegsT<1>;
+  static constexpr int kSumGroups = 2;  // one offset sum per Q4_0 block of the slice
+  using XRegs = XRegsT<2>;
 
   // bit position of the nibble of k = 8i + jj once extracted (jj >= 5 are
   // taken from the word shifted right by 12)
@@ -57,77 +76,88 @@ struct FmtQ4_0 {
 
   template <int M>
   __device__ static void load_x(XRegs& xr, const GemvParams& p, int kt, int slice, int lane) {
-    load_x_slice<kKW, M, 1>(xr, p, kt, slice, lane);
+    load_x_slice<kKW, M, 2>(xr, p, kt, slice, lane);
   }
 
   template <int M>
-  __device__ static void stage_x(float* xs, float (&xsum)[M], const XRegs& xr, int lane) {
-    stage_x_slice<M, 1>(xs, xsum, xr, lane,
-                        [](int kk) { return exp2i(109 - field_pos(kk & 7)); });
+  __device__ static void stage_x(float* xs, float (&xsum)[kSumGroups][M], const XRegs& xr, int lane) {
+    stage_x_slice<M, 2, kSumGroups>(xs, xsum, xr, lane,
+                                    [](int kk) { return exp2i(109 - field_pos(kk & 7)); });
   }
 
   template <int M, int RPW>
-  __device__ static void tile_math(const uint8_t* stage, const float* xs, const float (&xsum)[M],
-                                   RowAcc<M, RPW>& yacc, uint8_t*, int slice, int half, int lane,
-                                   uint64_t* empty_bar) {
+  __device__ static void tile_math(const uint8_t* stage, const float* xs,
+                                   const float (&xsum)[kSumGroups][M], RowAcc<M, RPW>& yacc,
+                                   uint8_t*, int slice, int half, int lane, uint64_t* empty_bar) {
     const int t = slice * 32 + lane;
     const int j0 = half * RPW;
-    uint4 cwd[RPW];
-#pragma unroll
-    for (int j = 0; j < RPW; ++j) cwd[j] = lds128(stage + ((j0 + j) * kLaneSlots + t) * 16);
-    const uint2 sc = *reinterpret_cast<const uint2*>(stage + kCodeBytes + t * 8);
-    release_stage(empty_bar, lane);
+    // rows per pass (register budget): all rows for small M, fewer above
+    constexpr int RP = (M > 12) ? 1 : ((M > 8 && RPW > 2) ? 2 : RPW);
+    // For large M the codes are loaded pass by pass and the stage is released
+    // after the last pass, to keep registers for the accumulators.
+    constexpr bool kLate = RP < RPW;
+    uint4 clo[RP], chi[RP];
+    if (!kLate) load_codes32<RP>(stage, j0, t, clo, chi);
+    const uint4 sc = lds128(stage + kCodeBytes + t * 16);
+    if (!kLate) release_stage(empty_bar, lane);
 
-    // scales of this lane's rows j0..j0+RPW-1 (two fp16 per 32-bit word)
-    float dr[RPW];
+    // scale of (row j0 + r, block b): fp16 number 2*(j0 + r) + b of sc
+    float dr[RPW][2];
 #pragma unroll
     for (int r = 0; r < RPW; ++r) {
-      const uint32_t sw = (RPW == 4) ? (r < 2 ? sc.x : sc.y) : (half ? sc.y : sc.x);
-      dr[r] = h2f((r & 1) ? (sw >> 16) : (sw & 0xffffu));
+      const uint32_t sw = (RPW == 4) ? word_of(sc, r) : (half ? word_of(sc, 2 + r) : word_of(sc, r));
+      dr[r][0] = h2f(sw & 0xffffu);
+      dr[r][1] = h2f(sw >> 16);
     }
-    // code offset 8: subtract 8 * sum(x) (in the 2^-40 scaled domain)
-    float off[M];
-#pragma unroll
-    for (int m = 0; m < M; ++m) off[m] = xsum[m] * (-8.0f * pow2f(kFieldExp));
 
-    constexpr int RP = (M > 8 && RPW > 2) ? 2 : RPW;  // rows per pass (register budget)
 #pragma unroll
     for (int pass = 0; pass < RPW / RP; ++pass) {
-      float2 acc[RP][M];
-#pragma unroll
-      for (int r = 0; r < RP; ++r)
-#pragma unroll
-        for (int m = 0; m < M; ++m) acc[r][m] = make_float2(off[m], 0.f);
-      constexpr int UI = (M > 8) ? 1 : 4;  // bound live ranges for large M
-#pragma unroll UI
-      for (int i = 0; i < 4; ++i) {
-        uint32_t fld[RP][8];
-#pragma unroll
-        for (int r = 0; r < RP; ++r) {
-          const uint32_t wv = word_of(cwd[pass * RP + r], i);
-          const uint32_t wh = wv >> 12;
-#pragma unroll
-          for (int jj = 0; jj < 8; ++jj)
-            fld[r][jj] = (jj <= 4 ? wv : wh) & (0xfu << field_pos(jj));
-        }
-#pragma unroll
-        for (int pp = 0; pp < 4; ++pp) {
-          float2 xv[M];
-          load_xpairs<M>(xs, 4 * i + pp, xv);
-#pragma unroll
-          for (int r = 0; r < RP; ++r) {
-            const float2 w2 = make_float2(u2f(fld[r][2 * pp]), u2f(fld[r][2 * pp + 1]));
-#pragma unroll
-            for (int m = 0; m < M; ++m) acc[r][m] = __ffma2_rn(w2, xv[m], acc[r][m]);
-          }
-        }
+      if (kLate) {
+        load_codes32<RP>(stage, j0 + pass * RP, t, clo, chi);
+        if (pass == RPW / RP - 1) release_stage(empty_bar, lane);
       }
 #pragma unroll
-      for (int r = 0; r < RP; ++r) {
-        float a[M];
+      for (int b = 0; b < 2; ++b) {
+        // code offset 8: start from -8 * sum(x) (in the 2^-40 scaled domain)
+        float2 acc[RP][M];
 #pragma unroll
-        for (int m = 0; m < M; ++m) a[m] = acc[r][m].x + acc[r][m].y;
-        yacc.add_row(pass * RP + r, dr[pass * RP + r], a);
+        for (int r = 0; r < RP; ++r)
+#pragma unroll
+          for (int m = 0; m < M; ++m)
+            acc[r][m] = make_float2(xsum[b][m] * (-8.0f * pow2f(kFieldExp)), 0.f);
+        constexpr int UI = (M > 8) ? 1 : 4;  // bound live ranges for large M
+#pragma unroll UI
+        for (int ii = 0; ii < 4; ++ii) {
+          const int i = 4 * b + ii;
+          uint32_t fld[RP][8];
+#pragma unroll
+          for (int r = 0; r < RP; ++r) {
+            const int rr = kLate ? r : pass * RP + r;
+            const uint32_t wv = word8(clo[rr], chi[rr], i);
+            const uint32_t wh = wv >> 12;
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj)
+              fld[r][jj] = (jj <= 4 ? wv : wh) & (0xfu << field_pos(jj));
+          }
+#pragma unroll
+          for (int pp = 0; pp < 4; ++pp) {
+            float2 xv[M];
+            load_xpairs<M>(xs, 4 * i + pp, xv);
+#pragma unroll
+            for (int r = 0; r < RP; ++r) {
+              const float2 w2 = make_float2(u2f(fld[r][2 * pp]), u2f(fld[r][2 * pp + 1]));
+#pragma unroll
+              for (int m = 0; m < M; ++m) acc[r][m] = __ffma2_rn(w2, xv[m], acc[r][m]);
+            }
+          }
+        }
+#pragma unroll
+        for (int r = 0; r < RP; ++r) {
+          float a[M];
+#pragma unroll
+          for (int m = 0; m < M; ++m) a[m] = acc[r][m].x + acc[r][m].y;
+          yacc.add_row(pass * RP + r, dr[pass * RP + r][b], a);
+        }
       }
     }
   }
@@ -135,20 +165,21 @@ struct FmtQ4_0 {
 
 // ----------------------------------------------------------------- PQ2_0 --
 //
-// Tile: 128 rows x 512 k (four PQ2 blocks).  Slice s <-> k 64s..64s+63,
-// i.e. half (s & 1) of block s >> 1; lane slot t = 32s + l <-> rows 4l..4l+3.
-//   codes  [j][t][16 B]  word i holds k = 16i..16i+15 of the slice, two-bit
-//          field jj at bits 2jj.
-//   scales [blk = 0..3][l][4 x fp16]  d of rows 4l..4l+3, block blk.
+// Tile: 128 rows x 1024 k (eight PQ2 blocks).  Slice s <-> block s of the
+// tile (128 k); lane slot t = 32s + l <-> rows 4l..4l+3.
+//   codes  word i (0..7) of (row, slot) holds k = 16i..16i+15 of the block,
+//          two-bit field jj at bits 2jj.
+//   scales [t][j = 0..3] fp16: d of row 4l+j, block s.
 struct FmtPQ2 {
-  static constexpr int kKW = 64;
-  static constexpr int kKT = kKW * kSlices;                   // 512
-  static constexpr int kCodeBytes = kLaneSlots * kRowsPerLane * 16;
-  static constexpr int kTileBytes = kCodeBytes + 4 * 32 * 8;  // 17408
-  __host__ __device__ static constexpr int stages(int) { return 6; }
+  static constexpr int kKW = 128;
+  static constexpr int kKT = kKW * kSlices;                       // 1024
+  static constexpr int kCodeBytes = kCodeBytes32;
+  static constexpr int kTileBytes = kCodeBytes + kLaneSlots * 8;  // 34816
+  __host__ __device__ static constexpr int stages(int M) { return M <= 4 ? 4 : (M <= 8 ? 3 : 2); }
   static constexpr int kSharedBytes = 0;
   static constexpr float kOutScale = kFieldOutScale;
-  using XRegs = XRegsT<2>;
+  static constexpr int kSumGroups = 1;
+  using XRegs = XRegsT<4>;
 
   __host__ __device__ static constexpr int field_pos(int jj) { return jj <= 10 ? 2 * jj : 2 * jj - 12; }
 
@@ -156,55 +187,55 @@ struct FmtPQ2 {
 
   template <int M>
   __device__ static void load_x(XRegs& xr, const GemvParams& p, int kt, int slice, int lane) {
-    load_x_slice<kKW, M, 2>(xr, p, kt, slice, lane);
+    load_x_slice<kKW, M, 4>(xr, p, kt, slice, lane);
   }
 
   template <int M>
-  __device__ static void stage_x(float* xs, float (&xsum)[M], const XRegs& xr, int lane) {
-    stage_x_slice<M, 2>(xs, xsum, xr, lane,
-                        [](int kk) { return exp2i(109 - field_pos(kk & 15)); });
+  __device__ static void stage_x(float* xs, float (&xsum)[kSumGroups][M], const XRegs& xr, int lane) {
+    stage_x_slice<M, 4, kSumGroups>(xs, xsum, xr, lane,
+                                    [](int kk) { return exp2i(109 - field_pos(kk & 15)); });
   }
 
   template <int M, int RPW>
-  __device__ static void tile_math(const uint8_t* stage, const float* xs, const float (&xsum)[M],
-                                   RowAcc<M, RPW>& yacc, uint8_t*, int slice, int half, int lane,
-                                   uint64_t* empty_bar) {
+  __device__ static void tile_math(const uint8_t* stage, const float* xs,
+                                   const float (&xsum)[kSumGroups][M], RowAcc<M, RPW>& yacc,
+                                   uint8_t*, int slice, int half, int lane, uint64_t* empty_bar) {
     const int t = slice * 32 + lane;
     const int j0 = half * RPW;
-    uint4 cwd[RPW];
-#pragma unroll
-    for (int j = 0; j < RPW; ++j) cwd[j] = lds128(stage + ((j0 + j) * kLaneSlots + t) * 16);
-    const uint2 sc =
-        *reinterpret_cast<const uint2*>(stage + kCodeBytes + ((slice >> 1) * 32 + lane) * 8);
-    release_stage(empty_bar, lane);
+    constexpr int RP = (M > 12) ? 1 : ((M > 8 && RPW > 2) ? 2 : RPW);
+    constexpr bool kLate = RP < RPW;  // see FmtQ4_0::tile_math
+    uint4 clo[RP], chi[RP];
+    if (!kLate) load_codes32<RP>(stage, j0, t, clo, chi);
+    const uint2 sc = *reinterpret_cast<const uint2*>(stage + kCodeBytes + t * 8);
+    if (!kLate) release_stage(empty_bar, lane);
 
-    // scales of this lane's rows j0..j0+RPW-1 (two fp16 per 32-bit word)
     float dr[RPW];
 #pragma unroll
     for (int r = 0; r < RPW; ++r) {
       const uint32_t sw = (RPW == 4) ? (r < 2 ? sc.x : sc.y) : (half ? sc.y : sc.x);
       dr[r] = h2f((r & 1) ? (sw >> 16) : (sw & 0xffffu));
     }
-    // code offset 1: subtract sum(x) (in the 2^-40 scaled domain)
-    float off[M];
-#pragma unroll
-    for (int m = 0; m < M; ++m) off[m] = xsum[m] * (-pow2f(kFieldExp));
 
-    constexpr int RP = (M > 8 && RPW > 2) ? 2 : RPW;
 #pragma unroll
     for (int pass = 0; pass < RPW / RP; ++pass) {
+      if (kLate) {
+        load_codes32<RP>(stage, j0 + pass * RP, t, clo, chi);
+        if (pass == RPW / RP - 1) release_stage(empty_bar, lane);
+      }
+      // code offset 1: start from -sum(x) (in the 2^-40 scaled domain)
       float2 acc[RP][M];
 #pragma unroll
       for (int r = 0; r < RP; ++r)
 #pragma unroll
-        for (int m = 0; m < M; ++m) acc[r][m] = make_float2(off[m], 0.f);
-      constexpr int UI = (M > 8) ? 1 : 4;  // bound live ranges for large M
+        for (int m = 0; m < M; ++m) acc[r][m] = make_float2(xsum[0][m] * (-pow2f(kFieldExp)), 0.f);
+      constexpr int UI = (M > 8) ? 1 : (M > 4 ? 2 : 8);
 #pragma unroll UI
-      for (int i = 0; i < 4; ++i) {
+      for (int i = 0; i < 8; ++i) {
         uint32_t wv[RP], wh[RP];
 #pragma unroll
         for (int r = 0; r < RP; ++r) {
-          wv[r] = word_of(cwd[pass * RP + r], i);
+          const int rr = kLate ? r : pass * RP + r;
+          wv[r] = word8(clo[rr], chi[rr], i);
           wh[r] = wv[r] >> 12;
         }
 #pragma unroll
@@ -213,9 +244,9 @@ struct FmtPQ2 {
           load_xpairs<M>(xs, 8 * i + pp, xv);
 #pragma unroll
           for (int r = 0; r < RP; ++r) {
-            const int j0 = 2 * pp, j1 = 2 * pp + 1;
-            const uint32_t f0 = (j0 <= 10 ? wv[r] : wh[r]) & (3u << field_pos(j0));
-            const uint32_t f1 = (j1 <= 10 ? wv[r] : wh[r]) & (3u << field_pos(j1));
+            const int f0i = 2 * pp, f1i = 2 * pp + 1;
+            const uint32_t f0 = (f0i <= 10 ? wv[r] : wh[r]) & (3u << field_pos(f0i));
+            const uint32_t f1 = (f1i <= 10 ? wv[r] : wh[r]) & (3u << field_pos(f1i));
             const float2 w2 = make_float2(u2f(f0), u2f(f1));
 #pragma unroll
             for (int m = 0; m < M; ++m) acc[r][m] = __ffma2_rn(w2, xv[m], acc[r][m]);

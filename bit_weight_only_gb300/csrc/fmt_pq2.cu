@@ -22,25 +22,27 @@ __device__ __forceinline__ uint32_t canon_code(const uint8_t* qs, int e) {
   return (qs[e >> 2] >> (2 * (e & 3))) & 3u;
 }
 
-// One thread per 32-bit code word of the prepared stream.
+// One thread per 32-bit code word of the prepared stream.  Word i = 4h + wi
+// of (row j, lane slot t) holds elements 16i..16i+15 of block `slice`.
 __global__ void prepare_codes(const uint8_t* __restrict__ canon, int64_t N, int64_t K, int nKT,
                               int64_t nwords, uint32_t* __restrict__ tiles) {
   constexpr int kWordsPerTile = F::kTileBytes / 4;
   constexpr int kCodeWords = F::kCodeBytes / 4;
   const int64_t nb = K / 128;
-  for (int64_t wi = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; wi < nwords;
-       wi += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t tile = wi / kCodeWords;
-    const int off = static_cast<int>(wi % kCodeWords);
-    const int chunk = off / 4, i = off % 4;
-    const int j = chunk / kLaneSlots, t = chunk % kLaneSlots;
+  for (int64_t wa = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; wa < nwords;
+       wa += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t tile = wa / kCodeWords;
+    const int off = static_cast<int>(wa % kCodeWords);
+    const int chunk = off / 4, wi = off % 4;
+    const int jh = chunk / kLaneSlots, t = chunk % kLaneSlots;
+    const int j = jh / 2, h = jh % 2;
     const int cw = t / 32, lane = t % 32;
     const int64_t n = (tile / nKT) * kTileRows + kRowsPerLane * lane + j;
-    const int64_t b = static_cast<int64_t>(tile % nKT) * 4 + (cw >> 1);
+    const int64_t b = static_cast<int64_t>(tile % nKT) * kSlices + cw;
     uint32_t word = 0;
     if (n < N && b < nb) {
       const uint8_t* qs = canon + (n * nb + b) * kBlockBytes + 2;
-      const int e0 = 64 * (cw & 1) + 16 * i;
+      const int e0 = 16 * (4 * h + wi);
 #pragma unroll
       for (int jj = 0; jj < 16; ++jj) word |= canon_code(qs, e0 + jj) << (2 * jj);
     }
@@ -48,15 +50,16 @@ __global__ void prepare_codes(const uint8_t* __restrict__ canon, int64_t N, int6
   }
 }
 
-// One thread per (tile, block-in-tile, lane): four fp16 scales.
+// One thread per (tile, t): the four fp16 scales of rows 4l..4l+3, block `slice`.
 __global__ void prepare_scales(const uint8_t* __restrict__ canon, int64_t N, int64_t K, int nKT,
                                int64_t nitems, uint8_t* __restrict__ tiles) {
   const int64_t nb = K / 128;
   for (int64_t it = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; it < nitems;
        it += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t tile = it / 128;
-    const int blk = static_cast<int>((it % 128) / 32), lane = static_cast<int>(it % 32);
-    const int64_t b = static_cast<int64_t>(tile % nKT) * 4 + blk;
+    const int64_t tile = it / kLaneSlots;
+    const int t = static_cast<int>(it % kLaneSlots);
+    const int cw = t / 32, lane = t % 32;
+    const int64_t b = static_cast<int64_t>(tile % nKT) * kSlices + cw;
     uint16_t h[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -70,7 +73,7 @@ __global__ void prepare_scales(const uint8_t* __restrict__ canon, int64_t N, int
     uint2 v;
     v.x = h[0] | (static_cast<uint32_t>(h[1]) << 16);
     v.y = h[2] | (static_cast<uint32_t>(h[3]) << 16);
-    *reinterpret_cast<uint2*>(tiles + tile * F::kTileBytes + F::kCodeBytes + (blk * 32 + lane) * 8) = v;
+    *reinterpret_cast<uint2*>(tiles + tile * F::kTileBytes + F::kCodeBytes + t * 8) = v;
   }
 }
 
@@ -85,13 +88,13 @@ __global__ void dequant_kernel(const uint8_t* __restrict__ tiles, int64_t N, int
     const int64_t tile = (n / kTileRows) * nKT + k / F::kKT;
     const int kk = static_cast<int>(k % F::kKT);
     const int cw = kk / F::kKW, el = kk % F::kKW;
+    const int i = el / 16, jj = el % 16;
     const int t = cw * 32 + lane;
     const uint8_t* tb = tiles + tile * F::kTileBytes;
-    const uint32_t word =
-        *reinterpret_cast<const uint32_t*>(tb + (j * kLaneSlots + t) * 16 + 4 * (el / 16));
-    const int c = static_cast<int>((word >> (2 * (el % 16))) & 3u);
-    const uint16_t hb = *reinterpret_cast<const uint16_t*>(
-        tb + F::kCodeBytes + ((cw >> 1) * 32 + lane) * 8 + 2 * j);
+    const uint32_t word = *reinterpret_cast<const uint32_t*>(
+        tb + ((j * 2 + i / 4) * kLaneSlots + t) * 16 + 4 * (i % 4));
+    const int c = static_cast<int>((word >> (2 * jj)) & 3u);
+    const uint16_t hb = *reinterpret_cast<const uint16_t*>(tb + F::kCodeBytes + t * 8 + 2 * j);
     w[e] = static_cast<float>(c - 1) * h2f(hb);  // exact
   }
 }
@@ -108,7 +111,7 @@ cudaError_t prepare(const PrepareArgs& a, cudaStream_t s) {
                                                       reinterpret_cast<uint32_t*>(a.tiles));
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const int64_t nitems = T * 128;
+  const int64_t nitems = T * kLaneSlots;
   prepare_scales<<<grid_for(nitems, 256), 256, 0, s>>>(a.packed, a.N, a.K, a.nKT, nitems, a.tiles);
   return cudaGetLastError();
 }

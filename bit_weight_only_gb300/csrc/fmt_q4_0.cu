@@ -23,32 +23,35 @@ __device__ __forceinline__ uint32_t canon_q(const uint8_t* qs, int e) {
   return e < 16 ? (qs[e] & 0xfu) : (qs[e - 16] >> 4);
 }
 
-// One thread per 32-bit code word of the prepared stream.
+// One thread per 32-bit code word of the prepared stream.  Word wi of half h
+// of (row j, lane slot t) holds elements 8wi..8wi+7 of block 2*slice + h.
 __global__ void prepare_codes(const uint8_t* __restrict__ canon, int64_t N, int64_t K, int nKT,
                               int64_t nwords, uint32_t* __restrict__ tiles) {
   constexpr int kWordsPerTile = F::kTileBytes / 4;
   constexpr int kCodeWords = F::kCodeBytes / 4;
   const int64_t nb = K / 32;
-  for (int64_t wi = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; wi < nwords;
-       wi += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t tile = wi / kCodeWords;
-    const int off = static_cast<int>(wi % kCodeWords);
-    const int chunk = off / 4, i = off % 4;
-    const int j = chunk / kLaneSlots, t = chunk % kLaneSlots;
+  for (int64_t wa = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; wa < nwords;
+       wa += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t tile = wa / kCodeWords;
+    const int off = static_cast<int>(wa % kCodeWords);
+    const int chunk = off / 4, wi = off % 4;
+    const int jh = chunk / kLaneSlots, t = chunk % kLaneSlots;
+    const int j = jh / 2, h = jh % 2;
     const int cw = t / 32, lane = t % 32;
     const int64_t n = (tile / nKT) * kTileRows + kRowsPerLane * lane + j;
-    const int64_t b = static_cast<int64_t>(tile % nKT) * kSlices + cw;
+    const int64_t b = static_cast<int64_t>(tile % nKT) * (F::kKT / 32) + 2 * cw + h;
     uint32_t word = 0;
     if (n < N && b < nb) {
       const uint8_t* qs = canon + (n * nb + b) * kBlockBytes + 2;
 #pragma unroll
-      for (int jj = 0; jj < 8; ++jj) word |= canon_q(qs, 8 * i + jj) << (4 * jj);
+      for (int jj = 0; jj < 8; ++jj) word |= canon_q(qs, 8 * wi + jj) << (4 * jj);
     }
     tiles[tile * kWordsPerTile + off] = word;
   }
 }
 
-// One thread per (tile, t): the four fp16 scales of rows 4l..4l+3.
+// One thread per (tile, t): the eight fp16 scales [j][b] of rows 4l..4l+3,
+// blocks 2*slice and 2*slice + 1.
 __global__ void prepare_scales(const uint8_t* __restrict__ canon, int64_t N, int64_t K, int nKT,
                                int64_t nitems, uint8_t* __restrict__ tiles) {
   const int64_t nb = K / 32;
@@ -57,21 +60,23 @@ __global__ void prepare_scales(const uint8_t* __restrict__ canon, int64_t N, int
     const int64_t tile = it / kLaneSlots;
     const int t = static_cast<int>(it % kLaneSlots);
     const int cw = t / 32, lane = t % 32;
-    const int64_t b = static_cast<int64_t>(tile % nKT) * kSlices + cw;
-    uint16_t h[4];
+    uint32_t v[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int64_t n = (tile / nKT) * kTileRows + kRowsPerLane * lane + j;
-      h[j] = 0;
-      if (n < N && b < nb) {
-        const uint8_t* blk = canon + (n * nb + b) * kBlockBytes;
-        h[j] = static_cast<uint16_t>(blk[0] | (blk[1] << 8));
+      uint32_t hw[2] = {0, 0};
+#pragma unroll
+      for (int bb = 0; bb < 2; ++bb) {
+        const int64_t b = static_cast<int64_t>(tile % nKT) * (F::kKT / 32) + 2 * cw + bb;
+        if (n < N && b < nb) {
+          const uint8_t* blk = canon + (n * nb + b) * kBlockBytes;
+          hw[bb] = static_cast<uint32_t>(blk[0] | (blk[1] << 8));
+        }
       }
+      v[j] = hw[0] | (hw[1] << 16);
     }
-    uint2 v;
-    v.x = h[0] | (static_cast<uint32_t>(h[1]) << 16);
-    v.y = h[2] | (static_cast<uint32_t>(h[3]) << 16);
-    *reinterpret_cast<uint2*>(tiles + tile * F::kTileBytes + F::kCodeBytes + t * 8) = v;
+    *reinterpret_cast<uint4*>(tiles + tile * F::kTileBytes + F::kCodeBytes + t * 16) =
+        make_uint4(v[0], v[1], v[2], v[3]);
   }
 }
 
@@ -87,11 +92,13 @@ __global__ void dequant_kernel(const uint8_t* __restrict__ tiles, int64_t N, int
     const int64_t tile = (n / kTileRows) * nKT + k / F::kKT;
     const int kk = static_cast<int>(k % F::kKT);
     const int cw = kk / F::kKW, el = kk % F::kKW;
+    const int h = el / 32, eb = el % 32;
     const int t = cw * 32 + lane;
     const uint8_t* tb = tiles + tile * F::kTileBytes;
-    const uint32_t word = *reinterpret_cast<const uint32_t*>(tb + (j * kLaneSlots + t) * 16 + 4 * (el / 8));
-    const int q = static_cast<int>((word >> (4 * (el % 8))) & 0xfu);
-    const uint16_t hb = *reinterpret_cast<const uint16_t*>(tb + F::kCodeBytes + t * 8 + 2 * j);
+    const uint32_t word =
+        *reinterpret_cast<const uint32_t*>(tb + ((j * 2 + h) * kLaneSlots + t) * 16 + 4 * (eb / 8));
+    const int q = static_cast<int>((word >> (4 * (eb % 8))) & 0xfu);
+    const uint16_t hb = *reinterpret_cast<const uint16_t*>(tb + F::kCodeBytes + t * 16 + 2 * (2 * j + h));
     w[e] = static_cast<float>(q - 8) * h2f(hb);  // exact: 4-bit int x fp16 fits fp32
   }
 }

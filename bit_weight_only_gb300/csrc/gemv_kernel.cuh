@@ -208,6 +208,13 @@ __global__ void __launch_bounds__(gemv_threads<M>(), 1) gemv_kernel(const GemvPa
     }
   }
 
+  // Programmatic dependent launch: the prologue above (barriers, tables, the
+  // first weight copies) touches nothing a previous kernel in the stream
+  // writes, so it may overlap that kernel's tail.  Everything below reads x
+  // or writes global memory, so it waits for the previous grid to finish.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
   // Position of tile t0 in the stream, advanced incrementally below.
   int64_t rt = t0 / p.nKT;
   int kt = static_cast<int>(t0 - rt * p.nKT);
@@ -237,7 +244,7 @@ __global__ void __launch_bounds__(gemv_threads<M>(), 1) gemv_kernel(const GemvPa
     }
 
     // Stage this tile's activations, then prefetch the next tile's.
-    float xsum[M];
+    float xsum[F::kSumGroups][M];
     __syncwarp();
     F::template stage_x<M>(xs, xsum, xr, lane);
     __syncwarp();
@@ -280,19 +287,23 @@ __global__ void __launch_bounds__(gemv_threads<M>(), 1) gemv_kernel(const GemvPa
         my_part[m * kTileRows + r] = v;
       }
     }
-    if (!owner) __threadfence();
     named_bar_sync(1, NT);
 
     if (!owner) {
+      // The barrier above orders every thread's partial stores before
+      // thread 0's device-scope fence and arrival (release); the last
+      // arriver fences again before the CTA reads the others' partials.
       const int64_t cf = cta_of_tile(cur_rt * p.nKT, p.T, G);
       const int64_t cl = cta_of_tile((cur_rt + 1) * p.nKT - 1, p.T, G);
       if (tid == 0) {
+        __threadfence();
         const int old = atomicAdd(&p.counters[cur_rt], 1);
-        s_flag = (old == static_cast<int>(cl - cf));
+        const bool last = (old == static_cast<int>(cl - cf));
+        if (last) __threadfence();
+        s_flag = last;
       }
       named_bar_sync(1, NT);
       if (s_flag) {
-        __threadfence();
         for (int o = tid; o < kTileRows * M; o += NT) {
           const int r = o % kTileRows;
           const int m = o / kTileRows;
@@ -346,8 +357,8 @@ __device__ __forceinline__ void load_x_slice(XRegsT<LPL>& xr, const GemvParams& 
     }
 }
 
-template <int M, int LPL, class Scale>
-__device__ __forceinline__ void stage_x_slice(float* xs, float (&xsum)[M],
+template <int M, int LPL, int SUBS, class Scale>
+__device__ __forceinline__ void stage_x_slice(float* xs, float (&xsum)[SUBS][M],
                                               const XRegsT<LPL>& xr, int lane, Scale scale) {
   constexpr int MP = mpad(M);
 #pragma unroll
@@ -360,9 +371,12 @@ __device__ __forceinline__ void stage_x_slice(float* xs, float (&xsum)[M],
       s += v;
       xs[((kk >> 1) * MP + m) * 2 + (kk & 1)] = v * scale(kk);
     }
+    // sums over each group of 32 / SUBS consecutive lanes, then gathered so
+    // every lane holds all SUBS group sums
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-    xsum[m] = s;
+    for (int off = 16 / SUBS; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+#pragma unroll
+    for (int g = 0; g < SUBS; ++g) xsum[g][m] = __shfl_sync(0xffffffffu, s, g * (32 / SUBS));
   }
   if (MP > M) {  // keep padding lanes of the vector loads finite
 #pragma unroll

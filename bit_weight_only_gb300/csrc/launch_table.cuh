@@ -11,10 +11,24 @@ namespace qgemv {
 
 template <class F>
 struct LaunchTable {
+  // Launched with programmatic stream serialization: the kernel may start
+  // while the previous kernel on the stream drains; it runs its prologue
+  // (barriers, tables, first weight copies) and then waits on the previous
+  // grid (griddepcontrol.wait) before reading x or writing anything.
   template <int M>
   static cudaError_t launch_m(const GemvParams& p, int grid, cudaStream_t s) {
-    gemv_kernel<F, M><<<grid, gemv_threads<M>(), gemv_smem_bytes<F, M>(), s>>>(p);
-    return cudaGetLastError();
+    static_assert(gemv_smem_bytes<F, M>() <= 227 * 1024, "shared memory budget exceeded");
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(gemv_threads<M>());
+    cfg.dynamicSmemBytes = gemv_smem_bytes<F, M>();
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemv_kernel<F, M>, p);
   }
 
   template <int M>
