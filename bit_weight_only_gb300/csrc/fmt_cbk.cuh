@@ -34,6 +34,17 @@ __device__ __forceinline__ uint32_t lds32(const uint8_t* base, uint32_t off) {
   return *reinterpret_cast<const uint32_t*>(base + off);
 }
 
+// acc[0] += a.lo * b.lo, acc[1] += a.hi * b.hi  (f16 x f16 products, exact;
+// f32 accumulation)
+__device__ __forceinline__ void fma_f16x2_f32x2(uint32_t a2, uint32_t b2, float (&acc)[2]) {
+  asm("{\n\t.reg .f16 al, ah, bl, bh;\n\t"
+      "mov.b32 {al, ah}, %2;\n\tmov.b32 {bl, bh}, %3;\n\t"
+      "fma.rn.f32.f16 %0, al, bl, %0;\n\t"
+      "fma.rn.f32.f16 %1, ah, bh, %1;\n\t}"
+      : "+f"(acc[0]), "+f"(acc[1])
+      : "r"(a2), "r"(b2));
+}
+
 // d = a.lo * b.lo + (a.hi * b.hi + c)   (f16 x f16 products, f32 accumulation)
 __device__ __forceinline__ float fma2_f16_f32(uint32_t a2, uint32_t b2, float c) {
   float d;
@@ -77,9 +88,13 @@ struct FmtCBK4 {
     load_x_slice<kKW, M, 2>(xr, p, kt, slice, lane);
   }
 
+  struct XScale {};
+  __device__ static void x_scales(XScale&, int) {}
+
   // fp16 pairs, unscaled: lane l holds k pair l of the slice
   template <int M>
-  __device__ static void stage_x(float* xs, float (&)[kSumGroups][M], const XRegs& xr, int lane) {
+  __device__ static void stage_x(float* xs, float (&)[kSumGroups][M], const XRegs& xr,
+                                 const XScale&, int lane) {
     constexpr int MP = mpad(M);
     uint32_t* xw = reinterpret_cast<uint32_t*>(xs);
 #pragma unroll
@@ -112,20 +127,23 @@ struct FmtCBK4 {
     const uint32_t lane4 = static_cast<uint32_t>(lane) << 2;
     const uint32_t* xw = reinterpret_cast<const uint32_t*>(xs);
 
-    float acc[RPW][M];
+    // two accumulators per (row, m): even k and odd k, two independent chains
+    float acc[RPW][M][2];
 #pragma unroll
     for (int j = 0; j < RPW; ++j)
 #pragma unroll
-      for (int m = 0; m < M; ++m) acc[j][m] = 0.f;
+      for (int m = 0; m < M; ++m) acc[j][m][0] = acc[j][m][1] = 0.f;
     constexpr int UI = (M > 8) ? 1 : (M > 4 ? 2 : 8);
 #pragma unroll UI
     for (int i = 0; i < 8; ++i) {     // word i: k pairs 4i..4i+3
+      uint4 x4 = make_uint4(0, 0, 0, 0);
+      if constexpr (M == 1) x4 = *reinterpret_cast<const uint4*>(xw + 4 * i);
 #pragma unroll
       for (int bp = 0; bp < 4; ++bp) {
         const int q = 4 * i + bp;
         uint32_t xp[M];
         if constexpr (M == 1) {
-          xp[0] = xw[q];
+          xp[0] = word_of(x4, bp);
         } else {
 #pragma unroll
           for (int m = 0; m < MP; m += 2) {
@@ -139,12 +157,17 @@ struct FmtCBK4 {
           const uint32_t wv = i < 4 ? word_of(clo[j], i) : word_of(chi[j], i - 4);
           const uint32_t c2 = lds32(lut, lut_offset(wv, lane4, bp));
 #pragma unroll
-          for (int m = 0; m < M; ++m) acc[j][m] = fma2_f16_f32(c2, xp[m], acc[j][m]);
+          for (int m = 0; m < M; ++m) fma_f16x2_f32x2(c2, xp[m], acc[j][m]);
         }
       }
     }
 #pragma unroll
-    for (int j = 0; j < RPW; ++j) yacc.add_row(j, 1.0f, acc[j]);
+    for (int j = 0; j < RPW; ++j) {
+      float a[M];
+#pragma unroll
+      for (int m = 0; m < M; ++m) a[m] = acc[j][m][0] + acc[j][m][1];
+      yacc.add_row(j, 1.0f, a);
+    }
   }
 };
 
@@ -177,8 +200,12 @@ struct FmtCBK8 {
     load_x_slice<kKW, M, 1>(xr, p, kt, slice, lane);
   }
 
+  struct XScale {};
+  __device__ static void x_scales(XScale&, int) {}
+
   template <int M>
-  __device__ static void stage_x(float* xs, float (&)[kSumGroups][M], const XRegs& xr, int lane) {
+  __device__ static void stage_x(float* xs, float (&)[kSumGroups][M], const XRegs& xr,
+                                 const XScale&, int lane) {
     constexpr int MP = mpad(M);
 #pragma unroll
     for (int m = 0; m < MP; ++m)
@@ -205,10 +232,13 @@ struct FmtCBK8 {
     constexpr int UI = (M > 8) ? 1 : (M > 4 ? 2 : 8);
 #pragma unroll UI
     for (int i = 0; i < 8; ++i) {       // word i: k = 4i..4i+3 -> pairs 2i, 2i+1
+      // both pairs of the word at once for M == 1 (one 128-bit load)
+      float2 xv2[2][M];
+      if constexpr (M == 1) load_xpair_run<M, 2>(xs, 2 * i, xv2);
 #pragma unroll
       for (int pp = 0; pp < 2; ++pp) {
-        float2 xv[M];
-        load_xpairs<M>(xs, 2 * i + pp, xv);
+        if constexpr (M > 1) load_xpairs<M>(xs, 2 * i + pp, xv2[pp]);
+        const float2 (&xv)[M] = xv2[pp];
 #pragma unroll
         for (int j = 0; j < RPW; ++j) {
           const uint32_t wv = i < 4 ? word_of(clo[j], i) : word_of(chi[j], i - 4);

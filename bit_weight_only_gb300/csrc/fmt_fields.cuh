@@ -79,10 +79,16 @@ struct FmtQ4_0 {
     load_x_slice<kKW, M, 2>(xr, p, kt, slice, lane);
   }
 
+  struct XScale { float v[2]; };
+  __device__ static void x_scales(XScale& sc, int lane) {
+#pragma unroll
+    for (int i = 0; i < 2; ++i) sc.v[i] = exp2i(109 - field_pos((2 * lane + i) & 7));
+  }
+
   template <int M>
-  __device__ static void stage_x(float* xs, float (&xsum)[kSumGroups][M], const XRegs& xr, int lane) {
-    stage_x_slice<M, 2, kSumGroups>(xs, xsum, xr, lane,
-                                    [](int kk) { return exp2i(109 - field_pos(kk & 7)); });
+  __device__ static void stage_x(float* xs, float (&xsum)[kSumGroups][M], const XRegs& xr,
+                                 const XScale& sc, int lane) {
+    stage_x_slice<M, 2, kSumGroups>(xs, xsum, xr, lane, sc.v);
   }
 
   template <int M, int RPW>
@@ -139,15 +145,15 @@ struct FmtQ4_0 {
             for (int jj = 0; jj < 8; ++jj)
               fld[r][jj] = (jj <= 4 ? wv : wh) & (0xfu << field_pos(jj));
           }
+          float2 xv[4][M];
+          load_xpair_run<M, 4>(xs, 4 * i, xv);
 #pragma unroll
           for (int pp = 0; pp < 4; ++pp) {
-            float2 xv[M];
-            load_xpairs<M>(xs, 4 * i + pp, xv);
 #pragma unroll
             for (int r = 0; r < RP; ++r) {
               const float2 w2 = make_float2(u2f(fld[r][2 * pp]), u2f(fld[r][2 * pp + 1]));
 #pragma unroll
-              for (int m = 0; m < M; ++m) acc[r][m] = __ffma2_rn(w2, xv[m], acc[r][m]);
+              for (int m = 0; m < M; ++m) acc[r][m] = __ffma2_rn(w2, xv[pp][m], acc[r][m]);
             }
           }
         }
@@ -190,10 +196,16 @@ struct FmtPQ2 {
     load_x_slice<kKW, M, 4>(xr, p, kt, slice, lane);
   }
 
+  struct XScale { float v[4]; };
+  __device__ static void x_scales(XScale& sc, int lane) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) sc.v[i] = exp2i(109 - field_pos((4 * lane + i) & 15));
+  }
+
   template <int M>
-  __device__ static void stage_x(float* xs, float (&xsum)[kSumGroups][M], const XRegs& xr, int lane) {
-    stage_x_slice<M, 4, kSumGroups>(xs, xsum, xr, lane,
-                                    [](int kk) { return exp2i(109 - field_pos(kk & 15)); });
+  __device__ static void stage_x(float* xs, float (&xsum)[kSumGroups][M], const XRegs& xr,
+                                 const XScale& sc, int lane) {
+    stage_x_slice<M, 4, kSumGroups>(xs, xsum, xr, lane, sc.v);
   }
 
   template <int M, int RPW>
@@ -239,9 +251,13 @@ struct FmtPQ2 {
           wh[r] = wv[r] >> 12;
         }
 #pragma unroll
-        for (int pp = 0; pp < 8; ++pp) {
-          float2 xv[M];
-          load_xpairs<M>(xs, 8 * i + pp, xv);
+        for (int ph = 0; ph < 2; ++ph) {
+        float2 xv4[4][M];
+        load_xpair_run<M, 4>(xs, 8 * i + 4 * ph, xv4);
+#pragma unroll
+        for (int pq = 0; pq < 4; ++pq) {
+          const int pp = 4 * ph + pq;
+          const float2 (&xv)[M] = xv4[pq];
 #pragma unroll
           for (int r = 0; r < RP; ++r) {
             const int f0i = 2 * pp, f1i = 2 * pp + 1;
@@ -251,6 +267,7 @@ struct FmtPQ2 {
 #pragma unroll
             for (int m = 0; m < M; ++m) acc[r][m] = __ffma2_rn(w2, xv[m], acc[r][m]);
           }
+        }
         }
       }
 #pragma unroll

@@ -220,6 +220,8 @@ __global__ void __launch_bounds__(gemv_threads<M>(), 1) gemv_kernel(const GemvPa
   int kt = static_cast<int>(t0 - rt * p.nKT);
   typename F::XRegs xr;
   if (ntiles > 0) F::template load_x<M>(xr, p, kt, slice, lane);
+  typename F::XScale xscale;  // per-lane activation scaling, the same for every tile
+  F::x_scales(xscale, lane);
 
   int s = 0;           // stage of the tile being computed
   uint32_t ph = 0;     // its fill parity
@@ -246,7 +248,7 @@ __global__ void __launch_bounds__(gemv_threads<M>(), 1) gemv_kernel(const GemvPa
     // Stage this tile's activations, then prefetch the next tile's.
     float xsum[F::kSumGroups][M];
     __syncwarp();
-    F::template stage_x<M>(xs, xsum, xr, lane);
+    F::template stage_x<M>(xs, xsum, xr, xscale, lane);
     __syncwarp();
     const int kt_next = (kt + 1 == p.nKT) ? 0 : kt + 1;
     if (i + 1 < ntiles) F::template load_x<M>(xr, p, kt_next, slice, lane);
@@ -304,14 +306,27 @@ __global__ void __launch_bounds__(gemv_threads<M>(), 1) gemv_kernel(const GemvPa
       }
       named_bar_sync(1, NT);
       if (s_flag) {
+        // Contributor cc wrote this row tile in its side-0 slot, except the
+        // first one when its range began in an earlier row tile (side 1).
+        const bool cf_side1 = (cf * p.T / G) < cur_rt * p.nKT;
         for (int o = tid; o < kTileRows * M; o += NT) {
           const int r = o % kTileRows;
           const int m = o / kTileRows;
           float v = 0.f;
-          for (int64_t cc = cf; cc <= cl; ++cc) {
-            const int64_t cc_first_rt = (cc * p.T / G) / p.nKT;
-            const int sd = (cur_rt == cc_first_rt) ? 0 : 1;
-            v += __ldcg(p.partials + (cc * 2 + sd) * kPartialStride + m * kTileRows + r);
+          // load up to eight partials at a time, then add them in order
+          for (int64_t c0 = cf; c0 <= cl; c0 += 8) {
+            float part[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const int64_t cc = c0 + u;
+              const int sd = (cc == cf && cf_side1) ? 1 : 0;
+              part[u] = (cc <= cl)
+                            ? __ldcg(p.partials + (cc * 2 + sd) * kPartialStride + m * kTileRows + r)
+                            : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              if (c0 + u <= cl) v += part[u];
           }
           const int64_t n = cur_rt * kTileRows + r;
           if (n < p.N) p.y[m * p.N + n] = v * F::kOutScale;
@@ -357,9 +372,10 @@ __device__ __forceinline__ void load_x_slice(XRegsT<LPL>& xr, const GemvParams& 
     }
 }
 
-template <int M, int LPL, int SUBS, class Scale>
+template <int M, int LPL, int SUBS>
 __device__ __forceinline__ void stage_x_slice(float* xs, float (&xsum)[SUBS][M],
-                                              const XRegsT<LPL>& xr, int lane, Scale scale) {
+                                              const XRegsT<LPL>& xr, int lane,
+                                              const float (&scale)[LPL]) {
   constexpr int MP = mpad(M);
 #pragma unroll
   for (int m = 0; m < M; ++m) {
@@ -369,7 +385,7 @@ __device__ __forceinline__ void stage_x_slice(float* xs, float (&xsum)[SUBS][M],
       const int kk = lane * LPL + i;  // position inside the slice
       const float v = h2f(xr.v[m][i]);
       s += v;
-      xs[((kk >> 1) * MP + m) * 2 + (kk & 1)] = v * scale(kk);
+      xs[((kk >> 1) * MP + m) * 2 + (kk & 1)] = v * scale[i];
     }
     // sums over each group of 32 / SUBS consecutive lanes, then gathered so
     // every lane holds all SUBS group sums
@@ -402,6 +418,23 @@ __device__ __forceinline__ void load_xpairs(const float* xs, int q, float2 (&out
       if (m < M) out[m] = make_float2(v.x, v.y);
       if (m + 1 < M) out[m + 1] = make_float2(v.z, v.w);
     }
+  }
+}
+
+// Load NP consecutive x pairs q0 .. q0+NP-1 (q0 even): 128-bit loads of two
+// pairs at a time when M == 1.
+template <int M, int NP>
+__device__ __forceinline__ void load_xpair_run(const float* xs, int q0, float2 (&out)[NP][M]) {
+  if constexpr (M == 1 && NP % 2 == 0) {
+#pragma unroll
+    for (int u = 0; u < NP; u += 2) {
+      const float4 v = lds128f(xs + (q0 + u) * 2);
+      out[u][0] = make_float2(v.x, v.y);
+      out[u + 1][0] = make_float2(v.z, v.w);
+    }
+  } else {
+#pragma unroll
+    for (int u = 0; u < NP; ++u) load_xpairs<M>(xs, q0 + u, out[u]);
   }
 }
 
