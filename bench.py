@@ -72,6 +72,10 @@ LLAMA7B = [("q", 4096, 4096), ("k", 4096, 4096), ("v", 4096, 4096), ("o", 4096, 
            ("gate", 11008, 4096), ("up", 11008, 4096), ("down", 4096, 11008)]
 
 
+LLAMA70B_AQLM = [("gate", 28672, 8192), ("up", 28672, 8192), ("down", 8192, 28672),
+                 ("q", 8192, 8192), ("o", 8192, 8192)]
+
+
 def cbk4_stack_specs(layers=32):
     specs = []
     for layer in range(layers):
@@ -92,6 +96,9 @@ WORKLOADS = {
     "pq2_down": (lambda: [("pq2_0", "down", 8192, 28672)], "pq2_0", "PQ2_0 down 8192x28672"),
     "cbk4_down": (lambda: [("cbk4", "down", 8192, 28672)], "cbk4", "CBK4 down 8192x28672"),
     "cbk8_head": (lambda: [("cbk8", "lm_head", 32000, 4096)], "cbk8", "CBK8 LM head 32000x4096"),
+    "aqlm_70b_layer": (lambda: [("aqlm_2x8", n, N, K) for n, N, K in LLAMA70B_AQLM], "aqlm_2x8",
+                       "70B-shaped AQLM 2x8 layer: gate, up 28672x8192, down 8192x28672, q, o 8192x8192"),
+    "aqlm_down": (lambda: [("aqlm_2x8", "down", 8192, 28672)], "aqlm_2x8", "AQLM 2x8 down 8192x28672"),
 }
 
 

@@ -33,12 +33,16 @@ struct FormatOps {
   // w_out[n*K + k] = exact decoded weight, read back from the prepared tiles
   cudaError_t (*dequant)(const uint8_t* tiles, const void* aux, int64_t N, int64_t K, int nKT,
                          float* w_out, cudaStream_t s);
+  int tile_rows = 128;              // output rows per prepared tile
+  int64_t partial_stride = 128 * 16;  // floats per stream-K partial slot
+  int64_t aux_per_row = 0;          // aux bytes per output row, after aux_bytes
 };
 
 const FormatOps* ops_q4_0();
 const FormatOps* ops_pq2();
 const FormatOps* ops_cbk4();
 const FormatOps* ops_cbk8();
+const FormatOps* ops_aqlm();
 
 // Record the calling thread's last error (what qgemv_last_error returns);
 // returns `code`.  QGEMV_OK clears it.

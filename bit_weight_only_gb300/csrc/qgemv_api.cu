@@ -48,6 +48,7 @@ const qgemv::FormatOps* ops_for(int format) {
     case QGEMV_PQ2_0: return qgemv::ops_pq2();
     case QGEMV_CBK4: return qgemv::ops_cbk4();
     case QGEMV_CBK8: return qgemv::ops_cbk8();
+    case QGEMV_AQLM_2X8: return qgemv::ops_aqlm();
   }
   return nullptr;
 }
@@ -200,7 +201,7 @@ qgemv_handle qgemv_create(int format, int64_t N, int64_t K, const void* packed, 
   h->N = N;
   h->K = K;
   h->ops = ops;
-  h->nRT = (N + qgemv::kTileRows - 1) / qgemv::kTileRows;
+  h->nRT = (N + ops->tile_rows - 1) / ops->tile_rows;
   h->nKT = static_cast<int>((K + ops->kt - 1) / ops->kt);
   h->T = h->nRT * h->nKT;
   h->grid = static_cast<int>(h->T < sms ? h->T : sms);
@@ -228,9 +229,10 @@ qgemv_handle qgemv_create(int format, int64_t N, int64_t K, const void* packed, 
   if (e != cudaSuccess) return cleanup(QGEMV_ERR_CUDA, "copying the canonical inputs", e);
 
   e = cudaMalloc(&h->tiles, static_cast<size_t>(h->T) * ops->tile_bytes);
-  if (e == cudaSuccess && ops->aux_bytes > 0) e = cudaMalloc(&h->aux, ops->aux_bytes);
+  const int64_t aux_bytes = ops->aux_bytes + ops->aux_per_row * N;
+  if (e == cudaSuccess && aux_bytes > 0) e = cudaMalloc(&h->aux, static_cast<size_t>(aux_bytes));
   if (e == cudaSuccess)
-    e = cudaMalloc(&h->partials, sizeof(float) * 2 * qgemv::kPartialStride * static_cast<size_t>(h->grid));
+    e = cudaMalloc(&h->partials, sizeof(float) * 2 * ops->partial_stride * static_cast<size_t>(h->grid));
   if (e == cudaSuccess) e = cudaMalloc(&h->counters, sizeof(int) * h->nRT);
   if (e == cudaSuccess) e = cudaMalloc(&h->err, sizeof(int));
   if (e == cudaSuccess) e = cudaMemset(h->counters, 0, sizeof(int) * h->nRT);

@@ -2,7 +2,8 @@
 
 Bars:
   * decoded weights (qgemv_dequant): bit-exact against the oracle's exact
-    values (every decoded weight is representable in fp32);
+    values rounded once to fp32 (a no-op except for AQLM, whose scaled sums
+    are not all representable);
   * GEMV: |y - y_ref| <= 1e-3 * sum_k |x_k w_nk| + 1e-6 for every output;
   * one-hot x: the matching column of W, bit-exact;
   * run to run and eager vs CUDA graph: bitwise identical;
@@ -20,9 +21,12 @@ from cases import MIN_K, make_case, make_x
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
-FORMATS = ["q4_0", "pq2_0", "cbk4", "cbk8"]
-SMALL = {"q4_0": (300, 800), "pq2_0": (300, 1152), "cbk4": (300, 802), "cbk8": (300, 777)}
-MULTI = {"q4_0": (2500, 8192), "pq2_0": (2500, 16384), "cbk4": (2500, 8192), "cbk8": (2500, 4096)}
+FORMATS = ["q4_0", "pq2_0", "cbk4", "cbk8", "aqlm_2x8"]
+SMALL = {"q4_0": (300, 800), "pq2_0": (300, 1152), "cbk4": (300, 802), "cbk8": (300, 777),
+         "aqlm_2x8": (300, 808)}
+# AQLM row blocks are 2048 rows x 128 inputs: 3 x 128 units keep several per CTA.
+MULTI = {"q4_0": (2500, 8192), "pq2_0": (2500, 16384), "cbk4": (2500, 8192), "cbk8": (2500, 4096),
+         "aqlm_2x8": (4500, 16384)}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -63,9 +67,14 @@ def test_dequant_bit_exact(fmt, shape):
             "edge": (129, MIN_K[fmt] * 9)}[shape]
     packed, scales, cb = make_case(fmt, N, K, tag="dq")
     h = qgemv.QGemv(fmt, N, K, packed, scales, cb)
-    w = h.dequant().cpu().numpy().astype(np.float64)
+    w = h.dequant().cpu().numpy()
     ref = oracle.dequant(fmt, N, K, packed, scales, cb)
-    assert np.array_equal(w, ref)
+    if fmt != "aqlm_2x8":
+        # one scale times a small integer or a centroid: exact in fp32
+        assert np.array_equal(ref.astype(np.float32).astype(np.float64), ref)
+    # AQLM's s * (c0 + c1) needs up to 36 significant bits: the decoded fp32
+    # weight is the exact value rounded once, to nearest even
+    assert np.array_equal(w, ref.astype(np.float32))
 
 
 # -------------------------------------------------------------- GEMV ----
@@ -118,9 +127,11 @@ def test_one_hot_rows_extract_columns_bit_exact(fmt):
     for i, k in enumerate(cols):
         x[i, k] = 1.0
     h = qgemv.QGemv(fmt, N, K, packed, scales, cb)
-    y = gpu_gemv(h, x).astype(np.float64)
+    y = gpu_gemv(h, x)
+    # column k of W, rounded once to fp32 (exact except for AQLM, where
+    # c0 + c1 is exact in fp32 and the one product by s_n rounds)
     for i, k in enumerate(cols):
-        assert np.array_equal(y[i], W[:, k]), f"column {k}"
+        assert np.array_equal(y[i], W[:, k].astype(np.float32)), f"column {k}"
 
 
 @pytest.mark.parametrize("fmt", FORMATS)
@@ -230,6 +241,9 @@ def sample_rows(N, n=48, seed=0):
     ("cbk8", 32000, 4096, (1, 4)),       # 7B LM head
     ("pq2_0", 34816, 5120, (1, 8)),      # fused gate+up, hidden 5120
     ("pq2_0", 5120, 17408, (1, 8)),      # down, MLP 17408
+    ("aqlm_2x8", 28672, 8192, (1, 2)),   # 70B gate / up
+    ("aqlm_2x8", 8192, 28672, (1, 3)),   # 70B down
+    ("aqlm_2x8", 8192, 8192, (1, 16)),   # 70B q / o
 ])
 def test_full_size_sampled_rows(fmt, N, K, Ms):
     if fmt == "q4_0":
