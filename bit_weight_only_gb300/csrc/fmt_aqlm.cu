@@ -67,6 +67,11 @@ constexpr int kMaxMB = 2;                   // activation rows per pass
 constexpr int64_t kPartialStride = int64_t(kRows) * kMaxMB;
 constexpr int kCodebookBytes = 2 * 256 * 8 * 2;
 constexpr int kErrSmemLayout = 4;
+constexpr int kErrTimeoutFixup = 8;
+constexpr uint32_t kEmpty = 0xffffffffu;       // an unwritten partial slot
+constexpr unsigned long long kFixupWaitNs = 2000000000ull;  // 2 s
+constexpr int kRing = 2 * kRPL;            // rows of codes per lane in the load ring
+constexpr int kPreWait = 3;                // ring rows requested before the grid dependency wait
 
 __host__ __device__ constexpr int smem_bytes_mb(int mb) { return 65536 + mb * 65536; }
 
@@ -83,6 +88,20 @@ __device__ __forceinline__ float lds_at(uint32_t addr) {
   return v;
 }
 
+__device__ __forceinline__ void st_relaxed(float* p, float v) {
+  asm volatile("st.relaxed.gpu.global.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_relaxed_u32(float* p, uint32_t v) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_relaxed_u32(const float* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ void sts_f32(uint32_t addr, float v) {
   asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
@@ -95,8 +114,12 @@ __device__ __forceinline__ uint4 ldg_stream(const uint8_t* p, uint64_t pol) {
   return v;
 }
 
+// Issued in program order with the code stream (volatile), so the small
+// loads the table build needs are not queued behind the codes.
 __device__ __forceinline__ uint32_t ldg_u32(const void* p) {
-  return __ldg(reinterpret_cast<const unsigned int*>(p));
+  uint32_t v;
+  asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
 }
 
 // D (16 x 8, f32) = A (16 x 8, f16, row) * B (8 x 8, f16, col).
@@ -115,25 +138,20 @@ __host__ __device__ constexpr uint32_t step_sel(int i) {
   return static_cast<uint32_t>((4 + i % 3) | ((i & 3) << 4) | (7 << 8) | (15 << 12));
 }
 
-// One unit's lookups: RPL rows x 32 code bytes, tables in buffer BUF.
+// One row's 32 code bytes of a chunk, tables in buffer BUF.
 template <int MB, int BUF>
-__device__ __forceinline__ void lookup_unit(const uint4 (&cr)[kRPL][2], const uint32_t (&L)[11],
-                                            float2 (&acc)[kRPL]) {
+__device__ __forceinline__ void lookup_row(const uint4 (&cr)[2], const uint32_t (&L)[11], float2& acc) {
   constexpr uint32_t kOff = BUF * 128;
+  const uint32_t w[8] = {cr[0].x, cr[0].y, cr[0].z, cr[0].w, cr[1].x, cr[1].y, cr[1].z, cr[1].w};
 #pragma unroll
-  for (int r = 0; r < kRPL; ++r) {
-    const uint32_t w[8] = {cr[r][0].x, cr[r][0].y, cr[r][0].z, cr[r][0].w,
-                           cr[r][1].x, cr[r][1].y, cr[r][1].z, cr[r][1].w};
-#pragma unroll
-    for (int i = 0; i < kPos; i += 2) {
-      const uint32_t a0 = prmt(w[i >> 2], L[i / 3], step_sel(i));
-      const uint32_t a1 = prmt(w[(i + 1) >> 2], L[(i + 1) / 3], step_sel(i + 1));
-      if constexpr (MB == 1) {
-        acc[r] = __fadd2_rn(acc[r], make_float2(lds_at<kOff>(a0), lds_at<kOff>(a1)));
-      } else {
-        acc[r] = __fadd2_rn(acc[r], make_float2(lds_at<kOff>(a0), lds_at<kOff + kSlab>(a0)));
-        acc[r] = __fadd2_rn(acc[r], make_float2(lds_at<kOff>(a1), lds_at<kOff + kSlab>(a1)));
-      }
+  for (int i = 0; i < kPos; i += 2) {
+    const uint32_t a0 = prmt(w[i >> 2], L[i / 3], step_sel(i));
+    const uint32_t a1 = prmt(w[(i + 1) >> 2], L[(i + 1) / 3], step_sel(i + 1));
+    if constexpr (MB == 1) {
+      acc = __fadd2_rn(acc, make_float2(lds_at<kOff>(a0), lds_at<kOff>(a1)));
+    } else {
+      acc = __fadd2_rn(acc, make_float2(lds_at<kOff>(a0), lds_at<kOff + kSlab>(a0)));
+      acc = __fadd2_rn(acc, make_float2(lds_at<kOff>(a1), lds_at<kOff + kSlab>(a1)));
     }
   }
 }
@@ -141,7 +159,8 @@ __device__ __forceinline__ void lookup_unit(const uint4 (&cr)[kRPL][2], const ui
 template <int MB>
 __global__ void __launch_bounds__(kThreads, 1) aqlm_gemv_kernel(const GemvParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ int s_flag;
+  __shared__ float s_sub[kThreads];
+  __shared__ float s_scale[kThreads];
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -197,14 +216,17 @@ __global__ void __launch_bounds__(kThreads, 1) aqlm_gemv_kernel(const GemvParams
   const uint32_t stX = R0 + eA * 256 + tauX * 4;
   const uint32_t stY = R0 + eA * 256 + tauY * 4;
 
+  // Codes stream through a ring of kRing rows per lane (two units): the
+  // load of row-step s + kRing - 1 is issued when row-step s is consumed, so
+  // about 112 KB per SM stay in flight.
   const uint64_t pol = l2_policy_evict_first();
-  auto load_codes = [&](uint4 (&cr)[kRPL][2], int64_t u) {
-    const uint8_t* t = p.tiles + u * kTileBytes + warp * 512 + lane * 16;
-#pragma unroll
-    for (int r = 0; r < kRPL; ++r) {
-      cr[r][0] = ldg_stream(t + (r * 2 + 0) * 16 * 512, pol);
-      cr[r][1] = ldg_stream(t + (r * 2 + 1) * 16 * 512, pol);
-    }
+  const int64_t nsteps = nunits * kRPL;
+  auto load_row = [&](uint4 (&cr)[2], int64_t s) {
+    const int64_t u = u0 + (s >> 2);
+    const int r = static_cast<int>(s & 3);
+    const uint8_t* t = p.tiles + u * kTileBytes + (r * 2) * 16 * 512 + warp * 512 + lane * 16;
+    cr[0] = ldg_stream(t, pol);
+    cr[1] = ldg_stream(t + 16 * 512, pol);
   };
   const int64_t ngroups = p.K / 8;
   auto load_xf = [&](uint32_t (&xf)[MB][2], int kc) {
@@ -232,30 +254,48 @@ __global__ void __launch_bounds__(kThreads, 1) aqlm_gemv_kernel(const GemvParams
     }
   };
 
-  uint4 cA[kRPL][2], cB[kRPL][2];
+  uint4 ring[kRing][2];
   uint32_t xf[MB][2];
   float2 acc[kRPL];
 #pragma unroll
   for (int r = 0; r < kRPL; ++r) acc[r] = make_float2(0.f, 0.f);
 
-  // Weights are constant: fetch the first unit's codes before waiting on the
-  // previous kernel in the stream.  x is read only after the wait.
-  if (nunits > 0) load_codes(cA, u0);
+  // Row blocks this CTA shares with other CTAs (does not "own"): at most the
+  // first and the last of its run.  Their partials are stored in the loop
+  // and combined after it, with no fence or atomic inside the loop.
+  auto owned = [&](int64_t r) { return r * nKC >= u0 && (r + 1) * nKC <= u1; };
+  auto shared_seg = [&](int side) -> int64_t {
+    if (nunits <= 0) return -1;
+    const int64_t rbF = u0 / nKC, rbL = (u1 - 1) / nKC;
+    if (side == 0) return owned(rbF) ? -1 : rbF;
+    return (rbL != rbF && !owned(rbL)) ? rbL : -1;
+  };
+
+  // Weights are constant: start the code stream before waiting on the
+  // previous kernel in the stream.  x is read only after the wait, ahead of
+  // the rest of the stream, so the first table build does not queue behind
+  // the codes.
+#pragma unroll
+  for (int k = 0; k < kPreWait; ++k)
+    if (k < nsteps) load_row(ring[k], k);
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
   int64_t rb = u0 / nKC;
   int kc = static_cast<int>(u0 - rb * nKC);
   auto next_kc = [&](int k) { return (k + 1 == nKC) ? 0 : k + 1; };
+  if (nunits > 0) load_xf(xf, kc);
+#pragma unroll
+  for (int k = kPreWait; k < kRing - 1; ++k)
+    if (k < nsteps) load_row(ring[k], k);
   if (nunits > 0) {
-    load_xf(xf, kc);
     build(xf, 0);
     if (nunits > 1) load_xf(xf, next_kc(kc));
   }
   __syncthreads();
 
   auto epilogue = [&](int64_t rbe) {
-    const bool owner = (rbe * nKC >= u0) && ((rbe + 1) * nKC <= u1);
+    const bool owner = owned(rbe);
     const int side = (rbe == u0 / nKC) ? 0 : 1;
     float* my_part = p.partials + (c * 2 + side) * kPartialStride;
 #pragma unroll
@@ -274,63 +314,28 @@ __global__ void __launch_bounds__(kThreads, 1) aqlm_gemv_kernel(const GemvParams
         if (owner) {
           if (n < p.N) p.y[m * p.N + n] = __half2float(scales[n]) * v[m];
         } else {
-          my_part[m * kRows + nl] = v[m];
+          st_relaxed(my_part + m * kRows + nl, v[m]);
         }
       }
     }
-    if (owner) return;
-    __syncthreads();
-    // The barrier orders every thread's partial stores before thread 0's
-    // device-scope fence and arrival; the last arriver fences again before
-    // the CTA reads the other contributors' partials.
-    const int64_t cf = cta_of_tile(rbe * nKC, p.T, G);
-    const int64_t cl = cta_of_tile((rbe + 1) * nKC - 1, p.T, G);
-    if (tid == 0) {
-      __threadfence();
-      const int old = atomicAdd(&p.counters[rbe], 1);
-      const bool last = (old == static_cast<int>(cl - cf));
-      if (last) __threadfence();
-      s_flag = last;
-    }
-    __syncthreads();
-    if (!s_flag) return;
-    // Contributor cc wrote this row block in its side-0 slot, except the
-    // first one when its run began in an earlier row block (side 1).
-    const bool cf_side1 = (cf * p.T / G) < rbe * nKC;
-    for (int o = tid; o < kRows * MB; o += kThreads) {
-      const int nl = o % kRows;
-      const int m = o / kRows;
-      float s = 0.f;
-      for (int64_t c0 = cf; c0 <= cl; c0 += 8) {
-        float part[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const int64_t cc = c0 + k;
-          const int sd = (cc == cf && cf_side1) ? 1 : 0;
-          part[k] = (cc <= cl) ? __ldcg(p.partials + (cc * 2 + sd) * kPartialStride + m * kRows + nl)
-                               : 0.f;
-        }
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          if (c0 + k <= cl) s += part[k];
-      }
-      const int64_t n = rbe * kRows + nl;
-      if (n < p.N) p.y[m * p.N + n] = __half2float(scales[n]) * s;
-    }
-    if (tid == 0) p.counters[rbe] = 0;
   };
 
-  // One unit: prefetch the next unit's codes, build the next unit's tables in
-  // the other buffer, look this unit up, finish the row block if it ends.
-  auto step = [&](auto buf_tag, uint4 (&cur)[kRPL][2], uint4 (&nxt)[kRPL][2], int64_t i) {
+  // One unit: build the next unit's tables in the other buffer, look this
+  // unit's rows up (refilling the ring), finish the row block if it ends.
+  auto unit = [&](auto buf_tag, int64_t i) {
     constexpr int BUF = decltype(buf_tag)::value;
     const int k1 = next_kc(kc);
     if (i + 1 < nunits) {
-      load_codes(nxt, u0 + i + 1);
       build(xf, (1 - BUF) * 128);
       if (i + 2 < nunits) load_xf(xf, next_kc(k1));
     }
-    lookup_unit<MB, BUF>(cur, L, acc);
+#pragma unroll
+    for (int r = 0; r < kRPL; ++r) {
+      const int64_t s = i * kRPL + r;
+      constexpr int kBase = BUF * kRPL;
+      if (s + kRing - 1 < nsteps) load_row(ring[(kBase + r + kRing - 1) % kRing], s + kRing - 1);
+      lookup_row<MB, BUF>(ring[kBase + r], L, acc[r]);
+    }
     if (k1 == 0 || i + 1 == nunits) {
       epilogue(rb);
 #pragma unroll
@@ -342,8 +347,98 @@ __global__ void __launch_bounds__(kThreads, 1) aqlm_gemv_kernel(const GemvParams
   };
 
   for (int64_t i = 0; i < nunits; i += 2) {
-    step(std::integral_constant<int, 0>{}, cA, cB, i);
-    if (i + 1 < nunits) step(std::integral_constant<int, 1>{}, cB, cA, i + 1);
+    unit(std::integral_constant<int, 0>{}, i);
+    if (i + 1 < nunits) unit(std::integral_constant<int, 1>{}, i + 1);
+  }
+
+  // ---- split row blocks: every contributor finishes a slice ----
+  // A partial slot holds the empty mark (bit pattern 0xffffffff, which no
+  // fp32 add produces) until its writer stores the partial sum.  The reader
+  // of a slot polls it (bounded), and puts the mark back once it has the
+  // value; the next launch writes its partials only after its grid
+  // dependency wait, i.e. after this launch has ended.  Slice k of S rows
+  // goes to the k-th contributor; each (row, m) item is summed by H threads
+  // over contiguous runs of contributors, then the H sub-sums in order, so
+  // the summation order depends only on the launch geometry.
+  const int64_t segA = shared_seg(0), segB = shared_seg(1);
+#pragma unroll 1
+  for (int sgi = 0; sgi < 2; ++sgi) {
+    const int64_t rbe = sgi == 0 ? segA : segB;
+    if (rbe < 0) continue;
+    const int64_t cf = cta_of_tile(rbe * nKC, p.T, G);
+    const int64_t cl = cta_of_tile((rbe + 1) * nKC - 1, p.T, G);
+    const int S = static_cast<int>(cl - cf + 1);
+    const int k = static_cast<int>(c - cf);
+    // Contributor cc wrote this row block in its side-0 slot, except the
+    // first one when its run began in an earlier row block (side 1).
+    const bool cf_side1 = (cf * p.T / G) < rbe * nKC;
+    const int r0 = (k * kRows) / S;
+    const int nr = ((k + 1) * kRows) / S - r0;
+    const int items = nr * MB;
+    const int H = items >= kThreads ? 1 : kThreads / items;
+    const int cpt = (S + H - 1) / H;
+    for (int t = tid; t < items * H; t += kThreads) {
+      const int item = t / H;
+      const int h = t % H;
+      const int nl = r0 + item % nr;
+      const int m = item / nr;
+      const int64_t n = rbe * kRows + nl;
+      const float sc = (h == 0 && n < p.N) ? __half2float(scales[n]) : 0.f;
+      float sum = 0.f;
+      for (int j0 = 0; j0 < cpt; j0 += 8) {
+        float* ptr[8];
+        uint32_t bits[8];
+        uint32_t pending = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int64_t cc = cf + int64_t(h) * cpt + j0 + j;
+          const int sd = (cc == cf && cf_side1) ? 1 : 0;
+          ptr[j] = p.partials + (cc * 2 + sd) * kPartialStride + m * kRows + nl;
+          bits[j] = 0u;
+          if (j0 + j < cpt && cc <= cl) pending |= 1u << j;
+        }
+        const unsigned long long t_start = global_timer_ns();
+        while (pending) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            if (pending & (1u << j)) bits[j] = ld_relaxed_u32(ptr[j]);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            if ((pending & (1u << j)) && bits[j] != kEmpty) pending &= ~(1u << j);
+          if (!pending) break;
+          if (global_timer_ns() - t_start > kFixupWaitNs) {
+            atomicOr(p.err, kErrTimeoutFixup);
+            break;
+          }
+          __nanosleep(32);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int64_t cc = cf + int64_t(h) * cpt + j0 + j;
+          if (j0 + j < cpt && cc <= cl) {
+            sum += __uint_as_float(bits[j]);
+            st_relaxed_u32(ptr[j], kEmpty);
+          }
+        }
+      }
+      if (H == 1) {
+        if (n < p.N) p.y[m * p.N + n] = sc * sum;
+      } else {
+        s_sub[t] = sum;
+        if (h == 0) s_scale[item] = sc;
+      }
+    }
+    if (H > 1) {
+      __syncthreads();
+      for (int item = tid; item < items; item += kThreads) {
+        float sum = 0.f;
+        for (int h = 0; h < H; ++h) sum += s_sub[item * H + h];
+        const int64_t n = rbe * kRows + r0 + item % nr;
+        const int m = item / nr;
+        if (n < p.N) p.y[m * p.N + n] = s_scale[item] * sum;
+      }
+      __syncthreads();
+    }
   }
 }
 

@@ -236,6 +236,9 @@ qgemv_handle qgemv_create(int format, int64_t N, int64_t K, const void* packed, 
   if (e == cudaSuccess) e = cudaMalloc(&h->counters, sizeof(int) * h->nRT);
   if (e == cudaSuccess) e = cudaMalloc(&h->err, sizeof(int));
   if (e == cudaSuccess) e = cudaMemset(h->counters, 0, sizeof(int) * h->nRT);
+  // partial slots start empty (all ones): the AQLM fix-up polls them
+  if (e == cudaSuccess)
+    e = cudaMemset(h->partials, 0xff, sizeof(float) * 2 * ops->partial_stride * static_cast<size_t>(h->grid));
   if (e == cudaSuccess) e = cudaMemset(h->err, 0, sizeof(int));
   if (e != cudaSuccess) return cleanup(QGEMV_ERR_CUDA, "allocating the handle's device buffers", e);
 
@@ -312,7 +315,10 @@ int qgemv_status(qgemv_handle h) {
   if (err) {
     // A run that gave up may have left stream-K counters half counted.
     cudaMemset(h->counters, 0, sizeof(int) * h->nRT);
+    cudaMemset(h->partials, 0xff, sizeof(float) * 2 * h->ops->partial_stride * static_cast<size_t>(h->grid));
     cudaMemset(h->err, 0, sizeof(int));
+    if (err & 4)
+      return set_error(QGEMV_ERR_CUDA, "a kernel found its shared-memory window unusable (code %d)", err);
     return set_error(QGEMV_ERR_TIMEOUT, "a kernel gave up a bounded wait (code %d)", err);
   }
   return ok();
