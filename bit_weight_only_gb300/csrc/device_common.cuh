@@ -17,6 +17,8 @@ constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 // Error word bits written by kernels (read by qgemv_status).
 constexpr int kErrTimeoutFull = 1;
 constexpr int kErrTimeoutEmpty = 2;
+constexpr int kErrTimeoutFixup = 8;                   // a split-K partial never arrived
+constexpr uint32_t kEmptySlot = 0xffffffffu;          // an unwritten partial slot
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -93,6 +95,20 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
 }
 
 __device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
+
+__device__ __forceinline__ void st_relaxed_f32(float* p, float v) {
+  asm volatile("st.relaxed.gpu.global.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_relaxed_u32(float* p, uint32_t v) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_relaxed_u32(const float* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
 
 __device__ __forceinline__ uint4 lds128(const void* p) {
   return *reinterpret_cast<const uint4*>(p);

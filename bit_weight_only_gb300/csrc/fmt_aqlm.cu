@@ -67,9 +67,6 @@ constexpr int kMaxMB = 2;                   // activation rows per pass
 constexpr int64_t kPartialStride = int64_t(kRows) * kMaxMB;
 constexpr int kCodebookBytes = 2 * 256 * 8 * 2;
 constexpr int kErrSmemLayout = 4;
-constexpr int kErrTimeoutFixup = 8;
-constexpr uint32_t kEmpty = 0xffffffffu;       // an unwritten partial slot
-constexpr unsigned long long kFixupWaitNs = 2000000000ull;  // 2 s
 constexpr int kRing = 2 * kRPL;            // rows of codes per lane in the load ring
 constexpr int kPreWait = 3;                // ring rows requested before the grid dependency wait
 
@@ -85,20 +82,6 @@ template <uint32_t OFF>
 __device__ __forceinline__ float lds_at(uint32_t addr) {
   float v;
   asm volatile("ld.shared.f32 %0, [%1+%2];" : "=f"(v) : "r"(addr), "n"(OFF));
-  return v;
-}
-
-__device__ __forceinline__ void st_relaxed(float* p, float v) {
-  asm volatile("st.relaxed.gpu.global.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
-}
-
-__device__ __forceinline__ void st_relaxed_u32(float* p, uint32_t v) {
-  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ uint32_t ld_relaxed_u32(const float* p) {
-  uint32_t v;
-  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
 
@@ -159,8 +142,8 @@ __device__ __forceinline__ void lookup_row(const uint4 (&cr)[2], const uint32_t 
 template <int MB>
 __global__ void __launch_bounds__(kThreads, 1) aqlm_gemv_kernel(const GemvParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ float s_sub[kThreads];
-  __shared__ float s_scale[kThreads];
+  __shared__ float s_sub[2 * kThreads];
+  __shared__ __align__(16) CtaPlan s_plan;
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -170,8 +153,8 @@ __global__ void __launch_bounds__(kThreads, 1) aqlm_gemv_kernel(const GemvParams
   const int hi = q >> 1;
   const int64_t G = gridDim.x;
   const int64_t c = blockIdx.x;
-  const int64_t u0 = c * p.T / G;
-  const int64_t u1 = (c + 1) * p.T / G;
+  const int64_t u0 = stream_split(c, p.T, G);
+  const int64_t u1 = stream_split(c + 1, p.T, G);
   const int64_t nunits = u1 - u0;
   const int nKC = p.nKT;
 
@@ -184,6 +167,8 @@ __global__ void __launch_bounds__(kThreads, 1) aqlm_gemv_kernel(const GemvParams
     if (tid == 0) atomicOr(p.err, kErrSmemLayout);
     return;
   }
+
+  fetch_plan(&s_plan, p.plan, c, tid);
 
   // Offset words: byte jj of L[k] is 4 * slot of step 3k + jj; byte 3 is R0 >> 16.
   uint32_t L[11];
@@ -264,12 +249,6 @@ __global__ void __launch_bounds__(kThreads, 1) aqlm_gemv_kernel(const GemvParams
   // first and the last of its run.  Their partials are stored in the loop
   // and combined after it, with no fence or atomic inside the loop.
   auto owned = [&](int64_t r) { return r * nKC >= u0 && (r + 1) * nKC <= u1; };
-  auto shared_seg = [&](int side) -> int64_t {
-    if (nunits <= 0) return -1;
-    const int64_t rbF = u0 / nKC, rbL = (u1 - 1) / nKC;
-    if (side == 0) return owned(rbF) ? -1 : rbF;
-    return (rbL != rbF && !owned(rbL)) ? rbL : -1;
-  };
 
   // Weights are constant: start the code stream before waiting on the
   // previous kernel in the stream.  x is read only after the wait, ahead of
@@ -281,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1) aqlm_gemv_kernel(const GemvParams
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
-  int64_t rb = u0 / nKC;
+  int64_t rb = div_fast(u0, nKC);
   int kc = static_cast<int>(u0 - rb * nKC);
   auto next_kc = [&](int k) { return (k + 1 == nKC) ? 0 : k + 1; };
   if (nunits > 0) load_xf(xf, kc);
@@ -296,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1) aqlm_gemv_kernel(const GemvParams
 
   auto epilogue = [&](int64_t rbe) {
     const bool owner = owned(rbe);
-    const int side = (rbe == u0 / nKC) ? 0 : 1;
+    const int side = (rbe * nKC <= u0) ? 0 : 1;
     float* my_part = p.partials + (c * 2 + side) * kPartialStride;
 #pragma unroll
     for (int r = 0; r < kRPL; ++r) {
@@ -314,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1) aqlm_gemv_kernel(const GemvParams
         if (owner) {
           if (n < p.N) p.y[m * p.N + n] = __half2float(scales[n]) * v[m];
         } else {
-          st_relaxed(my_part + m * kRows + nl, v[m]);
+          st_relaxed_f32(my_part + m * kRows + nl, v[m]);
         }
       }
     }
@@ -351,95 +330,10 @@ __global__ void __launch_bounds__(kThreads, 1) aqlm_gemv_kernel(const GemvParams
     if (i + 1 < nunits) unit(std::integral_constant<int, 1>{}, i + 1);
   }
 
-  // ---- split row blocks: every contributor finishes a slice ----
-  // A partial slot holds the empty mark (bit pattern 0xffffffff, which no
-  // fp32 add produces) until its writer stores the partial sum.  The reader
-  // of a slot polls it (bounded), and puts the mark back once it has the
-  // value; the next launch writes its partials only after its grid
-  // dependency wait, i.e. after this launch has ended.  Slice k of S rows
-  // goes to the k-th contributor; each (row, m) item is summed by H threads
-  // over contiguous runs of contributors, then the H sub-sums in order, so
-  // the summation order depends only on the launch geometry.
-  const int64_t segA = shared_seg(0), segB = shared_seg(1);
-#pragma unroll 1
-  for (int sgi = 0; sgi < 2; ++sgi) {
-    const int64_t rbe = sgi == 0 ? segA : segB;
-    if (rbe < 0) continue;
-    const int64_t cf = cta_of_tile(rbe * nKC, p.T, G);
-    const int64_t cl = cta_of_tile((rbe + 1) * nKC - 1, p.T, G);
-    const int S = static_cast<int>(cl - cf + 1);
-    const int k = static_cast<int>(c - cf);
-    // Contributor cc wrote this row block in its side-0 slot, except the
-    // first one when its run began in an earlier row block (side 1).
-    const bool cf_side1 = (cf * p.T / G) < rbe * nKC;
-    const int r0 = (k * kRows) / S;
-    const int nr = ((k + 1) * kRows) / S - r0;
-    const int items = nr * MB;
-    const int H = items >= kThreads ? 1 : kThreads / items;
-    const int cpt = (S + H - 1) / H;
-    for (int t = tid; t < items * H; t += kThreads) {
-      const int item = t / H;
-      const int h = t % H;
-      const int nl = r0 + item % nr;
-      const int m = item / nr;
-      const int64_t n = rbe * kRows + nl;
-      const float sc = (h == 0 && n < p.N) ? __half2float(scales[n]) : 0.f;
-      float sum = 0.f;
-      for (int j0 = 0; j0 < cpt; j0 += 8) {
-        float* ptr[8];
-        uint32_t bits[8];
-        uint32_t pending = 0;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int64_t cc = cf + int64_t(h) * cpt + j0 + j;
-          const int sd = (cc == cf && cf_side1) ? 1 : 0;
-          ptr[j] = p.partials + (cc * 2 + sd) * kPartialStride + m * kRows + nl;
-          bits[j] = 0u;
-          if (j0 + j < cpt && cc <= cl) pending |= 1u << j;
-        }
-        const unsigned long long t_start = global_timer_ns();
-        while (pending) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            if (pending & (1u << j)) bits[j] = ld_relaxed_u32(ptr[j]);
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            if ((pending & (1u << j)) && bits[j] != kEmpty) pending &= ~(1u << j);
-          if (!pending) break;
-          if (global_timer_ns() - t_start > kFixupWaitNs) {
-            atomicOr(p.err, kErrTimeoutFixup);
-            break;
-          }
-          __nanosleep(32);
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int64_t cc = cf + int64_t(h) * cpt + j0 + j;
-          if (j0 + j < cpt && cc <= cl) {
-            sum += __uint_as_float(bits[j]);
-            st_relaxed_u32(ptr[j], kEmpty);
-          }
-        }
-      }
-      if (H == 1) {
-        if (n < p.N) p.y[m * p.N + n] = sc * sum;
-      } else {
-        s_sub[t] = sum;
-        if (h == 0) s_scale[item] = sc;
-      }
-    }
-    if (H > 1) {
-      __syncthreads();
-      for (int item = tid; item < items; item += kThreads) {
-        float sum = 0.f;
-        for (int h = 0; h < H; ++h) sum += s_sub[item * H + h];
-        const int64_t n = rbe * kRows + r0 + item % nr;
-        const int m = item / nr;
-        if (n < p.N) p.y[m * p.N + n] = s_scale[item] * sum;
-      }
-      __syncthreads();
-    }
-  }
+  // ---- split row blocks: every contributor finishes a slice of rows ----
+  wait_plan();
+  if (s_plan.seg_rt[0] >= 0) finish_rows<kRows, MB, kThreads>(p, kPartialStride, s_plan, 0, scales, 1.f, s_sub, tid);
+  if (s_plan.seg_rt[1] >= 0) finish_rows<kRows, MB, kThreads>(p, kPartialStride, s_plan, 1, scales, 1.f, s_sub, tid);
 }
 
 // Canonical codes [N][K/8][2] -> prepared units (rotated per lane).

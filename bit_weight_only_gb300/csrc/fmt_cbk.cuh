@@ -74,12 +74,19 @@ struct FmtCBK4 {
   static constexpr int kSumGroups = 1;  // unused: codebook values carry no offset
   using XRegs = XRegsT<2>;
 
-  __device__ static void init_shared(uint8_t* lut, const GemvParams& p, int tid, int nthreads) {
+  // Warp w writes entries w, w + NT/32, ...; its 32 lanes write one entry's
+  // 32 lane copies (32 consecutive words: no bank conflict).  The 16
+  // centroids are read once per lane and passed around with shuffles.
+  template <int NT>
+  __device__ static void init_shared(uint8_t* lut, const GemvParams& p, int warp, int lane) {
+    constexpr int W = NT / 32;
     const uint16_t* cb = static_cast<const uint16_t*>(p.aux);
-    for (int i = tid; i < 256 * 32; i += nthreads) {
-      const int e = i >> 5, l = i & 31;
-      const uint32_t v = static_cast<uint32_t>(cb[e & 15]) | (static_cast<uint32_t>(cb[e >> 4]) << 16);
-      *reinterpret_cast<uint32_t*>(lut + e * 256 + l * 4) = v;
+    const uint32_t mine = cb[lane & 15];
+#pragma unroll 4
+    for (int e = warp; e < 256; e += W) {
+      const uint32_t lo = __shfl_sync(0xffffffffu, mine, e & 15);
+      const uint32_t hi = __shfl_sync(0xffffffffu, mine, e >> 4);
+      *reinterpret_cast<uint32_t*>(lut + e * 256 + lane * 4) = lo | (hi << 16);
     }
   }
 
@@ -187,11 +194,20 @@ struct FmtCBK8 {
   static constexpr int kSumGroups = 1;  // unused
   using XRegs = XRegsT<1>;
 
-  __device__ static void init_shared(uint8_t* lut, const GemvParams& p, int tid, int nthreads) {
+  // As for CBK4: warp w writes entries w + (NT/32)*j, one conflict-free row
+  // of 32 lane copies each; lane l first reads centroids 32*i + l.
+  template <int NT>
+  __device__ static void init_shared(uint8_t* lut, const GemvParams& p, int warp, int lane) {
+    constexpr int W = NT / 32;
     const uint16_t* cb = static_cast<const uint16_t*>(p.aux);
-    for (int i = tid; i < 256 * 32; i += nthreads) {
-      const int e = i >> 5, l = i & 31;
-      *reinterpret_cast<float*>(lut + e * 256 + l * 4) = h2f(cb[e]);
+    float reg[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) reg[i] = h2f(cb[32 * i + lane]);
+#pragma unroll
+    for (int j = 0; j < 256 / W; ++j) {
+      const int e = warp + W * j;  // (W * j) >> 5 == e >> 5 since W divides 32
+      const float v = __shfl_sync(0xffffffffu, reg[(W * j) >> 5], e & 31);
+      *reinterpret_cast<float*>(lut + e * 256 + lane * 4) = v;
     }
   }
 

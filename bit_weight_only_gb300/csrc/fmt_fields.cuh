@@ -72,6 +72,7 @@ struct FmtQ4_0 {
   // taken from the word shifted right by 12)
   __host__ __device__ static constexpr int field_pos(int jj) { return jj <= 4 ? 4 * jj : 4 * jj - 12; }
 
+  template <int NT>
   __device__ static void init_shared(uint8_t*, const GemvParams&, int, int) {}
 
   template <int M>
@@ -189,6 +190,7 @@ struct FmtPQ2 {
 
   __host__ __device__ static constexpr int field_pos(int jj) { return jj <= 10 ? 2 * jj : 2 * jj - 12; }
 
+  template <int NT>
   __device__ static void init_shared(uint8_t*, const GemvParams&, int, int) {}
 
   template <int M>

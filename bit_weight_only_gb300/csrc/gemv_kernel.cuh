@@ -12,10 +12,10 @@
 //     (16 bytes per row), so one 128-bit shared load per row per lane and no
 //     bank conflicts.
 //   * The stream of T tiles is split evenly over the grid ("stream-K"): CTA
-//     c owns tiles [c*T/G, (c+1)*T/G).  A row tile cut by a CTA boundary is
-//     finished by whichever of its contributors arrives last (an integer
-//     counter), which sums all partial results in contributor order: fixed
-//     order, no float atomics, bitwise reproducible.
+//     c owns tiles [c*T/G, (c+1)*T/G).  A row tile cut by CTA boundaries is
+//     finished, after the main loop, by all of its contributors together:
+//     each sums a slice of the rows from polled partial slots, in a fixed
+//     order (no atomics, no fences; bitwise reproducible).
 //   * One elected thread keeps an F::stages(M) ring of shared-memory stages
 //     filled with TMA bulk copies (cp.async.bulk, evict-first L2 policy),
 //     stages - 1 tiles ahead of the math, signalled through mbarriers.  There
@@ -50,12 +50,25 @@ constexpr int kTileRows = 32 * kRowsPerLane;       // 128
 constexpr int kMaxM = 16;
 constexpr int kPartialStride = kTileRows * kMaxM;  // floats per partial slot
 
+// Stream-K plan of one CTA, computed on the host when the handle is made:
+// the row tiles (at most the first and the last of its run) that it shares
+// with other CTAs, and its place among their contributors.
+struct CtaPlan {
+  int64_t seg_rt[2];     // shared row tiles, -1 if none
+  int64_t seg_cf[2];     // first contributor of each
+  int32_t seg_S[2];      // number of contributors
+  int32_t seg_r0[2];     // this CTA's slice of the rows: [r0, r0 + nr)
+  int32_t seg_nr[2];
+  int32_t seg_side1[2];  // 1: the first contributor's run began earlier (its side-1 slot)
+};
+static_assert(sizeof(CtaPlan) == 64, "CtaPlan is copied in 16-byte pieces");
+
 struct GemvParams {
   const uint8_t* tiles;  // prepared tiles (device)
   const __half* x;       // [M][K] fp16
   float* y;              // [M][N] fp32
-  float* partials;       // [gridDim.x][2][kPartialStride]
-  int* counters;         // [number of row tiles], zero between calls
+  float* partials;       // [gridDim.x][2][partial stride], all ones between calls
+  const CtaPlan* plan;   // [gridDim.x]
   int* err;              // error word (kErr* bits)
   const void* aux;       // format data (codebooks ...)
   int64_t N, K;
@@ -149,6 +162,147 @@ __device__ __forceinline__ int64_t cta_of_tile(int64_t t, int64_t T, int64_t G) 
   return ((t + 1) * G - 1) / T;
 }
 
+// Finish one shared row tile (ROWS output rows) as described by a CtaPlan
+// segment: sum rows [r0, r0 + nr) of each activation row over the S
+// contributors starting at CTA cf.  A partial slot holds the empty mark (all
+// ones, a pattern no fp32 add produces) until its writer stores the partial;
+// the reader polls it with a bounded wait and marks it empty again.  The
+// next launch writes partials only after its grid-dependency wait, i.e.
+// after this launch has ended.  Up to 16 contributors one thread sums an
+// item (row, m) alone; beyond that H threads sum contiguous runs of
+// contributors and the H sub-sums are added in order.  The order depends
+// only on the launch geometry, so results are bitwise reproducible.
+// y = sum * out_scale, times the fp16 row scale when row_scales is not null.
+template <int ROWS, int M, int NT>
+__device__ __forceinline__ void finish_rows(const GemvParams& p, int64_t stride, const CtaPlan& pl, int sg,
+                                            const __half* row_scales, float out_scale, float* s_sub,
+                                            int tid) {
+  const int64_t rt = pl.seg_rt[sg];
+  const int64_t cf = pl.seg_cf[sg];
+  const int S = pl.seg_S[sg];
+  const int r0 = pl.seg_r0[sg];
+  const int nr = pl.seg_nr[sg];
+  if (nr <= 0) return;  // more contributors than rows: this one has no slice
+  constexpr int B = M > 8 ? 8 : 16;  // slots polled at once (registers)
+  const int items = nr * M;
+  const int H = (S <= 16 || items >= NT) ? 1 : NT / items;
+  const int cpt = H == 1 ? S : (S + H - 1) / H;
+  // slot of contributor cf + i: side 1 only for the first one, if its run began earlier
+  const float* first_slot = p.partials + (cf * 2 + (pl.seg_side1[sg] ? 1 : 0)) * stride;
+  const float* base = p.partials + cf * 2 * stride;
+  for (int t = tid; t < items * H; t += NT) {
+    const int item = H == 1 ? t : t / H;
+    const int h = H == 1 ? 0 : t - item * H;
+    const int m = M == 1 ? 0 : item / nr;
+    const int r = r0 + (M == 1 ? item : item - m * nr);
+    const int64_t n = rt * ROWS + r;
+    float sc = out_scale;
+    if (row_scales != nullptr && h == 0 && n < p.N) sc *= __half2float(row_scales[n]);
+    const int64_t off = m * ROWS + r;
+    float sum = 0.f;
+    for (int j0 = h * cpt; j0 < (h + 1) * cpt && j0 < S; j0 += B) {
+      const int cnt = min(B, min((h + 1) * cpt, S) - j0);
+      uint32_t bits[B];
+      uint32_t pending = (1u << cnt) - 1u;
+      auto slot = [&](int j) {
+        const int i = j0 + j;
+        return const_cast<float*>(i == 0 ? first_slot + off : base + int64_t(i) * 2 * stride + off);
+      };
+      unsigned long long t_start = 0;
+      while (true) {
+#pragma unroll
+        for (int j = 0; j < B; ++j)
+          if (pending & (1u << j)) bits[j] = ld_relaxed_u32(slot(j));
+#pragma unroll
+        for (int j = 0; j < B; ++j)
+          if ((pending & (1u << j)) && bits[j] != kEmptySlot) pending &= ~(1u << j);
+        if (!pending) break;
+        // spin: each round is one L2 round trip; no sleep, whose granularity
+        // is far coarser than the waits hidden here
+        const unsigned long long now = global_timer_ns();
+        if (t_start == 0) t_start = now;
+        else if (now - t_start > kWaitLimitNs) {
+          atomicOr(p.err, kErrTimeoutFixup);
+          break;
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < B; ++j) {
+        if (j < cnt) {
+          sum += __uint_as_float(bits[j]);
+          st_relaxed_u32(slot(j), kEmptySlot);
+        }
+      }
+    }
+    if (H == 1) {
+      if (n < p.N) p.y[m * p.N + n] = sum * sc;
+    } else {
+      s_sub[t] = sum;
+      if (h == 0) s_sub[NT + item] = sc;
+    }
+  }
+  if (H > 1) {
+    __syncthreads();
+    for (int item = tid; item < items; item += NT) {
+      float sum = 0.f;
+      for (int h = 0; h < H; ++h) sum += s_sub[item * H + h];
+      const int m = item / nr;
+      const int64_t n = rt * ROWS + r0 + item - m * nr;
+      if (n < p.N) p.y[m * p.N + n] = sum * s_sub[NT + item];
+    }
+    __syncthreads();
+  }
+}
+
+// Out-of-line copy for large M, whose main loop needs every register.
+template <int ROWS, int M, int NT>
+__device__ __noinline__ void finish_rows_call(const GemvParams& p, int64_t stride, const CtaPlan& pl, int sg,
+                                              const __half* row_scales, float out_scale, float* s_sub,
+                                              int tid) {
+  finish_rows<ROWS, M, NT>(p, stride, pl, sg, row_scales, out_scale, s_sub, tid);
+}
+
+template <int ROWS, int M, int NT>
+__device__ __forceinline__ void finish_segment(const GemvParams& p, int64_t stride, const CtaPlan& pl, int sg,
+                                               const __half* row_scales, float out_scale, float* s_sub,
+                                               int tid) {
+  if constexpr (M > 8)
+    finish_rows_call<ROWS, M, NT>(p, stride, pl, sg, row_scales, out_scale, s_sub, tid);
+  else
+    finish_rows<ROWS, M, NT>(p, stride, pl, sg, row_scales, out_scale, s_sub, tid);
+}
+
+// CTA c's share of the stream: [c * T / G, (c + 1) * T / G), with 32-bit
+// divisions when the products fit (the common case).
+__device__ __forceinline__ int64_t stream_split(int64_t c, int64_t T, int64_t G) {
+  const int64_t prod = c * T;
+  if (prod < (int64_t(1) << 31) && G < (int64_t(1) << 31))
+    return static_cast<int64_t>(static_cast<uint32_t>(prod) / static_cast<uint32_t>(G));
+  return prod / G;
+}
+
+__device__ __forceinline__ int64_t div_fast(int64_t a, int64_t b) {
+  if (a < (int64_t(1) << 31) && b < (int64_t(1) << 31))
+    return static_cast<int64_t>(static_cast<uint32_t>(a) / static_cast<uint32_t>(b));
+  return a / b;
+}
+
+// Start copying this CTA's plan into shared memory (four 16-byte pieces,
+// asynchronous); wait_plan() must run before it is read.
+__device__ __forceinline__ void fetch_plan(CtaPlan* s_plan, const CtaPlan* plan, int64_t c, int tid) {
+  if (tid < 4) {
+    const uint32_t dst = smem_u32(reinterpret_cast<uint8_t*>(s_plan) + 16 * tid);
+    const void* src = reinterpret_cast<const uint8_t*>(plan + c) + 16 * tid;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n\tcp.async.commit_group;" ::"r"(dst), "l"(src)
+                 : "memory");
+  }
+}
+
+__device__ __forceinline__ void wait_plan() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  __syncthreads();
+}
+
 template <class F, int M>
 __global__ void __launch_bounds__(gemv_threads<M>(), 1) gemv_kernel(const GemvParams p) {
   constexpr int NS = F::stages(M);
@@ -167,8 +321,8 @@ __global__ void __launch_bounds__(gemv_threads<M>(), 1) gemv_kernel(const GemvPa
   uint8_t* fsh = reinterpret_cast<uint8_t*>(red + kSlices * kTileRows * RS);
   uint64_t* full = reinterpret_cast<uint64_t*>(fsh + F::kSharedBytes);
   uint64_t* empty = full + NS;
-  __shared__ int s_flag;
   __shared__ volatile int s_abort;
+  __shared__ __align__(16) CtaPlan s_plan;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -177,36 +331,36 @@ __global__ void __launch_bounds__(gemv_threads<M>(), 1) gemv_kernel(const GemvPa
   const int tid = threadIdx.x;
   const int64_t G = gridDim.x;
   const int64_t c = blockIdx.x;
-  const int64_t t0 = c * p.T / G;
-  const int64_t t1 = (c + 1) * p.T / G;
+  const int64_t t0 = stream_split(c, p.T, G);
+  const int64_t t1 = stream_split(c + 1, p.T, G);
 
-  if (tid == 0) {
+  // The elected thread initializes the barriers and at once starts filling
+  // the ring NS - 1 tiles ahead of the math, so the first tiles are in
+  // flight while the CTA builds the format's tables.
+  const int64_t ntiles = t1 - t0;
+  const bool elected = (tid == 0);
+  uint64_t pol = 0;
+  int64_t n_issued = 0;  // meaningful on the elected thread
+  if (elected) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kSlices * WPS);
     }
     s_abort = 0;
     fence_mbarrier_init();
-  }
-  F::init_shared(fsh, p, tid, NT);
-  __syncthreads();
-
-  float* xs = xs_all + warp * XS_FLOATS;
-  RowAcc<M, RPW> acc;
-  acc.init(red, slice, half, lane);
-
-  // The elected thread fills the ring NS - 1 tiles ahead of the math.
-  const int64_t ntiles = t1 - t0;
-  const bool elected = (tid == 0);
-  uint64_t pol = 0;
-  int64_t n_issued = 0;  // meaningful on the elected thread
-  if (elected) {
     pol = l2_policy_evict_first();
     for (; n_issued < NS - 1 && n_issued < ntiles; ++n_issued) {
       mbar_arrive_expect_tx(&full[n_issued], TB);
       bulk_g2s(ring + n_issued * TB, p.tiles + (t0 + n_issued) * TB, TB, &full[n_issued], pol);
     }
   }
+  fetch_plan(&s_plan, p.plan, c, tid);
+  F::template init_shared<NT>(fsh, p, warp, lane);
+  __syncthreads();
+
+  float* xs = xs_all + warp * XS_FLOATS;
+  RowAcc<M, RPW> acc;
+  acc.init(red, slice, half, lane);
 
   // Programmatic dependent launch: the prologue above (barriers, tables, the
   // first weight copies) touches nothing a previous kernel in the stream
@@ -216,7 +370,7 @@ __global__ void __launch_bounds__(gemv_threads<M>(), 1) gemv_kernel(const GemvPa
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // Position of tile t0 in the stream, advanced incrementally below.
-  int64_t rt = t0 / p.nKT;
+  int64_t rt = div_fast(t0, p.nKT);
   int kt = static_cast<int>(t0 - rt * p.nKT);
   typename F::XRegs xr;
   if (ntiles > 0) F::template load_x<M>(xr, p, kt, slice, lane);
@@ -274,7 +428,7 @@ __global__ void __launch_bounds__(gemv_threads<M>(), 1) gemv_kernel(const GemvPa
     named_bar_sync(1, NT);
 
     const bool owner = (cur_rt * p.nKT >= t0) && ((cur_rt + 1) * p.nKT <= t1);
-    const int side = (cur_rt == t0 / p.nKT) ? 0 : 1;
+    const int side = (cur_rt * p.nKT <= t0) ? 0 : 1;
     float* my_part = p.partials + (c * 2 + side) * kPartialStride;
     for (int o = tid; o < kTileRows * M; o += NT) {
       const int r = o % kTileRows;
@@ -286,63 +440,29 @@ __global__ void __launch_bounds__(gemv_threads<M>(), 1) gemv_kernel(const GemvPa
         const int64_t n = cur_rt * kTileRows + r;
         if (n < p.N) p.y[m * p.N + n] = v * F::kOutScale;
       } else {
-        my_part[m * kTileRows + r] = v;
+        st_relaxed_f32(my_part + m * kTileRows + r, v);
       }
     }
     named_bar_sync(1, NT);
-
-    if (!owner) {
-      // The barrier above orders every thread's partial stores before
-      // thread 0's device-scope fence and arrival (release); the last
-      // arriver fences again before the CTA reads the others' partials.
-      const int64_t cf = cta_of_tile(cur_rt * p.nKT, p.T, G);
-      const int64_t cl = cta_of_tile((cur_rt + 1) * p.nKT - 1, p.T, G);
-      if (tid == 0) {
-        __threadfence();
-        const int old = atomicAdd(&p.counters[cur_rt], 1);
-        const bool last = (old == static_cast<int>(cl - cf));
-        if (last) __threadfence();
-        s_flag = last;
-      }
-      named_bar_sync(1, NT);
-      if (s_flag) {
-        // Contributor cc wrote this row tile in its side-0 slot, except the
-        // first one when its range began in an earlier row tile (side 1).
-        const bool cf_side1 = (cf * p.T / G) < cur_rt * p.nKT;
-        for (int o = tid; o < kTileRows * M; o += NT) {
-          const int r = o % kTileRows;
-          const int m = o / kTileRows;
-          float v = 0.f;
-          // load up to eight partials at a time, then add them in order
-          for (int64_t c0 = cf; c0 <= cl; c0 += 8) {
-            float part[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const int64_t cc = c0 + u;
-              const int sd = (cc == cf && cf_side1) ? 1 : 0;
-              part[u] = (cc <= cl)
-                            ? __ldcg(p.partials + (cc * 2 + sd) * kPartialStride + m * kTileRows + r)
-                            : 0.f;
-            }
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-              if (c0 + u <= cl) v += part[u];
-          }
-          const int64_t n = cur_rt * kTileRows + r;
-          if (n < p.N) p.y[m * p.N + n] = v * F::kOutScale;
-        }
-        if (tid == 0) p.counters[cur_rt] = 0;
-      }
-    }
     acc.reset();
   }
 
   // Never leave while a copy issued by this CTA may still be landing (only
   // possible after an aborted run; normally every issued tile was consumed).
-  if (elected) {
+  if (elected && s_abort != 0) {
     for (int64_t u = (n_issued > NS ? n_issued - NS : 0); u < n_issued; ++u)
       mbar_wait_bounded(&full[u % NS], static_cast<uint32_t>((u / NS) & 1));
   }
+
+  // Row tiles shared with other CTAs (at most the first and the last of the
+  // run): every contributor finishes a slice of their rows from the polled
+  // partial slots.  The cross-slice buffer (at least 2 * NT floats) is free
+  // now and serves as the finishing scratch.
+  static_assert(kSlices * kTileRows * RS >= 2 * NT, "finishing scratch");
+  float* s_sub = red;
+  wait_plan();
+  if (s_plan.seg_rt[0] >= 0) finish_segment<kTileRows, M, NT>(p, kPartialStride, s_plan, 0, nullptr, F::kOutScale, s_sub, tid);
+  if (s_plan.seg_rt[1] >= 0) finish_segment<kTileRows, M, NT>(p, kPartialStride, s_plan, 1, nullptr, F::kOutScale, s_sub, tid);
 }
 
 // ------------------------------------------------- activation staging ----

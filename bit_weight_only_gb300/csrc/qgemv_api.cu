@@ -9,6 +9,7 @@
 #include <cstring>
 #include <mutex>
 #include <new>
+#include <vector>
 
 #include <cuda_runtime.h>
 
@@ -100,6 +101,45 @@ cudaError_t to_device(const void* src, size_t bytes, void** dst) {
   return e;
 }
 
+// The stream-K split of T tiles over G CTAs: CTA c runs [c*T/G, (c+1)*T/G).
+// A row tile (nKT consecutive tiles) that no single CTA covers is "shared";
+// its contributors are the CTAs whose runs touch it, and each later sums one
+// slice of its rows.  Computed once per handle so the kernels do no 64-bit
+// divisions.
+int64_t split_point(int64_t c, int64_t T, int64_t G) { return c * T / G; }
+int64_t cta_of(int64_t t, int64_t T, int64_t G) { return ((t + 1) * G - 1) / T; }
+
+std::vector<qgemv::CtaPlan> plan_stream_k(int64_t T, int64_t G, int64_t nKT, int64_t rows) {
+  std::vector<qgemv::CtaPlan> plan(static_cast<size_t>(G));
+  for (int64_t c = 0; c < G; ++c) {
+    qgemv::CtaPlan& pl = plan[static_cast<size_t>(c)];
+    std::memset(&pl, 0, sizeof(pl));
+    pl.seg_rt[0] = pl.seg_rt[1] = -1;
+    const int64_t t0 = split_point(c, T, G), t1 = split_point(c + 1, T, G);
+    if (t1 <= t0) continue;
+    auto owned = [&](int64_t r) { return r * nKT >= t0 && (r + 1) * nKT <= t1; };
+    const int64_t first = t0 / nKT, last = (t1 - 1) / nKT;
+    int sg = 0;
+    for (int64_t r : {first, last}) {
+      if (owned(r) || (sg == 1 && r == first)) {
+        ++sg;
+        continue;
+      }
+      const int64_t cf = cta_of(r * nKT, T, G);
+      const int64_t cl = cta_of((r + 1) * nKT - 1, T, G);
+      pl.seg_rt[sg] = r;
+      pl.seg_cf[sg] = cf;
+      const int64_t S = cl - cf + 1, k = c - cf;
+      pl.seg_S[sg] = static_cast<int32_t>(S);
+      pl.seg_r0[sg] = static_cast<int32_t>(k * rows / S);
+      pl.seg_nr[sg] = static_cast<int32_t>((k + 1) * rows / S - k * rows / S);
+      pl.seg_side1[sg] = split_point(cf, T, G) < r * nKT ? 1 : 0;
+      ++sg;
+    }
+  }
+  return plan;
+}
+
 std::once_flag g_setup_once[8];
 cudaError_t g_setup_err[8];
 
@@ -124,7 +164,7 @@ struct qgemv_ctx {
   uint8_t* tiles;
   void* aux;
   float* partials;
-  int* counters;
+  qgemv::CtaPlan* plan;
   int* err;
 };
 
@@ -216,7 +256,7 @@ qgemv_handle qgemv_create(int format, int64_t N, int64_t K, const void* packed, 
     cudaFree(h->tiles);
     cudaFree(h->aux);
     cudaFree(h->partials);
-    cudaFree(h->counters);
+    cudaFree(h->plan);
     cudaFree(h->err);
     h->magic = 0;
     delete h;
@@ -233,9 +273,12 @@ qgemv_handle qgemv_create(int format, int64_t N, int64_t K, const void* packed, 
   if (e == cudaSuccess && aux_bytes > 0) e = cudaMalloc(&h->aux, static_cast<size_t>(aux_bytes));
   if (e == cudaSuccess)
     e = cudaMalloc(&h->partials, sizeof(float) * 2 * ops->partial_stride * static_cast<size_t>(h->grid));
-  if (e == cudaSuccess) e = cudaMalloc(&h->counters, sizeof(int) * h->nRT);
+  if (e == cudaSuccess) e = cudaMalloc(&h->plan, sizeof(qgemv::CtaPlan) * h->grid);
   if (e == cudaSuccess) e = cudaMalloc(&h->err, sizeof(int));
-  if (e == cudaSuccess) e = cudaMemset(h->counters, 0, sizeof(int) * h->nRT);
+  if (e == cudaSuccess) {
+    std::vector<qgemv::CtaPlan> plan = plan_stream_k(h->T, h->grid, h->nKT, ops->tile_rows);
+    e = cudaMemcpy(h->plan, plan.data(), sizeof(qgemv::CtaPlan) * plan.size(), cudaMemcpyHostToDevice);
+  }
   // partial slots start empty (all ones): the AQLM fix-up polls them
   if (e == cudaSuccess)
     e = cudaMemset(h->partials, 0xff, sizeof(float) * 2 * ops->partial_stride * static_cast<size_t>(h->grid));
@@ -276,7 +319,7 @@ int qgemv_run(qgemv_handle h, const void* x, int M, float* y, void* stream) {
   p.x = static_cast<const __half*>(x);
   p.y = y;
   p.partials = h->partials;
-  p.counters = h->counters;
+  p.plan = h->plan;
   p.err = h->err;
   p.aux = h->aux;
   p.N = h->N;
@@ -313,8 +356,7 @@ int qgemv_status(qgemv_handle h) {
   if (e == cudaSuccess) e = cudaMemcpy(&err, h->err, sizeof(int), cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_error(e, "reading the kernel status");
   if (err) {
-    // A run that gave up may have left stream-K counters half counted.
-    cudaMemset(h->counters, 0, sizeof(int) * h->nRT);
+    // A run that gave up may have left partial slots written but unread.
     cudaMemset(h->partials, 0xff, sizeof(float) * 2 * h->ops->partial_stride * static_cast<size_t>(h->grid));
     cudaMemset(h->err, 0, sizeof(int));
     if (err & 4)
@@ -330,7 +372,7 @@ void qgemv_destroy(qgemv_handle h) {
   cudaFree(h->tiles);
   cudaFree(h->aux);
   cudaFree(h->partials);
-  cudaFree(h->counters);
+  cudaFree(h->plan);
   cudaFree(h->err);
   h->magic = 0;
   delete h;
