@@ -76,19 +76,34 @@ LLAMA70B_AQLM = [("gate", 28672, 8192), ("up", 28672, 8192), ("down", 8192, 2867
                  ("q", 8192, 8192), ("o", 8192, 8192)]
 
 
-def cbk4_stack_specs(layers=32):
+def cbk4_stack_specs(layers=32, stacked=True):
+    """The 7B projection stack.  stacked: q|k|v and gate|up, which share
+    their input, run as one stacked handle each (4 GEMV calls per layer)."""
     specs = []
     for layer in range(layers):
-        for name, N, K in LLAMA7B:
-            specs.append(("cbk4", f"L{layer}.{name}", N, K))
+        if stacked:
+            specs += [("cbk4", f"L{layer}.qkv", [4096, 4096, 4096], 4096),
+                      ("cbk4", f"L{layer}.o", 4096, 4096),
+                      ("cbk4", f"L{layer}.gate_up", [11008, 11008], 4096),
+                      ("cbk4", f"L{layer}.down", 4096, 11008)]
+        else:
+            for name, N, K in LLAMA7B:
+                specs.append(("cbk4", f"L{layer}.{name}", N, K))
     specs.append(("cbk8", "lm_head", 32000, 4096))
     return specs
+
+
+def total_rows(N):
+    return sum(N) if isinstance(N, (list, tuple)) else N
 
 
 WORKLOADS = {
     # name: (specs, dominant format, description)
     "cbk4_7b_stack": (lambda: cbk4_stack_specs(), "cbk4",
-                      "7B decoder projection stack, 224 x CBK4 + CBK8 LM head 32000x4096"),
+                      "7B decoder projection stack, 224 CBK4 projections (q|k|v and gate|up stacked: "
+                      "128 calls) + CBK8 LM head 32000x4096"),
+    "cbk4_7b_stack_unfused": (lambda: cbk4_stack_specs(stacked=False), "cbk4",
+                              "7B decoder projection stack, 224 CBK4 calls + CBK8 LM head 32000x4096"),
     "q4_0_4096": (lambda: [("q4_0", "q4_0", 4096, 4096)], "q4_0", "Q4_0 GEMV 4096x4096"),
     "q4_0_down": (lambda: [("q4_0", "down", 8192, 28672)], "q4_0", "Q4_0 down 8192x28672"),
     "pq2_5120": (lambda: [("pq2_0", "gate_up", 34816, 5120), ("pq2_0", "down", 5120, 17408)],
@@ -116,7 +131,7 @@ def build_handles(specs, M, device, seed=0):
     # all activations in one buffer and all outputs in another, so the end to
     # end run moves one input copy and one output copy per step
     x_all = torch.empty(sum(M * K for _, _, _, K in specs), dtype=torch.float16, device=device)
-    y_all = torch.empty(sum(M * N for _, _, N, _ in specs), dtype=torch.float32, device=device)
+    y_all = torch.empty(sum(M * total_rows(N) for _, _, N, _ in specs), dtype=torch.float32, device=device)
     xo = yo = 0
     c16 = inputs.cbk_centroids(16)
     c256 = inputs.cbk_centroids(256)
@@ -124,6 +139,23 @@ def build_handles(specs, M, device, seed=0):
     for fmt, name, N, K in specs:
         tag = f"bench/{name}"
         scales = cb = None
+        if isinstance(N, (list, tuple)):   # stacked projections, one codebook each
+            assert fmt == "cbk4"
+            segs = list(N)
+            packed = torch.cat([inputs.cbk_packed_cuda(f"{tag}/{s}", n, K, 4, p16, device, seed)
+                                for s, n in enumerate(segs)])
+            h = qgemv.QGemv.stacked(fmt, segs, K, packed, None, np.concatenate([c16] * len(segs)))
+            N = sum(segs)
+            nbytes = (qgemv.qgemv_packed_bytes(fmt, N, K) + canonical_extra_bytes(fmt, N) * len(segs)
+                      + 2 * M * K + 4 * M * N)
+            del packed
+            x = x_all[xo:xo + M * K].view(M, K)
+            x.copy_(inputs.x_fp16_cuda(f"{tag}/x", M, K, device=device, seed=seed))
+            y = y_all[yo:yo + M * N].view(M, N)
+            xo += M * K
+            yo += M * N
+            ops.append({"fmt": fmt, "name": name, "N": N, "K": K, "h": h, "x": x, "y": y, "bytes": nbytes})
+            continue
         if fmt == "cbk4":
             packed = inputs.cbk_packed_cuda(tag, N, K, 4, p16, device, seed)
             cb = c16
@@ -223,7 +255,7 @@ def run_ours(args, rank, world, device):
     # runs all of them back to back, so no copy is still in L2 when its turn
     # comes round again.
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
-    one_copy = sum(qgemv.qgemv_packed_bytes(f, N, K) for f, _, N, K in specs)
+    one_copy = sum(qgemv.qgemv_packed_bytes(f, total_rows(N), K) for f, _, N, K in specs)
     R = 1 if one_copy >= 3 * l2 else -(-3 * l2 // one_copy)
     copies = [build_handles(specs, M, device, seed=r) for r in range(R)]
     ops = [o for c_ops, _, _ in copies for o in c_ops]
@@ -380,7 +412,7 @@ def oracle_sample(workload, M, rows, seed=0):
     from bit_weight_only_gb300 import inputs
     specs_fn, dominant, _ = WORKLOADS[workload]
     fmt, name, N, K = next(s for s in specs_fn() if s[0] == dominant)
-    rows = min(rows, N)
+    rows = min(rows, total_rows(N))
     g = inputs.rng(f"cpu/{name}", seed)
     scales = cb = None
     if fmt == "cbk4":

@@ -419,7 +419,7 @@ cudaError_t prepare(const PrepareArgs& a, cudaStream_t s) {
   return e;
 }
 
-cudaError_t dequant(const uint8_t* tiles, const void* aux, int64_t N, int64_t K, int nKT,
+cudaError_t dequant(const uint8_t* tiles, const void* aux, const int32_t*, int64_t N, int64_t K, int nKT,
                     float* w_out, cudaStream_t s) {
   dequant_kernel<<<grid_for(N * (K / 8)), 256, 0, s>>>(tiles, static_cast<const uint8_t*>(aux), N, K,
                                                        nKT, w_out);
@@ -477,7 +477,7 @@ const FormatOps* ops_aqlm() {
   static const FormatOps ops = {
       /*format=*/5, aqlm::kKC, aqlm::kTileBytes, /*aux_bytes=*/aqlm::kCodebookBytes,
       &aqlm::smem_bytes, &aqlm::setup, &aqlm::launch, &aqlm::prepare, &aqlm::dequant,
-      /*tile_rows=*/aqlm::kRows, /*partial_stride=*/aqlm::kPartialStride, /*aux_per_row=*/2};
+      /*cb_entries=*/0, /*tile_rows=*/aqlm::kRows, /*partial_stride=*/aqlm::kPartialStride, /*aux_per_row=*/2};
   return &ops;
 }
 

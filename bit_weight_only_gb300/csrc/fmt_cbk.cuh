@@ -70,6 +70,7 @@ struct FmtCBK4 {
   static constexpr int kTileBytes = kLaneSlots * kRowsPerLane * 32;      // 32768
   __host__ __device__ static constexpr int stages(int M) { return M <= 4 ? 4 : 2; }
   static constexpr int kSharedBytes = kLutBytes;
+  static constexpr int kCbEntries = 16;
   static constexpr float kOutScale = 1.0f;
   static constexpr int kSumGroups = 1;  // unused: codebook values carry no offset
   using XRegs = XRegsT<2>;
@@ -78,9 +79,8 @@ struct FmtCBK4 {
   // 32 lane copies (32 consecutive words: no bank conflict).  The 16
   // centroids are read once per lane and passed around with shuffles.
   template <int NT>
-  __device__ static void init_shared(uint8_t* lut, const GemvParams& p, int warp, int lane) {
+  __device__ static void init_shared(uint8_t* lut, const uint16_t* cb, int warp, int lane) {
     constexpr int W = NT / 32;
-    const uint16_t* cb = static_cast<const uint16_t*>(p.aux);
     const uint32_t mine = cb[lane & 15];
 #pragma unroll 4
     for (int e = warp; e < 256; e += W) {
@@ -189,6 +189,7 @@ struct FmtCBK8 {
   static constexpr int kKT = kKW * kSlices;                              // 256
   static constexpr int kTileBytes = kLaneSlots * kRowsPerLane * 32;      // 32768
   __host__ __device__ static constexpr int stages(int M) { return M <= 4 ? 4 : 2; }
+  static constexpr int kCbEntries = 256;
   static constexpr int kSharedBytes = kLutBytes;
   static constexpr float kOutScale = 1.0f;
   static constexpr int kSumGroups = 1;  // unused
@@ -197,9 +198,8 @@ struct FmtCBK8 {
   // As for CBK4: warp w writes entries w + (NT/32)*j, one conflict-free row
   // of 32 lane copies each; lane l first reads centroids 32*i + l.
   template <int NT>
-  __device__ static void init_shared(uint8_t* lut, const GemvParams& p, int warp, int lane) {
+  __device__ static void init_shared(uint8_t* lut, const uint16_t* cb, int warp, int lane) {
     constexpr int W = NT / 32;
-    const uint16_t* cb = static_cast<const uint16_t*>(p.aux);
     float reg[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) reg[i] = h2f(cb[32 * i + lane]);
@@ -308,10 +308,12 @@ __global__ void prepare_kernel(const uint8_t* __restrict__ canon, int64_t N, int
   }
 }
 
-// Exact decode (codebook entry of each index) from the prepared tiles.
+// Exact decode (codebook entry of each index) from the prepared tiles; cb
+// holds one codebook (cb_stride 0) or one copy per row tile (cb_stride =
+// entries, stacked handles).
 template <class F, int kBitsPerIndex>
 __global__ void dequant_kernel(const uint8_t* __restrict__ tiles, const uint16_t* __restrict__ cb,
-                               int64_t N, int64_t K, int nKT, float* __restrict__ w) {
+                               int64_t cb_stride, int64_t N, int64_t K, int nKT, float* __restrict__ w) {
   const int64_t total = N * K;
   for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
        e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -326,8 +328,17 @@ __global__ void dequant_kernel(const uint8_t* __restrict__ tiles, const uint16_t
     const uint8_t byte = tiles[tile * F::kTileBytes + ((j * 2 + h) * kLaneSlots + cw * 32 + lane) * 16 +
                                byte_in_row % 16];
     const int idx = kBitsPerIndex == 8 ? byte : ((el & 1) ? (byte >> 4) : (byte & 15));
-    w[e] = h2f(cb[idx]);
+    w[e] = h2f(cb[(n / kTileRows) * cb_stride + idx]);
   }
+}
+
+// aux[rt][e] = codebook seg_of_rt[rt] entry e: one copy per row tile.
+template <int E>
+__global__ void expand_codebooks_kernel(const uint16_t* __restrict__ cbs, const int32_t* __restrict__ seg_of_rt,
+                                        int64_t nRT, uint16_t* __restrict__ out) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < nRT * E;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    out[i] = cbs[static_cast<int64_t>(seg_of_rt[i / E]) * E + i % E];
 }
 
 inline int grid_for(int64_t items, int threads) {

@@ -15,13 +15,17 @@ cudaError_t prepare(const PrepareArgs& a, cudaStream_t s) {
                                                                        nchunks, a.tiles);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  return cudaMemcpyAsync(a.aux, a.codebooks, 256 * sizeof(uint16_t), cudaMemcpyDeviceToDevice, s);
+  if (a.seg_of_rt == nullptr)  // one codebook
+    return cudaMemcpyAsync(a.aux, a.codebooks, 256 * sizeof(uint16_t), cudaMemcpyDeviceToDevice, s);
+  cbk::expand_codebooks_kernel<256><<<cbk::grid_for(a.nRT * 256, 256), 256, 0, s>>>(
+      a.codebooks, a.seg_of_rt, a.nRT, static_cast<uint16_t*>(a.aux));
+  return cudaGetLastError();
 }
 
-cudaError_t dequant(const uint8_t* tiles, const void* aux, int64_t N, int64_t K, int nKT, float* w,
-                    cudaStream_t s) {
+cudaError_t dequant(const uint8_t* tiles, const void* aux, const int32_t* seg_of_rt, int64_t N, int64_t K,
+                    int nKT, float* w, cudaStream_t s) {
   cbk::dequant_kernel<F, 8><<<cbk::grid_for(N * K, 256), 256, 0, s>>>(
-      tiles, static_cast<const uint16_t*>(aux), N, K, nKT, w);
+      tiles, static_cast<const uint16_t*>(aux), seg_of_rt ? 256 : 0, N, K, nKT, w);
   return cudaGetLastError();
 }
 
@@ -29,9 +33,9 @@ cudaError_t dequant(const uint8_t* tiles, const void* aux, int64_t N, int64_t K,
 
 const FormatOps* ops_cbk8() {
   static const FormatOps ops = {
-      /*format=*/3, F::kKT, F::kTileBytes, /*aux_bytes=*/256 * 2,
+      /*format=*/3, F::kKT, F::kTileBytes, /*aux_bytes=*/0,
       &LaunchTable<F>::smem_bytes, &LaunchTable<F>::setup, &LaunchTable<F>::launch,
-      &prepare, &dequant};
+      &prepare, &dequant, /*cb_entries=*/256};
   return &ops;
 }
 

@@ -72,8 +72,9 @@ struct FmtQ4_0 {
   // taken from the word shifted right by 12)
   __host__ __device__ static constexpr int field_pos(int jj) { return jj <= 4 ? 4 * jj : 4 * jj - 12; }
 
+  static constexpr int kCbEntries = 0;
   template <int NT>
-  __device__ static void init_shared(uint8_t*, const GemvParams&, int, int) {}
+  __device__ static void init_shared(uint8_t*, const uint16_t*, int, int) {}
 
   template <int M>
   __device__ static void load_x(XRegs& xr, const GemvParams& p, int kt, int slice, int lane) {
@@ -190,8 +191,9 @@ struct FmtPQ2 {
 
   __host__ __device__ static constexpr int field_pos(int jj) { return jj <= 10 ? 2 * jj : 2 * jj - 12; }
 
+  static constexpr int kCbEntries = 0;
   template <int NT>
-  __device__ static void init_shared(uint8_t*, const GemvParams&, int, int) {}
+  __device__ static void init_shared(uint8_t*, const uint16_t*, int, int) {}
 
   template <int M>
   __device__ static void load_x(XRegs& xr, const GemvParams& p, int kt, int slice, int lane) {

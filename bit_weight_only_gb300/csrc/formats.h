@@ -19,6 +19,8 @@ struct PrepareArgs {
   int nKT;                   // k tiles per row tile
   uint8_t* tiles;            // out: nRT * nKT * tile_bytes
   void* aux;                 // out: format data (aux_bytes), may be nullptr
+  int nseg;                  // codebooks (stacked handles; 1 otherwise)
+  const int32_t* seg_of_rt;  // device [nRT] codebook of each row tile, or nullptr
 };
 
 struct FormatOps {
@@ -31,8 +33,9 @@ struct FormatOps {
   cudaError_t (*launch)(int M, const GemvParams& p, int grid, cudaStream_t s);
   cudaError_t (*prepare)(const PrepareArgs& a, cudaStream_t s);
   // w_out[n*K + k] = exact decoded weight, read back from the prepared tiles
-  cudaError_t (*dequant)(const uint8_t* tiles, const void* aux, int64_t N, int64_t K, int nKT,
-                         float* w_out, cudaStream_t s);
+  cudaError_t (*dequant)(const uint8_t* tiles, const void* aux, const int32_t* seg_of_rt, int64_t N,
+                         int64_t K, int nKT, float* w_out, cudaStream_t s);
+  int cb_entries = 0;               // fp16 entries per codebook (CBK4 16, CBK8 256)
   int tile_rows = 128;              // output rows per prepared tile
   int64_t partial_stride = 128 * 16;  // floats per stream-K partial slot
   int64_t aux_per_row = 0;          // aux bytes per output row, after aux_bytes

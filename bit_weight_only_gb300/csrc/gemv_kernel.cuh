@@ -69,6 +69,7 @@ struct GemvParams {
   float* y;              // [M][N] fp32
   float* partials;       // [gridDim.x][2][partial stride], all ones between calls
   const CtaPlan* plan;   // [gridDim.x]
+  const int32_t* seg_of_rt;  // stacked table formats: [row tiles] segment of each; else null
   int* err;              // error word (kErr* bits)
   const void* aux;       // format data (codebooks ...)
   int64_t N, K;
@@ -303,6 +304,20 @@ __device__ __forceinline__ void wait_plan() {
   __syncthreads();
 }
 
+// The codebook of row tile rt (table formats): aux holds one codebook, or
+// for a stacked handle one copy per row tile.
+template <class F>
+__device__ __forceinline__ const uint16_t* table_of(const GemvParams& p, int64_t rt) {
+  return static_cast<const uint16_t*>(p.aux) + (p.seg_of_rt != nullptr ? rt * F::kCbEntries : 0);
+}
+
+// Table rebuild at a segment change of a stacked handle: rare, so out of
+// line, keeping the main loop's register allocation as without stacking.
+template <class F, int NT>
+__device__ __noinline__ void rebuild_table(uint8_t* lut, const uint16_t* cb, int warp, int lane) {
+  F::template init_shared<NT>(lut, cb, warp, lane);
+}
+
 template <class F, int M>
 __global__ void __launch_bounds__(gemv_threads<M>(), 1) gemv_kernel(const GemvParams p) {
   constexpr int NS = F::stages(M);
@@ -322,6 +337,7 @@ __global__ void __launch_bounds__(gemv_threads<M>(), 1) gemv_kernel(const GemvPa
   uint64_t* full = reinterpret_cast<uint64_t*>(fsh + F::kSharedBytes);
   uint64_t* empty = full + NS;
   __shared__ volatile int s_abort;
+  __shared__ int s_seg[2];
   __shared__ __align__(16) CtaPlan s_plan;
 
   const int warp = threadIdx.x >> 5;
@@ -333,6 +349,8 @@ __global__ void __launch_bounds__(gemv_threads<M>(), 1) gemv_kernel(const GemvPa
   const int64_t c = blockIdx.x;
   const int64_t t0 = stream_split(c, p.T, G);
   const int64_t t1 = stream_split(c + 1, p.T, G);
+
+  const int64_t rt_first = div_fast(t0, p.nKT);
 
   // The elected thread initializes the barriers and at once starts filling
   // the ring NS - 1 tiles ahead of the math, so the first tiles are in
@@ -355,7 +373,18 @@ __global__ void __launch_bounds__(gemv_threads<M>(), 1) gemv_kernel(const GemvPa
     }
   }
   fetch_plan(&s_plan, p.plan, c, tid);
-  F::template init_shared<NT>(fsh, p, warp, lane);
+  // Table formats keep one codebook copy per row tile in aux (stacked
+  // handles hold several codebooks); the first row tile's needs no lookup.
+  // Stacked handles (several codebooks): s_seg = segment of the table in
+  // shared memory and of the row tile after it, kept by thread 0.
+  if constexpr (F::kCbEntries > 0) {
+    if (p.seg_of_rt != nullptr && tid == 0 && ntiles > 0) {
+      const int64_t nRT = div_fast(p.T, p.nKT);
+      s_seg[0] = __ldg(p.seg_of_rt + rt_first);
+      s_seg[1] = rt_first + 1 < nRT ? __ldg(p.seg_of_rt + rt_first + 1) : s_seg[0];
+    }
+  }
+  F::template init_shared<NT>(fsh, table_of<F>(p, rt_first), warp, lane);
   __syncthreads();
 
   float* xs = xs_all + warp * XS_FLOATS;
@@ -382,6 +411,20 @@ __global__ void __launch_bounds__(gemv_threads<M>(), 1) gemv_kernel(const GemvPa
   int su = static_cast<int>(n_issued % NS);            // next stage to fill
   uint32_t phu = static_cast<uint32_t>((n_issued / NS) & 1);
   for (int64_t i = 0; i < ntiles; ++i) {
+    // A new row tile of a stacked handle may use another codebook: rebuild
+    // the table once every warp is done with the old one.
+    if constexpr (F::kCbEntries > 0) {
+      if (p.seg_of_rt != nullptr && kt == 0 && i > 0) {
+        __syncthreads();  // every warp is done with the old table and has read s_seg
+        if (s_seg[1] != s_seg[0]) rebuild_table<F, NT>(fsh, table_of<F>(p, rt), warp, lane);
+        __syncthreads();
+        if (tid == 0) {
+          const int64_t nRT = div_fast(p.T, p.nKT);
+          s_seg[0] = s_seg[1];
+          s_seg[1] = rt + 1 < nRT ? __ldg(p.seg_of_rt + rt + 1) : s_seg[0];
+        }
+      }
+    }
     bool abort = s_abort != 0;
 
     // Refill: tile u = i + NS - 1 goes to the stage released by tile

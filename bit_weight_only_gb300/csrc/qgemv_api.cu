@@ -165,6 +165,7 @@ struct qgemv_ctx {
   void* aux;
   float* partials;
   qgemv::CtaPlan* plan;
+  int32_t* seg_of_rt;  // inside aux (table formats), else nullptr
   int* err;
 };
 
@@ -183,8 +184,12 @@ int64_t qgemv_packed_bytes(int format, int64_t N, int64_t K) {
   return 0;
 }
 
-qgemv_handle qgemv_create(int format, int64_t N, int64_t K, const void* packed, const void* scales,
-                          const void* codebooks) {
+}  // extern "C"
+
+// Both create calls: `nseg` codebooks for the row segments `seg_rows`
+// (one segment covering all N rows for qgemv_create).
+static qgemv_handle create_impl(int format, int64_t N, int64_t K, const void* packed, const void* scales,
+                                const void* codebooks, int nseg, const int64_t* seg_rows) {
   const qgemv::FormatOps* ops = ops_for(format);
   if (k_multiple(format) == 0) {
     set_error(QGEMV_ERR_ARG, "unknown format %d", format);
@@ -245,6 +250,16 @@ qgemv_handle qgemv_create(int format, int64_t N, int64_t K, const void* packed, 
   h->nKT = static_cast<int>((K + ops->kt - 1) / ops->kt);
   h->T = h->nRT * h->nKT;
   h->grid = static_cast<int>(h->T < sms ? h->T : sms);
+  // codebook segment of every row tile (table formats)
+  std::vector<int32_t> seg_of_rt(static_cast<size_t>(h->nRT), 0);
+  {
+    int64_t row = 0;
+    for (int s = 0; s < nseg; ++s) {
+      for (int64_t r = row; r < row + seg_rows[s]; r += ops->tile_rows)
+        seg_of_rt[static_cast<size_t>(r / ops->tile_rows)] = s;
+      row += seg_rows[s];
+    }
+  }
 
   void *d_packed = nullptr, *d_scales = nullptr, *d_cb = nullptr;
   auto cleanup = [&](int code, const char* what, cudaError_t ce) -> qgemv_handle {
@@ -265,16 +280,25 @@ qgemv_handle qgemv_create(int format, int64_t N, int64_t K, const void* packed, 
 
   e = to_device(packed, static_cast<size_t>(qgemv_packed_bytes(format, N, K)), &d_packed);
   if (e == cudaSuccess) e = to_device(scales, 2 * scales_count(format, N), &d_scales);
-  if (e == cudaSuccess) e = to_device(codebooks, 2 * codebook_count(format), &d_cb);
+  if (e == cudaSuccess) e = to_device(codebooks, 2 * codebook_count(format) * nseg, &d_cb);
   if (e != cudaSuccess) return cleanup(QGEMV_ERR_CUDA, "copying the canonical inputs", e);
 
   e = cudaMalloc(&h->tiles, static_cast<size_t>(h->T) * ops->tile_bytes);
-  const int64_t aux_bytes = ops->aux_bytes + ops->aux_per_row * N;
+  // table formats: one codebook, or (stacked) one copy per row tile followed
+  // by the row tiles' segments
+  const bool stacked = ops->cb_entries > 0 && nseg > 1;
+  const int64_t table_bytes = int64_t(2) * ops->cb_entries * (stacked ? h->nRT : 1);
+  const int64_t aux_bytes = ops->cb_entries > 0 ? table_bytes + (stacked ? 4 * h->nRT : 0)
+                                                : ops->aux_bytes + ops->aux_per_row * N;
   if (e == cudaSuccess && aux_bytes > 0) e = cudaMalloc(&h->aux, static_cast<size_t>(aux_bytes));
   if (e == cudaSuccess)
     e = cudaMalloc(&h->partials, sizeof(float) * 2 * ops->partial_stride * static_cast<size_t>(h->grid));
   if (e == cudaSuccess) e = cudaMalloc(&h->plan, sizeof(qgemv::CtaPlan) * h->grid);
   if (e == cudaSuccess) e = cudaMalloc(&h->err, sizeof(int));
+  if (e == cudaSuccess && stacked) {
+    h->seg_of_rt = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(h->aux) + table_bytes);
+    e = cudaMemcpy(h->seg_of_rt, seg_of_rt.data(), 4 * seg_of_rt.size(), cudaMemcpyHostToDevice);
+  }
   if (e == cudaSuccess) {
     std::vector<qgemv::CtaPlan> plan = plan_stream_k(h->T, h->grid, h->nKT, ops->tile_rows);
     e = cudaMemcpy(h->plan, plan.data(), sizeof(qgemv::CtaPlan) * plan.size(), cudaMemcpyHostToDevice);
@@ -295,6 +319,8 @@ qgemv_handle qgemv_create(int format, int64_t N, int64_t K, const void* packed, 
   a.nKT = h->nKT;
   a.tiles = h->tiles;
   a.aux = h->aux;
+  a.nseg = nseg;
+  a.seg_of_rt = h->seg_of_rt;
   e = ops->prepare(a, 0);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return cleanup(QGEMV_ERR_CUDA, "preparing the tiles", e);
@@ -304,6 +330,41 @@ qgemv_handle qgemv_create(int format, int64_t N, int64_t K, const void* packed, 
   cudaFree(d_cb);
   ok();
   return h;
+}
+
+extern "C" {
+
+qgemv_handle qgemv_create(int format, int64_t N, int64_t K, const void* packed, const void* scales,
+                          const void* codebooks) {
+  const int64_t rows[1] = {N};
+  return create_impl(format, N, K, packed, scales, codebooks, 1, rows);
+}
+
+qgemv_handle qgemv_create_stacked(int format, int nseg, const int64_t* seg_rows, int64_t K,
+                                  const void* packed, const void* scales, const void* codebooks) {
+  const qgemv::FormatOps* ops = ops_for(format);
+  if (!ops || k_multiple(format) == 0) {
+    set_error(QGEMV_ERR_ARG, "unknown format %d", format);
+    return nullptr;
+  }
+  if (format == QGEMV_AQLM_2X8) {
+    set_error(QGEMV_ERR_ARG, "format %d cannot be stacked", format);
+    return nullptr;
+  }
+  if (nseg < 1 || !seg_rows) {
+    set_error(QGEMV_ERR_ARG, "nseg must be >= 1 with seg_rows given");
+    return nullptr;
+  }
+  int64_t N = 0;
+  for (int s = 0; s < nseg; ++s) {
+    if (seg_rows[s] <= 0 || (s + 1 < nseg && seg_rows[s] % ops->tile_rows)) {
+      set_error(QGEMV_ERR_ARG, "segment %d has %lld rows (must be > 0, and a multiple of %d but for the last)",
+                s, (long long)seg_rows[s], ops->tile_rows);
+      return nullptr;
+    }
+    N += seg_rows[s];
+  }
+  return create_impl(format, N, K, packed, scales, codebooks, ops->cb_entries > 0 ? nseg : 1, seg_rows);
 }
 
 static bool valid(qgemv_handle h) { return h && h->magic == kMagic; }
@@ -320,6 +381,7 @@ int qgemv_run(qgemv_handle h, const void* x, int M, float* y, void* stream) {
   p.y = y;
   p.partials = h->partials;
   p.plan = h->plan;
+  p.seg_of_rt = h->seg_of_rt;
   p.err = h->err;
   p.aux = h->aux;
   p.N = h->N;
@@ -334,7 +396,7 @@ int qgemv_run(qgemv_handle h, const void* x, int M, float* y, void* stream) {
 int qgemv_dequant(qgemv_handle h, float* w_out, void* stream) {
   if (!valid(h)) return set_error(QGEMV_ERR_ARG, "invalid handle");
   if (!w_out) return set_error(QGEMV_ERR_ARG, "w_out is NULL");
-  cudaError_t e = h->ops->dequant(h->tiles, h->aux, h->N, h->K, h->nKT, w_out,
+  cudaError_t e = h->ops->dequant(h->tiles, h->aux, h->seg_of_rt, h->N, h->K, h->nKT, w_out,
                                   static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_error(e, "launching the decode kernel");
   return ok();

@@ -26,6 +26,9 @@ _SIGNATURES = {
     "qgemv_packed_bytes": (ctypes.c_int64, [ctypes.c_int, ctypes.c_int64, ctypes.c_int64]),
     "qgemv_create": (ctypes.c_void_p, [ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
                                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
+    "qgemv_create_stacked": (ctypes.c_void_p, [ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_int64),
+                                               ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
+                                               ctypes.c_void_p]),
     "qgemv_run": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
                                  ctypes.c_void_p, ctypes.c_void_p]),
     "qgemv_dequant": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
@@ -99,6 +102,16 @@ def qgemv_create(fmt, N: int, K: int, packed: int, scales: int | None,
     return h
 
 
+def qgemv_create_stacked(fmt, seg_rows, K: int, packed: int, scales: int | None,
+                         codebooks: int | None) -> int:
+    """Several projections sharing K, rows stacked; one codebook per segment."""
+    rows = (ctypes.c_int64 * len(seg_rows))(*[int(r) for r in seg_rows])
+    h = load().qgemv_create_stacked(_fmt(fmt), len(seg_rows), rows, K, packed, scales, codebooks)
+    if not h:
+        raise QgemvError(qgemv_last_error_code(), qgemv_last_error())
+    return h
+
+
 def qgemv_run(h: int, x: int, M: int, y: int, stream=None) -> int:
     return _check(load().qgemv_run(h, x, M, y, _stream_ptr(stream)))
 
@@ -160,6 +173,19 @@ class QGemv:
         c, kc = _addr(codebooks)
         self.handle = qgemv_create(self.fmt, self.N, self.K, p, s, c)
         del kp, ks, kc
+
+    @classmethod
+    def stacked(cls, fmt, seg_rows, K: int, packed, scales=None, codebooks=None):
+        """One handle over projections with the same K (rows stacked in
+        order, codebook s for segment s): one run computes them all."""
+        self = cls.__new__(cls)
+        self.fmt, self.N, self.K = _fmt(fmt), int(sum(seg_rows)), int(K)
+        p, kp = _addr(packed)
+        s, ks = _addr(scales)
+        c, kc = _addr(codebooks)
+        self.handle = qgemv_create_stacked(self.fmt, list(seg_rows), self.K, p, s, c)
+        del kp, ks, kc
+        return self
 
     def run(self, x, y, stream=None):
         M = x.shape[0]

@@ -92,6 +92,26 @@ int64_t qgemv_packed_bytes(int format, int64_t N, int64_t K);
 qgemv_handle qgemv_create(int format, int64_t N, int64_t K, const void* packed,
                           const void* scales, const void* codebooks);
 
+/* Create one handle for several projections that share K and therefore the
+ * activations (the attention's q, k and v, or an MLP's gate and up): their
+ * weight rows stacked in order, so that one qgemv_run computes all of them,
+ * y = [y_0 | y_1 | ...] along N, with one launch instead of one per
+ * projection.  The pages fuse such projections in their runtimes; this call
+ * has no further counterpart there.
+ *   nseg >= 1 segments; segment s has seg_rows[s] > 0 output rows, and every
+ *     segment but the last must have a multiple of 128 rows (the prepared
+ *     tile height), so that no tile mixes two codebooks.
+ *   packed: the segments' canonical bytes one after the other, which is the
+ *     canonical layout of the stacked matrix (rows of all formats are
+ *     independent).
+ *   codebooks (CBK4, CBK8): nseg codebooks one after the other (16 or 256
+ *     fp16 each); segment s decodes with codebook s.  NULL for Q4_0 and
+ *     PQ2_0, whose stacked handle is the plain concatenation.
+ *   AQLM 2x8 is not accepted (QGEMV_ERR_ARG).
+ * Host or device pointers, copying, errors: as for qgemv_create.             */
+qgemv_handle qgemv_create_stacked(int format, int nseg, const int64_t* seg_rows, int64_t K,
+                                  const void* packed, const void* scales, const void* codebooks);
+
 /* y = x . dequant(W)^T for M rows.
  *   x: device fp16 [M][K] row-major, 4-byte aligned.
  *   y: device fp32 [M][N] row-major, 4-byte aligned; fully overwritten.

@@ -26,7 +26,7 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for f in ("qgemv_create", "qgemv_run", "qgemv_destroy", "qgemv_dequant",
+    for f in ("qgemv_create", "qgemv_create_stacked", "qgemv_run", "qgemv_destroy", "qgemv_dequant",
               "qgemv_last_error", "qgemv_packed_bytes", "qgemv_quantize_q4_0", "qgemv_status"):
         assert f in names
 
@@ -69,6 +69,19 @@ def test_run_rejects_bad_handle_and_m(lib):
     assert lib.qgemv_dequant(None, 16, None) == qgemv.QGEMV_ERR_ARG
     assert lib.qgemv_status(None) == qgemv.QGEMV_ERR_ARG
     lib.qgemv_destroy(None)  # NULL is accepted
+
+
+def test_stacked_create_rejects_bad_arguments_on_host(lib):
+    rows = (ctypes.c_int64 * 2)(100, 200)
+    assert not lib.qgemv_create_stacked(qgemv.CBK4, 2, rows, 256, 1, None, 1)
+    assert "multiple of 128" in qgemv.qgemv_last_error()
+    assert not lib.qgemv_create_stacked(qgemv.CBK4, 0, rows, 256, 1, None, 1)
+    assert qgemv.qgemv_last_error_code() == qgemv.QGEMV_ERR_ARG
+    ok_rows = (ctypes.c_int64 * 2)(2048, 2048)
+    assert not lib.qgemv_create_stacked(qgemv.AQLM_2X8, 2, ok_rows, 256, 1, 1, 1)
+    assert "cannot be stacked" in qgemv.qgemv_last_error()
+    assert not lib.qgemv_create_stacked(99, 1, ok_rows, 256, 1, None, None)
+    assert "unknown format" in qgemv.qgemv_last_error()
 
 
 def test_quantizer_rejects_bad_shape(lib):
