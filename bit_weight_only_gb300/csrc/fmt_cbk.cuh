@@ -74,6 +74,25 @@ struct FmtCBK4 {
   static constexpr float kOutScale = 1.0f;
   static constexpr int kSumGroups = 1;  // unused: codebook values carry no offset
   using XRegs = XRegsT<2>;
+  static constexpr int kTcStages = 2;
+  static constexpr int kTcBlockSteps = 0;  // no block scale
+
+  // centroids of row 4*lane + j of the slice, k in order (64 fp16): one
+  // table read per index byte gives the (even k, odd k) fp16 pair
+  __device__ static void tc_decode_row(const uint8_t* stage, int slice, int j, int lane, const uint8_t* lut,
+                                       uint32_t* dst) {
+    const int t = slice * 32 + lane;
+    const uint4 lo = lds128(stage + ((j * 2 + 0) * kLaneSlots + t) * 16);
+    const uint4 hi = lds128(stage + ((j * 2 + 1) * kLaneSlots + t) * 16);
+    const uint32_t lane4 = static_cast<uint32_t>(lane) << 2;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {  // word i: index bytes 4i .. 4i+3 = k pairs
+      const uint32_t w = i < 4 ? word_of(lo, i) : word_of(hi, i - 4);
+      sts128_u32(dst + 4 * i, lds32(lut, lut_offset(w, lane4, 0)), lds32(lut, lut_offset(w, lane4, 1)),
+                 lds32(lut, lut_offset(w, lane4, 2)), lds32(lut, lut_offset(w, lane4, 3)));
+    }
+  }
+  __device__ static float tc_scale(const uint8_t*, int, int, int, int) { return 1.f; }
 
   // Warp w writes entries w, w + NT/32, ...; its 32 lanes write one entry's
   // 32 lane copies (32 consecutive words: no bank conflict).  The 16
@@ -190,6 +209,8 @@ struct FmtCBK8 {
   static constexpr int kTileBytes = kLaneSlots * kRowsPerLane * 32;      // 32768
   __host__ __device__ static constexpr int stages(int M) { return M <= 4 ? 4 : 2; }
   static constexpr int kCbEntries = 256;
+  static constexpr int kTcStages = 2;
+  static constexpr int kTcBlockSteps = 0;
   static constexpr int kSharedBytes = kLutBytes;
   static constexpr float kOutScale = 1.0f;
   static constexpr int kSumGroups = 1;  // unused
@@ -197,6 +218,28 @@ struct FmtCBK8 {
 
   // As for CBK4: warp w writes entries w + (NT/32)*j, one conflict-free row
   // of 32 lane copies each; lane l first reads centroids 32*i + l.
+  // centroids of row 4*lane + j of the slice, k in order (32 fp16, exact)
+  __device__ static void tc_decode_row(const uint8_t* stage, int slice, int j, int lane, const uint8_t* lut,
+                                       uint32_t* dst) {
+    const int t = slice * 32 + lane;
+    const uint4 lo = lds128(stage + ((j * 2 + 0) * kLaneSlots + t) * 16);
+    const uint4 hi = lds128(stage + ((j * 2 + 1) * kLaneSlots + t) * 16);
+    const uint32_t lane4 = static_cast<uint32_t>(lane) << 2;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {  // word i: index bytes 4i .. 4i+3 = k 4i .. 4i+3
+      const uint32_t w = i < 4 ? word_of(lo, i) : word_of(hi, i - 4);
+      uint32_t v[2];
+#pragma unroll
+      for (int pp = 0; pp < 2; ++pp) {
+        const __half2 h = __floats2half2_rn(__uint_as_float(lds32(lut, lut_offset(w, lane4, 2 * pp))),
+                                            __uint_as_float(lds32(lut, lut_offset(w, lane4, 2 * pp + 1))));
+        v[pp] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+      *reinterpret_cast<uint2*>(dst + 2 * i) = make_uint2(v[0], v[1]);
+    }
+  }
+  __device__ static float tc_scale(const uint8_t*, int, int, int, int) { return 1.f; }
+
   template <int NT>
   __device__ static void init_shared(uint8_t* lut, const uint16_t* cb, int warp, int lane) {
     constexpr int W = NT / 32;

@@ -50,6 +50,13 @@ __device__ __forceinline__ uint32_t word8(const uint4& lo, const uint4& hi, int 
   return i < 4 ? word_of(lo, i) : word_of(hi, i - 4);
 }
 
+// ---------------------------------------------- tensor-core row decode --
+//
+// The tensor-core kernel (M > 4) decodes each 32-byte row chunk of a slice
+// into the slice's KW weights (or integer codes, when a block scale applies
+// later) as fp16, k in order, into one shared-memory row; every value is
+// exact in fp16.
+
 // ------------------------------------------------------------------ Q4_0 --
 //
 // Tile: 128 rows x 512 k.  Slice s <-> Q4_0 blocks 2s, 2s+1 of the tile
@@ -66,6 +73,30 @@ struct FmtQ4_0 {
   static constexpr int kSharedBytes = 0;
   static constexpr float kOutScale = kFieldOutScale;
   static constexpr int kSumGroups = 2;  // one offset sum per Q4_0 block of the slice
+  static constexpr int kTcStages = 2;
+  static constexpr int kTcBlockSteps = 2;  // k16 steps per scale block (32 k)
+
+  // codes q - 8 of row 4*lane + j of the slice, k in order (64 fp16)
+  __device__ static void tc_decode_row(const uint8_t* stage, int slice, int j, int lane, const uint8_t*,
+                                       uint32_t* dst) {
+    const int t = slice * 32 + lane;
+    const uint4 lo = lds128(stage + ((j * 2 + 0) * kLaneSlots + t) * 16);
+    const uint4 hi = lds128(stage + ((j * 2 + 1) * kLaneSlots + t) * 16);
+    constexpr uint32_t kBias = 0x64086408u;  // (1032, 1032)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {  // word i: k = 8i .. 8i+7
+      const uint32_t w = word8(lo, hi, i);
+      const uint32_t X = w & 0x0F0F0F0Fu, Y = (w >> 4) & 0x0F0F0F0Fu;
+      sts128_u32(dst + 4 * i, tc_nibble_pair(X, Y, tc_pair_sel(0), kBias), tc_nibble_pair(X, Y, tc_pair_sel(1), kBias),
+                 tc_nibble_pair(X, Y, tc_pair_sel(2), kBias), tc_nibble_pair(X, Y, tc_pair_sel(3), kBias));
+    }
+  }
+
+  // d of row 4*ql + j (ql = lane slot within the slice), block b of the slice
+  __device__ static float tc_scale(const uint8_t* stage, int slice, int ql, int j, int b) {
+    const int t = slice * 32 + ql;
+    return h2f(*reinterpret_cast<const uint16_t*>(stage + kCodeBytes + ((t * 4 + j) * 2 + b) * 2));
+  }
   using XRegs = XRegsT<2>;
 
   // bit position of the nibble of k = 8i + jj once extracted (jj >= 5 are
@@ -188,6 +219,36 @@ struct FmtPQ2 {
   static constexpr float kOutScale = kFieldOutScale;
   static constexpr int kSumGroups = 1;
   using XRegs = XRegsT<4>;
+  static constexpr int kTcStages = 2;
+  static constexpr int kTcBlockSteps = 8;  // one scale per slice (128 k)
+
+  // codes c - 1 of row 4*lane + j of the slice, k in order (128 fp16)
+  __device__ static void tc_decode_row(const uint8_t* stage, int slice, int j, int lane, const uint8_t*,
+                                       uint32_t* dst) {
+    const int t = slice * 32 + lane;
+    const uint4 lo = lds128(stage + ((j * 2 + 0) * kLaneSlots + t) * 16);
+    const uint4 hi = lds128(stage + ((j * 2 + 1) * kLaneSlots + t) * 16);
+    constexpr uint32_t kBias = 0x64016401u;  // (1025, 1025)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {  // word i: k = 16i .. 16i+15, field jj at bits 2jj
+      const uint32_t w = word8(lo, hi, i);
+      const uint32_t E0 = w & 0x03030303u, E1 = (w >> 2) & 0x03030303u;
+      const uint32_t E2 = (w >> 4) & 0x03030303u, E3 = (w >> 6) & 0x03030303u;
+      uint32_t v[8];
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {  // byte b: fields 4b .. 4b+3
+        v[2 * b] = tc_nibble_pair(E0, E1, tc_pair_sel(b), kBias);
+        v[2 * b + 1] = tc_nibble_pair(E2, E3, tc_pair_sel(b), kBias);
+      }
+      sts128_u32(dst + 8 * i, v[0], v[1], v[2], v[3]);
+      sts128_u32(dst + 8 * i + 4, v[4], v[5], v[6], v[7]);
+    }
+  }
+
+  __device__ static float tc_scale(const uint8_t* stage, int slice, int ql, int j, int) {
+    const int t = slice * 32 + ql;
+    return h2f(*reinterpret_cast<const uint16_t*>(stage + kCodeBytes + (t * 4 + j) * 2));
+  }
 
   __host__ __device__ static constexpr int field_pos(int jj) { return jj <= 10 ? 2 * jj : 2 * jj - 12; }
 

@@ -177,7 +177,7 @@ __device__ __forceinline__ int64_t cta_of_tile(int64_t t, int64_t T, int64_t G) 
 template <int ROWS, int M, int NT>
 __device__ __forceinline__ void finish_rows(const GemvParams& p, int64_t stride, const CtaPlan& pl, int sg,
                                             const __half* row_scales, float out_scale, float* s_sub,
-                                            int tid) {
+                                            int tid, int mrows = M) {
   const int64_t rt = pl.seg_rt[sg];
   const int64_t cf = pl.seg_cf[sg];
   const int S = pl.seg_S[sg];
@@ -185,7 +185,7 @@ __device__ __forceinline__ void finish_rows(const GemvParams& p, int64_t stride,
   const int nr = pl.seg_nr[sg];
   if (nr <= 0) return;  // more contributors than rows: this one has no slice
   constexpr int B = M > 8 ? 8 : 16;  // slots polled at once (registers)
-  const int items = nr * M;
+  const int items = nr * mrows;
   const int H = (S <= 16 || items >= NT) ? 1 : NT / items;
   const int cpt = H == 1 ? S : (S + H - 1) / H;
   // slot of contributor cf + i: side 1 only for the first one, if its run began earlier
@@ -195,7 +195,7 @@ __device__ __forceinline__ void finish_rows(const GemvParams& p, int64_t stride,
     const int item = H == 1 ? t : t / H;
     const int h = H == 1 ? 0 : t - item * H;
     const int m = M == 1 ? 0 : item / nr;
-    const int r = r0 + (M == 1 ? item : item - m * nr);
+    const int r = r0 + (M == 1 ? item : item - m * nr);  // M is mrows' upper bound
     const int64_t n = rt * ROWS + r;
     float sc = out_scale;
     if (row_scales != nullptr && h == 0 && n < p.N) sc *= __half2float(row_scales[n]);
@@ -259,18 +259,18 @@ __device__ __forceinline__ void finish_rows(const GemvParams& p, int64_t stride,
 template <int ROWS, int M, int NT>
 __device__ __noinline__ void finish_rows_call(const GemvParams& p, int64_t stride, const CtaPlan& pl, int sg,
                                               const __half* row_scales, float out_scale, float* s_sub,
-                                              int tid) {
-  finish_rows<ROWS, M, NT>(p, stride, pl, sg, row_scales, out_scale, s_sub, tid);
+                                              int tid, int mrows) {
+  finish_rows<ROWS, M, NT>(p, stride, pl, sg, row_scales, out_scale, s_sub, tid, mrows);
 }
 
 template <int ROWS, int M, int NT>
 __device__ __forceinline__ void finish_segment(const GemvParams& p, int64_t stride, const CtaPlan& pl, int sg,
                                                const __half* row_scales, float out_scale, float* s_sub,
-                                               int tid) {
+                                               int tid, int mrows = M) {
   if constexpr (M > 8)
-    finish_rows_call<ROWS, M, NT>(p, stride, pl, sg, row_scales, out_scale, s_sub, tid);
+    finish_rows_call<ROWS, M, NT>(p, stride, pl, sg, row_scales, out_scale, s_sub, tid, mrows);
   else
-    finish_rows<ROWS, M, NT>(p, stride, pl, sg, row_scales, out_scale, s_sub, tid);
+    finish_rows<ROWS, M, NT>(p, stride, pl, sg, row_scales, out_scale, s_sub, tid, mrows);
 }
 
 // CTA c's share of the stream: [c * T / G, (c + 1) * T / G), with 32-bit

@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include "gemv_kernel.cuh"
+#include "tc_kernel.cuh"
 
 namespace qgemv {
 
@@ -59,10 +60,32 @@ struct LaunchTable {
     QGEMV_SETUP(7) QGEMV_SETUP(8) QGEMV_SETUP(9) QGEMV_SETUP(10) QGEMV_SETUP(11) QGEMV_SETUP(12)
     QGEMV_SETUP(13) QGEMV_SETUP(14) QGEMV_SETUP(15) QGEMV_SETUP(16)
 #undef QGEMV_SETUP
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gemv_tc_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize, tc_smem_bytes<F>());
     return e;
   }
 
+  // M >= kTcMinM runs on the tensor cores (tc_kernel.cuh): one kernel for
+  // every such M, the activations padded to 16 rows.
+  static constexpr int kTcMinM = 5;
+
+  static cudaError_t launch_tc(const GemvParams& p, int M, int grid, cudaStream_t s) {
+    static_assert(tc_smem_bytes<F>() <= 227 * 1024 - 256, "shared memory budget exceeded");
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = tc_smem_bytes<F>();
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemv_tc_kernel<F>, p, M);
+  }
+
   static cudaError_t launch(int M, const GemvParams& p, int grid, cudaStream_t s) {
+    if (M >= kTcMinM && M <= kMaxM) return launch_tc(p, M, grid, s);
     switch (M) {
 #define QGEMV_LAUNCH(m) \
   case m:               \
