@@ -128,24 +128,4 @@ __host__ __device__ constexpr float pow2f(int e) {
   return e >= 0 ? (e == 0 ? 1.0f : 2.0f * pow2f(e - 1)) : 0.5f * pow2f(e + 1);
 }
 
-// ---- tensor-core path: fp16 rows from integer codes ----
-// q in 0..15 in byte p of X (low nibble of the pair) and of Y (high): the
-// fp16 pair (q_lo - off, q_hi - off), exact, via 1024 + q.
-__device__ __forceinline__ uint32_t tc_nibble_pair(uint32_t X, uint32_t Y, uint32_t sel, uint32_t bias2) {
-  uint32_t r;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(X), "r"(Y), "r"(sel));
-  r |= 0x64006400u;
-  const __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&r), *reinterpret_cast<const __half2*>(&bias2));
-  return *reinterpret_cast<const uint32_t*>(&h);
-}
-
-// selector of tc_nibble_pair for byte p: [X.b(p), sign 0, Y.b(p), sign 0]
-__host__ __device__ constexpr uint32_t tc_pair_sel(int p) {
-  return static_cast<uint32_t>(p | ((8 | p) << 4) | ((4 + p) << 8) | ((12 + p) << 12));
-}
-
-__device__ __forceinline__ void sts128_u32(uint32_t* dst, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  *reinterpret_cast<uint4*>(dst) = make_uint4(a, b, c, d);
-}
-
 }  // namespace qgemv

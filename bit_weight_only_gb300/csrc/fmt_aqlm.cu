@@ -36,10 +36,12 @@
 //
 // Work split: row blocks of 2048 rows x chunks of 128 inputs ("units"),
 // spread over a persistent grid stream-K style (each CTA a contiguous run of
-// units), partial sums of split row blocks finished by the last contributor
-// in a fixed order (deterministic).  Codes stream straight from HBM into
-// registers (128-bit loads, one unit ahead); shared memory carries only the
-// tables, whose reads are the binding on-chip resource.
+// units).  Split row blocks are finished after the main loop by all their
+// contributors, each summing a slice of rows from polled partial slots in a
+// fixed order (finish_rows, gemv_kernel.cuh; deterministic).  Codes stream
+// straight from HBM into registers (128-bit loads through an 8-row ring per
+// lane); shared memory carries only the tables, whose reads are the binding
+// on-chip resource.
 //
 // M > 1: a pass handles MB <= 2 activation rows (one 64 KB table slab each)
 // and a call with M rows makes ceil(M / 2) passes over the codes.

@@ -17,6 +17,7 @@
 #pragma once
 
 #include "gemv_kernel.cuh"
+#include "mma_kernel.cuh"
 
 namespace qgemv {
 
@@ -74,25 +75,6 @@ struct FmtCBK4 {
   static constexpr float kOutScale = 1.0f;
   static constexpr int kSumGroups = 1;  // unused: codebook values carry no offset
   using XRegs = XRegsT<2>;
-  static constexpr int kTcStages = 2;
-  static constexpr int kTcBlockSteps = 0;  // no block scale
-
-  // centroids of row 4*lane + j of the slice, k in order (64 fp16): one
-  // table read per index byte gives the (even k, odd k) fp16 pair
-  __device__ static void tc_decode_row(const uint8_t* stage, int slice, int j, int lane, const uint8_t* lut,
-                                       uint32_t* dst) {
-    const int t = slice * 32 + lane;
-    const uint4 lo = lds128(stage + ((j * 2 + 0) * kLaneSlots + t) * 16);
-    const uint4 hi = lds128(stage + ((j * 2 + 1) * kLaneSlots + t) * 16);
-    const uint32_t lane4 = static_cast<uint32_t>(lane) << 2;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {  // word i: index bytes 4i .. 4i+3 = k pairs
-      const uint32_t w = i < 4 ? word_of(lo, i) : word_of(hi, i - 4);
-      sts128_u32(dst + 4 * i, lds32(lut, lut_offset(w, lane4, 0)), lds32(lut, lut_offset(w, lane4, 1)),
-                 lds32(lut, lut_offset(w, lane4, 2)), lds32(lut, lut_offset(w, lane4, 3)));
-    }
-  }
-  __device__ static float tc_scale(const uint8_t*, int, int, int, int) { return 1.f; }
 
   // Warp w writes entries w, w + NT/32, ...; its 32 lanes write one entry's
   // 32 lane copies (32 consecutive words: no bank conflict).  The 16
@@ -107,6 +89,37 @@ struct FmtCBK4 {
       const uint32_t hi = __shfl_sync(0xffffffffu, mine, e >> 4);
       *reinterpret_cast<uint32_t*>(lut + e * 256 + lane * 4) = lo | (hi << 16);
     }
+  }
+
+  // ---- register-decode tensor-core path (mma_kernel.cuh) ----
+  // Thread q of a fragment row holds index word q of each half h of the
+  // row's slice chunk (k = 32h + 8q .. +7); k16 step ks takes bytes 2(ks%2)
+  // and 2(ks%2)+1 of word ks/2, i.e. k pairs (32h + 8q + 4(ks%2), +1) and
+  // (.. + 2, +3) with h = ks/2, each one table read.
+  static constexpr int kMmaSharedBytes = kLutBytes;
+  static constexpr int kMmaBlockSteps = 0;
+  static constexpr int kMmaXWords = 8;  // x[m][32h + 8q .. +7], h = 0, 1
+  __host__ __device__ static constexpr int mma_stages(int nb) { return nb == 1 ? 4 : 3; }
+  __host__ __device__ static constexpr bool mma_prefetch_x(int) { return true; }
+  template <int NT>
+  __device__ static void mma_init_shared(uint8_t* lut, const uint16_t* cb, int warp, int lane) {
+    init_shared<NT>(lut, cb, warp, lane);
+  }
+  __device__ static void mma_load_row(const uint8_t* stage, int slice, int l, int j, int q, uint32_t (&w)[2]) {
+    mma_row_words(stage, slice, l, j, q, w);
+  }
+  __device__ static uint2 mma_frag(const uint32_t (&w)[2], int ks, const uint8_t* lut, uint32_t lane4) {
+    const uint32_t wd = w[ks >> 1];
+    const int b = 2 * (ks & 1);
+    return make_uint2(lds32(lut, lut_offset(wd, lane4, b)), lds32(lut, lut_offset(wd, lane4, b + 1)));
+  }
+  __device__ static void mma_load_x(uint32_t (&xw)[kMmaXWords], const GemvParams& p, int M, int m, int64_t kb,
+                                    int q, bool vec) {
+    ld_x8(xw, p, M, m, kb + 8 * q, vec);
+    ld_x8(xw + 4, p, M, m, kb + 32 + 8 * q, vec);
+  }
+  __device__ static uint2 mma_bfrag(const uint32_t (&xw)[kMmaXWords], int ks) {
+    return make_uint2(xw[2 * ks], xw[2 * ks + 1]);
   }
 
   template <int M>
@@ -209,8 +222,6 @@ struct FmtCBK8 {
   static constexpr int kTileBytes = kLaneSlots * kRowsPerLane * 32;      // 32768
   __host__ __device__ static constexpr int stages(int M) { return M <= 4 ? 4 : 2; }
   static constexpr int kCbEntries = 256;
-  static constexpr int kTcStages = 2;
-  static constexpr int kTcBlockSteps = 0;
   static constexpr int kSharedBytes = kLutBytes;
   static constexpr float kOutScale = 1.0f;
   static constexpr int kSumGroups = 1;  // unused
@@ -218,28 +229,6 @@ struct FmtCBK8 {
 
   // As for CBK4: warp w writes entries w + (NT/32)*j, one conflict-free row
   // of 32 lane copies each; lane l first reads centroids 32*i + l.
-  // centroids of row 4*lane + j of the slice, k in order (32 fp16, exact)
-  __device__ static void tc_decode_row(const uint8_t* stage, int slice, int j, int lane, const uint8_t* lut,
-                                       uint32_t* dst) {
-    const int t = slice * 32 + lane;
-    const uint4 lo = lds128(stage + ((j * 2 + 0) * kLaneSlots + t) * 16);
-    const uint4 hi = lds128(stage + ((j * 2 + 1) * kLaneSlots + t) * 16);
-    const uint32_t lane4 = static_cast<uint32_t>(lane) << 2;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {  // word i: index bytes 4i .. 4i+3 = k 4i .. 4i+3
-      const uint32_t w = i < 4 ? word_of(lo, i) : word_of(hi, i - 4);
-      uint32_t v[2];
-#pragma unroll
-      for (int pp = 0; pp < 2; ++pp) {
-        const __half2 h = __floats2half2_rn(__uint_as_float(lds32(lut, lut_offset(w, lane4, 2 * pp))),
-                                            __uint_as_float(lds32(lut, lut_offset(w, lane4, 2 * pp + 1))));
-        v[pp] = *reinterpret_cast<const uint32_t*>(&h);
-      }
-      *reinterpret_cast<uint2*>(dst + 2 * i) = make_uint2(v[0], v[1]);
-    }
-  }
-  __device__ static float tc_scale(const uint8_t*, int, int, int, int) { return 1.f; }
-
   template <int NT>
   __device__ static void init_shared(uint8_t* lut, const uint16_t* cb, int warp, int lane) {
     constexpr int W = NT / 32;
@@ -252,6 +241,47 @@ struct FmtCBK8 {
       const float v = __shfl_sync(0xffffffffu, reg[(W * j) >> 5], e & 31);
       *reinterpret_cast<float*>(lut + e * 256 + lane * 4) = v;
     }
+  }
+
+  // ---- register-decode tensor-core path (mma_kernel.cuh) ----
+  // The table holds c[e] as fp16 (low half of the entry).  Thread q of a
+  // fragment row holds index word q of each half h of the slice chunk (k =
+  // 16h + 4q .. +3); k16 step ks takes word ks: k pairs (16ks + 4q, +1) and
+  // (16ks + 4q + 2, +3).
+  static constexpr int kMmaSharedBytes = kLutBytes;
+  static constexpr int kMmaBlockSteps = 0;
+  static constexpr int kMmaXWords = 4;  // x[m][16h + 4q .. +3], h = 0, 1
+  __host__ __device__ static constexpr int mma_stages(int nb) { return nb == 1 ? 4 : 3; }
+  __host__ __device__ static constexpr bool mma_prefetch_x(int) { return true; }
+  template <int NT>
+  __device__ static void mma_init_shared(uint8_t* lut, const uint16_t* cb, int warp, int lane) {
+    constexpr int W = NT / 32;
+    uint32_t reg[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) reg[i] = cb[32 * i + lane];
+#pragma unroll
+    for (int j = 0; j < 256 / W; ++j) {
+      const int e = warp + W * j;  // (W * j) >> 5 == e >> 5 since W divides 32
+      const uint32_t v = __shfl_sync(0xffffffffu, reg[(W * j) >> 5], e & 31);
+      *reinterpret_cast<uint32_t*>(lut + e * 256 + lane * 4) = v;
+    }
+  }
+  __device__ static void mma_load_row(const uint8_t* stage, int slice, int l, int j, int q, uint32_t (&w)[2]) {
+    mma_row_words(stage, slice, l, j, q, w);
+  }
+  __device__ static uint2 mma_frag(const uint32_t (&w)[2], int ks, const uint8_t* lut, uint32_t lane4) {
+    const uint32_t wd = w[ks];
+    const uint32_t c0 = lds32(lut, lut_offset(wd, lane4, 0)), c1 = lds32(lut, lut_offset(wd, lane4, 1));
+    const uint32_t c2 = lds32(lut, lut_offset(wd, lane4, 2)), c3 = lds32(lut, lut_offset(wd, lane4, 3));
+    return make_uint2(prmt(c0, c1, 0x5410u), prmt(c2, c3, 0x5410u));
+  }
+  __device__ static void mma_load_x(uint32_t (&xw)[kMmaXWords], const GemvParams& p, int M, int m, int64_t kb,
+                                    int q, bool vec) {
+    ld_x4(xw, p, M, m, kb + 4 * q, vec);
+    ld_x4(xw + 2, p, M, m, kb + 16 + 4 * q, vec);
+  }
+  __device__ static uint2 mma_bfrag(const uint32_t (&xw)[kMmaXWords], int ks) {
+    return make_uint2(xw[2 * ks], xw[2 * ks + 1]);
   }
 
   template <int M>

@@ -25,6 +25,7 @@
 #pragma once
 
 #include "gemv_kernel.cuh"
+#include "mma_kernel.cuh"
 
 namespace qgemv {
 
@@ -50,13 +51,6 @@ __device__ __forceinline__ uint32_t word8(const uint4& lo, const uint4& hi, int 
   return i < 4 ? word_of(lo, i) : word_of(hi, i - 4);
 }
 
-// ---------------------------------------------- tensor-core row decode --
-//
-// The tensor-core kernel (M > 4) decodes each 32-byte row chunk of a slice
-// into the slice's KW weights (or integer codes, when a block scale applies
-// later) as fp16, k in order, into one shared-memory row; every value is
-// exact in fp16.
-
 // ------------------------------------------------------------------ Q4_0 --
 //
 // Tile: 128 rows x 512 k.  Slice s <-> Q4_0 blocks 2s, 2s+1 of the tile
@@ -73,30 +67,46 @@ struct FmtQ4_0 {
   static constexpr int kSharedBytes = 0;
   static constexpr float kOutScale = kFieldOutScale;
   static constexpr int kSumGroups = 2;  // one offset sum per Q4_0 block of the slice
-  static constexpr int kTcStages = 2;
-  static constexpr int kTcBlockSteps = 2;  // k16 steps per scale block (32 k)
 
-  // codes q - 8 of row 4*lane + j of the slice, k in order (64 fp16)
-  __device__ static void tc_decode_row(const uint8_t* stage, int slice, int j, int lane, const uint8_t*,
-                                       uint32_t* dst) {
-    const int t = slice * 32 + lane;
-    const uint4 lo = lds128(stage + ((j * 2 + 0) * kLaneSlots + t) * 16);
-    const uint4 hi = lds128(stage + ((j * 2 + 1) * kLaneSlots + t) * 16);
-    constexpr uint32_t kBias = 0x64086408u;  // (1032, 1032)
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {  // word i: k = 8i .. 8i+7
-      const uint32_t w = word8(lo, hi, i);
-      const uint32_t X = w & 0x0F0F0F0Fu, Y = (w >> 4) & 0x0F0F0F0Fu;
-      sts128_u32(dst + 4 * i, tc_nibble_pair(X, Y, tc_pair_sel(0), kBias), tc_nibble_pair(X, Y, tc_pair_sel(1), kBias),
-                 tc_nibble_pair(X, Y, tc_pair_sel(2), kBias), tc_nibble_pair(X, Y, tc_pair_sel(3), kBias));
-    }
+  // ---- register-decode tensor-core path (mma_kernel.cuh) ----
+  // Thread q of a fragment row holds code word q of each block b of the
+  // slice (k = 32b + 8q .. +7).  k16 step ks lies in block b = ks / 2;
+  // with sub = ks % 2 its two k pairs are nibbles (2sub, 2sub + 4) and
+  // (2sub + 1, 2sub + 5) of that word: one LOP3 makes each pair 1024 + code
+  // (or 1024 + 16 code) as fp16, one HFMA2 turns it into code - 8, exactly.
+  static constexpr int kMmaSharedBytes = 0;
+  static constexpr int kMmaBlockSteps = 2;
+  static constexpr int kMmaXWords = 8;  // x[m][32b + 8q .. +7], b = 0, 1
+  __host__ __device__ static constexpr int mma_stages(int nb) { return nb == 1 ? 5 : 4; }
+  __host__ __device__ static constexpr bool mma_prefetch_x(int) { return true; }
+  template <int NT>
+  __device__ static void mma_init_shared(uint8_t*, const uint16_t*, int, int) {}
+  __device__ static void mma_load_row(const uint8_t* stage, int slice, int l, int j, int q, uint32_t (&w)[2]) {
+    mma_row_words(stage, slice, l, j, q, w);
+  }
+  __device__ static void mma_scales(const uint8_t* stage, int slice, int l, int j, float (&d)[2]) {
+    const int t = slice * 32 + l;
+    const __half2 h = *reinterpret_cast<const __half2*>(stage + kCodeBytes + (t * 4 + j) * 4);
+    const float2 f = __half22float2(h);
+    d[0] = f.x;
+    d[1] = f.y;
+  }
+  __device__ static uint2 mma_frag(const uint32_t (&w)[2], int ks, const uint8_t*, uint32_t) {
+    const uint32_t wd = (ks & 1) ? (w[ks >> 1] >> 8) : w[ks >> 1];
+    return make_uint2(hfma2_u32(field_pair(wd, 0x000F000Fu), 0x3C003C00u, 0xE408E408u),   // x1 - 1032
+                      hfma2_u32(field_pair(wd, 0x00F000F0u), 0x2C002C00u, 0xD480D480u));  // /16 - 72
+  }
+  __device__ static void mma_load_x(uint32_t (&xw)[kMmaXWords], const GemvParams& p, int M, int m, int64_t kb,
+                                    int q, bool vec) {
+    ld_x8(xw, p, M, m, kb + 8 * q, vec);
+    ld_x8(xw + 4, p, M, m, kb + 32 + 8 * q, vec);
+  }
+  __device__ static uint2 mma_bfrag(const uint32_t (&xw)[kMmaXWords], int ks) {
+    const uint32_t* X = xw + 4 * (ks >> 1);  // (x0,x1) (x2,x3) (x4,x5) (x6,x7) of the block's 8 k
+    const int sub = ks & 1;
+    return make_uint2(prmt(X[sub], X[sub + 2], 0x5410u), prmt(X[sub], X[sub + 2], 0x7632u));
   }
 
-  // d of row 4*ql + j (ql = lane slot within the slice), block b of the slice
-  __device__ static float tc_scale(const uint8_t* stage, int slice, int ql, int j, int b) {
-    const int t = slice * 32 + ql;
-    return h2f(*reinterpret_cast<const uint16_t*>(stage + kCodeBytes + ((t * 4 + j) * 2 + b) * 2));
-  }
   using XRegs = XRegsT<2>;
 
   // bit position of the nibble of k = 8i + jj once extracted (jj >= 5 are
@@ -219,35 +229,50 @@ struct FmtPQ2 {
   static constexpr float kOutScale = kFieldOutScale;
   static constexpr int kSumGroups = 1;
   using XRegs = XRegsT<4>;
-  static constexpr int kTcStages = 2;
-  static constexpr int kTcBlockSteps = 8;  // one scale per slice (128 k)
 
-  // codes c - 1 of row 4*lane + j of the slice, k in order (128 fp16)
-  __device__ static void tc_decode_row(const uint8_t* stage, int slice, int j, int lane, const uint8_t*,
-                                       uint32_t* dst) {
-    const int t = slice * 32 + lane;
-    const uint4 lo = lds128(stage + ((j * 2 + 0) * kLaneSlots + t) * 16);
-    const uint4 hi = lds128(stage + ((j * 2 + 1) * kLaneSlots + t) * 16);
-    constexpr uint32_t kBias = 0x64016401u;  // (1025, 1025)
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {  // word i: k = 16i .. 16i+15, field jj at bits 2jj
-      const uint32_t w = word8(lo, hi, i);
-      const uint32_t E0 = w & 0x03030303u, E1 = (w >> 2) & 0x03030303u;
-      const uint32_t E2 = (w >> 4) & 0x03030303u, E3 = (w >> 6) & 0x03030303u;
-      uint32_t v[8];
-#pragma unroll
-      for (int b = 0; b < 4; ++b) {  // byte b: fields 4b .. 4b+3
-        v[2 * b] = tc_nibble_pair(E0, E1, tc_pair_sel(b), kBias);
-        v[2 * b + 1] = tc_nibble_pair(E2, E3, tc_pair_sel(b), kBias);
-      }
-      sts128_u32(dst + 8 * i, v[0], v[1], v[2], v[3]);
-      sts128_u32(dst + 8 * i + 4, v[4], v[5], v[6], v[7]);
-    }
+  // ---- register-decode tensor-core path (mma_kernel.cuh) ----
+  // Thread q of a fragment row holds code word q of each half h of the
+  // slice (word 4h + q: k = 64h + 16q .. +15).  k16 step ks uses the word of
+  // half ks / 4; with sub = ks % 4
+  // its two k pairs are fields (2sub, 2sub + 8) and (2sub + 1, 2sub + 9) of
+  // that word.  Pair (f, f + 8), f' = f % 4, taken from the word shifted
+  // right by 8 when f >= 4: one LOP3 gives 1024 + 4^f' c per half as fp16,
+  // one HFMA2 (times 4^-f', minus 1024 4^-f' + 1) gives c - 1, exactly.
+  static constexpr int kMmaSharedBytes = 0;
+  static constexpr int kMmaBlockSteps = 8;
+  static constexpr int kMmaXWords = 16;  // x[m][64h + 16q .. +15], h = 0, 1
+  __host__ __device__ static constexpr int mma_stages(int) { return 5; }
+  __host__ __device__ static constexpr bool mma_prefetch_x(int nb) { return nb == 1; }
+  template <int NT>
+  __device__ static void mma_init_shared(uint8_t*, const uint16_t*, int, int) {}
+  __device__ static void mma_load_row(const uint8_t* stage, int slice, int l, int j, int q, uint32_t (&w)[2]) {
+    mma_row_words(stage, slice, l, j, q, w);
   }
-
-  __device__ static float tc_scale(const uint8_t* stage, int slice, int ql, int j, int) {
-    const int t = slice * 32 + ql;
-    return h2f(*reinterpret_cast<const uint16_t*>(stage + kCodeBytes + (t * 4 + j) * 2));
+  __device__ static void mma_scales(const uint8_t* stage, int slice, int l, int j, float (&d)[1]) {
+    const int t = slice * 32 + l;
+    d[0] = h2f(*reinterpret_cast<const uint16_t*>(stage + kCodeBytes + (t * 4 + j) * 2));
+  }
+  __device__ static uint32_t pq2_pair(uint32_t w, int f) {
+    constexpr uint32_t kScale[4] = {0x3C003C00u, 0x34003400u, 0x2C002C00u, 0x24002400u};  // 1, 1/4, 1/16, 1/64
+    constexpr uint32_t kOff[4] = {0xE401E401u, 0xDC04DC04u, 0xD410D410u, 0xCC40CC40u};    // -1025, -257, -65, -17
+    const int fp = f & 3;
+    const uint32_t src = f >= 4 ? (w >> 8) : w;
+    return hfma2_u32(field_pair(src, 0x00030003u << (2 * fp)), kScale[fp], kOff[fp]);
+  }
+  __device__ static uint2 mma_frag(const uint32_t (&w)[2], int ks, const uint8_t*, uint32_t) {
+    const uint32_t wd = w[ks >> 2];
+    const int sub = ks & 3;
+    return make_uint2(pq2_pair(wd, 2 * sub), pq2_pair(wd, 2 * sub + 1));
+  }
+  __device__ static void mma_load_x(uint32_t (&xw)[kMmaXWords], const GemvParams& p, int M, int m, int64_t kb,
+                                    int q, bool vec) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) ld_x8(xw + 4 * i, p, M, m, kb + 64 * (i >> 1) + 16 * q + 8 * (i & 1), vec);
+  }
+  __device__ static uint2 mma_bfrag(const uint32_t (&xw)[kMmaXWords], int ks) {
+    const uint32_t* X = xw + 8 * (ks >> 2);  // (x0,x1) .. (x14,x15) of the word's 16 k
+    const int sub = ks & 3;
+    return make_uint2(prmt(X[sub], X[sub + 4], 0x5410u), prmt(X[sub], X[sub + 4], 0x7632u));
   }
 
   __host__ __device__ static constexpr int field_pos(int jj) { return jj <= 10 ? 2 * jj : 2 * jj - 12; }

@@ -1,0 +1,428 @@
+// mma_kernel.cuh -- the tensor-core GEMV with register-level decode, for
+// every M = 1..16.
+//
+//   y[m][n] = sum_k x[m][k] * w[n][k]
+//
+// is computed as D = W * X^T with mma.m16n8k16 (f16 x f16 -> f32): the
+// weights are the 16 x 16 A operand (16 weight rows), the activations the
+// 16 x 8 B operand (8 activation rows; two B operands for M > 8), so an
+// activation block is padded to 8 rows, not 16.
+//
+//   * Same prepared tiles, TMA ring, stream-K split, CTA plans and polled
+//     split-K fix-up as gemv_kernel.
+//   * Sixteen warps, two per k-slice: warp (slice s, half h) covers slice s
+//     of every tile for row groups j = 2h, 2h + 1 (rows 4l + j, l = 0..31),
+//     as four 16-row m-tiles (j = 2h + mt/2, l = 16 (mt & 1) + 0..15).
+//   * Each thread reads the codes of its two fragment rows straight from the
+//     stage (a few 32/64-bit loads per row, conflict-free) and decodes them
+//     in registers into the A fragments -- no decoded copy of the weights is
+//     stored anywhere.  Inside a k16 step the fragment's k order is a
+//     permutation of the slice's k, chosen per format so that the decode is
+//     cheapest; the B fragments (activations, read from global memory a tile
+//     ahead) use the same permutation, so the products are unchanged.
+//   * Formats with a block scale (Q4_0: 32 k, PQ2_0: 128 k) accumulate the
+//     codes' products of a block (exact fp16 integers) and add d * block
+//     into the fp32 accumulator; the D fragment's rows are the thread's own
+//     weight rows, so the scales need no exchange.
+//   * At the end of a row tile the eight slices' results are added in a
+//     fixed tree order through shared memory, then stored to y or to the
+//     stream-K partial slots.
+//
+// Format hooks (members of the format struct): mma_stages(NB),
+// mma_prefetch_x(NB), kMmaSharedBytes, kMmaBlockSteps (0: no scale), kMmaXWords,
+// mma_init_shared, mma_load_row, mma_frag, mma_load_x, mma_bfrag and, with
+// a scale, mma_scales.
+#pragma once
+
+#include "gemv_kernel.cuh"
+
+namespace qgemv {
+
+constexpr int kMmaWarps = 16;
+constexpr int kMmaThreads = 32 * kMmaWarps;  // 512
+constexpr int kMmaTiles = 4;                 // 16-row m-tiles per warp
+
+// tree reduction buffer: [4 slots][2 halves][4 m-tiles][NB][32 lanes] float4
+template <int NB>
+__host__ __device__ constexpr int mma_red_bytes() { return 4 * 2 * kMmaTiles * NB * 32 * 16; }
+
+template <class F, int NB>
+__host__ __device__ constexpr int mma_smem_bytes() {
+  return F::mma_stages(NB) * F::kTileBytes + mma_red_bytes<NB>() + F::kMmaSharedBytes + 2 * F::mma_stages(NB) * 8;
+}
+
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
+
+// (a & mask) | 0x64006400: the two 16-bit fields as fp16 1024 + field
+__device__ __forceinline__ uint32_t field_pair(uint32_t a, uint32_t mask) {
+  uint32_t r;
+  asm("lop3.b32 %0, %1, %2, %3, 0xea;" : "=r"(r) : "r"(a), "r"(mask), "r"(0x64006400u));
+  return r;
+}
+
+// fp16x2 a * s + c (exact for the small integers and powers of two used here)
+__device__ __forceinline__ uint32_t hfma2_u32(uint32_t a, uint32_t s, uint32_t c) {
+  uint32_t r;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(s), "r"(c));
+  return r;
+}
+
+// Code word q of each 16-byte half of row (l, j)'s slice chunk, from the
+// codes region [j][h][t][16 B] (t = 32 slice + l).  A warp's eight rows of
+// one half are 128 contiguous bytes, so each of the two loads is one
+// conflict-free wavefront.
+__device__ __forceinline__ void mma_row_words(const uint8_t* stage, int slice, int l, int j, int q,
+                                              uint32_t (&w)[2]) {
+  const int t = slice * 32 + l;
+  w[0] = *reinterpret_cast<const uint32_t*>(stage + ((j * 2 + 0) * kLaneSlots + t) * 16 + 4 * q);
+  w[1] = *reinterpret_cast<const uint32_t*>(stage + ((j * 2 + 1) * kLaneSlots + t) * 16 + 4 * q);
+}
+
+// x[m][k0 .. k0+3] as two fp16 pairs (k0 a multiple of 4); zero for m >= M
+// and for k >= K.  `vec`: x is 16-byte aligned and K % 8 == 0.
+__device__ __forceinline__ void ld_x4(uint32_t* out, const GemvParams& p, int M, int m, int64_t k0, bool vec) {
+  if (m >= M || k0 >= p.K) {
+    out[0] = out[1] = 0u;
+    return;
+  }
+  const unsigned short* row = reinterpret_cast<const unsigned short*>(p.x) + m * p.K;
+  if (vec) {
+    const uint2 v = __ldg(reinterpret_cast<const uint2*>(row + k0));
+    out[0] = v.x; out[1] = v.y;
+    return;
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int64_t k = k0 + 2 * i;
+    const uint32_t lo = k < p.K ? __ldg(row + k) : 0u;
+    const uint32_t hi = k + 1 < p.K ? __ldg(row + k + 1) : 0u;
+    out[i] = lo | (hi << 16);
+  }
+}
+
+// x[m][k0 .. k0+7] as four fp16 pairs; zero for m >= M and for k >= K.  k0
+// is a multiple of 8; `vec`: x is 16-byte aligned and K % 8 == 0, so the
+// eight values are one aligned 16-byte load.
+__device__ __forceinline__ void ld_x8(uint32_t* out, const GemvParams& p, int M, int m, int64_t k0, bool vec) {
+  if (m >= M || k0 >= p.K) {
+    out[0] = out[1] = out[2] = out[3] = 0u;
+    return;
+  }
+  const unsigned short* row = reinterpret_cast<const unsigned short*>(p.x) + m * p.K;
+  if (vec) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(row + k0));
+    out[0] = v.x; out[1] = v.y; out[2] = v.z; out[3] = v.w;
+    return;
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int64_t k = k0 + 2 * i;
+    const uint32_t lo = k < p.K ? __ldg(row + k) : 0u;
+    const uint32_t hi = k + 1 < p.K ? __ldg(row + k + 1) : 0u;
+    out[i] = lo | (hi << 16);
+  }
+}
+
+template <class F, int NT>
+__device__ __noinline__ void mma_rebuild_table(uint8_t* lut, const uint16_t* cb, int warp, int lane) {
+  F::template mma_init_shared<NT>(lut, cb, warp, lane);
+}
+
+template <class F, int NB>
+__global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const GemvParams p, int M) {
+  constexpr int NS = F::mma_stages(NB);
+  constexpr int TB = F::kTileBytes;
+  constexpr int KS = F::kKW / 16;        // k16 steps per slice
+  constexpr int BS = F::kMmaBlockSteps;  // k16 steps per scale block, 0: none
+  constexpr int NBLK = BS > 0 ? KS / BS : 1;
+  constexpr int XW = F::kMmaXWords;      // activation words per (thread, activation row)
+  constexpr bool PF = F::mma_prefetch_x(NB);  // activations a tile ahead (registers permitting)
+  constexpr int NT = kMmaThreads;
+
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* ring = smem;
+  float4* red = reinterpret_cast<float4*>(smem + NS * TB);
+  uint8_t* fsh = smem + NS * TB + mma_red_bytes<NB>();
+  uint64_t* full = reinterpret_cast<uint64_t*>(fsh + F::kMmaSharedBytes);
+  uint64_t* empty = full + NS;
+  __shared__ volatile int s_abort;
+  __shared__ int s_seg[2];
+  __shared__ __align__(16) CtaPlan s_plan;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int q = lane & 3, gi = lane >> 2;
+  const int slice = warp % kSlices;
+  const int hf = warp / kSlices;
+  const int64_t G = gridDim.x;
+  const int64_t c = blockIdx.x;
+  const int64_t t0 = stream_split(c, p.T, G);
+  const int64_t t1 = stream_split(c + 1, p.T, G);
+  const int64_t ntiles = t1 - t0;
+  const int64_t rt_first = div_fast(t0, p.nKT);
+
+  const bool elected = (tid == 0);
+  uint64_t pol = 0;
+  int64_t n_issued = 0;
+  if (elected) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kMmaWarps);
+    }
+    s_abort = 0;
+    fence_mbarrier_init();
+    pol = l2_policy_evict_first();
+    for (; n_issued < NS - 1 && n_issued < ntiles; ++n_issued) {
+      mbar_arrive_expect_tx(&full[n_issued], TB);
+      bulk_g2s(ring + n_issued * TB, p.tiles + (t0 + n_issued) * TB, TB, &full[n_issued], pol);
+    }
+  }
+  fetch_plan(&s_plan, p.plan, c, tid);
+  if constexpr (F::kCbEntries > 0) {
+    if (p.seg_of_rt != nullptr && tid == 0 && ntiles > 0) {
+      const int64_t nRT = div_fast(p.T, p.nKT);
+      s_seg[0] = __ldg(p.seg_of_rt + rt_first);
+      s_seg[1] = rt_first + 1 < nRT ? __ldg(p.seg_of_rt + rt_first + 1) : s_seg[0];
+    }
+  }
+  F::template mma_init_shared<NT>(fsh, table_of<F>(p, rt_first), warp, lane);
+  __syncthreads();
+
+  // The prologue touches nothing a previous kernel writes; x and the outputs
+  // wait for the previous grid (programmatic dependent launch).
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
+  int64_t rt = rt_first;
+  int kt = static_cast<int>(t0 - rt * p.nKT);
+  const uint32_t lane4 = static_cast<uint32_t>(lane) << 2;
+  const bool xvec = (reinterpret_cast<uintptr_t>(p.x) & 15) == 0 && (p.K & 7) == 0;
+  // activation fragments of the thread's B rows m = gi + 8 nb (a tile ahead
+  // when PF, else loaded at the top of each tile)
+  uint32_t xw[NB][XW];
+  auto load_x = [&](uint32_t (&dst)[NB][XW], int ktile) {
+    const int64_t kb = static_cast<int64_t>(ktile) * F::kKT + slice * F::kKW;
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) F::mma_load_x(dst[nb], p, M, gi + 8 * nb, kb, q, xvec);
+  };
+  if constexpr (PF) {
+    if (ntiles > 0) load_x(xw, kt);
+  }
+
+  // acc[mt][nb]: D fragment of m-tile mt and activation block nb
+  float acc[kMmaTiles][NB][4];
+#pragma unroll
+  for (int mt = 0; mt < kMmaTiles; ++mt)
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[mt][nb][e] = 0.f;
+
+  int s = 0;
+  uint32_t ph = 0;
+  int su = static_cast<int>(n_issued % NS);
+  uint32_t phu = static_cast<uint32_t>((n_issued / NS) & 1);
+  for (int64_t i = 0; i < ntiles; ++i) {
+    if constexpr (F::kCbEntries > 0) {
+      if (p.seg_of_rt != nullptr && kt == 0 && i > 0) {
+        __syncthreads();
+        if (s_seg[1] != s_seg[0]) mma_rebuild_table<F, NT>(fsh, table_of<F>(p, rt), warp, lane);
+        __syncthreads();
+        if (tid == 0) {
+          const int64_t nRT = div_fast(p.T, p.nKT);
+          s_seg[0] = s_seg[1];
+          s_seg[1] = rt + 1 < nRT ? __ldg(p.seg_of_rt + rt + 1) : s_seg[0];
+        }
+      }
+    }
+    bool abort = s_abort != 0;
+    if (elected && !abort && n_issued < ntiles) {
+      if (n_issued >= NS && !mbar_wait_bounded(&empty[su], phu ^ 1)) {
+        atomicOr(p.err, kErrTimeoutEmpty);
+        s_abort = 1;
+        abort = true;
+      } else {
+        mbar_arrive_expect_tx(&full[su], TB);
+        bulk_g2s(ring + su * TB, p.tiles + (t0 + n_issued) * TB, TB, &full[su], pol);
+        ++n_issued;
+        if (++su == NS) { su = 0; phu ^= 1; }
+      }
+    }
+    const int kt_next = (kt + 1 == p.nKT) ? 0 : kt + 1;
+    uint32_t xn[PF ? NB : 1][PF ? XW : 1];
+    if constexpr (PF) {
+      if (i + 1 < ntiles) load_x(xn, kt_next);
+    } else {
+      load_x(xw, kt);
+    }
+
+    const bool ok = !abort && mbar_wait_bounded(&full[s], ph);
+    if (!ok) {
+      if (!abort && lane == 0) atomicOr(p.err, kErrTimeoutFull);
+      s_abort = 1;
+    } else {
+      const uint8_t* stage = ring + s * TB;
+      // codes (and scales) of the thread's eight rows, then release the stage
+      uint32_t w[kMmaTiles][2][2];
+      float d[kMmaTiles][2][NBLK];
+#pragma unroll
+      for (int mt = 0; mt < kMmaTiles; ++mt) {
+        const int j = 2 * hf + (mt >> 1);
+        const int l = 16 * (mt & 1) + gi;
+        F::mma_load_row(stage, slice, l, j, q, w[mt][0]);
+        F::mma_load_row(stage, slice, l + 8, j, q, w[mt][1]);
+        if constexpr (BS > 0) {
+          F::mma_scales(stage, slice, l, j, d[mt][0]);
+          F::mma_scales(stage, slice, l + 8, j, d[mt][1]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+
+      // MG m-tiles at a time, their MMAs interleaved so that consecutive MMAs
+      // are independent (all four for one activation block; one for two,
+      // which need twice the accumulators)
+      constexpr int MG = NB == 1 ? kMmaTiles : 1;
+#pragma unroll
+      for (int mg = 0; mg < kMmaTiles; mg += MG) {
+#pragma unroll
+        for (int blk = 0; blk < NBLK; ++blk) {
+          float tmp[MG][NB][4];
+#pragma unroll
+          for (int mi = 0; mi < MG; ++mi)
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) tmp[mi][nb][e] = 0.f;
+#pragma unroll
+          for (int ks = blk * (BS > 0 ? BS : KS); ks < (blk + 1) * (BS > 0 ? BS : KS); ++ks) {
+#pragma unroll
+            for (int mi = 0; mi < MG; ++mi) {
+              const int mt = mg + mi;
+              const uint2 r0 = F::mma_frag(w[mt][0], ks, fsh, lane4);  // row gi: (k lo pair, k hi pair)
+              const uint2 r1 = F::mma_frag(w[mt][1], ks, fsh, lane4);  // row gi + 8
+#pragma unroll
+              for (int nb = 0; nb < NB; ++nb) {
+                const uint2 b = F::mma_bfrag(xw[nb], ks);
+                if constexpr (BS > 0)
+                  mma_16816(tmp[mi][nb], r0.x, r1.x, r0.y, r1.y, b.x, b.y);
+                else
+                  mma_16816(acc[mt][nb], r0.x, r1.x, r0.y, r1.y, b.x, b.y);
+              }
+            }
+          }
+          if constexpr (BS > 0) {
+#pragma unroll
+            for (int mi = 0; mi < MG; ++mi)
+#pragma unroll
+              for (int nb = 0; nb < NB; ++nb) {
+                const int mt = mg + mi;
+                acc[mt][nb][0] = fmaf(d[mt][0][blk], tmp[mi][nb][0], acc[mt][nb][0]);
+                acc[mt][nb][1] = fmaf(d[mt][0][blk], tmp[mi][nb][1], acc[mt][nb][1]);
+                acc[mt][nb][2] = fmaf(d[mt][1][blk], tmp[mi][nb][2], acc[mt][nb][2]);
+                acc[mt][nb][3] = fmaf(d[mt][1][blk], tmp[mi][nb][3], acc[mt][nb][3]);
+              }
+          }
+        }
+      }
+    }
+    if (++s == NS) { s = 0; ph ^= 1; }
+    if constexpr (PF) {
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+        for (int e = 0; e < XW; ++e) xw[nb][e] = xn[nb][e];
+    }
+
+    const bool row_end = (kt_next == 0) || (i + 1 == ntiles);
+    const int64_t cur_rt = rt;
+    kt = kt_next;
+    if (kt_next == 0) ++rt;
+    if (!row_end) continue;
+
+    // ---- row-tile epilogue: add the eight slices' results in a fixed tree ----
+#pragma unroll 1
+    for (int width = 4; width >= 1; width >>= 1) {
+      if (slice >= width && slice < 2 * width) {
+#pragma unroll
+        for (int mt = 0; mt < kMmaTiles; ++mt)
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb)
+            red[(((slice - width) * 2 + hf) * kMmaTiles + mt) * NB * 32 + nb * 32 + lane] =
+                make_float4(acc[mt][nb][0], acc[mt][nb][1], acc[mt][nb][2], acc[mt][nb][3]);
+      }
+      named_bar_sync(1, NT);
+      if (slice < width) {
+#pragma unroll
+        for (int mt = 0; mt < kMmaTiles; ++mt)
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb) {
+            const float4 v = red[((slice * 2 + hf) * kMmaTiles + mt) * NB * 32 + nb * 32 + lane];
+            acc[mt][nb][0] += v.x;
+            acc[mt][nb][1] += v.y;
+            acc[mt][nb][2] += v.z;
+            acc[mt][nb][3] += v.w;
+          }
+      }
+      named_bar_sync(1, NT);
+    }
+    if (slice == 0) {
+      const bool owner = (cur_rt * p.nKT >= t0) && ((cur_rt + 1) * p.nKT <= t1);
+      const int side = (cur_rt * p.nKT <= t0) ? 0 : 1;
+      float* my_part = p.partials + (c * 2 + side) * kPartialStride;
+#pragma unroll
+      for (int mt = 0; mt < kMmaTiles; ++mt)
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            // D element e: weight row gi (+8 for e >= 2), activation row 2q + (e & 1)
+            const int m = 8 * nb + 2 * q + (e & 1);
+            const int l = 16 * (mt & 1) + gi + (e >> 1) * 8;
+            const int r = 4 * l + 2 * hf + (mt >> 1);
+            if (m < M) {
+              if (owner) {
+                const int64_t n = cur_rt * kTileRows + r;
+                if (n < p.N) p.y[m * p.N + n] = acc[mt][nb][e];
+              } else {
+                st_relaxed_f32(my_part + m * kTileRows + r, acc[mt][nb][e]);
+              }
+            }
+          }
+    }
+#pragma unroll
+    for (int mt = 0; mt < kMmaTiles; ++mt)
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[mt][nb][e] = 0.f;
+  }
+
+  if (elected && s_abort != 0) {
+    for (int64_t u = (n_issued > NS ? n_issued - NS : 0); u < n_issued; ++u)
+      mbar_wait_bounded(&full[u % NS], static_cast<uint32_t>((u / NS) & 1));
+  }
+
+  // split row tiles: the shared polled-slot finisher, with M activation rows
+  static_assert(mma_red_bytes<NB>() >= 2 * NT * 4, "finishing scratch");
+  float* s_sub = reinterpret_cast<float*>(red);
+  wait_plan();
+  if (s_plan.seg_rt[0] >= 0) finish_segment<kTileRows, 8 * NB, NT>(p, kPartialStride, s_plan, 0, nullptr, 1.0f, s_sub, tid, M);
+  if (s_plan.seg_rt[1] >= 0) finish_segment<kTileRows, 8 * NB, NT>(p, kPartialStride, s_plan, 1, nullptr, 1.0f, s_sub, tid, M);
+}
+
+}  // namespace qgemv

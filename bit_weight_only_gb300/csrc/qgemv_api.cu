@@ -440,6 +440,26 @@ void qgemv_destroy(qgemv_handle h) {
   delete h;
 }
 
+int qgemv_stream_k_plan(int64_t units, int grid, int64_t units_per_row_tile, int rows, int64_t* out) {
+  if (units <= 0 || grid <= 0 || units_per_row_tile <= 0 || rows <= 0 || out == nullptr ||
+      units % units_per_row_tile != 0 || grid > units)
+    return set_error(QGEMV_ERR_ARG, "qgemv_stream_k_plan: bad sizes");
+  const std::vector<qgemv::CtaPlan> plan = plan_stream_k(units, grid, units_per_row_tile, rows);
+  for (int c = 0; c < grid; ++c) {
+    const qgemv::CtaPlan& pl = plan[static_cast<size_t>(c)];
+    int64_t* o = out + static_cast<int64_t>(c) * 12;
+    for (int s = 0; s < 2; ++s) {
+      o[0 + s] = pl.seg_rt[s];
+      o[2 + s] = pl.seg_cf[s];
+      o[4 + s] = pl.seg_S[s];
+      o[6 + s] = pl.seg_r0[s];
+      o[8 + s] = pl.seg_nr[s];
+      o[10 + s] = pl.seg_side1[s];
+    }
+  }
+  return ok();
+}
+
 const char* qgemv_last_error(void) { return g_msg; }
 
 int qgemv_last_error_code(void) { return g_code; }

@@ -38,6 +38,8 @@ _SIGNATURES = {
     "qgemv_run_q4_0_noalloc": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
                                               ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
                                               ctypes.c_void_p]),
+    "qgemv_stream_k_plan": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int, ctypes.c_int64, ctypes.c_int,
+                                           ctypes.POINTER(ctypes.c_int64)]),
     "qgemv_destroy": (None, [ctypes.c_void_p]),
     "qgemv_last_error": (ctypes.c_char_p, []),
     "qgemv_last_error_code": (ctypes.c_int, []),
@@ -132,6 +134,16 @@ def qgemv_run_q4_0_noalloc(packed: int, N: int, K: int, x: int, M: int, y: int,
 
 def qgemv_status(h: int) -> int:
     return _check(load().qgemv_status(h))
+
+
+def qgemv_stream_k_plan(units: int, grid: int, units_per_row_tile: int, rows: int) -> list:
+    """The stream-K split the handles use (host only): per CTA a dict of its
+    two shared-row-tile segments, each field a pair (first, last row tile)."""
+    out = (ctypes.c_int64 * (12 * grid))()
+    _check(load().qgemv_stream_k_plan(units, grid, units_per_row_tile, rows, out))
+    keys = ("rt", "cf", "S", "r0", "nr", "side1")
+    return [{k: (out[12 * c + 2 * i], out[12 * c + 2 * i + 1]) for i, k in enumerate(keys)}
+            for c in range(grid)]
 
 
 def qgemv_destroy(h: int) -> None:

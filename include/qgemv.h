@@ -168,6 +168,20 @@ void qgemv_destroy(qgemv_handle h);
 int qgemv_run_q4_0_noalloc(const void* packed, int64_t N, int64_t K, const void* x, int M,
                            float* y, void* stream);
 
+/* The stream-K work split (host only, no GPU needed), as the handles use it:
+ * `units` work units (prepared tiles; for AQLM_2X8 blocks of 2048 rows x 128
+ * inputs) in row-major order, `units_per_row_tile` of them per row tile of
+ * `rows` output rows, split over `grid` CTAs, CTA c running units
+ * [c*units/grid, (c+1)*units/grid).  Writes 12
+ * int64 per CTA into `out` (caller-owned, grid*12 entries): for its two
+ * shared-row-tile segments s = 0 (first row tile of its run), 1 (last):
+ * out[c*12 + 0 + s] row tile (-1: none), [2 + s] first contributing CTA,
+ * [4 + s] number of contributors, [6 + s] first row of this CTA's slice of
+ * the rows to finish, [8 + s] rows in that slice, [10 + s] 1 if the first
+ * contributor's run began before the row tile.  Returns QGEMV_ERR_ARG if a
+ * size is not positive, units % units_per_row_tile != 0 or grid > units.   */
+int qgemv_stream_k_plan(int64_t units, int grid, int64_t units_per_row_tile, int rows, int64_t* out);
+
 /* Message and code of the last error on the calling thread ("" / 0 if none). */
 const char* qgemv_last_error(void);
 int qgemv_last_error_code(void);

@@ -118,6 +118,26 @@ def test_gemv_edge_shapes(fmt, N, Kmul):
 
 
 @pytest.mark.parametrize("fmt", FORMATS)
+@pytest.mark.parametrize("M", [1, 2, 7, 16])
+def test_gemv_x_only_4_byte_aligned(fmt, M):
+    """x starting 4 bytes past a 16-byte boundary (the API's minimum): the
+    activation loads must not assume 16-byte alignment."""
+    N, K = 300, 1024
+    packed, scales, cb = make_case(fmt, N, K, tag="xalign")
+    x_np = make_x(M, K, tag="xalign")
+    buf = torch.zeros(M * K + 8, dtype=torch.float16, device="cuda")
+    x = buf[2:2 + M * K].view(M, K)
+    assert x.data_ptr() % 16 == 4
+    x.copy_(cuda(x_np))
+    h = qgemv.QGemv(fmt, N, K, packed, scales, cb)
+    y = h.gemv(x)
+    torch.cuda.synchronize()
+    assert h.status() == qgemv.QGEMV_OK
+    y_ref, bound = oracle.gemv(fmt, N, K, packed, scales, cb, x_np)
+    assert_within(y.cpu().numpy(), y_ref, bound, f"{fmt} M={M} x offset 4 B")
+
+
+@pytest.mark.parametrize("fmt", FORMATS)
 def test_one_hot_rows_extract_columns_bit_exact(fmt):
     N, K = SMALL[fmt]
     packed, scales, cb = make_case(fmt, N, K, tag="onehot")

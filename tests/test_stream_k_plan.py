@@ -1,0 +1,107 @@
+"""Host-side checks of the stream-K work split (no GPU needed).
+
+The kernels split the stream of work units (prepared tiles, row tile after
+row tile) evenly over the CTAs.  A CTA writes a row tile's
+outputs itself when its run covers the whole row tile, else it stores its
+partial sums in one of its two slots: side 0 for the first row tile of its
+run (the one that began at or before its first unit), side 1 for the last.
+The host plan tells every contributor of a shared row tile where the other
+contributors' slots are and which rows it finishes.  These tests replay the
+kernels' owner/side rule against the plan that the library computes and
+check that every output row is produced exactly once from every unit."""
+import pytest
+
+from bit_weight_only_gb300 import build, qgemv
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return qgemv.load()
+
+
+def split(c, U, G):
+    return c * U // G
+
+
+def kernel_view(U, G, upr):
+    """What each CTA's kernel does: per row tile, the CTAs that store a
+    partial (with the slot side they use) and the CTA that writes y."""
+    writers, partials = {}, {}
+    for c in range(G):
+        u0, u1 = split(c, U, G), split(c + 1, U, G)
+        for rt in range(u0 // upr, (u1 - 1) // upr + 1):
+            owner = rt * upr >= u0 and (rt + 1) * upr <= u1
+            if owner:
+                writers.setdefault(rt, []).append(c)
+            else:
+                side = 0 if rt * upr <= u0 else 1
+                lo, hi = max(u0, rt * upr), min(u1, (rt + 1) * upr)
+                partials.setdefault(rt, []).append((c, side, lo, hi))
+    return writers, partials
+
+
+CASES = [
+    # (units = tiles, grid, tiles per row tile, rows)
+    (32 * 8, 152, 8, 128),          # 4096 x 4096 CBK4: 32 row tiles x 8 k tiles
+    (258 * 8, 152, 8, 128),         # 33024-row stack, 8 k tiles per row tile
+    (86 * 22, 152, 22, 128),        # 11008-wide down projection (Q4_0 / CBK4)
+    (7, 7, 1, 128),                 # one k tile per row tile, grid = tiles
+    (3 * 50, 152, 50, 128),         # long row tiles: several CTAs share each
+    (1000, 999, 10, 128),           # almost one tile per CTA
+    (35 * 4, 140, 4, 2048),         # AQLM units of 2048 rows
+    (17, 17, 17, 128),              # one row tile, one tile per CTA
+]
+
+
+@pytest.mark.parametrize("U, G, upr, rows", CASES)
+def test_plan_matches_the_kernels_split(lib, U, G, upr, rows):
+    G = min(G, U)
+    plan = qgemv.qgemv_stream_k_plan(U, G, upr, rows)
+    writers, partials = kernel_view(U, G, upr)
+    n_rt = U // upr
+    for rt in range(n_rt):
+        w, parts = writers.get(rt, []), partials.get(rt, [])
+        # every unit of the row tile is covered once, by one writer or by partials
+        if w:
+            assert len(w) == 1 and not parts
+            continue
+        covered = sorted((lo, hi) for _, _, lo, hi in parts)
+        assert covered[0][0] == rt * upr and covered[-1][1] == (rt + 1) * upr
+        assert all(a[1] == b[0] for a, b in zip(covered, covered[1:]))
+        ctas = [c for c, _, _, _ in parts]
+        assert ctas == list(range(ctas[0], ctas[0] + len(ctas)))
+        # each contributor's plan names this row tile once, with the same
+        # contributors, and the slot the first contributor really used
+        rows_done = []
+        for c, side, _, _ in parts:
+            segs = [s for s in range(2) if plan[c]["rt"][s] == rt]
+            assert len(segs) == 1, (rt, c, plan[c])
+            s = segs[0]
+            assert plan[c]["cf"][s] == ctas[0]
+            assert plan[c]["S"][s] == len(ctas)
+            first_side = [sd for cc, sd, _, _ in parts if cc == ctas[0]][0]
+            assert plan[c]["side1"][s] == first_side
+            # the later contributors used side 0 (the row tile began before them)
+            if c != ctas[0]:
+                assert side == 0
+            rows_done.extend(range(plan[c]["r0"][s], plan[c]["r0"][s] + plan[c]["nr"][s]))
+        assert sorted(rows_done) == list(range(rows))
+    # a CTA's plan names no row tile that it does not share
+    for c in range(G):
+        for s in range(2):
+            rt = plan[c]["rt"][s]
+            if rt >= 0:
+                assert any(cc == c for cc, _, _, _ in partials.get(rt, []))
+
+
+def test_plan_is_balanced_to_one_unit(lib):
+    U, G = 258 * 8, 152
+    sizes = [split(c + 1, U, G) - split(c, U, G) for c in range(G)]
+    assert max(sizes) - min(sizes) <= 1
+
+
+@pytest.mark.parametrize("args", [(0, 1, 1, 128), (10, 11, 10, 128), (12, 2, 5, 128), (10, 2, 5, 0)])
+def test_plan_rejects_bad_sizes(lib, args):
+    with pytest.raises(qgemv.QgemvError):
+        qgemv.qgemv_stream_k_plan(*args)
