@@ -334,8 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1) aqlm_gemv_kernel(const GemvParams
 
   // ---- split row blocks: every contributor finishes a slice of rows ----
   wait_plan();
-  if (s_plan.seg_rt[0] >= 0) finish_rows<kRows, MB, kThreads>(p, kPartialStride, s_plan, 0, scales, 1.f, s_sub, tid);
-  if (s_plan.seg_rt[1] >= 0) finish_rows<kRows, MB, kThreads>(p, kPartialStride, s_plan, 1, scales, 1.f, s_sub, tid);
+  finish_all<kRows, MB, kThreads>(p, kPartialStride, s_plan, scales, 1.f, s_sub, tid);
 }
 
 // Canonical codes [N][K/8][2] -> prepared units (rotated per lane).

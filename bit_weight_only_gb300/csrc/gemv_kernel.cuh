@@ -273,6 +273,24 @@ __device__ __forceinline__ void finish_segment(const GemvParams& p, int64_t stri
     finish_rows<ROWS, M, NT>(p, stride, pl, sg, row_scales, out_scale, s_sub, tid, mrows);
 }
 
+// Finish the CTA's shared row tiles (the two plan segments).  When it has
+// two and neither needs the split-contributor sums (S <= 16), half the
+// threads take each, so that the two waits for other CTAs' partials overlap
+// instead of adding up.
+template <int ROWS, int M, int NT>
+__device__ __forceinline__ void finish_all(const GemvParams& p, int64_t stride, const CtaPlan& pl,
+                                           const __half* row_scales, float out_scale, float* s_sub, int tid,
+                                           int mrows = M) {
+  const bool s0 = pl.seg_rt[0] >= 0, s1 = pl.seg_rt[1] >= 0;
+  if (s0 && s1 && pl.seg_S[0] <= 16 && pl.seg_S[1] <= 16) {
+    const int sg = tid < NT / 2 ? 0 : 1;
+    finish_segment<ROWS, M, NT / 2>(p, stride, pl, sg, row_scales, out_scale, s_sub, tid - sg * (NT / 2), mrows);
+    return;
+  }
+  if (s0) finish_segment<ROWS, M, NT>(p, stride, pl, 0, row_scales, out_scale, s_sub, tid, mrows);
+  if (s1) finish_segment<ROWS, M, NT>(p, stride, pl, 1, row_scales, out_scale, s_sub, tid, mrows);
+}
+
 // CTA c's share of the stream: [c * T / G, (c + 1) * T / G), with 32-bit
 // divisions when the products fit (the common case).
 __device__ __forceinline__ int64_t stream_split(int64_t c, int64_t T, int64_t G) {
@@ -504,8 +522,7 @@ __global__ void __launch_bounds__(gemv_threads<M>(), 1) gemv_kernel(const GemvPa
   static_assert(kSlices * kTileRows * RS >= 2 * NT, "finishing scratch");
   float* s_sub = red;
   wait_plan();
-  if (s_plan.seg_rt[0] >= 0) finish_segment<kTileRows, M, NT>(p, kPartialStride, s_plan, 0, nullptr, F::kOutScale, s_sub, tid);
-  if (s_plan.seg_rt[1] >= 0) finish_segment<kTileRows, M, NT>(p, kPartialStride, s_plan, 1, nullptr, F::kOutScale, s_sub, tid);
+  finish_all<kTileRows, M, NT>(p, kPartialStride, s_plan, nullptr, F::kOutScale, s_sub, tid);
 }
 
 // ------------------------------------------------- activation staging ----

@@ -421,8 +421,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const GemvPara
   static_assert(mma_red_bytes<NB>() >= 2 * NT * 4, "finishing scratch");
   float* s_sub = reinterpret_cast<float*>(red);
   wait_plan();
-  if (s_plan.seg_rt[0] >= 0) finish_segment<kTileRows, 8 * NB, NT>(p, kPartialStride, s_plan, 0, nullptr, 1.0f, s_sub, tid, M);
-  if (s_plan.seg_rt[1] >= 0) finish_segment<kTileRows, 8 * NB, NT>(p, kPartialStride, s_plan, 1, nullptr, 1.0f, s_sub, tid, M);
+  finish_all<kTileRows, 8 * NB, NT>(p, kPartialStride, s_plan, nullptr, 1.0f, s_sub, tid, M);
 }
 
 }  // namespace qgemv
