@@ -17,6 +17,7 @@ constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 // Error word bits written by kernels (read by qgemv_status).
 constexpr int kErrTimeoutFull = 1;
 constexpr int kErrTimeoutEmpty = 2;
+constexpr int kErrSmemLayout = 4;                      // shared memory too small for an aligned table
 constexpr int kErrTimeoutFixup = 8;                   // a split-K partial never arrived
 constexpr uint32_t kEmptySlot = 0xffffffffu;          // an unwritten partial slot
 

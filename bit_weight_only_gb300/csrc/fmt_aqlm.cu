@@ -68,7 +68,6 @@ constexpr uint32_t kSlab = 65536;           // one activation row's tables (2 bu
 constexpr int kMaxMB = 2;                   // activation rows per pass
 constexpr int64_t kPartialStride = int64_t(kRows) * kMaxMB;
 constexpr int kCodebookBytes = 2 * 256 * 8 * 2;
-constexpr int kErrSmemLayout = 4;
 constexpr int kRing = 2 * kRPL;            // rows of codes per lane in the load ring
 constexpr int kPreWait = 3;                // ring rows requested before the grid dependency wait
 

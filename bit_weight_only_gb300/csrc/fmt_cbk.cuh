@@ -108,10 +108,10 @@ struct FmtCBK4 {
   __device__ static void mma_load_row(const uint8_t* stage, int slice, int l, int j, int q, uint32_t (&w)[2]) {
     mma_row_words(stage, slice, l, j, q, w);
   }
-  __device__ static uint2 mma_frag(const uint32_t (&w)[2], int ks, const uint8_t* lut, uint32_t lane4) {
+  __device__ static uint2 mma_frag(const uint32_t (&w)[2], int ks, uint32_t lut_key) {
     const uint32_t wd = w[ks >> 1];
     const int b = 2 * (ks & 1);
-    return make_uint2(lds32(lut, lut_offset(wd, lane4, b)), lds32(lut, lut_offset(wd, lane4, b + 1)));
+    return make_uint2(lds32_at(lut_addr(wd, lut_key, b)), lds32_at(lut_addr(wd, lut_key, b + 1)));
   }
   __device__ static void mma_load_x(uint32_t (&xw)[kMmaXWords], const GemvParams& p, int M, int m, int64_t kb,
                                     int q, bool vec) {
@@ -269,10 +269,10 @@ struct FmtCBK8 {
   __device__ static void mma_load_row(const uint8_t* stage, int slice, int l, int j, int q, uint32_t (&w)[2]) {
     mma_row_words(stage, slice, l, j, q, w);
   }
-  __device__ static uint2 mma_frag(const uint32_t (&w)[2], int ks, const uint8_t* lut, uint32_t lane4) {
+  __device__ static uint2 mma_frag(const uint32_t (&w)[2], int ks, uint32_t lut_key) {
     const uint32_t wd = w[ks];
-    const uint32_t c0 = lds32(lut, lut_offset(wd, lane4, 0)), c1 = lds32(lut, lut_offset(wd, lane4, 1));
-    const uint32_t c2 = lds32(lut, lut_offset(wd, lane4, 2)), c3 = lds32(lut, lut_offset(wd, lane4, 3));
+    const uint32_t c0 = lds32_at(lut_addr(wd, lut_key, 0)), c1 = lds32_at(lut_addr(wd, lut_key, 1));
+    const uint32_t c2 = lds32_at(lut_addr(wd, lut_key, 2)), c3 = lds32_at(lut_addr(wd, lut_key, 3));
     return make_uint2(prmt(c0, c1, 0x5410u), prmt(c2, c3, 0x5410u));
   }
   __device__ static void mma_load_x(uint32_t (&xw)[kMmaXWords], const GemvParams& p, int M, int m, int64_t kb,

@@ -91,7 +91,7 @@ struct FmtQ4_0 {
     d[0] = f.x;
     d[1] = f.y;
   }
-  __device__ static uint2 mma_frag(const uint32_t (&w)[2], int ks, const uint8_t*, uint32_t) {
+  __device__ static uint2 mma_frag(const uint32_t (&w)[2], int ks, uint32_t) {
     const uint32_t wd = (ks & 1) ? (w[ks >> 1] >> 8) : w[ks >> 1];
     return make_uint2(hfma2_u32(field_pair(wd, 0x000F000Fu), 0x3C003C00u, 0xE408E408u),   // x1 - 1032
                       hfma2_u32(field_pair(wd, 0x00F000F0u), 0x2C002C00u, 0xD480D480u));  // /16 - 72
@@ -259,7 +259,7 @@ struct FmtPQ2 {
     const uint32_t src = f >= 4 ? (w >> 8) : w;
     return hfma2_u32(field_pair(src, 0x00030003u << (2 * fp)), kScale[fp], kOff[fp]);
   }
-  __device__ static uint2 mma_frag(const uint32_t (&w)[2], int ks, const uint8_t*, uint32_t) {
+  __device__ static uint2 mma_frag(const uint32_t (&w)[2], int ks, uint32_t) {
     const uint32_t wd = w[ks >> 2];
     const int sub = ks & 3;
     return make_uint2(pq2_pair(wd, 2 * sub), pq2_pair(wd, 2 * sub + 1));

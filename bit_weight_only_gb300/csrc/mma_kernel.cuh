@@ -46,9 +46,45 @@ constexpr int kMmaTiles = 4;                 // 16-row m-tiles per warp
 template <int NB>
 __host__ __device__ constexpr int mma_red_bytes() { return 4 * 2 * kMmaTiles * NB * 32 * 16; }
 
+// Shared memory.  Formats without a table: the stages, the reduction
+// buffer and the mbarriers, in that order.  Table formats (CBK4, CBK8): the
+// 64 KB table starts on a 64 KB boundary of the shared window, so that one
+// PRMT of the index byte with (table >> 16, lane * 4) is the whole address
+// of an entry (no add per lookup).  Before the table ("pre", at most 64 KB
+// less the window offset of the dynamic area): stage 0, the mbarriers and,
+// for one activation block, the reduction buffer; after it the other stages
+// and, for two blocks, the reduction buffer.
+constexpr int kMmaTableAlign = 65536;
+constexpr int kMmaPreSlack = 4096;  // room left for the window offset of the dynamic area
+template <class F, int NB>
+__host__ __device__ constexpr int mma_bar_bytes() { return 2 * F::mma_stages(NB) * 8; }
+template <class F, int NB>
+__host__ __device__ constexpr int mma_pre_bytes() {
+  return F::kTileBytes + mma_bar_bytes<F, NB>() + (NB == 1 ? mma_red_bytes<NB>() : 0);
+}
+template <class F, int NB>
+__host__ __device__ constexpr int mma_post_bytes() {
+  return (F::mma_stages(NB) - 1) * F::kTileBytes + (NB == 1 ? 0 : mma_red_bytes<NB>());
+}
 template <class F, int NB>
 __host__ __device__ constexpr int mma_smem_bytes() {
-  return F::mma_stages(NB) * F::kTileBytes + mma_red_bytes<NB>() + F::kMmaSharedBytes + 2 * F::mma_stages(NB) * 8;
+  return F::kMmaSharedBytes == 0
+             ? F::mma_stages(NB) * F::kTileBytes + mma_red_bytes<NB>() + mma_bar_bytes<F, NB>()
+             : kMmaTableAlign + F::kMmaSharedBytes + mma_post_bytes<F, NB>();
+}
+
+// Address of table entry (byte bsel of w) for the lane: key = (table >> 16)
+// in byte 2, lane * 4 in byte 0; the index byte goes to byte 1.
+__device__ __forceinline__ uint32_t lut_addr(uint32_t w, uint32_t key, int bsel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(key), "r"(w), "r"(0x3200u | ((4u + bsel) << 4)));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t lds32_at(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
 }
 
 __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
@@ -153,11 +189,37 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const GemvPara
   constexpr int NT = kMmaThreads;
 
   extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t* ring = smem;
-  float4* red = reinterpret_cast<float4*>(smem + NS * TB);
-  uint8_t* fsh = smem + NS * TB + mma_red_bytes<NB>();
-  uint64_t* full = reinterpret_cast<uint64_t*>(fsh + F::kMmaSharedBytes);
+  // stage s at ring0 (s = 0) or ringN + (s - 1) TB
+  uint8_t* ring0 = smem;
+  uint8_t* ringN = smem + TB;
+  float4* red;
+  uint8_t* fsh;
+  uint64_t* full;
+  uint32_t lut_key = 0;  // table formats: (table >> 16) << 16 | lane * 4
+  if constexpr (F::kMmaSharedBytes == 0) {
+    red = reinterpret_cast<float4*>(smem + NS * TB);
+    fsh = smem;  // unused
+    full = reinterpret_cast<uint64_t*>(smem + NS * TB + mma_red_bytes<NB>());
+  } else {
+    static_assert(F::kMmaSharedBytes == kMmaTableAlign, "one 64 KB table");
+    static_assert(mma_pre_bytes<F, NB>() + kMmaPreSlack <= kMmaTableAlign, "pre-table layout");
+    const uint32_t base = smem_u32(smem);
+    uint32_t dyn;
+    asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
+    const uint32_t R0 = (base + (kMmaTableAlign - 1)) & ~uint32_t(kMmaTableAlign - 1);
+    if (R0 - base < uint32_t(mma_pre_bytes<F, NB>()) ||
+        R0 + kMmaTableAlign + mma_post_bytes<F, NB>() > base + dyn) {
+      if (threadIdx.x == 0) atomicOr(p.err, kErrSmemLayout);
+      return;
+    }
+    fsh = smem + (R0 - base);
+    ringN = fsh + kMmaTableAlign;
+    full = reinterpret_cast<uint64_t*>(smem + TB);
+    red = reinterpret_cast<float4*>(NB == 1 ? smem + TB + mma_bar_bytes<F, NB>() : ringN + (NS - 1) * TB);
+    lut_key = (R0 & 0xFFFF0000u) | ((threadIdx.x & 31u) << 2);
+  }
   uint64_t* empty = full + NS;
+  auto stage_ptr = [&](int64_t s) { return s == 0 ? ring0 : ringN + (s - 1) * TB; };
   __shared__ volatile int s_abort;
   __shared__ int s_seg[2];
   __shared__ __align__(16) CtaPlan s_plan;
@@ -188,7 +250,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const GemvPara
     pol = l2_policy_evict_first();
     for (; n_issued < NS - 1 && n_issued < ntiles; ++n_issued) {
       mbar_arrive_expect_tx(&full[n_issued], TB);
-      bulk_g2s(ring + n_issued * TB, p.tiles + (t0 + n_issued) * TB, TB, &full[n_issued], pol);
+      bulk_g2s(stage_ptr(n_issued), p.tiles + (t0 + n_issued) * TB, TB, &full[n_issued], pol);
     }
   }
   fetch_plan(&s_plan, p.plan, c, tid);
@@ -209,7 +271,6 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const GemvPara
 
   int64_t rt = rt_first;
   int kt = static_cast<int>(t0 - rt * p.nKT);
-  const uint32_t lane4 = static_cast<uint32_t>(lane) << 2;
   const bool xvec = (reinterpret_cast<uintptr_t>(p.x) & 15) == 0 && (p.K & 7) == 0;
   // activation fragments of the thread's B rows m = gi + 8 nb (a tile ahead
   // when PF, else loaded at the top of each tile)
@@ -257,7 +318,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const GemvPara
         abort = true;
       } else {
         mbar_arrive_expect_tx(&full[su], TB);
-        bulk_g2s(ring + su * TB, p.tiles + (t0 + n_issued) * TB, TB, &full[su], pol);
+        bulk_g2s(stage_ptr(su), p.tiles + (t0 + n_issued) * TB, TB, &full[su], pol);
         ++n_issued;
         if (++su == NS) { su = 0; phu ^= 1; }
       }
@@ -275,7 +336,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const GemvPara
       if (!abort && lane == 0) atomicOr(p.err, kErrTimeoutFull);
       s_abort = 1;
     } else {
-      const uint8_t* stage = ring + s * TB;
+      const uint8_t* stage = stage_ptr(s);
       // codes (and scales) of the thread's eight rows, then release the stage
       uint32_t w[kMmaTiles][2][2];
       float d[kMmaTiles][2][NBLK];
@@ -313,8 +374,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const GemvPara
 #pragma unroll
             for (int mi = 0; mi < MG; ++mi) {
               const int mt = mg + mi;
-              const uint2 r0 = F::mma_frag(w[mt][0], ks, fsh, lane4);  // row gi: (k lo pair, k hi pair)
-              const uint2 r1 = F::mma_frag(w[mt][1], ks, fsh, lane4);  // row gi + 8
+              const uint2 r0 = F::mma_frag(w[mt][0], ks, lut_key);  // row gi: (k lo pair, k hi pair)
+              const uint2 r1 = F::mma_frag(w[mt][1], ks, lut_key);  // row gi + 8
 #pragma unroll
               for (int nb = 0; nb < NB; ++nb) {
                 const uint2 b = F::mma_bfrag(xw[nb], ks);
