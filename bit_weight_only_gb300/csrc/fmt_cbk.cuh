@@ -113,10 +113,10 @@ struct FmtCBK4 {
     const int b = 2 * (ks & 1);
     return make_uint2(lds32_at(lut_addr(wd, lut_key, b)), lds32_at(lut_addr(wd, lut_key, b + 1)));
   }
-  __device__ static void mma_load_x(uint32_t (&xw)[kMmaXWords], const GemvParams& p, int M, int m, int64_t kb,
-                                    int q, bool vec) {
-    ld_x8(xw, p, M, m, kb + 8 * q, vec);
-    ld_x8(xw + 4, p, M, m, kb + 32 + 8 * q, vec);
+  __device__ static void mma_load_x(uint32_t (&xw)[kMmaXWords], const unsigned short* row, int64_t K,
+                                    int64_t kb, int q, bool vec) {
+    ld_x8(xw, row, K, kb + 8 * q, vec);
+    ld_x8(xw + 4, row, K, kb + 32 + 8 * q, vec);
   }
   __device__ static uint2 mma_bfrag(const uint32_t (&xw)[kMmaXWords], int ks) {
     return make_uint2(xw[2 * ks], xw[2 * ks + 1]);
@@ -275,10 +275,10 @@ struct FmtCBK8 {
     const uint32_t c2 = lds32_at(lut_addr(wd, lut_key, 2)), c3 = lds32_at(lut_addr(wd, lut_key, 3));
     return make_uint2(prmt(c0, c1, 0x5410u), prmt(c2, c3, 0x5410u));
   }
-  __device__ static void mma_load_x(uint32_t (&xw)[kMmaXWords], const GemvParams& p, int M, int m, int64_t kb,
-                                    int q, bool vec) {
-    ld_x4(xw, p, M, m, kb + 4 * q, vec);
-    ld_x4(xw + 2, p, M, m, kb + 16 + 4 * q, vec);
+  __device__ static void mma_load_x(uint32_t (&xw)[kMmaXWords], const unsigned short* row, int64_t K,
+                                    int64_t kb, int q, bool vec) {
+    ld_x4(xw, row, K, kb + 4 * q, vec);
+    ld_x4(xw + 2, row, K, kb + 16 + 4 * q, vec);
   }
   __device__ static uint2 mma_bfrag(const uint32_t (&xw)[kMmaXWords], int ks) {
     return make_uint2(xw[2 * ks], xw[2 * ks + 1]);

@@ -96,10 +96,10 @@ struct FmtQ4_0 {
     return make_uint2(hfma2_u32(field_pair(wd, 0x000F000Fu), 0x3C003C00u, 0xE408E408u),   // x1 - 1032
                       hfma2_u32(field_pair(wd, 0x00F000F0u), 0x2C002C00u, 0xD480D480u));  // /16 - 72
   }
-  __device__ static void mma_load_x(uint32_t (&xw)[kMmaXWords], const GemvParams& p, int M, int m, int64_t kb,
-                                    int q, bool vec) {
-    ld_x8(xw, p, M, m, kb + 8 * q, vec);
-    ld_x8(xw + 4, p, M, m, kb + 32 + 8 * q, vec);
+  __device__ static void mma_load_x(uint32_t (&xw)[kMmaXWords], const unsigned short* row, int64_t K,
+                                    int64_t kb, int q, bool vec) {
+    ld_x8(xw, row, K, kb + 8 * q, vec);
+    ld_x8(xw + 4, row, K, kb + 32 + 8 * q, vec);
   }
   __device__ static uint2 mma_bfrag(const uint32_t (&xw)[kMmaXWords], int ks) {
     const uint32_t* X = xw + 4 * (ks >> 1);  // (x0,x1) (x2,x3) (x4,x5) (x6,x7) of the block's 8 k
@@ -264,10 +264,10 @@ struct FmtPQ2 {
     const int sub = ks & 3;
     return make_uint2(pq2_pair(wd, 2 * sub), pq2_pair(wd, 2 * sub + 1));
   }
-  __device__ static void mma_load_x(uint32_t (&xw)[kMmaXWords], const GemvParams& p, int M, int m, int64_t kb,
-                                    int q, bool vec) {
+  __device__ static void mma_load_x(uint32_t (&xw)[kMmaXWords], const unsigned short* row, int64_t K,
+                                    int64_t kb, int q, bool vec) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) ld_x8(xw + 4 * i, p, M, m, kb + 64 * (i >> 1) + 16 * q + 8 * (i & 1), vec);
+    for (int i = 0; i < 4; ++i) ld_x8(xw + 4 * i, row, K, kb + 64 * (i >> 1) + 16 * q + 8 * (i & 1), vec);
   }
   __device__ static uint2 mma_bfrag(const uint32_t (&xw)[kMmaXWords], int ks) {
     const uint32_t* X = xw + 8 * (ks >> 2);  // (x0,x1) .. (x14,x15) of the word's 16 k

@@ -96,6 +96,16 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// d = A * B (zero accumulator in)
+__device__ __forceinline__ void mma_16816_c0(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                             uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%10,%10,%10,%10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.0f));
+}
+
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t r;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
@@ -127,14 +137,14 @@ __device__ __forceinline__ void mma_row_words(const uint8_t* stage, int slice, i
   w[1] = *reinterpret_cast<const uint32_t*>(stage + ((j * 2 + 1) * kLaneSlots + t) * 16 + 4 * q);
 }
 
-// x[m][k0 .. k0+3] as two fp16 pairs (k0 a multiple of 4); zero for m >= M
-// and for k >= K.  `vec`: x is 16-byte aligned and K % 8 == 0.
-__device__ __forceinline__ void ld_x4(uint32_t* out, const GemvParams& p, int M, int m, int64_t k0, bool vec) {
-  if (m >= M || k0 >= p.K) {
+// Activation loads: `row` is x[m] (null for m >= M: zeros), K its length.
+// x[m][k0 .. k0+3] as two fp16 pairs (k0 a multiple of 4); zero for k >= K.
+// `vec`: x is 16-byte aligned and K % 8 == 0.
+__device__ __forceinline__ void ld_x4(uint32_t* out, const unsigned short* row, int64_t K, int64_t k0, bool vec) {
+  if (row == nullptr || k0 >= K) {
     out[0] = out[1] = 0u;
     return;
   }
-  const unsigned short* row = reinterpret_cast<const unsigned short*>(p.x) + m * p.K;
   if (vec) {
     const uint2 v = __ldg(reinterpret_cast<const uint2*>(row + k0));
     out[0] = v.x; out[1] = v.y;
@@ -143,21 +153,19 @@ __device__ __forceinline__ void ld_x4(uint32_t* out, const GemvParams& p, int M,
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
     const int64_t k = k0 + 2 * i;
-    const uint32_t lo = k < p.K ? __ldg(row + k) : 0u;
-    const uint32_t hi = k + 1 < p.K ? __ldg(row + k + 1) : 0u;
+    const uint32_t lo = k < K ? __ldg(row + k) : 0u;
+    const uint32_t hi = k + 1 < K ? __ldg(row + k + 1) : 0u;
     out[i] = lo | (hi << 16);
   }
 }
 
-// x[m][k0 .. k0+7] as four fp16 pairs; zero for m >= M and for k >= K.  k0
-// is a multiple of 8; `vec`: x is 16-byte aligned and K % 8 == 0, so the
-// eight values are one aligned 16-byte load.
-__device__ __forceinline__ void ld_x8(uint32_t* out, const GemvParams& p, int M, int m, int64_t k0, bool vec) {
-  if (m >= M || k0 >= p.K) {
+// x[m][k0 .. k0+7] as four fp16 pairs; zero for k >= K.  k0 is a multiple of
+// 8; with `vec` the eight values are one aligned 16-byte load.
+__device__ __forceinline__ void ld_x8(uint32_t* out, const unsigned short* row, int64_t K, int64_t k0, bool vec) {
+  if (row == nullptr || k0 >= K) {
     out[0] = out[1] = out[2] = out[3] = 0u;
     return;
   }
-  const unsigned short* row = reinterpret_cast<const unsigned short*>(p.x) + m * p.K;
   if (vec) {
     const uint4 v = __ldg(reinterpret_cast<const uint4*>(row + k0));
     out[0] = v.x; out[1] = v.y; out[2] = v.z; out[3] = v.w;
@@ -166,8 +174,8 @@ __device__ __forceinline__ void ld_x8(uint32_t* out, const GemvParams& p, int M,
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int64_t k = k0 + 2 * i;
-    const uint32_t lo = k < p.K ? __ldg(row + k) : 0u;
-    const uint32_t hi = k + 1 < p.K ? __ldg(row + k + 1) : 0u;
+    const uint32_t lo = k < K ? __ldg(row + k) : 0u;
+    const uint32_t hi = k + 1 < K ? __ldg(row + k + 1) : 0u;
     out[i] = lo | (hi << 16);
   }
 }
@@ -275,10 +283,14 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const GemvPara
   // activation fragments of the thread's B rows m = gi + 8 nb (a tile ahead
   // when PF, else loaded at the top of each tile)
   uint32_t xw[NB][XW];
+  const unsigned short* xrow[NB];
+#pragma unroll
+  for (int nb = 0; nb < NB; ++nb)
+    xrow[nb] = gi + 8 * nb < M ? reinterpret_cast<const unsigned short*>(p.x) + (gi + 8 * nb) * p.K : nullptr;
   auto load_x = [&](uint32_t (&dst)[NB][XW], int ktile) {
     const int64_t kb = static_cast<int64_t>(ktile) * F::kKT + slice * F::kKW;
 #pragma unroll
-    for (int nb = 0; nb < NB; ++nb) F::mma_load_x(dst[nb], p, M, gi + 8 * nb, kb, q, xvec);
+    for (int nb = 0; nb < NB; ++nb) F::mma_load_x(dst[nb], xrow[nb], p.K, kb, q, xvec);
   };
   if constexpr (PF) {
     if (ntiles > 0) load_x(xw, kt);
@@ -362,13 +374,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const GemvPara
       for (int mg = 0; mg < kMmaTiles; mg += MG) {
 #pragma unroll
         for (int blk = 0; blk < NBLK; ++blk) {
-          float tmp[MG][NB][4];
-#pragma unroll
-          for (int mi = 0; mi < MG; ++mi)
-#pragma unroll
-            for (int nb = 0; nb < NB; ++nb)
-#pragma unroll
-              for (int e = 0; e < 4; ++e) tmp[mi][nb][e] = 0.f;
+          float tmp[MG][NB][4];  // block sums (block formats); the first MMA writes them
 #pragma unroll
           for (int ks = blk * (BS > 0 ? BS : KS); ks < (blk + 1) * (BS > 0 ? BS : KS); ++ks) {
 #pragma unroll
@@ -379,9 +385,12 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const GemvPara
 #pragma unroll
               for (int nb = 0; nb < NB; ++nb) {
                 const uint2 b = F::mma_bfrag(xw[nb], ks);
-                if constexpr (BS > 0)
-                  mma_16816(tmp[mi][nb], r0.x, r1.x, r0.y, r1.y, b.x, b.y);
-                else
+                if constexpr (BS > 0) {
+                  if (ks == blk * BS)
+                    mma_16816_c0(tmp[mi][nb], r0.x, r1.x, r0.y, r1.y, b.x, b.y);
+                  else
+                    mma_16816(tmp[mi][nb], r0.x, r1.x, r0.y, r1.y, b.x, b.y);
+                } else
                   mma_16816(acc[mt][nb], r0.x, r1.x, r0.y, r1.y, b.x, b.y);
               }
             }
