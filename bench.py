@@ -362,7 +362,7 @@ def run_ours(args, rank, world, device):
     if os.path.exists(prof):
         try:
             pj = json.load(open(prof))
-            entry = pj.get(args.workload)
+            entry = pj.get(args.workload if M == 1 else f"{args.workload}/M={M}")
             if entry and entry.get("kernel_source_hash") == kernel_source_hash():
                 traffic = entry.get("dram_bytes_per_launch")
         except Exception:
