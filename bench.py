@@ -8,9 +8,11 @@ One JSON line on rank 0 (stdout); everything else goes to stderr.
 Default workload ("cbk4_7b_stack"): the projection stack of a 32-layer 7B
 decoder -- per layer q/k/v/o 4096x4096, gate/up 11008x4096, down 4096x11008
 (224 projections, 4-bit scalar codebook, 16 fp16 centroids each) plus a
-32000x4096 LM head with an 8-bit codebook (256 centroids) -- at M = 1.  One
-step is one token: all 225 GEMVs, replayed as CUDA graphs.  The stack is
-3.37 GB of packed weights, far larger than L2, so no flush is needed.
+32000x4096 LM head with an 8-bit codebook (256 centroids) -- at M = 1.  The
+projections that share their input run as one stacked handle each (q|k|v and
+gate|up), so one step is one token of 129 GEMV calls, replayed as CUDA
+graphs.  The stack is 3.37 GB of packed weights, far larger than L2, so no
+flush is needed.
 Inputs are synthetic and seeded (see bit_weight_only_gb300/inputs.py).
 
 The metric is the achieved weight-stream bandwidth: algorithmic bytes
