@@ -142,6 +142,7 @@ __device__ __forceinline__ void lookup_row(const uint4 (&cr)[2], const uint32_t 
 
 template <int MB>
 __global__ void __launch_bounds__(kThreads, 1) aqlm_gemv_kernel(const GemvParams p) {
+  if (static_cast<int>(blockIdx.x) == p.skip_cta) return;  // test hook (QGEMV_FAULT_SKIP_CTA)
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ float s_sub[2 * kThreads];
   __shared__ __align__(16) CtaPlan s_plan;
@@ -454,13 +455,16 @@ cudaError_t launch_pass(const GemvParams& p, int grid, cudaStream_t s) {
 }
 
 // M activation rows: passes of two rows, the last one of one row if M is odd.
-cudaError_t launch(int M, const GemvParams& p, int grid, cudaStream_t s) {
+// Passes of two activation rows, and one for an odd last row.  The two pass
+// kinds round differently, so in batch-invariant mode every row gets a
+// one-row pass of its own.
+cudaError_t launch(int M, const GemvParams& p, int grid, cudaStream_t s, bool batch_invariant) {
   cudaError_t e = cudaSuccess;
   for (int m0 = 0; m0 < M && e == cudaSuccess;) {
     GemvParams q = p;
     q.x = p.x + int64_t(m0) * p.K;
     q.y = p.y + int64_t(m0) * p.N;
-    if (M - m0 >= 2) {
+    if (M - m0 >= 2 && !batch_invariant) {
       e = launch_pass<2>(q, grid, s);
       m0 += 2;
     } else {

@@ -30,7 +30,9 @@ struct FormatOps {
   int64_t aux_bytes;
   int (*smem_bytes)(int M);
   cudaError_t (*setup)();  // one-time kernel attributes
-  cudaError_t (*launch)(int M, const GemvParams& p, int grid, cudaStream_t s);
+  // batch_invariant: every row's result must not depend on M (see
+  // qgemv_set_batch_invariant); the kernels are chosen accordingly.
+  cudaError_t (*launch)(int M, const GemvParams& p, int grid, cudaStream_t s, bool batch_invariant);
   cudaError_t (*prepare)(const PrepareArgs& a, cudaStream_t s);
   // w_out[n*K + k] = exact decoded weight, read back from the prepared tiles
   cudaError_t (*dequant)(const uint8_t* tiles, const void* aux, const int32_t* seg_of_rt, int64_t N,

@@ -75,6 +75,7 @@ struct GemvParams {
   int64_t N, K;
   int64_t T;             // tiles in the stream = nRT * nKT
   int nKT;               // k tiles per row tile
+  int skip_cta;          // test hook: this CTA does nothing (-1: none)
 };
 
 // Warps per slice for a given M: two while the whole accumulator set of a
@@ -358,6 +359,7 @@ __global__ void __launch_bounds__(gemv_threads<M>(), 1) gemv_kernel(const GemvPa
   __shared__ int s_seg[2];
   __shared__ __align__(16) CtaPlan s_plan;
 
+  if (static_cast<int>(blockIdx.x) == p.skip_cta) return;  // test hook (QGEMV_FAULT_SKIP_CTA)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int slice = warp % kSlices;

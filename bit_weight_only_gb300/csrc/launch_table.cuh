@@ -11,7 +11,11 @@ namespace qgemv {
 
 // M = 1: the CUDA-core kernel (gemv_kernel.cuh).  M = 2..16: the tensor-core
 // kernel with register-level decode (mma_kernel.cuh), one activation block
-// of 8 rows up to M = 8, two above.
+// of 8 rows up to M = 8, two above.  The tensor-core kernel computes every
+// activation row on its own (a column of the MMA's B operand, the same
+// instruction sequence, reduction tree and fix-up order for any M), so in
+// batch-invariant mode M = 1 runs there too and a row's bits never depend on
+// how many rows share the call.
 template <class F>
 struct LaunchTable {
   // Launched with programmatic stream serialization: the kernel may start
@@ -64,9 +68,9 @@ struct LaunchTable {
     return e;
   }
 
-  static cudaError_t launch(int M, const GemvParams& p, int grid, cudaStream_t s) {
-    if (M == 1) return launch_m1(p, grid, s);
-    if (M >= 2 && M <= 8) return launch_mma<1>(p, M, grid, s);
+  static cudaError_t launch(int M, const GemvParams& p, int grid, cudaStream_t s, bool batch_invariant) {
+    if (M == 1 && !batch_invariant) return launch_m1(p, grid, s);
+    if (M >= 1 && M <= 8) return launch_mma<1>(p, M, grid, s);
     if (M > 8 && M <= kMaxM) return launch_mma<2>(p, M, grid, s);
     return cudaErrorInvalidValue;
   }

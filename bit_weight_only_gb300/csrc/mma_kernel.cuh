@@ -196,6 +196,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const GemvPara
   constexpr bool PF = F::mma_prefetch_x(NB);  // activations a tile ahead (registers permitting)
   constexpr int NT = kMmaThreads;
 
+  if (static_cast<int>(blockIdx.x) == p.skip_cta) return;  // test hook (QGEMV_FAULT_SKIP_CTA)
   extern __shared__ __align__(128) uint8_t smem[];
   // stage s at ring0 (s = 0) or ringN + (s - 1) TB
   uint8_t* ring0 = smem;

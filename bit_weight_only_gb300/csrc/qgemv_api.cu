@@ -6,6 +6,7 @@
 // call aborts.
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <new>
@@ -86,11 +87,34 @@ bool is_device_pointer(const void* p) {
   return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
 }
 
+// Fault hooks for tests, read when a handle is created (host side only;
+// nothing on the device faults or hangs):
+//   QGEMV_FAULT_ALLOC=n     the n-th device allocation of the create call
+//                           fails as if the device were out of memory;
+//   QGEMV_FAULT_SKIP_CTA=c  the handle's runs launch CTA c as a no-op, so
+//                           the CTAs that share a row tile with it never get
+//                           its partial sums: their bounded fix-up waits run
+//                           out and qgemv_status reports QGEMV_ERR_TIMEOUT.
+int env_int(const char* name, int dflt) {
+  const char* v = std::getenv(name);
+  return v && *v ? std::atoi(v) : dflt;
+}
+thread_local int g_alloc_count = 0;  // device allocations of the current create call
+thread_local int g_alloc_fail = 0;   // QGEMV_FAULT_ALLOC of the current create call
+
+cudaError_t dev_alloc(void** dst, size_t bytes) {
+  if (++g_alloc_count == g_alloc_fail) {
+    *dst = nullptr;
+    return cudaErrorMemoryAllocation;
+  }
+  return cudaMalloc(dst, bytes);
+}
+
 // Copy `bytes` from a host or device pointer into a fresh device buffer.
 cudaError_t to_device(const void* src, size_t bytes, void** dst) {
   *dst = nullptr;
   if (bytes == 0) return cudaSuccess;
-  cudaError_t e = cudaMalloc(dst, bytes);
+  cudaError_t e = dev_alloc(dst, bytes);
   if (e != cudaSuccess) return e;
   e = cudaMemcpy(*dst, src, bytes, is_device_pointer(src) ? cudaMemcpyDeviceToDevice
                                                           : cudaMemcpyHostToDevice);
@@ -167,6 +191,8 @@ struct qgemv_ctx {
   qgemv::CtaPlan* plan;
   int32_t* seg_of_rt;  // inside aux (table formats), else nullptr
   int* err;
+  int batch_invariant;  // qgemv_set_batch_invariant
+  int skip_cta;         // QGEMV_FAULT_SKIP_CTA test hook, -1 normally
 };
 
 extern "C" {
@@ -242,6 +268,9 @@ static qgemv_handle create_impl(int format, int64_t N, int64_t K, const void* pa
     return nullptr;
   }
   h->magic = kMagic;
+  h->skip_cta = env_int("QGEMV_FAULT_SKIP_CTA", -1);
+  g_alloc_count = 0;
+  g_alloc_fail = env_int("QGEMV_FAULT_ALLOC", 0);
   h->format = format;
   h->N = N;
   h->K = K;
@@ -263,8 +292,14 @@ static qgemv_handle create_impl(int format, int64_t N, int64_t K, const void* pa
 
   void *d_packed = nullptr, *d_scales = nullptr, *d_cb = nullptr;
   auto cleanup = [&](int code, const char* what, cudaError_t ce) -> qgemv_handle {
-    if (ce != cudaSuccess) cuda_error(ce, what);
-    else set_error(code, "%s", what);
+    if (ce == cudaErrorMemoryAllocation) {
+      cudaGetLastError();  // a real allocation failure is sticky in the last-error state
+      set_error(QGEMV_ERR_NOMEM, "%s: out of device memory", what);
+    } else if (ce != cudaSuccess) {
+      cuda_error(ce, what);
+    } else {
+      set_error(code, "%s", what);
+    }
     cudaFree(d_packed);
     cudaFree(d_scales);
     cudaFree(d_cb);
@@ -283,18 +318,19 @@ static qgemv_handle create_impl(int format, int64_t N, int64_t K, const void* pa
   if (e == cudaSuccess) e = to_device(codebooks, 2 * codebook_count(format) * nseg, &d_cb);
   if (e != cudaSuccess) return cleanup(QGEMV_ERR_CUDA, "copying the canonical inputs", e);
 
-  e = cudaMalloc(&h->tiles, static_cast<size_t>(h->T) * ops->tile_bytes);
+  e = dev_alloc(reinterpret_cast<void**>(&h->tiles), static_cast<size_t>(h->T) * ops->tile_bytes);
   // table formats: one codebook, or (stacked) one copy per row tile followed
   // by the row tiles' segments
   const bool stacked = ops->cb_entries > 0 && nseg > 1;
   const int64_t table_bytes = int64_t(2) * ops->cb_entries * (stacked ? h->nRT : 1);
   const int64_t aux_bytes = ops->cb_entries > 0 ? table_bytes + (stacked ? 4 * h->nRT : 0)
                                                 : ops->aux_bytes + ops->aux_per_row * N;
-  if (e == cudaSuccess && aux_bytes > 0) e = cudaMalloc(&h->aux, static_cast<size_t>(aux_bytes));
+  if (e == cudaSuccess && aux_bytes > 0) e = dev_alloc(&h->aux, static_cast<size_t>(aux_bytes));
   if (e == cudaSuccess)
-    e = cudaMalloc(&h->partials, sizeof(float) * 2 * ops->partial_stride * static_cast<size_t>(h->grid));
-  if (e == cudaSuccess) e = cudaMalloc(&h->plan, sizeof(qgemv::CtaPlan) * h->grid);
-  if (e == cudaSuccess) e = cudaMalloc(&h->err, sizeof(int));
+    e = dev_alloc(reinterpret_cast<void**>(&h->partials),
+                  sizeof(float) * 2 * ops->partial_stride * static_cast<size_t>(h->grid));
+  if (e == cudaSuccess) e = dev_alloc(reinterpret_cast<void**>(&h->plan), sizeof(qgemv::CtaPlan) * h->grid);
+  if (e == cudaSuccess) e = dev_alloc(reinterpret_cast<void**>(&h->err), sizeof(int));
   if (e == cudaSuccess && stacked) {
     h->seg_of_rt = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(h->aux) + table_bytes);
     e = cudaMemcpy(h->seg_of_rt, seg_of_rt.data(), 4 * seg_of_rt.size(), cudaMemcpyHostToDevice);
@@ -388,8 +424,15 @@ int qgemv_run(qgemv_handle h, const void* x, int M, float* y, void* stream) {
   p.K = h->K;
   p.T = h->T;
   p.nKT = h->nKT;
-  cudaError_t e = h->ops->launch(M, p, h->grid, static_cast<cudaStream_t>(stream));
+  p.skip_cta = h->skip_cta;
+  cudaError_t e = h->ops->launch(M, p, h->grid, static_cast<cudaStream_t>(stream), h->batch_invariant != 0);
   if (e != cudaSuccess) return cuda_error(e, "launching the GEMV kernel");
+  return ok();
+}
+
+int qgemv_set_batch_invariant(qgemv_handle h, int on) {
+  if (!valid(h)) return set_error(QGEMV_ERR_ARG, "invalid handle");
+  h->batch_invariant = on ? 1 : 0;
   return ok();
 }
 

@@ -31,6 +31,7 @@ _SIGNATURES = {
                                                ctypes.c_void_p]),
     "qgemv_run": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
                                  ctypes.c_void_p, ctypes.c_void_p]),
+    "qgemv_set_batch_invariant": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int]),
     "qgemv_dequant": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "qgemv_quantize_q4_0": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
                                            ctypes.c_void_p, ctypes.c_void_p]),
@@ -132,6 +133,10 @@ def qgemv_run_q4_0_noalloc(packed: int, N: int, K: int, x: int, M: int, y: int,
     return _check(load().qgemv_run_q4_0_noalloc(packed, N, K, x, M, y, _stream_ptr(stream)))
 
 
+def qgemv_set_batch_invariant(h: int, on: bool) -> int:
+    return _check(load().qgemv_set_batch_invariant(h, 1 if on else 0))
+
+
 def qgemv_status(h: int) -> int:
     return _check(load().qgemv_status(h))
 
@@ -217,6 +222,9 @@ class QGemv:
 
     def status(self):
         return qgemv_status(self.handle)
+
+    def set_batch_invariant(self, on: bool = True):
+        qgemv_set_batch_invariant(self.handle, on)
 
     def close(self):
         if getattr(self, "handle", None):
