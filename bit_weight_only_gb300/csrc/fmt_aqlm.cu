@@ -458,10 +458,12 @@ cudaError_t launch_pass(const GemvParams& p, int grid, cudaStream_t s) {
 // Passes of two activation rows, and one for an odd last row.  The two pass
 // kinds round differently, so in batch-invariant mode every row gets a
 // one-row pass of its own.
-cudaError_t launch(int M, const GemvParams& p, int grid, cudaStream_t s, bool batch_invariant) {
+cudaError_t launch(int M, const GemvParams& p, const LaunchGeom& g, cudaStream_t s, bool batch_invariant) {
   cudaError_t e = cudaSuccess;
+  const int grid = g.grid;
   for (int m0 = 0; m0 < M && e == cudaSuccess;) {
     GemvParams q = p;
+    q.plan = g.plan;
     q.x = p.x + int64_t(m0) * p.K;
     q.y = p.y + int64_t(m0) * p.N;
     if (M - m0 >= 2 && !batch_invariant) {

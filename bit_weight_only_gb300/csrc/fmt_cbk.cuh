@@ -69,6 +69,7 @@ struct FmtCBK4 {
   static constexpr int kKW = 64;
   static constexpr int kKT = kKW * kSlices;                              // 512
   static constexpr int kTileBytes = kLaneSlots * kRowsPerLane * 32;      // 32768
+  static constexpr int kCtasPerSm = 1;  // the 64 KB table fits once per SM
   __host__ __device__ static constexpr int stages(int M) { return M <= 4 ? 4 : 2; }
   static constexpr int kSharedBytes = kLutBytes;
   static constexpr int kCbEntries = 16;
@@ -220,6 +221,7 @@ struct FmtCBK8 {
   static constexpr int kKW = 32;
   static constexpr int kKT = kKW * kSlices;                              // 256
   static constexpr int kTileBytes = kLaneSlots * kRowsPerLane * 32;      // 32768
+  static constexpr int kCtasPerSm = 1;  // the 64 KB table fits once per SM
   __host__ __device__ static constexpr int stages(int M) { return M <= 4 ? 4 : 2; }
   static constexpr int kCbEntries = 256;
   static constexpr int kSharedBytes = kLutBytes;

@@ -63,7 +63,9 @@ struct FmtQ4_0 {
   static constexpr int kKT = kKW * kSlices;                        // 512
   static constexpr int kCodeBytes = kCodeBytes32;
   static constexpr int kTileBytes = kCodeBytes + kLaneSlots * 16;  // 36864
-  __host__ __device__ static constexpr int stages(int M) { return M <= 4 ? 4 : 3; }
+  // M = 1 CUDA-core kernel: two CTAs of eight warps per SM, two stages each
+  static constexpr int kCtasPerSm = 2;
+  __host__ __device__ static constexpr int stages(int) { return 2; }
   static constexpr int kSharedBytes = 0;
   static constexpr float kOutScale = kFieldOutScale;
   static constexpr int kSumGroups = 2;  // one offset sum per Q4_0 block of the slice
@@ -224,7 +226,9 @@ struct FmtPQ2 {
   static constexpr int kKT = kKW * kSlices;                       // 1024
   static constexpr int kCodeBytes = kCodeBytes32;
   static constexpr int kTileBytes = kCodeBytes + kLaneSlots * 8;  // 34816
-  __host__ __device__ static constexpr int stages(int M) { return M <= 4 ? 4 : (M <= 8 ? 3 : 2); }
+  // M = 1 CUDA-core kernel: two CTAs of eight warps per SM, two stages each
+  static constexpr int kCtasPerSm = 2;
+  __host__ __device__ static constexpr int stages(int) { return 2; }
   static constexpr int kSharedBytes = 0;
   static constexpr float kOutScale = kFieldOutScale;
   static constexpr int kSumGroups = 1;

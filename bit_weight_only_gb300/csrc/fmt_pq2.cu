@@ -128,7 +128,8 @@ const FormatOps* ops_pq2() {
   static const FormatOps ops = {
       /*format=*/4, F::kKT, F::kTileBytes, /*aux_bytes=*/0,
       &LaunchTable<F>::smem_bytes, &LaunchTable<F>::setup, &LaunchTable<F>::launch,
-      &prepare, &dequant};
+      &prepare, &dequant, /*cb_entries=*/0, /*tile_rows=*/128, /*partial_stride=*/128 * 16,
+      /*aux_per_row=*/0, /*m1_ctas_per_sm=*/LaunchTable<F>::kM1CtasPerSm};
   return &ops;
 }
 

@@ -7,7 +7,8 @@
 
 namespace qgemv {
 
-struct GemvParams;  // gemv_kernel.cuh
+struct GemvParams;
+struct CtaPlan;  // gemv_kernel.cuh
 
 // Canonical inputs already on the device, plus the prepared-layout geometry.
 struct PrepareArgs {
@@ -23,6 +24,16 @@ struct PrepareArgs {
   const int32_t* seg_of_rt;  // device [nRT] codebook of each row tile, or nullptr
 };
 
+// Grids and stream-K plans of a handle: `grid`/`plan` for the tensor-core and
+// AQLM kernels (one CTA per SM), `grid_m1`/`plan_m1` for the M = 1 CUDA-core
+// kernel, which runs F::kCtasPerSm CTAs per SM (the same arrays when 1).
+struct LaunchGeom {
+  int grid;
+  const CtaPlan* plan;
+  int grid_m1;
+  const CtaPlan* plan_m1;
+};
+
 struct FormatOps {
   int format;
   int kt;          // k per tile
@@ -32,7 +43,7 @@ struct FormatOps {
   cudaError_t (*setup)();  // one-time kernel attributes
   // batch_invariant: every row's result must not depend on M (see
   // qgemv_set_batch_invariant); the kernels are chosen accordingly.
-  cudaError_t (*launch)(int M, const GemvParams& p, int grid, cudaStream_t s, bool batch_invariant);
+  cudaError_t (*launch)(int M, const GemvParams& p, const LaunchGeom& g, cudaStream_t s, bool batch_invariant);
   cudaError_t (*prepare)(const PrepareArgs& a, cudaStream_t s);
   // w_out[n*K + k] = exact decoded weight, read back from the prepared tiles
   cudaError_t (*dequant)(const uint8_t* tiles, const void* aux, const int32_t* seg_of_rt, int64_t N,
@@ -41,6 +52,7 @@ struct FormatOps {
   int tile_rows = 128;              // output rows per prepared tile
   int64_t partial_stride = 128 * 16;  // floats per stream-K partial slot
   int64_t aux_per_row = 0;          // aux bytes per output row, after aux_bytes
+  int m1_ctas_per_sm = 1;           // CTAs per SM of the M = 1 kernel (LaunchGeom::grid_m1)
 };
 
 const FormatOps* ops_q4_0();

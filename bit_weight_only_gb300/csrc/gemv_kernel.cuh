@@ -80,7 +80,11 @@ struct GemvParams {
 
 // Warps per slice for a given M: two while the whole accumulator set of a
 // lane fits in 128 registers, one above.
-__host__ __device__ constexpr int wps_for(int M) { return M <= 4 ? 2 : 1; }
+// A format with F::kCtasPerSm == 2 runs two independent CTAs of eight warps
+// per SM instead (their phases differ, which hides more latency; only
+// formats without a 64 KB table fit twice).
+template <class F>
+__host__ __device__ constexpr int wps_for(int M) { return (M <= 4 && F::kCtasPerSm == 1) ? 2 : 1; }
 
 // x rows stored per k pair; padded so vector loads stay aligned.
 __host__ __device__ constexpr int mpad(int M) { return M <= 2 ? M : (M + 3) / 4 * 4; }
@@ -150,14 +154,14 @@ struct RowAcc<M, RPW, true> {
 template <class F, int M>
 __host__ __device__ constexpr int gemv_smem_bytes() {
   return F::stages(M) * F::kTileBytes                              // tile ring
-         + kSlices * wps_for(M) * (F::kKW / 2) * mpad(M) * 8      // x pairs, per warp
+         + kSlices * wps_for<F>(M) * (F::kKW / 2) * mpad(M) * 8   // x pairs, per warp
          + kSlices * kTileRows * acc_stride(M) * 4                 // cross-slice reduction
          + F::kSharedBytes                                         // format tables
          + 2 * F::stages(M) * 8;                                   // mbarriers
 }
 
-template <int M>
-__host__ __device__ constexpr int gemv_threads() { return 32 * kSlices * wps_for(M); }
+template <class F, int M>
+__host__ __device__ constexpr int gemv_threads() { return 32 * kSlices * wps_for<F>(M); }
 
 // CTA that owns tile t when T tiles are split over G CTAs.
 __device__ __forceinline__ int64_t cta_of_tile(int64_t t, int64_t T, int64_t G) {
@@ -338,12 +342,12 @@ __device__ __noinline__ void rebuild_table(uint8_t* lut, const uint16_t* cb, int
 }
 
 template <class F, int M>
-__global__ void __launch_bounds__(gemv_threads<M>(), 1) gemv_kernel(const GemvParams p) {
+__global__ void __launch_bounds__(gemv_threads<F, M>(), F::kCtasPerSm) gemv_kernel(const GemvParams p) {
   constexpr int NS = F::stages(M);
   constexpr int TB = F::kTileBytes;
   constexpr int MP = mpad(M);
-  constexpr int WPS = wps_for(M);
-  constexpr int NT = gemv_threads<M>();
+  constexpr int WPS = wps_for<F>(M);
+  constexpr int NT = gemv_threads<F, M>();
   constexpr int RPW = kRowsPerLane / WPS;
   constexpr int XS_FLOATS = (F::kKW / 2) * MP * 2;  // per warp
   constexpr int RS = acc_stride(M);

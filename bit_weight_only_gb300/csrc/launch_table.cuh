@@ -35,11 +35,13 @@ struct LaunchTable {
     return cfg;
   }
 
+  static constexpr int kM1CtasPerSm = F::kCtasPerSm;
+
   static cudaError_t launch_m1(const GemvParams& p, int grid, cudaStream_t s) {
-    // 227 KB per CTA, less room for the kernel's few static bytes
-    static_assert(gemv_smem_bytes<F, 1>() <= 227 * 1024 - 256, "shared memory budget exceeded");
+    // 227 KB per SM shared by the CTAs, less room for each one's reserved and static bytes
+    static_assert(F::kCtasPerSm * (gemv_smem_bytes<F, 1>() + 2048) <= 228 * 1024, "shared memory budget exceeded");
     cudaLaunchAttribute attr[1];
-    const cudaLaunchConfig_t cfg = config(grid, gemv_threads<1>(), gemv_smem_bytes<F, 1>(), s, attr);
+    const cudaLaunchConfig_t cfg = config(grid, gemv_threads<F, 1>(), gemv_smem_bytes<F, 1>(), s, attr);
     return cudaLaunchKernelEx(&cfg, gemv_kernel<F, 1>, p);
   }
 
@@ -68,10 +70,16 @@ struct LaunchTable {
     return e;
   }
 
-  static cudaError_t launch(int M, const GemvParams& p, int grid, cudaStream_t s, bool batch_invariant) {
-    if (M == 1 && !batch_invariant) return launch_m1(p, grid, s);
-    if (M >= 1 && M <= 8) return launch_mma<1>(p, M, grid, s);
-    if (M > 8 && M <= kMaxM) return launch_mma<2>(p, M, grid, s);
+  static cudaError_t launch(int M, const GemvParams& p, const LaunchGeom& g, cudaStream_t s,
+                            bool batch_invariant) {
+    GemvParams q = p;
+    if (M == 1 && !batch_invariant) {
+      q.plan = g.plan_m1;
+      return launch_m1(q, g.grid_m1, s);
+    }
+    q.plan = g.plan;
+    if (M >= 1 && M <= 8) return launch_mma<1>(q, M, g.grid, s);
+    if (M > 8 && M <= kMaxM) return launch_mma<2>(q, M, g.grid, s);
     return cudaErrorInvalidValue;
   }
 };

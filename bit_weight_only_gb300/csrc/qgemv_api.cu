@@ -184,11 +184,13 @@ struct qgemv_ctx {
   int64_t nRT;
   int nKT;
   int64_t T;
-  int grid;
+  int grid;      // tensor-core and AQLM kernels: min(T, SMs)
+  int grid_m1;   // M = 1 CUDA-core kernel: min(T, SMs * m1_ctas_per_sm)
   uint8_t* tiles;
   void* aux;
   float* partials;
-  qgemv::CtaPlan* plan;
+  qgemv::CtaPlan* plan;     // [grid], then [grid_m1] for the M = 1 kernel if that grid differs
+  qgemv::CtaPlan* plan_m1;
   int32_t* seg_of_rt;  // inside aux (table formats), else nullptr
   int* err;
   int batch_invariant;  // qgemv_set_batch_invariant
@@ -279,6 +281,12 @@ static qgemv_handle create_impl(int format, int64_t N, int64_t K, const void* pa
   h->nKT = static_cast<int>((K + ops->kt - 1) / ops->kt);
   h->T = h->nRT * h->nKT;
   h->grid = static_cast<int>(h->T < sms ? h->T : sms);
+  {
+    const int64_t g1 = int64_t(sms) * ops->m1_ctas_per_sm;
+    h->grid_m1 = static_cast<int>(h->T < g1 ? h->T : g1);
+  }
+  const int slots_grid = h->grid > h->grid_m1 ? h->grid : h->grid_m1;  // partial slots for either grid
+  const int n_plans = h->grid + (h->grid_m1 != h->grid ? h->grid_m1 : 0);
   // codebook segment of every row tile (table formats)
   std::vector<int32_t> seg_of_rt(static_cast<size_t>(h->nRT), 0);
   {
@@ -328,8 +336,8 @@ static qgemv_handle create_impl(int format, int64_t N, int64_t K, const void* pa
   if (e == cudaSuccess && aux_bytes > 0) e = dev_alloc(&h->aux, static_cast<size_t>(aux_bytes));
   if (e == cudaSuccess)
     e = dev_alloc(reinterpret_cast<void**>(&h->partials),
-                  sizeof(float) * 2 * ops->partial_stride * static_cast<size_t>(h->grid));
-  if (e == cudaSuccess) e = dev_alloc(reinterpret_cast<void**>(&h->plan), sizeof(qgemv::CtaPlan) * h->grid);
+                  sizeof(float) * 2 * ops->partial_stride * static_cast<size_t>(slots_grid));
+  if (e == cudaSuccess) e = dev_alloc(reinterpret_cast<void**>(&h->plan), sizeof(qgemv::CtaPlan) * n_plans);
   if (e == cudaSuccess) e = dev_alloc(reinterpret_cast<void**>(&h->err), sizeof(int));
   if (e == cudaSuccess && stacked) {
     h->seg_of_rt = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(h->aux) + table_bytes);
@@ -337,11 +345,16 @@ static qgemv_handle create_impl(int format, int64_t N, int64_t K, const void* pa
   }
   if (e == cudaSuccess) {
     std::vector<qgemv::CtaPlan> plan = plan_stream_k(h->T, h->grid, h->nKT, ops->tile_rows);
+    if (h->grid_m1 != h->grid) {
+      const std::vector<qgemv::CtaPlan> plan1 = plan_stream_k(h->T, h->grid_m1, h->nKT, ops->tile_rows);
+      plan.insert(plan.end(), plan1.begin(), plan1.end());
+    }
     e = cudaMemcpy(h->plan, plan.data(), sizeof(qgemv::CtaPlan) * plan.size(), cudaMemcpyHostToDevice);
+    h->plan_m1 = h->grid_m1 != h->grid ? h->plan + h->grid : h->plan;
   }
   // partial slots start empty (all ones): the AQLM fix-up polls them
   if (e == cudaSuccess)
-    e = cudaMemset(h->partials, 0xff, sizeof(float) * 2 * ops->partial_stride * static_cast<size_t>(h->grid));
+    e = cudaMemset(h->partials, 0xff, sizeof(float) * 2 * ops->partial_stride * static_cast<size_t>(slots_grid));
   if (e == cudaSuccess) e = cudaMemset(h->err, 0, sizeof(int));
   if (e != cudaSuccess) return cleanup(QGEMV_ERR_CUDA, "allocating the handle's device buffers", e);
 
@@ -425,7 +438,8 @@ int qgemv_run(qgemv_handle h, const void* x, int M, float* y, void* stream) {
   p.T = h->T;
   p.nKT = h->nKT;
   p.skip_cta = h->skip_cta;
-  cudaError_t e = h->ops->launch(M, p, h->grid, static_cast<cudaStream_t>(stream), h->batch_invariant != 0);
+  const qgemv::LaunchGeom g = {h->grid, h->plan, h->grid_m1, h->plan_m1};
+  cudaError_t e = h->ops->launch(M, p, g, static_cast<cudaStream_t>(stream), h->batch_invariant != 0);
   if (e != cudaSuccess) return cuda_error(e, "launching the GEMV kernel");
   return ok();
 }
@@ -462,7 +476,9 @@ int qgemv_status(qgemv_handle h) {
   if (e != cudaSuccess) return cuda_error(e, "reading the kernel status");
   if (err) {
     // A run that gave up may have left partial slots written but unread.
-    cudaMemset(h->partials, 0xff, sizeof(float) * 2 * h->ops->partial_stride * static_cast<size_t>(h->grid));
+    cudaMemset(h->partials, 0xff,
+               sizeof(float) * 2 * h->ops->partial_stride *
+                   static_cast<size_t>(h->grid > h->grid_m1 ? h->grid : h->grid_m1));
     cudaMemset(h->err, 0, sizeof(int));
     if (err & 4)
       return set_error(QGEMV_ERR_CUDA, "a kernel found its shared-memory window unusable (code %d)", err);
