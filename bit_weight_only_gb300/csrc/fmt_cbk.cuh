@@ -99,7 +99,11 @@ struct FmtCBK4 {
   // (.. + 2, +3) with h = ks/2, each one table read.
   static constexpr int kMmaSharedBytes = kLutBytes;
   static constexpr int kMmaBlockSteps = 0;
+  struct MmaScales {};  // no block scale
   static constexpr int kMmaXWords = 8;  // x[m][32h + 8q .. +7], h = 0, 1
+  // one slice per warp, sixteen warps per CTA; the 64 KB table fits once per SM
+  __host__ __device__ static constexpr int mma_spw(int) { return 1; }
+  __host__ __device__ static constexpr int mma_ctas(int) { return 1; }
   __host__ __device__ static constexpr int mma_stages(int nb) { return nb == 1 ? 4 : 3; }
   __host__ __device__ static constexpr bool mma_prefetch_x(int) { return true; }
   template <int NT>
@@ -252,7 +256,11 @@ struct FmtCBK8 {
   // (16ks + 4q + 2, +3).
   static constexpr int kMmaSharedBytes = kLutBytes;
   static constexpr int kMmaBlockSteps = 0;
+  struct MmaScales {};  // no block scale
   static constexpr int kMmaXWords = 4;  // x[m][16h + 4q .. +3], h = 0, 1
+  // one slice per warp, sixteen warps per CTA; the 64 KB table fits once per SM
+  __host__ __device__ static constexpr int mma_spw(int) { return 1; }
+  __host__ __device__ static constexpr int mma_ctas(int) { return 1; }
   __host__ __device__ static constexpr int mma_stages(int nb) { return nb == 1 ? 4 : 3; }
   __host__ __device__ static constexpr bool mma_prefetch_x(int) { return true; }
   template <int NT>

@@ -79,20 +79,22 @@ struct FmtQ4_0 {
   static constexpr int kMmaSharedBytes = 0;
   static constexpr int kMmaBlockSteps = 2;
   static constexpr int kMmaXWords = 8;  // x[m][32b + 8q .. +7], b = 0, 1
-  __host__ __device__ static constexpr int mma_stages(int nb) { return nb == 1 ? 5 : 4; }
-  __host__ __device__ static constexpr bool mma_prefetch_x(int) { return true; }
+  // two slices per warp, eight warps per CTA, two CTAs per SM, two stages each
+  __host__ __device__ static constexpr int mma_spw(int) { return 2; }
+  __host__ __device__ static constexpr int mma_ctas(int) { return 2; }
+  __host__ __device__ static constexpr int mma_stages(int) { return 2; }
+  __host__ __device__ static constexpr bool mma_prefetch_x(int nb) { return nb == 1; }
   template <int NT>
   __device__ static void mma_init_shared(uint8_t*, const uint16_t*, int, int) {}
   __device__ static void mma_load_row(const uint8_t* stage, int slice, int l, int j, int q, uint32_t (&w)[2]) {
     mma_row_words(stage, slice, l, j, q, w);
   }
-  __device__ static void mma_scales(const uint8_t* stage, int slice, int l, int j, float (&d)[2]) {
+  struct MmaScales { uint32_t h2; };  // d of the row's two blocks, fp16 pair
+  __device__ static void mma_scales(const uint8_t* stage, int slice, int l, int j, MmaScales& d) {
     const int t = slice * 32 + l;
-    const __half2 h = *reinterpret_cast<const __half2*>(stage + kCodeBytes + (t * 4 + j) * 4);
-    const float2 f = __half22float2(h);
-    d[0] = f.x;
-    d[1] = f.y;
+    d.h2 = *reinterpret_cast<const uint32_t*>(stage + kCodeBytes + (t * 4 + j) * 4);
   }
+  __device__ static float mma_scale(const MmaScales& d, int blk) { return h2f(blk ? d.h2 >> 16 : d.h2 & 0xFFFFu); }
   __device__ static uint2 mma_frag(const uint32_t (&w)[2], int ks, uint32_t) {
     const uint32_t wd = (ks & 1) ? (w[ks >> 1] >> 8) : w[ks >> 1];
     return make_uint2(hfma2_u32(field_pair(wd, 0x000F000Fu), 0x3C003C00u, 0xE408E408u),   // x1 - 1032
@@ -245,17 +247,24 @@ struct FmtPQ2 {
   static constexpr int kMmaSharedBytes = 0;
   static constexpr int kMmaBlockSteps = 8;
   static constexpr int kMmaXWords = 16;  // x[m][64h + 16q .. +15], h = 0, 1
+  // One slice per warp, sixteen warps, one CTA per SM for every M: two
+  // slices per warp do not fit the activation registers of two blocks, and
+  // one geometry for all M keeps the summation order (batch invariance).
+  __host__ __device__ static constexpr int mma_spw(int) { return 1; }
+  __host__ __device__ static constexpr int mma_ctas(int) { return 1; }
   __host__ __device__ static constexpr int mma_stages(int) { return 5; }
-  __host__ __device__ static constexpr bool mma_prefetch_x(int nb) { return nb == 1; }
+  __host__ __device__ static constexpr bool mma_prefetch_x(int) { return false; }  // registers
   template <int NT>
   __device__ static void mma_init_shared(uint8_t*, const uint16_t*, int, int) {}
   __device__ static void mma_load_row(const uint8_t* stage, int slice, int l, int j, int q, uint32_t (&w)[2]) {
     mma_row_words(stage, slice, l, j, q, w);
   }
-  __device__ static void mma_scales(const uint8_t* stage, int slice, int l, int j, float (&d)[1]) {
+  struct MmaScales { float d; };  // d of the row's block (the whole slice)
+  __device__ static void mma_scales(const uint8_t* stage, int slice, int l, int j, MmaScales& d) {
     const int t = slice * 32 + l;
-    d[0] = h2f(*reinterpret_cast<const uint16_t*>(stage + kCodeBytes + (t * 4 + j) * 2));
+    d.d = h2f(*reinterpret_cast<const uint16_t*>(stage + kCodeBytes + (t * 4 + j) * 2));
   }
+  __device__ static float mma_scale(const MmaScales& d, int) { return d.d; }
   __device__ static uint32_t pq2_pair(uint32_t w, int f) {
     constexpr uint32_t kScale[4] = {0x3C003C00u, 0x34003400u, 0x2C002C00u, 0x24002400u};  // 1, 1/4, 1/16, 1/64
     constexpr uint32_t kOff[4] = {0xE401E401u, 0xDC04DC04u, 0xD410D410u, 0xCC40CC40u};    // -1025, -257, -65, -17

@@ -45,12 +45,21 @@ struct LaunchTable {
     return cudaLaunchKernelEx(&cfg, gemv_kernel<F, 1>, p);
   }
 
+  // The tensor-core kernel runs F::mma_ctas(NB) CTAs per SM: 1 (grid, plan)
+  // or as many as the M = 1 kernel (grid_m1, plan_m1).
   template <int NB>
-  static cudaError_t launch_mma(const GemvParams& p, int M, int grid, cudaStream_t s) {
-    static_assert(mma_smem_bytes<F, NB>() <= 227 * 1024 - 256, "shared memory budget exceeded");
+  static cudaError_t launch_mma(const GemvParams& p, int M, const LaunchGeom& g, cudaStream_t s) {
+    static_assert(F::mma_ctas(NB) == 1 || F::mma_ctas(NB) == F::kCtasPerSm, "tensor-core grid");
+    // batch invariance: both activation-block counts use one geometry
+    static_assert(F::mma_ctas(1) == F::mma_ctas(2) && F::mma_spw(1) == F::mma_spw(2), "one geometry for all M");
+    static_assert(F::mma_ctas(NB) * (mma_smem_bytes<F, NB>() + 2048) <= 228 * 1024,
+                  "shared memory budget exceeded");
+    GemvParams q = p;
+    q.plan = F::mma_ctas(NB) == 1 ? g.plan : g.plan_m1;
+    const int grid = F::mma_ctas(NB) == 1 ? g.grid : g.grid_m1;
     cudaLaunchAttribute attr[1];
-    const cudaLaunchConfig_t cfg = config(grid, kMmaThreads, mma_smem_bytes<F, NB>(), s, attr);
-    return cudaLaunchKernelEx(&cfg, gemv_mma_kernel<F, NB>, p, M);
+    const cudaLaunchConfig_t cfg = config(grid, mma_threads<F, NB>(), mma_smem_bytes<F, NB>(), s, attr);
+    return cudaLaunchKernelEx(&cfg, gemv_mma_kernel<F, NB>, q, M);
   }
 
   static int smem_bytes(int M) {
@@ -77,9 +86,8 @@ struct LaunchTable {
       q.plan = g.plan_m1;
       return launch_m1(q, g.grid_m1, s);
     }
-    q.plan = g.plan;
-    if (M >= 1 && M <= 8) return launch_mma<1>(q, M, g.grid, s);
-    if (M > 8 && M <= kMaxM) return launch_mma<2>(q, M, g.grid, s);
+    if (M >= 1 && M <= 8) return launch_mma<1>(q, M, g, s);
+    if (M > 8 && M <= kMaxM) return launch_mma<2>(q, M, g, s);
     return cudaErrorInvalidValue;
   }
 };

@@ -10,9 +10,12 @@
 //
 //   * Same prepared tiles, TMA ring, stream-K split, CTA plans and polled
 //     split-K fix-up as gemv_kernel.
-//   * Sixteen warps, two per k-slice: warp (slice s, half h) covers slice s
-//     of every tile for row groups j = 2h, 2h + 1 (rows 4l + j, l = 0..31),
-//     as four 16-row m-tiles (j = 2h + mt/2, l = 16 (mt & 1) + 0..15).
+//   * Two warps per group of F::mma_spw(NB) k-slices: warp (group g, half h)
+//     covers slices g * spw .. of every tile, one after the other, for
+//     row groups j = 2h, 2h + 1 (rows 4l + j, l = 0..31), as four 16-row
+//     m-tiles (j = 2h + mt/2, l = 16 (mt & 1) + 0..15).  Formats without a
+//     table use two slices per warp and run two CTAs of eight warps per SM,
+//     whose phases differ; the table formats sixteen warps, one CTA per SM.
 //   * Each thread reads the codes of its two fragment rows straight from the
 //     stage (a few 32/64-bit loads per row, conflict-free) and decodes them
 //     in registers into the A fragments -- no decoded copy of the weights is
@@ -31,16 +34,21 @@
 // Format hooks (members of the format struct): mma_stages(NB),
 // mma_prefetch_x(NB), kMmaSharedBytes, kMmaBlockSteps (0: no scale), kMmaXWords,
 // mma_init_shared, mma_load_row, mma_frag, mma_load_x, mma_bfrag and, with
-// a scale, mma_scales.
+// a scale, MmaScales, mma_scales and mma_scale.
 #pragma once
 
 #include "gemv_kernel.cuh"
 
 namespace qgemv {
 
-constexpr int kMmaWarps = 16;
-constexpr int kMmaThreads = 32 * kMmaWarps;  // 512
-constexpr int kMmaTiles = 4;                 // 16-row m-tiles per warp
+constexpr int kMmaTiles = 4;  // 16-row m-tiles per warp
+// Warps per CTA: two per group of F::mma_spw(NB) k-slices (one slice per
+// warp: 16 warps, one CTA per SM; two slices per warp: 8 warps, two CTAs per
+// SM, F::mma_ctas(NB)).
+template <class F, int NB>
+__host__ __device__ constexpr int mma_warps() { return 2 * kSlices / F::mma_spw(NB); }
+template <class F, int NB>
+__host__ __device__ constexpr int mma_threads() { return 32 * mma_warps<F, NB>(); }
 
 // tree reduction buffer: [4 slots][2 halves][4 m-tiles][NB][32 lanes] float4
 template <int NB>
@@ -186,7 +194,7 @@ __device__ __noinline__ void mma_rebuild_table(uint8_t* lut, const uint16_t* cb,
 }
 
 template <class F, int NB>
-__global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const GemvParams p, int M) {
+__global__ void __launch_bounds__(mma_threads<F, NB>(), F::mma_ctas(NB)) gemv_mma_kernel(const GemvParams p, int M) {
   constexpr int NS = F::mma_stages(NB);
   constexpr int TB = F::kTileBytes;
   constexpr int KS = F::kKW / 16;        // k16 steps per slice
@@ -194,7 +202,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const GemvPara
   constexpr int NBLK = BS > 0 ? KS / BS : 1;
   constexpr int XW = F::kMmaXWords;      // activation words per (thread, activation row)
   constexpr bool PF = F::mma_prefetch_x(NB);  // activations a tile ahead (registers permitting)
-  constexpr int NT = kMmaThreads;
+  constexpr int NT = mma_threads<F, NB>();
+  constexpr int NW = mma_warps<F, NB>();
+  constexpr int SPW = F::mma_spw(NB);     // k-slices per warp
+  constexpr int SG = kSlices / SPW;       // slice groups
 
   if (static_cast<int>(blockIdx.x) == p.skip_cta) return;  // test hook (QGEMV_FAULT_SKIP_CTA)
   extern __shared__ __align__(128) uint8_t smem[];
@@ -237,8 +248,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const GemvPara
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int q = lane & 3, gi = lane >> 2;
-  const int slice = warp % kSlices;
-  const int hf = warp / kSlices;
+  const int sgrp = warp % SG;  // slice group: slices sgrp * SPW .. + SPW - 1
+  const int hf = warp / SG;
   const int64_t G = gridDim.x;
   const int64_t c = blockIdx.x;
   const int64_t t0 = stream_split(c, p.T, G);
@@ -252,7 +263,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const GemvPara
   if (elected) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kMmaWarps);
+      mbar_init(&empty[s], NW);
     }
     s_abort = 0;
     fence_mbarrier_init();
@@ -281,17 +292,20 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const GemvPara
   int64_t rt = rt_first;
   int kt = static_cast<int>(t0 - rt * p.nKT);
   const bool xvec = (reinterpret_cast<uintptr_t>(p.x) & 15) == 0 && (p.K & 7) == 0;
-  // activation fragments of the thread's B rows m = gi + 8 nb (a tile ahead
-  // when PF, else loaded at the top of each tile)
-  uint32_t xw[NB][XW];
+  // activation fragments of the thread's B rows m = gi + 8 nb for each of
+  // its slices (a tile ahead when PF, else loaded at the top of each tile)
+  uint32_t xw[SPW][NB][XW];
   const unsigned short* xrow[NB];
 #pragma unroll
   for (int nb = 0; nb < NB; ++nb)
     xrow[nb] = gi + 8 * nb < M ? reinterpret_cast<const unsigned short*>(p.x) + (gi + 8 * nb) * p.K : nullptr;
-  auto load_x = [&](uint32_t (&dst)[NB][XW], int ktile) {
-    const int64_t kb = static_cast<int64_t>(ktile) * F::kKT + slice * F::kKW;
+  auto load_x = [&](uint32_t (&dst)[SPW][NB][XW], int ktile) {
 #pragma unroll
-    for (int nb = 0; nb < NB; ++nb) F::mma_load_x(dst[nb], xrow[nb], p.K, kb, q, xvec);
+    for (int ss = 0; ss < SPW; ++ss) {
+      const int64_t kb = static_cast<int64_t>(ktile) * F::kKT + (sgrp * SPW + ss) * F::kKW;
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb) F::mma_load_x(dst[ss][nb], xrow[nb], p.K, kb, q, xvec);
+    }
   };
   if constexpr (PF) {
     if (ntiles > 0) load_x(xw, kt);
@@ -337,7 +351,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const GemvPara
       }
     }
     const int kt_next = (kt + 1 == p.nKT) ? 0 : kt + 1;
-    uint32_t xn[PF ? NB : 1][PF ? XW : 1];
+    uint32_t xn[PF ? SPW : 1][PF ? NB : 1][PF ? XW : 1];
     if constexpr (PF) {
       if (i + 1 < ntiles) load_x(xn, kt_next);
     } else {
@@ -350,63 +364,71 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const GemvPara
       s_abort = 1;
     } else {
       const uint8_t* stage = stage_ptr(s);
-      // codes (and scales) of the thread's eight rows, then release the stage
-      uint32_t w[kMmaTiles][2][2];
-      float d[kMmaTiles][2][NBLK];
 #pragma unroll
-      for (int mt = 0; mt < kMmaTiles; ++mt) {
-        const int j = 2 * hf + (mt >> 1);
-        const int l = 16 * (mt & 1) + gi;
-        F::mma_load_row(stage, slice, l, j, q, w[mt][0]);
-        F::mma_load_row(stage, slice, l + 8, j, q, w[mt][1]);
-        if constexpr (BS > 0) {
-          F::mma_scales(stage, slice, l, j, d[mt][0]);
-          F::mma_scales(stage, slice, l + 8, j, d[mt][1]);
+      for (int ss = 0; ss < SPW; ++ss) {
+        const int slice = sgrp * SPW + ss;
+        // codes (and scales) of the thread's eight rows in this slice; after
+        // the warp's last slice, release the stage
+        uint32_t w[kMmaTiles][2][2];
+        typename F::MmaScales d[kMmaTiles][2];  // block scales of the rows, read per block
+#pragma unroll
+        for (int mt = 0; mt < kMmaTiles; ++mt) {
+          const int j = 2 * hf + (mt >> 1);
+          const int l = 16 * (mt & 1) + gi;
+          F::mma_load_row(stage, slice, l, j, q, w[mt][0]);
+          F::mma_load_row(stage, slice, l + 8, j, q, w[mt][1]);
+          if constexpr (BS > 0) {
+            F::mma_scales(stage, slice, l, j, d[mt][0]);
+            F::mma_scales(stage, slice, l + 8, j, d[mt][1]);
+          }
         }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
+        if (ss == SPW - 1) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[s]);
+        }
 
-      // MG m-tiles at a time, their MMAs interleaved so that consecutive MMAs
-      // are independent (all four for one activation block; one for two,
-      // which need twice the accumulators)
-      constexpr int MG = NB == 1 ? kMmaTiles : 1;
+        // MG m-tiles at a time, their MMAs interleaved so that consecutive
+        // MMAs are independent (all four for one activation block; one for
+        // two, which need twice the accumulators)
+        constexpr int MG = NB == 1 ? kMmaTiles : 1;
 #pragma unroll
-      for (int mg = 0; mg < kMmaTiles; mg += MG) {
+        for (int mg = 0; mg < kMmaTiles; mg += MG) {
 #pragma unroll
-        for (int blk = 0; blk < NBLK; ++blk) {
-          float tmp[MG][NB][4];  // block sums (block formats); the first MMA writes them
+          for (int blk = 0; blk < NBLK; ++blk) {
+            float tmp[MG][NB][4];  // block sums (block formats); the first MMA writes them
 #pragma unroll
-          for (int ks = blk * (BS > 0 ? BS : KS); ks < (blk + 1) * (BS > 0 ? BS : KS); ++ks) {
+            for (int ks = blk * (BS > 0 ? BS : KS); ks < (blk + 1) * (BS > 0 ? BS : KS); ++ks) {
 #pragma unroll
-            for (int mi = 0; mi < MG; ++mi) {
-              const int mt = mg + mi;
-              const uint2 r0 = F::mma_frag(w[mt][0], ks, lut_key);  // row gi: (k lo pair, k hi pair)
-              const uint2 r1 = F::mma_frag(w[mt][1], ks, lut_key);  // row gi + 8
+              for (int mi = 0; mi < MG; ++mi) {
+                const int mt = mg + mi;
+                const uint2 r0 = F::mma_frag(w[mt][0], ks, lut_key);  // row gi: (k lo pair, k hi pair)
+                const uint2 r1 = F::mma_frag(w[mt][1], ks, lut_key);  // row gi + 8
 #pragma unroll
-              for (int nb = 0; nb < NB; ++nb) {
-                const uint2 b = F::mma_bfrag(xw[nb], ks);
-                if constexpr (BS > 0) {
-                  if (ks == blk * BS)
-                    mma_16816_c0(tmp[mi][nb], r0.x, r1.x, r0.y, r1.y, b.x, b.y);
-                  else
-                    mma_16816(tmp[mi][nb], r0.x, r1.x, r0.y, r1.y, b.x, b.y);
-                } else
-                  mma_16816(acc[mt][nb], r0.x, r1.x, r0.y, r1.y, b.x, b.y);
+                for (int nb = 0; nb < NB; ++nb) {
+                  const uint2 bf = F::mma_bfrag(xw[ss][nb], ks);
+                  if constexpr (BS > 0) {
+                    if (ks == blk * BS)
+                      mma_16816_c0(tmp[mi][nb], r0.x, r1.x, r0.y, r1.y, bf.x, bf.y);
+                    else
+                      mma_16816(tmp[mi][nb], r0.x, r1.x, r0.y, r1.y, bf.x, bf.y);
+                  } else
+                    mma_16816(acc[mt][nb], r0.x, r1.x, r0.y, r1.y, bf.x, bf.y);
+                }
               }
             }
-          }
-          if constexpr (BS > 0) {
+            if constexpr (BS > 0) {
 #pragma unroll
-            for (int mi = 0; mi < MG; ++mi)
+              for (int mi = 0; mi < MG; ++mi)
 #pragma unroll
-              for (int nb = 0; nb < NB; ++nb) {
-                const int mt = mg + mi;
-                acc[mt][nb][0] = fmaf(d[mt][0][blk], tmp[mi][nb][0], acc[mt][nb][0]);
-                acc[mt][nb][1] = fmaf(d[mt][0][blk], tmp[mi][nb][1], acc[mt][nb][1]);
-                acc[mt][nb][2] = fmaf(d[mt][1][blk], tmp[mi][nb][2], acc[mt][nb][2]);
-                acc[mt][nb][3] = fmaf(d[mt][1][blk], tmp[mi][nb][3], acc[mt][nb][3]);
-              }
+                for (int nb = 0; nb < NB; ++nb) {
+                  const int mt = mg + mi;
+                  const float d0 = F::mma_scale(d[mt][0], blk), d1 = F::mma_scale(d[mt][1], blk);
+                  acc[mt][nb][0] = fmaf(d0, tmp[mi][nb][0], acc[mt][nb][0]);
+                  acc[mt][nb][1] = fmaf(d0, tmp[mi][nb][1], acc[mt][nb][1]);
+                  acc[mt][nb][2] = fmaf(d1, tmp[mi][nb][2], acc[mt][nb][2]);
+                  acc[mt][nb][3] = fmaf(d1, tmp[mi][nb][3], acc[mt][nb][3]);
+                }
+            }
           }
         }
       }
@@ -414,9 +436,11 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const GemvPara
     if (++s == NS) { s = 0; ph ^= 1; }
     if constexpr (PF) {
 #pragma unroll
-      for (int nb = 0; nb < NB; ++nb)
+      for (int ss = 0; ss < SPW; ++ss)
 #pragma unroll
-        for (int e = 0; e < XW; ++e) xw[nb][e] = xn[nb][e];
+        for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+          for (int e = 0; e < XW; ++e) xw[ss][nb][e] = xn[ss][nb][e];
     }
 
     const bool row_end = (kt_next == 0) || (i + 1 == ntiles);
@@ -425,24 +449,24 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const GemvPara
     if (kt_next == 0) ++rt;
     if (!row_end) continue;
 
-    // ---- row-tile epilogue: add the eight slices' results in a fixed tree ----
+    // ---- row-tile epilogue: add the slice groups' results in a fixed tree ----
 #pragma unroll 1
-    for (int width = 4; width >= 1; width >>= 1) {
-      if (slice >= width && slice < 2 * width) {
+    for (int width = SG / 2; width >= 1; width >>= 1) {
+      if (sgrp >= width && sgrp < 2 * width) {
 #pragma unroll
         for (int mt = 0; mt < kMmaTiles; ++mt)
 #pragma unroll
           for (int nb = 0; nb < NB; ++nb)
-            red[(((slice - width) * 2 + hf) * kMmaTiles + mt) * NB * 32 + nb * 32 + lane] =
+            red[(((sgrp - width) * 2 + hf) * kMmaTiles + mt) * NB * 32 + nb * 32 + lane] =
                 make_float4(acc[mt][nb][0], acc[mt][nb][1], acc[mt][nb][2], acc[mt][nb][3]);
       }
       named_bar_sync(1, NT);
-      if (slice < width) {
+      if (sgrp < width) {
 #pragma unroll
         for (int mt = 0; mt < kMmaTiles; ++mt)
 #pragma unroll
           for (int nb = 0; nb < NB; ++nb) {
-            const float4 v = red[((slice * 2 + hf) * kMmaTiles + mt) * NB * 32 + nb * 32 + lane];
+            const float4 v = red[((sgrp * 2 + hf) * kMmaTiles + mt) * NB * 32 + nb * 32 + lane];
             acc[mt][nb][0] += v.x;
             acc[mt][nb][1] += v.y;
             acc[mt][nb][2] += v.z;
@@ -451,7 +475,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const GemvPara
       }
       named_bar_sync(1, NT);
     }
-    if (slice == 0) {
+    if (sgrp == 0) {
       const bool owner = (cur_rt * p.nKT >= t0) && ((cur_rt + 1) * p.nKT <= t1);
       const int side = (cur_rt * p.nKT <= t0) ? 0 : 1;
       float* my_part = p.partials + (c * 2 + side) * kPartialStride;
