@@ -70,6 +70,7 @@ struct FmtCBK4 {
   static constexpr int kKT = kKW * kSlices;                              // 512
   static constexpr int kTileBytes = kLaneSlots * kRowsPerLane * 32;      // 32768
   static constexpr int kCtasPerSm = 1;  // the 64 KB table fits once per SM
+  static constexpr bool kTileParity = true;  // so the two warps of a slice take alternate tiles
   __host__ __device__ static constexpr int stages(int M) { return M <= 4 ? 4 : 2; }
   static constexpr int kSharedBytes = kLutBytes;
   static constexpr int kCbEntries = 16;
@@ -226,6 +227,7 @@ struct FmtCBK8 {
   static constexpr int kKT = kKW * kSlices;                              // 256
   static constexpr int kTileBytes = kLaneSlots * kRowsPerLane * 32;      // 32768
   static constexpr int kCtasPerSm = 1;  // the 64 KB table fits once per SM
+  static constexpr bool kTileParity = true;  // so the two warps of a slice take alternate tiles
   __host__ __device__ static constexpr int stages(int M) { return M <= 4 ? 4 : 2; }
   static constexpr int kCbEntries = 256;
   static constexpr int kSharedBytes = kLutBytes;

@@ -65,6 +65,7 @@ struct FmtQ4_0 {
   static constexpr int kTileBytes = kCodeBytes + kLaneSlots * 16;  // 36864
   // M = 1 CUDA-core kernel: two CTAs of eight warps per SM, two stages each
   static constexpr int kCtasPerSm = 2;
+  static constexpr bool kTileParity = false;
   __host__ __device__ static constexpr int stages(int) { return 2; }
   static constexpr int kSharedBytes = 0;
   static constexpr float kOutScale = kFieldOutScale;
@@ -230,6 +231,7 @@ struct FmtPQ2 {
   static constexpr int kTileBytes = kCodeBytes + kLaneSlots * 8;  // 34816
   // M = 1 CUDA-core kernel: two CTAs of eight warps per SM, two stages each
   static constexpr int kCtasPerSm = 2;
+  static constexpr bool kTileParity = false;
   __host__ __device__ static constexpr int stages(int) { return 2; }
   static constexpr int kSharedBytes = 0;
   static constexpr float kOutScale = kFieldOutScale;

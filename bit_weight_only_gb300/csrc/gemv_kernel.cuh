@@ -151,11 +151,22 @@ struct RowAcc<M, RPW, true> {
 };
 
 // Dynamic shared memory of gemv_kernel<F, M>.
+// Tile parity (formats with F::kTileParity, which cannot run two CTAs per
+// SM): the two warps of a slice take alternate tiles, each for all four rows
+// of its lanes, instead of splitting the rows; the two halves of the CTA then
+// do not wait on the same tile.  Their partial sums meet at the row-tile end.
+template <class F, int M>
+__host__ __device__ constexpr bool tile_parity() { return F::kTileParity && wps_for<F>(M) == 2; }
+// partial-sum slots of the cross-slice reduction (per slice, and per half
+// with tile parity)
+template <class F, int M>
+__host__ __device__ constexpr int red_slots() { return tile_parity<F, M>() ? 2 * kSlices : kSlices; }
+
 template <class F, int M>
 __host__ __device__ constexpr int gemv_smem_bytes() {
   return F::stages(M) * F::kTileBytes                              // tile ring
          + kSlices * wps_for<F>(M) * (F::kKW / 2) * mpad(M) * 8   // x pairs, per warp
-         + kSlices * kTileRows * acc_stride(M) * 4                 // cross-slice reduction
+         + red_slots<F, M>() * kTileRows * acc_stride(M) * 4       // cross-slice reduction
          + F::kSharedBytes                                         // format tables
          + 2 * F::stages(M) * 8;                                   // mbarriers
 }
@@ -348,7 +359,8 @@ __global__ void __launch_bounds__(gemv_threads<F, M>(), F::kCtasPerSm) gemv_kern
   constexpr int MP = mpad(M);
   constexpr int WPS = wps_for<F>(M);
   constexpr int NT = gemv_threads<F, M>();
-  constexpr int RPW = kRowsPerLane / WPS;
+  constexpr bool PAR = tile_parity<F, M>();
+  constexpr int RPW = PAR ? kRowsPerLane : kRowsPerLane / WPS;
   constexpr int XS_FLOATS = (F::kKW / 2) * MP * 2;  // per warp
   constexpr int RS = acc_stride(M);
 
@@ -356,7 +368,7 @@ __global__ void __launch_bounds__(gemv_threads<F, M>(), F::kCtasPerSm) gemv_kern
   uint8_t* ring = smem;
   float* xs_all = reinterpret_cast<float*>(smem + NS * TB);
   float* red = xs_all + kSlices * WPS * XS_FLOATS;
-  uint8_t* fsh = reinterpret_cast<uint8_t*>(red + kSlices * kTileRows * RS);
+  uint8_t* fsh = reinterpret_cast<uint8_t*>(red + red_slots<F, M>() * kTileRows * RS);
   uint64_t* full = reinterpret_cast<uint64_t*>(fsh + F::kSharedBytes);
   uint64_t* empty = full + NS;
   __shared__ volatile int s_abort;
@@ -386,7 +398,7 @@ __global__ void __launch_bounds__(gemv_threads<F, M>(), F::kCtasPerSm) gemv_kern
   if (elected) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kSlices * WPS);
+      mbar_init(&empty[s], PAR ? kSlices : kSlices * WPS);  // with tile parity one half uses a stage
     }
     s_abort = 0;
     fence_mbarrier_init();
@@ -413,7 +425,10 @@ __global__ void __launch_bounds__(gemv_threads<F, M>(), F::kCtasPerSm) gemv_kern
 
   float* xs = xs_all + warp * XS_FLOATS;
   RowAcc<M, RPW> acc;
-  acc.init(red, slice, half, lane);
+  // reduction slot and row half of this warp (tile parity: all rows, a slot per half)
+  const int rslot = PAR ? half * kSlices + slice : slice;
+  const int rhalf = PAR ? 0 : half;
+  acc.init(red, rslot, rhalf, lane);
 
   // Programmatic dependent launch: the prologue above (barriers, tables, the
   // first weight copies) touches nothing a previous kernel in the stream
@@ -425,8 +440,11 @@ __global__ void __launch_bounds__(gemv_threads<F, M>(), F::kCtasPerSm) gemv_kern
   // Position of tile t0 in the stream, advanced incrementally below.
   int64_t rt = div_fast(t0, p.nKT);
   int kt = static_cast<int>(t0 - rt * p.nKT);
+  // x of the next tile this warp computes (tile parity: every second tile)
+  constexpr int TSTEP = PAR ? 2 : 1;
+  const int first = PAR ? half : 0;
   typename F::XRegs xr;
-  if (ntiles > 0) F::template load_x<M>(xr, p, kt, slice, lane);
+  if (first < ntiles) F::template load_x<M>(xr, p, static_cast<int>((kt + first) % p.nKT), slice, lane);
   typename F::XScale xscale;  // per-lane activation scaling, the same for every tile
   F::x_scales(xscale, lane);
 
@@ -466,21 +484,24 @@ __global__ void __launch_bounds__(gemv_threads<F, M>(), F::kCtasPerSm) gemv_kern
       }
     }
 
-    // Stage this tile's activations, then prefetch the next tile's.
-    float xsum[F::kSumGroups][M];
-    __syncwarp();
-    F::template stage_x<M>(xs, xsum, xr, xscale, lane);
-    __syncwarp();
     const int kt_next = (kt + 1 == p.nKT) ? 0 : kt + 1;
-    if (i + 1 < ntiles) F::template load_x<M>(xr, p, kt_next, slice, lane);
+    if (!PAR || (i & 1) == half) {
+      // Stage this tile's activations, then prefetch those of the warp's next tile.
+      float xsum[F::kSumGroups][M];
+      __syncwarp();
+      F::template stage_x<M>(xs, xsum, xr, xscale, lane);
+      __syncwarp();
+      if (i + TSTEP < ntiles)
+        F::template load_x<M>(xr, p, PAR ? static_cast<int>((kt + 2) % p.nKT) : kt_next, slice, lane);
 
-    const bool ok = !abort && mbar_wait_bounded(&full[s], ph);
-    if (!ok) {
-      if (!abort && lane == 0) atomicOr(p.err, kErrTimeoutFull);
-      s_abort = 1;
-    } else {
-      F::template tile_math<M, RPW>(ring + s * TB, xs, xsum, acc, fsh, slice, half, lane,
-                                    &empty[s]);
+      const bool ok = !abort && mbar_wait_bounded(&full[s], ph);
+      if (!ok) {
+        if (!abort && lane == 0) atomicOr(p.err, kErrTimeoutFull);
+        s_abort = 1;
+      } else {
+        F::template tile_math<M, RPW>(ring + s * TB, xs, xsum, acc, fsh, slice, rhalf, lane,
+                                      &empty[s]);
+      }
     }
     if (++s == NS) { s = 0; ph ^= 1; }
 
@@ -491,7 +512,7 @@ __global__ void __launch_bounds__(gemv_threads<F, M>(), F::kCtasPerSm) gemv_kern
     if (!row_end) continue;
 
     // ---- row-tile epilogue: add the slices' partials in slice order ----
-    acc.flush(red, slice, half, lane);
+    acc.flush(red, rslot, rhalf, lane);
     named_bar_sync(1, NT);
 
     const bool owner = (cur_rt * p.nKT >= t0) && ((cur_rt + 1) * p.nKT <= t1);
@@ -502,7 +523,7 @@ __global__ void __launch_bounds__(gemv_threads<F, M>(), F::kCtasPerSm) gemv_kern
       const int m = o / kTileRows;
       float v = 0.f;
 #pragma unroll
-      for (int w = 0; w < kSlices; ++w) v += red[(w * kTileRows + r) * RS + m];
+      for (int w = 0; w < red_slots<F, M>(); ++w) v += red[(w * kTileRows + r) * RS + m];
       if (owner) {
         const int64_t n = cur_rt * kTileRows + r;
         if (n < p.N) p.y[m * p.N + n] = v * F::kOutScale;
