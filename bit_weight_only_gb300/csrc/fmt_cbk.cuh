@@ -46,18 +46,6 @@ __device__ __forceinline__ void fma_f16x2_f32x2(uint32_t a2, uint32_t b2, float 
       : "r"(a2), "r"(b2));
 }
 
-// d = a.lo * b.lo + (a.hi * b.hi + c)   (f16 x f16 products, f32 accumulation)
-__device__ __forceinline__ float fma2_f16_f32(uint32_t a2, uint32_t b2, float c) {
-  float d;
-  asm("{\n\t.reg .f16 al, ah, bl, bh;\n\t.reg .f32 t;\n\t"
-      "mov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
-      "fma.rn.f32.f16 t, ah, bh, %3;\n\t"
-      "fma.rn.f32.f16 %0, al, bl, t;\n\t}"
-      : "=f"(d)
-      : "r"(a2), "r"(b2), "f"(c));
-  return d;
-}
-
 // ------------------------------------------------------------------ CBK4 --
 //
 // Tile: 128 rows x 512 k.  Slice s <-> k 64s..64s+63, lane slot t = 32s + l

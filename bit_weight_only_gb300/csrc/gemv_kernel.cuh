@@ -174,11 +174,6 @@ __host__ __device__ constexpr int gemv_smem_bytes() {
 template <class F, int M>
 __host__ __device__ constexpr int gemv_threads() { return 32 * kSlices * wps_for<F>(M); }
 
-// CTA that owns tile t when T tiles are split over G CTAs.
-__device__ __forceinline__ int64_t cta_of_tile(int64_t t, int64_t T, int64_t G) {
-  return ((t + 1) * G - 1) / T;
-}
-
 // Finish one shared row tile (ROWS output rows) as described by a CtaPlan
 // segment: sum rows [r0, r0 + nr) of each activation row over the S
 // contributors starting at CTA cf.  A partial slot holds the empty mark (all
