@@ -5,9 +5,10 @@
 //
 // Decode: a table lookup in shared memory per index byte.  The table is
 // replicated once per lane (entry e of lane l at byte e*256 + l*4), so the 32
-// lanes of a warp always hit 32 different banks whatever their indices, and
-// the byte offset of an entry is built from the index byte with one PRMT
-// (index byte -> bits 8..15, lane*4 -> bits 0..7).
+// lanes of a warp always hit 32 different banks whatever their indices.  The
+// table sits on a 64 KB boundary of the shared window, so the whole shared
+// address of an entry is one PRMT of the index byte (-> bits 8..15) with the
+// lane's key (table >> 16 -> bits 16..23, lane*4 -> bits 0..7).
 //   CBK4: one byte = two indices (k even in the low nibble, k odd in the
 //         high nibble); the entry is the fp16 pair (c[lo], c[hi]), and the
 //         products with the fp16 activations accumulate in fp32 with the
@@ -23,16 +24,10 @@ namespace qgemv {
 
 constexpr int kLutBytes = 256 * 256;  // 256 entries x 64 four-byte slots
 
-// byte offset in the lane-replicated table of index byte `bsel` (0..3) of w
-__device__ __forceinline__ uint32_t lut_offset(uint32_t w, uint32_t lane4, int bsel) {
-  // result bytes: [0] = lane4.b0, [1] = w.b(bsel), [2] = [3] = lane4.b1 (= 0)
-  uint32_t r;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(lane4), "r"(w), "r"(0x1100u | ((4u + bsel) << 4)));
-  return r;
-}
-
-__device__ __forceinline__ uint32_t lds32(const uint8_t* base, uint32_t off) {
-  return *reinterpret_cast<const uint32_t*>(base + off);
+// Key of the lane's table entries for lut_addr: the table (on a 64 KB
+// boundary of the shared window) >> 16 in byte 2, lane * 4 in byte 0.
+__device__ __forceinline__ uint32_t lut_key_of(const uint8_t* lut, int lane) {
+  return smem_u32(lut) | (static_cast<uint32_t>(lane) << 2);
 }
 
 // acc[0] += a.lo * b.lo, acc[1] += a.hi * b.hi  (f16 x f16 products, exact;
@@ -157,7 +152,7 @@ struct FmtCBK4 {
     uint4 clo[RPW], chi[RPW];
     load_codes32<RPW>(stage, j0, t, clo, chi);
     release_stage(empty_bar, lane);
-    const uint32_t lane4 = static_cast<uint32_t>(lane) << 2;
+    const uint32_t key = lut_key_of(lut, lane);
     const uint32_t* xw = reinterpret_cast<const uint32_t*>(xs);
 
     // two accumulators per (row, m): even k and odd k, two independent chains
@@ -188,7 +183,7 @@ struct FmtCBK4 {
 #pragma unroll
         for (int j = 0; j < RPW; ++j) {
           const uint32_t wv = i < 4 ? word_of(clo[j], i) : word_of(chi[j], i - 4);
-          const uint32_t c2 = lds32(lut, lut_offset(wv, lane4, bp));
+          const uint32_t c2 = lds32_at(lut_addr(wv, key, bp));
 #pragma unroll
           for (int m = 0; m < M; ++m) fma_f16x2_f32x2(c2, xp[m], acc[j][m]);
         }
@@ -311,7 +306,7 @@ struct FmtCBK8 {
     uint4 clo[RPW], chi[RPW];
     FmtCBK4::load_codes32<RPW>(stage, j0, t, clo, chi);
     release_stage(empty_bar, lane);
-    const uint32_t lane4 = static_cast<uint32_t>(lane) << 2;
+    const uint32_t key = lut_key_of(lut, lane);
 
     float2 acc[RPW][M];
 #pragma unroll
@@ -331,8 +326,8 @@ struct FmtCBK8 {
 #pragma unroll
         for (int j = 0; j < RPW; ++j) {
           const uint32_t wv = i < 4 ? word_of(clo[j], i) : word_of(chi[j], i - 4);
-          const float2 w2 = make_float2(__uint_as_float(lds32(lut, lut_offset(wv, lane4, 2 * pp))),
-                                        __uint_as_float(lds32(lut, lut_offset(wv, lane4, 2 * pp + 1))));
+          const float2 w2 = make_float2(__uint_as_float(lds32_at(lut_addr(wv, key, 2 * pp))),
+                                        __uint_as_float(lds32_at(lut_addr(wv, key, 2 * pp + 1))));
 #pragma unroll
           for (int m = 0; m < M; ++m) acc[j][m] = __ffma2_rn(w2, xv[m], acc[j][m]);
         }

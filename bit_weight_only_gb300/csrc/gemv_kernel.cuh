@@ -162,13 +162,28 @@ __host__ __device__ constexpr bool tile_parity() { return F::kTileParity && wps_
 template <class F, int M>
 __host__ __device__ constexpr int red_slots() { return tile_parity<F, M>() ? 2 * kSlices : kSlices; }
 
+// Table formats (a 64 KB lane-replicated table) place the table on a 64 KB
+// boundary of the shared window, so that one PRMT of an index byte with
+// (table >> 16, lane * 4) is the whole address of an entry, with no add per
+// lookup.  Before the table ("pre", at most 64 KB less the window offset of
+// the dynamic area): stage 0, the staged x, the reduction slots and the
+// mbarriers; after it the other stages.  Formats without a table keep one
+// block: ring, x, reduction slots, mbarriers.
+constexpr int kTableAlign = 65536;
+constexpr int kTablePreSlack = 4096;  // room left for the window offset of the dynamic area
+
 template <class F, int M>
-__host__ __device__ constexpr int gemv_smem_bytes() {
-  return F::stages(M) * F::kTileBytes                              // tile ring
+__host__ __device__ constexpr int gemv_pre_bytes() {
+  return F::kTileBytes                                             // stage 0
          + kSlices * wps_for<F>(M) * (F::kKW / 2) * mpad(M) * 8   // x pairs, per warp
          + red_slots<F, M>() * kTileRows * acc_stride(M) * 4       // cross-slice reduction
-         + F::kSharedBytes                                         // format tables
-         + 2 * F::stages(M) * 8;                                   // mbarriers
+         + (2 * F::stages(M) * 8 + 127) / 128 * 128;               // mbarriers (stage 1 stays 128-aligned)
+}
+
+template <class F, int M>
+__host__ __device__ constexpr int gemv_smem_bytes() {
+  return F::kSharedBytes == 0 ? gemv_pre_bytes<F, M>() + (F::stages(M) - 1) * F::kTileBytes
+                              : kTableAlign + F::kSharedBytes + (F::stages(M) - 1) * F::kTileBytes;
 }
 
 template <class F, int M>
@@ -360,17 +375,38 @@ __global__ void __launch_bounds__(gemv_threads<F, M>(), F::kCtasPerSm) gemv_kern
   constexpr int RS = acc_stride(M);
 
   extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t* ring = smem;
-  float* xs_all = reinterpret_cast<float*>(smem + NS * TB);
+  // stage s at ring0 (s = 0) or ringN + (s - 1) TB
+  uint8_t* ring0 = smem;
+  float* xs_all = reinterpret_cast<float*>(smem + TB);
   float* red = xs_all + kSlices * WPS * XS_FLOATS;
-  uint8_t* fsh = reinterpret_cast<uint8_t*>(red + red_slots<F, M>() * kTileRows * RS);
-  uint64_t* full = reinterpret_cast<uint64_t*>(fsh + F::kSharedBytes);
-  uint64_t* empty = full + NS;
+  uint64_t* full = reinterpret_cast<uint64_t*>(red + red_slots<F, M>() * kTileRows * RS);
+  uint8_t* ringN;
+  uint8_t* fsh;
   __shared__ volatile int s_abort;
   __shared__ int s_seg[2];
   __shared__ __align__(16) CtaPlan s_plan;
 
   if (static_cast<int>(blockIdx.x) == p.skip_cta) return;  // test hook (QGEMV_FAULT_SKIP_CTA)
+  if constexpr (F::kSharedBytes == 0) {
+    ringN = smem + gemv_pre_bytes<F, M>();
+    fsh = smem;  // unused
+  } else {
+    static_assert(F::kSharedBytes == kTableAlign, "one 64 KB table");
+    static_assert(gemv_pre_bytes<F, M>() + kTablePreSlack <= kTableAlign, "pre-table layout");
+    const uint32_t base = smem_u32(smem);
+    uint32_t dyn;
+    asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
+    const uint32_t R0 = (base + (kTableAlign - 1)) & ~uint32_t(kTableAlign - 1);
+    if (R0 - base < uint32_t(gemv_pre_bytes<F, M>()) ||
+        R0 + kTableAlign + (NS - 1) * TB > base + dyn) {
+      if (threadIdx.x == 0) atomicOr(p.err, kErrSmemLayout);
+      return;
+    }
+    fsh = smem + (R0 - base);
+    ringN = fsh + kTableAlign;
+  }
+  uint64_t* empty = full + NS;
+  auto stage_ptr = [&](int st) { return st == 0 ? ring0 : ringN + (st - 1) * TB; };
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int slice = warp % kSlices;
@@ -398,9 +434,9 @@ __global__ void __launch_bounds__(gemv_threads<F, M>(), F::kCtasPerSm) gemv_kern
     s_abort = 0;
     fence_mbarrier_init();
     pol = l2_policy_evict_first();
-    for (; n_issued < NS - 1 && n_issued < ntiles; ++n_issued) {
+    for (; n_issued < (PAR ? NS : NS - 1) && n_issued < ntiles; ++n_issued) {
       mbar_arrive_expect_tx(&full[n_issued], TB);
-      bulk_g2s(ring + n_issued * TB, p.tiles + (t0 + n_issued) * TB, TB, &full[n_issued], pol);
+      bulk_g2s(stage_ptr(static_cast<int>(n_issued)), p.tiles + (t0 + n_issued) * TB, TB, &full[n_issued], pol);
     }
   }
   fetch_plan(&s_plan, p.plan, c, tid);
@@ -433,83 +469,61 @@ __global__ void __launch_bounds__(gemv_threads<F, M>(), F::kCtasPerSm) gemv_kern
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // Position of tile t0 in the stream, advanced incrementally below.
-  int64_t rt = div_fast(t0, p.nKT);
+  int64_t rt = rt_first;
+  const int nKT = static_cast<int>(p.nKT);
   int kt = static_cast<int>(t0 - rt * p.nKT);
+  const int nt = static_cast<int>(ntiles);
+  const bool stacked = F::kCbEntries > 0 && p.seg_of_rt != nullptr;
+  // k-tile index k (< nKT + 2) reduced into [0, nKT)
+  auto wrap_kt = [nKT](int k) {
+    if (k >= nKT) k -= nKT;
+    if (k >= nKT) k -= nKT;
+    return k;
+  };
   // x of the next tile this warp computes (tile parity: every second tile)
   constexpr int TSTEP = PAR ? 2 : 1;
   const int first = PAR ? half : 0;
   typename F::XRegs xr;
-  if (first < ntiles) F::template load_x<M>(xr, p, static_cast<int>((kt + first) % p.nKT), slice, lane);
+  if (first < nt) F::template load_x<M>(xr, p, wrap_kt(kt + first), slice, lane);
   typename F::XScale xscale;  // per-lane activation scaling, the same for every tile
   F::x_scales(xscale, lane);
 
-  int s = 0;           // stage of the tile being computed
-  uint32_t ph = 0;     // its fill parity
-  int su = static_cast<int>(n_issued % NS);            // next stage to fill
-  uint32_t phu = static_cast<uint32_t>((n_issued / NS) & 1);
-  for (int64_t i = 0; i < ntiles; ++i) {
-    // A new row tile of a stacked handle may use another codebook: rebuild
-    // the table once every warp is done with the old one.
-    if constexpr (F::kCbEntries > 0) {
-      if (p.seg_of_rt != nullptr && kt == 0 && i > 0) {
-        __syncthreads();  // every warp is done with the old table and has read s_seg
-        if (s_seg[1] != s_seg[0]) rebuild_table<F, NT>(fsh, table_of<F>(p, rt), warp, lane);
-        __syncthreads();
-        if (tid == 0) {
-          const int64_t nRT = div_fast(p.T, p.nKT);
-          s_seg[0] = s_seg[1];
-          s_seg[1] = rt + 1 < nRT ? __ldg(p.seg_of_rt + rt + 1) : s_seg[0];
-        }
-      }
+  // A new row tile of a stacked handle may use another codebook: rebuild
+  // the table once every warp is done with the old one.
+  auto next_table = [&]() {
+    __syncthreads();  // every warp is done with the old table and has read s_seg
+    if (s_seg[1] != s_seg[0]) rebuild_table<F, NT>(fsh, table_of<F>(p, rt), warp, lane);
+    __syncthreads();
+    if (tid == 0) {
+      const int64_t nRT = div_fast(p.T, p.nKT);
+      s_seg[0] = s_seg[1];
+      s_seg[1] = rt + 1 < nRT ? __ldg(p.seg_of_rt + rt + 1) : s_seg[0];
     }
-    bool abort = s_abort != 0;
+  };
 
-    // Refill: tile u = i + NS - 1 goes to the stage released by tile
-    // u - NS = i - 1, whose codes every warp loaded one iteration ago.
-    if (elected && !abort && n_issued < ntiles) {
-      if (n_issued >= NS && !mbar_wait_bounded(&empty[su], phu ^ 1)) {
-        atomicOr(p.err, kErrTimeoutEmpty);
-        s_abort = 1;
-        abort = true;
-      } else {
-        mbar_arrive_expect_tx(&full[su], TB);
-        bulk_g2s(ring + su * TB, p.tiles + (t0 + n_issued) * TB, TB, &full[su], pol);
-        ++n_issued;
-        if (++su == NS) { su = 0; phu ^= 1; }
-      }
+  // The warp's part of tile j (stage st, fill parity par): stage its x,
+  // prefetch the x of the warp's next tile (k-tile kt_pref), wait for the
+  // codes, compute.
+  auto compute_tile = [&](int j, int st, uint32_t par, int kt_pref, bool abort) {
+    float xsum[F::kSumGroups][M];
+    __syncwarp();
+    F::template stage_x<M>(xs, xsum, xr, xscale, lane);
+    __syncwarp();
+    if (j + TSTEP < nt) F::template load_x<M>(xr, p, kt_pref, slice, lane);
+    const bool ok = !abort && mbar_wait_bounded(&full[st], par);
+    if (!ok) {
+      if (!abort && lane == 0) atomicOr(p.err, kErrTimeoutFull);
+      s_abort = 1;
+    } else {
+      F::template tile_math<M, RPW>(stage_ptr(st), xs, xsum, acc, fsh, slice, rhalf, lane, &empty[st]);
     }
+  };
 
-    const int kt_next = (kt + 1 == p.nKT) ? 0 : kt + 1;
-    if (!PAR || (i & 1) == half) {
-      // Stage this tile's activations, then prefetch those of the warp's next tile.
-      float xsum[F::kSumGroups][M];
-      __syncwarp();
-      F::template stage_x<M>(xs, xsum, xr, xscale, lane);
-      __syncwarp();
-      if (i + TSTEP < ntiles)
-        F::template load_x<M>(xr, p, PAR ? static_cast<int>((kt + 2) % p.nKT) : kt_next, slice, lane);
-
-      const bool ok = !abort && mbar_wait_bounded(&full[s], ph);
-      if (!ok) {
-        if (!abort && lane == 0) atomicOr(p.err, kErrTimeoutFull);
-        s_abort = 1;
-      } else {
-        F::template tile_math<M, RPW>(ring + s * TB, xs, xsum, acc, fsh, slice, rhalf, lane,
-                                      &empty[s]);
-      }
-    }
-    if (++s == NS) { s = 0; ph ^= 1; }
-
-    const bool row_end = (kt_next == 0) || (i + 1 == ntiles);
-    const int64_t cur_rt = rt;
-    kt = kt_next;
-    if (kt_next == 0) ++rt;
-    if (!row_end) continue;
-
-    // ---- row-tile epilogue: add the slices' partials in slice order ----
+  // Row-tile epilogue: add the slices' partials in slice order; the owner of
+  // a whole row tile writes y, a contributor to a shared one its partials.
+  auto row_epilogue = [&](int64_t cur_rt) {
     acc.flush(red, rslot, rhalf, lane);
     named_bar_sync(1, NT);
-
     const bool owner = (cur_rt * p.nKT >= t0) && ((cur_rt + 1) * p.nKT <= t1);
     const int side = (cur_rt * p.nKT <= t0) ? 0 : 1;
     float* my_part = p.partials + (c * 2 + side) * kPartialStride;
@@ -528,13 +542,95 @@ __global__ void __launch_bounds__(gemv_threads<F, M>(), F::kCtasPerSm) gemv_kern
     }
     named_bar_sync(1, NT);
     acc.reset();
-  }
+  };
 
-  // Never leave while a copy issued by this CTA may still be landing (only
-  // possible after an aborted run; normally every issued tile was consumed).
-  if (elected && s_abort != 0) {
-    for (int64_t u = (n_issued > NS ? n_issued - NS : 0); u < n_issued; ++u)
-      mbar_wait_bounded(&full[u % NS], static_cast<uint32_t>((u / NS) & 1));
+  if constexpr (PAR) {
+    // Tile parity: tile j lives in stage j % NS and is computed by half
+    // j % 2, so (NS even) each half owns every second stage.  Each half runs
+    // its own pipeline over its own tiles: at its tile j its first thread
+    // refills the stage of its tile j - 2 (released one tile ago) with tile
+    // j + NS - 2.  The prologue issued tiles 0 .. NS - 1.  Both halves walk
+    // the run row tile by row tile and meet at each row-tile end.
+    static_assert(NS % 2 == 0 && NS >= 4, "tile parity: each half owns every second stage");
+    const bool leader = (lane == 0) && (slice == 0);
+    const uint64_t lpol = leader ? l2_policy_evict_first() : 0;
+    int u_last = -1;  // leader: last tile of its parity issued (by the prologue or by itself)
+    for (int u = half; u < NS && u < nt; u += 2) u_last = u;
+    int i = 0;  // first tile of the current row tile segment
+    while (i < nt) {
+      if (stacked && i > 0) next_table();
+      const int iend = i + min(nt - i, nKT - kt);
+#pragma unroll 1
+      for (int j = i + ((i ^ half) & 1); j < iend; j += 2) {
+        bool abort = s_abort != 0;
+        const int u = j + NS - 2;
+        if (leader && !abort && j >= 2 && u < nt) {
+          const int su = u % NS;
+          if (!mbar_wait_bounded(&empty[su], static_cast<uint32_t>(((u - NS) / NS) & 1))) {
+            atomicOr(p.err, kErrTimeoutEmpty);
+            s_abort = 1;
+            abort = true;
+          } else {
+            mbar_arrive_expect_tx(&full[su], TB);
+            bulk_g2s(stage_ptr(su), p.tiles + (t0 + u) * TB, TB, &full[su], lpol);
+            u_last = u;
+          }
+        }
+        compute_tile(j, j % NS, static_cast<uint32_t>((j / NS) & 1), wrap_kt(kt + (j - i) + 2), abort);
+      }
+      row_epilogue(rt);
+      i = iend;
+      kt = 0;
+      ++rt;
+    }
+    // Never leave while a copy issued by this half may still be landing
+    // (only possible after an aborted run): wait for the last fill of each
+    // of the half's stages.
+    if (leader && s_abort != 0) {
+      for (int u = u_last; u >= 0 && u > u_last - NS; u -= 2)
+        mbar_wait_bounded(&full[u % NS], static_cast<uint32_t>((u / NS) & 1));
+    }
+  } else {
+    int s = 0;           // stage of the tile being computed
+    uint32_t ph = 0;     // its fill parity
+    int su = static_cast<int>(n_issued % NS);            // next stage to fill
+    uint32_t phu = static_cast<uint32_t>((n_issued / NS) & 1);
+    for (int i = 0; i < nt; ++i) {
+      if (stacked && kt == 0 && i > 0) next_table();
+      bool abort = s_abort != 0;
+
+      // Refill: tile u = i + NS - 1 goes to the stage released by tile
+      // u - NS = i - 1, whose codes every warp loaded one iteration ago.
+      if (elected && !abort && n_issued < ntiles) {
+        if (n_issued >= NS && !mbar_wait_bounded(&empty[su], phu ^ 1)) {
+          atomicOr(p.err, kErrTimeoutEmpty);
+          s_abort = 1;
+          abort = true;
+        } else {
+          mbar_arrive_expect_tx(&full[su], TB);
+          bulk_g2s(stage_ptr(su), p.tiles + (t0 + n_issued) * TB, TB, &full[su], pol);
+          ++n_issued;
+          if (++su == NS) { su = 0; phu ^= 1; }
+        }
+      }
+
+      const int kt_next = (kt + 1 == nKT) ? 0 : kt + 1;
+      compute_tile(i, s, ph, kt_next, abort);
+      if (++s == NS) { s = 0; ph ^= 1; }
+
+      const bool row_end = (kt_next == 0) || (i + 1 == nt);
+      const int64_t cur_rt = rt;
+      kt = kt_next;
+      if (kt_next == 0) ++rt;
+      if (row_end) row_epilogue(cur_rt);
+    }
+
+    // Never leave while a copy issued by this CTA may still be landing (only
+    // possible after an aborted run; normally every issued tile was consumed).
+    if (elected && s_abort != 0) {
+      for (int64_t u = (n_issued > NS ? n_issued - NS : 0); u < n_issued; ++u)
+        mbar_wait_bounded(&full[u % NS], static_cast<uint32_t>((u / NS) & 1));
+    }
   }
 
   // Row tiles shared with other CTAs (at most the first and the last of the
@@ -642,7 +738,12 @@ __device__ __forceinline__ void load_xpair_run(const float* xs, int q0, float2 (
 
 __device__ __forceinline__ void release_stage(uint64_t* empty_bar, int lane) {
   __syncwarp();
-  if (lane == 0) mbar_arrive(empty_bar);
+  // lane 0 arrives (a predicated instruction, no divergent branch)
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.eq.u32 p, %1, 0;\n\t"
+      "@p mbarrier.arrive.shared::cta.b64 _, [%0];\n\t}" ::"r"(smem_u32(empty_bar)),
+      "r"(lane)
+      : "memory");
 }
 
 __device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {

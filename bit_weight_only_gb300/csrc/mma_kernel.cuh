@@ -62,8 +62,6 @@ __host__ __device__ constexpr int mma_red_bytes() { return 4 * 2 * kMmaTiles * N
 // less the window offset of the dynamic area): stage 0, the mbarriers and,
 // for one activation block, the reduction buffer; after it the other stages
 // and, for two blocks, the reduction buffer.
-constexpr int kMmaTableAlign = 65536;
-constexpr int kMmaPreSlack = 4096;  // room left for the window offset of the dynamic area
 template <class F, int NB>
 __host__ __device__ constexpr int mma_bar_bytes() { return 2 * F::mma_stages(NB) * 8; }
 template <class F, int NB>
@@ -78,7 +76,7 @@ template <class F, int NB>
 __host__ __device__ constexpr int mma_smem_bytes() {
   return F::kMmaSharedBytes == 0
              ? F::mma_stages(NB) * F::kTileBytes + mma_red_bytes<NB>() + mma_bar_bytes<F, NB>()
-             : kMmaTableAlign + F::kMmaSharedBytes + mma_post_bytes<F, NB>();
+             : kTableAlign + F::kMmaSharedBytes + mma_post_bytes<F, NB>();
 }
 
 // Address of table entry (byte bsel of w) for the lane: key = (table >> 16)
@@ -221,19 +219,19 @@ __global__ void __launch_bounds__(mma_threads<F, NB>(), F::mma_ctas(NB)) gemv_mm
     fsh = smem;  // unused
     full = reinterpret_cast<uint64_t*>(smem + NS * TB + mma_red_bytes<NB>());
   } else {
-    static_assert(F::kMmaSharedBytes == kMmaTableAlign, "one 64 KB table");
-    static_assert(mma_pre_bytes<F, NB>() + kMmaPreSlack <= kMmaTableAlign, "pre-table layout");
+    static_assert(F::kMmaSharedBytes == kTableAlign, "one 64 KB table");
+    static_assert(mma_pre_bytes<F, NB>() + kTablePreSlack <= kTableAlign, "pre-table layout");
     const uint32_t base = smem_u32(smem);
     uint32_t dyn;
     asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
-    const uint32_t R0 = (base + (kMmaTableAlign - 1)) & ~uint32_t(kMmaTableAlign - 1);
+    const uint32_t R0 = (base + (kTableAlign - 1)) & ~uint32_t(kTableAlign - 1);
     if (R0 - base < uint32_t(mma_pre_bytes<F, NB>()) ||
-        R0 + kMmaTableAlign + mma_post_bytes<F, NB>() > base + dyn) {
+        R0 + kTableAlign + mma_post_bytes<F, NB>() > base + dyn) {
       if (threadIdx.x == 0) atomicOr(p.err, kErrSmemLayout);
       return;
     }
     fsh = smem + (R0 - base);
-    ringN = fsh + kMmaTableAlign;
+    ringN = fsh + kTableAlign;
     full = reinterpret_cast<uint64_t*>(smem + TB);
     red = reinterpret_cast<float4*>(NB == 1 ? smem + TB + mma_bar_bytes<F, NB>() : ringN + (NS - 1) * TB);
     lut_key = (R0 & 0xFFFF0000u) | ((threadIdx.x & 31u) << 2);
