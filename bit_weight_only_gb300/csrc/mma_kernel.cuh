@@ -252,12 +252,12 @@ __global__ void __launch_bounds__(mma_threads<F, NB>(), F::mma_ctas(NB)) gemv_mm
   const int64_t c = blockIdx.x;
   const int64_t t0 = stream_split(c, p.T, G);
   const int64_t t1 = stream_split(c + 1, p.T, G);
-  const int64_t ntiles = t1 - t0;
+  const int ntiles = static_cast<int>(t1 - t0);
   const int64_t rt_first = div_fast(t0, p.nKT);
 
   const bool elected = (tid == 0);
   uint64_t pol = 0;
-  int64_t n_issued = 0;
+  int n_issued = 0;
   if (elected) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(&full[s], 1);
@@ -322,9 +322,11 @@ __global__ void __launch_bounds__(mma_threads<F, NB>(), F::mma_ctas(NB)) gemv_mm
   uint32_t ph = 0;
   int su = static_cast<int>(n_issued % NS);
   uint32_t phu = static_cast<uint32_t>((n_issued / NS) & 1);
-  for (int64_t i = 0; i < ntiles; ++i) {
+  const int nt = ntiles;
+  const bool stacked = F::kCbEntries > 0 && p.seg_of_rt != nullptr;
+  for (int i = 0; i < nt; ++i) {
     if constexpr (F::kCbEntries > 0) {
-      if (p.seg_of_rt != nullptr && kt == 0 && i > 0) {
+      if (stacked && kt == 0 && i > 0) {
         __syncthreads();
         if (s_seg[1] != s_seg[0]) mma_rebuild_table<F, NT>(fsh, table_of<F>(p, rt), warp, lane);
         __syncthreads();
@@ -351,7 +353,7 @@ __global__ void __launch_bounds__(mma_threads<F, NB>(), F::mma_ctas(NB)) gemv_mm
     const int kt_next = (kt + 1 == p.nKT) ? 0 : kt + 1;
     uint32_t xn[PF ? SPW : 1][PF ? NB : 1][PF ? XW : 1];
     if constexpr (PF) {
-      if (i + 1 < ntiles) load_x(xn, kt_next);
+      if (i + 1 < nt) load_x(xn, kt_next);
     } else {
       load_x(xw, kt);
     }
@@ -381,8 +383,7 @@ __global__ void __launch_bounds__(mma_threads<F, NB>(), F::mma_ctas(NB)) gemv_mm
           }
         }
         if (ss == SPW - 1) {
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&empty[s]);
+          release_stage(&empty[s], lane);
         }
 
         // MG m-tiles at a time, their MMAs interleaved so that consecutive
@@ -441,7 +442,7 @@ __global__ void __launch_bounds__(mma_threads<F, NB>(), F::mma_ctas(NB)) gemv_mm
           for (int e = 0; e < XW; ++e) xw[ss][nb][e] = xn[ss][nb][e];
     }
 
-    const bool row_end = (kt_next == 0) || (i + 1 == ntiles);
+    const bool row_end = (kt_next == 0) || (i + 1 == nt);
     const int64_t cur_rt = rt;
     kt = kt_next;
     if (kt_next == 0) ++rt;
@@ -506,7 +507,7 @@ __global__ void __launch_bounds__(mma_threads<F, NB>(), F::mma_ctas(NB)) gemv_mm
   }
 
   if (elected && s_abort != 0) {
-    for (int64_t u = (n_issued > NS ? n_issued - NS : 0); u < n_issued; ++u)
+    for (int u = (n_issued > NS ? n_issued - NS : 0); u < n_issued; ++u)
       mbar_wait_bounded(&full[u % NS], static_cast<uint32_t>((u / NS) & 1));
   }
 
