@@ -390,7 +390,7 @@ def run_ours(args, rank, world, device):
                    "parallelism": f"replicas{world}", "peak_hbm_gbs": peak,
                    "frac_of_peak": round(value / world / peak, 4)},
         "roofline": {"bound": "hbm",
-                     "kernel": (f"aqlm_gemv_kernel<MB={min(M, 2)}> x {-(-M // 2)} passes" if dominant == "aqlm_2x8"
+                     "kernel": (f"aqlm_gemv_kernel<MB={M}>" if dominant == "aqlm_2x8" and M <= 2
                                 else f"gemv_kernel<{dominant}, M=1>" if M == 1
                                 else f"gemv_mma_kernel<{dominant}, NB={1 if M <= 8 else 2}>"),
                      "achieved": round(dom_achieved, 2), "peak": peak, "unit": "GB/s",
@@ -400,7 +400,7 @@ def run_ours(args, rank, world, device):
                      "avg_launch_us": round(dom_ms / K / max(1, dom_launches) * 1e3, 3)},
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": K_e2e},
-        "gpu_launches": sum(-(-M // 2) if o["fmt"] == "aqlm_2x8" else 1 for o in ops) * K,
+        "gpu_launches": len(ops) * K,  # one launch per GEMV (AQLM: one table pass for M <= 2, else the tensor-core kernel)
         "clocks": clocks,
     }
     if not args.no_cpu_baseline and world == 1:

@@ -82,6 +82,14 @@ struct FmtCBK4 {
   // and 2(ks%2)+1 of word ks/2, i.e. k pairs (32h + 8q + 4(ks%2), +1) and
   // (.. + 2, +3) with h = ks/2, each one table read.
   static constexpr int kMmaSharedBytes = kLutBytes;
+  // entry address bits of the lane: table >> 16 in byte 2, lane * 4 in byte 0
+  __device__ static uint32_t mma_lut_key(uint32_t table, int lane) {
+    return (table & 0xFFFF0000u) | (static_cast<uint32_t>(lane) << 2);
+  }
+  static constexpr int kMmaRowWords = 2;   // words q of the two 16-byte halves
+  static constexpr int kMmaCodebooks = 1;
+  static constexpr bool kMmaRowScales = false;
+  __device__ static const __half* mma_row_scales(const GemvParams&) { return nullptr; }
   static constexpr int kMmaBlockSteps = 0;
   struct MmaScales {};  // no block scale
   static constexpr int kMmaXWords = 8;  // x[m][32h + 8q .. +7], h = 0, 1
@@ -97,7 +105,7 @@ struct FmtCBK4 {
   __device__ static void mma_load_row(const uint8_t* stage, int slice, int l, int j, int q, uint32_t (&w)[2]) {
     mma_row_words(stage, slice, l, j, q, w);
   }
-  __device__ static uint2 mma_frag(const uint32_t (&w)[2], int ks, uint32_t lut_key) {
+  __device__ static uint2 mma_frag(const uint32_t (&w)[2], int ks, uint32_t lut_key, int) {
     const uint32_t wd = w[ks >> 1];
     const int b = 2 * (ks & 1);
     return make_uint2(lds32_at(lut_addr(wd, lut_key, b)), lds32_at(lut_addr(wd, lut_key, b + 1)));
@@ -240,6 +248,14 @@ struct FmtCBK8 {
   // 16h + 4q .. +3); k16 step ks takes word ks: k pairs (16ks + 4q, +1) and
   // (16ks + 4q + 2, +3).
   static constexpr int kMmaSharedBytes = kLutBytes;
+  // entry address bits of the lane: table >> 16 in byte 2, lane * 4 in byte 0
+  __device__ static uint32_t mma_lut_key(uint32_t table, int lane) {
+    return (table & 0xFFFF0000u) | (static_cast<uint32_t>(lane) << 2);
+  }
+  static constexpr int kMmaRowWords = 2;   // words q of the two 16-byte halves
+  static constexpr int kMmaCodebooks = 1;
+  static constexpr bool kMmaRowScales = false;
+  __device__ static const __half* mma_row_scales(const GemvParams&) { return nullptr; }
   static constexpr int kMmaBlockSteps = 0;
   struct MmaScales {};  // no block scale
   static constexpr int kMmaXWords = 4;  // x[m][16h + 4q .. +3], h = 0, 1
@@ -264,7 +280,7 @@ struct FmtCBK8 {
   __device__ static void mma_load_row(const uint8_t* stage, int slice, int l, int j, int q, uint32_t (&w)[2]) {
     mma_row_words(stage, slice, l, j, q, w);
   }
-  __device__ static uint2 mma_frag(const uint32_t (&w)[2], int ks, uint32_t lut_key) {
+  __device__ static uint2 mma_frag(const uint32_t (&w)[2], int ks, uint32_t lut_key, int) {
     const uint32_t wd = w[ks];
     const uint32_t c0 = lds32_at(lut_addr(wd, lut_key, 0)), c1 = lds32_at(lut_addr(wd, lut_key, 1));
     const uint32_t c2 = lds32_at(lut_addr(wd, lut_key, 2)), c3 = lds32_at(lut_addr(wd, lut_key, 3));

@@ -78,6 +78,10 @@ struct FmtQ4_0 {
   // (2sub + 1, 2sub + 5) of that word: one LOP3 makes each pair 1024 + code
   // (or 1024 + 16 code) as fp16, one HFMA2 turns it into code - 8, exactly.
   static constexpr int kMmaSharedBytes = 0;
+  static constexpr int kMmaRowWords = 2;   // words q of the two 16-byte halves
+  static constexpr int kMmaCodebooks = 1;
+  static constexpr bool kMmaRowScales = false;
+  __device__ static const __half* mma_row_scales(const GemvParams&) { return nullptr; }
   static constexpr int kMmaBlockSteps = 2;
   static constexpr int kMmaXWords = 8;  // x[m][32b + 8q .. +7], b = 0, 1
   // two slices per warp, eight warps per CTA, two CTAs per SM, two stages each
@@ -96,7 +100,7 @@ struct FmtQ4_0 {
     d.h2 = *reinterpret_cast<const uint32_t*>(stage + kCodeBytes + (t * 4 + j) * 4);
   }
   __device__ static float mma_scale(const MmaScales& d, int blk) { return h2f(blk ? d.h2 >> 16 : d.h2 & 0xFFFFu); }
-  __device__ static uint2 mma_frag(const uint32_t (&w)[2], int ks, uint32_t) {
+  __device__ static uint2 mma_frag(const uint32_t (&w)[2], int ks, uint32_t, int) {
     const uint32_t wd = (ks & 1) ? (w[ks >> 1] >> 8) : w[ks >> 1];
     return make_uint2(hfma2_u32(field_pair(wd, 0x000F000Fu), 0x3C003C00u, 0xE408E408u),   // x1 - 1032
                       hfma2_u32(field_pair(wd, 0x00F000F0u), 0x2C002C00u, 0xD480D480u));  // /16 - 72
@@ -247,6 +251,10 @@ struct FmtPQ2 {
   // right by 8 when f >= 4: one LOP3 gives 1024 + 4^f' c per half as fp16,
   // one HFMA2 (times 4^-f', minus 1024 4^-f' + 1) gives c - 1, exactly.
   static constexpr int kMmaSharedBytes = 0;
+  static constexpr int kMmaRowWords = 2;   // words q of the two 16-byte halves
+  static constexpr int kMmaCodebooks = 1;
+  static constexpr bool kMmaRowScales = false;
+  __device__ static const __half* mma_row_scales(const GemvParams&) { return nullptr; }
   static constexpr int kMmaBlockSteps = 8;
   static constexpr int kMmaXWords = 16;  // x[m][64h + 16q .. +15], h = 0, 1
   // One slice per warp, sixteen warps, one CTA per SM for every M: two
@@ -255,7 +263,7 @@ struct FmtPQ2 {
   __host__ __device__ static constexpr int mma_spw(int) { return 1; }
   __host__ __device__ static constexpr int mma_ctas(int) { return 1; }
   __host__ __device__ static constexpr int mma_stages(int) { return 5; }
-  __host__ __device__ static constexpr bool mma_prefetch_x(int) { return false; }  // registers
+  __host__ __device__ static constexpr bool mma_prefetch_x(int nb) { return nb == 1; }  // registers
   template <int NT>
   __device__ static void mma_init_shared(uint8_t*, const uint16_t*, int, int) {}
   __device__ static void mma_load_row(const uint8_t* stage, int slice, int l, int j, int q, uint32_t (&w)[2]) {
@@ -274,7 +282,7 @@ struct FmtPQ2 {
     const uint32_t src = f >= 4 ? (w >> 8) : w;
     return hfma2_u32(field_pair(src, 0x00030003u << (2 * fp)), kScale[fp], kOff[fp]);
   }
-  __device__ static uint2 mma_frag(const uint32_t (&w)[2], int ks, uint32_t) {
+  __device__ static uint2 mma_frag(const uint32_t (&w)[2], int ks, uint32_t, int) {
     const uint32_t wd = w[ks >> 2];
     const int sub = ks & 3;
     return make_uint2(pq2_pair(wd, 2 * sub), pq2_pair(wd, 2 * sub + 1));

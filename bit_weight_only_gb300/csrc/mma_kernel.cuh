@@ -31,10 +31,16 @@
 //     fixed tree order through shared memory, then stored to y or to the
 //     stream-K partial slots.
 //
+//   * Additive formats (AQLM 2x8) make one A fragment per codebook and one
+//     MMA each into the same accumulator; a per-row output scale is applied
+//     when the row's sum is stored.
+//
 // Format hooks (members of the format struct): mma_stages(NB),
 // mma_prefetch_x(NB), kMmaSharedBytes, kMmaBlockSteps (0: no scale), kMmaXWords,
-// mma_init_shared, mma_load_row, mma_frag, mma_load_x, mma_bfrag and, with
-// a scale, MmaScales, mma_scales and mma_scale.
+// kMmaRowWords (code words per fragment row and slice), kMmaCodebooks,
+// kMmaRowScales (and mma_row_scales), mma_init_shared, mma_lut_key (table
+// formats), mma_load_row, mma_frag, mma_load_x, mma_bfrag and, with a block
+// scale, MmaScales, mma_scales and mma_scale.
 #pragma once
 
 #include "gemv_kernel.cuh"
@@ -213,7 +219,7 @@ __global__ void __launch_bounds__(mma_threads<F, NB>(), F::mma_ctas(NB)) gemv_mm
   float4* red;
   uint8_t* fsh;
   uint64_t* full;
-  uint32_t lut_key = 0;  // table formats: (table >> 16) << 16 | lane * 4
+  uint32_t lut_key = 0;  // table formats: the lane's entry address bits (F::mma_lut_key)
   if constexpr (F::kMmaSharedBytes == 0) {
     red = reinterpret_cast<float4*>(smem + NS * TB);
     fsh = smem;  // unused
@@ -234,7 +240,7 @@ __global__ void __launch_bounds__(mma_threads<F, NB>(), F::mma_ctas(NB)) gemv_mm
     ringN = fsh + kTableAlign;
     full = reinterpret_cast<uint64_t*>(smem + TB);
     red = reinterpret_cast<float4*>(NB == 1 ? smem + TB + mma_bar_bytes<F, NB>() : ringN + (NS - 1) * TB);
-    lut_key = (R0 & 0xFFFF0000u) | ((threadIdx.x & 31u) << 2);
+    lut_key = F::mma_lut_key(R0, static_cast<int>(threadIdx.x & 31u));
   }
   uint64_t* empty = full + NS;
   auto stage_ptr = [&](int64_t s) { return s == 0 ? ring0 : ringN + (s - 1) * TB; };
@@ -369,7 +375,7 @@ __global__ void __launch_bounds__(mma_threads<F, NB>(), F::mma_ctas(NB)) gemv_mm
         const int slice = sgrp * SPW + ss;
         // codes (and scales) of the thread's eight rows in this slice; after
         // the warp's last slice, release the stage
-        uint32_t w[kMmaTiles][2][2];
+        uint32_t w[kMmaTiles][2][F::kMmaRowWords];
         typename F::MmaScales d[kMmaTiles][2];  // block scales of the rows, read per block
 #pragma unroll
         for (int mt = 0; mt < kMmaTiles; ++mt) {
@@ -397,21 +403,28 @@ __global__ void __launch_bounds__(mma_threads<F, NB>(), F::mma_ctas(NB)) gemv_mm
             float tmp[MG][NB][4];  // block sums (block formats); the first MMA writes them
 #pragma unroll
             for (int ks = blk * (BS > 0 ? BS : KS); ks < (blk + 1) * (BS > 0 ? BS : KS); ++ks) {
+              // one A fragment per codebook (additive formats sum two); the
+              // codebook loop is outside the m-tile loop so that MMAs into
+              // the same accumulator are not adjacent
 #pragma unroll
-              for (int mi = 0; mi < MG; ++mi) {
-                const int mt = mg + mi;
-                const uint2 r0 = F::mma_frag(w[mt][0], ks, lut_key);  // row gi: (k lo pair, k hi pair)
-                const uint2 r1 = F::mma_frag(w[mt][1], ks, lut_key);  // row gi + 8
+              for (int cb = 0; cb < F::kMmaCodebooks; ++cb) {
 #pragma unroll
-                for (int nb = 0; nb < NB; ++nb) {
-                  const uint2 bf = F::mma_bfrag(xw[ss][nb], ks);
-                  if constexpr (BS > 0) {
-                    if (ks == blk * BS)
-                      mma_16816_c0(tmp[mi][nb], r0.x, r1.x, r0.y, r1.y, bf.x, bf.y);
-                    else
-                      mma_16816(tmp[mi][nb], r0.x, r1.x, r0.y, r1.y, bf.x, bf.y);
-                  } else
-                    mma_16816(acc[mt][nb], r0.x, r1.x, r0.y, r1.y, bf.x, bf.y);
+                for (int mi = 0; mi < MG; ++mi) {
+                  const int mt = mg + mi;
+                  const uint2 r0 = F::mma_frag(w[mt][0], ks, lut_key, cb);  // row gi: (k lo pair, k hi pair)
+                  const uint2 r1 = F::mma_frag(w[mt][1], ks, lut_key, cb);  // row gi + 8
+#pragma unroll
+                  for (int nb = 0; nb < NB; ++nb) {
+                    const uint2 bf = F::mma_bfrag(xw[ss][nb], ks);
+                    if constexpr (BS > 0) {
+                      static_assert(BS == 0 || F::kMmaCodebooks == 1, "block scales with one codebook");
+                      if (ks == blk * BS)
+                        mma_16816_c0(tmp[mi][nb], r0.x, r1.x, r0.y, r1.y, bf.x, bf.y);
+                      else
+                        mma_16816(tmp[mi][nb], r0.x, r1.x, r0.y, r1.y, bf.x, bf.y);
+                    } else
+                      mma_16816(acc[mt][nb], r0.x, r1.x, r0.y, r1.y, bf.x, bf.y);
+                  }
                 }
               }
             }
@@ -491,7 +504,12 @@ __global__ void __launch_bounds__(mma_threads<F, NB>(), F::mma_ctas(NB)) gemv_mm
             if (m < M) {
               if (owner) {
                 const int64_t n = cur_rt * kTileRows + r;
-                if (n < p.N) p.y[m * p.N + n] = acc[mt][nb][e];
+                if (n < p.N) {
+                  if constexpr (F::kMmaRowScales)
+                    p.y[m * p.N + n] = __half2float(F::mma_row_scales(p)[n]) * acc[mt][nb][e];
+                  else
+                    p.y[m * p.N + n] = acc[mt][nb][e];
+                }
               } else {
                 st_relaxed_f32(my_part + m * kTileRows + r, acc[mt][nb][e]);
               }
@@ -515,7 +533,9 @@ __global__ void __launch_bounds__(mma_threads<F, NB>(), F::mma_ctas(NB)) gemv_mm
   static_assert(mma_red_bytes<NB>() >= 2 * NT * 4, "finishing scratch");
   float* s_sub = reinterpret_cast<float*>(red);
   wait_plan();
-  finish_all<kTileRows, 8 * NB, NT>(p, kPartialStride, s_plan, nullptr, 1.0f, s_sub, tid, M);
+  const __half* row_scales = nullptr;  // per-row output scales (F::kMmaRowScales), applied at the finish
+  if constexpr (F::kMmaRowScales) row_scales = F::mma_row_scales(p);
+  finish_all<kTileRows, 8 * NB, NT>(p, kPartialStride, s_plan, row_scales, 1.0f, s_sub, tid, M);
 }
 
 }  // namespace qgemv

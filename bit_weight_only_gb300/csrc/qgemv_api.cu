@@ -21,6 +21,11 @@
 namespace {
 
 constexpr uint32_t kMagic = 0x51474d56u;  // "QGMV"
+// Internal format id: the tensor-core layout of an AQLM 2x8 matrix, held by
+// every AQLM handle next to its table-path layout and used from
+// kAqlmMmaMinM activation rows on (and for every M in batch-invariant mode).
+constexpr int kAqlmMma = 6;
+constexpr int kAqlmMmaMinM = 3;
 
 thread_local char g_msg[512] = "";
 thread_local int g_code = QGEMV_OK;
@@ -51,6 +56,7 @@ const qgemv::FormatOps* ops_for(int format) {
     case QGEMV_CBK4: return qgemv::ops_cbk4();
     case QGEMV_CBK8: return qgemv::ops_cbk8();
     case QGEMV_AQLM_2X8: return qgemv::ops_aqlm();
+    case kAqlmMma: return qgemv::ops_aqlm_mma();
   }
   return nullptr;
 }
@@ -63,17 +69,19 @@ int64_t k_multiple(int format) {
     case QGEMV_CBK8: return 1;
     case QGEMV_PQ2_0: return 128;
     case QGEMV_AQLM_2X8: return 8;
+    case kAqlmMma: return 8;
   }
   return 0;
 }
 
-int64_t scales_count(int format, int64_t N) { return format == QGEMV_AQLM_2X8 ? N : 0; }
+int64_t scales_count(int format, int64_t N) { return format == QGEMV_AQLM_2X8 || format == kAqlmMma ? N : 0; }
 
 int64_t codebook_count(int format) {
   switch (format) {
     case QGEMV_CBK4: return 16;
     case QGEMV_CBK8: return 256;
     case QGEMV_AQLM_2X8: return 2 * 256 * 8;
+    case kAqlmMma: return 2 * 256 * 8;
   }
   return 0;
 }
@@ -195,6 +203,7 @@ struct qgemv_ctx {
   int* err;
   int batch_invariant;  // qgemv_set_batch_invariant
   int skip_cta;         // QGEMV_FAULT_SKIP_CTA test hook, -1 normally
+  qgemv_ctx* mma;       // AQLM: the tensor-core companion (format kAqlmMma), else nullptr
 };
 
 extern "C" {
@@ -214,10 +223,23 @@ int64_t qgemv_packed_bytes(int format, int64_t N, int64_t K) {
 
 }  // extern "C"
 
+static int64_t canonical_bytes(int format, int64_t N, int64_t K) {
+  return qgemv_packed_bytes(format == kAqlmMma ? QGEMV_AQLM_2X8 : format, N, K);
+}
+
+extern "C" {
+
+}  // extern "C"
+
+static void free_handle(qgemv_ctx* h);
+
 // Both create calls: `nseg` codebooks for the row segments `seg_rows`
-// (one segment covering all N rows for qgemv_create).
+// (one segment covering all N rows for qgemv_create).  `nested`: the
+// companion of an AQLM handle, created within the same create call (the
+// allocation fault counter keeps counting).
 static qgemv_handle create_impl(int format, int64_t N, int64_t K, const void* packed, const void* scales,
-                                const void* codebooks, int nseg, const int64_t* seg_rows) {
+                                const void* codebooks, int nseg, const int64_t* seg_rows,
+                                bool nested = false) {
   const qgemv::FormatOps* ops = ops_for(format);
   if (k_multiple(format) == 0) {
     set_error(QGEMV_ERR_ARG, "unknown format %d", format);
@@ -271,8 +293,10 @@ static qgemv_handle create_impl(int format, int64_t N, int64_t K, const void* pa
   }
   h->magic = kMagic;
   h->skip_cta = env_int("QGEMV_FAULT_SKIP_CTA", -1);
-  g_alloc_count = 0;
-  g_alloc_fail = env_int("QGEMV_FAULT_ALLOC", 0);
+  if (!nested) {
+    g_alloc_count = 0;
+    g_alloc_fail = env_int("QGEMV_FAULT_ALLOC", 0);
+  }
   h->format = format;
   h->N = N;
   h->K = K;
@@ -321,7 +345,7 @@ static qgemv_handle create_impl(int format, int64_t N, int64_t K, const void* pa
     return nullptr;
   };
 
-  e = to_device(packed, static_cast<size_t>(qgemv_packed_bytes(format, N, K)), &d_packed);
+  e = to_device(packed, static_cast<size_t>(canonical_bytes(format, N, K)), &d_packed);
   if (e == cudaSuccess) e = to_device(scales, 2 * scales_count(format, N), &d_scales);
   if (e == cudaSuccess) e = to_device(codebooks, 2 * codebook_count(format) * nseg, &d_cb);
   if (e != cudaSuccess) return cleanup(QGEMV_ERR_CUDA, "copying the canonical inputs", e);
@@ -377,6 +401,13 @@ static qgemv_handle create_impl(int format, int64_t N, int64_t K, const void* pa
   cudaFree(d_packed);
   cudaFree(d_scales);
   cudaFree(d_cb);
+  if (format == QGEMV_AQLM_2X8) {
+    h->mma = create_impl(kAqlmMma, N, K, packed, scales, codebooks, 1, seg_rows, true);
+    if (!h->mma) {  // the error is set
+      free_handle(h);
+      return nullptr;
+    }
+  }
   ok();
   return h;
 }
@@ -385,6 +416,10 @@ extern "C" {
 
 qgemv_handle qgemv_create(int format, int64_t N, int64_t K, const void* packed, const void* scales,
                           const void* codebooks) {
+  if (format == kAqlmMma) {
+    set_error(QGEMV_ERR_ARG, "unknown format %d", format);
+    return nullptr;
+  }
   const int64_t rows[1] = {N};
   return create_impl(format, N, K, packed, scales, codebooks, 1, rows);
 }
@@ -396,7 +431,7 @@ qgemv_handle qgemv_create_stacked(int format, int nseg, const int64_t* seg_rows,
     set_error(QGEMV_ERR_ARG, "unknown format %d", format);
     return nullptr;
   }
-  if (format == QGEMV_AQLM_2X8) {
+  if (format == QGEMV_AQLM_2X8 || format == kAqlmMma) {
     set_error(QGEMV_ERR_ARG, "format %d cannot be stacked", format);
     return nullptr;
   }
@@ -424,6 +459,8 @@ int qgemv_run(qgemv_handle h, const void* x, int M, float* y, void* stream) {
   if (!x || !y) return set_error(QGEMV_ERR_ARG, "x or y is NULL");
   if ((reinterpret_cast<uintptr_t>(x) & 3) || (reinterpret_cast<uintptr_t>(y) & 3))
     return set_error(QGEMV_ERR_ALIGN, "x and y must be 4-byte aligned");
+  const bool inv = h->batch_invariant != 0;
+  if (h->mma && (M >= kAqlmMmaMinM || inv)) h = h->mma;  // AQLM: the tensor-core layout
   qgemv::GemvParams p;
   p.tiles = h->tiles;
   p.x = static_cast<const __half*>(x);
@@ -439,7 +476,7 @@ int qgemv_run(qgemv_handle h, const void* x, int M, float* y, void* stream) {
   p.nKT = h->nKT;
   p.skip_cta = h->skip_cta;
   const qgemv::LaunchGeom g = {h->grid, h->plan, h->grid_m1, h->plan_m1};
-  cudaError_t e = h->ops->launch(M, p, g, static_cast<cudaStream_t>(stream), h->batch_invariant != 0);
+  cudaError_t e = h->ops->launch(M, p, g, static_cast<cudaStream_t>(stream), inv);
   if (e != cudaSuccess) return cuda_error(e, "launching the GEMV kernel");
   return ok();
 }
@@ -472,14 +509,20 @@ int qgemv_status(qgemv_handle h) {
   if (!valid(h)) return set_error(QGEMV_ERR_ARG, "invalid handle");
   cudaError_t e = cudaDeviceSynchronize();
   int err = 0;
-  if (e == cudaSuccess) e = cudaMemcpy(&err, h->err, sizeof(int), cudaMemcpyDeviceToHost);
+  for (qgemv_ctx* k = h; k != nullptr && e == cudaSuccess; k = k->mma) {  // the handle and its companion
+    int ek = 0;
+    e = cudaMemcpy(&ek, k->err, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && ek) {
+      // A run that gave up may have left partial slots written but unread.
+      cudaMemset(k->partials, 0xff,
+                 sizeof(float) * 2 * k->ops->partial_stride *
+                     static_cast<size_t>(k->grid > k->grid_m1 ? k->grid : k->grid_m1));
+      cudaMemset(k->err, 0, sizeof(int));
+      err |= ek;
+    }
+  }
   if (e != cudaSuccess) return cuda_error(e, "reading the kernel status");
   if (err) {
-    // A run that gave up may have left partial slots written but unread.
-    cudaMemset(h->partials, 0xff,
-               sizeof(float) * 2 * h->ops->partial_stride *
-                   static_cast<size_t>(h->grid > h->grid_m1 ? h->grid : h->grid_m1));
-    cudaMemset(h->err, 0, sizeof(int));
     if (err & 4)
       return set_error(QGEMV_ERR_CUDA, "a kernel found its shared-memory window unusable (code %d)", err);
     return set_error(QGEMV_ERR_TIMEOUT, "a kernel gave up a bounded wait (code %d)", err);
@@ -490,13 +533,7 @@ int qgemv_status(qgemv_handle h) {
 void qgemv_destroy(qgemv_handle h) {
   if (!valid(h)) return;
   cudaDeviceSynchronize();
-  cudaFree(h->tiles);
-  cudaFree(h->aux);
-  cudaFree(h->partials);
-  cudaFree(h->plan);
-  cudaFree(h->err);
-  h->magic = 0;
-  delete h;
+  free_handle(h);
 }
 
 int qgemv_stream_k_plan(int64_t units, int grid, int64_t units_per_row_tile, int rows, int64_t* out) {
@@ -524,3 +561,15 @@ const char* qgemv_last_error(void) { return g_msg; }
 int qgemv_last_error_code(void) { return g_code; }
 
 }  // extern "C"
+
+// A handle's device buffers, its companion's, and the handle itself.
+static void free_handle(qgemv_ctx* h) {
+  if (h->mma) free_handle(h->mma);
+  cudaFree(h->tiles);
+  cudaFree(h->aux);
+  cudaFree(h->partials);
+  cudaFree(h->plan);
+  cudaFree(h->err);
+  h->magic = 0;
+  delete h;
+}
