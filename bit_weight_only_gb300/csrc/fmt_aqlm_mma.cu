@@ -59,8 +59,10 @@ struct FmtAQLM {
   static constexpr int kMmaXWords = 16;  // x[m][16 ks + 4q .. +3], ks = 0..7
   __host__ __device__ static constexpr int mma_spw(int) { return 1; }
   __host__ __device__ static constexpr int mma_ctas(int) { return 1; }
+  // one activation block: tile parity (two halves of eight warps, alternate tiles)
+  __host__ __device__ static constexpr bool mma_par(int nb) { return nb == 1; }
   __host__ __device__ static constexpr int mma_stages(int nb) { return nb == 1 ? 4 : 3; }
-  __host__ __device__ static constexpr bool mma_prefetch_x(int nb) { return nb == 1; }  // registers
+  __host__ __device__ static constexpr bool mma_prefetch_x(int) { return false; }  // registers (no gain measured)
 
   // table >> 16 in byte 2; (gi & 3) * 32 + q * 8 in byte 0 (codebook 1: + 128)
   __device__ static uint32_t mma_lut_key(uint32_t table, int lane) {
@@ -192,33 +194,35 @@ cudaError_t dequant(const uint8_t* tiles, const void* aux, const int32_t*, int64
   return cudaGetLastError();
 }
 
-template <int NB>
+template <int NB, bool PAR = false>
 cudaError_t launch_nb(const GemvParams& p, int M, const LaunchGeom& g, cudaStream_t s) {
-  static_assert(mma_smem_bytes<F, NB>() + 2048 <= 228 * 1024, "shared memory budget exceeded");
+  static_assert(mma_smem_bytes<F, NB, PAR>() + 2048 <= 228 * 1024, "shared memory budget exceeded");
   GemvParams q = p;
   q.plan = g.plan;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(g.grid);
-  cfg.blockDim = dim3(mma_threads<F, NB>());
-  cfg.dynamicSmemBytes = mma_smem_bytes<F, NB>();
+  cfg.blockDim = dim3(mma_threads<F, NB, PAR>());
+  cfg.dynamicSmemBytes = mma_smem_bytes<F, NB, PAR>();
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemv_mma_kernel<F, NB>, q, M);
+  return cudaLaunchKernelEx(&cfg, gemv_mma_kernel<F, NB, PAR>, q, M);
 }
 
-// Every M runs the same instruction sequence per activation row (one B
-// column each), so a row's bits do not depend on M.
-cudaError_t launch(int M, const GemvParams& p, const LaunchGeom& g, cudaStream_t s, bool) {
-  if (M >= 1 && M <= 8) return launch_nb<1>(p, M, g, s);
+// Batch-invariant mode: every M runs the default geometry, the same
+// instruction sequence per activation row (one B column each), so a row's
+// bits do not depend on M.  Otherwise one activation block runs the
+// tile-parity geometry.
+cudaError_t launch(int M, const GemvParams& p, const LaunchGeom& g, cudaStream_t s, bool batch_invariant) {
+  if (M >= 1 && M <= 8) return batch_invariant ? launch_nb<1>(p, M, g, s) : launch_nb<1, true>(p, M, g, s);
   if (M > 8 && M <= kMaxM) return launch_nb<2>(p, M, g, s);
   return cudaErrorInvalidValue;
 }
 
-int smem_bytes(int M) { return M <= 8 ? mma_smem_bytes<F, 1>() : mma_smem_bytes<F, 2>(); }
+int smem_bytes(int M) { return M <= 8 ? mma_smem_bytes<F, 1, true>() : mma_smem_bytes<F, 2>(); }
 
 cudaError_t setup() {
   cudaError_t e = cudaFuncSetAttribute(gemv_mma_kernel<F, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -226,6 +230,9 @@ cudaError_t setup() {
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(gemv_mma_kernel<F, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              mma_smem_bytes<F, 2>());
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(gemv_mma_kernel<F, 1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             mma_smem_bytes<F, 1, true>());
   return e;
 }
 

@@ -96,6 +96,8 @@ struct FmtCBK4 {
   // one slice per warp, sixteen warps per CTA; the 64 KB table fits once per SM
   __host__ __device__ static constexpr int mma_spw(int) { return 1; }
   __host__ __device__ static constexpr int mma_ctas(int) { return 1; }
+  // one activation block: tile parity (two halves of eight warps, alternate tiles)
+  __host__ __device__ static constexpr bool mma_par(int nb) { return nb == 1; }
   __host__ __device__ static constexpr int mma_stages(int nb) { return nb == 1 ? 4 : 3; }
   __host__ __device__ static constexpr bool mma_prefetch_x(int) { return true; }
   template <int NT>
@@ -262,6 +264,8 @@ struct FmtCBK8 {
   // one slice per warp, sixteen warps per CTA; the 64 KB table fits once per SM
   __host__ __device__ static constexpr int mma_spw(int) { return 1; }
   __host__ __device__ static constexpr int mma_ctas(int) { return 1; }
+  // one activation block: tile parity (two halves of eight warps, alternate tiles)
+  __host__ __device__ static constexpr bool mma_par(int nb) { return nb == 1; }
   __host__ __device__ static constexpr int mma_stages(int nb) { return nb == 1 ? 4 : 3; }
   __host__ __device__ static constexpr bool mma_prefetch_x(int) { return true; }
   template <int NT>

@@ -87,6 +87,7 @@ struct FmtQ4_0 {
   // two slices per warp, eight warps per CTA, two CTAs per SM, two stages each
   __host__ __device__ static constexpr int mma_spw(int) { return 2; }
   __host__ __device__ static constexpr int mma_ctas(int) { return 2; }
+  __host__ __device__ static constexpr bool mma_par(int) { return false; }  // two CTAs per SM instead
   __host__ __device__ static constexpr int mma_stages(int) { return 2; }
   __host__ __device__ static constexpr bool mma_prefetch_x(int nb) { return nb == 1; }
   template <int NT>
@@ -262,6 +263,8 @@ struct FmtPQ2 {
   // one geometry for all M keeps the summation order (batch invariance).
   __host__ __device__ static constexpr int mma_spw(int) { return 1; }
   __host__ __device__ static constexpr int mma_ctas(int) { return 1; }
+  // tile parity measured 2-5% slower for PQ2_0 (M = 2 and 8): not used
+  __host__ __device__ static constexpr bool mma_par(int) { return false; }
   __host__ __device__ static constexpr int mma_stages(int) { return 5; }
   __host__ __device__ static constexpr bool mma_prefetch_x(int nb) { return nb == 1; }  // registers
   template <int NT>

@@ -46,25 +46,28 @@ struct LaunchTable {
   }
 
   // The tensor-core kernel runs F::mma_ctas(NB) CTAs per SM: 1 (grid, plan)
-  // or as many as the M = 1 kernel (grid_m1, plan_m1).
-  template <int NB>
+  // or as many as the M = 1 kernel (grid_m1, plan_m1).  PAR: the tile-parity
+  // geometry (F::mma_par), used for one activation block outside
+  // batch-invariant mode.
+  template <int NB, bool PAR = false>
   static cudaError_t launch_mma(const GemvParams& p, int M, const LaunchGeom& g, cudaStream_t s) {
     static_assert(F::mma_ctas(NB) == 1 || F::mma_ctas(NB) == F::kCtasPerSm, "tensor-core grid");
-    // batch invariance: both activation-block counts use one geometry
+    // batch invariance: both activation-block counts of the default geometry
+    // are the same geometry
     static_assert(F::mma_ctas(1) == F::mma_ctas(2) && F::mma_spw(1) == F::mma_spw(2), "one geometry for all M");
-    static_assert(F::mma_ctas(NB) * (mma_smem_bytes<F, NB>() + 2048) <= 228 * 1024,
+    static_assert(F::mma_ctas(NB) * (mma_smem_bytes<F, NB, PAR>() + 2048) <= 228 * 1024,
                   "shared memory budget exceeded");
     GemvParams q = p;
     q.plan = F::mma_ctas(NB) == 1 ? g.plan : g.plan_m1;
     const int grid = F::mma_ctas(NB) == 1 ? g.grid : g.grid_m1;
     cudaLaunchAttribute attr[1];
-    const cudaLaunchConfig_t cfg = config(grid, mma_threads<F, NB>(), mma_smem_bytes<F, NB>(), s, attr);
-    return cudaLaunchKernelEx(&cfg, gemv_mma_kernel<F, NB>, q, M);
+    const cudaLaunchConfig_t cfg = config(grid, mma_threads<F, NB, PAR>(), mma_smem_bytes<F, NB, PAR>(), s, attr);
+    return cudaLaunchKernelEx(&cfg, gemv_mma_kernel<F, NB, PAR>, q, M);
   }
 
   static int smem_bytes(int M) {
     if (M == 1) return gemv_smem_bytes<F, 1>();
-    if (M >= 2 && M <= 8) return mma_smem_bytes<F, 1>();
+    if (M >= 2 && M <= 8) return F::mma_par(1) ? mma_smem_bytes<F, 1, true>() : mma_smem_bytes<F, 1>();
     if (M > 8 && M <= kMaxM) return mma_smem_bytes<F, 2>();
     return 0;
   }
@@ -76,6 +79,11 @@ struct LaunchTable {
       e = cudaFuncSetAttribute(gemv_mma_kernel<F, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, mma_smem_bytes<F, 1>());
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(gemv_mma_kernel<F, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, mma_smem_bytes<F, 2>());
+    if constexpr (F::mma_par(1)) {
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(gemv_mma_kernel<F, 1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 mma_smem_bytes<F, 1, true>());
+    }
     return e;
   }
 
@@ -86,7 +94,12 @@ struct LaunchTable {
       q.plan = g.plan_m1;
       return launch_m1(q, g.grid_m1, s);
     }
-    if (M >= 1 && M <= 8) return launch_mma<1>(q, M, g, s);
+    if (M >= 1 && M <= 8) {
+      if constexpr (F::mma_par(1)) {
+        if (!batch_invariant) return launch_mma<1, true>(q, M, g, s);
+      }
+      return launch_mma<1>(q, M, g, s);
+    }
     if (M > 8 && M <= kMaxM) return launch_mma<2>(q, M, g, s);
     return cudaErrorInvalidValue;
   }

@@ -48,13 +48,19 @@
 namespace qgemv {
 
 constexpr int kMmaTiles = 4;  // 16-row m-tiles per warp
-// Warps per CTA: two per group of F::mma_spw(NB) k-slices (one slice per
-// warp: 16 warps, one CTA per SM; two slices per warp: 8 warps, two CTAs per
-// SM, F::mma_ctas(NB)).
-template <class F, int NB>
-__host__ __device__ constexpr int mma_warps() { return 2 * kSlices / F::mma_spw(NB); }
-template <class F, int NB>
-__host__ __device__ constexpr int mma_threads() { return 32 * mma_warps<F, NB>(); }
+// Geometry.  Default: two warps per group of F::mma_spw(NB) k-slices (one
+// slice per warp: 16 warps, one CTA per SM; two slices per warp: 8 warps, two
+// CTAs per SM, F::mma_ctas(NB)).  Tile parity (PAR; one-CTA-per-SM formats):
+// 16 warps in two halves that take alternate tiles, each half eight warps of
+// two slices each, with four stages (two per half).
+template <class F, int NB, bool PAR = false>
+__host__ __device__ constexpr int mma_spw_of() { return PAR ? 2 : F::mma_spw(NB); }
+template <class F, int NB, bool PAR = false>
+__host__ __device__ constexpr int mma_stages_of() { return PAR ? 4 : F::mma_stages(NB); }
+template <class F, int NB, bool PAR = false>
+__host__ __device__ constexpr int mma_warps() { return PAR ? 16 : 2 * kSlices / F::mma_spw(NB); }
+template <class F, int NB, bool PAR = false>
+__host__ __device__ constexpr int mma_threads() { return 32 * mma_warps<F, NB, PAR>(); }
 
 // tree reduction buffer: [4 slots][2 halves][4 m-tiles][NB][32 lanes] float4
 template <int NB>
@@ -68,21 +74,21 @@ __host__ __device__ constexpr int mma_red_bytes() { return 4 * 2 * kMmaTiles * N
 // less the window offset of the dynamic area): stage 0, the mbarriers and,
 // for one activation block, the reduction buffer; after it the other stages
 // and, for two blocks, the reduction buffer.
-template <class F, int NB>
-__host__ __device__ constexpr int mma_bar_bytes() { return 2 * F::mma_stages(NB) * 8; }
-template <class F, int NB>
+template <class F, int NB, bool PAR = false>
+__host__ __device__ constexpr int mma_bar_bytes() { return 2 * mma_stages_of<F, NB, PAR>() * 8; }
+template <class F, int NB, bool PAR = false>
 __host__ __device__ constexpr int mma_pre_bytes() {
-  return F::kTileBytes + mma_bar_bytes<F, NB>() + (NB == 1 ? mma_red_bytes<NB>() : 0);
+  return F::kTileBytes + mma_bar_bytes<F, NB, PAR>() + (NB == 1 ? mma_red_bytes<NB>() : 0);
 }
-template <class F, int NB>
+template <class F, int NB, bool PAR = false>
 __host__ __device__ constexpr int mma_post_bytes() {
-  return (F::mma_stages(NB) - 1) * F::kTileBytes + (NB == 1 ? 0 : mma_red_bytes<NB>());
+  return (mma_stages_of<F, NB, PAR>() - 1) * F::kTileBytes + (NB == 1 ? 0 : mma_red_bytes<NB>());
 }
-template <class F, int NB>
+template <class F, int NB, bool PAR = false>
 __host__ __device__ constexpr int mma_smem_bytes() {
   return F::kMmaSharedBytes == 0
-             ? F::mma_stages(NB) * F::kTileBytes + mma_red_bytes<NB>() + mma_bar_bytes<F, NB>()
-             : kTableAlign + F::kMmaSharedBytes + mma_post_bytes<F, NB>();
+             ? mma_stages_of<F, NB, PAR>() * F::kTileBytes + mma_red_bytes<NB>() + mma_bar_bytes<F, NB, PAR>()
+             : kTableAlign + F::kMmaSharedBytes + mma_post_bytes<F, NB, PAR>();
 }
 
 // Address of table entry (byte bsel of w) for the lane: key = (table >> 16)
@@ -197,19 +203,21 @@ __device__ __noinline__ void mma_rebuild_table(uint8_t* lut, const uint16_t* cb,
   F::template mma_init_shared<NT>(lut, cb, warp, lane);
 }
 
-template <class F, int NB>
-__global__ void __launch_bounds__(mma_threads<F, NB>(), F::mma_ctas(NB)) gemv_mma_kernel(const GemvParams p, int M) {
-  constexpr int NS = F::mma_stages(NB);
+template <class F, int NB, bool PAR = false>
+__global__ void __launch_bounds__(mma_threads<F, NB, PAR>(), F::mma_ctas(NB)) gemv_mma_kernel(const GemvParams p, int M) {
+  constexpr int NS = mma_stages_of<F, NB, PAR>();
   constexpr int TB = F::kTileBytes;
   constexpr int KS = F::kKW / 16;        // k16 steps per slice
   constexpr int BS = F::kMmaBlockSteps;  // k16 steps per scale block, 0: none
   constexpr int NBLK = BS > 0 ? KS / BS : 1;
   constexpr int XW = F::kMmaXWords;      // activation words per (thread, activation row)
   constexpr bool PF = F::mma_prefetch_x(NB);  // activations a tile ahead (registers permitting)
-  constexpr int NT = mma_threads<F, NB>();
-  constexpr int NW = mma_warps<F, NB>();
-  constexpr int SPW = F::mma_spw(NB);     // k-slices per warp
-  constexpr int SG = kSlices / SPW;       // slice groups
+  constexpr int NT = mma_threads<F, NB, PAR>();
+  constexpr int NW = mma_warps<F, NB, PAR>();
+  constexpr int SPW = mma_spw_of<F, NB, PAR>();  // k-slices per warp
+  constexpr int SG = kSlices / SPW;              // slice groups
+  constexpr int TG = PAR ? 2 * SG : SG;          // partial sums per row added at a row-tile end
+  static_assert(!PAR || (F::mma_ctas(NB) == 1 && NS % 2 == 0 && NS >= 4), "tile parity geometry");
 
   if (static_cast<int>(blockIdx.x) == p.skip_cta) return;  // test hook (QGEMV_FAULT_SKIP_CTA)
   extern __shared__ __align__(128) uint8_t smem[];
@@ -226,20 +234,20 @@ __global__ void __launch_bounds__(mma_threads<F, NB>(), F::mma_ctas(NB)) gemv_mm
     full = reinterpret_cast<uint64_t*>(smem + NS * TB + mma_red_bytes<NB>());
   } else {
     static_assert(F::kMmaSharedBytes == kTableAlign, "one 64 KB table");
-    static_assert(mma_pre_bytes<F, NB>() + kTablePreSlack <= kTableAlign, "pre-table layout");
+    static_assert(mma_pre_bytes<F, NB, PAR>() + kTablePreSlack <= kTableAlign, "pre-table layout");
     const uint32_t base = smem_u32(smem);
     uint32_t dyn;
     asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
     const uint32_t R0 = (base + (kTableAlign - 1)) & ~uint32_t(kTableAlign - 1);
-    if (R0 - base < uint32_t(mma_pre_bytes<F, NB>()) ||
-        R0 + kTableAlign + mma_post_bytes<F, NB>() > base + dyn) {
+    if (R0 - base < uint32_t(mma_pre_bytes<F, NB, PAR>()) ||
+        R0 + kTableAlign + mma_post_bytes<F, NB, PAR>() > base + dyn) {
       if (threadIdx.x == 0) atomicOr(p.err, kErrSmemLayout);
       return;
     }
     fsh = smem + (R0 - base);
     ringN = fsh + kTableAlign;
     full = reinterpret_cast<uint64_t*>(smem + TB);
-    red = reinterpret_cast<float4*>(NB == 1 ? smem + TB + mma_bar_bytes<F, NB>() : ringN + (NS - 1) * TB);
+    red = reinterpret_cast<float4*>(NB == 1 ? smem + TB + mma_bar_bytes<F, NB, PAR>() : ringN + (NS - 1) * TB);
     lut_key = F::mma_lut_key(R0, static_cast<int>(threadIdx.x & 31u));
   }
   uint64_t* empty = full + NS;
@@ -252,8 +260,12 @@ __global__ void __launch_bounds__(mma_threads<F, NB>(), F::mma_ctas(NB)) gemv_mm
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int q = lane & 3, gi = lane >> 2;
-  const int sgrp = warp % SG;  // slice group: slices sgrp * SPW .. + SPW - 1
-  const int hf = warp / SG;
+  // slice group sgrp (slices sgrp * SPW .. + SPW - 1), row half hf; with
+  // tile parity, warp 8 par + 4 hf + sgrp computes the tiles j with j % 2 == par
+  const int par = PAR ? warp >> 3 : 0;
+  const int sgrp = PAR ? warp & 3 : warp % SG;
+  const int hf = PAR ? (warp >> 2) & 1 : warp / SG;
+  const int ti = par * SG + sgrp;  // index of the warp's partial sums in the row-tile tree
   const int64_t G = gridDim.x;
   const int64_t c = blockIdx.x;
   const int64_t t0 = stream_split(c, p.T, G);
@@ -267,12 +279,12 @@ __global__ void __launch_bounds__(mma_threads<F, NB>(), F::mma_ctas(NB)) gemv_mm
   if (elected) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], NW);
+      mbar_init(&empty[s], PAR ? NW / 2 : NW);  // with tile parity one half uses a stage
     }
     s_abort = 0;
     fence_mbarrier_init();
     pol = l2_policy_evict_first();
-    for (; n_issued < NS - 1 && n_issued < ntiles; ++n_issued) {
+    for (; n_issued < (PAR ? NS : NS - 1) && n_issued < ntiles; ++n_issued) {
       mbar_arrive_expect_tx(&full[n_issued], TB);
       bulk_g2s(stage_ptr(n_issued), p.tiles + (t0 + n_issued) * TB, TB, &full[n_issued], pol);
     }
@@ -311,8 +323,15 @@ __global__ void __launch_bounds__(mma_threads<F, NB>(), F::mma_ctas(NB)) gemv_mm
       for (int nb = 0; nb < NB; ++nb) F::mma_load_x(dst[ss][nb], xrow[nb], p.K, kb, q, xvec);
     }
   };
+  const int nKT = static_cast<int>(p.nKT);
+  // k-tile index k (< nKT + 2) reduced into [0, nKT)
+  auto wrap_kt = [nKT](int k) {
+    if (k >= nKT) k -= nKT;
+    if (k >= nKT) k -= nKT;
+    return k;
+  };
   if constexpr (PF) {
-    if (ntiles > 0) load_x(xw, kt);
+    if (par < ntiles) load_x(xw, wrap_kt(kt + par));
   }
 
   // acc[mt][nb]: D fragment of m-tile mt and activation block nb
@@ -324,128 +343,113 @@ __global__ void __launch_bounds__(mma_threads<F, NB>(), F::mma_ctas(NB)) gemv_mm
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[mt][nb][e] = 0.f;
 
-  int s = 0;
-  uint32_t ph = 0;
-  int su = static_cast<int>(n_issued % NS);
-  uint32_t phu = static_cast<uint32_t>((n_issued / NS) & 1);
   const int nt = ntiles;
   const bool stacked = F::kCbEntries > 0 && p.seg_of_rt != nullptr;
-  for (int i = 0; i < nt; ++i) {
-    if constexpr (F::kCbEntries > 0) {
-      if (stacked && kt == 0 && i > 0) {
-        __syncthreads();
-        if (s_seg[1] != s_seg[0]) mma_rebuild_table<F, NT>(fsh, table_of<F>(p, rt), warp, lane);
-        __syncthreads();
-        if (tid == 0) {
-          const int64_t nRT = div_fast(p.T, p.nKT);
-          s_seg[0] = s_seg[1];
-          s_seg[1] = rt + 1 < nRT ? __ldg(p.seg_of_rt + rt + 1) : s_seg[0];
-        }
-      }
+  // A new row tile of a stacked handle may use another codebook: rebuild the
+  // table once every warp is done with the old one.
+  auto next_table = [&]() {
+    __syncthreads();
+    if (s_seg[1] != s_seg[0]) mma_rebuild_table<F, NT>(fsh, table_of<F>(p, rt), warp, lane);
+    __syncthreads();
+    if (tid == 0) {
+      const int64_t nRT = div_fast(p.T, p.nKT);
+      s_seg[0] = s_seg[1];
+      s_seg[1] = rt + 1 < nRT ? __ldg(p.seg_of_rt + rt + 1) : s_seg[0];
     }
-    bool abort = s_abort != 0;
-    if (elected && !abort && n_issued < ntiles) {
-      if (n_issued >= NS && !mbar_wait_bounded(&empty[su], phu ^ 1)) {
-        atomicOr(p.err, kErrTimeoutEmpty);
-        s_abort = 1;
-        abort = true;
-      } else {
-        mbar_arrive_expect_tx(&full[su], TB);
-        bulk_g2s(stage_ptr(su), p.tiles + (t0 + n_issued) * TB, TB, &full[su], pol);
-        ++n_issued;
-        if (++su == NS) { su = 0; phu ^= 1; }
-      }
-    }
-    const int kt_next = (kt + 1 == p.nKT) ? 0 : kt + 1;
+  };
+
+  // The warp's part of the tile in stage st (fill parity fp), k-tile kt_cur:
+  // activations (those of the warp's next tile, k-tile kt_pref, when PF),
+  // wait for the codes, decode and multiply.
+  auto compute_tile = [&](int st, uint32_t fp, int kt_cur, int kt_pref, bool pref, bool abort) {
     uint32_t xn[PF ? SPW : 1][PF ? NB : 1][PF ? XW : 1];
     if constexpr (PF) {
-      if (i + 1 < nt) load_x(xn, kt_next);
+      if (pref) load_x(xn, kt_pref);
     } else {
-      load_x(xw, kt);
+      load_x(xw, kt_cur);
     }
 
-    const bool ok = !abort && mbar_wait_bounded(&full[s], ph);
-    if (!ok) {
-      if (!abort && lane == 0) atomicOr(p.err, kErrTimeoutFull);
-      s_abort = 1;
-    } else {
-      const uint8_t* stage = stage_ptr(s);
-#pragma unroll
-      for (int ss = 0; ss < SPW; ++ss) {
-        const int slice = sgrp * SPW + ss;
-        // codes (and scales) of the thread's eight rows in this slice; after
-        // the warp's last slice, release the stage
-        uint32_t w[kMmaTiles][2][F::kMmaRowWords];
-        typename F::MmaScales d[kMmaTiles][2];  // block scales of the rows, read per block
-#pragma unroll
-        for (int mt = 0; mt < kMmaTiles; ++mt) {
-          const int j = 2 * hf + (mt >> 1);
-          const int l = 16 * (mt & 1) + gi;
-          F::mma_load_row(stage, slice, l, j, q, w[mt][0]);
-          F::mma_load_row(stage, slice, l + 8, j, q, w[mt][1]);
-          if constexpr (BS > 0) {
-            F::mma_scales(stage, slice, l, j, d[mt][0]);
-            F::mma_scales(stage, slice, l + 8, j, d[mt][1]);
+      const bool ok = !abort && mbar_wait_bounded(&full[st], fp);
+      if (!ok) {
+        if (!abort && lane == 0) atomicOr(p.err, kErrTimeoutFull);
+        s_abort = 1;
+      } else {
+        const uint8_t* stage = stage_ptr(st);
+  #pragma unroll
+        for (int ss = 0; ss < SPW; ++ss) {
+          const int slice = sgrp * SPW + ss;
+          // codes (and scales) of the thread's eight rows in this slice; after
+          // the warp's last slice, release the stage
+          uint32_t w[kMmaTiles][2][F::kMmaRowWords];
+          typename F::MmaScales d[kMmaTiles][2];  // block scales of the rows, read per block
+  #pragma unroll
+          for (int mt = 0; mt < kMmaTiles; ++mt) {
+            const int j = 2 * hf + (mt >> 1);
+            const int l = 16 * (mt & 1) + gi;
+            F::mma_load_row(stage, slice, l, j, q, w[mt][0]);
+            F::mma_load_row(stage, slice, l + 8, j, q, w[mt][1]);
+            if constexpr (BS > 0) {
+              F::mma_scales(stage, slice, l, j, d[mt][0]);
+              F::mma_scales(stage, slice, l + 8, j, d[mt][1]);
+            }
           }
-        }
-        if (ss == SPW - 1) {
-          release_stage(&empty[s], lane);
-        }
+          if (ss == SPW - 1) {
+            release_stage(&empty[st], lane);
+          }
 
-        // MG m-tiles at a time, their MMAs interleaved so that consecutive
-        // MMAs are independent (all four for one activation block; one for
-        // two, which need twice the accumulators)
-        constexpr int MG = NB == 1 ? kMmaTiles : 1;
-#pragma unroll
-        for (int mg = 0; mg < kMmaTiles; mg += MG) {
-#pragma unroll
-          for (int blk = 0; blk < NBLK; ++blk) {
-            float tmp[MG][NB][4];  // block sums (block formats); the first MMA writes them
-#pragma unroll
-            for (int ks = blk * (BS > 0 ? BS : KS); ks < (blk + 1) * (BS > 0 ? BS : KS); ++ks) {
-              // one A fragment per codebook (additive formats sum two); the
-              // codebook loop is outside the m-tile loop so that MMAs into
-              // the same accumulator are not adjacent
-#pragma unroll
-              for (int cb = 0; cb < F::kMmaCodebooks; ++cb) {
-#pragma unroll
-                for (int mi = 0; mi < MG; ++mi) {
-                  const int mt = mg + mi;
-                  const uint2 r0 = F::mma_frag(w[mt][0], ks, lut_key, cb);  // row gi: (k lo pair, k hi pair)
-                  const uint2 r1 = F::mma_frag(w[mt][1], ks, lut_key, cb);  // row gi + 8
-#pragma unroll
-                  for (int nb = 0; nb < NB; ++nb) {
-                    const uint2 bf = F::mma_bfrag(xw[ss][nb], ks);
-                    if constexpr (BS > 0) {
-                      static_assert(BS == 0 || F::kMmaCodebooks == 1, "block scales with one codebook");
-                      if (ks == blk * BS)
-                        mma_16816_c0(tmp[mi][nb], r0.x, r1.x, r0.y, r1.y, bf.x, bf.y);
-                      else
-                        mma_16816(tmp[mi][nb], r0.x, r1.x, r0.y, r1.y, bf.x, bf.y);
-                    } else
-                      mma_16816(acc[mt][nb], r0.x, r1.x, r0.y, r1.y, bf.x, bf.y);
+          // MG m-tiles at a time, their MMAs interleaved so that consecutive
+          // MMAs are independent (all four for one activation block; one for
+          // two, which need twice the accumulators)
+          constexpr int MG = NB == 1 ? kMmaTiles : 1;
+  #pragma unroll
+          for (int mg = 0; mg < kMmaTiles; mg += MG) {
+  #pragma unroll
+            for (int blk = 0; blk < NBLK; ++blk) {
+              float tmp[MG][NB][4];  // block sums (block formats); the first MMA writes them
+  #pragma unroll
+              for (int ks = blk * (BS > 0 ? BS : KS); ks < (blk + 1) * (BS > 0 ? BS : KS); ++ks) {
+                // one A fragment per codebook (additive formats sum two); the
+                // codebook loop is outside the m-tile loop so that MMAs into
+                // the same accumulator are not adjacent
+  #pragma unroll
+                for (int cb = 0; cb < F::kMmaCodebooks; ++cb) {
+  #pragma unroll
+                  for (int mi = 0; mi < MG; ++mi) {
+                    const int mt = mg + mi;
+                    const uint2 r0 = F::mma_frag(w[mt][0], ks, lut_key, cb);  // row gi: (k lo pair, k hi pair)
+                    const uint2 r1 = F::mma_frag(w[mt][1], ks, lut_key, cb);  // row gi + 8
+  #pragma unroll
+                    for (int nb = 0; nb < NB; ++nb) {
+                      const uint2 bf = F::mma_bfrag(xw[ss][nb], ks);
+                      if constexpr (BS > 0) {
+                        static_assert(BS == 0 || F::kMmaCodebooks == 1, "block scales with one codebook");
+                        if (ks == blk * BS)
+                          mma_16816_c0(tmp[mi][nb], r0.x, r1.x, r0.y, r1.y, bf.x, bf.y);
+                        else
+                          mma_16816(tmp[mi][nb], r0.x, r1.x, r0.y, r1.y, bf.x, bf.y);
+                      } else
+                        mma_16816(acc[mt][nb], r0.x, r1.x, r0.y, r1.y, bf.x, bf.y);
+                    }
                   }
                 }
               }
-            }
-            if constexpr (BS > 0) {
-#pragma unroll
-              for (int mi = 0; mi < MG; ++mi)
-#pragma unroll
-                for (int nb = 0; nb < NB; ++nb) {
-                  const int mt = mg + mi;
-                  const float d0 = F::mma_scale(d[mt][0], blk), d1 = F::mma_scale(d[mt][1], blk);
-                  acc[mt][nb][0] = fmaf(d0, tmp[mi][nb][0], acc[mt][nb][0]);
-                  acc[mt][nb][1] = fmaf(d0, tmp[mi][nb][1], acc[mt][nb][1]);
-                  acc[mt][nb][2] = fmaf(d1, tmp[mi][nb][2], acc[mt][nb][2]);
-                  acc[mt][nb][3] = fmaf(d1, tmp[mi][nb][3], acc[mt][nb][3]);
-                }
+              if constexpr (BS > 0) {
+  #pragma unroll
+                for (int mi = 0; mi < MG; ++mi)
+  #pragma unroll
+                  for (int nb = 0; nb < NB; ++nb) {
+                    const int mt = mg + mi;
+                    const float d0 = F::mma_scale(d[mt][0], blk), d1 = F::mma_scale(d[mt][1], blk);
+                    acc[mt][nb][0] = fmaf(d0, tmp[mi][nb][0], acc[mt][nb][0]);
+                    acc[mt][nb][1] = fmaf(d0, tmp[mi][nb][1], acc[mt][nb][1]);
+                    acc[mt][nb][2] = fmaf(d1, tmp[mi][nb][2], acc[mt][nb][2]);
+                    acc[mt][nb][3] = fmaf(d1, tmp[mi][nb][3], acc[mt][nb][3]);
+                  }
+              }
             }
           }
         }
       }
-    }
-    if (++s == NS) { s = 0; ph ^= 1; }
     if constexpr (PF) {
 #pragma unroll
       for (int ss = 0; ss < SPW; ++ss)
@@ -454,79 +458,151 @@ __global__ void __launch_bounds__(mma_threads<F, NB>(), F::mma_ctas(NB)) gemv_mm
 #pragma unroll
           for (int e = 0; e < XW; ++e) xw[ss][nb][e] = xn[ss][nb][e];
     }
+  };
 
-    const bool row_end = (kt_next == 0) || (i + 1 == nt);
-    const int64_t cur_rt = rt;
-    kt = kt_next;
-    if (kt_next == 0) ++rt;
-    if (!row_end) continue;
-
-    // ---- row-tile epilogue: add the slice groups' results in a fixed tree ----
-#pragma unroll 1
-    for (int width = SG / 2; width >= 1; width >>= 1) {
-      if (sgrp >= width && sgrp < 2 * width) {
-#pragma unroll
+  // Row-tile epilogue: add the TG partial sums of every row in a fixed tree,
+  // then store them to y or to the stream-K partial slots.
+  auto row_epilogue = [&](int64_t cur_rt) {
+  #pragma unroll 1
+      for (int width = TG / 2; width >= 1; width >>= 1) {
+        if (ti >= width && ti < 2 * width) {
+  #pragma unroll
+          for (int mt = 0; mt < kMmaTiles; ++mt)
+  #pragma unroll
+            for (int nb = 0; nb < NB; ++nb)
+              red[(((ti - width) * 2 + hf) * kMmaTiles + mt) * NB * 32 + nb * 32 + lane] =
+                  make_float4(acc[mt][nb][0], acc[mt][nb][1], acc[mt][nb][2], acc[mt][nb][3]);
+        }
+        named_bar_sync(1, NT);
+        if (ti < width) {
+  #pragma unroll
+          for (int mt = 0; mt < kMmaTiles; ++mt)
+  #pragma unroll
+            for (int nb = 0; nb < NB; ++nb) {
+              const float4 v = red[((ti * 2 + hf) * kMmaTiles + mt) * NB * 32 + nb * 32 + lane];
+              acc[mt][nb][0] += v.x;
+              acc[mt][nb][1] += v.y;
+              acc[mt][nb][2] += v.z;
+              acc[mt][nb][3] += v.w;
+            }
+        }
+        named_bar_sync(1, NT);
+      }
+      if (ti == 0) {
+        const bool owner = (cur_rt * p.nKT >= t0) && ((cur_rt + 1) * p.nKT <= t1);
+        const int side = (cur_rt * p.nKT <= t0) ? 0 : 1;
+        float* my_part = p.partials + (c * 2 + side) * kPartialStride;
+  #pragma unroll
         for (int mt = 0; mt < kMmaTiles; ++mt)
-#pragma unroll
+  #pragma unroll
           for (int nb = 0; nb < NB; ++nb)
-            red[(((sgrp - width) * 2 + hf) * kMmaTiles + mt) * NB * 32 + nb * 32 + lane] =
-                make_float4(acc[mt][nb][0], acc[mt][nb][1], acc[mt][nb][2], acc[mt][nb][3]);
-      }
-      named_bar_sync(1, NT);
-      if (sgrp < width) {
-#pragma unroll
-        for (int mt = 0; mt < kMmaTiles; ++mt)
-#pragma unroll
-          for (int nb = 0; nb < NB; ++nb) {
-            const float4 v = red[((sgrp * 2 + hf) * kMmaTiles + mt) * NB * 32 + nb * 32 + lane];
-            acc[mt][nb][0] += v.x;
-            acc[mt][nb][1] += v.y;
-            acc[mt][nb][2] += v.z;
-            acc[mt][nb][3] += v.w;
-          }
-      }
-      named_bar_sync(1, NT);
-    }
-    if (sgrp == 0) {
-      const bool owner = (cur_rt * p.nKT >= t0) && ((cur_rt + 1) * p.nKT <= t1);
-      const int side = (cur_rt * p.nKT <= t0) ? 0 : 1;
-      float* my_part = p.partials + (c * 2 + side) * kPartialStride;
-#pragma unroll
-      for (int mt = 0; mt < kMmaTiles; ++mt)
-#pragma unroll
-        for (int nb = 0; nb < NB; ++nb)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            // D element e: weight row gi (+8 for e >= 2), activation row 2q + (e & 1)
-            const int m = 8 * nb + 2 * q + (e & 1);
-            const int l = 16 * (mt & 1) + gi + (e >> 1) * 8;
-            const int r = 4 * l + 2 * hf + (mt >> 1);
-            if (m < M) {
-              if (owner) {
-                const int64_t n = cur_rt * kTileRows + r;
-                if (n < p.N) {
-                  if constexpr (F::kMmaRowScales)
-                    p.y[m * p.N + n] = __half2float(F::mma_row_scales(p)[n]) * acc[mt][nb][e];
-                  else
-                    p.y[m * p.N + n] = acc[mt][nb][e];
+  #pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              // D element e: weight row gi (+8 for e >= 2), activation row 2q + (e & 1)
+              const int m = 8 * nb + 2 * q + (e & 1);
+              const int l = 16 * (mt & 1) + gi + (e >> 1) * 8;
+              const int r = 4 * l + 2 * hf + (mt >> 1);
+              if (m < M) {
+                if (owner) {
+                  const int64_t n = cur_rt * kTileRows + r;
+                  if (n < p.N) {
+                    if constexpr (F::kMmaRowScales)
+                      p.y[m * p.N + n] = __half2float(F::mma_row_scales(p)[n]) * acc[mt][nb][e];
+                    else
+                      p.y[m * p.N + n] = acc[mt][nb][e];
+                  }
+                } else {
+                  st_relaxed_f32(my_part + m * kTileRows + r, acc[mt][nb][e]);
                 }
-              } else {
-                st_relaxed_f32(my_part + m * kTileRows + r, acc[mt][nb][e]);
               }
             }
-          }
-    }
-#pragma unroll
-    for (int mt = 0; mt < kMmaTiles; ++mt)
-#pragma unroll
-      for (int nb = 0; nb < NB; ++nb)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[mt][nb][e] = 0.f;
-  }
+      }
+  #pragma unroll
+      for (int mt = 0; mt < kMmaTiles; ++mt)
+  #pragma unroll
+        for (int nb = 0; nb < NB; ++nb)
+  #pragma unroll
+          for (int e = 0; e < 4; ++e) acc[mt][nb][e] = 0.f;
+  };
 
-  if (elected && s_abort != 0) {
-    for (int u = (n_issued > NS ? n_issued - NS : 0); u < n_issued; ++u)
-      mbar_wait_bounded(&full[u % NS], static_cast<uint32_t>((u / NS) & 1));
+  if constexpr (PAR) {
+    // Tile parity: tile j sits in stage j % NS and is computed by half j % 2,
+    // so each half owns every second stage and runs its own pipeline: at its
+    // tile j its first thread refills the stage of its tile j - 2 (released
+    // one tile ago) with tile j + NS - 2.  The prologue issued tiles
+    // 0 .. NS - 1.  Both halves walk the run row tile by row tile and meet at
+    // each row-tile end.
+    const bool leader = (lane == 0) && ((warp & 7) == 0);
+    const uint64_t lpol = leader ? l2_policy_evict_first() : 0;
+    int u_last = -1;  // leader: last tile of its parity issued (by the prologue or by itself)
+    for (int u = par; u < NS && u < nt; u += 2) u_last = u;
+    int i = 0;  // first tile of the current row tile segment
+    while (i < nt) {
+      if (stacked && i > 0) next_table();
+      const int iend = i + min(nt - i, nKT - kt);
+#pragma unroll 1
+      for (int j = i + ((i ^ par) & 1); j < iend; j += 2) {
+        bool abort = s_abort != 0;
+        const int u = j + NS - 2;
+        if (leader && !abort && j >= 2 && u < nt) {
+          const int sn = u % NS;
+          if (!mbar_wait_bounded(&empty[sn], static_cast<uint32_t>(((u - NS) / NS) & 1))) {
+            atomicOr(p.err, kErrTimeoutEmpty);
+            s_abort = 1;
+            abort = true;
+          } else {
+            mbar_arrive_expect_tx(&full[sn], TB);
+            bulk_g2s(stage_ptr(sn), p.tiles + (t0 + u) * TB, TB, &full[sn], lpol);
+            u_last = u;
+          }
+        }
+        const int ktj = kt + (j - i);
+        compute_tile(j % NS, static_cast<uint32_t>((j / NS) & 1), ktj, wrap_kt(ktj + 2), j + 2 < nt, abort);
+      }
+      row_epilogue(rt);
+      i = iend;
+      kt = 0;
+      ++rt;
+    }
+    // Never leave while a copy issued by this half may still be landing
+    // (only after an aborted run): wait for the last fill of each of its stages.
+    if (leader && s_abort != 0) {
+      for (int u = u_last; u >= 0 && u > u_last - NS; u -= 2)
+        mbar_wait_bounded(&full[u % NS], static_cast<uint32_t>((u / NS) & 1));
+    }
+  } else {
+    int s = 0;
+    uint32_t ph = 0;
+    int su = static_cast<int>(n_issued % NS);
+    uint32_t phu = static_cast<uint32_t>((n_issued / NS) & 1);
+    for (int i = 0; i < nt; ++i) {
+      if (stacked && kt == 0 && i > 0) next_table();
+      bool abort = s_abort != 0;
+      if (elected && !abort && n_issued < ntiles) {
+        if (n_issued >= NS && !mbar_wait_bounded(&empty[su], phu ^ 1)) {
+          atomicOr(p.err, kErrTimeoutEmpty);
+          s_abort = 1;
+          abort = true;
+        } else {
+          mbar_arrive_expect_tx(&full[su], TB);
+          bulk_g2s(stage_ptr(su), p.tiles + (t0 + n_issued) * TB, TB, &full[su], pol);
+          ++n_issued;
+          if (++su == NS) { su = 0; phu ^= 1; }
+        }
+      }
+      const int kt_next = (kt + 1 == nKT) ? 0 : kt + 1;
+      compute_tile(s, ph, kt, kt_next, i + 1 < nt, abort);
+      if (++s == NS) { s = 0; ph ^= 1; }
+      const bool row_end = (kt_next == 0) || (i + 1 == nt);
+      const int64_t cur_rt = rt;
+      kt = kt_next;
+      if (kt_next == 0) ++rt;
+      if (row_end) row_epilogue(cur_rt);
+    }
+    if (elected && s_abort != 0) {
+      for (int u = (n_issued > NS ? n_issued - NS : 0); u < n_issued; ++u)
+        mbar_wait_bounded(&full[u % NS], static_cast<uint32_t>((u / NS) & 1));
+    }
   }
 
   // split row tiles: the shared polled-slot finisher, with M activation rows
