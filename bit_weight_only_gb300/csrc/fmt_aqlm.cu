@@ -293,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1) aqlm_gemv_kernel(const GemvParams
 #pragma unroll
       for (int m = 0; m < MB; ++m) {
         if (owner) {
-          if (n < p.N) p.y[m * p.N + n] = __half2float(scales[n]) * v[m];
+          if (n < p.N) store_y(p, m * p.N + n, __fmul_rn(__half2float(scales[n]), v[m]));
         } else {
           st_relaxed_f32(my_part + m * kRows + nl, v[m]);
         }
@@ -466,6 +466,7 @@ cudaError_t launch(int M, const GemvParams& p, const LaunchGeom& g, cudaStream_t
     q.plan = g.plan;
     q.x = p.x + int64_t(m0) * p.K;
     q.y = p.y + int64_t(m0) * p.N;
+    q.residual = p.residual != nullptr ? p.residual + int64_t(m0) * p.N : nullptr;
     if (M - m0 >= 2 && !batch_invariant) {
       e = launch_pass<2>(q, grid, s);
       m0 += 2;

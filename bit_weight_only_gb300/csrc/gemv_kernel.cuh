@@ -76,7 +76,15 @@ struct GemvParams {
   int64_t T;             // tiles in the stream = nRT * nKT
   int nKT;               // k tiles per row tile
   int skip_cta;          // test hook: this CTA does nothing (-1: none)
+  const float* residual; // [M][N] fp32 added to y in the store (may be y itself), or null
 };
+
+// y[idx] = v, plus the residual in one fp32 add (never fused with the
+// product that made v) when the call has one.  The residual element is read
+// and y written by the same thread, so residual may alias y.
+__device__ __forceinline__ void store_y(const GemvParams& p, int64_t idx, float v) {
+  p.y[idx] = p.residual != nullptr ? __fadd_rn(v, p.residual[idx]) : v;
+}
 
 // Warps per slice for a given M: two while the whole accumulator set of a
 // lane fits in 128 registers, one above.
@@ -262,7 +270,7 @@ __device__ __forceinline__ void finish_rows(const GemvParams& p, int64_t stride,
       }
     }
     if (H == 1) {
-      if (n < p.N) p.y[m * p.N + n] = sum * sc;
+      if (n < p.N) store_y(p, m * p.N + n, __fmul_rn(sum, sc));
     } else {
       s_sub[t] = sum;
       if (h == 0) s_sub[NT + item] = sc;
@@ -275,7 +283,7 @@ __device__ __forceinline__ void finish_rows(const GemvParams& p, int64_t stride,
       for (int h = 0; h < H; ++h) sum += s_sub[item * H + h];
       const int m = item / nr;
       const int64_t n = rt * ROWS + r0 + item - m * nr;
-      if (n < p.N) p.y[m * p.N + n] = sum * s_sub[NT + item];
+      if (n < p.N) store_y(p, m * p.N + n, __fmul_rn(sum, s_sub[NT + item]));
     }
     __syncthreads();
   }
@@ -535,7 +543,7 @@ __global__ void __launch_bounds__(gemv_threads<F, M>(), F::kCtasPerSm) gemv_kern
       for (int w = 0; w < red_slots<F, M>(); ++w) v += red[(w * kTileRows + r) * RS + m];
       if (owner) {
         const int64_t n = cur_rt * kTileRows + r;
-        if (n < p.N) p.y[m * p.N + n] = v * F::kOutScale;
+        if (n < p.N) store_y(p, m * p.N + n, __fmul_rn(v, F::kOutScale));
       } else {
         st_relaxed_f32(my_part + m * kTileRows + r, v);
       }

@@ -507,9 +507,9 @@ __global__ void __launch_bounds__(mma_threads<F, NB, PAR>(), F::mma_ctas(NB)) ge
                   const int64_t n = cur_rt * kTileRows + r;
                   if (n < p.N) {
                     if constexpr (F::kMmaRowScales)
-                      p.y[m * p.N + n] = __half2float(F::mma_row_scales(p)[n]) * acc[mt][nb][e];
+                      store_y(p, m * p.N + n, __fmul_rn(__half2float(F::mma_row_scales(p)[n]), acc[mt][nb][e]));
                     else
-                      p.y[m * p.N + n] = acc[mt][nb][e];
+                      store_y(p, m * p.N + n, acc[mt][nb][e]);
                   }
                 } else {
                   st_relaxed_f32(my_part + m * kTileRows + r, acc[mt][nb][e]);

@@ -453,12 +453,16 @@ qgemv_handle qgemv_create_stacked(int format, int nseg, const int64_t* seg_rows,
 
 static bool valid(qgemv_handle h) { return h && h->magic == kMagic; }
 
-int qgemv_run(qgemv_handle h, const void* x, int M, float* y, void* stream) {
+}  // extern "C"
+
+// Both run calls; `residual` is null for qgemv_run.
+static int run_impl(qgemv_handle h, const void* x, int M, float* y, const float* residual, void* stream) {
   if (!valid(h)) return set_error(QGEMV_ERR_ARG, "invalid handle");
   if (M < 1 || M > qgemv::kMaxM) return set_error(QGEMV_ERR_ARG, "M=%d outside [1, 16]", M);
   if (!x || !y) return set_error(QGEMV_ERR_ARG, "x or y is NULL");
-  if ((reinterpret_cast<uintptr_t>(x) & 3) || (reinterpret_cast<uintptr_t>(y) & 3))
-    return set_error(QGEMV_ERR_ALIGN, "x and y must be 4-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(x) & 3) || (reinterpret_cast<uintptr_t>(y) & 3) ||
+      (reinterpret_cast<uintptr_t>(residual) & 3))
+    return set_error(QGEMV_ERR_ALIGN, "x, y and residual must be 4-byte aligned");
   const bool inv = h->batch_invariant != 0;
   if (h->mma && (M >= kAqlmMmaMinM || inv)) h = h->mma;  // AQLM: the tensor-core layout
   qgemv::GemvParams p;
@@ -475,10 +479,22 @@ int qgemv_run(qgemv_handle h, const void* x, int M, float* y, void* stream) {
   p.T = h->T;
   p.nKT = h->nKT;
   p.skip_cta = h->skip_cta;
+  p.residual = residual;
   const qgemv::LaunchGeom g = {h->grid, h->plan, h->grid_m1, h->plan_m1};
   cudaError_t e = h->ops->launch(M, p, g, static_cast<cudaStream_t>(stream), inv);
   if (e != cudaSuccess) return cuda_error(e, "launching the GEMV kernel");
   return ok();
+}
+
+extern "C" {
+
+int qgemv_run(qgemv_handle h, const void* x, int M, float* y, void* stream) {
+  return run_impl(h, x, M, y, nullptr, stream);
+}
+
+int qgemv_run_residual(qgemv_handle h, const void* x, int M, float* y, const float* residual, void* stream) {
+  if (!residual) return set_error(QGEMV_ERR_ARG, "residual is NULL");
+  return run_impl(h, x, M, y, residual, stream);
 }
 
 int qgemv_set_batch_invariant(qgemv_handle h, int on) {

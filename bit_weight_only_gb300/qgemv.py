@@ -31,6 +31,8 @@ _SIGNATURES = {
                                                ctypes.c_void_p]),
     "qgemv_run": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
                                  ctypes.c_void_p, ctypes.c_void_p]),
+    "qgemv_run_residual": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                                          ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "qgemv_set_batch_invariant": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int]),
     "qgemv_dequant": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "qgemv_quantize_q4_0": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
@@ -117,6 +119,10 @@ def qgemv_create_stacked(fmt, seg_rows, K: int, packed: int, scales: int | None,
 
 def qgemv_run(h: int, x: int, M: int, y: int, stream=None) -> int:
     return _check(load().qgemv_run(h, x, M, y, _stream_ptr(stream)))
+
+
+def qgemv_run_residual(h: int, x: int, M: int, y: int, residual: int, stream=None) -> int:
+    return _check(load().qgemv_run_residual(h, x, M, y, residual, _stream_ptr(stream)))
 
 
 def qgemv_dequant(h: int, w_out: int, stream=None) -> int:
@@ -207,6 +213,11 @@ class QGemv:
     def run(self, x, y, stream=None):
         M = x.shape[0]
         qgemv_run(self.handle, x.data_ptr(), M, y.data_ptr(), stream)
+        return y
+
+    def run_residual(self, x, y, residual, stream=None):
+        """y = residual + x . W^T (residual may be y itself)."""
+        qgemv_run_residual(self.handle, x.data_ptr(), x.shape[0], y.data_ptr(), residual.data_ptr(), stream)
         return y
 
     def gemv(self, x, stream=None):

@@ -122,6 +122,19 @@ qgemv_handle qgemv_create_stacked(int format, int nseg, const int64_t* seg_rows,
  * bitwise reproducible run to run for a given (handle, M).                  */
 int qgemv_run(qgemv_handle h, const void* x, int M, float* y, void* stream);
 
+/* y = residual + x . dequant(W)^T for M rows: the residual add of a decoder
+ * layer's attention-output and MLP-down projections done in the GEMV's own
+ * store instead of a separate kernel ("Trapetum benchmarks", "Short-context
+ * decode, step by step": the residual add inside the o and down reduces).
+ *   residual: device fp32 [M][N] row-major, 4-byte aligned, not NULL.  It may
+ *     be y itself (y += x . W^T): each element is read and then written by
+ *     the same thread.
+ *   x, y, M, stream and the handle: as for qgemv_run.
+ * Each output is the value qgemv_run would store, plus the residual in one
+ * fp32 add (round to nearest), so the two calls agree bit for bit.         */
+int qgemv_run_residual(qgemv_handle h, const void* x, int M, float* y, const float* residual,
+                       void* stream);
+
 /* Batch-invariant mode (off by default): when on, row m of y from any call
  * is bitwise the same whatever M the call has and wherever the row sits in
  * the batch (the same x row gives the same y row alone or batched, as a

@@ -181,6 +181,28 @@ def quantize_q4_0(w, N: int, K: int) -> np.ndarray:
     return out
 
 
+def gemv_residual(fmt, N: int, K: int, packed, scales, codebooks, x, residual, rows=None,
+                  nthreads: int | None = None):
+    """Reference GEMV with the residual add of the fused attention-output and
+    MLP-down projections ("Trapetum benchmarks", "Short-context decode, step
+    by step"): y = residual + x . W^T, in fp64.  residual: [M, N].  Returns
+    (y, bound), bound being the GEMV's sum of |x * w| (fp64, [M, len(rows)])."""
+    y, b = gemv(fmt, N, K, packed, scales, codebooks, x, rows=rows, nthreads=nthreads)
+    r = np.asarray(residual, dtype=np.float64)
+    if r.shape != (y.shape[0], N):
+        raise ValueError("residual must be [M, N]")
+    if rows is not None:
+        r = r[:, np.asarray(rows, dtype=np.int64)]
+    return y + r, b
+
+
+def within_tolerance_residual(y, y_ref, bound):
+    """Acceptance with a residual: the GEMV's bound, plus one fp32 rounding of
+    the sum (2^-24 of its magnitude; 2^-23 of the exact value covers both)."""
+    y = np.asarray(y, dtype=np.float64)
+    return np.abs(y - y_ref) <= 1e-3 * bound + 1e-6 + 2.0 ** -23 * np.abs(y_ref)
+
+
 def within_tolerance(y, y_ref, bound, rel: float = 1e-3, abs_: float = 1e-6):
     """Elementwise GEMV acceptance: |y - y_ref| <= rel * bound + abs."""
     y = np.asarray(y, dtype=np.float64)

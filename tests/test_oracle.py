@@ -352,6 +352,37 @@ def test_gemv_row_subset_and_threads_agree():
     assert np.array_equal(ys, y[:, rows]) and np.array_equal(bs, b[:, rows])
 
 
+@pytest.mark.parametrize("fmt", ["cbk4", "aqlm_2x8"])
+def test_gemv_residual_special_cases(fmt):
+    """Pin: the residual form reduces to the residual itself for x = 0 and to
+    the plain GEMV for a zero residual; row subsets take the residual's
+    columns of the same rows."""
+    N, K = 29, 256
+    packed, scales, cb = make_case(fmt, N, K)
+    g = inputs.rng("pin/residual")
+    r = g.standard_normal((3, N))
+    zero_x = np.zeros((3, K), dtype=np.float16)
+    y0, b0 = oracle.gemv_residual(fmt, N, K, packed, scales, cb, zero_x, r)
+    assert np.array_equal(y0, r) and np.array_equal(b0, np.zeros_like(r))
+    x = inputs.x_fp16(g, 3, K)
+    y, b = oracle.gemv(fmt, N, K, packed, scales, cb, x)
+    yz, bz = oracle.gemv_residual(fmt, N, K, packed, scales, cb, x, np.zeros((3, N)))
+    assert np.array_equal(yz, y) and np.array_equal(bz, b)
+    rows = [5, 0, 28]
+    ys, _ = oracle.gemv_residual(fmt, N, K, packed, scales, cb, x, r, rows=rows)
+    yf, _ = oracle.gemv_residual(fmt, N, K, packed, scales, cb, x, r)
+    assert np.array_equal(ys, yf[:, rows])
+
+
+def test_residual_tolerance_rule():
+    y_ref = np.array([1.0e6, 0.0, -3.0])
+    bound = np.array([0.0, 0.0, 1.0])
+    # one fp32 rounding of a large sum (an ulp of 1e6 in fp32 is 0.0625)
+    assert oracle.within_tolerance_residual([1.0e6 + 0.0625, 0.0, -3.0 + 9e-4], y_ref, bound).all()
+    assert not oracle.within_tolerance_residual([1.0e6 + 0.5, 0.0, -3.0], y_ref, bound).all()
+    assert not oracle.within_tolerance_residual([1.0e6, 0.0, -3.0 - 2e-3], y_ref, bound).all()
+
+
 def test_tolerance_rule():
     y_ref = np.array([1.0, -2.0, 0.0])
     bound = np.array([10.0, 2.0, 0.0])
