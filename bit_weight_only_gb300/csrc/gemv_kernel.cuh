@@ -1,8 +1,11 @@
-// gemv_kernel.cuh -- the weight-streaming GEMV kernel shared by all formats.
+// gemv_kernel.cuh -- the CUDA-core weight-streaming GEMV kernel of the tile
+// formats (Q4_0, PQ2_0, CBK4, CBK8), used for M = 1, and the stream-K
+// finisher shared by every kernel.
 //
 //   y[m][n] = sum_k x[m][k] * w[n][k]      (1 <= M <= 16, fp32 accumulation)
 //
-// Design (one persistent CTA per SM):
+// Design (a persistent grid: one CTA per SM, or two for formats without a
+// table):
 //   * The weights were re-laid out at create time into "tiles" of
 //     kTileRows (128) output rows x F::kKT inputs, each tile one contiguous
 //     run of F::kTileBytes bytes, stored in (row tile, k tile) order.  The
@@ -16,21 +19,21 @@
 //     finished, after the main loop, by all of its contributors together:
 //     each sums a slice of the rows from polled partial slots, in a fixed
 //     order (no atomics, no fences; bitwise reproducible).
-//   * One elected thread keeps an F::stages(M) ring of shared-memory stages
-//     filled with TMA bulk copies (cp.async.bulk, evict-first L2 policy),
-//     stages - 1 tiles ahead of the math, signalled through mbarriers.  There
-//     is no separate producer warp.
-//   * WPS warps serve each slice: with WPS = 1 (eight warps) lane l of the
-//     slice's warp owns rows 4l..4l+3; with WPS = 2 (sixteen warps, used for
-//     small M where registers allow it, to hide more latency) the two warps
-//     of a slice split those four rows.  Each lane loads its codes, releases
-//     the stage, then decodes in registers and accumulates in fp32.  The
-//     activations of the slice are staged per tile in a per-warp shared
-//     buffer (prefetched from global one tile ahead), in the pre-scaled form
-//     the format's decode wants.
-//   * At the end of a row tile the eight slices' partial sums are added in
-//     slice order through shared memory and written to y (or to the
-//     stream-K workspace).
+//   * TMA bulk copies (cp.async.bulk, evict-first L2 policy) fill a ring of
+//     F::stages(M) shared-memory stages, signalled through mbarriers.  There
+//     is no separate producer warp: one thread of a computing warp issues.
+//   * Eight warps (one per slice; two CTAs per SM) or sixteen.  With sixteen
+//     (the table formats) the two warps of a slice take alternate tiles
+//     ("tile parity"), each for all four rows of its lanes; tile j sits in
+//     stage j mod 4, so each half of the CTA owns every second stage and
+//     runs its own pipeline.  Each lane loads its codes, releases the stage,
+//     then decodes in registers and accumulates in fp32.  The activations of
+//     the slice are staged per tile in a per-warp shared buffer (prefetched
+//     from global one tile ahead), in the pre-scaled form the format's decode
+//     wants.
+//   * At the end of a row tile the slices' (and halves') partial sums are
+//     added in a fixed order through shared memory and written to y (or to
+//     the stream-K workspace).
 // Every mbarrier wait is bounded; a timeout sets an error word, skips the
 // remaining math and still meets every named barrier, so the kernel always
 // returns.

@@ -138,11 +138,12 @@ int qgemv_run_residual(qgemv_handle h, const void* x, int M, float* y, const flo
 /* Batch-invariant mode (off by default): when on, row m of y from any call
  * is bitwise the same whatever M the call has and wherever the row sits in
  * the batch (the same x row gives the same y row alone or batched, as a
- * verifier comparing batched and single-row decodes needs).  Off, M = 1 runs
- * a faster kernel (and AQLM 2x8 pairs rows), whose bits may differ in the
- * last places (all within the accuracy bound).  On, AQLM 2x8 makes one pass
- * over the codes per activation row.  Takes effect for runs issued after
- * the call; returns QGEMV_ERR_ARG for an invalid handle.                   */
+ * verifier comparing batched and single-row decodes needs).  Off, M = 1 and
+ * M = 2..8 run faster kernel geometries (and AQLM 2x8 with M <= 2 its
+ * per-group table path), whose bits may differ in the last places (all
+ * within the accuracy bound).  On, every M runs the tensor-core kernel's
+ * default geometry (AQLM 2x8: its tensor-core layout).  Takes effect for
+ * runs issued after the call; returns QGEMV_ERR_ARG for an invalid handle. */
 int qgemv_set_batch_invariant(qgemv_handle h, int on);
 
 /* Write the decoded weights, fp32 [N][K] row-major, to device memory w_out
