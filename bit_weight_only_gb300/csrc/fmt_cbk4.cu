@@ -36,7 +36,8 @@ const FormatOps* ops_cbk4() {
       /*format=*/2, F::kKT, F::kTileBytes, /*aux_bytes=*/0,
       &LaunchTable<F>::smem_bytes, &LaunchTable<F>::setup, &LaunchTable<F>::launch,
       &prepare, &dequant, /*cb_entries=*/16, /*tile_rows=*/128, /*partial_stride=*/128 * 16,
-      /*aux_per_row=*/0, /*m1_ctas_per_sm=*/LaunchTable<F>::kM1CtasPerSm};
+      /*aux_per_row=*/0, /*m1_ctas_per_sm=*/LaunchTable<F>::kM1CtasPerSm,
+      /*rowgroup=*/1};
   return &ops;
 }
 

@@ -32,6 +32,7 @@ struct LaunchGeom {
   const CtaPlan* plan;
   int grid_m1;
   const CtaPlan* plan_m1;
+  int grid_rg;  // M = 1 row-group kernel (table formats, whole rows per CTA): its grid, 0 if not used
 };
 
 struct FormatOps {
@@ -53,6 +54,7 @@ struct FormatOps {
   int64_t partial_stride = 128 * 16;  // floats per stream-K partial slot
   int64_t aux_per_row = 0;          // aux bytes per output row, after aux_bytes
   int m1_ctas_per_sm = 1;           // CTAs per SM of the M = 1 kernel (LaunchGeom::grid_m1)
+  int rowgroup = 0;                 // has the M = 1 row-group kernel (rowgroup_kernel.cuh)
 };
 
 const FormatOps* ops_q4_0();

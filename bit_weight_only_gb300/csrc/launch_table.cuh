@@ -6,6 +6,7 @@
 
 #include "gemv_kernel.cuh"
 #include "mma_kernel.cuh"
+#include "rowgroup_kernel.cuh"
 
 namespace qgemv {
 
@@ -65,6 +66,15 @@ struct LaunchTable {
     return cudaLaunchKernelEx(&cfg, gemv_mma_kernel<F, NB, PAR>, q, M);
   }
 
+  // M = 1, whole 32-row groups per CTA (table formats; the handle decides,
+  // LaunchGeom::grid_rg).
+  static cudaError_t launch_rg(const GemvParams& p, int grid, cudaStream_t s) {
+    static_assert(rg_smem_bytes<F>() + 2048 <= 228 * 1024, "shared memory budget exceeded");
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = config(grid, kRgThreads, rg_smem_bytes<F>(), s, attr);
+    return cudaLaunchKernelEx(&cfg, gemv_rowgroup_kernel<F>, p);
+  }
+
   static int smem_bytes(int M) {
     if (M == 1) return gemv_smem_bytes<F, 1>();
     if (M >= 2 && M <= 8) return F::mma_par(1) ? mma_smem_bytes<F, 1, true>() : mma_smem_bytes<F, 1>();
@@ -84,6 +94,11 @@ struct LaunchTable {
         e = cudaFuncSetAttribute(gemv_mma_kernel<F, 1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  mma_smem_bytes<F, 1, true>());
     }
+    if constexpr (F::kTileParity) {
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(gemv_rowgroup_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 rg_smem_bytes<F>());
+    }
     return e;
   }
 
@@ -91,6 +106,9 @@ struct LaunchTable {
                             bool batch_invariant) {
     GemvParams q = p;
     if (M == 1 && !batch_invariant) {
+      if constexpr (F::kTileParity) {
+        if (g.grid_rg > 0) return launch_rg(q, g.grid_rg, s);
+      }
       q.plan = g.plan_m1;
       return launch_m1(q, g.grid_m1, s);
     }

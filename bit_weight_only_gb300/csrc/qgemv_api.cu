@@ -99,6 +99,9 @@ bool is_device_pointer(const void* p) {
 // nothing on the device faults or hangs):
 //   QGEMV_FAULT_ALLOC=n     the n-th device allocation of the create call
 //                           fails as if the device were out of memory;
+//   QGEMV_ROWGROUP=0|1      (not a fault) forbid or force the M = 1
+//                           row-group kernel of the table formats, so that
+//                           tests cover both M = 1 kernels on any shape;
 //   QGEMV_FAULT_SKIP_CTA=c  the handle's runs launch CTA c as a no-op, so
 //                           the CTAs that share a row tile with it never get
 //                           its partial sums: their bounded fix-up waits run
@@ -194,6 +197,7 @@ struct qgemv_ctx {
   int64_t T;
   int grid;      // tensor-core and AQLM kernels: min(T, SMs)
   int grid_m1;   // M = 1 CUDA-core kernel: min(T, SMs * m1_ctas_per_sm)
+  int grid_rg;   // M = 1 row-group kernel (table formats): min(units, SMs), 0 if not used
   uint8_t* tiles;
   void* aux;
   float* partials;
@@ -308,6 +312,23 @@ static qgemv_handle create_impl(int format, int64_t N, int64_t K, const void* pa
   {
     const int64_t g1 = int64_t(sms) * ops->m1_ctas_per_sm;
     h->grid_m1 = static_cast<int>(h->T < g1 ? h->T : g1);
+  }
+  // The row-group kernel (whole 32-row groups per CTA, no split-K finish)
+  // for matrices of at most one row group per SM whose busiest CTA then
+  // streams no more than the stream-K split's busiest one.  Measured on the
+  // 7B shapes: the 4096 x 4096 projection gains 10%; with several row groups
+  // per CTA (q|k|v, gate|up) the per-group epilogues and codebook changes
+  // cost more than the split-K finish they save.
+  if (ops->rowgroup) {
+    const int64_t U = h->nRT * 4, nch = (h->nKT + 3) / 4;
+    const int64_t Grg = U < sms ? U : sms;
+    const int64_t rg_bytes = (U + Grg - 1) / Grg * h->nKT * (ops->tile_bytes / 4);
+    const int64_t sk_bytes = (h->T + h->grid_m1 - 1) / h->grid_m1 * ops->tile_bytes;
+    bool use = nch >= 2 && U <= sms && nseg == 1 && rg_bytes <= sk_bytes;
+    const int force = env_int("QGEMV_ROWGROUP", -1);
+    if (force == 0) use = false;
+    if (force == 1) use = true;
+    h->grid_rg = use ? static_cast<int>(Grg) : 0;
   }
   const int slots_grid = h->grid > h->grid_m1 ? h->grid : h->grid_m1;  // partial slots for either grid
   const int n_plans = h->grid + (h->grid_m1 != h->grid ? h->grid_m1 : 0);
@@ -480,7 +501,7 @@ static int run_impl(qgemv_handle h, const void* x, int M, float* y, const float*
   p.nKT = h->nKT;
   p.skip_cta = h->skip_cta;
   p.residual = residual;
-  const qgemv::LaunchGeom g = {h->grid, h->plan, h->grid_m1, h->plan_m1};
+  const qgemv::LaunchGeom g = {h->grid, h->plan, h->grid_m1, h->plan_m1, h->grid_rg};
   cudaError_t e = h->ops->launch(M, p, g, static_cast<cudaStream_t>(stream), inv);
   if (e != cudaSuccess) return cuda_error(e, "launching the GEMV kernel");
   return ok();

@@ -43,6 +43,7 @@ def test_lost_partial_times_out_and_the_context_stays_usable(fmt, M, monkeypatch
     packed, scales, cb = make_case(fmt, N, K, tag="fault")
     x_np = make_x(M, K, tag="fault")
     x = torch.from_numpy(x_np).cuda()
+    monkeypatch.setenv("QGEMV_ROWGROUP", "0")  # the split-K kernels, whose fix-up waits for the lost CTA
     monkeypatch.setenv("QGEMV_FAULT_SKIP_CTA", "0")
     bad = qgemv.QGemv(fmt, N, K, packed, scales, cb)
     monkeypatch.delenv("QGEMV_FAULT_SKIP_CTA")
