@@ -418,7 +418,9 @@ def run_ours(args, rank, world, device):
                    "frac_of_peak": round(value / world / peak, 4)},
         "roofline": {"bound": "hbm",
                      "kernel": (f"aqlm_gemv_kernel<MB={M}>" if dominant == "aqlm_2x8" and M <= 2
-                                else f"gemv_kernel<{dominant}, M=1>" if M == 1
+                                else (f"gemv_kernel<{dominant}, M=1>"
+                                      + (" and gemv_rowgroup_kernel (matrices of at most one 32-row group per SM)"
+                                         if dominant in ("cbk4", "cbk8") else "")) if M == 1
                                 else f"gemv_mma_kernel<{dominant}, NB={1 if M <= 8 else 2}>"),
                      "achieved": round(dom_achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(dom_achieved / peak, 4), "peak_kind": peak_kind,
