@@ -167,7 +167,7 @@ int qgemv_status(qgemv_handle h);
  * NULL is accepted and ignored.                                             */
 void qgemv_destroy(qgemv_handle h);
 
-/* Allocation-free Q4_0 GEMV.  No counterpart in the paper: this is a service
+/* Allocation-free Q4_0 GEMV.  No counterpart in the source pages: a service
  * for callers that cannot allocate device memory when they need the product,
  * for instance code running inside a framework whose caching allocator owns
  * all device memory, or a latency-critical loop that must not pay for (or
