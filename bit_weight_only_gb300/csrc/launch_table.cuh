@@ -10,9 +10,11 @@
 
 namespace qgemv {
 
-// M = 1: the CUDA-core kernel (gemv_kernel.cuh).  M = 2..16: the tensor-core
-// kernel with register-level decode (mma_kernel.cuh), one activation block
-// of 8 rows up to M = 8, two above.  The tensor-core kernel computes every
+// M = 1: the CUDA-core kernel (gemv_kernel.cuh), or for table formats whose
+// handle chose it the row-group kernel (rowgroup_kernel.cuh).  M = 2..16: the
+// tensor-core kernel with register-level decode (mma_kernel.cuh), one
+// activation block of 8 rows up to M = 8 (tile-parity geometry where the
+// format has it), two above.  The tensor-core kernel computes every
 // activation row on its own (a column of the MMA's B operand, the same
 // instruction sequence, reduction tree and fix-up order for any M), so in
 // batch-invariant mode M = 1 runs there too and a row's bits never depend on
