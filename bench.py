@@ -269,6 +269,16 @@ class ClockSampler:
 
 # ----------------------------------------------------------- our arm ------
 
+def max_over_ranks(values, world, device):
+    """Each value's maximum over the ranks (the slowest rank sets the job's
+    time); the values themselves on one rank."""
+    import torch
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return t.tolist()
+
+
 def run_ours(args, rank, world, device):
     import torch
     from bit_weight_only_gb300 import build, qgemv
@@ -374,10 +384,7 @@ def run_ours(args, rank, world, device):
             stream.synchronize()
     e2e_s = time.perf_counter() - t0
 
-    t = torch.tensor([total_ms, dom_ms, e2e_s], dtype=torch.float64, device=device)
-    if world > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    total_ms, dom_ms, e2e_s = t.tolist()
+    total_ms, dom_ms, e2e_s = max_over_ranks([total_ms, dom_ms, e2e_s], world, device)
     if rank != 0:
         return None
 
