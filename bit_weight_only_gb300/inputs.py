@@ -109,6 +109,17 @@ def cbk_packed(g: np.random.Generator, N: int, K: int, bits: int, probs) -> np.n
     raise ValueError("bits must be 4 or 8")
 
 
+def cbk_row_codebooks(g: np.random.Generator, N: int, L: int = 16, sigma=(0.01, 0.03)) -> np.ndarray:
+    """Per-output-row fp32 codebooks [N, L]: row n's L mid-rank quantiles of
+    N(0, s_n), s_n drawn uniformly from `sigma`, plus a jitter of a tenth of
+    the smallest gap (so rows differ beyond a scale); sorted ascending."""
+    base = ndtri((np.arange(L) + 0.5) / L)
+    s = g.uniform(sigma[0], sigma[1], size=(N, 1))
+    gap = np.min(np.diff(base))
+    jitter = g.uniform(-0.1, 0.1, size=(N, L)) * gap
+    return np.sort((base[None, :] + jitter) * s, axis=1).astype(np.float32)
+
+
 def pq2_packed(g: np.random.Generator, N: int, K: int, sigma: float = 0.02) -> np.ndarray:
     """Canonical PQ2_0 rows: N*K/128 blocks of {fp16 d, 32 code bytes}."""
     nb = K // 128

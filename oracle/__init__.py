@@ -21,9 +21,9 @@ import numpy as np
 
 from . import build as _build
 
-Q4_0, CBK4, CBK8, PQ2_0, AQLM_2X8 = 1, 2, 3, 4, 5
+Q4_0, CBK4, CBK8, PQ2_0, AQLM_2X8, CBK4_ROW = 1, 2, 3, 4, 5, 6
 FORMATS = {"q4_0": Q4_0, "cbk4": CBK4, "cbk8": CBK8, "pq2_0": PQ2_0,
-           "aqlm_2x8": AQLM_2X8}
+           "aqlm_2x8": AQLM_2X8, "cbk4_row": CBK4_ROW}
 
 _lib = None
 
@@ -46,6 +46,8 @@ def _load():
         lib.oracle_scales_count.restype = i64
         lib.oracle_codebook_count.argtypes = [c_int]
         lib.oracle_codebook_count.restype = i64
+        lib.oracle_codebook_bytes.argtypes = [c_int, i64]
+        lib.oracle_codebook_bytes.restype = i64
         lib.oracle_dequant_row.argtypes = [c_int, i64, i64, vp, vp, vp, i64, vp]
         lib.oracle_dequant_row.restype = c_int
         lib.oracle_dequant.argtypes = [c_int, i64, i64, vp, vp, vp, vp]
@@ -93,6 +95,11 @@ def codebook_count(fmt) -> int:
     return int(_load().oracle_codebook_count(_fmt(fmt)))
 
 
+def codebook_bytes(fmt, N: int) -> int:
+    """Bytes of the codebooks input of an N-row matrix (cbk4_row: fp32 [N][16])."""
+    return int(_load().oracle_codebook_bytes(_fmt(fmt), N))
+
+
 def half_to_double(bits: int) -> float:
     return float(_load().oracle_half_to_double(int(bits) & 0xFFFF))
 
@@ -112,6 +119,11 @@ def _check(fmt, N, K, packed, scales, codebooks):
     s = _u16(scales)
     if scales_count(f, N, K) and (s is None or s.size != scales_count(f, N, K)):
         raise ValueError("scales missing or of the wrong size")
+    if f == CBK4_ROW:  # fp32 [N][16], passed as bytes
+        c = None if codebooks is None else np.ascontiguousarray(codebooks, dtype=np.float32).view(np.uint8).reshape(-1)
+        if c is None or c.size != codebook_bytes(f, N):
+            raise ValueError("codebooks missing or of the wrong size")
+        return f, p, s, c
     c = _u16(codebooks)
     if codebook_count(f) and (c is None or c.size != codebook_count(f)):
         raise ValueError("codebooks missing or of the wrong size")

@@ -24,6 +24,11 @@
  *   CBK4/CBK8 -- "Trapetum benchmarks", sections "Kernel microbenchmarks"
  *                (4-bit index into K = 16 centroids, uint8 index into 256) and
  *                "Model-level results"; one codebook per projection.
+ *   CBK4_ROW  -- "Trapetum benchmarks", "Model-level results": the runtime's
+ *                own 4-bit files, with one k-means codebook of 16 centroids per
+ *                weight column of the pages' (input, output) layout, i.e. per
+ *                output row here, stored as fp32 (the legacy file's size is
+ *                reproduced with 16 fp32 values per output row).
  *   PQ2_0     -- "Making a ternary reasoning model fast in vLLM", section
  *                "Anatomy of a PQ2_0 block": {half d; uint8 qs[32]}, 34 bytes
  *                per 128 weights, codes 0/1/2/3 -> -1/0/+1/+2, two-bit fields
@@ -45,6 +50,8 @@
  *   R4 PQ2_0: byte j of a block holds elements 4j..4j+3, lowest bits first.
  *   R5 AQLM 2x8: codes [N][K/8][2] (codebook 0 first), codebooks [2][256][8]
  *      fp16, one fp16 scale per output row multiplying the summed vector.
+ *   R10 CBK4_ROW: indices as CBK4 (R3); codebooks fp32 [N][16], row n's 16
+ *      centroids contiguous, little-endian.
  *   All multi-byte values are little-endian.
  */
 #include <math.h>
@@ -57,6 +64,7 @@
 #define ORACLE_CBK8 3
 #define ORACLE_PQ2_0 4
 #define ORACLE_AQLM_2X8 5
+#define ORACLE_CBK4_ROW 6
 
 #define ORACLE_OK 0
 #define ORACLE_ERR_ARG 1
@@ -118,6 +126,7 @@ int64_t oracle_packed_bytes(int fmt, int64_t N, int64_t K) {
   switch (fmt) {
     case ORACLE_Q4_0: return (K % 32) ? 0 : N * (K / 32) * 18;
     case ORACLE_CBK4: return (K % 2) ? 0 : N * (K / 2);
+    case ORACLE_CBK4_ROW: return (K % 2) ? 0 : N * (K / 2);
     case ORACLE_CBK8: return N * K;
     case ORACLE_PQ2_0: return (K % 128) ? 0 : N * (K / 128) * 34;
     case ORACLE_AQLM_2X8: return (K % 8) ? 0 : N * (K / 8) * 2;
@@ -131,7 +140,8 @@ int64_t oracle_scales_count(int fmt, int64_t N, int64_t K) {
   return fmt == ORACLE_AQLM_2X8 ? N : 0;
 }
 
-/* Number of fp16 values in the `codebooks` input. */
+/* Number of fp16 values in the `codebooks` input (formats with one codebook
+ * per matrix). */
 int64_t oracle_codebook_count(int fmt) {
   switch (fmt) {
     case ORACLE_CBK4: return 16;
@@ -139,6 +149,21 @@ int64_t oracle_codebook_count(int fmt) {
     case ORACLE_AQLM_2X8: return 2 * 256 * 8;
   }
   return 0;
+}
+
+/* Bytes of the `codebooks` input for an N-row matrix. */
+int64_t oracle_codebook_bytes(int fmt, int64_t N) {
+  if (fmt == ORACLE_CBK4_ROW) return N * 16 * 4; /* fp32 [N][16] (reading R10) */
+  return 2 * oracle_codebook_count(fmt);
+}
+
+/* fp32 value i of a little-endian byte array, exactly. */
+static double rdf32(const uint8_t* p, int64_t i) {
+  uint32_t u = (uint32_t)p[4 * i] | ((uint32_t)p[4 * i + 1] << 8) | ((uint32_t)p[4 * i + 2] << 16) |
+               ((uint32_t)p[4 * i + 3] << 24);
+  float f;
+  memcpy(&f, &u, 4);
+  return (double)f;
 }
 
 /* ------------------------------------------------------------- dequant ---- */
@@ -149,7 +174,8 @@ int oracle_dequant_row(int fmt, int64_t N, int64_t K, const uint8_t* packed,
                        int64_t n, double* w) {
   if (oracle_packed_bytes(fmt, N, K) == 0 || n < 0 || n >= N || !packed || !w)
     return ORACLE_ERR_ARG;
-  if ((fmt == ORACLE_CBK4 || fmt == ORACLE_CBK8 || fmt == ORACLE_AQLM_2X8) && !codebooks)
+  if ((fmt == ORACLE_CBK4 || fmt == ORACLE_CBK8 || fmt == ORACLE_AQLM_2X8 || fmt == ORACLE_CBK4_ROW) &&
+      !codebooks)
     return ORACLE_ERR_ARG;
   if (fmt == ORACLE_AQLM_2X8 && !scales) return ORACLE_ERR_ARG;
 
@@ -173,6 +199,14 @@ int oracle_dequant_row(int fmt, int64_t N, int64_t K, const uint8_t* packed,
     for (int64_t j = 0; j < K / 2; ++j) {
       w[2 * j] = oracle_half_to_double(codebooks[row[j] & 0x0f]);
       w[2 * j + 1] = oracle_half_to_double(codebooks[row[j] >> 4]);
+    }
+  } else if (fmt == ORACLE_CBK4_ROW) {
+    /* as CBK4 (reading R3), with row n's own 16 fp32 centroids (reading R10) */
+    const uint8_t* row = packed + n * (K / 2);
+    const uint8_t* cb = (const uint8_t*)codebooks + n * 16 * 4;
+    for (int64_t j = 0; j < K / 2; ++j) {
+      w[2 * j] = rdf32(cb, row[j] & 0x0f);
+      w[2 * j + 1] = rdf32(cb, row[j] >> 4);
     }
   } else if (fmt == ORACLE_CBK8) {
     /* 8-bit index into 256 centroids */

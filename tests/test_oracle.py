@@ -90,6 +90,12 @@ def test_cbk_byte_accounting_reconstructs_7b_file_sizes(golden_dir):
     norms = 65 * 4096 * 4
     legacy = (idx + rows * 16 * 4 + emb + oracle.packed_bytes("cbk4", 32000, 4096)
               + 32000 * 16 * 4 + norms)
+    # the per-row-codebook format's own accounting (indices + fp32 codebooks)
+    # gives the same projections-plus-head bytes
+    per_row = 32 * sum(oracle.packed_bytes("cbk4_row", n, k) + oracle.codebook_bytes("cbk4_row", n)
+                       for n, k in shapes)
+    per_row += oracle.packed_bytes("cbk4_row", 32000, 4096) + oracle.codebook_bytes("cbk4_row", 32000)
+    assert 0 < gb["legacy_file_bytes"] - (per_row + emb + norms) < 1024
     new = (idx + rows * 16 * 4 + emb + oracle.packed_bytes("cbk8", 32000, 4096)
            + 32000 * 256 * 4 + norms)
     assert 0 < gb["legacy_file_bytes"] - legacy < 1024
@@ -237,6 +243,41 @@ def test_cbk4_value_multiset_is_codebook_of_nibbles():
         assert sorted(w[n]) == sorted(cb[nib].astype(np.float64))
 
 
+def test_cbk4_row_with_one_shared_codebook_is_cbk4():
+    """Pin (reduction to a pinned format): when every row's fp32 codebook is
+    the same fp16-representable codebook, the per-row format decodes exactly
+    like CBK4 with that codebook."""
+    N, K = 9, 64
+    g = inputs.rng("pin/cbk4_row/shared")
+    packed = g.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    c16 = inputs.cbk_centroids(16)
+    rows = np.tile(c16.astype(np.float32), (N, 1))
+    assert np.array_equal(oracle.dequant("cbk4_row", N, K, packed, None, rows),
+                          oracle.dequant("cbk4", N, K, packed, None, c16))
+
+
+def test_cbk4_row_uses_each_rows_own_codebook():
+    """Pin (closed form, brute force): row n's codebook c_n[i] = 1000 n + i
+    (exact in fp32) decodes every nibble i of row n to 1000 n + i, for all 16
+    values, low nibble first; changing one row's codebook changes only that
+    row."""
+    N, K = 4, 32
+    packed = np.zeros((N, K // 2), dtype=np.uint8)
+    for n in range(N):
+        for j in range(K // 2):
+            packed[n, j] = (j % 16) | (((j + n + 5) % 16) << 4)
+    cb = (1000.0 * np.arange(N)[:, None] + np.arange(16)[None, :]).astype(np.float32)
+    W = oracle.dequant("cbk4_row", N, K, packed, None, cb)
+    for n in range(N):
+        for j in range(K // 2):
+            assert W[n, 2 * j] == 1000 * n + j % 16
+            assert W[n, 2 * j + 1] == 1000 * n + (j + n + 5) % 16
+    cb2 = cb.copy()
+    cb2[2] = -cb2[2]
+    W2 = oracle.dequant("cbk4_row", N, K, packed, None, cb2)
+    assert np.array_equal(W2[[0, 1, 3]], W[[0, 1, 3]]) and np.array_equal(W2[2], -W[2])
+
+
 def test_cbk8_all_256_indices():
     cb = (np.arange(256) / 256.0).astype(np.float16)
     row = np.arange(256, dtype=np.uint8)[::-1].copy()
@@ -287,7 +328,7 @@ def test_aqlm_group_order():
 
 # ---------------------------------------------------------------- GEMV ---
 
-FORMAT_CASES = ["q4_0", "cbk4", "cbk8", "pq2_0", "aqlm_2x8"]
+FORMAT_CASES = ["q4_0", "cbk4", "cbk8", "pq2_0", "aqlm_2x8", "cbk4_row"]
 
 
 def make_case(fmt, N, K, tag="pin", seed=0):
@@ -295,6 +336,9 @@ def make_case(fmt, N, K, tag="pin", seed=0):
     g = inputs.rng(f"{tag}/{fmt}/{N}x{K}", seed)
     if fmt == "q4_0":
         return oracle.quantize_q4_0(inputs.w_fp32(g, N, K), N, K), None, None
+    if fmt == "cbk4_row":
+        cb = inputs.cbk_row_codebooks(g, N)
+        return inputs.cbk_packed(g, N, K, 4, inputs.cbk_cell_probs(inputs.cbk_centroids(16))), None, cb
     if fmt in ("cbk4", "cbk8"):
         L = 16 if fmt == "cbk4" else 256
         cb = inputs.cbk_centroids(L)

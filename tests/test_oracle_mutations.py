@@ -32,6 +32,9 @@ MUTATIONS = {
     "cbk4 nibble order": [("w[2 * j] = oracle_half_to_double(codebooks[row[j] & 0x0f]);",
                            "w[2 * j] = oracle_half_to_double(codebooks[row[j] >> 4]);")],
     "cbk8 index off by one bit": [("codebooks[row[k]]", "codebooks[row[k] ^ 1]")],
+    "cbk4_row neighbour's codebook": [("const uint8_t* cb = (const uint8_t*)codebooks + n * 16 * 4;",
+                                       "const uint8_t* cb = (const uint8_t*)codebooks + (n ^ 1) * 16 * 4;")],
+    "cbk4_row nibble order": [("w[2 * j] = rdf32(cb, row[j] & 0x0f);", "w[2 * j] = rdf32(cb, row[j] >> 4);")],
     "bound without abs": [("b += fabs(t);", "b += t;")],
     "x transposed against w": [("double t = xd[m * K + k] * w[k];",
                                 "double t = xd[m * K + (K - 1 - k)] * w[k];")],
