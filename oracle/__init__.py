@@ -57,6 +57,10 @@ def _load():
         lib.oracle_gemv.restype = c_int
         lib.oracle_quantize_q4_0.argtypes = [vp, i64, i64, vp]
         lib.oracle_quantize_q4_0.restype = c_int
+        lib.oracle_quantize_x_int8.argtypes = [vp, i64, i64, vp, vp]
+        lib.oracle_quantize_x_int8.restype = c_int
+        lib.oracle_gemv_pq2_int8.argtypes = [i64, i64, vp, vp, i64, vp, vp, c_int]
+        lib.oracle_gemv_pq2_int8.restype = c_int
         _lib = lib
     return _lib
 
@@ -219,3 +223,35 @@ def within_tolerance(y, y_ref, bound, rel: float = 1e-3, abs_: float = 1e-6):
     """Elementwise GEMV acceptance: |y - y_ref| <= rel * bound + abs."""
     y = np.asarray(y, dtype=np.float64)
     return np.abs(y - y_ref) <= rel * bound + abs_
+
+
+def quantize_x_int8(x):
+    """The PQ2_0 integer path's activation quantizer (reading R11): fp16
+    [M, K] (K % 128 == 0) -> (q int8 [M, K], a fp32 [M, K/128]) with
+    x ~ a * q per group of 128."""
+    x = np.ascontiguousarray(x, dtype=np.float16)
+    M, K = x.shape
+    q = np.empty((M, K), dtype=np.int8)
+    a = np.empty((M, K // 128), dtype=np.float32)
+    rc = _load().oracle_quantize_x_int8(_ptr(_u16(x)), M, K, _ptr(q), _ptr(a))
+    if rc:
+        raise ValueError(f"oracle_quantize_x_int8 failed ({rc})")
+    return q, a
+
+
+def gemv_pq2_int8(N: int, K: int, packed, x, nthreads: int | None = None):
+    """PQ2_0 GEMV on the integer path: INT8 activations per group of 128,
+    integer inner sums, d * a applied per block.  Returns (y, bound), fp64
+    [M, N]; bound is the sum of |terms| of the same expansion."""
+    p = _u8(packed)
+    if p is None or p.size != packed_bytes("pq2_0", N, K):
+        raise ValueError("packed missing or of the wrong size")
+    x = np.ascontiguousarray(x, dtype=np.float16)
+    M = x.shape[0]
+    y = np.empty((M, N), dtype=np.float64)
+    b = np.empty((M, N), dtype=np.float64)
+    rc = _load().oracle_gemv_pq2_int8(N, K, _ptr(p), _ptr(_u16(x)), M, _ptr(y), _ptr(b),
+                                      int(nthreads or os.cpu_count() or 1))
+    if rc:
+        raise RuntimeError(f"oracle_gemv_pq2_int8 failed ({rc})")
+    return y, b

@@ -33,6 +33,9 @@
  *                "Anatomy of a PQ2_0 block": {half d; uint8 qs[32]}, 34 bytes
  *                per 128 weights, codes 0/1/2/3 -> -1/0/+1/+2, two-bit fields
  *                read from the low end of each byte.
+ *   PQ2_0 int8 -- the same page, on quantising the activation too: INT8
+ *                activations per group of 128, integer inner sums, the block
+ *                scale times the group scale applied once per block.
  *   AQLM 2x8  -- "Trapetum benchmarks", sections "Additive vector-quantization
  *                GEMV" and "Llama-2-70B in 2 bits": per group of 8 weights
  *                two uint8 codes into two 256x8 fp16 codebooks, summed, and a
@@ -52,6 +55,9 @@
  *      fp16, one fp16 scale per output row multiplying the summed vector.
  *   R10 CBK4_ROW: indices as CBK4 (R3); codebooks fp32 [N][16], row n's 16
  *      centroids contiguous, little-endian.
+ *   R11 PQ2_0 integer activations: per group of 128, a = fl32(max|x| / 127),
+ *      q = clamp(rint(fl32(x / a)), -127, 127) with ties to even; a zero
+ *      group has a = 0 and q = 0 (see oracle_quantize_x_int8).
  *   All multi-byte values are little-endian.
  */
 #include <math.h>
@@ -346,4 +352,91 @@ int oracle_quantize_q4_0(const float* wf, int64_t N, int64_t K, uint8_t* out) {
     }
   }
   return ORACLE_OK;
+}
+
+/* -------------------------------------------- PQ2_0 integer activations ---- */
+
+/* The PQ2_0 integer path ("Making a ternary reasoning model fast in vLLM",
+ * the section on quantising the activation too): each group of 128
+ * activations (one PQ2_0 block's inputs) is scaled to signed INT8,
+ * x_i ~ a * q_i with q_i in [-127, 127], so a block's inner sum over its
+ * ternary codes is an integer, and floating point is used once per block to
+ * apply d * a.  Lossy: the GEMV tolerance is measured against this path, and
+ * its distance to the exact GEMV is reported separately.
+ * Reading R11 (the pages do not fix the scale or the rounding):
+ *   amax = max_i |x_i| over the group (exact), a = fl32(amax / 127),
+ *   q_i  = clamp(rint(fl32(x_i / a)), -127, 127), ties to even; a = 0 gives
+ *   q_i = 0.  fl32 is one IEEE float operation, round to nearest even.     */
+int oracle_quantize_x_int8(const uint16_t* x, int64_t M, int64_t K, int8_t* q, float* a) {
+  if (!x || !q || !a || M <= 0 || K <= 0 || K % 128) return ORACLE_ERR_ARG;
+  int64_t ng = K / 128;
+  for (int64_t m = 0; m < M; ++m) {
+    for (int64_t g = 0; g < ng; ++g) {
+      const uint16_t* xg = x + m * K + g * 128;
+      float amax = 0.0f;
+      for (int i = 0; i < 128; ++i) {
+        float v = fabsf((float)oracle_half_to_double(xg[i]));
+        if (v > amax) amax = v;
+      }
+      float s = amax / 127.0f;
+      a[m * ng + g] = s;
+      for (int i = 0; i < 128; ++i) {
+        int qi = 0;
+        if (s != 0.0f) {
+          float r = rintf((float)oracle_half_to_double(xg[i]) / s);
+          qi = r > 127.0f ? 127 : (r < -127.0f ? -127 : (int)r);
+        }
+        q[m * K + g * 128 + i] = (int8_t)qi;
+      }
+    }
+  }
+  return ORACLE_OK;
+}
+
+/* y[m][n] = sum_b d_b * a[m][b] * sum_{i in block b} (c_i - 1) * q[m][i],
+ * the integer inner sums exact and the rest in fp64 (each d * a * sum has at
+ * most 11 + 24 + 15 significant bits, so it is exact too); bound[m][n] is
+ * the same sum over |terms|.  y and bound are fp64 [M][N].                  */
+int oracle_gemv_pq2_int8(int64_t N, int64_t K, const uint8_t* packed, const uint16_t* x, int64_t M,
+                         double* y, double* bound, int nthreads) {
+  if (oracle_packed_bytes(ORACLE_PQ2_0, N, K) == 0 || !packed || !x || !y || M <= 0) return ORACLE_ERR_ARG;
+  int64_t nb = K / 128;
+  int8_t* q = (int8_t*)malloc((size_t)(M * K));
+  float* a = (float*)malloc(sizeof(float) * (size_t)(M * nb));
+  if (!q || !a) {
+    free(q);
+    free(a);
+    return ORACLE_ERR_NOMEM;
+  }
+  int rc = oracle_quantize_x_int8(x, M, K, q, a);
+  if (rc == ORACLE_OK) {
+#if defined(_OPENMP)
+#pragma omp parallel for num_threads(nthreads > 0 ? nthreads : 1) schedule(dynamic, 4)
+#endif
+    for (int64_t n = 0; n < N; ++n) {
+      for (int64_t m = 0; m < M; ++m) {
+        double s = 0.0, bnd = 0.0;
+        for (int64_t b = 0; b < nb; ++b) {
+          const uint8_t* blk = packed + (n * nb + b) * 34;
+          double d = oracle_half_to_double(rd16(blk));
+          const uint8_t* qs = blk + 2;
+          int64_t isum = 0, iabs = 0;
+          for (int e = 0; e < 128; ++e) {
+            int c = (qs[e / 4] >> (2 * (e % 4))) & 3; /* reading R4 */
+            int t = (c - 1) * q[m * K + b * 128 + e];
+            isum += t;
+            iabs += t < 0 ? -t : t;
+          }
+          double da = d * (double)a[m * nb + b];
+          s += da * (double)isum;
+          bnd += fabs(da) * (double)iabs;
+        }
+        y[m * N + n] = s;
+        if (bound) bound[m * N + n] = bnd;
+      }
+    }
+  }
+  free(q);
+  free(a);
+  return rc;
 }

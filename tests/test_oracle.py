@@ -149,6 +149,96 @@ def test_pq2_second_block_and_row_use_their_own_scale():
     assert np.all(w[1, :128] == 4.0) and np.all(w[1, 128:] == 8.0)
 
 
+# ------------------------------------------------- PQ2 integer path ---
+
+def test_int8_quantizer_scale_range_and_ties(golden_dir):
+    """Pin: the group scale maps the group's largest |x| to +-q_max; ties
+    round to even; a zero group has scale 0 and codes 0."""
+    gi = json.load(open(os.path.join(golden_dir, "pq2_int8.json")))
+    G, QM = gi["group"], gi["q_max"]
+    x = np.zeros((2, 3 * G), dtype=np.float16)
+    # group 0: amax = 127 makes the scale exactly 1, so x / a is x itself
+    x[0, :8] = [127.0, 2.5, 3.5, -2.5, -0.5, 1.5, -126.5, 0.25]
+    # group 1: random; group 2: all zero; row 1: negative extreme
+    x[0, G:2 * G] = inputs.x_fp16(inputs.rng("int8/x"), 1, G)[0]
+    x[1, :G] = -np.abs(inputs.x_fp16(inputs.rng("int8/x2"), 1, G)[0])
+    q, a = oracle.quantize_x_int8(x)
+    assert q.dtype == np.int8 and q.shape == x.shape and a.shape == (2, 3)
+    assert a[0, 0] == 1.0
+    assert list(q[0, :8]) == [127, 2, 4, -2, 0, 2, -126, 0]
+    assert np.all(q[0, 8:G] == 0)
+    assert a[0, 2] == 0.0 and np.all(q[0, 2 * G:] == 0)
+    assert a[1, 1] == 0.0 and a[1, 2] == 0.0 and np.all(q[1, G:] == 0)
+    for m, g in ((0, 1), (1, 0)):
+        xg = x[m, g * G:(g + 1) * G].astype(np.float64)
+        qg = q[m, g * G:(g + 1) * G].astype(np.int64)
+        amax = np.abs(xg).max()
+        assert abs(a[m, g] * QM - amax) <= amax * 2.0 ** -23
+        assert np.abs(qg).max() == QM and np.all(np.abs(qg) <= QM)
+        assert qg[np.argmax(np.abs(xg))] == np.sign(xg[np.argmax(np.abs(xg))]) * QM
+        # each code is a nearest integer of x / a (up to one fp32 rounding)
+        assert np.all(np.abs(xg / float(a[m, g]) - qg) <= 0.5 + QM * 2.0 ** -23)
+
+
+def _on_grid_x(seed: str, M: int, K: int, zero_groups=()):
+    """x_i = q_i * 2^-7 with integer |q_i| <= 127 and one +-127 per group:
+    the int8 scale is then 2^-7 exactly and quantisation is lossless."""
+    g = inputs.rng(seed)
+    q = g.integers(-127, 128, size=(M, K))
+    q[:, ::128] = np.where(g.random((M, K // 128)) < 0.5, -127, 127)
+    for m, grp in zero_groups:
+        q[m, grp * 128:(grp + 1) * 128] = 0
+    return (q * 2.0 ** -7).astype(np.float16)
+
+
+def test_pq2_int8_is_exact_for_activations_on_the_int8_grid():
+    """Pin: when every activation is a_g * q_i exactly, the integer path
+    reproduces the exact PQ2_0 GEMV (all sums are exact in fp64)."""
+    N, K, M = 37, 1024, 3
+    packed = inputs.pq2_packed(inputs.rng("int8/w"), N, K)
+    x = _on_grid_x("int8/grid", M, K, zero_groups=[(1, 2), (2, 7)])
+    q, a = oracle.quantize_x_int8(x)
+    assert a[0, 0] == 2.0 ** -7 and a[1, 2] == 0.0
+    assert np.array_equal(q.astype(np.float64) * np.repeat(a, 128, axis=1), x.astype(np.float64))
+    y, b = oracle.gemv_pq2_int8(N, K, packed, x)
+    ye, be = oracle.gemv("pq2_0", N, K, packed, None, None, x)
+    assert np.array_equal(y, ye) and np.array_equal(b, be)
+
+
+def test_pq2_int8_page_maximum_inner_sum(golden_dir):
+    """Pin: all-(+1) codes against a group at the positive maximum give the
+    page's largest inner sum; all-(-1) codes against the negative maximum
+    give the same; the result is d * a * sum."""
+    gi = json.load(open(os.path.join(golden_dir, "pq2_int8.json")))
+    G = gi["group"]
+    for code_byte, xv in ((0xAA, 1.0), (0x00, -1.0)):
+        packed = np.concatenate([_pq2_block(0.5, bytes([code_byte] * 32)),
+                                 _pq2_block(2.0, bytes([0x55] * 32))])
+        x = np.full((1, 2 * G), xv, dtype=np.float16)
+        y, b = oracle.gemv_pq2_int8(1, 2 * G, packed, x)
+        a = float(np.float32(1.0) / np.float32(gi["q_max"]))
+        assert y[0, 0] == 0.5 * a * gi["max_inner_sum"] and b[0, 0] == y[0, 0]
+        assert gi["max_inner_sum"] == G * gi["q_max"]
+
+
+def test_pq2_int8_error_within_quantisation_bound():
+    """Pin: against the exact GEMV, the integer path errs by at most half a
+    step of each group's scale per nonzero weight (plus one fp32 rounding of
+    x / a), and it does err on general activations."""
+    N, K, M = 64, 2048, 4
+    packed = inputs.pq2_packed(inputs.rng("int8/w2"), N, K)
+    x = inputs.x_fp16(inputs.rng("int8/x3"), M, K)
+    y, b = oracle.gemv_pq2_int8(N, K, packed, x)
+    ye, _ = oracle.gemv("pq2_0", N, K, packed, None, None, x)
+    _, a = oracle.quantize_x_int8(x)
+    W = np.abs(oracle.dequant("pq2_0", N, K, packed))
+    step = np.repeat(a.astype(np.float64), 128, axis=1)          # [M, K]
+    lim = (step * (0.5 + 127 * 2.0 ** -23)) @ W.T
+    assert np.all(np.abs(y - ye) <= lim * (1 + 1e-12))
+    assert np.count_nonzero(y != ye) > y.size // 2
+    assert np.all(b >= np.abs(y))
+
+
 # ---------------------------------------------------------------- Q4_0 ---
 
 def test_q4_0_roundtrip_is_exact_for_representable_blocks():

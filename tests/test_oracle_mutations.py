@@ -35,6 +35,12 @@ MUTATIONS = {
     "cbk4_row neighbour's codebook": [("const uint8_t* cb = (const uint8_t*)codebooks + n * 16 * 4;",
                                        "const uint8_t* cb = (const uint8_t*)codebooks + (n ^ 1) * 16 * 4;")],
     "cbk4_row nibble order": [("w[2 * j] = rdf32(cb, row[j] & 0x0f);", "w[2 * j] = rdf32(cb, row[j] >> 4);")],
+    "int8 ties away from zero": [("float r = rintf(", "float r = roundf(")],
+    "int8 scale over 128": [("float s = amax / 127.0f;", "float s = amax / 128.0f;")],
+    "int8 block scale dropped": [("double da = d * (double)a[m * nb + b];", "double da = (double)a[m * nb + b];")],
+    "int8 group scale of row 0": [("double da = d * (double)a[m * nb + b];", "double da = d * (double)a[b];")],
+    "int8 codes of the next group": [("int t = (c - 1) * q[m * K + b * 128 + e];",
+                                      "int t = (c - 1) * q[m * K + ((b + 1) % nb) * 128 + e];")],
     "bound without abs": [("b += fabs(t);", "b += t;")],
     "x transposed against w": [("double t = xd[m * K + k] * w[k];",
                                 "double t = xd[m * K + (K - 1 - k)] * w[k];")],
