@@ -298,6 +298,11 @@ def run_ours(args, rank, world, device):
     R = 1 if one_copy >= 3 * l2 else -(-3 * l2 // one_copy)
     copies = [build_handles(specs, M, device, seed=r) for r in range(R)]
     ops = [o for c_ops, _, _ in copies for o in c_ops]
+    if args.x_int8:  # PQ2_0 integer path: INT8 activations per group of 128
+        for o in ops:
+            if o["fmt"] == "pq2_0":
+                o["h"].set_x_int8(True)
+                o["x_int8"] = True
     log(f"[bench] rank {rank}: {len(specs)} GEMVs x {R} copies ready in {time.time() - t_setup:.1f}s")
 
     step_bytes = sum(o["bytes"] for o in ops)
@@ -398,7 +403,8 @@ def run_ours(args, rank, world, device):
     if os.path.exists(prof):
         try:
             pj = json.load(open(prof))
-            entry = pj.get(args.workload if M == 1 else f"{args.workload}/M={M}")
+            entry = pj.get((args.workload if M == 1 else f"{args.workload}/M={M}")
+                           + ("/x_int8" if args.x_int8 else ""))
             if entry and entry.get("kernel_source_hash") == kernel_source_hash():
                 traffic = entry.get("dram_bytes_per_launch")
         except Exception:
@@ -415,16 +421,18 @@ def run_ours(args, rank, world, device):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f32",
+        "dtype": "int8xint2->int32, f32" if args.x_int8 else "f32",
         "data": "synthetic",
-        "config": {"workload": args.workload, "description": desc, "M": M,
+        "config": {"workload": args.workload, "description": desc + (", INT8 activations" if args.x_int8 else ""),
+                   "M": M, "x_int8": bool(args.x_int8),
                    "gemvs_per_step": len(ops), "bytes_per_step": step_bytes,
                    "l2": (f"weights larger than 3x L2 ({l2 >> 20} MiB): no flush needed" if R == 1 else
                           f"weights rotate through {R} copies ({R * one_copy / 1e6:.0f} MB > 3x L2 of {l2 >> 20} MiB)"),
                    "parallelism": f"replicas{world}", "peak_hbm_gbs": peak,
                    "frac_of_peak": round(value / world / peak, 4)},
         "roofline": {"bound": "hbm",
-                     "kernel": (f"aqlm_gemv_kernel<MB={M}>" if dominant == "aqlm_2x8" and M <= 2
+                     "kernel": ("gemv_kernel<FmtPQ2I8, M=1>, one launch per activation row" if args.x_int8
+                                else f"aqlm_gemv_kernel<MB={M}>" if dominant == "aqlm_2x8" and M <= 2
                                 else (f"gemv_kernel<{dominant}, M=1>"
                                       + (" and gemv_rowgroup_kernel (matrices of at most one 32-row group per SM)"
                                          if dominant in ("cbk4", "cbk8") else "")) if M == 1
@@ -436,11 +444,13 @@ def run_ours(args, rank, world, device):
                      "avg_launch_us": round(dom_ms / K / max(1, dom_launches) * 1e3, 3)},
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": K_e2e},
-        "gpu_launches": len(ops) * K,  # one launch per GEMV (AQLM: one table pass for M <= 2, else the tensor-core kernel)
+        # one launch per GEMV (AQLM: one table pass for M <= 2, else the
+        # tensor-core kernel); the INT8 path launches once per activation row
+        "gpu_launches": sum(M if o.get("x_int8") else 1 for o in ops) * K,
         "clocks": clocks,
     }
     if not args.no_cpu_baseline and world == 1:
-        line["cpu_baseline"] = cpu_baseline(args.workload, M, budget_s=args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(args.workload, M, budget_s=args.cpu_seconds, x_int8=args.x_int8)
     return line
 
 
@@ -472,29 +482,34 @@ def oracle_sample(workload, M, rows, seed=0):
     return fmt, name, rows, K, packed, scales, cb, x, nbytes
 
 
-def time_oracle(workload, M, rows, threads, reps=1):
+def time_oracle(workload, M, rows, threads, reps=1, x_int8=False):
     import oracle
     fmt, name, rows, K, packed, scales, cb, x, nbytes = oracle_sample(workload, M, rows)
+    int8 = x_int8 and fmt == "pq2_0"
     t0 = time.perf_counter()
     for _ in range(reps):
-        oracle.gemv(fmt, rows, K, packed, scales, cb, x, nthreads=threads)
+        if int8:
+            oracle.gemv_pq2_int8(rows, K, packed, x, nthreads=threads)
+        else:
+            oracle.gemv(fmt, rows, K, packed, scales, cb, x, nthreads=threads)
     dt = time.perf_counter() - t0
-    return dt, nbytes * reps, f"{reps} x {rows} rows of {name} ({fmt}, K={K}), M={M}"
+    return dt, nbytes * reps, (f"{reps} x {rows} rows of {name} ({fmt}{', INT8 activations' if int8 else ''}, "
+                               f"K={K}), M={M}")
 
 
-def cpu_baseline(workload, M, budget_s=15.0):
+def cpu_baseline(workload, M, budget_s=15.0, x_int8=False):
     """The oracle as it stands on the host cores, on a bounded sample (about
     budget_s seconds of work: repeated passes over rows of the workload's
     first matrix)."""
     threads = os.cpu_count() or 1
     rows, reps = 256, 1
-    dt, nbytes, desc = time_oracle(workload, M, rows, threads, reps)
+    dt, nbytes, desc = time_oracle(workload, M, rows, threads, reps, x_int8)
     while dt < budget_s / 2:
         if rows < 4096:
             rows *= 4
         else:
             reps = max(reps * 2, int(reps * budget_s / max(dt, 1e-3) * 0.6))
-        dt, nbytes, desc = time_oracle(workload, M, rows, threads, reps)
+        dt, nbytes, desc = time_oracle(workload, M, rows, threads, reps, x_int8)
     return {"value": round(nbytes / dt / 1e9, 4), "unit": UNIT, "cores": threads,
             "kind": "oracle", "sample": desc, "seconds": round(dt, 3)}
 
@@ -506,15 +521,16 @@ def run_reference(args, rank, world):
     total_budget = args.cpu_seconds * 4
     per_step = max(0.05, total_budget / max(1, args.steps + args.warmup))
     rows = 64
-    dt, nbytes, desc = time_oracle(args.workload, args.m, rows, threads)
+    i8 = args.x_int8
+    dt, nbytes, desc = time_oracle(args.workload, args.m, rows, threads, x_int8=i8)
     while dt < per_step / 2 and rows < 65536:
         rows *= 2
-        dt, nbytes, desc = time_oracle(args.workload, args.m, rows, threads)
+        dt, nbytes, desc = time_oracle(args.workload, args.m, rows, threads, x_int8=i8)
     for _ in range(args.warmup):
-        time_oracle(args.workload, args.m, rows, threads)
+        time_oracle(args.workload, args.m, rows, threads, x_int8=i8)
     times = []
     for _ in range(args.steps):
-        dt, nbytes, desc = time_oracle(args.workload, args.m, rows, threads)
+        dt, nbytes, desc = time_oracle(args.workload, args.m, rows, threads, x_int8=i8)
         times.append(dt)
     tot = sum(times)
     value = nbytes * len(times) / tot / 1e9
@@ -524,8 +540,8 @@ def run_reference(args, rank, world):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(tot / len(times) * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": args.workload, "description": wdesc, "M": args.m,
-                   "parallelism": f"replicas{world}"},
+        "config": {"workload": args.workload, "description": wdesc + (", INT8 activations" if i8 else ""),
+                   "M": args.m, "x_int8": bool(i8), "parallelism": f"replicas{world}"},
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": threads,
                          "kind": "oracle", "sample": desc},
         "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -545,9 +561,13 @@ def main():
     ap.add_argument("--m", type=int, default=1)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--x-int8", action="store_true",
+                    help="PQ2_0 workloads: INT8 activations (the integer path, lossy by design)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.x_int8 and WORKLOADS[args.workload][1] != "pq2_0":
+        ap.error("--x-int8 needs a PQ2_0 workload")
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

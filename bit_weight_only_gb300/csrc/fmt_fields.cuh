@@ -397,4 +397,155 @@ struct FmtPQ2 {
   }
 };
 
+// -------------------------------------------- PQ2_0, INT8 activations --
+//
+// The integer path of "Making a ternary reasoning model fast in vLLM" (the
+// section on quantising the activation too): every group of 128
+// activations -- one PQ2_0 block's inputs, i.e. one slice of a tile -- is
+// scaled to signed INT8, x_i ~ a q_i with
+//     a = fl32(max |x_i| / 127),   q_i = clamp(rint(fl32(x_i / a)), -127, 127)
+// (IEEE divisions, ties to even; a zero group has a = 0, q = 0), so the inner
+// sum over the block's codes is an integer, and floating point is used once
+// per block: y += d * (a * sum_i (c_i - 1) q_i).  Lossy by design; the
+// weights are the plain PQ2_0 tiles.
+//
+// Staging puts the group's INT8 codes in the order the code words want:
+// lane l holds x at k = 16 (l / 4) + 4 b + (l % 4), b = 0..3, so its four q
+// packed into one word form, for code word i = l / 4 (k = 16 i .. 16 i + 15),
+// the word Q_s (s = l % 4) whose byte b is q[16 i + 4 b + s].  A code word
+// w holds field jj (k = 16 i + jj) at bits 2 jj, so byte b of
+//     w & 0x03030303, w & 0x0C0C0C0C, (w >> 4) & 0x03030303, (w >> 4) & 0x0C0C0C0C
+// is field 4b, 4 x field 4b+1, field 4b+2, 4 x field 4b+3: four DP4As against
+// Q_0 .. Q_3 give sum c q over sixteen weights (the two "times 4" terms in
+// their own accumulator, divided by 4 exactly at the end of the block).
+// The offset c - 1 is applied with the group's sum of q.
+
+// Warp-collective: the 128 values of one group, four per lane, to INT8.
+// Every lane gets the group scale a and the group sum of q.
+__device__ __forceinline__ void quant_i8_group(const float (&f)[4], float& a, int (&q)[4], int& qsum) {
+  float am = fmaxf(fmaxf(fabsf(f[0]), fabsf(f[1])), fmaxf(fabsf(f[2]), fabsf(f[3])));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, off));
+  a = __fdiv_rn(am, 127.0f);
+  int sum = 0;
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    int v = 0;
+    if (a != 0.0f) v = min(127, max(-127, __float2int_rn(__fdiv_rn(f[b], a))));
+    q[b] = v;
+    sum += v;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+  qsum = sum;
+}
+
+// Position (inside its group of 128) of lane l's b-th activation.
+__host__ __device__ constexpr int i8_pos(int lane, int b) { return 16 * (lane >> 2) + 4 * b + (lane & 3); }
+
+struct FmtPQ2I8 {
+  static constexpr int kKW = FmtPQ2::kKW;  // 128: one block, one INT8 group
+  static constexpr int kKT = FmtPQ2::kKT;
+  static constexpr int kCodeBytes = FmtPQ2::kCodeBytes;
+  static constexpr int kTileBytes = FmtPQ2::kTileBytes;
+  static constexpr int kCtasPerSm = 2;
+  static constexpr bool kTileParity = false;
+  __host__ __device__ static constexpr int stages(int) { return 2; }
+  static constexpr int kSharedBytes = 0;
+  static constexpr float kOutScale = 1.0f;
+  static constexpr int kSumGroups = 2;  // [0]: the group's sum of q (exact in fp32), [1]: its scale a
+  static constexpr int kCbEntries = 0;
+  using XRegs = XRegsT<4>;
+  struct XScale {};
+
+  template <int NT>
+  __device__ static void init_shared(uint8_t*, const uint16_t*, int, int) {}
+  __device__ static void x_scales(XScale&, int) {}
+
+  template <int M>
+  __device__ static void load_x(XRegs& xr, const GemvParams& p, int kt, int slice, int lane) {
+    const int64_t kbase = static_cast<int64_t>(kt) * kKT + slice * kKW;
+    const unsigned short* xb = reinterpret_cast<const unsigned short*>(p.x);
+#pragma unroll
+    for (int m = 0; m < M; ++m)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const int64_t k = kbase + i8_pos(lane, b);
+        xr.v[m][b] = (k < p.K) ? __ldg(xb + m * p.K + k) : static_cast<unsigned short>(0);
+      }
+  }
+
+  // xs (per warp): for each m, 32 words Q (128 bytes), word l from lane l.
+  template <int M>
+  __device__ static void stage_x(float* xs, float (&xsum)[kSumGroups][M], const XRegs& xr, const XScale&,
+                                 int lane) {
+    uint32_t* xq = reinterpret_cast<uint32_t*>(xs);
+#pragma unroll
+    for (int m = 0; m < M; ++m) {
+      float f[4];
+#pragma unroll
+      for (int b = 0; b < 4; ++b) f[b] = h2f(xr.v[m][b]);
+      float a;
+      int q[4], qsum;
+      quant_i8_group(f, a, q, qsum);
+      xq[m * 32 + lane] = (static_cast<uint32_t>(q[0]) & 0xffu) | ((static_cast<uint32_t>(q[1]) & 0xffu) << 8) |
+                          ((static_cast<uint32_t>(q[2]) & 0xffu) << 16) | (static_cast<uint32_t>(q[3]) << 24);
+      xsum[0][m] = static_cast<float>(qsum);
+      xsum[1][m] = a;
+    }
+  }
+
+  template <int M, int RPW>
+  __device__ static void tile_math(const uint8_t* stage, const float* xs,
+                                   const float (&xsum)[kSumGroups][M], RowAcc<M, RPW>& yacc,
+                                   uint8_t*, int slice, int half, int lane, uint64_t* empty_bar) {
+    static_assert(RPW == kRowsPerLane, "one warp per slice: the lane's four rows");
+    const int t = slice * 32 + lane;
+    uint4 clo[RPW], chi[RPW];
+    load_codes32<RPW>(stage, 0, t, clo, chi);
+    const uint2 sc = *reinterpret_cast<const uint2*>(stage + kCodeBytes + t * 8);
+    release_stage(empty_bar, lane);
+
+    int lo[RPW][M], hi[RPW][M];
+#pragma unroll
+    for (int r = 0; r < RPW; ++r)
+#pragma unroll
+      for (int m = 0; m < M; ++m) lo[r][m] = hi[r][m] = 0;
+    const uint8_t* xq = reinterpret_cast<const uint8_t*>(xs);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      uint4 Q[M];
+#pragma unroll
+      for (int m = 0; m < M; ++m) Q[m] = lds128(xq + m * 128 + 16 * i);
+#pragma unroll
+      for (int r = 0; r < RPW; ++r) {
+        const uint32_t w = word8(clo[r], chi[r], i);
+        const uint32_t w4 = w >> 4;
+        const int c0 = static_cast<int>(w & 0x03030303u), c1 = static_cast<int>(w & 0x0C0C0C0Cu);
+        const int c2 = static_cast<int>(w4 & 0x03030303u), c3 = static_cast<int>(w4 & 0x0C0C0C0Cu);
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+          lo[r][m] = __dp4a(c0, static_cast<int>(Q[m].x), lo[r][m]);
+          hi[r][m] = __dp4a(c1, static_cast<int>(Q[m].y), hi[r][m]);
+          lo[r][m] = __dp4a(c2, static_cast<int>(Q[m].z), lo[r][m]);
+          hi[r][m] = __dp4a(c3, static_cast<int>(Q[m].w), hi[r][m]);
+        }
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < RPW; ++r) {
+      const uint32_t sw = r < 2 ? sc.x : sc.y;
+      const float d = h2f((r & 1) ? (sw >> 16) : (sw & 0xffffu));
+      float v[M];
+#pragma unroll
+      for (int m = 0; m < M; ++m) {
+        // hi is four times an integer, so the shift divides exactly
+        const int inner = lo[r][m] + (hi[r][m] >> 2) - static_cast<int>(xsum[0][m]);
+        v[m] = __fmul_rn(xsum[1][m], static_cast<float>(inner));
+      }
+      yacc.add_row(r, d, v);
+    }
+  }
+};
+
 }  // namespace qgemv

@@ -1,5 +1,6 @@
-// fmt_pq2.cu -- PQ2_0: re-layout (prepare), exact decode export and the
-// launch table of the GEMV kernel for M = 1..16.
+// fmt_pq2.cu -- PQ2_0: re-layout (prepare), exact decode export, the
+// launch table of the GEMV kernel for M = 1..16, and the INT8-activation
+// path (FmtPQ2I8) with its activation quantizer.
 //
 // Canonical PQ2_0 ("Making a ternary reasoning model fast in vLLM", section
 // "Anatomy of a PQ2_0 block"): per output row n, K/128 blocks of
@@ -122,15 +123,78 @@ cudaError_t dequant(const uint8_t* tiles, const void*, const int32_t*, int64_t N
   return cudaGetLastError();
 }
 
+// ---- INT8 activations (FmtPQ2I8): the same tiles, the M = 1 kernel ----
+
+using I8 = LaunchTable<FmtPQ2I8>;
+
+cudaError_t setup() {
+  cudaError_t e = LaunchTable<F>::setup();
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(gemv_kernel<FmtPQ2I8, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             gemv_smem_bytes<FmtPQ2I8, 1>());
+  return e;
+}
+
+// One launch of the M = 1 kernel per activation row: each row's result is
+// that of a one-row call (batch invariant by construction).  Consecutive
+// launches on the stream are ordered by the kernel's grid-dependency wait.
+cudaError_t launch_x_int8(int M, const GemvParams& p, const LaunchGeom& g, cudaStream_t s) {
+  if (M < 1 || M > kMaxM) return cudaErrorInvalidValue;
+  for (int m = 0; m < M; ++m) {
+    GemvParams q = p;
+    q.x = p.x + m * p.K;
+    q.y = p.y + m * p.N;
+    q.residual = p.residual != nullptr ? p.residual + m * p.N : nullptr;
+    q.plan = g.plan_m1;
+    const cudaError_t e = I8::launch_m1(q, g.grid_m1, s);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+// One warp per group of 128 activations: the same quantizer as the GEMV's
+// staging, written out in plain [M][K] order with the scales [M][K/128].
+__global__ void quantize_x_int8_kernel(const unsigned short* __restrict__ x, int64_t groups, int64_t K,
+                                       int8_t* __restrict__ q, float* __restrict__ a) {
+  const int lane = threadIdx.x & 31;
+  const int64_t ng = K / 128;
+  const int64_t wstride = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t gi = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5; gi < groups;
+       gi += wstride) {
+    const int64_t base = (gi / ng) * K + (gi % ng) * 128;
+    float f[4];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) f[b] = h2f(__ldg(x + base + i8_pos(lane, b)));
+    float sc;
+    int qv[4], qsum;
+    quant_i8_group(f, sc, qv, qsum);
+#pragma unroll
+    for (int b = 0; b < 4; ++b) q[base + i8_pos(lane, b)] = static_cast<int8_t>(qv[b]);
+    if (lane == 0) a[gi] = sc;
+  }
+}
+
 }  // namespace
 
 const FormatOps* ops_pq2() {
   static const FormatOps ops = {
       /*format=*/4, F::kKT, F::kTileBytes, /*aux_bytes=*/0,
-      &LaunchTable<F>::smem_bytes, &LaunchTable<F>::setup, &LaunchTable<F>::launch,
+      &LaunchTable<F>::smem_bytes, &setup, &LaunchTable<F>::launch,
       &prepare, &dequant, /*cb_entries=*/0, /*tile_rows=*/128, /*partial_stride=*/128 * 16,
-      /*aux_per_row=*/0, /*m1_ctas_per_sm=*/LaunchTable<F>::kM1CtasPerSm};
+      /*aux_per_row=*/0, /*m1_ctas_per_sm=*/LaunchTable<F>::kM1CtasPerSm, /*rowgroup=*/0,
+      /*launch_x_int8=*/&launch_x_int8};
+  static_assert(I8::kM1CtasPerSm == LaunchTable<F>::kM1CtasPerSm && FmtPQ2I8::kKT == F::kKT &&
+                    FmtPQ2I8::kTileBytes == F::kTileBytes,
+                "the INT8 path runs on the PQ2_0 handle's tiles, grid and plan");
   return &ops;
+}
+
+cudaError_t quantize_x_int8(const void* x, int64_t M, int64_t K, int8_t* q, float* a, cudaStream_t s) {
+  const int64_t groups = M * (K / 128);
+  const int64_t blocks = (groups + 7) / 8;
+  quantize_x_int8_kernel<<<static_cast<int>(blocks > 4096 ? 4096 : blocks), 256, 0, s>>>(
+      static_cast<const unsigned short*>(x), groups, K, q, a);
+  return cudaGetLastError();
 }
 
 }  // namespace qgemv

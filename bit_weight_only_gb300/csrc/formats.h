@@ -55,6 +55,8 @@ struct FormatOps {
   int64_t aux_per_row = 0;          // aux bytes per output row, after aux_bytes
   int m1_ctas_per_sm = 1;           // CTAs per SM of the M = 1 kernel (LaunchGeom::grid_m1)
   int rowgroup = 0;                 // has the M = 1 row-group kernel (rowgroup_kernel.cuh)
+  // PQ2_0 only: the run with INT8 activations (qgemv_set_x_int8), else nullptr
+  cudaError_t (*launch_x_int8)(int M, const GemvParams& p, const LaunchGeom& g, cudaStream_t s) = nullptr;
 };
 
 const FormatOps* ops_q4_0();
@@ -67,6 +69,10 @@ const FormatOps* ops_aqlm_mma();  // internal: the AQLM tensor-core layout
 // Record the calling thread's last error (what qgemv_last_error returns);
 // returns `code`.  QGEMV_OK clears it.
 int report_error(int code, const char* msg);
+
+// PQ2_0 INT8 activation quantizer: x fp16 [M][K] (K % 128 == 0) -> q int8
+// [M][K], a fp32 [M][K/128]; the GEMV's own staging arithmetic.
+cudaError_t quantize_x_int8(const void* x, int64_t M, int64_t K, int8_t* q, float* a, cudaStream_t s);
 
 // Q4_0 quantizer (canonical output).
 cudaError_t quantize_q4_0(const float* w, int64_t N, int64_t K, uint8_t* out, cudaStream_t s);

@@ -1,6 +1,6 @@
 // gemv_kernel.cuh -- the CUDA-core weight-streaming GEMV kernel of the tile
-// formats (Q4_0, PQ2_0, CBK4, CBK8), used for M = 1, and the stream-K
-// finisher shared by every kernel.
+// formats (Q4_0, PQ2_0, CBK4, CBK8, and PQ2_0 with INT8 activations), used
+// for M = 1, and the stream-K finisher shared by every kernel.
 //
 //   y[m][n] = sum_k x[m][k] * w[n][k]      (1 <= M <= 16, fp32 accumulation)
 //

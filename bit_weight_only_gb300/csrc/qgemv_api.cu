@@ -206,6 +206,7 @@ struct qgemv_ctx {
   int32_t* seg_of_rt;  // inside aux (table formats), else nullptr
   int* err;
   int batch_invariant;  // qgemv_set_batch_invariant
+  int x_int8;           // qgemv_set_x_int8 (PQ2_0)
   int skip_cta;         // QGEMV_FAULT_SKIP_CTA test hook, -1 normally
   qgemv_ctx* mma;       // AQLM: the tensor-core companion (format kAqlmMma), else nullptr
 };
@@ -502,7 +503,8 @@ static int run_impl(qgemv_handle h, const void* x, int M, float* y, const float*
   p.skip_cta = h->skip_cta;
   p.residual = residual;
   const qgemv::LaunchGeom g = {h->grid, h->plan, h->grid_m1, h->plan_m1, h->grid_rg};
-  cudaError_t e = h->ops->launch(M, p, g, static_cast<cudaStream_t>(stream), inv);
+  cudaError_t e = h->x_int8 ? h->ops->launch_x_int8(M, p, g, static_cast<cudaStream_t>(stream))
+                            : h->ops->launch(M, p, g, static_cast<cudaStream_t>(stream), inv);
   if (e != cudaSuccess) return cuda_error(e, "launching the GEMV kernel");
   return ok();
 }
@@ -521,6 +523,24 @@ int qgemv_run_residual(qgemv_handle h, const void* x, int M, float* y, const flo
 int qgemv_set_batch_invariant(qgemv_handle h, int on) {
   if (!valid(h)) return set_error(QGEMV_ERR_ARG, "invalid handle");
   h->batch_invariant = on ? 1 : 0;
+  return ok();
+}
+
+int qgemv_set_x_int8(qgemv_handle h, int on) {
+  if (!valid(h)) return set_error(QGEMV_ERR_ARG, "invalid handle");
+  if (h->ops->launch_x_int8 == nullptr)
+    return set_error(QGEMV_ERR_ARG, "INT8 activations need a PQ2_0 handle (format %d)", h->format);
+  h->x_int8 = on ? 1 : 0;
+  return ok();
+}
+
+int qgemv_quantize_x_int8(const void* x, int M, int64_t K, int8_t* q_out, float* a_out, void* stream) {
+  if (!x || !q_out || !a_out) return set_error(QGEMV_ERR_ARG, "x, q_out or a_out is NULL");
+  if (M < 1 || K <= 0 || K % 128) return set_error(QGEMV_ERR_ARG, "M must be >= 1 and K a positive multiple of 128");
+  if ((reinterpret_cast<uintptr_t>(x) & 1) || (reinterpret_cast<uintptr_t>(a_out) & 3))
+    return set_error(QGEMV_ERR_ALIGN, "x must be 2-byte and a_out 4-byte aligned");
+  cudaError_t e = qgemv::quantize_x_int8(x, M, K, q_out, a_out, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_error(e, "launching the activation quantizer");
   return ok();
 }
 

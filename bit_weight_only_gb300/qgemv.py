@@ -34,6 +34,9 @@ _SIGNATURES = {
     "qgemv_run_residual": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
                                           ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "qgemv_set_batch_invariant": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int]),
+    "qgemv_set_x_int8": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int]),
+    "qgemv_quantize_x_int8": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64,
+                                             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "qgemv_dequant": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "qgemv_quantize_q4_0": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
                                            ctypes.c_void_p, ctypes.c_void_p]),
@@ -143,6 +146,14 @@ def qgemv_set_batch_invariant(h: int, on: bool) -> int:
     return _check(load().qgemv_set_batch_invariant(h, 1 if on else 0))
 
 
+def qgemv_set_x_int8(h: int, on: bool) -> int:
+    return _check(load().qgemv_set_x_int8(h, 1 if on else 0))
+
+
+def qgemv_quantize_x_int8(x: int, M: int, K: int, q_out: int, a_out: int, stream=None) -> int:
+    return _check(load().qgemv_quantize_x_int8(x, M, K, q_out, a_out, _stream_ptr(stream)))
+
+
 def qgemv_status(h: int) -> int:
     return _check(load().qgemv_status(h))
 
@@ -237,6 +248,9 @@ class QGemv:
     def set_batch_invariant(self, on: bool = True):
         qgemv_set_batch_invariant(self.handle, on)
 
+    def set_x_int8(self, on: bool = True):
+        qgemv_set_x_int8(self.handle, on)
+
     def close(self):
         if getattr(self, "handle", None):
             qgemv_destroy(self.handle)
@@ -256,3 +270,14 @@ def quantize_q4_0(w, stream=None):
     out = torch.empty(qgemv_packed_bytes(Q4_0, N, K), dtype=torch.uint8, device=w.device)
     qgemv_quantize_q4_0(w.contiguous().data_ptr(), N, K, out.data_ptr(), stream)
     return out
+
+
+def quantize_x_int8(x, stream=None):
+    """PQ2_0 INT8 activation quantizer on the GPU: fp16 CUDA tensor [M, K]
+    -> (int8 [M, K], fp32 scales [M, K/128]) CUDA tensors."""
+    import torch
+    M, K = x.shape
+    q = torch.empty((M, K), dtype=torch.int8, device=x.device)
+    a = torch.empty((M, K // 128), dtype=torch.float32, device=x.device)
+    qgemv_quantize_x_int8(x.contiguous().data_ptr(), M, K, q.data_ptr(), a.data_ptr(), stream)
+    return q, a

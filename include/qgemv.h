@@ -146,6 +146,32 @@ int qgemv_run_residual(qgemv_handle h, const void* x, int M, float* y, const flo
  * runs issued after the call; returns QGEMV_ERR_ARG for an invalid handle. */
 int qgemv_set_batch_invariant(qgemv_handle h, int on);
 
+/* INT8 activations for a PQ2_0 handle (off by default): the integer path of
+ * "Making a ternary reasoning model fast in vLLM" (the section on quantising
+ * the activation too).  When on, runs quantize each group of 128 activations
+ * of a row to signed INT8 exactly as qgemv_quantize_x_int8 does, take every
+ * block's inner sum over its codes in integer arithmetic (four-way INT8 dot
+ * products) and apply d * a once per block in fp32.  The result is that of
+ * the quantized activations: lossy against qgemv_run with the mode off (the
+ * quantization error is a property of the method, at most half a step of
+ * each group's scale per nonzero weight), and accurate to the usual fp32
+ * bound against the exact integer-path value.  Each activation row is one
+ * launch of the one-row kernel, so results never depend on M.  Works with
+ * qgemv_run and qgemv_run_residual; takes effect for runs issued after the
+ * call.  Returns QGEMV_ERR_ARG for an invalid handle or a handle that is not
+ * PQ2_0 (stacked PQ2_0 handles are accepted).                               */
+int qgemv_set_x_int8(qgemv_handle h, int on);
+
+/* The INT8 activation quantizer of the PQ2_0 integer path, on the device:
+ *   x: device fp16 [M][K] row-major, K a positive multiple of 128, M >= 1;
+ *   q_out: device int8 [M][K];  a_out: device fp32 [M][K/128].
+ * Per group g of 128 consecutive inputs of a row: a = fl32(max|x| / 127),
+ * q = clamp(rint(fl32(x / a)), -127, 127) with IEEE fp32 divisions and
+ * ties to even; an all-zero group gives a = 0 and q = 0.  The same device
+ * arithmetic as the GEMV's staging (for tests and for callers that keep
+ * the quantized activations).  Asynchronous on `stream`.                   */
+int qgemv_quantize_x_int8(const void* x, int M, int64_t K, int8_t* q_out, float* a_out, void* stream);
+
 /* Write the decoded weights, fp32 [N][K] row-major, to device memory w_out
  * (the exact value of every weight; read back from the prepared tiles, so it
  * also checks the re-layout).  Asynchronous on `stream`.                     */
