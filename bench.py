@@ -269,6 +269,12 @@ class ClockSampler:
 
 # ----------------------------------------------------------- our arm ------
 
+def x_int8_launches(M):
+    """Launches of one PQ2_0 INT8-path call: rows go four, then two, then one
+    at a time."""
+    return M // 4 + (M % 4) // 2 + M % 2
+
+
 def max_over_ranks(values, world, device):
     """Each value's maximum over the ranks (the slowest rank sets the job's
     time); the values themselves on one rank."""
@@ -431,7 +437,7 @@ def run_ours(args, rank, world, device):
                    "parallelism": f"replicas{world}", "peak_hbm_gbs": peak,
                    "frac_of_peak": round(value / world / peak, 4)},
         "roofline": {"bound": "hbm",
-                     "kernel": ("gemv_kernel<FmtPQ2I8, M=1>, one launch per activation row" if args.x_int8
+                     "kernel": ("gemv_kernel<FmtPQ2I8, MB>, MB = 4, 2, 1 activation rows per launch" if args.x_int8
                                 else f"aqlm_gemv_kernel<MB={M}>" if dominant == "aqlm_2x8" and M <= 2
                                 else (f"gemv_kernel<{dominant}, M=1>"
                                       + (" and gemv_rowgroup_kernel (matrices of at most one 32-row group per SM)"
@@ -445,8 +451,8 @@ def run_ours(args, rank, world, device):
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": K_e2e},
         # one launch per GEMV (AQLM: one table pass for M <= 2, else the
-        # tensor-core kernel); the INT8 path launches once per activation row
-        "gpu_launches": sum(M if o.get("x_int8") else 1 for o in ops) * K,
+        # tensor-core kernel); the INT8 path launches once per 4, 2 or 1 rows
+        "gpu_launches": sum(x_int8_launches(M) if o.get("x_int8") else 1 for o in ops) * K,
         "clocks": clocks,
     }
     if not args.no_cpu_baseline and world == 1:

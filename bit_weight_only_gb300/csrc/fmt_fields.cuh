@@ -500,50 +500,56 @@ struct FmtPQ2I8 {
                                    const float (&xsum)[kSumGroups][M], RowAcc<M, RPW>& yacc,
                                    uint8_t*, int slice, int half, int lane, uint64_t* empty_bar) {
     static_assert(RPW == kRowsPerLane, "one warp per slice: the lane's four rows");
+    // rows per pass: all four up to M = 2; above, two at a time (the codes of
+    // the later rows are loaded, and the stage released, in the last pass)
+    constexpr int RP = M > 2 ? 2 : RPW;
     const int t = slice * 32 + lane;
-    uint4 clo[RPW], chi[RPW];
-    load_codes32<RPW>(stage, 0, t, clo, chi);
     const uint2 sc = *reinterpret_cast<const uint2*>(stage + kCodeBytes + t * 8);
-    release_stage(empty_bar, lane);
-
-    int lo[RPW][M], hi[RPW][M];
-#pragma unroll
-    for (int r = 0; r < RPW; ++r)
-#pragma unroll
-      for (int m = 0; m < M; ++m) lo[r][m] = hi[r][m] = 0;
     const uint8_t* xq = reinterpret_cast<const uint8_t*>(xs);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      uint4 Q[M];
+    for (int pass = 0; pass < RPW / RP; ++pass) {
+      uint4 clo[RP], chi[RP];
+      load_codes32<RP>(stage, pass * RP, t, clo, chi);
+      if (pass == RPW / RP - 1) release_stage(empty_bar, lane);
+      int lo[RP][M], hi[RP][M];
 #pragma unroll
-      for (int m = 0; m < M; ++m) Q[m] = lds128(xq + m * 128 + 16 * i);
+      for (int r = 0; r < RP; ++r)
 #pragma unroll
-      for (int r = 0; r < RPW; ++r) {
-        const uint32_t w = word8(clo[r], chi[r], i);
-        const uint32_t w4 = w >> 4;
-        const int c0 = static_cast<int>(w & 0x03030303u), c1 = static_cast<int>(w & 0x0C0C0C0Cu);
-        const int c2 = static_cast<int>(w4 & 0x03030303u), c3 = static_cast<int>(w4 & 0x0C0C0C0Cu);
+        for (int m = 0; m < M; ++m) lo[r][m] = hi[r][m] = 0;
 #pragma unroll
-        for (int m = 0; m < M; ++m) {
-          lo[r][m] = __dp4a(c0, static_cast<int>(Q[m].x), lo[r][m]);
-          hi[r][m] = __dp4a(c1, static_cast<int>(Q[m].y), hi[r][m]);
-          lo[r][m] = __dp4a(c2, static_cast<int>(Q[m].z), lo[r][m]);
-          hi[r][m] = __dp4a(c3, static_cast<int>(Q[m].w), hi[r][m]);
+      for (int i = 0; i < 8; ++i) {
+        uint4 Q[M];
+#pragma unroll
+        for (int m = 0; m < M; ++m) Q[m] = lds128(xq + m * 128 + 16 * i);
+#pragma unroll
+        for (int r = 0; r < RP; ++r) {
+          const uint32_t w = word8(clo[r], chi[r], i);
+          const uint32_t w4 = w >> 4;
+          const int c0 = static_cast<int>(w & 0x03030303u), c1 = static_cast<int>(w & 0x0C0C0C0Cu);
+          const int c2 = static_cast<int>(w4 & 0x03030303u), c3 = static_cast<int>(w4 & 0x0C0C0C0Cu);
+#pragma unroll
+          for (int m = 0; m < M; ++m) {
+            lo[r][m] = __dp4a(c0, static_cast<int>(Q[m].x), lo[r][m]);
+            hi[r][m] = __dp4a(c1, static_cast<int>(Q[m].y), hi[r][m]);
+            lo[r][m] = __dp4a(c2, static_cast<int>(Q[m].z), lo[r][m]);
+            hi[r][m] = __dp4a(c3, static_cast<int>(Q[m].w), hi[r][m]);
+          }
         }
       }
-    }
 #pragma unroll
-    for (int r = 0; r < RPW; ++r) {
-      const uint32_t sw = r < 2 ? sc.x : sc.y;
-      const float d = h2f((r & 1) ? (sw >> 16) : (sw & 0xffffu));
-      float v[M];
+      for (int r = 0; r < RP; ++r) {
+        const int row = pass * RP + r;
+        const uint32_t sw = row < 2 ? sc.x : sc.y;
+        const float d = h2f((row & 1) ? (sw >> 16) : (sw & 0xffffu));
+        float v[M];
 #pragma unroll
-      for (int m = 0; m < M; ++m) {
-        // hi is four times an integer, so the shift divides exactly
-        const int inner = lo[r][m] + (hi[r][m] >> 2) - static_cast<int>(xsum[0][m]);
-        v[m] = __fmul_rn(xsum[1][m], static_cast<float>(inner));
+        for (int m = 0; m < M; ++m) {
+          // hi is four times an integer, so the shift divides exactly
+          const int inner = lo[r][m] + (hi[r][m] >> 2) - static_cast<int>(xsum[0][m]);
+          v[m] = __fmul_rn(xsum[1][m], static_cast<float>(inner));
+        }
+        yacc.add_row(row, d, v);
       }
-      yacc.add_row(r, d, v);
     }
   }
 };

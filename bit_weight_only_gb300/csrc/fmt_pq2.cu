@@ -127,27 +127,53 @@ cudaError_t dequant(const uint8_t* tiles, const void*, const int32_t*, int64_t N
 
 using I8 = LaunchTable<FmtPQ2I8>;
 
+template <int MB>
+cudaError_t set_i8_smem() {
+  static_assert(FmtPQ2I8::kCtasPerSm * (gemv_smem_bytes<FmtPQ2I8, MB>() + 2048) <= 228 * 1024,
+                "shared memory budget exceeded");
+  return cudaFuncSetAttribute(gemv_kernel<FmtPQ2I8, MB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              gemv_smem_bytes<FmtPQ2I8, MB>());
+}
+
 cudaError_t setup() {
   cudaError_t e = LaunchTable<F>::setup();
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(gemv_kernel<FmtPQ2I8, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             gemv_smem_bytes<FmtPQ2I8, 1>());
+  if (e == cudaSuccess) e = set_i8_smem<1>();
+  if (e == cudaSuccess) e = set_i8_smem<2>();
+  if (e == cudaSuccess) e = set_i8_smem<4>();
   return e;
 }
 
-// One launch of the M = 1 kernel per activation row: each row's result is
-// that of a one-row call (batch invariant by construction).  Consecutive
-// launches on the stream are ordered by the kernel's grid-dependency wait.
+// Activation rows [m0, m0 + MB) of the call in one launch of the CUDA-core
+// kernel (the M = 1 grid and stream-K plan).
+template <int MB>
+cudaError_t launch_i8_rows(const GemvParams& p, int m0, const LaunchGeom& g, cudaStream_t s) {
+  GemvParams q = p;
+  q.x = p.x + m0 * p.K;
+  q.y = p.y + m0 * p.N;
+  q.residual = p.residual != nullptr ? p.residual + m0 * p.N : nullptr;
+  q.plan = g.plan_m1;
+  cudaLaunchAttribute attr[1];
+  const cudaLaunchConfig_t cfg =
+      I8::config(g.grid_m1, gemv_threads<FmtPQ2I8, MB>(), gemv_smem_bytes<FmtPQ2I8, MB>(), s, attr);
+  return cudaLaunchKernelEx(&cfg, gemv_kernel<FmtPQ2I8, MB>, q);
+}
+
+// Up to four activation rows per launch (the weights are read once per
+// launch); rows are computed independently of each other with the same
+// instructions and summation order in every instantiation, so a row's bits
+// do not depend on M or on its place in the batch.  Consecutive launches on
+// the stream are ordered by the kernel's grid-dependency wait.
 cudaError_t launch_x_int8(int M, const GemvParams& p, const LaunchGeom& g, cudaStream_t s) {
   if (M < 1 || M > kMaxM) return cudaErrorInvalidValue;
-  for (int m = 0; m < M; ++m) {
-    GemvParams q = p;
-    q.x = p.x + m * p.K;
-    q.y = p.y + m * p.N;
-    q.residual = p.residual != nullptr ? p.residual + m * p.N : nullptr;
-    q.plan = g.plan_m1;
-    const cudaError_t e = I8::launch_m1(q, g.grid_m1, s);
+  int m0 = 0;
+  while (m0 < M) {
+    const int rem = M - m0;
+    const int mb = rem >= 4 ? 4 : (rem >= 2 ? 2 : 1);
+    const cudaError_t e = mb == 4   ? launch_i8_rows<4>(p, m0, g, s)
+                          : mb == 2 ? launch_i8_rows<2>(p, m0, g, s)
+                                    : launch_i8_rows<1>(p, m0, g, s);
     if (e != cudaSuccess) return e;
+    m0 += mb;
   }
   return cudaSuccess;
 }

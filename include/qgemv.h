@@ -155,8 +155,10 @@ int qgemv_set_batch_invariant(qgemv_handle h, int on);
  * the quantized activations: lossy against qgemv_run with the mode off (the
  * quantization error is a property of the method, at most half a step of
  * each group's scale per nonzero weight), and accurate to the usual fp32
- * bound against the exact integer-path value.  Each activation row is one
- * launch of the one-row kernel, so results never depend on M.  Works with
+ * bound against the exact integer-path value.  Up to four activation rows
+ * share a launch (the weights are read once per launch); every row is
+ * computed with the same instructions and summation order whatever M, so a
+ * row's bits never depend on M or on its place in the batch.  Works with
  * qgemv_run and qgemv_run_residual; takes effect for runs issued after the
  * call.  Returns QGEMV_ERR_ARG for an invalid handle or a handle that is not
  * PQ2_0 (stacked PQ2_0 handles are accepted).                               */
