@@ -139,6 +139,16 @@ def aqlm_inputs(g: np.random.Generator, N: int, K: int):
     return codes, scales, codebooks
 
 
+def aqlm_1x16_inputs(g: np.random.Generator, N: int, K: int, sigma: float = 0.014):
+    """(codes u16 [N, K/8], scales fp16 [N], codebook fp16 [65536, 8]): codes
+    uniform, entries N(0, sigma) (about the spread of a 2x8 sum of two
+    N(0, 0.01) entries), scales U(0.5, 1.5)."""
+    codes = g.integers(0, 65536, size=(N, K // 8), dtype=np.uint16)
+    codebook = (g.standard_normal((65536, 8), dtype=np.float32) * np.float32(sigma)).astype(np.float16)
+    scales = g.uniform(0.5, 1.5, size=N).astype(np.float32).astype(np.float16)
+    return codes, scales, codebook
+
+
 # --------------------------------------------------------------- device ----
 
 def _torch():
@@ -211,3 +221,15 @@ def aqlm_inputs_cuda(tag: str, N: int, K: int, device="cuda", seed: int = 0):
     scales = (torch.rand(N, generator=_gen(tag + "/s", seed, device), device=device)
               + 0.5).to(torch.float16)
     return codes, scales, codebooks
+
+
+def aqlm_1x16_inputs_cuda(tag: str, N: int, K: int, sigma: float = 0.014, device="cuda", seed: int = 0):
+    torch = _torch()
+    # uniform 16-bit patterns, held as int16 (torch has no uint16 arithmetic)
+    codes = torch.randint(-32768, 32768, (N, K // 8), generator=_gen(tag + "/codes", seed, device),
+                          device=device, dtype=torch.int32).to(torch.int16)
+    codebook = (torch.randn((65536, 8), generator=_gen(tag + "/cb", seed, device),
+                            device=device) * sigma).to(torch.float16)
+    scales = (torch.rand(N, generator=_gen(tag + "/s", seed, device), device=device)
+              + 0.5).to(torch.float16)
+    return codes, scales, codebook

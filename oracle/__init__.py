@@ -21,9 +21,9 @@ import numpy as np
 
 from . import build as _build
 
-Q4_0, CBK4, CBK8, PQ2_0, AQLM_2X8, CBK4_ROW = 1, 2, 3, 4, 5, 6
+Q4_0, CBK4, CBK8, PQ2_0, AQLM_2X8, CBK4_ROW, AQLM_1X16 = 1, 2, 3, 4, 5, 6, 7
 FORMATS = {"q4_0": Q4_0, "cbk4": CBK4, "cbk8": CBK8, "pq2_0": PQ2_0,
-           "aqlm_2x8": AQLM_2X8, "cbk4_row": CBK4_ROW}
+           "aqlm_2x8": AQLM_2X8, "cbk4_row": CBK4_ROW, "aqlm_1x16": AQLM_1X16}
 
 _lib = None
 

@@ -40,6 +40,10 @@
  *                GEMV" and "Llama-2-70B in 2 bits": per group of 8 weights
  *                two uint8 codes into two 256x8 fp16 codebooks, summed, and a
  *                per-output-row scale.
+ *   AQLM 1x16 -- "Trapetum benchmarks", "Llama-2-70B PV-tuned in 1x16, with
+ *                exact speculative decoding": one codebook of 65,536 entries
+ *                of 8 fp16 values per matrix, one 16-bit code per group of 8
+ *                weights (still 2 bits per weight), and the row scales.
  *
  * Readings where the pages are silent (each also listed in the design notes):
  *   R1 Q4_0 nibble order: byte i of a block holds element i in its low nibble
@@ -55,6 +59,9 @@
  *      fp16, one fp16 scale per output row multiplying the summed vector.
  *   R10 CBK4_ROW: indices as CBK4 (R3); codebooks fp32 [N][16], row n's 16
  *      centroids contiguous, little-endian.
+ *   R12 AQLM 1x16: codes [N][K/8] uint16 little-endian, codebook [65536][8]
+ *      fp16 (entry-major), one fp16 scale per output row multiplying the
+ *      looked-up vector (as R5).
  *   R11 PQ2_0 integer activations: per group of 128, a = fl32(max|x| / 127),
  *      q = clamp(rint(fl32(x / a)), -127, 127) with ties to even; a zero
  *      group has a = 0 and q = 0 (see oracle_quantize_x_int8).
@@ -71,6 +78,7 @@
 #define ORACLE_PQ2_0 4
 #define ORACLE_AQLM_2X8 5
 #define ORACLE_CBK4_ROW 6
+#define ORACLE_AQLM_1X16 7
 
 #define ORACLE_OK 0
 #define ORACLE_ERR_ARG 1
@@ -136,6 +144,7 @@ int64_t oracle_packed_bytes(int fmt, int64_t N, int64_t K) {
     case ORACLE_CBK8: return N * K;
     case ORACLE_PQ2_0: return (K % 128) ? 0 : N * (K / 128) * 34;
     case ORACLE_AQLM_2X8: return (K % 8) ? 0 : N * (K / 8) * 2;
+    case ORACLE_AQLM_1X16: return (K % 8) ? 0 : N * (K / 8) * 2;
   }
   return 0;
 }
@@ -143,7 +152,7 @@ int64_t oracle_packed_bytes(int fmt, int64_t N, int64_t K) {
 /* Number of fp16 values in the `scales` input. */
 int64_t oracle_scales_count(int fmt, int64_t N, int64_t K) {
   (void)K;
-  return fmt == ORACLE_AQLM_2X8 ? N : 0;
+  return (fmt == ORACLE_AQLM_2X8 || fmt == ORACLE_AQLM_1X16) ? N : 0;
 }
 
 /* Number of fp16 values in the `codebooks` input (formats with one codebook
@@ -153,6 +162,7 @@ int64_t oracle_codebook_count(int fmt) {
     case ORACLE_CBK4: return 16;
     case ORACLE_CBK8: return 256;
     case ORACLE_AQLM_2X8: return 2 * 256 * 8;
+    case ORACLE_AQLM_1X16: return 65536 * 8;
   }
   return 0;
 }
@@ -180,10 +190,11 @@ int oracle_dequant_row(int fmt, int64_t N, int64_t K, const uint8_t* packed,
                        int64_t n, double* w) {
   if (oracle_packed_bytes(fmt, N, K) == 0 || n < 0 || n >= N || !packed || !w)
     return ORACLE_ERR_ARG;
-  if ((fmt == ORACLE_CBK4 || fmt == ORACLE_CBK8 || fmt == ORACLE_AQLM_2X8 || fmt == ORACLE_CBK4_ROW) &&
+  if ((fmt == ORACLE_CBK4 || fmt == ORACLE_CBK8 || fmt == ORACLE_AQLM_2X8 || fmt == ORACLE_CBK4_ROW ||
+       fmt == ORACLE_AQLM_1X16) &&
       !codebooks)
     return ORACLE_ERR_ARG;
-  if (fmt == ORACLE_AQLM_2X8 && !scales) return ORACLE_ERR_ARG;
+  if ((fmt == ORACLE_AQLM_2X8 || fmt == ORACLE_AQLM_1X16) && !scales) return ORACLE_ERR_ARG;
 
   if (fmt == ORACLE_Q4_0) {
     /* block = { fp16 d ; uint8 qs[16] }, 18 bytes, 32 weights; value (q-8)*d */
@@ -230,6 +241,14 @@ int oracle_dequant_row(int fmt, int64_t N, int64_t K, const uint8_t* packed,
         int c = (qs[e / 4] >> (2 * (e % 4))) & 3; /* reading R4 */
         w[b * 128 + e] = (double)(c - 1) * d;
       }
+    }
+  } else if (fmt == ORACLE_AQLM_1X16) {
+    /* w[n][8g+j] = s_n * C[code][j], code = 16 bits little-endian (reading R12) */
+    int64_t ng = K / 8;
+    double s = oracle_half_to_double(scales[n]);
+    for (int64_t g = 0; g < ng; ++g) {
+      int code = rd16(packed + (n * ng + g) * 2);
+      for (int j = 0; j < 8; ++j) w[g * 8 + j] = s * oracle_half_to_double(codebooks[code * 8 + j]);
     }
   } else { /* ORACLE_AQLM_2X8 */
     /* w[n][8g+j] = s_n * (C0[code0][j] + C1[code1][j])   (reading R5)     */

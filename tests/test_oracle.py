@@ -149,6 +149,58 @@ def test_pq2_second_block_and_row_use_their_own_scale():
     assert np.all(w[1, :128] == 4.0) and np.all(w[1, 128:] == 8.0)
 
 
+# ------------------------------------------------------------ AQLM 1x16 ---
+
+def test_aqlm_1x16_byte_budget(golden_dir):
+    """Pin: 16-bit codes per 8 weights are still 2 bits per weight, and the
+    codebook of 65,536 entries of 8 fp16 values is the page's 1 MiB."""
+    gb = json.load(open(os.path.join(golden_dir, "aqlm_1x16.json")))
+    N, K = 4096, 4096
+    assert oracle.packed_bytes("aqlm_1x16", N, K) * 8 == N * K * gb["bits_per_weight"]
+    assert oracle.packed_bytes("aqlm_1x16", N, K) == N * (K // gb["group"]) * gb["code_bits"] // 8
+    assert oracle.codebook_count("aqlm_1x16") == gb["codebook_entries"] * gb["entry_values"]
+    assert oracle.codebook_count("aqlm_1x16") * 2 == gb["codebook_bytes"]
+    assert oracle.scales_count("aqlm_1x16", N, K) == N
+    assert oracle.packed_bytes("aqlm_1x16", 4, 12) == 0
+
+
+def test_aqlm_1x16_is_2x8_with_the_sum_codebook():
+    """Pin (reduction): a 1x16 codebook whose entry a + 256 b is C0[a] + C1[b]
+    decodes the 2x8 code bytes (a, b) to the 2x8 weights, exactly (the sums
+    are exact in fp16: multiples of 2^-8 below 1/2)."""
+    g = np.random.default_rng(21)
+    N, K = 37, 256
+    C = (g.integers(-64, 65, size=(2, 256, 8)) * 2.0 ** -8).astype(np.float16)
+    C16 = (C[0][None, :, :].astype(np.float64) + C[1][:, None, :].astype(np.float64)).reshape(65536, 8)
+    assert np.array_equal(C16.astype(np.float16).astype(np.float64), C16)   # exact in fp16
+    C16 = C16.astype(np.float16)   # entry b * 256 + a
+    codes = g.integers(0, 256, size=(N, K // 8, 2), dtype=np.uint8)
+    scales = g.uniform(0.5, 1.5, size=N).astype(np.float16)
+    w2 = oracle.dequant("aqlm_2x8", N, K, codes, scales, C)
+    w16 = oracle.dequant("aqlm_1x16", N, K, codes, scales, C16)
+    assert np.array_equal(w2, w16)
+    x = inputs.x_fp16(inputs.rng("1x16/x"), 3, K)
+    y2, b2 = oracle.gemv("aqlm_2x8", N, K, codes, scales, C, x)
+    y16, b16 = oracle.gemv("aqlm_1x16", N, K, codes, scales, C16, x)
+    assert np.array_equal(y2, y16) and np.array_equal(b2, b16)
+
+
+def test_aqlm_1x16_single_entry_closed_form():
+    """Pin: one group coded 0xBEEF (bytes EF BE) reads entry 48879 times the
+    row scale; every other group reads the zero entry 0."""
+    N, K = 3, 64
+    cb = np.zeros((65536, 8), dtype=np.float16)
+    cb[0xBEEF] = np.arange(1, 9) * 0.125
+    cb[0xEFBE] = -1.0   # the byte-swapped index must not be read
+    codes = np.zeros((N, K // 8), dtype=np.uint16)
+    codes[1, 5] = 0xBEEF
+    scales = np.array([1.0, 2.0, 4.0], dtype=np.float16)
+    w = oracle.dequant("aqlm_1x16", N, K, codes, scales, cb)
+    expect = np.zeros((N, K))
+    expect[1, 40:48] = 2.0 * np.arange(1, 9) * 0.125
+    assert np.array_equal(w, expect)
+
+
 # ------------------------------------------------- PQ2 integer path ---
 
 def test_int8_quantizer_scale_range_and_ties(golden_dir):

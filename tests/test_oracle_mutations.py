@@ -41,6 +41,11 @@ MUTATIONS = {
     "int8 group scale of row 0": [("double da = d * (double)a[m * nb + b];", "double da = d * (double)a[b];")],
     "int8 codes of the next group": [("int t = (c - 1) * q[m * K + b * 128 + e];",
                                       "int t = (c - 1) * q[m * K + ((b + 1) % nb) * 128 + e];")],
+    "aqlm_1x16 big-endian code": [("int code = rd16(packed + (n * ng + g) * 2);",
+                                   "int code = (packed[(n * ng + g) * 2] << 8) | packed[(n * ng + g) * 2 + 1];")],
+    "aqlm_1x16 scale dropped": [("w[g * 8 + j] = s * oracle_half_to_double(codebooks[code * 8 + j]);",
+                                 "w[g * 8 + j] = oracle_half_to_double(codebooks[code * 8 + j]);")],
+    "aqlm_1x16 entry stride": [("codebooks[code * 8 + j]", "codebooks[(code >> 1) * 8 + j]")],
     "bound without abs": [("b += fabs(t);", "b += t;")],
     "x transposed against w": [("double t = xd[m * K + k] * w[k];",
                                 "double t = xd[m * K + (K - 1 - k)] * w[k];")],
