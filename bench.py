@@ -145,11 +145,15 @@ WORKLOADS = {
     "aqlm_70b_layer": (lambda: [("aqlm_2x8", n, N, K) for n, N, K in LLAMA70B_AQLM], "aqlm_2x8",
                        "70B-shaped AQLM 2x8 layer: gate, up 28672x8192, down 8192x28672, q, o 8192x8192"),
     "aqlm_down": (lambda: [("aqlm_2x8", "down", 8192, 28672)], "aqlm_2x8", "AQLM 2x8 down 8192x28672"),
+    "aqlm1x16_70b_layer": (lambda: [("aqlm_1x16", n, N, K) for n, N, K in LLAMA70B_AQLM], "aqlm_1x16",
+                           "70B-shaped AQLM 1x16 layer: gate, up 28672x8192, down 8192x28672, q, o 8192x8192"),
+    "aqlm1x16_down": (lambda: [("aqlm_1x16", "down", 8192, 28672)], "aqlm_1x16", "AQLM 1x16 down 8192x28672"),
 }
 
 
 def canonical_extra_bytes(fmt, N):
-    return {"q4_0": 0, "pq2_0": 0, "cbk4": 32, "cbk8": 512, "aqlm_2x8": 2 * N + 8192}[fmt]
+    return {"q4_0": 0, "pq2_0": 0, "cbk4": 32, "cbk8": 512, "aqlm_2x8": 2 * N + 8192,
+            "aqlm_1x16": 2 * N + 65536 * 8 * 2}[fmt]
 
 
 def build_handles(specs, M, device, seed=0):
@@ -199,6 +203,8 @@ def build_handles(specs, M, device, seed=0):
             del w
         elif fmt == "aqlm_2x8":
             packed, scales, cb = inputs.aqlm_inputs_cuda(tag, N, K, device=device, seed=seed)
+        elif fmt == "aqlm_1x16":
+            packed, scales, cb = inputs.aqlm_1x16_inputs_cuda(tag, N, K, device=device, seed=seed)
         else:
             raise ValueError(fmt)
         h = qgemv.QGemv(fmt, N, K, packed, scales, cb)
@@ -438,6 +444,8 @@ def run_ours(args, rank, world, device):
                    "frac_of_peak": round(value / world / peak, 4)},
         "roofline": {"bound": "hbm",
                      "kernel": ("gemv_kernel<FmtPQ2I8, MB>, MB = 4, 2, 1 activation rows per launch" if args.x_int8
+                                else "gemv_1x16_kernel (codebook entries gathered from L2: a 32-byte sector "
+                                     "per group of 8 weights bounds it before HBM does)" if dominant == "aqlm_1x16"
                                 else f"aqlm_gemv_kernel<MB={M}>" if dominant == "aqlm_2x8" and M <= 2
                                 else (f"gemv_kernel<{dominant}, M=1>"
                                       + (" and gemv_rowgroup_kernel (matrices of at most one 32-row group per SM)"
@@ -480,6 +488,8 @@ def oracle_sample(workload, M, rows, seed=0):
         packed = inputs.pq2_packed(g, rows, K)
     elif fmt == "q4_0":
         packed = inputs.q4_0_random_blocks(g, rows, K)
+    elif fmt == "aqlm_1x16":
+        packed, scales, cb = inputs.aqlm_1x16_inputs(g, rows, K)
     else:
         packed, scales, cb = inputs.aqlm_inputs(g, rows, K)
     x = inputs.x_fp16(inputs.rng("cpu/x", seed), M, K)

@@ -454,7 +454,6 @@ cudaError_t launch_pass(const GemvParams& p, int grid, cudaStream_t s) {
   return cudaLaunchKernelEx(&cfg, aqlm_gemv_kernel<MB>, p);
 }
 
-// M activation rows: passes of two rows, the last one of one row if M is odd.
 // Passes of two activation rows, and one for an odd last row.  The two pass
 // kinds round differently, so in batch-invariant mode every row gets a
 // one-row pass of its own.

@@ -65,6 +65,7 @@ const FormatOps* ops_cbk4();
 const FormatOps* ops_cbk8();
 const FormatOps* ops_aqlm();
 const FormatOps* ops_aqlm_mma();  // internal: the AQLM tensor-core layout
+const FormatOps* ops_aqlm_1x16();
 
 // Record the calling thread's last error (what qgemv_last_error returns);
 // returns `code`.  QGEMV_OK clears it.

@@ -57,6 +57,7 @@ const qgemv::FormatOps* ops_for(int format) {
     case QGEMV_CBK8: return qgemv::ops_cbk8();
     case QGEMV_AQLM_2X8: return qgemv::ops_aqlm();
     case kAqlmMma: return qgemv::ops_aqlm_mma();
+    case QGEMV_AQLM_1X16: return qgemv::ops_aqlm_1x16();
   }
   return nullptr;
 }
@@ -70,11 +71,14 @@ int64_t k_multiple(int format) {
     case QGEMV_PQ2_0: return 128;
     case QGEMV_AQLM_2X8: return 8;
     case kAqlmMma: return 8;
+    case QGEMV_AQLM_1X16: return 8;
   }
   return 0;
 }
 
-int64_t scales_count(int format, int64_t N) { return format == QGEMV_AQLM_2X8 || format == kAqlmMma ? N : 0; }
+int64_t scales_count(int format, int64_t N) {
+  return format == QGEMV_AQLM_2X8 || format == kAqlmMma || format == QGEMV_AQLM_1X16 ? N : 0;
+}
 
 int64_t codebook_count(int format) {
   switch (format) {
@@ -82,6 +86,7 @@ int64_t codebook_count(int format) {
     case QGEMV_CBK8: return 256;
     case QGEMV_AQLM_2X8: return 2 * 256 * 8;
     case kAqlmMma: return 2 * 256 * 8;
+    case QGEMV_AQLM_1X16: return 65536 * 8;
   }
   return 0;
 }
@@ -222,6 +227,7 @@ int64_t qgemv_packed_bytes(int format, int64_t N, int64_t K) {
     case QGEMV_CBK8: return N * K;
     case QGEMV_PQ2_0: return N * (K / 128) * 34;
     case QGEMV_AQLM_2X8: return N * (K / 8) * 2;
+    case QGEMV_AQLM_1X16: return N * (K / 8) * 2;
   }
   return 0;
 }
@@ -453,7 +459,7 @@ qgemv_handle qgemv_create_stacked(int format, int nseg, const int64_t* seg_rows,
     set_error(QGEMV_ERR_ARG, "unknown format %d", format);
     return nullptr;
   }
-  if (format == QGEMV_AQLM_2X8 || format == kAqlmMma) {
+  if (format == QGEMV_AQLM_2X8 || format == kAqlmMma || format == QGEMV_AQLM_1X16) {
     set_error(QGEMV_ERR_ARG, "format %d cannot be stacked", format);
     return nullptr;
   }

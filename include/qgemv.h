@@ -61,7 +61,14 @@ typedef enum {
    * weights along K two uint8 codes; w[n][8g+j] = s[n] * (C0[c0][j] +
    * C1[c1][j]).  packed = codes uint8 [N][K/8][2] (codebook 0 first);
    * scales = fp16 [N]; codebooks = fp16 [2][256][8]; K % 8 == 0.          */
-  QGEMV_AQLM_2X8 = 5
+  QGEMV_AQLM_2X8 = 5,
+  /* AQLM 1x16 ("Trapetum benchmarks", the PV-tuned Llama-2-70B in 1x16): one
+   * codebook of 65,536 entries of 8 fp16 values per matrix and one 16-bit
+   * code per group of 8 weights along K (2 bits per weight); w[n][8g+j] =
+   * s[n] * C[code][j].  packed = codes uint16 little-endian [N][K/8];
+   * scales = fp16 [N]; codebooks = fp16 [65536][8] (1 MiB); K % 8 == 0.
+   * (Value 6 is reserved inside the library.)                              */
+  QGEMV_AQLM_1X16 = 7
 } qgemv_format;
 
 /* Status codes. */
@@ -107,7 +114,7 @@ qgemv_handle qgemv_create(int format, int64_t N, int64_t K, const void* packed,
  *   codebooks (CBK4, CBK8): nseg codebooks one after the other (16 or 256
  *     fp16 each); segment s decodes with codebook s.  NULL for Q4_0 and
  *     PQ2_0, whose stacked handle is the plain concatenation.
- *   AQLM 2x8 is not accepted (QGEMV_ERR_ARG).
+ *   AQLM 2x8 and 1x16 are not accepted (QGEMV_ERR_ARG).
  * Host or device pointers, copying, errors: as for qgemv_create.             */
 qgemv_handle qgemv_create_stacked(int format, int nseg, const int64_t* seg_rows, int64_t K,
                                   const void* packed, const void* scales, const void* codebooks);

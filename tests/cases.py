@@ -11,7 +11,7 @@ import numpy as np
 
 from bit_weight_only_gb300 import inputs
 
-MIN_K = {"q4_0": 32, "cbk4": 2, "cbk8": 1, "pq2_0": 128, "aqlm_2x8": 8}
+MIN_K = {"q4_0": 32, "cbk4": 2, "cbk8": 1, "pq2_0": 128, "aqlm_2x8": 8, "aqlm_1x16": 8}
 
 
 def make_case(fmt: str, N: int, K: int, tag: str = "case", seed: int = 0):
@@ -26,6 +26,8 @@ def make_case(fmt: str, N: int, K: int, tag: str = "case", seed: int = 0):
         return inputs.pq2_packed(g, N, K), None, None
     if fmt == "aqlm_2x8":
         return inputs.aqlm_inputs(g, N, K)
+    if fmt == "aqlm_1x16":
+        return inputs.aqlm_1x16_inputs(g, N, K)
     raise ValueError(fmt)
 
 
