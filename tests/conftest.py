@@ -10,6 +10,13 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
+    config.addinivalue_line("markers", "late: kernels new to the suite; run after the rest, so that "
+                            "under -x a failure there cannot hide the other results")
+
+
+def pytest_collection_modifyitems(config, items):
+    items[:] = ([it for it in items if it.get_closest_marker("late") is None]
+                + [it for it in items if it.get_closest_marker("late") is not None])
 
 
 def cuda_available() -> bool:

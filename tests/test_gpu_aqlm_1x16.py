@@ -20,7 +20,7 @@ from bit_weight_only_gb300 import build, inputs, qgemv
 from cases import make_case, make_x
 
 torch = pytest.importorskip("torch")
-pytestmark = pytest.mark.gpu
+pytestmark = [pytest.mark.gpu, pytest.mark.late]
 
 FMT = "aqlm_1x16"
 

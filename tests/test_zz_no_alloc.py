@@ -5,8 +5,9 @@ they need the product: it takes the canonical blocks, x and y from the
 caller and keeps its split-K scratch in a fixed static device array.  These
 tests call it through the C ABI and check it against the regular entry point
 (a handle made with qgemv_create) on two calls in a row, within the GEMV
-tolerance |a - b| <= 1e-3 * sum_k |x w| + 1e-6.  This file is collected last
-so that a run stopping at the first failure has already run every other test.
+tolerance |a - b| <= 1e-3 * sum_k |x w| + 1e-6.  This file is collected after
+the other established tests (only tests marked ``late`` follow it) so that a
+run stopping at the first failure has already run them.
 """
 import numpy as np
 import pytest
