@@ -148,12 +148,17 @@ WORKLOADS = {
     "aqlm1x16_70b_layer": (lambda: [("aqlm_1x16", n, N, K) for n, N, K in LLAMA70B_AQLM], "aqlm_1x16",
                            "70B-shaped AQLM 1x16 layer: gate, up 28672x8192, down 8192x28672, q, o 8192x8192"),
     "aqlm1x16_down": (lambda: [("aqlm_1x16", "down", 8192, 28672)], "aqlm_1x16", "AQLM 1x16 down 8192x28672"),
+    "cbk4row_7b_layer": (lambda: [("cbk4_row", n, N, K) for n, N, K in LLAMA7B], "cbk4_row",
+                         "7B decoder layer, CBK4 with per-row fp32 codebooks: q, k, v, o 4096x4096, "
+                         "gate, up 11008x4096, down 4096x11008"),
+    "cbk4row_down": (lambda: [("cbk4_row", "down", 8192, 28672)], "cbk4_row",
+                     "CBK4 with per-row fp32 codebooks, down 8192x28672"),
 }
 
 
 def canonical_extra_bytes(fmt, N):
     return {"q4_0": 0, "pq2_0": 0, "cbk4": 32, "cbk8": 512, "aqlm_2x8": 2 * N + 8192,
-            "aqlm_1x16": 2 * N + 65536 * 8 * 2}[fmt]
+            "aqlm_1x16": 2 * N + 65536 * 8 * 2, "cbk4_row": 64 * N}[fmt]
 
 
 def build_handles(specs, M, device, seed=0):
@@ -205,6 +210,9 @@ def build_handles(specs, M, device, seed=0):
             packed, scales, cb = inputs.aqlm_inputs_cuda(tag, N, K, device=device, seed=seed)
         elif fmt == "aqlm_1x16":
             packed, scales, cb = inputs.aqlm_1x16_inputs_cuda(tag, N, K, device=device, seed=seed)
+        elif fmt == "cbk4_row":
+            packed = inputs.cbk_packed_cuda(tag, N, K, 4, p16, device, seed)
+            cb = inputs.cbk_row_codebooks(inputs.rng(f"{tag}/cb", seed), N)
         else:
             raise ValueError(fmt)
         h = qgemv.QGemv(fmt, N, K, packed, scales, cb)
@@ -446,6 +454,8 @@ def run_ours(args, rank, world, device):
                      "kernel": ("gemv_kernel<FmtPQ2I8, MB>, MB = 4, 2, 1 activation rows per launch" if args.x_int8
                                 else "gemv_1x16_kernel (codebook entries gathered from L2: a 32-byte sector "
                                      "per group of 8 weights bounds it before HBM does)" if dominant == "aqlm_1x16"
+                                else "gemv_kernel<FmtCBK4R, MB>, MB = 2, 1 activation rows per launch"
+                                if dominant == "cbk4_row"
                                 else f"aqlm_gemv_kernel<MB={M}>" if dominant == "aqlm_2x8" and M <= 2
                                 else (f"gemv_kernel<{dominant}, M=1>"
                                       + (" and gemv_rowgroup_kernel (matrices of at most one 32-row group per SM)"
@@ -459,8 +469,10 @@ def run_ours(args, rank, world, device):
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": K_e2e},
         # one launch per GEMV (AQLM: one table pass for M <= 2, else the
-        # tensor-core kernel); the INT8 path launches once per 4, 2 or 1 rows
-        "gpu_launches": sum(x_int8_launches(M) if o.get("x_int8") else 1 for o in ops) * K,
+        # tensor-core kernel); the INT8 path launches once per 4, 2 or 1
+        # rows, CBK4_ROW once per 2 or 1
+        "gpu_launches": sum(x_int8_launches(M) if o.get("x_int8") else
+                            (M + 1) // 2 if o["fmt"] == "cbk4_row" else 1 for o in ops) * K,
         "clocks": clocks,
     }
     if not args.no_cpu_baseline and world == 1:
@@ -490,6 +502,9 @@ def oracle_sample(workload, M, rows, seed=0):
         packed = inputs.q4_0_random_blocks(g, rows, K)
     elif fmt == "aqlm_1x16":
         packed, scales, cb = inputs.aqlm_1x16_inputs(g, rows, K)
+    elif fmt == "cbk4_row":
+        packed = inputs.cbk_packed(g, rows, K, 4, inputs.cbk_cell_probs(inputs.cbk_centroids(16)))
+        cb = inputs.cbk_row_codebooks(g, rows)
     else:
         packed, scales, cb = inputs.aqlm_inputs(g, rows, K)
     x = inputs.x_fp16(inputs.rng("cpu/x", seed), M, K)

@@ -363,6 +363,124 @@ struct FmtCBK8 {
   }
 };
 
+// ------------------------------------------------ CBK4, per-row codebooks --
+//
+// The pages' own 4-bit files ("Trapetum benchmarks", "Model-level results")
+// carry one 16-centroid codebook per output row, in fp32.  Same tiles and
+// indices as CBK4; the codebooks of a row tile (128 rows x 16 fp32, 8 KB)
+// live in shared memory as T[j][c][l] = centroid c of row 4l + j (byte
+// j*2048 + c*128 + l*4 of the 64 KB-aligned table region), so lane l's
+// lookups always hit bank l whatever the indices.  A row tile's table is
+// built when the CTA starts it (the stacked-handle machinery of gemv_kernel,
+// with one segment per row tile).  The entry is fp32, so each weight is one
+// lookup (the address: the index nibble shifted to bits 7..10 OR the lane's
+// row base) and the products with fp32 activation pairs accumulate with
+// FFMA2.  Tile parity as CBK4 (sixteen warps, alternate tiles).
+struct FmtCBK4R {
+  static constexpr int kKW = 64;
+  static constexpr int kKT = kKW * kSlices;                              // 512
+  static constexpr int kTileBytes = kLaneSlots * kRowsPerLane * 32;      // 32768
+  static constexpr int kCtasPerSm = 1;
+  static constexpr bool kTileParity = true;
+  __host__ __device__ static constexpr int stages(int M) { return M <= 4 ? 4 : 2; }
+  static constexpr int kSharedBytes = kLutBytes;    // the table region (8 KB of it used)
+  static constexpr int kCbEntries = kTileRows * 16 * 2;  // fp16-sized units of a row tile's codebooks (8 KB)
+  static constexpr float kOutScale = 1.0f;
+  static constexpr int kSumGroups = 1;  // unused
+  using XRegs = XRegsT<2>;
+  static_assert(kKT == FmtCBK4::kKT && kTileBytes == FmtCBK4::kTileBytes, "the CBK4 tiles");
+
+  // cb: the row tile's codebooks, fp32 [128 rows][16]; entry e of the
+  // table (word e) is T[j = e / 512][c = (e / 32) % 16][l = e % 32].
+  template <int NT>
+  __device__ static void init_shared(uint8_t* lut, const uint16_t* cb, int warp, int lane) {
+    const float* cbf = reinterpret_cast<const float*>(cb);
+    float* T = reinterpret_cast<float*>(lut);
+    for (int e = warp * 32 + lane; e < kTileRows * 16; e += NT) {
+      const int l = e & 31, c = (e >> 5) & 15, j = e >> 9;
+      T[e] = __ldg(cbf + (kRowsPerLane * l + j) * 16 + c);
+    }
+  }
+
+  template <int M>
+  __device__ static void load_x(XRegs& xr, const GemvParams& p, int kt, int slice, int lane) {
+    load_x_slice<kKW, M, 2>(xr, p, kt, slice, lane);
+  }
+
+  struct XScale {};
+  __device__ static void x_scales(XScale&, int) {}
+
+  // fp32 pairs: lane l holds k pair l of the slice
+  template <int M>
+  __device__ static void stage_x(float* xs, float (&)[kSumGroups][M], const XRegs& xr, const XScale&,
+                                 int lane) {
+    constexpr int MP = mpad(M);
+#pragma unroll
+    for (int m = 0; m < MP; ++m)
+      *reinterpret_cast<float2*>(xs + (lane * MP + m) * 2) =
+          m < M ? make_float2(h2f(xr.v[m][0]), h2f(xr.v[m][1])) : make_float2(0.f, 0.f);
+  }
+
+  // Byte offset of the centroid of nibble n (0..7) of w in its row's table
+  // column: the index times 128, at bits 7..10.
+  template <int n>
+  __device__ static uint32_t nib_off(uint32_t w) {
+    if constexpr (4 * n >= 7) return (w >> (4 * n - 7)) & 0x780u;
+    else return (w << (7 - 4 * n)) & 0x780u;
+  }
+
+  template <int M, int RPW>
+  __device__ static void tile_math(const uint8_t* stage, const float* xs,
+                                   const float (&)[kSumGroups][M], RowAcc<M, RPW>& yacc,
+                                   uint8_t* lut, int slice, int half, int lane,
+                                   uint64_t* empty_bar) {
+    const int t = slice * 32 + lane;
+    const int j0 = half * RPW;
+    uint4 clo[RPW], chi[RPW];
+    FmtCBK4::load_codes32<RPW>(stage, j0, t, clo, chi);
+    release_stage(empty_bar, lane);
+    // the table is 64 KB-aligned: bits 7..10 of every row base are free
+    const uint32_t tbase = smem_u32(lut) + static_cast<uint32_t>(lane) * 4;
+
+    float2 acc[RPW][M];
+#pragma unroll
+    for (int j = 0; j < RPW; ++j)
+#pragma unroll
+      for (int m = 0; m < M; ++m) acc[j][m] = make_float2(0.f, 0.f);
+    constexpr int UI = (M > 1) ? 2 : 8;
+#pragma unroll UI
+    for (int i = 0; i < 8; ++i) {  // word i: k pairs 4i..4i+3 (byte bp: k = 2(4i+bp), +1)
+      float2 xv4[4][M];
+      load_xpair_run<M, 4>(xs, 4 * i, xv4);
+#pragma unroll
+      for (int j = 0; j < RPW; ++j) {
+        const uint32_t wv = i < 4 ? word_of(clo[j], i) : word_of(chi[j], i - 4);
+        const uint32_t base = tbase + static_cast<uint32_t>(j0 + j) * 2048u;
+        float2 w2[4];
+        w2[0] = make_float2(__uint_as_float(lds32_at(base | nib_off<0>(wv))),
+                            __uint_as_float(lds32_at(base | nib_off<1>(wv))));
+        w2[1] = make_float2(__uint_as_float(lds32_at(base | nib_off<2>(wv))),
+                            __uint_as_float(lds32_at(base | nib_off<3>(wv))));
+        w2[2] = make_float2(__uint_as_float(lds32_at(base | nib_off<4>(wv))),
+                            __uint_as_float(lds32_at(base | nib_off<5>(wv))));
+        w2[3] = make_float2(__uint_as_float(lds32_at(base | nib_off<6>(wv))),
+                            __uint_as_float(lds32_at(base | nib_off<7>(wv))));
+#pragma unroll
+        for (int bp = 0; bp < 4; ++bp)
+#pragma unroll
+          for (int m = 0; m < M; ++m) acc[j][m] = __ffma2_rn(w2[bp], xv4[bp][m], acc[j][m]);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < RPW; ++j) {
+      float a[M];
+#pragma unroll
+      for (int m = 0; m < M; ++m) a[m] = acc[j][m].x + acc[j][m].y;
+      yacc.add_row(j, 1.0f, a);
+    }
+  }
+};
+
 }  // namespace qgemv
 
 namespace qgemv {

@@ -57,6 +57,9 @@ struct FormatOps {
   int rowgroup = 0;                 // has the M = 1 row-group kernel (rowgroup_kernel.cuh)
   // PQ2_0 only: the run with INT8 activations (qgemv_set_x_int8), else nullptr
   cudaError_t (*launch_x_int8)(int M, const GemvParams& p, const LaunchGeom& g, cudaStream_t s) = nullptr;
+  // one codebook table per row tile, built from per-row codebooks (CBK4_ROW):
+  // aux holds cb_entries fp16-sized units per row tile and seg_of_rt[rt] = rt
+  int row_tables = 0;
 };
 
 const FormatOps* ops_q4_0();
@@ -66,6 +69,7 @@ const FormatOps* ops_cbk8();
 const FormatOps* ops_aqlm();
 const FormatOps* ops_aqlm_mma();  // internal: the AQLM tensor-core layout
 const FormatOps* ops_aqlm_1x16();
+const FormatOps* ops_cbk4_row();
 
 // Record the calling thread's last error (what qgemv_last_error returns);
 // returns `code`.  QGEMV_OK clears it.

@@ -58,6 +58,7 @@ const qgemv::FormatOps* ops_for(int format) {
     case QGEMV_AQLM_2X8: return qgemv::ops_aqlm();
     case kAqlmMma: return qgemv::ops_aqlm_mma();
     case QGEMV_AQLM_1X16: return qgemv::ops_aqlm_1x16();
+    case QGEMV_CBK4_ROW: return qgemv::ops_cbk4_row();
   }
   return nullptr;
 }
@@ -72,6 +73,7 @@ int64_t k_multiple(int format) {
     case QGEMV_AQLM_2X8: return 8;
     case kAqlmMma: return 8;
     case QGEMV_AQLM_1X16: return 8;
+    case QGEMV_CBK4_ROW: return 2;
   }
   return 0;
 }
@@ -87,6 +89,7 @@ int64_t codebook_count(int format) {
     case QGEMV_AQLM_2X8: return 2 * 256 * 8;
     case kAqlmMma: return 2 * 256 * 8;
     case QGEMV_AQLM_1X16: return 65536 * 8;
+    case QGEMV_CBK4_ROW: return 16;  // per output row, fp32
   }
   return 0;
 }
@@ -180,8 +183,8 @@ std::vector<qgemv::CtaPlan> plan_stream_k(int64_t T, int64_t G, int64_t nKT, int
   return plan;
 }
 
-std::once_flag g_setup_once[8];
-cudaError_t g_setup_err[8];
+std::once_flag g_setup_once[16];
+cudaError_t g_setup_err[16];
 
 }  // namespace
 
@@ -228,6 +231,7 @@ int64_t qgemv_packed_bytes(int format, int64_t N, int64_t K) {
     case QGEMV_PQ2_0: return N * (K / 128) * 34;
     case QGEMV_AQLM_2X8: return N * (K / 8) * 2;
     case QGEMV_AQLM_1X16: return N * (K / 8) * 2;
+    case QGEMV_CBK4_ROW: return N * (K / 2);
   }
   return 0;
 }
@@ -341,7 +345,9 @@ static qgemv_handle create_impl(int format, int64_t N, int64_t K, const void* pa
   const int n_plans = h->grid + (h->grid_m1 != h->grid ? h->grid_m1 : 0);
   // codebook segment of every row tile (table formats)
   std::vector<int32_t> seg_of_rt(static_cast<size_t>(h->nRT), 0);
-  {
+  if (ops->row_tables) {  // a table of its own for every row tile
+    for (int64_t r = 0; r < h->nRT; ++r) seg_of_rt[static_cast<size_t>(r)] = static_cast<int32_t>(r);
+  } else {
     int64_t row = 0;
     for (int s = 0; s < nseg; ++s) {
       for (int64_t r = row; r < row + seg_rows[s]; r += ops->tile_rows)
@@ -375,13 +381,15 @@ static qgemv_handle create_impl(int format, int64_t N, int64_t K, const void* pa
 
   e = to_device(packed, static_cast<size_t>(canonical_bytes(format, N, K)), &d_packed);
   if (e == cudaSuccess) e = to_device(scales, 2 * scales_count(format, N), &d_scales);
-  if (e == cudaSuccess) e = to_device(codebooks, 2 * codebook_count(format) * nseg, &d_cb);
+  const int64_t cb_bytes = format == QGEMV_CBK4_ROW ? 4 * codebook_count(format) * N  // fp32 per row
+                                                    : 2 * codebook_count(format) * nseg;
+  if (e == cudaSuccess) e = to_device(codebooks, static_cast<size_t>(cb_bytes), &d_cb);
   if (e != cudaSuccess) return cleanup(QGEMV_ERR_CUDA, "copying the canonical inputs", e);
 
   e = dev_alloc(reinterpret_cast<void**>(&h->tiles), static_cast<size_t>(h->T) * ops->tile_bytes);
   // table formats: one codebook, or (stacked) one copy per row tile followed
   // by the row tiles' segments
-  const bool stacked = ops->cb_entries > 0 && nseg > 1;
+  const bool stacked = ops->cb_entries > 0 && (nseg > 1 || ops->row_tables);
   const int64_t table_bytes = int64_t(2) * ops->cb_entries * (stacked ? h->nRT : 1);
   const int64_t aux_bytes = ops->cb_entries > 0 ? table_bytes + (stacked ? 4 * h->nRT : 0)
                                                 : ops->aux_bytes + ops->aux_per_row * N;
@@ -459,7 +467,7 @@ qgemv_handle qgemv_create_stacked(int format, int nseg, const int64_t* seg_rows,
     set_error(QGEMV_ERR_ARG, "unknown format %d", format);
     return nullptr;
   }
-  if (format == QGEMV_AQLM_2X8 || format == kAqlmMma || format == QGEMV_AQLM_1X16) {
+  if (format == QGEMV_AQLM_2X8 || format == kAqlmMma || format == QGEMV_AQLM_1X16 || format == QGEMV_CBK4_ROW) {
     set_error(QGEMV_ERR_ARG, "format %d cannot be stacked", format);
     return nullptr;
   }

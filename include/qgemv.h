@@ -68,7 +68,15 @@ typedef enum {
    * s[n] * C[code][j].  packed = codes uint16 little-endian [N][K/8];
    * scales = fp16 [N]; codebooks = fp16 [65536][8] (1 MiB); K % 8 == 0.
    * (Value 6 is reserved inside the library.)                              */
-  QGEMV_AQLM_1X16 = 7
+  QGEMV_AQLM_1X16 = 7,
+  /* CBK4 with one codebook per output row, the pages' own 4-bit file layout
+   * ("Trapetum benchmarks", "Model-level results": a 16-centroid k-means
+   * codebook per output channel, stored in fp32): packed = uint8 [N][K/2]
+   * as QGEMV_CBK4; codebooks = fp32 [N][16], row n's centroids together
+   * (64 bytes per row); K % 2 == 0; scales = NULL.  Every M runs the
+   * CUDA-core kernel (fp32 centroids), at most two activation rows per
+   * launch; a row's bits do not depend on M.                               */
+  QGEMV_CBK4_ROW = 8
 } qgemv_format;
 
 /* Status codes. */
@@ -114,7 +122,9 @@ qgemv_handle qgemv_create(int format, int64_t N, int64_t K, const void* packed,
  *   codebooks (CBK4, CBK8): nseg codebooks one after the other (16 or 256
  *     fp16 each); segment s decodes with codebook s.  NULL for Q4_0 and
  *     PQ2_0, whose stacked handle is the plain concatenation.
- *   AQLM 2x8 and 1x16 are not accepted (QGEMV_ERR_ARG).
+ *   AQLM 2x8, AQLM 1x16 and CBK4_ROW are not accepted (QGEMV_ERR_ARG; the
+ *   rows of a CBK4_ROW matrix carry their own codebooks, so one handle over
+ *   the concatenated rows does the same).
  * Host or device pointers, copying, errors: as for qgemv_create.             */
 qgemv_handle qgemv_create_stacked(int format, int nseg, const int64_t* seg_rows, int64_t K,
                                   const void* packed, const void* scales, const void* codebooks);
