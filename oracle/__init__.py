@@ -61,6 +61,14 @@ def _load():
         lib.oracle_quantize_x_int8.restype = c_int
         lib.oracle_gemv_pq2_int8.argtypes = [i64, i64, vp, vp, i64, vp, vp, c_int]
         lib.oracle_gemv_pq2_int8.restype = c_int
+        lib.oracle_gemv_pq2_int8_q.argtypes = [i64, i64, vp, vp, vp, i64, vp, vp, c_int]
+        lib.oracle_gemv_pq2_int8_q.restype = c_int
+        lib.oracle_quantize_f32_int8.argtypes = [vp, i64, i64, vp, vp]
+        lib.oracle_quantize_f32_int8.restype = c_int
+        lib.oracle_hadamard.argtypes = [vp, i64, i64, c_int, vp, vp]
+        lib.oracle_hadamard.restype = c_int
+        lib.oracle_hadamard_f32.argtypes = [vp, i64, i64, c_int, vp, vp]
+        lib.oracle_hadamard_f32.restype = c_int
         _lib = lib
     return _lib
 
@@ -255,3 +263,79 @@ def gemv_pq2_int8(N: int, K: int, packed, x, nthreads: int | None = None):
     if rc:
         raise RuntimeError(f"oracle_gemv_pq2_int8 failed ({rc})")
     return y, b
+
+
+def quantize_f32_int8(v):
+    """The quantizer of ``quantize_x_int8`` on fp32 activations [M, K]."""
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    M, K = v.shape
+    q = np.empty((M, K), dtype=np.int8)
+    a = np.empty((M, K // 128), dtype=np.float32)
+    rc = _load().oracle_quantize_f32_int8(_ptr(v), M, K, _ptr(q), _ptr(a))
+    if rc:
+        raise ValueError(f"oracle_quantize_f32_int8 failed ({rc})")
+    return q, a
+
+
+def gemv_pq2_int8_q(N: int, K: int, packed, q, a, nthreads: int | None = None):
+    """PQ2_0 integer-path GEMV on given INT8 codes q [M, K] and group scales
+    a [M, K/128].  Returns (y, bound), fp64 [M, N]."""
+    p = _u8(packed)
+    if p is None or p.size != packed_bytes("pq2_0", N, K):
+        raise ValueError("packed missing or of the wrong size")
+    q = np.ascontiguousarray(q, dtype=np.int8)
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    M = q.shape[0]
+    y = np.empty((M, N), dtype=np.float64)
+    b = np.empty((M, N), dtype=np.float64)
+    rc = _load().oracle_gemv_pq2_int8_q(N, K, _ptr(p), _ptr(q), _ptr(a), M, _ptr(y), _ptr(b),
+                                        int(nthreads or os.cpu_count() or 1))
+    if rc:
+        raise RuntimeError(f"oracle_gemv_pq2_int8_q failed ({rc})")
+    return y, b
+
+
+def _signs(signs, K):
+    if signs is None:
+        return None
+    s = np.ascontiguousarray(signs, dtype=np.int8)
+    if s.shape != (K,) or not np.all(np.abs(s) == 1):
+        raise ValueError("signs must be +-1, one per input position")
+    return s
+
+
+def hadamard(x, B: int = 1024, signs=None):
+    """Exact fp64 Hadamard mixing of each block of B inputs (reading R13):
+    y = B^-1/2 H_B (s . x).  x: [M, K]; signs: +-1 [K] or None."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    M, K = x.shape
+    s = _signs(signs, K)
+    y = np.empty((M, K), dtype=np.float64)
+    rc = _load().oracle_hadamard(_ptr(x), M, K, int(B), _ptr(s), _ptr(y))
+    if rc:
+        raise ValueError(f"oracle_hadamard failed ({rc})")
+    return y
+
+
+def hadamard_f32(x, B: int = 1024, signs=None):
+    """The page's fp32 butterfly form of ``hadamard`` (the values the INT8
+    codes of the fused prologue are decided on)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    M, K = x.shape
+    s = _signs(signs, K)
+    y = np.empty((M, K), dtype=np.float32)
+    rc = _load().oracle_hadamard_f32(_ptr(x), M, K, int(B), _ptr(s), _ptr(y))
+    if rc:
+        raise ValueError(f"oracle_hadamard_f32 failed ({rc})")
+    return y
+
+
+def prepare_x_int8(x, B: int = 0, signs=None):
+    """The activation prologue of the PQ2_0 integer path: with B > 0 the
+    Hadamard mixing (fp32 butterfly) and then INT8 quantization of the fp32
+    result; with B = 0 the INT8 quantization of x itself.  x fp16 [M, K].
+    Returns (q, a)."""
+    x = np.ascontiguousarray(x, dtype=np.float16)
+    if B == 0:
+        return quantize_x_int8(x)
+    return quantize_f32_int8(hadamard_f32(x.astype(np.float32), B, signs))

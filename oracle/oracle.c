@@ -62,6 +62,9 @@
  *   R12 AQLM 1x16: codes [N][K/8] uint16 little-endian, codebook [65536][8]
  *      fp16 (entry-major), one fp16 scale per output row multiplying the
  *      looked-up vector (as R5).
+ *   R13 Hadamard mixing: signs are a +-1 int8 vector over the row width K;
+ *      the transform used for INT8 codes is the page's fp32 butterfly in
+ *      stage order h = 1, 2, ..., then times fl32(B^(-1/2)).
  *   R11 PQ2_0 integer activations: per group of 128, a = fl32(max|x| / 127),
  *      q = clamp(rint(fl32(x / a)), -127, 127) with ties to even; a zero
  *      group has a = 0 and q = 0 (see oracle_quantize_x_int8).
@@ -386,29 +389,97 @@ int oracle_quantize_q4_0(const float* wf, int64_t N, int64_t K, uint8_t* out) {
  *   amax = max_i |x_i| over the group (exact), a = fl32(amax / 127),
  *   q_i  = clamp(rint(fl32(x_i / a)), -127, 127), ties to even; a = 0 gives
  *   q_i = 0.  fl32 is one IEEE float operation, round to nearest even.     */
+/* One group of 128 values to INT8 (reading R11). */
+static void quant_group_i8(const float* f, int8_t* q, float* a) {
+  float amax = 0.0f;
+  for (int i = 0; i < 128; ++i) {
+    float v = fabsf(f[i]);
+    if (v > amax) amax = v;
+  }
+  float s = amax / 127.0f;
+  *a = s;
+  for (int i = 0; i < 128; ++i) {
+    int qi = 0;
+    if (s != 0.0f) {
+      float r = rintf(f[i] / s);
+      qi = r > 127.0f ? 127 : (r < -127.0f ? -127 : (int)r);
+    }
+    q[i] = (int8_t)qi;
+  }
+}
+
 int oracle_quantize_x_int8(const uint16_t* x, int64_t M, int64_t K, int8_t* q, float* a) {
   if (!x || !q || !a || M <= 0 || K <= 0 || K % 128) return ORACLE_ERR_ARG;
   int64_t ng = K / 128;
-  for (int64_t m = 0; m < M; ++m) {
+  float f[128];
+  for (int64_t m = 0; m < M; ++m)
     for (int64_t g = 0; g < ng; ++g) {
-      const uint16_t* xg = x + m * K + g * 128;
-      float amax = 0.0f;
-      for (int i = 0; i < 128; ++i) {
-        float v = fabsf((float)oracle_half_to_double(xg[i]));
-        if (v > amax) amax = v;
-      }
-      float s = amax / 127.0f;
-      a[m * ng + g] = s;
-      for (int i = 0; i < 128; ++i) {
-        int qi = 0;
-        if (s != 0.0f) {
-          float r = rintf((float)oracle_half_to_double(xg[i]) / s);
-          qi = r > 127.0f ? 127 : (r < -127.0f ? -127 : (int)r);
-        }
-        q[m * K + g * 128 + i] = (int8_t)qi;
-      }
+      for (int i = 0; i < 128; ++i) f[i] = (float)oracle_half_to_double(x[m * K + g * 128 + i]);
+      quant_group_i8(f, q + m * K + g * 128, a + m * ng + g);
     }
-  }
+  return ORACLE_OK;
+}
+
+/* The same quantizer on fp32 activations (the output of the Hadamard
+ * mixing below, which the fused prologue quantizes without rounding it to
+ * fp16 first). */
+int oracle_quantize_f32_int8(const float* x, int64_t M, int64_t K, int8_t* q, float* a) {
+  if (!x || !q || !a || M <= 0 || K <= 0 || K % 128) return ORACLE_ERR_ARG;
+  int64_t ng = K / 128;
+  for (int64_t m = 0; m < M; ++m)
+    for (int64_t g = 0; g < ng; ++g) quant_group_i8(x + m * K + g * 128, q + m * K + g * 128, a + m * ng + g);
+  return ORACLE_OK;
+}
+
+/* ------------------------------------------------ Hadamard mixing ---- */
+
+/* "Making a ternary reasoning model fast in vLLM", the section on mixing
+ * the inputs: before a projection, each block of B consecutive inputs (B a
+ * power of two, 1024 in the page's model) is mixed by the Hadamard
+ * transform, after an elementwise sign flip s (a +-1 vector over the whole
+ * row width, the same for every row):
+ *     y = B^(-1/2) H_B (s . x)   per block,   H_B[i][j] = (-1)^popcount(i & j).
+ * This is that definition written out in fp64 (O(B^2) per block); signs may
+ * be NULL (all +1).  x, y: fp64 [M][K]; signs: int8 [K].                     */
+int oracle_hadamard(const double* x, int64_t M, int64_t K, int B, const int8_t* signs, double* y) {
+  if (!x || !y || M <= 0 || K <= 0 || B < 1 || (B & (B - 1)) || K % B) return ORACLE_ERR_ARG;
+  double scale = 1.0 / sqrt((double)B);
+  for (int64_t m = 0; m < M; ++m)
+    for (int64_t b0 = 0; b0 < K; b0 += B)
+      for (int i = 0; i < B; ++i) {
+        double acc = 0.0;
+        for (int j = 0; j < B; ++j) {
+          double v = x[m * K + b0 + j] * (signs ? (double)signs[b0 + j] : 1.0);
+          acc += (__builtin_popcount((unsigned)(i & j)) & 1) ? -v : v;
+        }
+        y[m * K + b0 + i] = acc * scale;
+      }
+  return ORACLE_OK;
+}
+
+/* The same transform as the page computes it (reading R13): in fp32, the
+ * signs applied first, then log2(B) butterfly stages h = 1, 2, 4, ... B/2,
+ * each replacing the pair (u at i, w at i + h; bit h of i clear) by
+ * (u + w, u - w), then every value times fl32(B^(-1/2)).  Each step is one
+ * fp32 operation in a fixed order, so a kernel that takes the same steps
+ * gets the same bits; the INT8 codes of the fused prologue are decided on
+ * these values.  x, y: fp32 [M][K].                                         */
+int oracle_hadamard_f32(const float* x, int64_t M, int64_t K, int B, const int8_t* signs, float* y) {
+  if (!x || !y || M <= 0 || K <= 0 || B < 1 || (B & (B - 1)) || K % B) return ORACLE_ERR_ARG;
+  float scale = (float)(1.0 / sqrt((double)B));
+  for (int64_t m = 0; m < M; ++m)
+    for (int64_t b0 = 0; b0 < K; b0 += B) {
+      float* v = y + m * K + b0;
+      for (int i = 0; i < B; ++i) v[i] = x[m * K + b0 + i] * (signs ? (float)signs[b0 + i] : 1.0f);
+      for (int h = 1; h < B; h <<= 1)
+        for (int i = 0; i < B; ++i)
+          if (!(i & h)) {
+            float u = v[i], w = v[i + h];
+            v[i] = u + w;
+            v[i + h] = u - w;
+          }
+      for (int i = 0; i < B; ++i) v[i] = v[i] * scale;
+    }
   return ORACLE_OK;
 }
 
@@ -416,45 +487,55 @@ int oracle_quantize_x_int8(const uint16_t* x, int64_t M, int64_t K, int8_t* q, f
  * the integer inner sums exact and the rest in fp64 (each d * a * sum has at
  * most 11 + 24 + 15 significant bits, so it is exact too); bound[m][n] is
  * the same sum over |terms|.  y and bound are fp64 [M][N].                  */
+/* The integer-path GEMV on activations already quantized: q int8 [M][K],
+ * a fp32 [M][K/128] (one scale per group of 128). */
+int oracle_gemv_pq2_int8_q(int64_t N, int64_t K, const uint8_t* packed, const int8_t* q, const float* a,
+                           int64_t M, double* y, double* bound, int nthreads) {
+  if (oracle_packed_bytes(ORACLE_PQ2_0, N, K) == 0 || !packed || !q || !a || !y || M <= 0) return ORACLE_ERR_ARG;
+  int64_t nb = K / 128;
+  (void)nthreads;
+#if defined(_OPENMP)
+#pragma omp parallel for num_threads(nthreads > 0 ? nthreads : 1) schedule(dynamic, 4)
+#endif
+  for (int64_t n = 0; n < N; ++n) {
+    for (int64_t m = 0; m < M; ++m) {
+      double s = 0.0, bnd = 0.0;
+      for (int64_t b = 0; b < nb; ++b) {
+        const uint8_t* blk = packed + (n * nb + b) * 34;
+        double d = oracle_half_to_double(rd16(blk));
+        const uint8_t* qs = blk + 2;
+        int64_t isum = 0, iabs = 0;
+        for (int e = 0; e < 128; ++e) {
+          int c = (qs[e / 4] >> (2 * (e % 4))) & 3; /* reading R4 */
+          int t = (c - 1) * q[m * K + b * 128 + e];
+          isum += t;
+          iabs += t < 0 ? -t : t;
+        }
+        double da = d * (double)a[m * nb + b];
+        s += da * (double)isum;
+        bnd += fabs(da) * (double)iabs;
+      }
+      y[m * N + n] = s;
+      if (bound) bound[m * N + n] = bnd;
+    }
+  }
+  return ORACLE_OK;
+}
+
+/* The integer path from fp16 activations: quantize (R11), then the GEMV on
+ * the codes.  y and bound are fp64 [M][N]. */
 int oracle_gemv_pq2_int8(int64_t N, int64_t K, const uint8_t* packed, const uint16_t* x, int64_t M,
                          double* y, double* bound, int nthreads) {
   if (oracle_packed_bytes(ORACLE_PQ2_0, N, K) == 0 || !packed || !x || !y || M <= 0) return ORACLE_ERR_ARG;
-  int64_t nb = K / 128;
   int8_t* q = (int8_t*)malloc((size_t)(M * K));
-  float* a = (float*)malloc(sizeof(float) * (size_t)(M * nb));
+  float* a = (float*)malloc(sizeof(float) * (size_t)(M * (K / 128)));
   if (!q || !a) {
     free(q);
     free(a);
     return ORACLE_ERR_NOMEM;
   }
   int rc = oracle_quantize_x_int8(x, M, K, q, a);
-  if (rc == ORACLE_OK) {
-#if defined(_OPENMP)
-#pragma omp parallel for num_threads(nthreads > 0 ? nthreads : 1) schedule(dynamic, 4)
-#endif
-    for (int64_t n = 0; n < N; ++n) {
-      for (int64_t m = 0; m < M; ++m) {
-        double s = 0.0, bnd = 0.0;
-        for (int64_t b = 0; b < nb; ++b) {
-          const uint8_t* blk = packed + (n * nb + b) * 34;
-          double d = oracle_half_to_double(rd16(blk));
-          const uint8_t* qs = blk + 2;
-          int64_t isum = 0, iabs = 0;
-          for (int e = 0; e < 128; ++e) {
-            int c = (qs[e / 4] >> (2 * (e % 4))) & 3; /* reading R4 */
-            int t = (c - 1) * q[m * K + b * 128 + e];
-            isum += t;
-            iabs += t < 0 ? -t : t;
-          }
-          double da = d * (double)a[m * nb + b];
-          s += da * (double)isum;
-          bnd += fabs(da) * (double)iabs;
-        }
-        y[m * N + n] = s;
-        if (bound) bound[m * N + n] = bnd;
-      }
-    }
-  }
+  if (rc == ORACLE_OK) rc = oracle_gemv_pq2_int8_q(N, K, packed, q, a, M, y, bound, nthreads);
   free(q);
   free(a);
   return rc;

@@ -291,6 +291,85 @@ def test_pq2_int8_error_within_quantisation_bound():
     assert np.all(b >= np.abs(y))
 
 
+# ------------------------------------------------------ Hadamard mixing ---
+
+def test_hadamard_is_the_library_sylvester_matrix():
+    """Pin (library routine): per block, y = B^-1/2 H (s . x) with scipy's
+    Sylvester Hadamard matrix, for several B; blocks are independent."""
+    sl = pytest.importorskip("scipy.linalg")
+    g = np.random.default_rng(31)
+    for B in (1, 2, 8, 64, 1024):
+        K = 2 * B
+        x = g.standard_normal((3, K))
+        s = g.choice([-1, 1], size=K).astype(np.int8)
+        y = oracle.hadamard(x, B, s)
+        H = sl.hadamard(B) / np.sqrt(B)
+        for b in range(2):
+            blk = slice(b * B, (b + 1) * B)
+            ref = (x[:, blk] * s[blk]) @ H.T
+            assert np.allclose(y[:, blk], ref, rtol=0, atol=1e-12 * max(1.0, np.abs(ref).max()))
+
+
+def test_hadamard_closed_forms_and_involution():
+    """Pin: e_0 spreads to B^-1/2 everywhere, a constant block concentrates
+    in element 0, the normalised transform is its own inverse and keeps the
+    norm, and signs act as a sign flip of the inputs."""
+    B = 1024
+    e0 = np.zeros((1, B))
+    e0[0, 0] = 1.0
+    assert np.array_equal(oracle.hadamard(e0, B), np.full((1, B), 1.0 / 32))
+    ones = oracle.hadamard(np.ones((1, B)), B)
+    assert ones[0, 0] == 32.0 and np.all(ones[0, 1:] == 0.0)
+    g = np.random.default_rng(8)
+    x = g.standard_normal((2, 2 * B))
+    y = oracle.hadamard(x, B)
+    assert np.allclose(oracle.hadamard(y, B), x, rtol=0, atol=1e-12)
+    assert np.allclose(np.linalg.norm(y, axis=1), np.linalg.norm(x, axis=1), rtol=1e-13)
+    s = g.choice([-1, 1], size=2 * B).astype(np.int8)
+    assert np.array_equal(oracle.hadamard(x, B, s), oracle.hadamard(x * s, B))
+
+
+def test_hadamard_f32_butterfly_matches_the_definition():
+    """Pin: on small integers every butterfly is exact in fp32, so the page's
+    fp32 form equals the exact transform bit for bit (a wrong sign, pairing
+    or skipped stage fails); on general inputs it is within log2(B) fp32
+    roundings of it."""
+    g = np.random.default_rng(5)
+    B = 1024
+    x = g.integers(-8, 9, size=(2, 3 * B)).astype(np.float32)
+    s = g.choice([-1, 1], size=3 * B).astype(np.int8)
+    yf = oracle.hadamard_f32(x, B, s).astype(np.float64)
+    assert np.array_equal(yf, oracle.hadamard(x.astype(np.float64), B, s))
+    xr = inputs.x_fp16(inputs.rng("had/x"), 2, 3 * B).astype(np.float32)
+    yf = oracle.hadamard_f32(xr, B, s).astype(np.float64)
+    ye = oracle.hadamard(xr.astype(np.float64), B, s)
+    lim = 11 * 2.0 ** -24 * np.repeat(np.abs(xr).reshape(2, 3, B).sum(axis=2), B, axis=1) / 32
+    assert np.all(np.abs(yf - ye) <= lim)
+    assert np.count_nonzero(yf != ye) > 0
+
+
+def test_prepared_activations_and_codes_gemv():
+    """Pin: the fp32 quantizer agrees with the fp16 one on fp16 values; the
+    prologue without mixing is the plain quantizer, with mixing it quantizes
+    the fp32 transform; the GEMV on given codes reproduces the fp16-input
+    integer GEMV."""
+    K, N = 2048, 33
+    x = inputs.x_fp16(inputs.rng("prep/x"), 3, K)
+    q16, a16 = oracle.quantize_x_int8(x)
+    q32, a32 = oracle.quantize_f32_int8(x.astype(np.float32))
+    assert np.array_equal(q16, q32) and np.array_equal(a16, a32)
+    q0, a0 = oracle.prepare_x_int8(x, 0)
+    assert np.array_equal(q0, q16) and np.array_equal(a0, a16)
+    s = np.random.default_rng(2).choice([-1, 1], size=K).astype(np.int8)
+    qh, ah = oracle.prepare_x_int8(x, 1024, s)
+    qr, ar = oracle.quantize_f32_int8(oracle.hadamard_f32(x.astype(np.float32), 1024, s))
+    assert np.array_equal(qh, qr) and np.array_equal(ah, ar)
+    packed = inputs.pq2_packed(inputs.rng("prep/w"), N, K)
+    y1, b1 = oracle.gemv_pq2_int8_q(N, K, packed, q16, a16)
+    y2, b2 = oracle.gemv_pq2_int8(N, K, packed, x)
+    assert np.array_equal(y1, y2) and np.array_equal(b1, b2)
+
+
 # ---------------------------------------------------------------- Q4_0 ---
 
 def test_q4_0_roundtrip_is_exact_for_representable_blocks():

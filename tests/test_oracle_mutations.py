@@ -46,6 +46,13 @@ MUTATIONS = {
     "aqlm_1x16 scale dropped": [("w[g * 8 + j] = s * oracle_half_to_double(codebooks[code * 8 + j]);",
                                  "w[g * 8 + j] = oracle_half_to_double(codebooks[code * 8 + j]);")],
     "aqlm_1x16 entry stride": [("codebooks[code * 8 + j]", "codebooks[(code >> 1) * 8 + j]")],
+    "hadamard parity of i | j": [("__builtin_popcount((unsigned)(i & j))", "__builtin_popcount((unsigned)(i | j))")],
+    "hadamard signs ignored": [("double v = x[m * K + b0 + j] * (signs ? (double)signs[b0 + j] : 1.0);",
+                                "double v = x[m * K + b0 + j];")],
+    "butterfly difference reversed": [("v[i + h] = u - w;", "v[i + h] = w - u;")],
+    "butterfly first stage skipped": [("for (int h = 1; h < B; h <<= 1)", "for (int h = 2; h < B; h <<= 1)")],
+    "butterfly signs ignored": [("v[i] = x[m * K + b0 + i] * (signs ? (float)signs[b0 + i] : 1.0f);",
+                                 "v[i] = x[m * K + b0 + i];")],
     "bound without abs": [("b += fabs(t);", "b += t;")],
     "x transposed against w": [("double t = xd[m * K + k] * w[k];",
                                 "double t = xd[m * K + (K - 1 - k)] * w[k];")],
