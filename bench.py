@@ -323,6 +323,11 @@ def run_ours(args, rank, world, device):
             if o["fmt"] == "pq2_0":
                 o["h"].set_x_int8(True)
                 o["x_int8"] = True
+                if args.prepared is not None:  # the prologue (Hadamard mixing, codes) then the GEMV
+                    M_, K_ = o["x"].shape
+                    o["xq"] = torch.empty(qgemv.qgemv_xq_bytes(M_, K_), dtype=torch.uint8, device=device)
+                    o["signs"] = (torch.randint(0, 2, (K_,), device=device, dtype=torch.int8) * 2 - 1
+                                  if args.prepared else None)
     log(f"[bench] rank {rank}: {len(specs)} GEMVs x {R} copies ready in {time.time() - t_setup:.1f}s")
 
     step_bytes = sum(o["bytes"] for o in ops)
@@ -340,7 +345,15 @@ def run_ours(args, rank, world, device):
         torch.cuda.synchronize()
         with torch.cuda.graph(g, stream=stream):
             for o in group:
-                o["h"].run(o["x"], o["y"], stream=torch.cuda.current_stream())
+                cs = torch.cuda.current_stream()
+                if "xq" in o:
+                    M_, K_ = o["x"].shape
+                    qgemv.qgemv_prepare_x_int8(o["x"].data_ptr(), M_, K_,
+                                               None if o["signs"] is None else o["signs"].data_ptr(),
+                                               args.prepared, o["xq"].data_ptr(), cs)
+                    o["h"].run_xq(o["xq"], M_, o["y"], stream=cs)
+                else:
+                    o["h"].run(o["x"], o["y"], stream=cs)
         graphs.append(g)
     g_dom, g_rest = graphs
 
@@ -443,8 +456,11 @@ def run_ours(args, rank, world, device):
         "vs_baseline": None,
         "dtype": "int8xint2->int32, f32" if args.x_int8 else "f32",
         "data": "synthetic",
-        "config": {"workload": args.workload, "description": desc + (", INT8 activations" if args.x_int8 else ""),
-                   "M": M, "x_int8": bool(args.x_int8),
+        "config": {"workload": args.workload,
+                   "description": desc + (", INT8 activations" if args.x_int8 else "")
+                   + ("" if args.prepared is None else
+                      ", prepared by qgemv_prepare_x_int8" + (" with Hadamard mixing (1024)" if args.prepared else "")),
+                   "M": M, "x_int8": bool(args.x_int8), "prepared_x": args.prepared,
                    "gemvs_per_step": len(ops), "bytes_per_step": step_bytes,
                    "l2": (f"weights larger than 3x L2 ({l2 >> 20} MiB): no flush needed" if R == 1 else
                           f"weights rotate through {R} copies ({R * one_copy / 1e6:.0f} MB > 3x L2 of {l2 >> 20} MiB)"),
@@ -471,12 +487,13 @@ def run_ours(args, rank, world, device):
         # one launch per GEMV (AQLM: one table pass for M <= 2, else the
         # tensor-core kernel); the INT8 path launches once per 4, 2 or 1
         # rows, CBK4_ROW once per 2 or 1
-        "gpu_launches": sum(x_int8_launches(M) if o.get("x_int8") else
+        "gpu_launches": sum((x_int8_launches(M) + (1 if "xq" in o else 0)) if o.get("x_int8") else
                             (M + 1) // 2 if o["fmt"] == "cbk4_row" else 1 for o in ops) * K,
         "clocks": clocks,
     }
     if not args.no_cpu_baseline and world == 1:
-        line["cpu_baseline"] = cpu_baseline(args.workload, M, budget_s=args.cpu_seconds, x_int8=args.x_int8)
+        line["cpu_baseline"] = cpu_baseline(args.workload, M, budget_s=args.cpu_seconds, x_int8=args.x_int8,
+                                            prepared=args.prepared)
     return line
 
 
@@ -513,13 +530,17 @@ def oracle_sample(workload, M, rows, seed=0):
     return fmt, name, rows, K, packed, scales, cb, x, nbytes
 
 
-def time_oracle(workload, M, rows, threads, reps=1, x_int8=False):
+def time_oracle(workload, M, rows, threads, reps=1, x_int8=False, prepared=None):
     import oracle
     fmt, name, rows, K, packed, scales, cb, x, nbytes = oracle_sample(workload, M, rows)
     int8 = x_int8 and fmt == "pq2_0"
+    signs = np.random.default_rng(0).choice([-1, 1], size=K).astype(np.int8) if prepared else None
     t0 = time.perf_counter()
     for _ in range(reps):
-        if int8:
+        if int8 and prepared is not None:
+            q, a = oracle.prepare_x_int8(x, prepared, signs)
+            oracle.gemv_pq2_int8_q(rows, K, packed, q, a, nthreads=threads)
+        elif int8:
             oracle.gemv_pq2_int8(rows, K, packed, x, nthreads=threads)
         else:
             oracle.gemv(fmt, rows, K, packed, scales, cb, x, nthreads=threads)
@@ -528,19 +549,19 @@ def time_oracle(workload, M, rows, threads, reps=1, x_int8=False):
                                f"K={K}), M={M}")
 
 
-def cpu_baseline(workload, M, budget_s=15.0, x_int8=False):
+def cpu_baseline(workload, M, budget_s=15.0, x_int8=False, prepared=None):
     """The oracle as it stands on the host cores, on a bounded sample (about
     budget_s seconds of work: repeated passes over rows of the workload's
     first matrix)."""
     threads = os.cpu_count() or 1
     rows, reps = 256, 1
-    dt, nbytes, desc = time_oracle(workload, M, rows, threads, reps, x_int8)
+    dt, nbytes, desc = time_oracle(workload, M, rows, threads, reps, x_int8, prepared)
     while dt < budget_s / 2:
         if rows < 4096:
             rows *= 4
         else:
             reps = max(reps * 2, int(reps * budget_s / max(dt, 1e-3) * 0.6))
-        dt, nbytes, desc = time_oracle(workload, M, rows, threads, reps, x_int8)
+        dt, nbytes, desc = time_oracle(workload, M, rows, threads, reps, x_int8, prepared)
     return {"value": round(nbytes / dt / 1e9, 4), "unit": UNIT, "cores": threads,
             "kind": "oracle", "sample": desc, "seconds": round(dt, 3)}
 
@@ -552,16 +573,16 @@ def run_reference(args, rank, world):
     total_budget = args.cpu_seconds * 4
     per_step = max(0.05, total_budget / max(1, args.steps + args.warmup))
     rows = 64
-    i8 = args.x_int8
-    dt, nbytes, desc = time_oracle(args.workload, args.m, rows, threads, x_int8=i8)
+    i8, pr = args.x_int8, args.prepared
+    dt, nbytes, desc = time_oracle(args.workload, args.m, rows, threads, x_int8=i8, prepared=pr)
     while dt < per_step / 2 and rows < 65536:
         rows *= 2
-        dt, nbytes, desc = time_oracle(args.workload, args.m, rows, threads, x_int8=i8)
+        dt, nbytes, desc = time_oracle(args.workload, args.m, rows, threads, x_int8=i8, prepared=pr)
     for _ in range(args.warmup):
-        time_oracle(args.workload, args.m, rows, threads, x_int8=i8)
+        time_oracle(args.workload, args.m, rows, threads, x_int8=i8, prepared=pr)
     times = []
     for _ in range(args.steps):
-        dt, nbytes, desc = time_oracle(args.workload, args.m, rows, threads, x_int8=i8)
+        dt, nbytes, desc = time_oracle(args.workload, args.m, rows, threads, x_int8=i8, prepared=pr)
         times.append(dt)
     tot = sum(times)
     value = nbytes * len(times) / tot / 1e9
@@ -572,7 +593,7 @@ def run_reference(args, rank, world):
         "ms_per_step": round(tot / len(times) * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": args.workload, "description": wdesc + (", INT8 activations" if i8 else ""),
-                   "M": args.m, "x_int8": bool(i8), "parallelism": f"replicas{world}"},
+                   "M": args.m, "x_int8": bool(i8), "prepared_x": pr, "parallelism": f"replicas{world}"},
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": threads,
                          "kind": "oracle", "sample": desc},
         "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -594,11 +615,16 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--x-int8", action="store_true",
                     help="PQ2_0 workloads: INT8 activations (the integer path, lossy by design)")
+    ap.add_argument("--prepared", type=int, choices=[0, 1024], default=None,
+                    help="with --x-int8: run the activation prologue (qgemv_prepare_x_int8, Hadamard "
+                         "block 0 or 1024) and the GEMV on its codes (qgemv_run_xq) in every step")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.x_int8 and WORKLOADS[args.workload][1] != "pq2_0":
         ap.error("--x-int8 needs a PQ2_0 workload")
+    if args.prepared is not None and not args.x_int8:
+        ap.error("--prepared needs --x-int8")
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -554,4 +554,49 @@ struct FmtPQ2I8 {
   }
 };
 
+// PQ2_0 on prepared INT8 activations (qgemv_prepare_x_int8, which also
+// applies the Hadamard mixing when asked): the codes of each group of 128
+// are stored in the staging order (word l of a group is the word lane l
+// stages), with the group's scale and code sum beside them, so staging is a
+// copy and the quantization runs once per activation vector, not once per
+// row tile.  The math is FmtPQ2I8's.
+struct FmtPQ2I8P : FmtPQ2I8 {
+  struct XRegs {
+    uint32_t w[kMaxM];
+    float a[kMaxM];
+    int qs[kMaxM];
+  };
+
+  template <int M>
+  __device__ static void load_x(XRegs& xr, const GemvParams& p, int kt, int slice, int lane) {
+    const int64_t G = p.K / 128;
+    const int64_t g = static_cast<int64_t>(kt) * kSlices + slice;  // the slice's group
+    const uint32_t* xw = reinterpret_cast<const uint32_t*>(p.x);
+#pragma unroll
+    for (int m = 0; m < M; ++m) {
+      if (g < G) {
+        xr.w[m] = __ldg(xw + (m * p.K + g * 128) / 4 + lane);
+        xr.a[m] = __ldg(p.x_scale + m * G + g);
+        xr.qs[m] = __ldg(p.x_qsum + m * G + g);
+      } else {  // past the row: no codes
+        xr.w[m] = 0u;
+        xr.a[m] = 0.f;
+        xr.qs[m] = 0;
+      }
+    }
+  }
+
+  template <int M>
+  __device__ static void stage_x(float* xs, float (&xsum)[kSumGroups][M], const XRegs& xr, const XScale&,
+                                 int lane) {
+    uint32_t* xq = reinterpret_cast<uint32_t*>(xs);
+#pragma unroll
+    for (int m = 0; m < M; ++m) {
+      xq[m * 32 + lane] = xr.w[m];
+      xsum[0][m] = static_cast<float>(xr.qs[m]);
+      xsum[1][m] = xr.a[m];
+    }
+  }
+};
+
 }  // namespace qgemv

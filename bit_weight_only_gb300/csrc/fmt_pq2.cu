@@ -135,11 +135,21 @@ cudaError_t set_i8_smem() {
                               gemv_smem_bytes<FmtPQ2I8, MB>());
 }
 
+template <class FI, int MB>
+cudaError_t set_i8_smem_of() {
+  static_assert(FI::kCtasPerSm * (gemv_smem_bytes<FI, MB>() + 2048) <= 228 * 1024, "shared memory budget exceeded");
+  return cudaFuncSetAttribute(gemv_kernel<FI, MB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              gemv_smem_bytes<FI, MB>());
+}
+
 cudaError_t setup() {
   cudaError_t e = LaunchTable<F>::setup();
   if (e == cudaSuccess) e = set_i8_smem<1>();
   if (e == cudaSuccess) e = set_i8_smem<2>();
   if (e == cudaSuccess) e = set_i8_smem<4>();
+  if (e == cudaSuccess) e = set_i8_smem_of<FmtPQ2I8P, 1>();
+  if (e == cudaSuccess) e = set_i8_smem_of<FmtPQ2I8P, 2>();
+  if (e == cudaSuccess) e = set_i8_smem_of<FmtPQ2I8P, 4>();
   return e;
 }
 
@@ -178,6 +188,149 @@ cudaError_t launch_x_int8(int M, const GemvParams& p, const LaunchGeom& g, cudaS
   return cudaSuccess;
 }
 
+// ---- prepared INT8 activations (FmtPQ2I8P) ----
+
+// Rows [m0, m0 + MB) of a call on prepared activations in one launch.
+template <int MB>
+cudaError_t launch_xq_rows(const GemvParams& p, int m0, const LaunchGeom& g, cudaStream_t s) {
+  const int64_t G = p.K / 128;
+  GemvParams q = p;
+  q.x = reinterpret_cast<const __half*>(reinterpret_cast<const uint8_t*>(p.x) + m0 * p.K);
+  q.x_scale = p.x_scale + m0 * G;
+  q.x_qsum = p.x_qsum + m0 * G;
+  q.y = p.y + m0 * p.N;
+  q.residual = p.residual != nullptr ? p.residual + m0 * p.N : nullptr;
+  q.plan = g.plan_m1;
+  cudaLaunchAttribute attr[1];
+  const cudaLaunchConfig_t cfg =
+      I8::config(g.grid_m1, gemv_threads<FmtPQ2I8P, MB>(), gemv_smem_bytes<FmtPQ2I8P, MB>(), s, attr);
+  return cudaLaunchKernelEx(&cfg, gemv_kernel<FmtPQ2I8P, MB>, q);
+}
+
+// As launch_x_int8: four, two, then one activation rows per launch.
+cudaError_t launch_xq(int M, const GemvParams& p, const LaunchGeom& g, cudaStream_t s) {
+  if (M < 1 || M > kMaxM) return cudaErrorInvalidValue;
+  int m0 = 0;
+  while (m0 < M) {
+    const int rem = M - m0;
+    const int mb = rem >= 4 ? 4 : (rem >= 2 ? 2 : 1);
+    const cudaError_t e = mb == 4   ? launch_xq_rows<4>(p, m0, g, s)
+                          : mb == 2 ? launch_xq_rows<2>(p, m0, g, s)
+                                    : launch_xq_rows<1>(p, m0, g, s);
+    if (e != cudaSuccess) return e;
+    m0 += mb;
+  }
+  return cudaSuccess;
+}
+
+// Packed word of four INT8 codes, lowest byte first.
+__device__ __forceinline__ uint32_t pack4(const int (&q)[4]) {
+  return (static_cast<uint32_t>(q[0]) & 0xffu) | ((static_cast<uint32_t>(q[1]) & 0xffu) << 8) |
+         ((static_cast<uint32_t>(q[2]) & 0xffu) << 16) | (static_cast<uint32_t>(q[3]) << 24);
+}
+
+// Prologue without mixing: one warp per group of 128, the GEMV staging's
+// quantizer; lane l's packed word is word l of the group.
+__global__ void prepare_x_plain_kernel(const unsigned short* __restrict__ x, int64_t groups, int64_t K,
+                                       uint32_t* __restrict__ xq, float* __restrict__ xa,
+                                       int32_t* __restrict__ xs) {
+  const int lane = threadIdx.x & 31;
+  const int64_t ng = K / 128;
+  const int64_t wstride = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t gi = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5; gi < groups;
+       gi += wstride) {
+    const int64_t base = (gi / ng) * K + (gi % ng) * 128;
+    float f[4];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) f[b] = h2f(__ldg(x + base + i8_pos(lane, b)));
+    float a;
+    int q[4], qsum;
+    quant_i8_group(f, a, q, qsum);
+    xq[base / 4 + lane] = pack4(q);
+    if (lane == 0) {
+      xa[gi] = a;
+      xs[gi] = qsum;
+    }
+  }
+}
+
+// Prologue with the Hadamard mixing of each block of 1024 inputs, fused with
+// the quantization.  One warp per block; lane l holds inputs 32l .. 32l+31
+// of it.  The steps are the fp32 steps of the page's transform in its order:
+// signs, butterflies h = 1 .. 16 inside the lane, h = 32 .. 512 across lanes
+// (the lane whose bit is clear keeps u + w, the other u - w), then times
+// 2^-5.  A group of 128 is four lanes: the scale and code sum are reduced
+// over them, and each code goes to its staging position in the group.
+__global__ void prepare_x_hadamard_kernel(const unsigned short* __restrict__ x, const int8_t* __restrict__ signs,
+                                          int64_t blocks, int64_t K, uint8_t* __restrict__ xq,
+                                          float* __restrict__ xa, int32_t* __restrict__ xs) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nb = K / 1024;
+  const int64_t wstride = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const unsigned int* xw = reinterpret_cast<const unsigned int*>(x);
+  for (int64_t bi = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5; bi < blocks;
+       bi += wstride) {
+    const int64_t b0 = (bi % nb) * 1024;                // block start within the row
+    const int64_t base = (bi / nb) * K + b0 + 32 * lane;  // this lane's first input
+    float v[32];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      const unsigned int u = __ldg(xw + base / 2 + r);
+      v[2 * r] = h2f(u & 0xffffu);
+      v[2 * r + 1] = h2f(u >> 16);
+    }
+    if (signs != nullptr) {
+#pragma unroll
+      for (int r = 0; r < 32; ++r) v[r] = v[r] * static_cast<float>(__ldg(signs + b0 + 32 * lane + r));
+    }
+#pragma unroll
+    for (int h = 1; h < 32; h <<= 1)
+#pragma unroll
+      for (int r = 0; r < 32; ++r)
+        if (!(r & h)) {
+          const float u = v[r], w = v[r + h];
+          v[r] = u + w;
+          v[r + h] = u - w;
+        }
+#pragma unroll
+    for (int hl = 1; hl < 32; hl <<= 1) {
+      const bool upper = (lane & hl) != 0;
+#pragma unroll
+      for (int r = 0; r < 32; ++r) {
+        const float other = __shfl_xor_sync(0xffffffffu, v[r], hl);
+        v[r] = upper ? other - v[r] : v[r] + other;
+      }
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int r = 0; r < 32; ++r) {
+      v[r] = v[r] * 0.03125f;
+      amax = fmaxf(amax, fabsf(v[r]));
+    }
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    const float a = __fdiv_rn(amax, 127.0f);
+    const int64_t gstart = (bi / nb) * K + b0 + 128 * (lane >> 2);  // this lane's group
+    int qsum = 0;
+#pragma unroll
+    for (int r = 0; r < 32; ++r) {
+      int qv = 0;
+      if (a != 0.0f) qv = min(127, max(-127, __float2int_rn(__fdiv_rn(v[r], a))));
+      qsum += qv;
+      const int e = 32 * (lane & 3) + r;                        // position in the group
+      const int dst = 16 * (e >> 4) + 4 * (e & 3) + ((e >> 2) & 3);  // its staging position
+      xq[gstart + dst] = static_cast<uint8_t>(qv);
+    }
+    qsum += __shfl_xor_sync(0xffffffffu, qsum, 1);
+    qsum += __shfl_xor_sync(0xffffffffu, qsum, 2);
+    if ((lane & 3) == 0) {
+      const int64_t gi = gstart / 128;  // = m * K/128 + group
+      xa[gi] = a;
+      xs[gi] = qsum;
+    }
+  }
+}
+
 // One warp per group of 128 activations: the same quantizer as the GEMV's
 // staging, written out in plain [M][K] order with the scales [M][K/128].
 __global__ void quantize_x_int8_kernel(const unsigned short* __restrict__ x, int64_t groups, int64_t K,
@@ -208,11 +361,31 @@ const FormatOps* ops_pq2() {
       &LaunchTable<F>::smem_bytes, &setup, &LaunchTable<F>::launch,
       &prepare, &dequant, /*cb_entries=*/0, /*tile_rows=*/128, /*partial_stride=*/128 * 16,
       /*aux_per_row=*/0, /*m1_ctas_per_sm=*/LaunchTable<F>::kM1CtasPerSm, /*rowgroup=*/0,
-      /*launch_x_int8=*/&launch_x_int8};
+      /*launch_x_int8=*/&launch_x_int8, /*row_tables=*/0, /*launch_xq=*/&launch_xq};
   static_assert(I8::kM1CtasPerSm == LaunchTable<F>::kM1CtasPerSm && FmtPQ2I8::kKT == F::kKT &&
                     FmtPQ2I8::kTileBytes == F::kTileBytes,
                 "the INT8 path runs on the PQ2_0 handle's tiles, grid and plan");
   return &ops;
+}
+
+cudaError_t prepare_x_int8(const void* x, int64_t M, int64_t K, const int8_t* signs, int hadamard_block,
+                           void* xq, cudaStream_t s) {
+  uint8_t* q = static_cast<uint8_t*>(xq);
+  float* xa = reinterpret_cast<float*>(q + M * K);
+  int32_t* xs = reinterpret_cast<int32_t*>(q + M * K + 4 * M * (K / 128));
+  const unsigned short* xh = static_cast<const unsigned short*>(x);
+  if (hadamard_block == 0) {
+    const int64_t groups = M * (K / 128);
+    const int64_t blocks = (groups + 7) / 8;
+    prepare_x_plain_kernel<<<static_cast<int>(blocks > 4096 ? 4096 : blocks), 256, 0, s>>>(
+        xh, groups, K, reinterpret_cast<uint32_t*>(q), xa, xs);
+  } else {
+    const int64_t nblk = M * (K / 1024);
+    const int64_t blocks = (nblk + 3) / 4;
+    prepare_x_hadamard_kernel<<<static_cast<int>(blocks > 4096 ? 4096 : blocks), 128, 0, s>>>(
+        xh, signs, nblk, K, q, xa, xs);
+  }
+  return cudaGetLastError();
 }
 
 cudaError_t quantize_x_int8(const void* x, int64_t M, int64_t K, int8_t* q, float* a, cudaStream_t s) {

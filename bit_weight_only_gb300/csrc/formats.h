@@ -60,6 +60,8 @@ struct FormatOps {
   // one codebook table per row tile, built from per-row codebooks (CBK4_ROW):
   // aux holds cb_entries fp16-sized units per row tile and seg_of_rt[rt] = rt
   int row_tables = 0;
+  // PQ2_0 only: the run on prepared INT8 activations (qgemv_run_xq), else nullptr
+  cudaError_t (*launch_xq)(int M, const GemvParams& p, const LaunchGeom& g, cudaStream_t s) = nullptr;
 };
 
 const FormatOps* ops_q4_0();
@@ -78,6 +80,12 @@ int report_error(int code, const char* msg);
 // PQ2_0 INT8 activation quantizer: x fp16 [M][K] (K % 128 == 0) -> q int8
 // [M][K], a fp32 [M][K/128]; the GEMV's own staging arithmetic.
 cudaError_t quantize_x_int8(const void* x, int64_t M, int64_t K, int8_t* q, float* a, cudaStream_t s);
+
+// PQ2_0 activation prologue: INT8 codes (staging order), scales and code
+// sums of x fp16 [M][K] into xq (qgemv_xq_bytes), after the Hadamard mixing
+// of blocks of hadamard_block (0: none, or 1024) with optional signs [K].
+cudaError_t prepare_x_int8(const void* x, int64_t M, int64_t K, const int8_t* signs, int hadamard_block,
+                           void* xq, cudaStream_t s);
 
 // Q4_0 quantizer (canonical output).
 cudaError_t quantize_q4_0(const float* w, int64_t N, int64_t K, uint8_t* out, cudaStream_t s);

@@ -80,6 +80,10 @@ struct GemvParams {
   int nKT;               // k tiles per row tile
   int skip_cta;          // test hook: this CTA does nothing (-1: none)
   const float* residual; // [M][N] fp32 added to y in the store (may be y itself), or null
+  // PQ2_0 on prepared INT8 activations (x then points to their codes):
+  // group scales and group code sums, [M][K/128]; null otherwise
+  const float* x_scale;
+  const int32_t* x_qsum;
 };
 
 // y[idx] = v, plus the residual in one fp32 add (never fused with the

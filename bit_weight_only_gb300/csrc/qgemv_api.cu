@@ -491,16 +491,8 @@ static bool valid(qgemv_handle h) { return h && h->magic == kMagic; }
 
 }  // extern "C"
 
-// Both run calls; `residual` is null for qgemv_run.
-static int run_impl(qgemv_handle h, const void* x, int M, float* y, const float* residual, void* stream) {
-  if (!valid(h)) return set_error(QGEMV_ERR_ARG, "invalid handle");
-  if (M < 1 || M > qgemv::kMaxM) return set_error(QGEMV_ERR_ARG, "M=%d outside [1, 16]", M);
-  if (!x || !y) return set_error(QGEMV_ERR_ARG, "x or y is NULL");
-  if ((reinterpret_cast<uintptr_t>(x) & 3) || (reinterpret_cast<uintptr_t>(y) & 3) ||
-      (reinterpret_cast<uintptr_t>(residual) & 3))
-    return set_error(QGEMV_ERR_ALIGN, "x, y and residual must be 4-byte aligned");
-  const bool inv = h->batch_invariant != 0;
-  if (h->mma && (M >= kAqlmMmaMinM || inv)) h = h->mma;  // AQLM: the tensor-core layout
+// Kernel parameters of a run of handle h.
+static qgemv::GemvParams params_of(const qgemv_ctx* h, const void* x, float* y, const float* residual) {
   qgemv::GemvParams p;
   p.tiles = h->tiles;
   p.x = static_cast<const __half*>(x);
@@ -516,6 +508,28 @@ static int run_impl(qgemv_handle h, const void* x, int M, float* y, const float*
   p.nKT = h->nKT;
   p.skip_cta = h->skip_cta;
   p.residual = residual;
+  p.x_scale = nullptr;
+  p.x_qsum = nullptr;
+  return p;
+}
+
+static int check_run_args(qgemv_handle h, const void* x, int M, float* y, const float* residual) {
+  if (!valid(h)) return set_error(QGEMV_ERR_ARG, "invalid handle");
+  if (M < 1 || M > qgemv::kMaxM) return set_error(QGEMV_ERR_ARG, "M=%d outside [1, 16]", M);
+  if (!x || !y) return set_error(QGEMV_ERR_ARG, "x or y is NULL");
+  if ((reinterpret_cast<uintptr_t>(x) & 3) || (reinterpret_cast<uintptr_t>(y) & 3) ||
+      (reinterpret_cast<uintptr_t>(residual) & 3))
+    return set_error(QGEMV_ERR_ALIGN, "x, y and residual must be 4-byte aligned");
+  return QGEMV_OK;
+}
+
+// Both run calls; `residual` is null for qgemv_run.
+static int run_impl(qgemv_handle h, const void* x, int M, float* y, const float* residual, void* stream) {
+  const int rc = check_run_args(h, x, M, y, residual);
+  if (rc != QGEMV_OK) return rc;
+  const bool inv = h->batch_invariant != 0;
+  if (h->mma && (M >= kAqlmMmaMinM || inv)) h = h->mma;  // AQLM: the tensor-core layout
+  const qgemv::GemvParams p = params_of(h, x, y, residual);
   const qgemv::LaunchGeom g = {h->grid, h->plan, h->grid_m1, h->plan_m1, h->grid_rg};
   cudaError_t e = h->x_int8 ? h->ops->launch_x_int8(M, p, g, static_cast<cudaStream_t>(stream))
                             : h->ops->launch(M, p, g, static_cast<cudaStream_t>(stream), inv);
@@ -545,6 +559,43 @@ int qgemv_set_x_int8(qgemv_handle h, int on) {
   if (h->ops->launch_x_int8 == nullptr)
     return set_error(QGEMV_ERR_ARG, "INT8 activations need a PQ2_0 handle (format %d)", h->format);
   h->x_int8 = on ? 1 : 0;
+  return ok();
+}
+
+int64_t qgemv_xq_bytes(int M, int64_t K) {
+  if (M < 1 || K <= 0 || K % 128) return 0;
+  return int64_t(M) * K + 8 * int64_t(M) * (K / 128);
+}
+
+int qgemv_prepare_x_int8(const void* x, int M, int64_t K, const int8_t* signs, int hadamard_block, void* xq,
+                         void* stream) {
+  if (!x || !xq) return set_error(QGEMV_ERR_ARG, "x or xq is NULL");
+  if (M < 1 || K <= 0 || K % 128) return set_error(QGEMV_ERR_ARG, "M must be >= 1 and K a positive multiple of 128");
+  if (hadamard_block != 0 && hadamard_block != 1024)
+    return set_error(QGEMV_ERR_ARG, "hadamard_block must be 0 or 1024 (got %d)", hadamard_block);
+  if (hadamard_block != 0 && K % hadamard_block)
+    return set_error(QGEMV_ERR_ARG, "K=%lld is not a multiple of the Hadamard block", (long long)K);
+  if (hadamard_block == 0 && signs)
+    return set_error(QGEMV_ERR_ARG, "signs apply only with the Hadamard mixing");
+  if ((reinterpret_cast<uintptr_t>(x) & 3) || (reinterpret_cast<uintptr_t>(xq) & 3))
+    return set_error(QGEMV_ERR_ALIGN, "x and xq must be 4-byte aligned");
+  cudaError_t e = qgemv::prepare_x_int8(x, M, K, signs, hadamard_block, xq, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_error(e, "launching the activation prologue");
+  return ok();
+}
+
+int qgemv_run_xq(qgemv_handle h, const void* xq, int M, float* y, const float* residual, void* stream) {
+  const int rc = check_run_args(h, xq, M, y, residual);
+  if (rc != QGEMV_OK) return rc;
+  if (h->ops->launch_xq == nullptr)
+    return set_error(QGEMV_ERR_ARG, "prepared INT8 activations need a PQ2_0 handle (format %d)", h->format);
+  qgemv::GemvParams p = params_of(h, xq, y, residual);
+  const uint8_t* base = static_cast<const uint8_t*>(xq);
+  p.x_scale = reinterpret_cast<const float*>(base + int64_t(M) * h->K);
+  p.x_qsum = reinterpret_cast<const int32_t*>(base + int64_t(M) * h->K + 4 * int64_t(M) * (h->K / 128));
+  const qgemv::LaunchGeom g = {h->grid, h->plan, h->grid_m1, h->plan_m1, h->grid_rg};
+  cudaError_t e = h->ops->launch_xq(M, p, g, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_error(e, "launching the GEMV kernel");
   return ok();
 }
 

@@ -36,6 +36,11 @@ _SIGNATURES = {
                                           ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "qgemv_set_batch_invariant": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int]),
     "qgemv_set_x_int8": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int]),
+    "qgemv_xq_bytes": (ctypes.c_int64, [ctypes.c_int, ctypes.c_int64]),
+    "qgemv_prepare_x_int8": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_void_p,
+                                            ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]),
+    "qgemv_run_xq": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
+                                    ctypes.c_void_p, ctypes.c_void_p]),
     "qgemv_quantize_x_int8": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64,
                                              ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "qgemv_dequant": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
@@ -155,6 +160,19 @@ def qgemv_quantize_x_int8(x: int, M: int, K: int, q_out: int, a_out: int, stream
     return _check(load().qgemv_quantize_x_int8(x, M, K, q_out, a_out, _stream_ptr(stream)))
 
 
+def qgemv_xq_bytes(M: int, K: int) -> int:
+    return int(load().qgemv_xq_bytes(M, K))
+
+
+def qgemv_prepare_x_int8(x: int, M: int, K: int, signs: int | None, hadamard_block: int, xq: int,
+                         stream=None) -> int:
+    return _check(load().qgemv_prepare_x_int8(x, M, K, signs, hadamard_block, xq, _stream_ptr(stream)))
+
+
+def qgemv_run_xq(h: int, xq: int, M: int, y: int, residual: int | None = None, stream=None) -> int:
+    return _check(load().qgemv_run_xq(h, xq, M, y, residual, _stream_ptr(stream)))
+
+
 def qgemv_status(h: int) -> int:
     return _check(load().qgemv_status(h))
 
@@ -252,6 +270,12 @@ class QGemv:
     def set_x_int8(self, on: bool = True):
         qgemv_set_x_int8(self.handle, on)
 
+    def run_xq(self, xq, M: int, y, residual=None, stream=None):
+        """y (+ residual) from prepared INT8 activations (``prepare_x_int8``)."""
+        qgemv_run_xq(self.handle, xq.data_ptr(), M, y.data_ptr(),
+                     None if residual is None else residual.data_ptr(), stream)
+        return y
+
     def close(self):
         if getattr(self, "handle", None):
             qgemv_destroy(self.handle)
@@ -282,3 +306,18 @@ def quantize_x_int8(x, stream=None):
     a = torch.empty((M, K // 128), dtype=torch.float32, device=x.device)
     qgemv_quantize_x_int8(x.contiguous().data_ptr(), M, K, q.data_ptr(), a.data_ptr(), stream)
     return q, a
+
+
+def prepare_x_int8(x, hadamard_block: int = 0, signs=None, stream=None):
+    """PQ2_0 activation prologue on the GPU: fp16 CUDA tensor [M, K] -> the
+    prepared uint8 CUDA buffer of ``qgemv_xq_bytes(M, K)`` bytes (INT8 codes in
+    staging order, group scales, group code sums), after the Hadamard mixing
+    of blocks of 1024 when ``hadamard_block`` is 1024 (signs: int8 CUDA
+    tensor [K] of +-1, or None)."""
+    import torch
+    M, K = x.shape
+    xq = torch.empty(qgemv_xq_bytes(M, K), dtype=torch.uint8, device=x.device)
+    qgemv_prepare_x_int8(x.contiguous().data_ptr(), M, K, None if signs is None else signs.data_ptr(),
+                         hadamard_block, xq.data_ptr(), stream)
+    return xq
+

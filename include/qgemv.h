@@ -191,6 +191,46 @@ int qgemv_set_x_int8(qgemv_handle h, int on);
  * the quantized activations).  Asynchronous on `stream`.                   */
 int qgemv_quantize_x_int8(const void* x, int M, int64_t K, int8_t* q_out, float* a_out, void* stream);
 
+/* Prepared INT8 activations for PQ2_0 handles: the activation prologue of
+ * the integer path, run once per activation vector and shared by every
+ * projection that reads it (q, k and v; gate and up), with the Hadamard
+ * mixing of "Making a ternary reasoning model fast in vLLM" (the section on
+ * mixing the inputs) fused in when asked.
+ *
+ * Bytes of the prepared buffer of M rows of K inputs (K % 128 == 0), or 0
+ * for invalid sizes: M*K codes, then M*K/128 fp32 scales, then M*K/128
+ * int32 code sums.                                                          */
+int64_t qgemv_xq_bytes(int M, int64_t K);
+
+/* Fill xq (device, qgemv_xq_bytes(M, K) bytes, 4-byte aligned) from x
+ * (device fp16 [M][K], 4-byte aligned).
+ *   hadamard_block = 0: the codes of x itself, exactly as
+ *     qgemv_quantize_x_int8 computes them.
+ *   hadamard_block = 1024 (K % 1024 == 0): each block of 1024 inputs is
+ *     first mixed, v = 2^-5 H (s . x) with H the 1024 x 1024 Sylvester
+ *     Hadamard matrix, computed in fp32 as the page does (signs, then
+ *     butterfly stages h = 1, 2, ..., 512 replacing (u, w) by (u + w,
+ *     u - w), then the scaling), and the fp32 values v are quantized.
+ *     signs: device int8 [K] of +1 / -1 over the row width (the same for
+ *     every row), or NULL for none.
+ * Layout of xq: row m's codes at byte m*K; within each group of 128 inputs
+ * the code of input 16i + 4b + s (i = 0..7, b = 0..3, s = 0..3) is at byte
+ * 16i + 4s + b of the group (the order the GEMV stages them); the scale of
+ * group g of row m is float m*K/128 + g after the codes, and its code sum
+ * the int32 of the same index after the scales.  Asynchronous on `stream`; returns
+ * QGEMV_ERR_ARG for bad sizes, a block other than 0 or 1024, or signs
+ * without the mixing; QGEMV_ERR_ALIGN for misaligned pointers.             */
+int qgemv_prepare_x_int8(const void* x, int M, int64_t K, const int8_t* signs, int hadamard_block, void* xq,
+                         void* stream);
+
+/* y = residual + (prepared INT8 activations) . dequant(W)^T for a PQ2_0
+ * handle: the integer path of qgemv_set_x_int8 on codes from
+ * qgemv_prepare_x_int8 (with the same M and the handle's K).  With
+ * hadamard_block = 0 the result equals qgemv_run in INT8 mode bit for bit.
+ * residual may be NULL (plain store) or y itself.  The handle's INT8 mode
+ * setting does not matter here.  Asynchronous; as qgemv_run otherwise.     */
+int qgemv_run_xq(qgemv_handle h, const void* xq, int M, float* y, const float* residual, void* stream);
+
 /* Write the decoded weights, fp32 [N][K] row-major, to device memory w_out
  * (the exact value of every weight; read back from the prepared tiles, so it
  * also checks the re-layout).  Asynchronous on `stream`.                     */

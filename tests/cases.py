@@ -36,3 +36,18 @@ def make_case(fmt: str, N: int, K: int, tag: str = "case", seed: int = 0):
 
 def make_x(M: int, K: int, tag: str = "x", seed: int = 0) -> np.ndarray:
     return inputs.x_fp16(inputs.rng(f"{tag}/{M}x{K}", seed), M, K)
+
+
+def unpack_xq(xq, M: int, K: int):
+    """(codes int8 [M, K] in input order, scales fp32 [M, K/128], code sums
+    int32 [M, K/128]) of a prepared INT8 activation buffer (the layout
+    include/qgemv.h gives for qgemv_prepare_x_int8)."""
+    b = xq.cpu().numpy() if hasattr(xq, "cpu") else np.asarray(xq)
+    G = K // 128
+    codes = b[:M * K].view(np.int8).reshape(M, G, 128)
+    e = np.arange(128)
+    staged = 16 * (e >> 4) + 4 * (e & 3) + ((e >> 2) & 3)   # byte of input e within its group
+    q = codes[:, :, staged].reshape(M, K)
+    a = b[M * K:M * K + 4 * M * G].view(np.float32).reshape(M, G)
+    s = b[M * K + 4 * M * G:M * K + 8 * M * G].view(np.int32).reshape(M, G)
+    return q, a, s

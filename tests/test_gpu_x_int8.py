@@ -13,6 +13,11 @@ Bars:
   * the residual form is fl32(plain + residual), bit for bit;
   * the mode is refused for other formats and switching it off restores the
     exact path bit for bit.
+Prepared activations (qgemv_prepare_x_int8, with and without the fused
+Hadamard mixing of blocks of 1024): codes, scales and code sums bit for bit
+the oracle's ``prepare_x_int8``; qgemv_run_xq within the bound of the
+oracle's integer GEMV on those codes, and without mixing bit for bit the
+INT8-mode qgemv_run.
 Shapes cover ragged row and k tails, split row tiles and the full-size
 5120 / 17408 PQ2_0 projections (gate+up 34816 x 5120, down 5120 x 17408).
 """
@@ -21,7 +26,7 @@ import pytest
 
 import oracle
 from bit_weight_only_gb300 import build, inputs, qgemv
-from cases import make_case, make_x
+from cases import make_case, make_x, unpack_xq
 
 torch = pytest.importorskip("torch")
 pytestmark = [pytest.mark.gpu, pytest.mark.late]
@@ -172,4 +177,81 @@ def test_quantizer_argument_errors():
     assert lib.qgemv_quantize_x_int8(x.data_ptr(), 1, 200, q.data_ptr(), a.data_ptr(), None) == qgemv.QGEMV_ERR_ARG
     assert lib.qgemv_quantize_x_int8(x.data_ptr(), 0, 256, q.data_ptr(), a.data_ptr(), None) == qgemv.QGEMV_ERR_ARG
     assert lib.qgemv_quantize_x_int8(None, 1, 256, q.data_ptr(), a.data_ptr(), None) == qgemv.QGEMV_ERR_ARG
+    torch.cuda.synchronize()
+
+
+def _signs(K, B):
+    return np.random.default_rng(K).choice([-1, 1], size=K).astype(np.int8) if B else None
+
+
+def _pq2_handle(N, K, tag):
+    if N * K > (1 << 24):
+        packed_dev = inputs.pq2_packed_cuda(f"{tag}/{N}x{K}", N, K)
+        packed = packed_dev.cpu().numpy()
+        return qgemv.QGemv("pq2_0", N, K, packed_dev), packed
+    packed, _, _ = make_case("pq2_0", N, K, tag=tag)
+    return qgemv.QGemv("pq2_0", N, K, packed), packed
+
+
+@pytest.mark.parametrize("B", [0, 1024])
+@pytest.mark.parametrize("M,K", [(1, 1024), (3, 5120), (2, 17408)])
+def test_prepared_activations_match_oracle(B, M, K):
+    x_np = _special_x(M, K, tag="i8p")
+    signs = _signs(K, B)
+    xq = qgemv.prepare_x_int8(torch.from_numpy(x_np).cuda(), B,
+                              None if signs is None else torch.from_numpy(signs).cuda())
+    torch.cuda.synchronize()
+    q, a, qs = unpack_xq(xq, M, K)
+    qo, ao = oracle.prepare_x_int8(x_np, B, signs)
+    assert np.array_equal(q, qo)
+    assert np.array_equal(a.view(np.uint32), ao.view(np.uint32))
+    assert np.array_equal(qs, qo.reshape(M, K // 128, 128).sum(axis=2, dtype=np.int64))
+
+
+@pytest.mark.parametrize("B", [0, 1024])
+@pytest.mark.parametrize("N,K,M", [(700, 2048, 1), (5120, 17408, 1), (34816, 5120, 2), (700, 3072, 5)])
+def test_run_xq_matches_oracle(B, N, K, M):
+    h, packed = _pq2_handle(N, K, "i8xq")
+    x_np = make_x(M, K, tag="i8xq")
+    signs = _signs(K, B)
+    x = torch.from_numpy(x_np).cuda()
+    xq = qgemv.prepare_x_int8(x, B, None if signs is None else torch.from_numpy(signs).cuda())
+    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    h.run_xq(xq, M, y)
+    torch.cuda.synchronize()
+    assert h.status() == qgemv.QGEMV_OK
+    q, a = oracle.prepare_x_int8(x_np, B, signs)
+    y_ref, bound = oracle.gemv_pq2_int8_q(N, K, packed, q, a)
+    ok = oracle.within_tolerance(y.cpu().numpy(), y_ref, bound)
+    assert ok.all(), f"{N}x{K} M={M} B={B}: {np.count_nonzero(~ok)} outputs out of tolerance"
+    if B == 0:  # the same codes and arithmetic as the INT8 mode of qgemv_run
+        h.set_x_int8(True)
+        y2 = h.gemv(x)
+        torch.cuda.synchronize()
+        assert torch.equal(y, y2)
+
+
+def test_run_xq_residual_and_refusals():
+    N, K, M = 700, 2048, 3
+    h, _ = _pq2_handle(N, K, "i8xqr")
+    x = torch.from_numpy(make_x(M, K, tag="i8xqr")).cuda()
+    xq = qgemv.prepare_x_int8(x, 1024, None)
+    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    h.run_xq(xq, M, y)
+    r = torch.from_numpy(np.random.default_rng(6).standard_normal((M, N)).astype(np.float32)).cuda()
+    yr = torch.empty_like(y)
+    h.run_xq(xq, M, yr, residual=r)
+    torch.cuda.synchronize()
+    assert torch.equal(yr, y + r)
+
+    lib = qgemv.load()
+    packed, _, cb = make_case("cbk4", N, K, tag="i8xqrefuse")
+    hc = qgemv.QGemv("cbk4", N, K, packed, None, cb)
+    assert lib.qgemv_run_xq(hc.handle, xq.data_ptr(), M, y.data_ptr(), None, None) == qgemv.QGEMV_ERR_ARG
+    s = torch.ones(K, dtype=torch.int8, device="cuda")
+    assert lib.qgemv_prepare_x_int8(x.data_ptr(), M, K, None, 512, xq.data_ptr(), None) == qgemv.QGEMV_ERR_ARG
+    assert lib.qgemv_prepare_x_int8(x.data_ptr(), M, K, s.data_ptr(), 0, xq.data_ptr(), None) == qgemv.QGEMV_ERR_ARG
+    assert lib.qgemv_prepare_x_int8(x.data_ptr(), M, 1280, None, 1024, xq.data_ptr(), None) == qgemv.QGEMV_ERR_ARG
+    assert qgemv.qgemv_xq_bytes(M, K) == M * K + 8 * M * (K // 128)
+    assert qgemv.qgemv_xq_bytes(M, 100) == 0
     torch.cuda.synchronize()
