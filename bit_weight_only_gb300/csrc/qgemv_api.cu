@@ -242,10 +242,6 @@ static int64_t canonical_bytes(int format, int64_t N, int64_t K) {
   return qgemv_packed_bytes(format == kAqlmMma ? QGEMV_AQLM_2X8 : format, N, K);
 }
 
-extern "C" {
-
-}  // extern "C"
-
 static void free_handle(qgemv_ctx* h);
 
 // Both create calls: `nseg` codebooks for the row segments `seg_rows`

@@ -45,6 +45,29 @@ def test_packed_bytes_matches_formats(lib):
     assert qgemv.qgemv_packed_bytes("cbk8", 7, 9) == 63
     assert qgemv.qgemv_packed_bytes("q4_0", 7, 48) == 0
     assert qgemv.qgemv_packed_bytes(99, 7, 64) == 0
+    assert qgemv.qgemv_packed_bytes(6, 7, 64) == 0   # reserved inside the library
+
+
+@pytest.mark.parametrize("fmt, N, K", [("aqlm_1x16", 8192, 28672), ("aqlm_1x16", 3, 12), ("cbk4_row", 11008, 4096),
+                                       ("cbk4_row", 5, 7), ("q4_0", 9, 96), ("pq2_0", 9, 384), ("cbk8", 3, 5)])
+def test_packed_bytes_agree_with_the_oracle(lib, fmt, N, K):
+    """The library's canonical sizes and the oracle's, written separately, agree."""
+    import oracle
+    assert qgemv.qgemv_packed_bytes(fmt, N, K) == oracle.packed_bytes(fmt, N, K)
+
+
+def test_prepared_activation_sizes_and_host_checks(lib):
+    assert qgemv.qgemv_xq_bytes(3, 5120) == 3 * 5120 + 8 * 3 * 40
+    assert qgemv.qgemv_xq_bytes(0, 5120) == 0 and qgemv.qgemv_xq_bytes(1, 100) == 0
+    # rejected on the host, before any launch
+    assert lib.qgemv_prepare_x_int8(None, 1, 1024, None, 0, 16, None) == qgemv.QGEMV_ERR_ARG
+    assert lib.qgemv_prepare_x_int8(16, 1, 1024, None, 512, 16, None) == qgemv.QGEMV_ERR_ARG
+    assert lib.qgemv_prepare_x_int8(16, 1, 1280, None, 1024, 16, None) == qgemv.QGEMV_ERR_ARG
+    assert lib.qgemv_prepare_x_int8(16, 1, 1024, 16, 0, 16, None) == qgemv.QGEMV_ERR_ARG
+    assert lib.qgemv_prepare_x_int8(18, 1, 1024, None, 0, 16, None) == qgemv.QGEMV_ERR_ALIGN
+    assert lib.qgemv_quantize_x_int8(16, 1, 200, 16, 16, None) == qgemv.QGEMV_ERR_ARG
+    assert lib.qgemv_run_xq(None, 16, 1, 16, None, None) == qgemv.QGEMV_ERR_ARG
+    assert lib.qgemv_set_x_int8(None, 1) == qgemv.QGEMV_ERR_ARG
 
 
 @pytest.mark.parametrize("args, fragment", [
@@ -54,6 +77,11 @@ def test_packed_bytes_matches_formats(lib):
     ((qgemv.PQ2_0, 8, 64, 1, None, None), "invalid shape"),
     ((qgemv.Q4_0, 8, 64, None, None, None), "packed is NULL"),
     ((qgemv.Q4_0, 8, 64, 1, 1, None), "takes no scales"),
+    ((qgemv.AQLM_1X16, 8, 12, 1, 1, 1), "invalid shape"),
+    ((qgemv.AQLM_1X16, 8, 64, 1, None, 1), "needs scales"),
+    ((qgemv.CBK4_ROW, 8, 64, 1, None, None), "needs codebooks"),
+    ((qgemv.CBK4_ROW, 8, 63, 1, None, 1), "invalid shape"),
+    ((6, 8, 64, 1, None, None), "unknown format"),
 ])
 def test_create_rejects_bad_arguments_on_host(lib, args, fragment):
     h = lib.qgemv_create(*args)
@@ -82,6 +110,10 @@ def test_stacked_create_rejects_bad_arguments_on_host(lib):
     assert "cannot be stacked" in qgemv.qgemv_last_error()
     assert not lib.qgemv_create_stacked(99, 1, ok_rows, 256, 1, None, None)
     assert "unknown format" in qgemv.qgemv_last_error()
+    assert not lib.qgemv_create_stacked(qgemv.AQLM_1X16, 2, ok_rows, 256, 1, 1, 1)
+    assert "cannot be stacked" in qgemv.qgemv_last_error()
+    assert not lib.qgemv_create_stacked(qgemv.CBK4_ROW, 2, ok_rows, 256, 1, None, 1)
+    assert "cannot be stacked" in qgemv.qgemv_last_error()
 
 
 def test_quantizer_rejects_bad_shape(lib):
