@@ -21,9 +21,9 @@ import numpy as np
 
 from . import build as _build
 
-Q4_0, CBK4, CBK8, PQ2_0, AQLM_2X8, CBK4_ROW, AQLM_1X16 = 1, 2, 3, 4, 5, 6, 7
+Q4_0, CBK4, CBK8, PQ2_0, AQLM_2X8, CBK4_ROW, AQLM_1X16, CBK8_ROW = 1, 2, 3, 4, 5, 6, 7, 8
 FORMATS = {"q4_0": Q4_0, "cbk4": CBK4, "cbk8": CBK8, "pq2_0": PQ2_0,
-           "aqlm_2x8": AQLM_2X8, "cbk4_row": CBK4_ROW, "aqlm_1x16": AQLM_1X16}
+           "aqlm_2x8": AQLM_2X8, "cbk4_row": CBK4_ROW, "aqlm_1x16": AQLM_1X16, "cbk8_row": CBK8_ROW}
 
 _lib = None
 
@@ -131,7 +131,7 @@ def _check(fmt, N, K, packed, scales, codebooks):
     s = _u16(scales)
     if scales_count(f, N, K) and (s is None or s.size != scales_count(f, N, K)):
         raise ValueError("scales missing or of the wrong size")
-    if f == CBK4_ROW:  # fp32 [N][16], passed as bytes
+    if f in (CBK4_ROW, CBK8_ROW):  # fp32 [N][16] or [N][256], passed as bytes
         c = None if codebooks is None else np.ascontiguousarray(codebooks, dtype=np.float32).view(np.uint8).reshape(-1)
         if c is None or c.size != codebook_bytes(f, N):
             raise ValueError("codebooks missing or of the wrong size")

@@ -58,7 +58,8 @@
  *   R5 AQLM 2x8: codes [N][K/8][2] (codebook 0 first), codebooks [2][256][8]
  *      fp16, one fp16 scale per output row multiplying the summed vector.
  *   R10 CBK4_ROW: indices as CBK4 (R3); codebooks fp32 [N][16], row n's 16
- *      centroids contiguous, little-endian.
+ *      centroids contiguous, little-endian.  CBK8_ROW likewise: one index
+ *      byte per weight, codebooks fp32 [N][256] (the 8-bit head's).
  *   R12 AQLM 1x16: codes [N][K/8] uint16 little-endian, codebook [65536][8]
  *      fp16 (entry-major), one fp16 scale per output row multiplying the
  *      looked-up vector (as R5).
@@ -82,6 +83,7 @@
 #define ORACLE_AQLM_2X8 5
 #define ORACLE_CBK4_ROW 6
 #define ORACLE_AQLM_1X16 7
+#define ORACLE_CBK8_ROW 8
 
 #define ORACLE_OK 0
 #define ORACLE_ERR_ARG 1
@@ -145,6 +147,7 @@ int64_t oracle_packed_bytes(int fmt, int64_t N, int64_t K) {
     case ORACLE_CBK4: return (K % 2) ? 0 : N * (K / 2);
     case ORACLE_CBK4_ROW: return (K % 2) ? 0 : N * (K / 2);
     case ORACLE_CBK8: return N * K;
+    case ORACLE_CBK8_ROW: return N * K;
     case ORACLE_PQ2_0: return (K % 128) ? 0 : N * (K / 128) * 34;
     case ORACLE_AQLM_2X8: return (K % 8) ? 0 : N * (K / 8) * 2;
     case ORACLE_AQLM_1X16: return (K % 8) ? 0 : N * (K / 8) * 2;
@@ -172,7 +175,8 @@ int64_t oracle_codebook_count(int fmt) {
 
 /* Bytes of the `codebooks` input for an N-row matrix. */
 int64_t oracle_codebook_bytes(int fmt, int64_t N) {
-  if (fmt == ORACLE_CBK4_ROW) return N * 16 * 4; /* fp32 [N][16] (reading R10) */
+  if (fmt == ORACLE_CBK4_ROW) return N * 16 * 4;   /* fp32 [N][16] (reading R10) */
+  if (fmt == ORACLE_CBK8_ROW) return N * 256 * 4;  /* fp32 [N][256] (reading R10) */
   return 2 * oracle_codebook_count(fmt);
 }
 
@@ -194,7 +198,7 @@ int oracle_dequant_row(int fmt, int64_t N, int64_t K, const uint8_t* packed,
   if (oracle_packed_bytes(fmt, N, K) == 0 || n < 0 || n >= N || !packed || !w)
     return ORACLE_ERR_ARG;
   if ((fmt == ORACLE_CBK4 || fmt == ORACLE_CBK8 || fmt == ORACLE_AQLM_2X8 || fmt == ORACLE_CBK4_ROW ||
-       fmt == ORACLE_AQLM_1X16) &&
+       fmt == ORACLE_AQLM_1X16 || fmt == ORACLE_CBK8_ROW) &&
       !codebooks)
     return ORACLE_ERR_ARG;
   if ((fmt == ORACLE_AQLM_2X8 || fmt == ORACLE_AQLM_1X16) && !scales) return ORACLE_ERR_ARG;
@@ -228,6 +232,11 @@ int oracle_dequant_row(int fmt, int64_t N, int64_t K, const uint8_t* packed,
       w[2 * j] = rdf32(cb, row[j] & 0x0f);
       w[2 * j + 1] = rdf32(cb, row[j] >> 4);
     }
+  } else if (fmt == ORACLE_CBK8_ROW) {
+    /* one byte per weight, row n's own 256 fp32 centroids (reading R10) */
+    const uint8_t* row = packed + n * K;
+    const uint8_t* cb = (const uint8_t*)codebooks + n * 256 * 4;
+    for (int64_t k = 0; k < K; ++k) w[k] = rdf32(cb, row[k]);
   } else if (fmt == ORACLE_CBK8) {
     /* 8-bit index into 256 centroids */
     const uint8_t* row = packed + n * K;

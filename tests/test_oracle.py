@@ -98,6 +98,8 @@ def test_cbk_byte_accounting_reconstructs_7b_file_sizes(golden_dir):
     assert 0 < gb["legacy_file_bytes"] - (per_row + emb + norms) < 1024
     new = (idx + rows * 16 * 4 + emb + oracle.packed_bytes("cbk8", 32000, 4096)
            + 32000 * 256 * 4 + norms)
+    head8 = oracle.packed_bytes("cbk8_row", 32000, 4096) + oracle.codebook_bytes("cbk8_row", 32000)
+    assert head8 == oracle.packed_bytes("cbk8", 32000, 4096) + 32000 * 256 * 4
     assert 0 < gb["legacy_file_bytes"] - legacy < 1024
     assert 0 < gb["new_file_bytes"] - new < 1024
     # the 8-bit head's extra bytes explain the two files' difference to 8 bytes
@@ -497,6 +499,28 @@ def test_cbk4_row_uses_each_rows_own_codebook():
     cb2[2] = -cb2[2]
     W2 = oracle.dequant("cbk4_row", N, K, packed, None, cb2)
     assert np.array_equal(W2[[0, 1, 3]], W[[0, 1, 3]]) and np.array_equal(W2[2], -W[2])
+
+
+def test_cbk8_row_with_one_shared_codebook_is_cbk8():
+    """Pin (reduction): every row carrying the same fp16-representable
+    256-entry codebook decodes as CBK8 with that codebook."""
+    N, K = 9, 300
+    g = inputs.rng("pin/cbk8_row/shared")
+    cb = inputs.cbk_centroids(256)
+    packed = g.integers(0, 256, size=(N, K), dtype=np.uint8)
+    rows = np.tile(cb.astype(np.float32), (N, 1))
+    assert np.array_equal(oracle.dequant("cbk8_row", N, K, packed, None, rows),
+                          oracle.dequant("cbk8", N, K, packed, None, cb))
+
+
+def test_cbk8_row_uses_each_rows_own_codebook():
+    """Pin (closed form): with row n's centroid i = 1000 n + i every index of
+    every row decodes to exactly that value."""
+    N, K = 5, 256
+    cb = (1000.0 * np.arange(N)[:, None] + np.arange(256)[None, :]).astype(np.float32)
+    packed = np.tile(np.arange(256, dtype=np.uint8)[::-1], (N, 1))
+    W = oracle.dequant("cbk8_row", N, K, packed, None, cb)
+    assert np.array_equal(W, cb[:, ::-1].astype(np.float64))
 
 
 def test_cbk8_all_256_indices():

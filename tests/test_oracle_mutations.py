@@ -53,6 +53,10 @@ MUTATIONS = {
     "butterfly first stage skipped": [("for (int h = 1; h < B; h <<= 1)", "for (int h = 2; h < B; h <<= 1)")],
     "butterfly signs ignored": [("v[i] = x[m * K + b0 + i] * (signs ? (float)signs[b0 + i] : 1.0f);",
                                  "v[i] = x[m * K + b0 + i];")],
+    "cbk8_row neighbour's codebook": [("const uint8_t* cb = (const uint8_t*)codebooks + n * 256 * 4;",
+                                       "const uint8_t* cb = (const uint8_t*)codebooks + (n ^ 1) * 256 * 4;")],
+    "cbk8_row index bit flipped": [("for (int64_t k = 0; k < K; ++k) w[k] = rdf32(cb, row[k]);",
+                                    "for (int64_t k = 0; k < K; ++k) w[k] = rdf32(cb, row[k] ^ 1);")],
     "bound without abs": [("b += fabs(t);", "b += t;")],
     "x transposed against w": [("double t = xd[m * K + k] * w[k];",
                                 "double t = xd[m * K + (K - 1 - k)] * w[k];")],
