@@ -153,12 +153,14 @@ WORKLOADS = {
                          "gate, up 11008x4096, down 4096x11008"),
     "cbk4row_down": (lambda: [("cbk4_row", "down", 8192, 28672)], "cbk4_row",
                      "CBK4 with per-row fp32 codebooks, down 8192x28672"),
+    "cbk8row_head": (lambda: [("cbk8_row", "lm_head", 32000, 4096)], "cbk8_row",
+                     "CBK8 LM head 32000x4096 with per-row fp32 codebooks (256 per row)"),
 }
 
 
 def canonical_extra_bytes(fmt, N):
     return {"q4_0": 0, "pq2_0": 0, "cbk4": 32, "cbk8": 512, "aqlm_2x8": 2 * N + 8192,
-            "aqlm_1x16": 2 * N + 65536 * 8 * 2, "cbk4_row": 64 * N}[fmt]
+            "aqlm_1x16": 2 * N + 65536 * 8 * 2, "cbk4_row": 64 * N, "cbk8_row": 1024 * N}[fmt]
 
 
 def build_handles(specs, M, device, seed=0):
@@ -213,6 +215,9 @@ def build_handles(specs, M, device, seed=0):
         elif fmt == "cbk4_row":
             packed = inputs.cbk_packed_cuda(tag, N, K, 4, p16, device, seed)
             cb = inputs.cbk_row_codebooks(inputs.rng(f"{tag}/cb", seed), N)
+        elif fmt == "cbk8_row":
+            packed = inputs.cbk_packed_cuda(tag, N, K, 8, p256, device, seed)
+            cb = inputs.cbk_row_codebooks(inputs.rng(f"{tag}/cb", seed), N, L=256)
         else:
             raise ValueError(fmt)
         h = qgemv.QGemv(fmt, N, K, packed, scales, cb)
@@ -472,6 +477,8 @@ def run_ours(args, rank, world, device):
                                      "per group of 8 weights bounds it before HBM does)" if dominant == "aqlm_1x16"
                                 else "gemv_kernel<FmtCBK4R, MB>, MB = 2, 1 activation rows per launch"
                                 if dominant == "cbk4_row"
+                                else "gemv_rowcb8_kernel<MB> (one warp per row, its codebook in shared memory)"
+                                if dominant == "cbk8_row"
                                 else f"aqlm_gemv_kernel<MB={M}>" if dominant == "aqlm_2x8" and M <= 2
                                 else (f"gemv_kernel<{dominant}, M=1>"
                                       + (" and gemv_rowgroup_kernel (matrices of at most one 32-row group per SM)"
@@ -522,6 +529,9 @@ def oracle_sample(workload, M, rows, seed=0):
     elif fmt == "cbk4_row":
         packed = inputs.cbk_packed(g, rows, K, 4, inputs.cbk_cell_probs(inputs.cbk_centroids(16)))
         cb = inputs.cbk_row_codebooks(g, rows)
+    elif fmt == "cbk8_row":
+        packed = inputs.cbk_packed(g, rows, K, 8, inputs.cbk_cell_probs(inputs.cbk_centroids(256)))
+        cb = inputs.cbk_row_codebooks(g, rows, L=256)
     else:
         packed, scales, cb = inputs.aqlm_inputs(g, rows, K)
     x = inputs.x_fp16(inputs.rng("cpu/x", seed), M, K)

@@ -72,6 +72,7 @@ const FormatOps* ops_aqlm();
 const FormatOps* ops_aqlm_mma();  // internal: the AQLM tensor-core layout
 const FormatOps* ops_aqlm_1x16();
 const FormatOps* ops_cbk4_row();
+const FormatOps* ops_cbk8_row();
 
 // Record the calling thread's last error (what qgemv_last_error returns);
 // returns `code`.  QGEMV_OK clears it.

@@ -59,6 +59,7 @@ const qgemv::FormatOps* ops_for(int format) {
     case kAqlmMma: return qgemv::ops_aqlm_mma();
     case QGEMV_AQLM_1X16: return qgemv::ops_aqlm_1x16();
     case QGEMV_CBK4_ROW: return qgemv::ops_cbk4_row();
+    case QGEMV_CBK8_ROW: return qgemv::ops_cbk8_row();
   }
   return nullptr;
 }
@@ -74,6 +75,7 @@ int64_t k_multiple(int format) {
     case kAqlmMma: return 8;
     case QGEMV_AQLM_1X16: return 8;
     case QGEMV_CBK4_ROW: return 2;
+    case QGEMV_CBK8_ROW: return 1;
   }
   return 0;
 }
@@ -90,6 +92,7 @@ int64_t codebook_count(int format) {
     case kAqlmMma: return 2 * 256 * 8;
     case QGEMV_AQLM_1X16: return 65536 * 8;
     case QGEMV_CBK4_ROW: return 16;  // per output row, fp32
+    case QGEMV_CBK8_ROW: return 256;  // per output row, fp32
   }
   return 0;
 }
@@ -232,6 +235,7 @@ int64_t qgemv_packed_bytes(int format, int64_t N, int64_t K) {
     case QGEMV_AQLM_2X8: return N * (K / 8) * 2;
     case QGEMV_AQLM_1X16: return N * (K / 8) * 2;
     case QGEMV_CBK4_ROW: return N * (K / 2);
+    case QGEMV_CBK8_ROW: return N * K;
   }
   return 0;
 }
@@ -267,6 +271,10 @@ static qgemv_handle create_impl(int format, int64_t N, int64_t K, const void* pa
   }
   if (N > (int64_t(1) << 31) || K > (int64_t(1) << 31)) {
     set_error(QGEMV_ERR_ARG, "N and K must be at most 2^31");
+    return nullptr;
+  }
+  if (format == QGEMV_CBK8_ROW && K > 65536) {  // one activation row is staged in shared memory
+    set_error(QGEMV_ERR_ARG, "CBK8_ROW takes K up to 65536 (got %lld)", (long long)K);
     return nullptr;
   }
   if (!packed) {
@@ -377,8 +385,9 @@ static qgemv_handle create_impl(int format, int64_t N, int64_t K, const void* pa
 
   e = to_device(packed, static_cast<size_t>(canonical_bytes(format, N, K)), &d_packed);
   if (e == cudaSuccess) e = to_device(scales, 2 * scales_count(format, N), &d_scales);
-  const int64_t cb_bytes = format == QGEMV_CBK4_ROW ? 4 * codebook_count(format) * N  // fp32 per row
-                                                    : 2 * codebook_count(format) * nseg;
+  const bool per_row_cb = format == QGEMV_CBK4_ROW || format == QGEMV_CBK8_ROW;
+  const int64_t cb_bytes = per_row_cb ? 4 * codebook_count(format) * N  // fp32 per row
+                                      : 2 * codebook_count(format) * nseg;
   if (e == cudaSuccess) e = to_device(codebooks, static_cast<size_t>(cb_bytes), &d_cb);
   if (e != cudaSuccess) return cleanup(QGEMV_ERR_CUDA, "copying the canonical inputs", e);
 
@@ -463,7 +472,8 @@ qgemv_handle qgemv_create_stacked(int format, int nseg, const int64_t* seg_rows,
     set_error(QGEMV_ERR_ARG, "unknown format %d", format);
     return nullptr;
   }
-  if (format == QGEMV_AQLM_2X8 || format == kAqlmMma || format == QGEMV_AQLM_1X16 || format == QGEMV_CBK4_ROW) {
+  if (format == QGEMV_AQLM_2X8 || format == kAqlmMma || format == QGEMV_AQLM_1X16 || format == QGEMV_CBK4_ROW ||
+      format == QGEMV_CBK8_ROW) {
     set_error(QGEMV_ERR_ARG, "format %d cannot be stacked", format);
     return nullptr;
   }

@@ -15,9 +15,9 @@ import os
 
 import numpy as np
 
-Q4_0, CBK4, CBK8, PQ2_0, AQLM_2X8, AQLM_1X16, CBK4_ROW = 1, 2, 3, 4, 5, 7, 8
+Q4_0, CBK4, CBK8, PQ2_0, AQLM_2X8, AQLM_1X16, CBK4_ROW, CBK8_ROW = 1, 2, 3, 4, 5, 7, 8, 9
 FORMATS = {"q4_0": Q4_0, "cbk4": CBK4, "cbk8": CBK8, "pq2_0": PQ2_0, "aqlm_2x8": AQLM_2X8,
-           "aqlm_1x16": AQLM_1X16, "cbk4_row": CBK4_ROW}
+           "aqlm_1x16": AQLM_1X16, "cbk4_row": CBK4_ROW, "cbk8_row": CBK8_ROW}
 QGEMV_OK, QGEMV_ERR_ARG, QGEMV_ERR_ALIGN, QGEMV_ERR_CUDA, QGEMV_ERR_TIMEOUT, QGEMV_ERR_NOMEM = range(6)
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "libqgemv.so")

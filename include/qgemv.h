@@ -76,7 +76,13 @@ typedef enum {
    * (64 bytes per row); K % 2 == 0; scales = NULL.  Every M runs the
    * CUDA-core kernel (fp32 centroids), at most two activation rows per
    * launch; a row's bits do not depend on M.                               */
-  QGEMV_CBK4_ROW = 8
+  QGEMV_CBK4_ROW = 8,
+  /* CBK8 with one codebook per output row, the 8-bit LM head of the same
+   * files (256 fp32 centroids per row): packed = uint8 [N][K]; codebooks =
+   * fp32 [N][256] (1 KB per row); 1 <= K <= 65536; scales = NULL.  One warp
+   * per output row, the row's codebook in shared memory; a row's bits do not
+   * depend on M.                                                            */
+  QGEMV_CBK8_ROW = 9
 } qgemv_format;
 
 /* Status codes. */
@@ -122,9 +128,9 @@ qgemv_handle qgemv_create(int format, int64_t N, int64_t K, const void* packed,
  *   codebooks (CBK4, CBK8): nseg codebooks one after the other (16 or 256
  *     fp16 each); segment s decodes with codebook s.  NULL for Q4_0 and
  *     PQ2_0, whose stacked handle is the plain concatenation.
- *   AQLM 2x8, AQLM 1x16 and CBK4_ROW are not accepted (QGEMV_ERR_ARG; the
- *   rows of a CBK4_ROW matrix carry their own codebooks, so one handle over
- *   the concatenated rows does the same).
+ *   AQLM 2x8, AQLM 1x16, CBK4_ROW and CBK8_ROW are not accepted
+ *   (QGEMV_ERR_ARG; the rows of a per-row-codebook matrix carry their own
+ *   codebooks, so one handle over the concatenated rows does the same).
  * Host or device pointers, copying, errors: as for qgemv_create.             */
 qgemv_handle qgemv_create_stacked(int format, int nseg, const int64_t* seg_rows, int64_t K,
                                   const void* packed, const void* scales, const void* codebooks);

@@ -11,7 +11,8 @@ import numpy as np
 
 from bit_weight_only_gb300 import inputs
 
-MIN_K = {"q4_0": 32, "cbk4": 2, "cbk8": 1, "pq2_0": 128, "aqlm_2x8": 8, "aqlm_1x16": 8, "cbk4_row": 2}
+MIN_K = {"q4_0": 32, "cbk4": 2, "cbk8": 1, "pq2_0": 128, "aqlm_2x8": 8, "aqlm_1x16": 8, "cbk4_row": 2,
+         "cbk8_row": 1}
 
 
 def make_case(fmt: str, N: int, K: int, tag: str = "case", seed: int = 0):
@@ -28,6 +29,9 @@ def make_case(fmt: str, N: int, K: int, tag: str = "case", seed: int = 0):
         return inputs.aqlm_inputs(g, N, K)
     if fmt == "aqlm_1x16":
         return inputs.aqlm_1x16_inputs(g, N, K)
+    if fmt == "cbk8_row":  # codebooks fp32 [N, 256], one per output row
+        cb = inputs.cbk_row_codebooks(g, N, L=256)
+        return inputs.cbk_packed(g, N, K, 8, inputs.cbk_cell_probs(inputs.cbk_centroids(256))), None, cb
     if fmt == "cbk4_row":  # codebooks fp32 [N, 16], one per output row
         cb = inputs.cbk_row_codebooks(g, N)
         return inputs.cbk_packed(g, N, K, 4, inputs.cbk_cell_probs(inputs.cbk_centroids(16))), None, cb

@@ -49,7 +49,8 @@ def test_packed_bytes_matches_formats(lib):
 
 
 @pytest.mark.parametrize("fmt, N, K", [("aqlm_1x16", 8192, 28672), ("aqlm_1x16", 3, 12), ("cbk4_row", 11008, 4096),
-                                       ("cbk4_row", 5, 7), ("q4_0", 9, 96), ("pq2_0", 9, 384), ("cbk8", 3, 5)])
+                                       ("cbk4_row", 5, 7), ("q4_0", 9, 96), ("pq2_0", 9, 384), ("cbk8", 3, 5),
+                                       ("cbk8_row", 32000, 4096), ("cbk8_row", 3, 5)])
 def test_packed_bytes_agree_with_the_oracle(lib, fmt, N, K):
     """The library's canonical sizes and the oracle's, written separately, agree."""
     import oracle
@@ -81,6 +82,8 @@ def test_prepared_activation_sizes_and_host_checks(lib):
     ((qgemv.AQLM_1X16, 8, 64, 1, None, 1), "needs scales"),
     ((qgemv.CBK4_ROW, 8, 64, 1, None, None), "needs codebooks"),
     ((qgemv.CBK4_ROW, 8, 63, 1, None, 1), "invalid shape"),
+    ((qgemv.CBK8_ROW, 8, 70000, 1, None, 1), "K up to 65536"),
+    ((qgemv.CBK8_ROW, 8, 64, 1, None, None), "needs codebooks"),
     ((6, 8, 64, 1, None, None), "unknown format"),
 ])
 def test_create_rejects_bad_arguments_on_host(lib, args, fragment):
