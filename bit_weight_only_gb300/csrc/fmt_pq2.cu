@@ -150,6 +150,7 @@ cudaError_t setup() {
   if (e == cudaSuccess) e = set_i8_smem_of<FmtPQ2I8P, 1>();
   if (e == cudaSuccess) e = set_i8_smem_of<FmtPQ2I8P, 2>();
   if (e == cudaSuccess) e = set_i8_smem_of<FmtPQ2I8P, 4>();
+  if (e == cudaSuccess) e = LaunchTable<F>::setup_glu();
   return e;
 }
 
@@ -361,7 +362,8 @@ const FormatOps* ops_pq2() {
       &LaunchTable<F>::smem_bytes, &setup, &LaunchTable<F>::launch,
       &prepare, &dequant, /*cb_entries=*/0, /*tile_rows=*/128, /*partial_stride=*/128 * 16,
       /*aux_per_row=*/0, /*m1_ctas_per_sm=*/LaunchTable<F>::kM1CtasPerSm, /*rowgroup=*/0,
-      /*launch_x_int8=*/&launch_x_int8, /*row_tables=*/0, /*launch_xq=*/&launch_xq};
+      /*launch_x_int8=*/&launch_x_int8, /*row_tables=*/0, /*launch_xq=*/&launch_xq,
+      /*launch_glu=*/&LaunchTable<F>::launch_glu};
   static_assert(I8::kM1CtasPerSm == LaunchTable<F>::kM1CtasPerSm && FmtPQ2I8::kKT == F::kKT &&
                     FmtPQ2I8::kTileBytes == F::kTileBytes,
                 "the INT8 path runs on the PQ2_0 handle's tiles, grid and plan");

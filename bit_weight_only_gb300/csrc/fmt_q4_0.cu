@@ -170,12 +170,22 @@ cudaError_t quantize_q4_0(const float* w, int64_t N, int64_t K, uint8_t* out, cu
   return cudaGetLastError();
 }
 
+namespace {
+cudaError_t setup_all() {
+  cudaError_t e = LaunchTable<F>::setup();
+  if (e == cudaSuccess) e = LaunchTable<F>::setup_glu();
+  return e;
+}
+}  // namespace
+
 const FormatOps* ops_q4_0() {
   static const FormatOps ops = {
       /*format=*/1, F::kKT, F::kTileBytes, /*aux_bytes=*/0,
-      &LaunchTable<F>::smem_bytes, &LaunchTable<F>::setup, &LaunchTable<F>::launch,
+      &LaunchTable<F>::smem_bytes, &setup_all, &LaunchTable<F>::launch,
       &prepare, &dequant, /*cb_entries=*/0, /*tile_rows=*/128, /*partial_stride=*/128 * 16,
-      /*aux_per_row=*/0, /*m1_ctas_per_sm=*/LaunchTable<F>::kM1CtasPerSm};
+      /*aux_per_row=*/0, /*m1_ctas_per_sm=*/LaunchTable<F>::kM1CtasPerSm, /*rowgroup=*/0,
+      /*launch_x_int8=*/nullptr, /*row_tables=*/0, /*launch_xq=*/nullptr,
+      /*launch_glu=*/&LaunchTable<F>::launch_glu};
   return &ops;
 }
 

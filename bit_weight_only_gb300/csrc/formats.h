@@ -62,6 +62,8 @@ struct FormatOps {
   int row_tables = 0;
   // PQ2_0 only: the run on prepared INT8 activations (qgemv_run_xq), else nullptr
   cudaError_t (*launch_xq)(int M, const GemvParams& p, const LaunchGeom& g, cudaStream_t s) = nullptr;
+  // Q4_0, PQ2_0: the fused SiLU(gate) * up run of a GLU handle (qgemv_create_glu), else nullptr
+  cudaError_t (*launch_glu)(int M, const GemvParams& p, const LaunchGeom& g, cudaStream_t s) = nullptr;
 };
 
 const FormatOps* ops_q4_0();

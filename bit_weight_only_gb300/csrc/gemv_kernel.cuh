@@ -332,6 +332,56 @@ __device__ __forceinline__ void finish_all(const GemvParams& p, int64_t stride, 
   if (s1) finish_segment<ROWS, M, NT>(p, stride, pl, 1, row_scales, out_scale, s_sub, tid, mrows);
 }
 
+// y[m][n] = SiLU(g) * u for a GLU handle (output width p.N / 2): SiLU(g) =
+// g / (1 + e^-g) in fp32 (expf, IEEE division), then one fp32 product.
+__device__ __forceinline__ void glu_store(const GemvParams& p, int m, int64_t n, float g, float u) {
+  const int64_t nout = p.N / 2;
+  if (n < nout) p.y[m * nout + n] = __fmul_rn(g / (1.0f + expf(-g)), u);
+}
+
+// Read one partial slot with a bounded poll and mark it empty again.
+__device__ __forceinline__ float take_slot(const GemvParams& p, float* slot) {
+  unsigned long long t_start = 0;
+  uint32_t bits;
+  while ((bits = ld_relaxed_u32(slot)) == kEmptySlot) {
+    const unsigned long long now = global_timer_ns();
+    if (t_start == 0) t_start = now;
+    else if (now - t_start > kWaitLimitNs) {
+      atomicOr(p.err, kErrTimeoutFixup);
+      return 0.f;
+    }
+  }
+  st_relaxed_u32(slot, kEmptySlot);
+  return __uint_as_float(bits);
+}
+
+// Finish a shared row tile of a GLU handle (plan segment sg, whose row slice
+// counts gate/up row pairs, 0..63): for each pair and activation row, the
+// gate and up sums over the S contributors in order, then SiLU(gate) * up.
+template <int M, int NT>
+__device__ __noinline__ void finish_rows_glu(const GemvParams& p, const CtaPlan& pl, int sg, float out_scale,
+                                             int tid) {
+  const int64_t rt = pl.seg_rt[sg];
+  const int64_t cf = pl.seg_cf[sg];
+  const int S = pl.seg_S[sg];
+  const int r0 = pl.seg_r0[sg];
+  const int nr = pl.seg_nr[sg];
+  if (nr <= 0) return;
+  float* first_slot = p.partials + (cf * 2 + (pl.seg_side1[sg] ? 1 : 0)) * kPartialStride;
+  float* base = p.partials + cf * 2 * kPartialStride;
+  for (int t = tid; t < nr * M; t += NT) {
+    const int m = t / nr;
+    const int r = r0 + (t - m * nr);
+    float g = 0.f, u = 0.f;
+    for (int i = 0; i < S; ++i) {
+      float* sl = (i == 0 ? first_slot : base + int64_t(i) * 2 * kPartialStride) + m * kTileRows;
+      g += take_slot(p, sl + r);
+      u += take_slot(p, sl + kTileRows / 2 + r);
+    }
+    glu_store(p, m, rt * (kTileRows / 2) + r, __fmul_rn(g, out_scale), __fmul_rn(u, out_scale));
+  }
+}
+
 // CTA c's share of the stream: [c * T / G, (c + 1) * T / G), with 32-bit
 // divisions when the products fit (the common case).
 __device__ __forceinline__ int64_t stream_split(int64_t c, int64_t T, int64_t G) {
@@ -377,7 +427,11 @@ __device__ __noinline__ void rebuild_table(uint8_t* lut, const uint16_t* cb, int
   F::template init_shared<NT>(lut, cb, warp, lane);
 }
 
-template <class F, int M>
+// GLU: the handle's rows are a gate and an up projection interleaved in
+// 64-row halves of every row tile (gate rows 64t .. 64t+63 are tile t's rows
+// 0..63, the up rows the same, rows 64..127), and y[m][64t + r] =
+// SiLU(gate) * up (glu_store, finish_rows_glu); p.N counts both halves.
+template <class F, int M, bool GLU = false>
 __global__ void __launch_bounds__(gemv_threads<F, M>(), F::kCtasPerSm) gemv_kernel(const GemvParams p) {
   constexpr int NS = F::stages(M);
   constexpr int TB = F::kTileBytes;
@@ -542,6 +596,30 @@ __global__ void __launch_bounds__(gemv_threads<F, M>(), F::kCtasPerSm) gemv_kern
     const bool owner = (cur_rt * p.nKT >= t0) && ((cur_rt + 1) * p.nKT <= t1);
     const int side = (cur_rt * p.nKT <= t0) ? 0 : 1;
     float* my_part = p.partials + (c * 2 + side) * kPartialStride;
+    if constexpr (GLU) {
+      if (owner) {  // a gate row and its up row per item
+        for (int o = tid; o < (kTileRows / 2) * M; o += NT) {
+          const int r = o % (kTileRows / 2);
+          const int m = o / (kTileRows / 2);
+          float g = 0.f, u = 0.f;
+#pragma unroll
+          for (int w = 0; w < red_slots<F, M>(); ++w) {
+            g += red[(w * kTileRows + r) * RS + m];
+            u += red[(w * kTileRows + kTileRows / 2 + r) * RS + m];
+          }
+          glu_store(p, m, cur_rt * (kTileRows / 2) + r, __fmul_rn(g, F::kOutScale), __fmul_rn(u, F::kOutScale));
+        }
+      } else {
+        for (int o = tid; o < kTileRows * M; o += NT) {
+          const int r = o % kTileRows;
+          const int m = o / kTileRows;
+          float v = 0.f;
+#pragma unroll
+          for (int w = 0; w < red_slots<F, M>(); ++w) v += red[(w * kTileRows + r) * RS + m];
+          st_relaxed_f32(my_part + m * kTileRows + r, v);
+        }
+      }
+    } else {
     for (int o = tid; o < kTileRows * M; o += NT) {
       const int r = o % kTileRows;
       const int m = o / kTileRows;
@@ -554,6 +632,7 @@ __global__ void __launch_bounds__(gemv_threads<F, M>(), F::kCtasPerSm) gemv_kern
       } else {
         st_relaxed_f32(my_part + m * kTileRows + r, v);
       }
+    }
     }
     named_bar_sync(1, NT);
     acc.reset();
@@ -655,7 +734,12 @@ __global__ void __launch_bounds__(gemv_threads<F, M>(), F::kCtasPerSm) gemv_kern
   static_assert(kSlices * kTileRows * RS >= 2 * NT, "finishing scratch");
   float* s_sub = red;
   wait_plan();
-  finish_all<kTileRows, M, NT>(p, kPartialStride, s_plan, nullptr, F::kOutScale, s_sub, tid);
+  if constexpr (GLU) {
+    for (int sg = 0; sg < 2; ++sg)
+      if (s_plan.seg_rt[sg] >= 0) finish_rows_glu<M, NT>(p, s_plan, sg, F::kOutScale, tid);
+  } else {
+    finish_all<kTileRows, M, NT>(p, kPartialStride, s_plan, nullptr, F::kOutScale, s_sub, tid);
+  }
 }
 
 // ------------------------------------------------- activation staging ----

@@ -77,6 +77,29 @@ struct LaunchTable {
     return cudaLaunchKernelEx(&cfg, gemv_rowgroup_kernel<F>, p);
   }
 
+  // GLU handles (gate and up interleaved; gemv_kernel's GLU epilogue): the
+  // M = 1 CUDA-core kernel once per activation row, on the M = 1 grid and
+  // its plan (made with 64-row halves).
+  static cudaError_t setup_glu() {
+    return cudaFuncSetAttribute(gemv_kernel<F, 1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                gemv_smem_bytes<F, 1>());
+  }
+  static cudaError_t launch_glu(int M, const GemvParams& p, const LaunchGeom& g, cudaStream_t s) {
+    if (M < 1 || M > kMaxM) return cudaErrorInvalidValue;
+    for (int m = 0; m < M; ++m) {
+      GemvParams q = p;
+      q.x = p.x + m * p.K;
+      q.y = p.y + m * (p.N / 2);
+      q.residual = nullptr;
+      q.plan = g.plan_m1;
+      cudaLaunchAttribute attr[1];
+      const cudaLaunchConfig_t cfg = config(g.grid_m1, gemv_threads<F, 1>(), gemv_smem_bytes<F, 1>(), s, attr);
+      const cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_kernel<F, 1, true>, q);
+      if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+  }
+
   static int smem_bytes(int M) {
     if (M == 1) return gemv_smem_bytes<F, 1>();
     if (M >= 2 && M <= 8) return F::mma_par(1) ? mma_smem_bytes<F, 1, true>() : mma_smem_bytes<F, 1>();

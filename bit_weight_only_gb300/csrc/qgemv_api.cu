@@ -218,6 +218,7 @@ struct qgemv_ctx {
   int* err;
   int batch_invariant;  // qgemv_set_batch_invariant
   int x_int8;           // qgemv_set_x_int8 (PQ2_0)
+  int glu;              // qgemv_create_glu: gate and up interleaved, output SiLU(gate) * up
   int skip_cta;         // QGEMV_FAULT_SKIP_CTA test hook, -1 normally
   qgemv_ctx* mma;       // AQLM: the tensor-core companion (format kAqlmMma), else nullptr
 };
@@ -254,7 +255,7 @@ static void free_handle(qgemv_ctx* h);
 // allocation fault counter keeps counting).
 static qgemv_handle create_impl(int format, int64_t N, int64_t K, const void* packed, const void* scales,
                                 const void* codebooks, int nseg, const int64_t* seg_rows,
-                                bool nested = false) {
+                                bool nested = false, bool glu = false) {
   const qgemv::FormatOps* ops = ops_for(format);
   if (k_multiple(format) == 0) {
     set_error(QGEMV_ERR_ARG, "unknown format %d", format);
@@ -317,6 +318,7 @@ static qgemv_handle create_impl(int format, int64_t N, int64_t K, const void* pa
     g_alloc_fail = env_int("QGEMV_FAULT_ALLOC", 0);
   }
   h->format = format;
+  h->glu = glu ? 1 : 0;
   h->N = N;
   h->K = K;
   h->ops = ops;
@@ -334,7 +336,7 @@ static qgemv_handle create_impl(int format, int64_t N, int64_t K, const void* pa
   // 7B shapes: the 4096 x 4096 projection gains 10%; with several row groups
   // per CTA (q|k|v, gate|up) the per-group epilogues and codebook changes
   // cost more than the split-K finish they save.
-  if (ops->rowgroup) {
+  if (ops->rowgroup && !glu) {
     const int64_t U = h->nRT * 4, nch = (h->nKT + 3) / 4;
     const int64_t Grg = U < sms ? U : sms;
     const int64_t rg_bytes = (U + Grg - 1) / Grg * h->nKT * (ops->tile_bytes / 4);
@@ -409,9 +411,11 @@ static qgemv_handle create_impl(int format, int64_t N, int64_t K, const void* pa
     e = cudaMemcpy(h->seg_of_rt, seg_of_rt.data(), 4 * seg_of_rt.size(), cudaMemcpyHostToDevice);
   }
   if (e == cudaSuccess) {
-    std::vector<qgemv::CtaPlan> plan = plan_stream_k(h->T, h->grid, h->nKT, ops->tile_rows);
+    // a GLU handle's shared row tiles are finished in gate/up row pairs
+    const int plan_rows = glu ? ops->tile_rows / 2 : ops->tile_rows;
+    std::vector<qgemv::CtaPlan> plan = plan_stream_k(h->T, h->grid, h->nKT, plan_rows);
     if (h->grid_m1 != h->grid) {
-      const std::vector<qgemv::CtaPlan> plan1 = plan_stream_k(h->T, h->grid_m1, h->nKT, ops->tile_rows);
+      const std::vector<qgemv::CtaPlan> plan1 = plan_stream_k(h->T, h->grid_m1, h->nKT, plan_rows);
       plan.insert(plan.end(), plan1.begin(), plan1.end());
     }
     e = cudaMemcpy(h->plan, plan.data(), sizeof(qgemv::CtaPlan) * plan.size(), cudaMemcpyHostToDevice);
@@ -493,6 +497,53 @@ qgemv_handle qgemv_create_stacked(int format, int nseg, const int64_t* seg_rows,
   return create_impl(format, N, K, packed, scales, codebooks, ops->cb_entries > 0 ? nseg : 1, seg_rows);
 }
 
+qgemv_handle qgemv_create_glu(int format, int64_t N, int64_t K, const void* packed_gate, const void* packed_up) {
+  const qgemv::FormatOps* ops = ops_for(format);
+  if (!ops || format == kAqlmMma || ops->launch_glu == nullptr) {
+    set_error(QGEMV_ERR_ARG, "format %d has no fused SiLU(gate) * up (Q4_0 and PQ2_0 have)", format);
+    return nullptr;
+  }
+  if (!packed_gate || !packed_up) {
+    set_error(QGEMV_ERR_ARG, "packed_gate or packed_up is NULL");
+    return nullptr;
+  }
+  const int64_t half = ops->tile_rows / 2;
+  const int64_t row_bytes = qgemv_packed_bytes(format, 1, K);
+  if (N <= 0 || N % half || row_bytes == 0 || N > (int64_t(1) << 30)) {
+    set_error(QGEMV_ERR_ARG, "invalid GLU shape N=%lld K=%lld (N must be a positive multiple of %lld)",
+              (long long)N, (long long)K, (long long)half);
+    return nullptr;
+  }
+  // gate rows 64b .. 64b+63, then up rows 64b .. 64b+63, for every block b:
+  // the canonical bytes of the interleaved 2N-row matrix
+  g_alloc_count = 0;
+  g_alloc_fail = env_int("QGEMV_FAULT_ALLOC", 0);
+  void* inter = nullptr;
+  const int64_t blk = half * row_bytes;
+  cudaError_t e = dev_alloc(&inter, static_cast<size_t>(2 * N * row_bytes));
+  for (int64_t b = 0; e == cudaSuccess && b < N / half; ++b) {
+    e = cudaMemcpy(static_cast<uint8_t*>(inter) + (2 * b) * blk, static_cast<const uint8_t*>(packed_gate) + b * blk,
+                   static_cast<size_t>(blk), cudaMemcpyDefault);
+    if (e == cudaSuccess)
+      e = cudaMemcpy(static_cast<uint8_t*>(inter) + (2 * b + 1) * blk, static_cast<const uint8_t*>(packed_up) + b * blk,
+                     static_cast<size_t>(blk), cudaMemcpyDefault);
+  }
+  if (e != cudaSuccess) {
+    cudaFree(inter);
+    if (e == cudaErrorMemoryAllocation) {
+      cudaGetLastError();
+      set_error(QGEMV_ERR_NOMEM, "interleaving gate and up: out of device memory");
+    } else {
+      cuda_error(e, "interleaving gate and up");
+    }
+    return nullptr;
+  }
+  const int64_t rows[1] = {2 * N};
+  qgemv_handle h = create_impl(format, 2 * N, K, inter, nullptr, nullptr, 1, rows, true, true);
+  cudaFree(inter);
+  return h;
+}
+
 static bool valid(qgemv_handle h) { return h && h->magic == kMagic; }
 
 }  // extern "C"
@@ -533,6 +584,14 @@ static int check_run_args(qgemv_handle h, const void* x, int M, float* y, const 
 static int run_impl(qgemv_handle h, const void* x, int M, float* y, const float* residual, void* stream) {
   const int rc = check_run_args(h, x, M, y, residual);
   if (rc != QGEMV_OK) return rc;
+  if (h->glu) {
+    if (residual) return set_error(QGEMV_ERR_ARG, "a GLU handle takes no residual");
+    const qgemv::GemvParams p = params_of(h, x, y, nullptr);
+    const qgemv::LaunchGeom g = {h->grid, h->plan, h->grid_m1, h->plan_m1, 0};
+    const cudaError_t e = h->ops->launch_glu(M, p, g, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_error(e, "launching the GEMV kernel");
+    return ok();
+  }
   const bool inv = h->batch_invariant != 0;
   if (h->mma && (M >= kAqlmMmaMinM || inv)) h = h->mma;  // AQLM: the tensor-core layout
   const qgemv::GemvParams p = params_of(h, x, y, residual);
@@ -562,8 +621,8 @@ int qgemv_set_batch_invariant(qgemv_handle h, int on) {
 
 int qgemv_set_x_int8(qgemv_handle h, int on) {
   if (!valid(h)) return set_error(QGEMV_ERR_ARG, "invalid handle");
-  if (h->ops->launch_x_int8 == nullptr)
-    return set_error(QGEMV_ERR_ARG, "INT8 activations need a PQ2_0 handle (format %d)", h->format);
+  if (h->ops->launch_x_int8 == nullptr || h->glu)
+    return set_error(QGEMV_ERR_ARG, "INT8 activations need a PQ2_0 handle without GLU (format %d)", h->format);
   h->x_int8 = on ? 1 : 0;
   return ok();
 }
@@ -593,8 +652,9 @@ int qgemv_prepare_x_int8(const void* x, int M, int64_t K, const int8_t* signs, i
 int qgemv_run_xq(qgemv_handle h, const void* xq, int M, float* y, const float* residual, void* stream) {
   const int rc = check_run_args(h, xq, M, y, residual);
   if (rc != QGEMV_OK) return rc;
-  if (h->ops->launch_xq == nullptr)
-    return set_error(QGEMV_ERR_ARG, "prepared INT8 activations need a PQ2_0 handle (format %d)", h->format);
+  if (h->ops->launch_xq == nullptr || h->glu)
+    return set_error(QGEMV_ERR_ARG, "prepared INT8 activations need a PQ2_0 handle without GLU (format %d)",
+                     h->format);
   qgemv::GemvParams p = params_of(h, xq, y, residual);
   const uint8_t* base = static_cast<const uint8_t*>(xq);
   p.x_scale = reinterpret_cast<const float*>(base + int64_t(M) * h->K);

@@ -36,6 +36,8 @@ _SIGNATURES = {
                                           ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "qgemv_set_batch_invariant": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int]),
     "qgemv_set_x_int8": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int]),
+    "qgemv_create_glu": (ctypes.c_void_p, [ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
+                                           ctypes.c_void_p, ctypes.c_void_p]),
     "qgemv_xq_bytes": (ctypes.c_int64, [ctypes.c_int, ctypes.c_int64]),
     "qgemv_prepare_x_int8": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_void_p,
                                             ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]),
@@ -121,6 +123,14 @@ def qgemv_create_stacked(fmt, seg_rows, K: int, packed: int, scales: int | None,
     """Several projections sharing K, rows stacked; one codebook per segment."""
     rows = (ctypes.c_int64 * len(seg_rows))(*[int(r) for r in seg_rows])
     h = load().qgemv_create_stacked(_fmt(fmt), len(seg_rows), rows, K, packed, scales, codebooks)
+    if not h:
+        raise QgemvError(qgemv_last_error_code(), qgemv_last_error())
+    return h
+
+
+def qgemv_create_glu(fmt, N: int, K: int, packed_gate: int, packed_up: int) -> int:
+    """Gate and up projections in one handle whose runs store SiLU(gate) * up."""
+    h = load().qgemv_create_glu(_fmt(fmt), N, K, packed_gate, packed_up)
     if not h:
         raise QgemvError(qgemv_last_error_code(), qgemv_last_error())
     return h
@@ -238,6 +248,18 @@ class QGemv:
         c, kc = _addr(codebooks)
         self.handle = qgemv_create_stacked(self.fmt, list(seg_rows), self.K, p, s, c)
         del kp, ks, kc
+        return self
+
+    @classmethod
+    def glu(cls, fmt, N: int, K: int, packed_gate, packed_up):
+        """Fused MLP gate/up: ``gemv(x)`` returns SiLU(x . G^T) * (x . U^T),
+        fp32 [M, N]."""
+        self = cls.__new__(cls)
+        self.fmt, self.N, self.K = _fmt(fmt), int(N), int(K)
+        g, kg = _addr(packed_gate)
+        u, ku = _addr(packed_up)
+        self.handle = qgemv_create_glu(self.fmt, self.N, self.K, g, u)
+        del kg, ku
         return self
 
     def run(self, x, y, stream=None):

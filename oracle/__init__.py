@@ -339,3 +339,32 @@ def prepare_x_int8(x, B: int = 0, signs=None):
     if B == 0:
         return quantize_x_int8(x)
     return quantize_f32_int8(hadamard_f32(x.astype(np.float32), B, signs))
+
+
+def silu(v):
+    """SiLU (the gate activation of the pages' MLP), v / (1 + exp(-v)), fp64."""
+    v = np.asarray(v, dtype=np.float64)
+    return v / (1.0 + np.exp(-v))
+
+
+def gemv_glu(fmt, N: int, K: int, packed_gate, packed_up, x, nthreads: int | None = None):
+    """The fused gate/up projection of a decoder MLP: y = SiLU(x . G^T) * (x . U^T)
+    for two matrices of the same format and shape [N, K] (formats without
+    scales or codebooks).  Returns (y, g, u, bound_g, bound_u), fp64 [M, N]."""
+    g, bg = gemv(fmt, N, K, packed_gate, None, None, x, nthreads=nthreads)
+    u, bu = gemv(fmt, N, K, packed_up, None, None, x, nthreads=nthreads)
+    return silu(g) * u, g, u, bg, bu
+
+
+def within_tolerance_glu(y, g, u, bound_g, bound_u):
+    """Acceptance for SiLU(g) * u (reading R14): each GEMV output may be off by
+    its own bound e = 1e-3 * B + 1e-6; SiLU's slope is below 1.1, so the
+    product may be off by 1.1 e_g (|u| + e_u) + |SiLU(g)| e_u, plus a few fp32
+    roundings of the result (expf, the division and the product)."""
+    y = np.asarray(y, dtype=np.float64)
+    eg = 1e-3 * np.asarray(bound_g) + 1e-6
+    eu = 1e-3 * np.asarray(bound_u) + 1e-6
+    sg = np.abs(silu(g))
+    au = np.abs(u)
+    lim = 1.1 * eg * (au + eu) + sg * eu + 2.0 ** -20 * (sg + 1.1 * eg) * (au + eu)
+    return np.abs(y - silu(g) * u) <= lim

@@ -119,6 +119,16 @@ def test_stacked_create_rejects_bad_arguments_on_host(lib):
     assert "cannot be stacked" in qgemv.qgemv_last_error()
 
 
+def test_glu_create_rejects_bad_arguments_on_host(lib):
+    assert not lib.qgemv_create_glu(qgemv.CBK4, 128, 256, 1, 1)
+    assert "no fused" in qgemv.qgemv_last_error()
+    assert not lib.qgemv_create_glu(qgemv.PQ2_0, 100, 256, 1, 1)
+    assert "multiple of 64" in qgemv.qgemv_last_error()
+    assert not lib.qgemv_create_glu(qgemv.Q4_0, 128, 48, 1, 1)
+    assert not lib.qgemv_create_glu(qgemv.Q4_0, 128, 64, None, 1)
+    assert qgemv.qgemv_last_error_code() == qgemv.QGEMV_ERR_ARG
+
+
 def test_quantizer_rejects_bad_shape(lib):
     assert lib.qgemv_quantize_q4_0(16, 4, 48, 16, None) == qgemv.QGEMV_ERR_ARG
     assert lib.qgemv_quantize_q4_0(None, 4, 64, 16, None) == qgemv.QGEMV_ERR_ARG

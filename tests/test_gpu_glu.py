@@ -1,0 +1,101 @@
+"""GPU parity of the fused MLP gate/up projection (qgemv_create_glu):
+y = SiLU(x . G^T) * (x . U^T) in one launch per activation row, against the
+oracle's ``gemv_glu`` with the bound of ``within_tolerance_glu`` (each GEMV
+sum within its own 1e-3 * sum |x w| + 1e-6, propagated through SiLU and the
+product, plus a few fp32 roundings).
+
+Covered: Q4_0 and PQ2_0; shapes whose row tiles are split between CTAs
+(the pair finisher) and owned whole (the epilogue); the 7B MLP's gate/up
+11008 x 4096 and the 5120/17408 model's 17408 x 5120 at full size on
+sampled outputs; M = 1 and 3; the dequant of the interleaved rows; and the
+refusals (codebook formats, N not a multiple of 64, residual, INT8 mode).
+"""
+import numpy as np
+import pytest
+
+import oracle
+from bit_weight_only_gb300 import build, inputs, qgemv
+from cases import make_case, make_x
+
+torch = pytest.importorskip("torch")
+pytestmark = [pytest.mark.gpu, pytest.mark.late]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    build.build()
+    qgemv.load()
+
+
+def _pair(fmt, N, K, tag):
+    if fmt == "q4_0":
+        g = inputs.rng(f"{tag}/gate")
+        u = inputs.rng(f"{tag}/up")
+        return (oracle.quantize_q4_0(inputs.w_fp32(g, N, K), N, K),
+                oracle.quantize_q4_0(inputs.w_fp32(u, N, K), N, K))
+    return (make_case(fmt, N, K, tag=f"{tag}/gate")[0], make_case(fmt, N, K, tag=f"{tag}/up")[0])
+
+
+@pytest.mark.parametrize("fmt", ["q4_0", "pq2_0"])
+@pytest.mark.parametrize("N,K", [(192, 1024), (704, 2048), (4096, 4096)])
+@pytest.mark.parametrize("M", [1, 3])
+def test_glu_matches_oracle(fmt, N, K, M):
+    pg, pu = _pair(fmt, N, K, f"glu/{fmt}/{N}x{K}")
+    h = qgemv.QGemv.glu(fmt, N, K, pg, pu)
+    x_np = make_x(M, K, tag="glu")
+    y = h.gemv(torch.from_numpy(x_np).cuda())
+    torch.cuda.synchronize()
+    assert h.status() == qgemv.QGEMV_OK
+    assert y.shape == (M, N)
+    y_ref, g, u, bg, bu = oracle.gemv_glu(fmt, N, K, pg, pu, x_np)
+    ok = oracle.within_tolerance_glu(y.cpu().numpy(), g, u, bg, bu)
+    assert ok.all(), f"{fmt} {N}x{K} M={M}: {np.count_nonzero(~ok)} outputs out of tolerance"
+
+
+@pytest.mark.parametrize("fmt,N,K", [("q4_0", 11008, 4096), ("pq2_0", 17408, 5120)])
+def test_glu_full_size_sampled(fmt, N, K):
+    pg, pu = _pair(fmt, N, K, f"glufull/{fmt}")
+    h = qgemv.QGemv.glu(fmt, N, K, pg, pu)
+    x_np = make_x(1, K, tag="glufull")
+    y = h.gemv(torch.from_numpy(x_np).cuda()).cpu().numpy()
+    assert h.status() == qgemv.QGEMV_OK
+    rows = np.unique(np.concatenate([[0, 63, 64, 127, N // 2, N - 65, N - 1],
+                                     np.random.default_rng(1).integers(0, N, 48)]))
+    g, bg = oracle.gemv(fmt, N, K, pg, None, None, x_np, rows=rows)
+    u, bu = oracle.gemv(fmt, N, K, pu, None, None, x_np, rows=rows)
+    ok = oracle.within_tolerance_glu(y[:, rows], g, u, bg, bu)
+    assert ok.all(), f"{fmt} {N}x{K}: {np.count_nonzero(~ok)} sampled outputs out of tolerance"
+
+
+def test_glu_dequant_is_the_interleaved_rows():
+    N, K = 192, 1024
+    pg, pu = _pair("pq2_0", N, K, "gludq")
+    h = qgemv.QGemv.glu("pq2_0", N, K, pg, pu)
+    # the handle's N is the output width; its decoded matrix has 2N rows
+    w = torch.empty((2 * N, K), dtype=torch.float32, device="cuda")
+    qgemv.qgemv_dequant(h.handle, w.data_ptr())
+    torch.cuda.synchronize()
+    G = oracle.dequant("pq2_0", N, K, pg)
+    U = oracle.dequant("pq2_0", N, K, pu)
+    inter = np.concatenate([blk for b in range(N // 64) for blk in (G[64 * b:64 * b + 64], U[64 * b:64 * b + 64])])
+    assert np.array_equal(w.cpu().numpy().astype(np.float64), inter)
+
+
+def test_glu_refusals():
+    lib = qgemv.load()
+    N, K = 192, 1024
+    pg, pu = _pair("pq2_0", N, K, "glurefuse")
+    packed, _, cb = make_case("cbk4", N, K, tag="glurefuse")
+    with pytest.raises(qgemv.QgemvError):
+        qgemv.QGemv.glu("cbk4", N, K, packed, packed)
+    with pytest.raises(qgemv.QgemvError):
+        qgemv.QGemv.glu("pq2_0", 100, K, pg[:100 * (K // 128) * 34], pu[:100 * (K // 128) * 34])
+    h = qgemv.QGemv.glu("pq2_0", N, K, pg, pu)
+    x = torch.from_numpy(make_x(1, K, tag="glurefuse")).cuda()
+    y = torch.empty((1, N), dtype=torch.float32, device="cuda")
+    r = torch.zeros((1, N), dtype=torch.float32, device="cuda")
+    assert lib.qgemv_run_residual(h.handle, x.data_ptr(), 1, y.data_ptr(), r.data_ptr(), None) == qgemv.QGEMV_ERR_ARG
+    assert lib.qgemv_set_x_int8(h.handle, 1) == qgemv.QGEMV_ERR_ARG
+    torch.cuda.synchronize()

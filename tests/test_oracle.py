@@ -372,6 +372,43 @@ def test_prepared_activations_and_codes_gemv():
     assert np.array_equal(y1, y2) and np.array_equal(b1, b2)
 
 
+# --------------------------------------------------- SiLU(gate) * up ---
+
+def test_silu_is_x_times_the_library_logistic():
+    """Pin (library routine and closed forms): SiLU(v) = v * expit(v); SiLU(0)
+    = 0; it tends to v for large v and to 0 for very negative v."""
+    sp = pytest.importorskip("scipy.special")
+    v = np.linspace(-30, 30, 1201)
+    assert np.allclose(oracle.silu(v), v * sp.expit(v), rtol=1e-14, atol=1e-300)
+    assert oracle.silu(0.0) == 0.0
+    assert abs(oracle.silu(40.0) - 40.0) < 1e-12 and abs(oracle.silu(-40.0)) < 1e-15
+
+
+def test_gemv_glu_one_hot_closed_form():
+    """Pin: a one-hot x picks column k of both matrices, so the fused output
+    is SiLU(G[:, k]) * U[:, k]."""
+    N, K = 40, 256
+    pg = inputs.pq2_packed(inputs.rng("glu/g"), N, K)
+    pu = inputs.pq2_packed(inputs.rng("glu/u"), N, K)
+    G = oracle.dequant("pq2_0", N, K, pg)
+    U = oracle.dequant("pq2_0", N, K, pu)
+    x = np.zeros((2, K), dtype=np.float16)
+    x[0, 3] = 1.0
+    x[1, 200] = 1.0
+    y, g, u, _, _ = oracle.gemv_glu("pq2_0", N, K, pg, pu, x)
+    assert np.array_equal(g[0], G[:, 3]) and np.array_equal(u[1], U[:, 200])
+    v = G[:, 3]
+    assert np.allclose(y[0], v / (1 + np.exp(-v)) * U[:, 3], rtol=1e-15, atol=0)
+
+
+def test_glu_tolerance_rule():
+    g = np.array([1.0, -2.0]); u = np.array([3.0, 0.5])
+    bg = np.array([10.0, 10.0]); bu = np.array([1.0, 1.0])
+    y_ref = oracle.silu(g) * u
+    assert oracle.within_tolerance_glu(y_ref + 1e-3 * 10 * 3 * 1.05, g, u, bg, bu)[0]
+    assert not oracle.within_tolerance_glu(y_ref + 0.1, g, u, bg, bu).any()
+
+
 # ---------------------------------------------------------------- Q4_0 ---
 
 def test_q4_0_roundtrip_is_exact_for_representable_blocks():
