@@ -155,6 +155,9 @@ WORKLOADS = {
                      "CBK4 with per-row fp32 codebooks, down 8192x28672"),
     "cbk8row_head": (lambda: [("cbk8_row", "lm_head", 32000, 4096)], "cbk8_row",
                      "CBK8 LM head 32000x4096 with per-row fp32 codebooks (256 per row)"),
+    "pq2_5120_glu": (lambda: [("pq2_0_glu", "gate_up", 17408, 5120), ("pq2_0", "down", 5120, 17408)], "pq2_0_glu",
+                     "PQ2_0 MLP of the 5120/17408 model: gate and up 17408x5120 with SiLU(gate)*up fused "
+                     "(one launch), then down 5120x17408"),
 }
 
 
@@ -194,6 +197,19 @@ def build_handles(specs, M, device, seed=0):
             y = y_all[yo:yo + M * N].view(M, N)
             xo += M * K
             yo += M * N
+            ops.append({"fmt": fmt, "name": name, "N": N, "K": K, "h": h, "x": x, "y": y, "bytes": nbytes})
+            continue
+        if fmt == "pq2_0_glu":  # gate and up in one handle, output SiLU(gate) * up
+            pg = inputs.pq2_packed_cuda(f"{tag}/gate", N, K, device=device, seed=seed)
+            pu = inputs.pq2_packed_cuda(f"{tag}/up", N, K, device=device, seed=seed)
+            h = qgemv.QGemv.glu("pq2_0", N, K, pg, pu)
+            del pg, pu
+            x = x_all[xo:xo + M * K].view(M, K)
+            x.copy_(inputs.x_fp16_cuda(f"{tag}/x", M, K, device=device, seed=seed))
+            y = y_all[yo:yo + M * N].view(M, N)
+            xo += M * K
+            yo += M * N
+            nbytes = 2 * qgemv.qgemv_packed_bytes("pq2_0", N, K) + 2 * M * K + 4 * M * N
             ops.append({"fmt": fmt, "name": name, "N": N, "K": K, "h": h, "x": x, "y": y, "bytes": nbytes})
             continue
         if fmt == "cbk4":
@@ -319,7 +335,8 @@ def run_ours(args, rank, world, device):
     # runs all of them back to back, so no copy is still in L2 when its turn
     # comes round again.
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
-    one_copy = sum(qgemv.qgemv_packed_bytes(f, total_rows(N), K) for f, _, N, K in specs)
+    one_copy = sum(qgemv.qgemv_packed_bytes(f if f != "pq2_0_glu" else "pq2_0", total_rows(N), K)
+                   * (2 if f == "pq2_0_glu" else 1) for f, _, N, K in specs)
     R = 1 if one_copy >= 3 * l2 else -(-3 * l2 // one_copy)
     copies = [build_handles(specs, M, device, seed=r) for r in range(R)]
     ops = [o for c_ops, _, _ in copies for o in c_ops]
@@ -479,6 +496,8 @@ def run_ours(args, rank, world, device):
                                 if dominant == "cbk4_row"
                                 else "gemv_rowcb8_kernel<MB> (one warp per row, its codebook in shared memory)"
                                 if dominant == "cbk8_row"
+                                else "gemv_kernel<FmtPQ2, 1, GLU> (gate and up interleaved, SiLU(gate)*up stored)"
+                                if dominant == "pq2_0_glu"
                                 else f"aqlm_gemv_kernel<MB={M}>" if dominant == "aqlm_2x8" and M <= 2
                                 else (f"gemv_kernel<{dominant}, M=1>"
                                       + (" and gemv_rowgroup_kernel (matrices of at most one 32-row group per SM)"
@@ -495,7 +514,8 @@ def run_ours(args, rank, world, device):
         # tensor-core kernel); the INT8 path launches once per 4, 2 or 1
         # rows, CBK4_ROW once per 2 or 1
         "gpu_launches": sum((x_int8_launches(M) + (1 if "xq" in o else 0)) if o.get("x_int8") else
-                            (M + 1) // 2 if o["fmt"] == "cbk4_row" else 1 for o in ops) * K,
+                            (M + 1) // 2 if o["fmt"] == "cbk4_row" else
+                            M if o["fmt"] == "pq2_0_glu" else 1 for o in ops) * K,
         "clocks": clocks,
     }
     if not args.no_cpu_baseline and world == 1:
@@ -522,6 +542,8 @@ def oracle_sample(workload, M, rows, seed=0):
         packed = inputs.cbk_packed(g, rows, K, 8, inputs.cbk_cell_probs(cb))
     elif fmt == "pq2_0":
         packed = inputs.pq2_packed(g, rows, K)
+    elif fmt == "pq2_0_glu":  # (gate, up)
+        packed = (inputs.pq2_packed(g, rows, K), inputs.pq2_packed(g, rows, K))
     elif fmt == "q4_0":
         packed = inputs.q4_0_random_blocks(g, rows, K)
     elif fmt == "aqlm_1x16":
@@ -535,7 +557,8 @@ def oracle_sample(workload, M, rows, seed=0):
     else:
         packed, scales, cb = inputs.aqlm_inputs(g, rows, K)
     x = inputs.x_fp16(inputs.rng("cpu/x", seed), M, K)
-    nbytes = (packed.nbytes + (0 if scales is None else scales.nbytes)
+    pbytes = sum(a.nbytes for a in packed) if isinstance(packed, tuple) else packed.nbytes
+    nbytes = (pbytes + (0 if scales is None else scales.nbytes)
               + (0 if cb is None else cb.nbytes) + x.nbytes + 4 * M * rows)
     return fmt, name, rows, K, packed, scales, cb, x, nbytes
 
@@ -547,7 +570,9 @@ def time_oracle(workload, M, rows, threads, reps=1, x_int8=False, prepared=None)
     signs = np.random.default_rng(0).choice([-1, 1], size=K).astype(np.int8) if prepared else None
     t0 = time.perf_counter()
     for _ in range(reps):
-        if int8 and prepared is not None:
+        if fmt == "pq2_0_glu":
+            oracle.gemv_glu("pq2_0", rows, K, packed[0], packed[1], x, nthreads=threads)
+        elif int8 and prepared is not None:
             q, a = oracle.prepare_x_int8(x, prepared, signs)
             oracle.gemv_pq2_int8_q(rows, K, packed, q, a, nthreads=threads)
         elif int8:
