@@ -339,15 +339,18 @@ __device__ __forceinline__ void glu_store(const GemvParams& p, int m, int64_t n,
   if (n < nout) p.y[m * nout + n] = __fmul_rn(g / (1.0f + expf(-g)), u);
 }
 
-// Read one partial slot with a bounded poll and mark it empty again.
-__device__ __forceinline__ float take_slot(const GemvParams& p, float* slot) {
+// Read one partial slot with a bounded poll and mark it empty again.  After
+// a wait of this thread has given up (gave_up), later slots are not waited
+// for, so a run whose partials never come ends after one time limit.
+__device__ __forceinline__ float take_slot(const GemvParams& p, float* slot, bool& gave_up) {
   unsigned long long t_start = 0;
   uint32_t bits;
   while ((bits = ld_relaxed_u32(slot)) == kEmptySlot) {
     const unsigned long long now = global_timer_ns();
     if (t_start == 0) t_start = now;
-    else if (now - t_start > kWaitLimitNs) {
+    else if (gave_up || now - t_start > kWaitLimitNs) {
       atomicOr(p.err, kErrTimeoutFixup);
+      gave_up = true;
       return 0.f;
     }
   }
@@ -369,14 +372,15 @@ __device__ __noinline__ void finish_rows_glu(const GemvParams& p, const CtaPlan&
   if (nr <= 0) return;
   float* first_slot = p.partials + (cf * 2 + (pl.seg_side1[sg] ? 1 : 0)) * kPartialStride;
   float* base = p.partials + cf * 2 * kPartialStride;
+  bool gave_up = false;
   for (int t = tid; t < nr * M; t += NT) {
     const int m = t / nr;
     const int r = r0 + (t - m * nr);
     float g = 0.f, u = 0.f;
     for (int i = 0; i < S; ++i) {
       float* sl = (i == 0 ? first_slot : base + int64_t(i) * 2 * kPartialStride) + m * kTileRows;
-      g += take_slot(p, sl + r);
-      u += take_slot(p, sl + kTileRows / 2 + r);
+      g += take_slot(p, sl + r, gave_up);
+      u += take_slot(p, sl + kTileRows / 2 + r, gave_up);
     }
     glu_store(p, m, rt * (kTileRows / 2) + r, __fmul_rn(g, out_scale), __fmul_rn(u, out_scale));
   }
