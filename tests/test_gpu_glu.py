@@ -99,3 +99,30 @@ def test_glu_refusals():
     assert lib.qgemv_run_residual(h.handle, x.data_ptr(), 1, y.data_ptr(), r.data_ptr(), None) == qgemv.QGEMV_ERR_ARG
     assert lib.qgemv_set_x_int8(h.handle, 1) == qgemv.QGEMV_ERR_ARG
     torch.cuda.synchronize()
+
+
+def test_glu_lost_cta_times_out_and_context_survives(monkeypatch):
+    """QGEMV_FAULT_SKIP_CTA: one 128-row tile (64 gate/up pairs) split over
+    every CTA, CTA 0 a no-op: the pair finisher's bounded waits give up, the
+    status reports the timeout, and a normal GLU handle then computes
+    correctly (the failure is made on the host; nothing traps or hangs)."""
+    import time
+    N, K = 64, 32768
+    pg, pu = _pair("pq2_0", N, K, "glufault")
+    x_np = make_x(1, K, tag="glufault")
+    x = torch.from_numpy(x_np).cuda()
+    monkeypatch.setenv("QGEMV_FAULT_SKIP_CTA", "0")
+    bad = qgemv.QGemv.glu("pq2_0", N, K, pg, pu)
+    monkeypatch.delenv("QGEMV_FAULT_SKIP_CTA")
+    good = qgemv.QGemv.glu("pq2_0", N, K, pg, pu)
+    t0 = time.time()
+    bad.gemv(x)
+    with pytest.raises(qgemv.QgemvError) as err:
+        bad.status()
+    assert err.value.code == qgemv.QGEMV_ERR_TIMEOUT
+    assert time.time() - t0 < 60
+    y = good.gemv(x)
+    torch.cuda.synchronize()
+    assert good.status() == qgemv.QGEMV_OK
+    y_ref, g, u, bg, bu = oracle.gemv_glu("pq2_0", N, K, pg, pu, x_np)
+    assert oracle.within_tolerance_glu(y.cpu().numpy(), g, u, bg, bu).all()
