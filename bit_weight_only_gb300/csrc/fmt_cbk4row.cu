@@ -70,6 +70,7 @@ cudaError_t set_smem() {
 cudaError_t setup() {
   cudaError_t e = set_smem<1>();
   if (e == cudaSuccess) e = set_smem<2>();
+  if (e == cudaSuccess) e = LaunchTable<F>::setup_glu();
   return e;
 }
 
@@ -107,7 +108,8 @@ const FormatOps* ops_cbk4_row() {
       /*format=*/8, F::kKT, F::kTileBytes, /*aux_bytes=*/0,
       &smem_bytes, &setup, &launch, &prepare, &dequant, /*cb_entries=*/F::kCbEntries, /*tile_rows=*/128,
       /*partial_stride=*/128 * 16, /*aux_per_row=*/0, /*m1_ctas_per_sm=*/F::kCtasPerSm, /*rowgroup=*/0,
-      /*launch_x_int8=*/nullptr, /*row_tables=*/1};
+      /*launch_x_int8=*/nullptr, /*row_tables=*/1, /*launch_xq=*/nullptr,
+      /*launch_glu=*/&LaunchTable<F>::launch_glu};
   return &ops;
 }
 

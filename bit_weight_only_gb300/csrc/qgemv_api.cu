@@ -497,14 +497,22 @@ qgemv_handle qgemv_create_stacked(int format, int nseg, const int64_t* seg_rows,
   return create_impl(format, N, K, packed, scales, codebooks, ops->cb_entries > 0 ? nseg : 1, seg_rows);
 }
 
-qgemv_handle qgemv_create_glu(int format, int64_t N, int64_t K, const void* packed_gate, const void* packed_up) {
+qgemv_handle qgemv_create_glu(int format, int64_t N, int64_t K, const void* packed_gate, const void* packed_up,
+                              const void* codebooks_gate, const void* codebooks_up) {
   const qgemv::FormatOps* ops = ops_for(format);
   if (!ops || format == kAqlmMma || ops->launch_glu == nullptr) {
-    set_error(QGEMV_ERR_ARG, "format %d has no fused SiLU(gate) * up (Q4_0 and PQ2_0 have)", format);
+    set_error(QGEMV_ERR_ARG, "format %d has no fused SiLU(gate) * up (Q4_0, PQ2_0 and CBK4_ROW have)", format);
     return nullptr;
   }
   if (!packed_gate || !packed_up) {
     set_error(QGEMV_ERR_ARG, "packed_gate or packed_up is NULL");
+    return nullptr;
+  }
+  const bool row_cb = format == QGEMV_CBK4_ROW;  // per-row codebooks travel with their rows
+  if (row_cb != (codebooks_gate != nullptr && codebooks_up != nullptr) ||
+      (!row_cb && (codebooks_gate != nullptr || codebooks_up != nullptr))) {
+    set_error(QGEMV_ERR_ARG, row_cb ? "CBK4_ROW needs both codebook arrays" : "format %d takes no codebooks",
+              format);
     return nullptr;
   }
   const int64_t half = ops->tile_rows / 2;
@@ -519,17 +527,27 @@ qgemv_handle qgemv_create_glu(int format, int64_t N, int64_t K, const void* pack
   g_alloc_count = 0;
   g_alloc_fail = env_int("QGEMV_FAULT_ALLOC", 0);
   void* inter = nullptr;
-  const int64_t blk = half * row_bytes;
+  void* inter_cb = nullptr;
+  // interleave 64-row blocks of two row-major arrays of `rb` bytes per row
+  auto interleave = [&](void* dst, const void* a, const void* b, int64_t rb) {
+    const int64_t blk = half * rb;
+    cudaError_t ce = cudaSuccess;
+    for (int64_t i = 0; ce == cudaSuccess && i < N / half; ++i) {
+      ce = cudaMemcpy(static_cast<uint8_t*>(dst) + (2 * i) * blk, static_cast<const uint8_t*>(a) + i * blk,
+                      static_cast<size_t>(blk), cudaMemcpyDefault);
+      if (ce == cudaSuccess)
+        ce = cudaMemcpy(static_cast<uint8_t*>(dst) + (2 * i + 1) * blk, static_cast<const uint8_t*>(b) + i * blk,
+                        static_cast<size_t>(blk), cudaMemcpyDefault);
+    }
+    return ce;
+  };
   cudaError_t e = dev_alloc(&inter, static_cast<size_t>(2 * N * row_bytes));
-  for (int64_t b = 0; e == cudaSuccess && b < N / half; ++b) {
-    e = cudaMemcpy(static_cast<uint8_t*>(inter) + (2 * b) * blk, static_cast<const uint8_t*>(packed_gate) + b * blk,
-                   static_cast<size_t>(blk), cudaMemcpyDefault);
-    if (e == cudaSuccess)
-      e = cudaMemcpy(static_cast<uint8_t*>(inter) + (2 * b + 1) * blk, static_cast<const uint8_t*>(packed_up) + b * blk,
-                     static_cast<size_t>(blk), cudaMemcpyDefault);
-  }
+  if (e == cudaSuccess) e = interleave(inter, packed_gate, packed_up, row_bytes);
+  if (e == cudaSuccess && row_cb) e = dev_alloc(&inter_cb, static_cast<size_t>(2 * N * 16 * 4));
+  if (e == cudaSuccess && row_cb) e = interleave(inter_cb, codebooks_gate, codebooks_up, 16 * 4);
   if (e != cudaSuccess) {
     cudaFree(inter);
+    cudaFree(inter_cb);
     if (e == cudaErrorMemoryAllocation) {
       cudaGetLastError();
       set_error(QGEMV_ERR_NOMEM, "interleaving gate and up: out of device memory");
@@ -539,8 +557,9 @@ qgemv_handle qgemv_create_glu(int format, int64_t N, int64_t K, const void* pack
     return nullptr;
   }
   const int64_t rows[1] = {2 * N};
-  qgemv_handle h = create_impl(format, 2 * N, K, inter, nullptr, nullptr, 1, rows, true, true);
+  qgemv_handle h = create_impl(format, 2 * N, K, inter, nullptr, inter_cb, 1, rows, true, true);
   cudaFree(inter);
+  cudaFree(inter_cb);
   return h;
 }
 

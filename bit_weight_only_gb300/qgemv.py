@@ -37,7 +37,7 @@ _SIGNATURES = {
     "qgemv_set_batch_invariant": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int]),
     "qgemv_set_x_int8": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int]),
     "qgemv_create_glu": (ctypes.c_void_p, [ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
-                                           ctypes.c_void_p, ctypes.c_void_p]),
+                                           ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "qgemv_xq_bytes": (ctypes.c_int64, [ctypes.c_int, ctypes.c_int64]),
     "qgemv_prepare_x_int8": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_void_p,
                                             ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]),
@@ -128,9 +128,10 @@ def qgemv_create_stacked(fmt, seg_rows, K: int, packed: int, scales: int | None,
     return h
 
 
-def qgemv_create_glu(fmt, N: int, K: int, packed_gate: int, packed_up: int) -> int:
+def qgemv_create_glu(fmt, N: int, K: int, packed_gate: int, packed_up: int,
+                     codebooks_gate: int | None = None, codebooks_up: int | None = None) -> int:
     """Gate and up projections in one handle whose runs store SiLU(gate) * up."""
-    h = load().qgemv_create_glu(_fmt(fmt), N, K, packed_gate, packed_up)
+    h = load().qgemv_create_glu(_fmt(fmt), N, K, packed_gate, packed_up, codebooks_gate, codebooks_up)
     if not h:
         raise QgemvError(qgemv_last_error_code(), qgemv_last_error())
     return h
@@ -251,15 +252,17 @@ class QGemv:
         return self
 
     @classmethod
-    def glu(cls, fmt, N: int, K: int, packed_gate, packed_up):
+    def glu(cls, fmt, N: int, K: int, packed_gate, packed_up, codebooks_gate=None, codebooks_up=None):
         """Fused MLP gate/up: ``gemv(x)`` returns SiLU(x . G^T) * (x . U^T),
-        fp32 [M, N]."""
+        fp32 [M, N] (codebooks: CBK4_ROW's per-row fp32 [N, 16] arrays)."""
         self = cls.__new__(cls)
         self.fmt, self.N, self.K = _fmt(fmt), int(N), int(K)
         g, kg = _addr(packed_gate)
         u, ku = _addr(packed_up)
-        self.handle = qgemv_create_glu(self.fmt, self.N, self.K, g, u)
-        del kg, ku
+        cg, kcg = _addr(codebooks_gate)
+        cu, kcu = _addr(codebooks_up)
+        self.handle = qgemv_create_glu(self.fmt, self.N, self.K, g, u, cg, cu)
+        del kg, ku, kcg, kcu
         return self
 
     def run(self, x, y, stream=None):

@@ -140,12 +140,15 @@ qgemv_handle qgemv_create_stacked(int format, int nseg, const int64_t* seg_rows,
  * [m][n], SiLU(v) = v / (1 + e^-v): the gate/up GEMV with "SiLU(gate) * up
  * in the reduce" of "Trapetum benchmarks" ("Short-context decode, step by
  * step"), one launch per activation row and no separate activation kernel.
- *   format: QGEMV_Q4_0 or QGEMV_PQ2_0 (formats without codebooks, since the
- *     gate and up rows share the prepared tiles).
+ *   format: QGEMV_Q4_0, QGEMV_PQ2_0 or QGEMV_CBK4_ROW (the gate and up rows
+ *     share the prepared tiles, so formats with one codebook per matrix are
+ *     refused; per-row codebooks travel with their rows).
  *   N: rows of each projection (the output width), a positive multiple of
  *     64; K as for qgemv_create.
  *   packed_gate, packed_up: each projection's canonical bytes (host or
  *     device), copied.  The handle holds them interleaved in 64-row blocks.
+ *   codebooks_gate, codebooks_up: CBK4_ROW's fp32 [N][16] codebooks of each
+ *     projection; NULL for the other formats.
  * Runs: qgemv_run with y fp32 [M][N]; the residual form is refused, and so
  * are qgemv_set_x_int8 and qgemv_run_xq.  qgemv_dequant of such a handle
  * writes the 2N interleaved rows (64 gate rows, then the 64 up rows of the
@@ -153,7 +156,7 @@ qgemv_handle qgemv_create_stacked(int format, int nseg, const int64_t* seg_rows,
  * (expf, an IEEE division, one product) of the two GEMV sums.
  * Returns NULL on error (QGEMV_ERR_ARG for another format or a bad N).     */
 qgemv_handle qgemv_create_glu(int format, int64_t N, int64_t K, const void* packed_gate,
-                              const void* packed_up);
+                              const void* packed_up, const void* codebooks_gate, const void* codebooks_up);
 
 /* y = x . dequant(W)^T for M rows.
  *   x: device fp16 [M][K] row-major, 4-byte aligned.

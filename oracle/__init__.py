@@ -347,12 +347,14 @@ def silu(v):
     return v / (1.0 + np.exp(-v))
 
 
-def gemv_glu(fmt, N: int, K: int, packed_gate, packed_up, x, nthreads: int | None = None):
+def gemv_glu(fmt, N: int, K: int, packed_gate, packed_up, x, nthreads: int | None = None,
+             codebooks_gate=None, codebooks_up=None):
     """The fused gate/up projection of a decoder MLP: y = SiLU(x . G^T) * (x . U^T)
-    for two matrices of the same format and shape [N, K] (formats without
-    scales or codebooks).  Returns (y, g, u, bound_g, bound_u), fp64 [M, N]."""
-    g, bg = gemv(fmt, N, K, packed_gate, None, None, x, nthreads=nthreads)
-    u, bu = gemv(fmt, N, K, packed_up, None, None, x, nthreads=nthreads)
+    for two matrices of the same format and shape [N, K] (no scales; each
+    its own codebooks where the format has them).  Returns
+    (y, g, u, bound_g, bound_u), fp64 [M, N]."""
+    g, bg = gemv(fmt, N, K, packed_gate, None, codebooks_gate, x, nthreads=nthreads)
+    u, bu = gemv(fmt, N, K, packed_up, None, codebooks_up, x, nthreads=nthreads)
     return silu(g) * u, g, u, bg, bu
 
 

@@ -38,18 +38,26 @@ def _pair(fmt, N, K, tag):
     return (make_case(fmt, N, K, tag=f"{tag}/gate")[0], make_case(fmt, N, K, tag=f"{tag}/up")[0])
 
 
-@pytest.mark.parametrize("fmt", ["q4_0", "pq2_0"])
+def _codebooks(fmt, N, K, tag):
+    if fmt != "cbk4_row":
+        return None, None
+    return make_case(fmt, N, K, tag=f"{tag}/gate")[2], make_case(fmt, N, K, tag=f"{tag}/up")[2]
+
+
+@pytest.mark.parametrize("fmt", ["q4_0", "pq2_0", "cbk4_row"])
 @pytest.mark.parametrize("N,K", [(192, 1024), (704, 2048), (4096, 4096)])
 @pytest.mark.parametrize("M", [1, 3])
 def test_glu_matches_oracle(fmt, N, K, M):
-    pg, pu = _pair(fmt, N, K, f"glu/{fmt}/{N}x{K}")
-    h = qgemv.QGemv.glu(fmt, N, K, pg, pu)
+    tag = f"glu/{fmt}/{N}x{K}"
+    pg, pu = _pair(fmt, N, K, tag)
+    cg, cu = _codebooks(fmt, N, K, tag)
+    h = qgemv.QGemv.glu(fmt, N, K, pg, pu, cg, cu)
     x_np = make_x(M, K, tag="glu")
     y = h.gemv(torch.from_numpy(x_np).cuda())
     torch.cuda.synchronize()
     assert h.status() == qgemv.QGEMV_OK
     assert y.shape == (M, N)
-    y_ref, g, u, bg, bu = oracle.gemv_glu(fmt, N, K, pg, pu, x_np)
+    y_ref, g, u, bg, bu = oracle.gemv_glu(fmt, N, K, pg, pu, x_np, codebooks_gate=cg, codebooks_up=cu)
     ok = oracle.within_tolerance_glu(y.cpu().numpy(), g, u, bg, bu)
     assert ok.all(), f"{fmt} {N}x{K} M={M}: {np.count_nonzero(~ok)} outputs out of tolerance"
 
