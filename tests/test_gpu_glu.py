@@ -4,7 +4,8 @@ oracle's ``gemv_glu`` with the bound of ``within_tolerance_glu`` (each GEMV
 sum within its own 1e-3 * sum |x w| + 1e-6, propagated through SiLU and the
 product, plus a few fp32 roundings).
 
-Covered: Q4_0 and PQ2_0; shapes whose row tiles are split between CTAs
+Covered: Q4_0, PQ2_0 and CBK4_ROW (per-row codebooks interleaved with their
+rows); shapes whose row tiles are split between CTAs
 (the pair finisher) and owned whole (the epilogue); the 7B MLP's gate/up
 11008 x 4096 and the 5120/17408 model's 17408 x 5120 at full size on
 sampled outputs; M = 1 and 3; the dequant of the interleaved rows; and the
