@@ -51,6 +51,10 @@ CASES = [
     (1000, 999, 10, 128),           # almost one tile per CTA
     (35 * 4, 140, 4, 2048),         # AQLM units of 2048 rows
     (17, 17, 17, 128),              # one row tile, one tile per CTA
+    # GLU handles: the finisher's row slices count gate/up pairs (64 per tile)
+    (172 * 8, 304, 8, 64),          # 7B gate|up interleaved (11008 pairs), Q4_0, two CTAs per SM
+    (32, 32, 32, 64),               # one row tile split over 32 CTAs (the lost-CTA test's shape)
+    (272 * 5, 304, 5, 64),          # 17408 pairs x 5120, PQ2_0
 ]
 
 
