@@ -489,20 +489,20 @@ def run_ours(args, rank, world, device):
                    "parallelism": f"replicas{world}", "peak_hbm_gbs": peak,
                    "frac_of_peak": round(value / world / peak, 4)},
         "roofline": {"bound": "hbm",
-                     "kernel": ("gemv_kernel<FmtPQ2I8, MB>, MB = 4, 2, 1 activation rows per launch" if args.x_int8
-                                else "gemv_1x16_kernel (codebook entries gathered from L2: a 32-byte sector "
+                     "kernel": ("wstream_kernel<FmtPQ2I8, MB>, MB = 4, 2, 1 activation rows per launch" if args.x_int8
+                                else "aqlm1x16_kernel (codebook entries gathered from L2: a 32-byte sector "
                                      "per group of 8 weights bounds it before HBM does)" if dominant == "aqlm_1x16"
-                                else "gemv_kernel<FmtCBK4R, MB>, MB = 2, 1 activation rows per launch"
+                                else "wstream_kernel<FmtCBK4R, MB>, MB = 2, 1 activation rows per launch"
                                 if dominant == "cbk4_row"
-                                else "gemv_rowcb8_kernel<MB> (one warp per row, its codebook in shared memory)"
+                                else "rowcb8_kernel<MB> (one warp per row, its codebook in shared memory)"
                                 if dominant == "cbk8_row"
-                                else "gemv_kernel<FmtPQ2, 1, GLU> (gate and up interleaved, SiLU(gate)*up stored)"
+                                else "wstream_kernel<FmtPQ2, 1, GLU> (gate and up interleaved, SiLU(gate)*up stored)"
                                 if dominant == "pq2_0_glu"
-                                else f"aqlm_gemv_kernel<MB={M}>" if dominant == "aqlm_2x8" and M <= 2
-                                else (f"gemv_kernel<{dominant}, M=1>"
-                                      + (" and gemv_rowgroup_kernel (matrices of at most one 32-row group per SM)"
+                                else f"aqlm_table_kernel<MB={M}>" if dominant == "aqlm_2x8" and M <= 2
+                                else (f"wstream_kernel<{dominant}, M=1>"
+                                      + (" and rowgroup_stream_kernel (matrices of at most one 32-row group per SM)"
                                          if dominant in ("cbk4", "cbk8") else "")) if M == 1
-                                else f"gemv_mma_kernel<{dominant}, NB={1 if M <= 8 else 2}>"),
+                                else f"wstream_mma_kernel<{dominant}, NB={1 if M <= 8 else 2}>"),
                      "achieved": round(dom_achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(dom_achieved / peak, 4), "peak_kind": peak_kind,
                      "traffic": traffic,

@@ -141,7 +141,7 @@ __device__ __forceinline__ void lookup_row(const uint4 (&cr)[2], const uint32_t 
 }
 
 template <int MB>
-__global__ void __launch_bounds__(kThreads, 1) aqlm_gemv_kernel(const GemvParams p) {
+__global__ void __launch_bounds__(kThreads, 1) aqlm_table_kernel(const RunParams p) {
   if (static_cast<int>(blockIdx.x) == p.skip_cta) return;  // test hook (QGEMV_FAULT_SKIP_CTA)
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ float s_sub[2 * kThreads];
@@ -430,16 +430,16 @@ cudaError_t dequant(const uint8_t* tiles, const void* aux, const int32_t*, int64
 int smem_bytes(int M) { return smem_bytes_mb(M >= 2 ? 2 : 1); }
 
 cudaError_t setup() {
-  cudaError_t e = cudaFuncSetAttribute(aqlm_gemv_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(aqlm_table_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        smem_bytes_mb(1));
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(aqlm_gemv_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(aqlm_table_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem_bytes_mb(2));
   return e;
 }
 
 template <int MB>
-cudaError_t launch_pass(const GemvParams& p, int grid, cudaStream_t s) {
+cudaError_t launch_pass(const RunParams& p, int grid, cudaStream_t s) {
   static_assert(smem_bytes_mb(MB) <= 227 * 1024, "shared memory budget exceeded");
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -451,17 +451,17 @@ cudaError_t launch_pass(const GemvParams& p, int grid, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, aqlm_gemv_kernel<MB>, p);
+  return cudaLaunchKernelEx(&cfg, aqlm_table_kernel<MB>, p);
 }
 
 // Passes of two activation rows, and one for an odd last row.  The two pass
 // kinds round differently, so in batch-invariant mode every row gets a
 // one-row pass of its own.
-cudaError_t launch(int M, const GemvParams& p, const LaunchGeom& g, cudaStream_t s, bool batch_invariant) {
+cudaError_t launch(int M, const RunParams& p, const LaunchGeom& g, cudaStream_t s, bool batch_invariant) {
   cudaError_t e = cudaSuccess;
   const int grid = g.grid;
   for (int m0 = 0; m0 < M && e == cudaSuccess;) {
-    GemvParams q = p;
+    RunParams q = p;
     q.plan = g.plan;
     q.x = p.x + int64_t(m0) * p.K;
     q.y = p.y + int64_t(m0) * p.N;

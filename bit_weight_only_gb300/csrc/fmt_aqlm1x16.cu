@@ -52,7 +52,7 @@ __device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
 }
 
 template <int MB>
-__global__ void __launch_bounds__(kThreads) gemv_1x16_kernel(const GemvParams p, int M) {
+__global__ void __launch_bounds__(kThreads) aqlm1x16_kernel(const RunParams p, int M) {
   const uint4* cb = static_cast<const uint4*>(p.aux);
   const unsigned short* scales =
       reinterpret_cast<const unsigned short*>(static_cast<const uint8_t*>(p.aux) + kCodebookBytes);
@@ -170,7 +170,7 @@ int smem_bytes(int) { return 0; }
 cudaError_t setup() { return cudaSuccess; }
 
 template <int MB>
-cudaError_t launch_mb(const GemvParams& p, int M, cudaStream_t s) {
+cudaError_t launch_mb(const RunParams& p, int M, cudaStream_t s) {
   const int64_t blocks = (p.N + kWarps - 1) / kWarps;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(blocks < 65535 ? blocks : 65535));
@@ -182,13 +182,13 @@ cudaError_t launch_mb(const GemvParams& p, int M, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemv_1x16_kernel<MB>, p, M);
+  return cudaLaunchKernelEx(&cfg, aqlm1x16_kernel<MB>, p, M);
 }
 
 // One launch for all M rows (each code and entry read once per call); the
 // instantiation only sizes the accumulators, so every M gives every row the
 // same bits (batch invariant in either mode).
-cudaError_t launch(int M, const GemvParams& p, const LaunchGeom&, cudaStream_t s, bool) {
+cudaError_t launch(int M, const RunParams& p, const LaunchGeom&, cudaStream_t s, bool) {
   if (M < 1 || M > kMaxM) return cudaErrorInvalidValue;
   if (M == 1) return launch_mb<1>(p, M, s);
   if (M == 2) return launch_mb<2>(p, M, s);

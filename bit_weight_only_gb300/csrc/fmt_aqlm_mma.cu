@@ -5,7 +5,7 @@
 // quantization):  w[n][8g + j] = s_n * (C0[c0(n, g)][j] + C1[c1(n, g)][j]).
 // The per-group table path costs one table read per code byte and
 // activation row, so its time grows with M.  Here the codebook vectors are
-// the A operands of mma.m16n8k16 instead (gemv_mma_kernel, mma_kernel.cuh):
+// the A operands of mma.m16n8k16 instead (wstream_mma_kernel, mma_kernel.cuh):
 //
 //     y[m][n] = s_n * sum_g ( <C0[c0(n, g)], x[m]_g> + <C1[c1(n, g)], x[m]_g> )
 //
@@ -51,7 +51,7 @@ struct FmtAQLM {
   static constexpr int kMmaRowWords = 4;  // the 16 code bytes of the thread's half of the row
   static constexpr int kMmaCodebooks = 2;
   static constexpr bool kMmaRowScales = true;
-  __device__ static const __half* mma_row_scales(const GemvParams& p) {
+  __device__ static const __half* mma_row_scales(const RunParams& p) {
     return reinterpret_cast<const __half*>(static_cast<const uint8_t*>(p.aux) + kCodebookBytes);
   }
   static constexpr int kMmaBlockSteps = 0;
@@ -195,9 +195,9 @@ cudaError_t dequant(const uint8_t* tiles, const void* aux, const int32_t*, int64
 }
 
 template <int NB, bool PAR = false>
-cudaError_t launch_nb(const GemvParams& p, int M, const LaunchGeom& g, cudaStream_t s) {
+cudaError_t launch_nb(const RunParams& p, int M, const LaunchGeom& g, cudaStream_t s) {
   static_assert(mma_smem_bytes<F, NB, PAR>() + 2048 <= 228 * 1024, "shared memory budget exceeded");
-  GemvParams q = p;
+  RunParams q = p;
   q.plan = g.plan;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(g.grid);
@@ -209,14 +209,14 @@ cudaError_t launch_nb(const GemvParams& p, int M, const LaunchGeom& g, cudaStrea
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemv_mma_kernel<F, NB, PAR>, q, M);
+  return cudaLaunchKernelEx(&cfg, wstream_mma_kernel<F, NB, PAR>, q, M);
 }
 
 // Batch-invariant mode: every M runs the default geometry, the same
 // instruction sequence per activation row (one B column each), so a row's
 // bits do not depend on M.  Otherwise one activation block runs the
 // tile-parity geometry.
-cudaError_t launch(int M, const GemvParams& p, const LaunchGeom& g, cudaStream_t s, bool batch_invariant) {
+cudaError_t launch(int M, const RunParams& p, const LaunchGeom& g, cudaStream_t s, bool batch_invariant) {
   if (M >= 1 && M <= 8) return batch_invariant ? launch_nb<1>(p, M, g, s) : launch_nb<1, true>(p, M, g, s);
   if (M > 8 && M <= kMaxM) return launch_nb<2>(p, M, g, s);
   return cudaErrorInvalidValue;
@@ -225,13 +225,13 @@ cudaError_t launch(int M, const GemvParams& p, const LaunchGeom& g, cudaStream_t
 int smem_bytes(int M) { return M <= 8 ? mma_smem_bytes<F, 1, true>() : mma_smem_bytes<F, 2>(); }
 
 cudaError_t setup() {
-  cudaError_t e = cudaFuncSetAttribute(gemv_mma_kernel<F, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(wstream_mma_kernel<F, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        mma_smem_bytes<F, 1>());
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(gemv_mma_kernel<F, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(wstream_mma_kernel<F, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              mma_smem_bytes<F, 2>());
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(gemv_mma_kernel<F, 1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(wstream_mma_kernel<F, 1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              mma_smem_bytes<F, 1, true>());
   return e;
 }

@@ -89,7 +89,7 @@ struct FmtCBK4 {
   static constexpr int kMmaRowWords = 2;   // words q of the two 16-byte halves
   static constexpr int kMmaCodebooks = 1;
   static constexpr bool kMmaRowScales = false;
-  __device__ static const __half* mma_row_scales(const GemvParams&) { return nullptr; }
+  __device__ static const __half* mma_row_scales(const RunParams&) { return nullptr; }
   static constexpr int kMmaBlockSteps = 0;
   struct MmaScales {};  // no block scale
   static constexpr int kMmaXWords = 8;  // x[m][32h + 8q .. +7], h = 0, 1
@@ -122,7 +122,7 @@ struct FmtCBK4 {
   }
 
   template <int M>
-  __device__ static void load_x(XRegs& xr, const GemvParams& p, int kt, int slice, int lane) {
+  __device__ static void load_x(XRegs& xr, const RunParams& p, int kt, int slice, int lane) {
     load_x_slice<kKW, M, 2>(xr, p, kt, slice, lane);
   }
 
@@ -257,7 +257,7 @@ struct FmtCBK8 {
   static constexpr int kMmaRowWords = 2;   // words q of the two 16-byte halves
   static constexpr int kMmaCodebooks = 1;
   static constexpr bool kMmaRowScales = false;
-  __device__ static const __half* mma_row_scales(const GemvParams&) { return nullptr; }
+  __device__ static const __half* mma_row_scales(const RunParams&) { return nullptr; }
   static constexpr int kMmaBlockSteps = 0;
   struct MmaScales {};  // no block scale
   static constexpr int kMmaXWords = 4;  // x[m][16h + 4q .. +3], h = 0, 1
@@ -300,7 +300,7 @@ struct FmtCBK8 {
   }
 
   template <int M>
-  __device__ static void load_x(XRegs& xr, const GemvParams& p, int kt, int slice, int lane) {
+  __device__ static void load_x(XRegs& xr, const RunParams& p, int kt, int slice, int lane) {
     load_x_slice<kKW, M, 1>(xr, p, kt, slice, lane);
   }
 
@@ -371,7 +371,7 @@ struct FmtCBK8 {
 // live in shared memory as T[j][c][l] = centroid c of row 4l + j (byte
 // j*2048 + c*128 + l*4 of the 64 KB-aligned table region), so lane l's
 // lookups always hit bank l whatever the indices.  A row tile's table is
-// built when the CTA starts it (the stacked-handle machinery of gemv_kernel,
+// built when the CTA starts it (the stacked-handle machinery of wstream_kernel,
 // with one segment per row tile).  The entry is fp32, so each weight is one
 // lookup (the address: the index nibble shifted to bits 7..10 OR the lane's
 // row base) and the products with fp32 activation pairs accumulate with
@@ -403,7 +403,7 @@ struct FmtCBK4R {
   }
 
   template <int M>
-  __device__ static void load_x(XRegs& xr, const GemvParams& p, int kt, int slice, int lane) {
+  __device__ static void load_x(XRegs& xr, const RunParams& p, int kt, int slice, int lane) {
     load_x_slice<kKW, M, 2>(xr, p, kt, slice, lane);
   }
 

@@ -63,7 +63,7 @@ cudaError_t dequant(const uint8_t* tiles, const void* aux, const int32_t*, int64
 template <int MB>
 cudaError_t set_smem() {
   static_assert(gemv_smem_bytes<F, MB>() + 2048 <= 228 * 1024, "shared memory budget exceeded");
-  return cudaFuncSetAttribute(gemv_kernel<F, MB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(wstream_kernel<F, MB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               gemv_smem_bytes<F, MB>());
 }
 
@@ -77,8 +77,8 @@ cudaError_t setup() {
 int smem_bytes(int M) { return M == 1 ? gemv_smem_bytes<F, 1>() : gemv_smem_bytes<F, 2>(); }
 
 template <int MB>
-cudaError_t launch_rows(const GemvParams& p, int m0, const LaunchGeom& g, cudaStream_t s) {
-  GemvParams q = p;
+cudaError_t launch_rows(const RunParams& p, int m0, const LaunchGeom& g, cudaStream_t s) {
+  RunParams q = p;
   q.x = p.x + m0 * p.K;
   q.y = p.y + m0 * p.N;
   q.residual = p.residual != nullptr ? p.residual + m0 * p.N : nullptr;
@@ -86,11 +86,11 @@ cudaError_t launch_rows(const GemvParams& p, int m0, const LaunchGeom& g, cudaSt
   cudaLaunchAttribute attr[1];
   const cudaLaunchConfig_t cfg =
       LaunchTable<F>::config(g.grid_m1, gemv_threads<F, MB>(), gemv_smem_bytes<F, MB>(), s, attr);
-  return cudaLaunchKernelEx(&cfg, gemv_kernel<F, MB>, q);
+  return cudaLaunchKernelEx(&cfg, wstream_kernel<F, MB>, q);
 }
 
 // Two activation rows per launch, one for an odd last row.
-cudaError_t launch(int M, const GemvParams& p, const LaunchGeom& g, cudaStream_t s, bool) {
+cudaError_t launch(int M, const RunParams& p, const LaunchGeom& g, cudaStream_t s, bool) {
   if (M < 1 || M > kMaxM) return cudaErrorInvalidValue;
   for (int m0 = 0; m0 < M;) {
     const int mb = M - m0 >= 2 ? 2 : 1;

@@ -49,7 +49,7 @@ __device__ __forceinline__ float lds_f32(uint32_t addr) {
 }
 
 template <int MB>
-__global__ void __launch_bounds__(kThreads) gemv_rowcb8_kernel(const GemvParams p, int M) {
+__global__ void __launch_bounds__(kThreads) rowcb8_kernel(const RunParams p, int M) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
@@ -172,7 +172,7 @@ cudaError_t dequant(const uint8_t* tiles, const void* aux, const int32_t*, int64
 
 template <int MB>
 cudaError_t set_smem() {
-  return cudaFuncSetAttribute(gemv_rowcb8_kernel<MB>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+  return cudaFuncSetAttribute(rowcb8_kernel<MB>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
 }
 
 cudaError_t setup() {
@@ -187,8 +187,8 @@ cudaError_t setup() {
 int smem_bytes(int) { return kSmemLimit; }
 
 template <int MB>
-cudaError_t launch_mb(const GemvParams& p, int m0, int mrows, int sms, cudaStream_t s) {
-  GemvParams q = p;
+cudaError_t launch_mb(const RunParams& p, int m0, int mrows, int sms, cudaStream_t s) {
+  RunParams q = p;
   q.x = p.x + m0 * p.K;
   q.y = p.y + m0 * p.N;
   q.residual = p.residual != nullptr ? p.residual + m0 * p.N : nullptr;
@@ -207,13 +207,13 @@ cudaError_t launch_mb(const GemvParams& p, int m0, int mrows, int sms, cudaStrea
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemv_rowcb8_kernel<MB>, q, mrows);
+  return cudaLaunchKernelEx(&cfg, rowcb8_kernel<MB>, q, mrows);
 }
 
 // Row blocks: the smallest instantiation (1, 2, 4, 8, 16 rows) that holds
 // the remaining rows, halved while its staged activations do not fit;
 // launch after launch.  A row's arithmetic is the same in every block size.
-cudaError_t launch(int M, const GemvParams& p, const LaunchGeom& g, cudaStream_t s, bool) {
+cudaError_t launch(int M, const RunParams& p, const LaunchGeom& g, cudaStream_t s, bool) {
   if (M < 1 || M > kMaxM) return cudaErrorInvalidValue;
   const int sms = g.grid;  // min(tiles, SMs): the SM count for any matrix of at least that many rows
   for (int m0 = 0; m0 < M;) {

@@ -81,7 +81,7 @@ struct FmtQ4_0 {
   static constexpr int kMmaRowWords = 2;   // words q of the two 16-byte halves
   static constexpr int kMmaCodebooks = 1;
   static constexpr bool kMmaRowScales = false;
-  __device__ static const __half* mma_row_scales(const GemvParams&) { return nullptr; }
+  __device__ static const __half* mma_row_scales(const RunParams&) { return nullptr; }
   static constexpr int kMmaBlockSteps = 2;
   static constexpr int kMmaXWords = 8;  // x[m][32b + 8q .. +7], b = 0, 1
   // two slices per warp, eight warps per CTA, two CTAs per SM, two stages each
@@ -128,7 +128,7 @@ struct FmtQ4_0 {
   __device__ static void init_shared(uint8_t*, const uint16_t*, int, int) {}
 
   template <int M>
-  __device__ static void load_x(XRegs& xr, const GemvParams& p, int kt, int slice, int lane) {
+  __device__ static void load_x(XRegs& xr, const RunParams& p, int kt, int slice, int lane) {
     load_x_slice<kKW, M, 2>(xr, p, kt, slice, lane);
   }
 
@@ -255,7 +255,7 @@ struct FmtPQ2 {
   static constexpr int kMmaRowWords = 2;   // words q of the two 16-byte halves
   static constexpr int kMmaCodebooks = 1;
   static constexpr bool kMmaRowScales = false;
-  __device__ static const __half* mma_row_scales(const GemvParams&) { return nullptr; }
+  __device__ static const __half* mma_row_scales(const RunParams&) { return nullptr; }
   static constexpr int kMmaBlockSteps = 8;
   static constexpr int kMmaXWords = 16;  // x[m][64h + 16q .. +15], h = 0, 1
   // One slice per warp, sixteen warps, one CTA per SM for every M: two
@@ -308,7 +308,7 @@ struct FmtPQ2 {
   __device__ static void init_shared(uint8_t*, const uint16_t*, int, int) {}
 
   template <int M>
-  __device__ static void load_x(XRegs& xr, const GemvParams& p, int kt, int slice, int lane) {
+  __device__ static void load_x(XRegs& xr, const RunParams& p, int kt, int slice, int lane) {
     load_x_slice<kKW, M, 4>(xr, p, kt, slice, lane);
   }
 
@@ -463,7 +463,7 @@ struct FmtPQ2I8 {
   __device__ static void x_scales(XScale&, int) {}
 
   template <int M>
-  __device__ static void load_x(XRegs& xr, const GemvParams& p, int kt, int slice, int lane) {
+  __device__ static void load_x(XRegs& xr, const RunParams& p, int kt, int slice, int lane) {
     const int64_t kbase = static_cast<int64_t>(kt) * kKT + slice * kKW;
     const unsigned short* xb = reinterpret_cast<const unsigned short*>(p.x);
 #pragma unroll
@@ -568,7 +568,7 @@ struct FmtPQ2I8P : FmtPQ2I8 {
   };
 
   template <int M>
-  __device__ static void load_x(XRegs& xr, const GemvParams& p, int kt, int slice, int lane) {
+  __device__ static void load_x(XRegs& xr, const RunParams& p, int kt, int slice, int lane) {
     const int64_t G = p.K / 128;
     const int64_t g = static_cast<int64_t>(kt) * kSlices + slice;  // the slice's group
     const uint32_t* xw = reinterpret_cast<const uint32_t*>(p.x);

@@ -131,14 +131,14 @@ template <int MB>
 cudaError_t set_i8_smem() {
   static_assert(FmtPQ2I8::kCtasPerSm * (gemv_smem_bytes<FmtPQ2I8, MB>() + 2048) <= 228 * 1024,
                 "shared memory budget exceeded");
-  return cudaFuncSetAttribute(gemv_kernel<FmtPQ2I8, MB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(wstream_kernel<FmtPQ2I8, MB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               gemv_smem_bytes<FmtPQ2I8, MB>());
 }
 
 template <class FI, int MB>
 cudaError_t set_i8_smem_of() {
   static_assert(FI::kCtasPerSm * (gemv_smem_bytes<FI, MB>() + 2048) <= 228 * 1024, "shared memory budget exceeded");
-  return cudaFuncSetAttribute(gemv_kernel<FI, MB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(wstream_kernel<FI, MB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               gemv_smem_bytes<FI, MB>());
 }
 
@@ -157,8 +157,8 @@ cudaError_t setup() {
 // Activation rows [m0, m0 + MB) of the call in one launch of the CUDA-core
 // kernel (the M = 1 grid and stream-K plan).
 template <int MB>
-cudaError_t launch_i8_rows(const GemvParams& p, int m0, const LaunchGeom& g, cudaStream_t s) {
-  GemvParams q = p;
+cudaError_t launch_i8_rows(const RunParams& p, int m0, const LaunchGeom& g, cudaStream_t s) {
+  RunParams q = p;
   q.x = p.x + m0 * p.K;
   q.y = p.y + m0 * p.N;
   q.residual = p.residual != nullptr ? p.residual + m0 * p.N : nullptr;
@@ -166,7 +166,7 @@ cudaError_t launch_i8_rows(const GemvParams& p, int m0, const LaunchGeom& g, cud
   cudaLaunchAttribute attr[1];
   const cudaLaunchConfig_t cfg =
       I8::config(g.grid_m1, gemv_threads<FmtPQ2I8, MB>(), gemv_smem_bytes<FmtPQ2I8, MB>(), s, attr);
-  return cudaLaunchKernelEx(&cfg, gemv_kernel<FmtPQ2I8, MB>, q);
+  return cudaLaunchKernelEx(&cfg, wstream_kernel<FmtPQ2I8, MB>, q);
 }
 
 // Up to four activation rows per launch (the weights are read once per
@@ -174,7 +174,7 @@ cudaError_t launch_i8_rows(const GemvParams& p, int m0, const LaunchGeom& g, cud
 // instructions and summation order in every instantiation, so a row's bits
 // do not depend on M or on its place in the batch.  Consecutive launches on
 // the stream are ordered by the kernel's grid-dependency wait.
-cudaError_t launch_x_int8(int M, const GemvParams& p, const LaunchGeom& g, cudaStream_t s) {
+cudaError_t launch_x_int8(int M, const RunParams& p, const LaunchGeom& g, cudaStream_t s) {
   if (M < 1 || M > kMaxM) return cudaErrorInvalidValue;
   int m0 = 0;
   while (m0 < M) {
@@ -193,9 +193,9 @@ cudaError_t launch_x_int8(int M, const GemvParams& p, const LaunchGeom& g, cudaS
 
 // Rows [m0, m0 + MB) of a call on prepared activations in one launch.
 template <int MB>
-cudaError_t launch_xq_rows(const GemvParams& p, int m0, const LaunchGeom& g, cudaStream_t s) {
+cudaError_t launch_xq_rows(const RunParams& p, int m0, const LaunchGeom& g, cudaStream_t s) {
   const int64_t G = p.K / 128;
-  GemvParams q = p;
+  RunParams q = p;
   q.x = reinterpret_cast<const __half*>(reinterpret_cast<const uint8_t*>(p.x) + m0 * p.K);
   q.x_scale = p.x_scale + m0 * G;
   q.x_qsum = p.x_qsum + m0 * G;
@@ -205,11 +205,11 @@ cudaError_t launch_xq_rows(const GemvParams& p, int m0, const LaunchGeom& g, cud
   cudaLaunchAttribute attr[1];
   const cudaLaunchConfig_t cfg =
       I8::config(g.grid_m1, gemv_threads<FmtPQ2I8P, MB>(), gemv_smem_bytes<FmtPQ2I8P, MB>(), s, attr);
-  return cudaLaunchKernelEx(&cfg, gemv_kernel<FmtPQ2I8P, MB>, q);
+  return cudaLaunchKernelEx(&cfg, wstream_kernel<FmtPQ2I8P, MB>, q);
 }
 
 // As launch_x_int8: four, two, then one activation rows per launch.
-cudaError_t launch_xq(int M, const GemvParams& p, const LaunchGeom& g, cudaStream_t s) {
+cudaError_t launch_xq(int M, const RunParams& p, const LaunchGeom& g, cudaStream_t s) {
   if (M < 1 || M > kMaxM) return cudaErrorInvalidValue;
   int m0 = 0;
   while (m0 < M) {

@@ -7,7 +7,7 @@
 
 namespace qgemv {
 
-struct GemvParams;
+struct RunParams;
 struct CtaPlan;  // gemv_kernel.cuh
 
 // Canonical inputs already on the device, plus the prepared-layout geometry.
@@ -44,7 +44,7 @@ struct FormatOps {
   cudaError_t (*setup)();  // one-time kernel attributes
   // batch_invariant: every row's result must not depend on M (see
   // qgemv_set_batch_invariant); the kernels are chosen accordingly.
-  cudaError_t (*launch)(int M, const GemvParams& p, const LaunchGeom& g, cudaStream_t s, bool batch_invariant);
+  cudaError_t (*launch)(int M, const RunParams& p, const LaunchGeom& g, cudaStream_t s, bool batch_invariant);
   cudaError_t (*prepare)(const PrepareArgs& a, cudaStream_t s);
   // w_out[n*K + k] = exact decoded weight, read back from the prepared tiles
   cudaError_t (*dequant)(const uint8_t* tiles, const void* aux, const int32_t* seg_of_rt, int64_t N,
@@ -56,14 +56,14 @@ struct FormatOps {
   int m1_ctas_per_sm = 1;           // CTAs per SM of the M = 1 kernel (LaunchGeom::grid_m1)
   int rowgroup = 0;                 // has the M = 1 row-group kernel (rowgroup_kernel.cuh)
   // PQ2_0 only: the run with INT8 activations (qgemv_set_x_int8), else nullptr
-  cudaError_t (*launch_x_int8)(int M, const GemvParams& p, const LaunchGeom& g, cudaStream_t s) = nullptr;
+  cudaError_t (*launch_x_int8)(int M, const RunParams& p, const LaunchGeom& g, cudaStream_t s) = nullptr;
   // one codebook table per row tile, built from per-row codebooks (CBK4_ROW):
   // aux holds cb_entries fp16-sized units per row tile and seg_of_rt[rt] = rt
   int row_tables = 0;
   // PQ2_0 only: the run on prepared INT8 activations (qgemv_run_xq), else nullptr
-  cudaError_t (*launch_xq)(int M, const GemvParams& p, const LaunchGeom& g, cudaStream_t s) = nullptr;
+  cudaError_t (*launch_xq)(int M, const RunParams& p, const LaunchGeom& g, cudaStream_t s) = nullptr;
   // Q4_0, PQ2_0: the fused SiLU(gate) * up run of a GLU handle (qgemv_create_glu), else nullptr
-  cudaError_t (*launch_glu)(int M, const GemvParams& p, const LaunchGeom& g, cudaStream_t s) = nullptr;
+  cudaError_t (*launch_glu)(int M, const RunParams& p, const LaunchGeom& g, cudaStream_t s) = nullptr;
 };
 
 const FormatOps* ops_q4_0();

@@ -66,7 +66,7 @@ struct CtaPlan {
 };
 static_assert(sizeof(CtaPlan) == 64, "CtaPlan is copied in 16-byte pieces");
 
-struct GemvParams {
+struct RunParams {
   const uint8_t* tiles;  // prepared tiles (device)
   const __half* x;       // [M][K] fp16
   float* y;              // [M][N] fp32
@@ -89,7 +89,7 @@ struct GemvParams {
 // y[idx] = v, plus the residual in one fp32 add (never fused with the
 // product that made v) when the call has one.  The residual element is read
 // and y written by the same thread, so residual may alias y.
-__device__ __forceinline__ void store_y(const GemvParams& p, int64_t idx, float v) {
+__device__ __forceinline__ void store_y(const RunParams& p, int64_t idx, float v) {
   p.y[idx] = p.residual != nullptr ? __fadd_rn(v, p.residual[idx]) : v;
 }
 
@@ -165,7 +165,7 @@ struct RowAcc<M, RPW, true> {
   __device__ __forceinline__ void flush(float*, int, int, int) {}
 };
 
-// Dynamic shared memory of gemv_kernel<F, M>.
+// Dynamic shared memory of wstream_kernel<F, M>.
 // Tile parity (formats with F::kTileParity, which cannot run two CTAs per
 // SM): the two warps of a slice take alternate tiles, each for all four rows
 // of its lanes, instead of splitting the rows; the two halves of the CTA then
@@ -216,7 +216,7 @@ __host__ __device__ constexpr int gemv_threads() { return 32 * kSlices * wps_for
 // only on the launch geometry, so results are bitwise reproducible.
 // y = sum * out_scale, times the fp16 row scale when row_scales is not null.
 template <int ROWS, int M, int NT>
-__device__ __forceinline__ void finish_rows(const GemvParams& p, int64_t stride, const CtaPlan& pl, int sg,
+__device__ __forceinline__ void finish_rows(const RunParams& p, int64_t stride, const CtaPlan& pl, int sg,
                                             const __half* row_scales, float out_scale, float* s_sub,
                                             int tid, int mrows = M) {
   const int64_t rt = pl.seg_rt[sg];
@@ -298,14 +298,14 @@ __device__ __forceinline__ void finish_rows(const GemvParams& p, int64_t stride,
 
 // Out-of-line copy for large M, whose main loop needs every register.
 template <int ROWS, int M, int NT>
-__device__ __noinline__ void finish_rows_call(const GemvParams& p, int64_t stride, const CtaPlan& pl, int sg,
+__device__ __noinline__ void finish_rows_call(const RunParams& p, int64_t stride, const CtaPlan& pl, int sg,
                                               const __half* row_scales, float out_scale, float* s_sub,
                                               int tid, int mrows) {
   finish_rows<ROWS, M, NT>(p, stride, pl, sg, row_scales, out_scale, s_sub, tid, mrows);
 }
 
 template <int ROWS, int M, int NT>
-__device__ __forceinline__ void finish_segment(const GemvParams& p, int64_t stride, const CtaPlan& pl, int sg,
+__device__ __forceinline__ void finish_segment(const RunParams& p, int64_t stride, const CtaPlan& pl, int sg,
                                                const __half* row_scales, float out_scale, float* s_sub,
                                                int tid, int mrows = M) {
   if constexpr (M > 8)
@@ -319,7 +319,7 @@ __device__ __forceinline__ void finish_segment(const GemvParams& p, int64_t stri
 // threads take each, so that the two waits for other CTAs' partials overlap
 // instead of adding up.
 template <int ROWS, int M, int NT>
-__device__ __forceinline__ void finish_all(const GemvParams& p, int64_t stride, const CtaPlan& pl,
+__device__ __forceinline__ void finish_all(const RunParams& p, int64_t stride, const CtaPlan& pl,
                                            const __half* row_scales, float out_scale, float* s_sub, int tid,
                                            int mrows = M) {
   const bool s0 = pl.seg_rt[0] >= 0, s1 = pl.seg_rt[1] >= 0;
@@ -334,7 +334,7 @@ __device__ __forceinline__ void finish_all(const GemvParams& p, int64_t stride, 
 
 // y[m][n] = SiLU(g) * u for a GLU handle (output width p.N / 2): SiLU(g) =
 // g / (1 + e^-g) in fp32 (expf, IEEE division), then one fp32 product.
-__device__ __forceinline__ void glu_store(const GemvParams& p, int m, int64_t n, float g, float u) {
+__device__ __forceinline__ void glu_store(const RunParams& p, int m, int64_t n, float g, float u) {
   const int64_t nout = p.N / 2;
   if (n < nout) p.y[m * nout + n] = __fmul_rn(g / (1.0f + expf(-g)), u);
 }
@@ -342,7 +342,7 @@ __device__ __forceinline__ void glu_store(const GemvParams& p, int m, int64_t n,
 // Read one partial slot with a bounded poll and mark it empty again.  After
 // a wait of this thread has given up (gave_up), later slots are not waited
 // for, so a run whose partials never come ends after one time limit.
-__device__ __forceinline__ float take_slot(const GemvParams& p, float* slot, bool& gave_up) {
+__device__ __forceinline__ float take_slot(const RunParams& p, float* slot, bool& gave_up) {
   unsigned long long t_start = 0;
   uint32_t bits;
   while ((bits = ld_relaxed_u32(slot)) == kEmptySlot) {
@@ -362,7 +362,7 @@ __device__ __forceinline__ float take_slot(const GemvParams& p, float* slot, boo
 // counts gate/up row pairs, 0..63): for each pair and activation row, the
 // gate and up sums over the S contributors in order, then SiLU(gate) * up.
 template <int M, int NT>
-__device__ __noinline__ void finish_rows_glu(const GemvParams& p, const CtaPlan& pl, int sg, float out_scale,
+__device__ __noinline__ void finish_rows_glu(const RunParams& p, const CtaPlan& pl, int sg, float out_scale,
                                              int tid) {
   const int64_t rt = pl.seg_rt[sg];
   const int64_t cf = pl.seg_cf[sg];
@@ -420,7 +420,7 @@ __device__ __forceinline__ void wait_plan() {
 // The codebook of row tile rt (table formats): aux holds one codebook, or
 // for a stacked handle one copy per row tile.
 template <class F>
-__device__ __forceinline__ const uint16_t* table_of(const GemvParams& p, int64_t rt) {
+__device__ __forceinline__ const uint16_t* table_of(const RunParams& p, int64_t rt) {
   return static_cast<const uint16_t*>(p.aux) + (p.seg_of_rt != nullptr ? rt * F::kCbEntries : 0);
 }
 
@@ -436,7 +436,7 @@ __device__ __noinline__ void rebuild_table(uint8_t* lut, const uint16_t* cb, int
 // 0..63, the up rows the same, rows 64..127), and y[m][64t + r] =
 // SiLU(gate) * up (glu_store, finish_rows_glu); p.N counts both halves.
 template <class F, int M, bool GLU = false>
-__global__ void __launch_bounds__(gemv_threads<F, M>(), F::kCtasPerSm) gemv_kernel(const GemvParams p) {
+__global__ void __launch_bounds__(gemv_threads<F, M>(), F::kCtasPerSm) wstream_kernel(const RunParams p) {
   constexpr int NS = F::stages(M);
   constexpr int TB = F::kTileBytes;
   constexpr int MP = mpad(M);
@@ -760,7 +760,7 @@ struct XRegsT {
 };
 
 template <int KW, int M, int LPL>
-__device__ __forceinline__ void load_x_slice(XRegsT<LPL>& xr, const GemvParams& p, int kt,
+__device__ __forceinline__ void load_x_slice(XRegsT<LPL>& xr, const RunParams& p, int kt,
                                              int slice, int lane) {
   const int64_t kbase = static_cast<int64_t>(kt) * (KW * kSlices) + slice * KW + lane * LPL;
   const unsigned short* xb = reinterpret_cast<const unsigned short*>(p.x);

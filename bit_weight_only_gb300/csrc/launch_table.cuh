@@ -40,12 +40,12 @@ struct LaunchTable {
 
   static constexpr int kM1CtasPerSm = F::kCtasPerSm;
 
-  static cudaError_t launch_m1(const GemvParams& p, int grid, cudaStream_t s) {
+  static cudaError_t launch_m1(const RunParams& p, int grid, cudaStream_t s) {
     // 227 KB per SM shared by the CTAs, less room for each one's reserved and static bytes
     static_assert(F::kCtasPerSm * (gemv_smem_bytes<F, 1>() + 2048) <= 228 * 1024, "shared memory budget exceeded");
     cudaLaunchAttribute attr[1];
     const cudaLaunchConfig_t cfg = config(grid, gemv_threads<F, 1>(), gemv_smem_bytes<F, 1>(), s, attr);
-    return cudaLaunchKernelEx(&cfg, gemv_kernel<F, 1>, p);
+    return cudaLaunchKernelEx(&cfg, wstream_kernel<F, 1>, p);
   }
 
   // The tensor-core kernel runs F::mma_ctas(NB) CTAs per SM: 1 (grid, plan)
@@ -53,48 +53,48 @@ struct LaunchTable {
   // geometry (F::mma_par), used for one activation block outside
   // batch-invariant mode.
   template <int NB, bool PAR = false>
-  static cudaError_t launch_mma(const GemvParams& p, int M, const LaunchGeom& g, cudaStream_t s) {
+  static cudaError_t launch_mma(const RunParams& p, int M, const LaunchGeom& g, cudaStream_t s) {
     static_assert(F::mma_ctas(NB) == 1 || F::mma_ctas(NB) == F::kCtasPerSm, "tensor-core grid");
     // batch invariance: both activation-block counts of the default geometry
     // are the same geometry
     static_assert(F::mma_ctas(1) == F::mma_ctas(2) && F::mma_spw(1) == F::mma_spw(2), "one geometry for all M");
     static_assert(F::mma_ctas(NB) * (mma_smem_bytes<F, NB, PAR>() + 2048) <= 228 * 1024,
                   "shared memory budget exceeded");
-    GemvParams q = p;
+    RunParams q = p;
     q.plan = F::mma_ctas(NB) == 1 ? g.plan : g.plan_m1;
     const int grid = F::mma_ctas(NB) == 1 ? g.grid : g.grid_m1;
     cudaLaunchAttribute attr[1];
     const cudaLaunchConfig_t cfg = config(grid, mma_threads<F, NB, PAR>(), mma_smem_bytes<F, NB, PAR>(), s, attr);
-    return cudaLaunchKernelEx(&cfg, gemv_mma_kernel<F, NB, PAR>, q, M);
+    return cudaLaunchKernelEx(&cfg, wstream_mma_kernel<F, NB, PAR>, q, M);
   }
 
   // M = 1, whole 32-row groups per CTA (table formats; the handle decides,
   // LaunchGeom::grid_rg).
-  static cudaError_t launch_rg(const GemvParams& p, int grid, cudaStream_t s) {
+  static cudaError_t launch_rg(const RunParams& p, int grid, cudaStream_t s) {
     static_assert(rg_smem_bytes<F>() + 2048 <= 228 * 1024, "shared memory budget exceeded");
     cudaLaunchAttribute attr[1];
     const cudaLaunchConfig_t cfg = config(grid, kRgThreads, rg_smem_bytes<F>(), s, attr);
-    return cudaLaunchKernelEx(&cfg, gemv_rowgroup_kernel<F>, p);
+    return cudaLaunchKernelEx(&cfg, rowgroup_stream_kernel<F>, p);
   }
 
-  // GLU handles (gate and up interleaved; gemv_kernel's GLU epilogue): the
+  // GLU handles (gate and up interleaved; wstream_kernel's GLU epilogue): the
   // M = 1 CUDA-core kernel once per activation row, on the M = 1 grid and
   // its plan (made with 64-row halves).
   static cudaError_t setup_glu() {
-    return cudaFuncSetAttribute(gemv_kernel<F, 1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    return cudaFuncSetAttribute(wstream_kernel<F, 1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 gemv_smem_bytes<F, 1>());
   }
-  static cudaError_t launch_glu(int M, const GemvParams& p, const LaunchGeom& g, cudaStream_t s) {
+  static cudaError_t launch_glu(int M, const RunParams& p, const LaunchGeom& g, cudaStream_t s) {
     if (M < 1 || M > kMaxM) return cudaErrorInvalidValue;
     for (int m = 0; m < M; ++m) {
-      GemvParams q = p;
+      RunParams q = p;
       q.x = p.x + m * p.K;
       q.y = p.y + m * (p.N / 2);
       q.residual = nullptr;
       q.plan = g.plan_m1;
       cudaLaunchAttribute attr[1];
       const cudaLaunchConfig_t cfg = config(g.grid_m1, gemv_threads<F, 1>(), gemv_smem_bytes<F, 1>(), s, attr);
-      const cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_kernel<F, 1, true>, q);
+      const cudaError_t e = cudaLaunchKernelEx(&cfg, wstream_kernel<F, 1, true>, q);
       if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
@@ -108,28 +108,28 @@ struct LaunchTable {
   }
 
   static cudaError_t setup() {
-    cudaError_t e = cudaFuncSetAttribute(gemv_kernel<F, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(wstream_kernel<F, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          gemv_smem_bytes<F, 1>());
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(gemv_mma_kernel<F, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, mma_smem_bytes<F, 1>());
+      e = cudaFuncSetAttribute(wstream_mma_kernel<F, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, mma_smem_bytes<F, 1>());
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(gemv_mma_kernel<F, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, mma_smem_bytes<F, 2>());
+      e = cudaFuncSetAttribute(wstream_mma_kernel<F, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, mma_smem_bytes<F, 2>());
     if constexpr (F::mma_par(1)) {
       if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(gemv_mma_kernel<F, 1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(wstream_mma_kernel<F, 1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  mma_smem_bytes<F, 1, true>());
     }
     if constexpr (F::kTileParity) {
       if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(gemv_rowgroup_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(rowgroup_stream_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  rg_smem_bytes<F>());
     }
     return e;
   }
 
-  static cudaError_t launch(int M, const GemvParams& p, const LaunchGeom& g, cudaStream_t s,
+  static cudaError_t launch(int M, const RunParams& p, const LaunchGeom& g, cudaStream_t s,
                             bool batch_invariant) {
-    GemvParams q = p;
+    RunParams q = p;
     if (M == 1 && !batch_invariant) {
       if constexpr (F::kTileParity) {
         if (g.grid_rg > 0) return launch_rg(q, g.grid_rg, s);

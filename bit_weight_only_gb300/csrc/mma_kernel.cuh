@@ -9,7 +9,7 @@
 // activation block is padded to 8 rows, not 16.
 //
 //   * Same prepared tiles, TMA ring, stream-K split, CTA plans and polled
-//     split-K fix-up as gemv_kernel.
+//     split-K fix-up as wstream_kernel.
 //   * Two warps per group of F::mma_spw(NB) k-slices: warp (group g, half h)
 //     covers slices g * spw .. of every tile, one after the other, for
 //     row groups j = 2h, 2h + 1 (rows 4l + j, l = 0..31), as four 16-row
@@ -204,7 +204,7 @@ __device__ __noinline__ void mma_rebuild_table(uint8_t* lut, const uint16_t* cb,
 }
 
 template <class F, int NB, bool PAR = false>
-__global__ void __launch_bounds__(mma_threads<F, NB, PAR>(), F::mma_ctas(NB)) gemv_mma_kernel(const GemvParams p, int M) {
+__global__ void __launch_bounds__(mma_threads<F, NB, PAR>(), F::mma_ctas(NB)) wstream_mma_kernel(const RunParams p, int M) {
   constexpr int NS = mma_stages_of<F, NB, PAR>();
   constexpr int TB = F::kTileBytes;
   constexpr int KS = F::kKW / 16;        // k16 steps per slice

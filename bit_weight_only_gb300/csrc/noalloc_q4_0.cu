@@ -119,7 +119,10 @@ q4_0_noalloc_kernel(const uint8_t* __restrict__ packed, int64_t N, int64_t K,
 }
 
 // Once per device, with that device current: the device address of the
-// scratch array and the kernel's shared-memory limit.
+// scratch array and the kernel's shared-memory limit.  Only a successful
+// set-up is remembered: after a failure (for instance a first call made
+// during a stream capture) the error is cleared from the thread's CUDA state
+// and the next call tries again.
 const DeviceSetup* setup_device(int dev) {
   std::lock_guard<std::mutex> lock(g_setup_mu);
   DeviceSetup& s = g_setup[dev];
@@ -128,7 +131,12 @@ const DeviceSetup* setup_device(int dev) {
     if (s.err == cudaSuccess)
       s.err = cudaFuncSetAttribute(q4_0_noalloc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    16 * kChunkK * static_cast<int>(sizeof(float)));
-    s.done = true;
+    if (s.err == cudaSuccess) {
+      s.done = true;
+    } else {
+      s.scratch = nullptr;
+      cudaGetLastError();
+    }
   }
   return &s;
 }
@@ -162,9 +170,10 @@ extern "C" int qgemv_run_q4_0_noalloc(const void* packed, int64_t N, int64_t K, 
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) return fail(QGEMV_ERR_CUDA, "no usable device");
   const DeviceSetup* s = setup_device(dev);
-  if (s->err != cudaSuccess) {
+  if (!s->done) {
     char buf[256];
-    snprintf(buf, sizeof(buf), "scratch set-up failed: %s", cudaGetErrorString(s->err));
+    snprintf(buf, sizeof(buf), "scratch set-up failed (retried on the next call): %s",
+             cudaGetErrorString(s->err));
     return fail(QGEMV_ERR_CUDA, buf);
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);

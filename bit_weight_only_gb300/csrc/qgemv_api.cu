@@ -568,8 +568,8 @@ static bool valid(qgemv_handle h) { return h && h->magic == kMagic; }
 }  // extern "C"
 
 // Kernel parameters of a run of handle h.
-static qgemv::GemvParams params_of(const qgemv_ctx* h, const void* x, float* y, const float* residual) {
-  qgemv::GemvParams p;
+static qgemv::RunParams params_of(const qgemv_ctx* h, const void* x, float* y, const float* residual) {
+  qgemv::RunParams p;
   p.tiles = h->tiles;
   p.x = static_cast<const __half*>(x);
   p.y = y;
@@ -605,7 +605,7 @@ static int run_impl(qgemv_handle h, const void* x, int M, float* y, const float*
   if (rc != QGEMV_OK) return rc;
   if (h->glu) {
     if (residual) return set_error(QGEMV_ERR_ARG, "a GLU handle takes no residual");
-    const qgemv::GemvParams p = params_of(h, x, y, nullptr);
+    const qgemv::RunParams p = params_of(h, x, y, nullptr);
     const qgemv::LaunchGeom g = {h->grid, h->plan, h->grid_m1, h->plan_m1, 0};
     const cudaError_t e = h->ops->launch_glu(M, p, g, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_error(e, "launching the GEMV kernel");
@@ -613,7 +613,7 @@ static int run_impl(qgemv_handle h, const void* x, int M, float* y, const float*
   }
   const bool inv = h->batch_invariant != 0;
   if (h->mma && (M >= kAqlmMmaMinM || inv)) h = h->mma;  // AQLM: the tensor-core layout
-  const qgemv::GemvParams p = params_of(h, x, y, residual);
+  const qgemv::RunParams p = params_of(h, x, y, residual);
   const qgemv::LaunchGeom g = {h->grid, h->plan, h->grid_m1, h->plan_m1, h->grid_rg};
   cudaError_t e = h->x_int8 ? h->ops->launch_x_int8(M, p, g, static_cast<cudaStream_t>(stream))
                             : h->ops->launch(M, p, g, static_cast<cudaStream_t>(stream), inv);
@@ -674,7 +674,7 @@ int qgemv_run_xq(qgemv_handle h, const void* xq, int M, float* y, const float* r
   if (h->ops->launch_xq == nullptr || h->glu)
     return set_error(QGEMV_ERR_ARG, "prepared INT8 activations need a PQ2_0 handle without GLU (format %d)",
                      h->format);
-  qgemv::GemvParams p = params_of(h, xq, y, residual);
+  qgemv::RunParams p = params_of(h, xq, y, residual);
   const uint8_t* base = static_cast<const uint8_t*>(xq);
   p.x_scale = reinterpret_cast<const float*>(base + int64_t(M) * h->K);
   p.x_qsum = reinterpret_cast<const int32_t*>(base + int64_t(M) * h->K + 4 * int64_t(M) * (h->K / 128));

@@ -11,14 +11,14 @@
 // takes units [c*U/G, (c+1)*U/G) whole (U = 4 * row tiles).
 //
 // A stage holds kRgSub consecutive k tiles of a unit (32 KB).  As in
-// gemv_kernel's tile parity, the sixteen warps form two halves that take
+// wstream_kernel's tile parity, the sixteen warps form two halves that take
 // alternate stages, one warp per slice, each half with its own pipeline over
 // two of the four stages; a lane computes its one row of the unit for its
 // slice (the format's tile_math with one row per lane), and at the end of a
 // unit the sixteen slices' sums of each row are added in a fixed order and
 // stored to y.  A warp stages the activations of a whole stage at once and
 // fetches those of its next stage a stage ahead.  Every wait is bounded and
-// reported as in gemv_kernel.
+// reported as in wstream_kernel.
 #pragma once
 
 #include "gemv_kernel.cuh"
@@ -46,7 +46,7 @@ __host__ __device__ constexpr int rg_smem_bytes() {
 }
 
 template <class F>
-__global__ void __launch_bounds__(kRgThreads, 1) gemv_rowgroup_kernel(const GemvParams p) {
+__global__ void __launch_bounds__(kRgThreads, 1) rowgroup_stream_kernel(const RunParams p) {
   constexpr int M = 1;
   constexpr int NS = 4;
   constexpr int SB = kRgSub * 2 * kRgPiece;  // stage bytes

@@ -223,12 +223,24 @@ def _addr(a):
     return a.data_ptr(), a
 
 
+def _current(stream):
+    """The stream a torch-level call runs on: the one given, else torch's
+    current stream (the C calls themselves take NULL as the legacy default
+    stream)."""
+    if stream is not None:
+        return stream
+    import torch
+    return torch.cuda.current_stream().cuda_stream
+
+
 class QGemv:
     """One packed weight matrix on the GPU.
 
     ``QGemv(fmt, N, K, packed, scales=None, codebooks=None)`` copies the
     canonical inputs into the library; ``gemv(x)`` returns y = x . W^T as a
-    new fp32 CUDA tensor, ``run(x, y)`` writes into ``y``."""
+    new fp32 CUDA tensor, ``run(x, y)`` writes into ``y``.  Runs are ordered
+    on ``stream`` when one is given, else on torch's current stream, like the
+    torch operations around them."""
 
     def __init__(self, fmt, N: int, K: int, packed, scales=None, codebooks=None):
         self.fmt, self.N, self.K = _fmt(fmt), int(N), int(K)
@@ -267,12 +279,13 @@ class QGemv:
 
     def run(self, x, y, stream=None):
         M = x.shape[0]
-        qgemv_run(self.handle, x.data_ptr(), M, y.data_ptr(), stream)
+        qgemv_run(self.handle, x.data_ptr(), M, y.data_ptr(), _current(stream))
         return y
 
     def run_residual(self, x, y, residual, stream=None):
         """y = residual + x . W^T (residual may be y itself)."""
-        qgemv_run_residual(self.handle, x.data_ptr(), x.shape[0], y.data_ptr(), residual.data_ptr(), stream)
+        qgemv_run_residual(self.handle, x.data_ptr(), x.shape[0], y.data_ptr(), residual.data_ptr(),
+                           _current(stream))
         return y
 
     def gemv(self, x, stream=None):
@@ -283,7 +296,7 @@ class QGemv:
     def dequant(self, stream=None):
         import torch
         w = torch.empty((self.N, self.K), dtype=torch.float32, device="cuda")
-        qgemv_dequant(self.handle, w.data_ptr(), stream)
+        qgemv_dequant(self.handle, w.data_ptr(), _current(stream))
         return w
 
     def status(self):
@@ -298,7 +311,7 @@ class QGemv:
     def run_xq(self, xq, M: int, y, residual=None, stream=None):
         """y (+ residual) from prepared INT8 activations (``prepare_x_int8``)."""
         qgemv_run_xq(self.handle, xq.data_ptr(), M, y.data_ptr(),
-                     None if residual is None else residual.data_ptr(), stream)
+                     None if residual is None else residual.data_ptr(), _current(stream))
         return y
 
     def close(self):
@@ -318,7 +331,7 @@ def quantize_q4_0(w, stream=None):
     import torch
     N, K = w.shape
     out = torch.empty(qgemv_packed_bytes(Q4_0, N, K), dtype=torch.uint8, device=w.device)
-    qgemv_quantize_q4_0(w.contiguous().data_ptr(), N, K, out.data_ptr(), stream)
+    qgemv_quantize_q4_0(w.contiguous().data_ptr(), N, K, out.data_ptr(), _current(stream))
     return out
 
 
@@ -329,7 +342,7 @@ def quantize_x_int8(x, stream=None):
     M, K = x.shape
     q = torch.empty((M, K), dtype=torch.int8, device=x.device)
     a = torch.empty((M, K // 128), dtype=torch.float32, device=x.device)
-    qgemv_quantize_x_int8(x.contiguous().data_ptr(), M, K, q.data_ptr(), a.data_ptr(), stream)
+    qgemv_quantize_x_int8(x.contiguous().data_ptr(), M, K, q.data_ptr(), a.data_ptr(), _current(stream))
     return q, a
 
 
@@ -343,6 +356,6 @@ def prepare_x_int8(x, hadamard_block: int = 0, signs=None, stream=None):
     M, K = x.shape
     xq = torch.empty(qgemv_xq_bytes(M, K), dtype=torch.uint8, device=x.device)
     qgemv_prepare_x_int8(x.contiguous().data_ptr(), M, K, None if signs is None else signs.data_ptr(),
-                         hadamard_block, xq.data_ptr(), stream)
+                         hadamard_block, xq.data_ptr(), _current(stream))
     return xq
 

@@ -301,7 +301,9 @@ void qgemv_destroy(qgemv_handle h);
  * worth of work on one context) race on the array: serialize them.
  * The first call on a device finds the array's device address
  * (cudaGetSymbolAddress) with that device current and sets the kernel's
- * shared-memory limit; make that first call before any stream capture.
+ * shared-memory limit; make that first call before any stream capture.  If
+ * that set-up fails, the call returns QGEMV_ERR_CUDA, nothing is remembered
+ * and the next call on the device tries the set-up again.
  * Asynchronous on `stream`; results are bitwise reproducible call to call.  */
 int qgemv_run_q4_0_noalloc(const void* packed, int64_t N, int64_t K, const void* x, int M,
                            float* y, void* stream);

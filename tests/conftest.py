@@ -14,9 +14,17 @@ def pytest_configure(config):
                             "under -x a failure there cannot hide the other results")
 
 
+# The allocation-free entry point's tests run after everything else, the
+# ``late`` ones included.
+LAST_FILE = "test_zz_no_alloc.py"
+
+
 def pytest_collection_modifyitems(config, items):
-    items[:] = ([it for it in items if it.get_closest_marker("late") is None]
-                + [it for it in items if it.get_closest_marker("late") is not None])
+    def rank(it):
+        if it.fspath.basename == LAST_FILE:
+            return 2
+        return 1 if it.get_closest_marker("late") is not None else 0
+    items[:] = sorted(items, key=rank)  # stable: collection order within a rank
 
 
 def cuda_available() -> bool:

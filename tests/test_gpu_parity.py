@@ -287,3 +287,27 @@ def test_full_size_sampled_rows(fmt, N, K, Ms):
             y = gpu_gemv(h, x)[:, rows]
             y_ref, bound = oracle.gemv(fmt, N, K, packed, scales, cb, x, rows=rows)
             assert_within(y, y_ref, bound, f"{fmt} {N}x{K} M={M}")
+
+
+def test_torch_side_stream_orders_with_torch_work():
+    """QGemv calls without an explicit stream run on torch's current stream:
+    on a side stream, the activations written there just before and the
+    output read there just after are ordered with the GEMV, and the result
+    equals the default-stream run bit for bit."""
+    N, K = MULTI["cbk4"]
+    packed, scales, cb = make_case("cbk4", N, K, tag="sidestream")
+    h = qgemv.QGemv("cbk4", N, K, packed, scales, cb)
+    x_np = make_x(3, K, tag="sidestream")
+    y_default = gpu_gemv(h, x_np)
+    s = torch.cuda.Stream()
+    src = cuda(x_np)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        x = torch.empty_like(src)
+        torch.cuda._sleep(1_000_000)  # keep the side stream busy so that an unordered run would race
+        x.copy_(src)
+        y = h.gemv(x)
+        y_host = y.to("cpu", non_blocking=False)
+    torch.cuda.synchronize()
+    assert h.status() == qgemv.QGEMV_OK
+    assert np.array_equal(y_host.numpy(), y_default)

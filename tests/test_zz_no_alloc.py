@@ -3,11 +3,14 @@
 It serves callers that cannot allocate device memory at the point where
 they need the product: it takes the canonical blocks, x and y from the
 caller and keeps its split-K scratch in a fixed static device array.  These
-tests call it through the C ABI and check it against the regular entry point
-(a handle made with qgemv_create) on two calls in a row, within the GEMV
-tolerance |a - b| <= 1e-3 * sum_k |x w| + 1e-6.  This file is collected after
-the other established tests (only tests marked ``late`` follow it) so that a
-run stopping at the first failure has already run them.
+tests call it through the C ABI on two calls in a row and check every output
+against the fp64 oracle (|y - y_ref| <= 1e-3 * sum_k |x w| + 1e-6) and
+against the regular entry point (a handle made with qgemv_create), within
+the same bound.  The shapes cover one K chunk, several whole chunks and a
+short last chunk (K not a multiple of the 2048-input chunk: a zero-padded
+activation tail and a short partial), at M = 1 to 16.  This file is
+collected after every other test, so that a run stopping at the first
+failure has already run them.
 """
 import numpy as np
 import pytest
@@ -28,16 +31,18 @@ def _lib():
 
 
 @pytest.mark.parametrize("N, K, M", [(300, 800, 1),      # one K chunk: no scratch partials
-                                     (2500, 8192, 4),    # four chunks
-                                     (8192, 4096, 16)])  # two chunks, widest M
-def test_noalloc_matches_regular_entry_point_on_two_calls(N, K, M):
+                                     (2500, 8192, 4),    # four whole chunks
+                                     (8192, 4096, 16),   # two chunks, widest M
+                                     (4096, 11008, 8),   # six chunks, the last 768 inputs (7B down)
+                                     (100, 2080, 3)])    # two chunks, the last 32 inputs
+def test_noalloc_matches_oracle_and_regular_entry_point_on_two_calls(N, K, M):
     packed = inputs.q4_0_random_blocks(inputs.rng(f"noalloc/{N}x{K}"), N, K)
     x_np = inputs.x_fp16(inputs.rng(f"noalloc/x/{M}x{K}"), M, K)
     x = torch.from_numpy(x_np).cuda()
     h = qgemv.QGemv("q4_0", N, K, packed)
     y_regular = h.gemv(x)
     packed_dev = torch.from_numpy(packed).cuda()
-    _, bound = oracle.gemv("q4_0", N, K, packed, None, None, x_np)
+    y_ref, bound = oracle.gemv("q4_0", N, K, packed, None, None, x_np)
     outs = []
     for _ in range(2):
         y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
@@ -46,9 +51,11 @@ def test_noalloc_matches_regular_entry_point_on_two_calls(N, K, M):
         assert rc == qgemv.QGEMV_OK, qgemv.qgemv_last_error()
         torch.cuda.synchronize()
         outs.append(y.cpu().numpy())
-    ref = y_regular.cpu().numpy()
+    regular = y_regular.cpu().numpy()
     for y in outs:
-        assert np.all(np.abs(y.astype(np.float64) - ref) <= 1e-3 * bound + 1e-6)
+        ok = oracle.within_tolerance(y, y_ref, bound)
+        assert ok.all(), f"{np.count_nonzero(~ok)} outputs out of tolerance against the oracle"
+        assert np.all(np.abs(y.astype(np.float64) - regular) <= 1e-3 * bound + 1e-6)
     assert np.array_equal(outs[0], outs[1])
 
 
