@@ -37,7 +37,8 @@ const FormatOps* ops_cbk8() {
       &LaunchTable<F>::smem_bytes, &LaunchTable<F>::setup, &LaunchTable<F>::launch,
       &prepare, &dequant, /*cb_entries=*/256, /*tile_rows=*/128, /*partial_stride=*/128 * 16,
       /*aux_per_row=*/0, /*m1_ctas_per_sm=*/LaunchTable<F>::kM1CtasPerSm,
-      /*rowgroup=*/1};
+      /*rowgroup=*/1, /*launch_x_int8=*/nullptr, /*row_tables=*/0, /*launch_xq=*/nullptr,
+      /*launch_glu=*/nullptr, /*tc5_min_m=*/kTc5DefaultMinM};
   return &ops;
 }
 

@@ -33,6 +33,7 @@ struct LaunchGeom {
   int grid_m1;
   const CtaPlan* plan_m1;
   int grid_rg;  // M = 1 row-group kernel (table formats, whole rows per CTA): its grid, 0 if not used
+  int tc5_min_m;  // calls with at least this many rows run the tensor-memory kernel (0: never)
 };
 
 struct FormatOps {
@@ -64,7 +65,13 @@ struct FormatOps {
   cudaError_t (*launch_xq)(int M, const RunParams& p, const LaunchGeom& g, cudaStream_t s) = nullptr;
   // Q4_0, PQ2_0: the fused SiLU(gate) * up run of a GLU handle (qgemv_create_glu), else nullptr
   cudaError_t (*launch_glu)(int M, const RunParams& p, const LaunchGeom& g, cudaStream_t s) = nullptr;
+  // formats with the tensor-memory kernel (tc5_kernel.cuh): the smallest M
+  // that runs it by default (0: not by default)
+  int tc5_min_m = 0;
 };
+
+// The formats that have the tensor-memory kernel (tc5_kernel.cuh).
+inline bool has_tc5(int format) { return format >= 1 && format <= 4; }  // Q4_0, CBK4, CBK8, PQ2_0
 
 const FormatOps* ops_q4_0();
 const FormatOps* ops_pq2();

@@ -7,6 +7,7 @@
 #include "gemv_kernel.cuh"
 #include "mma_kernel.cuh"
 #include "rowgroup_kernel.cuh"
+#include "tc5_kernel.cuh"
 
 namespace qgemv {
 
@@ -100,6 +101,19 @@ struct LaunchTable {
     return cudaSuccess;
   }
 
+  // The tensor-memory kernel (tc5_kernel.cuh; one CTA per SM, the handle's
+  // grid and plan), for the formats that have it: MT = 8 accumulator columns
+  // read back up to M = 8, 16 above.
+  template <int MT>
+  static cudaError_t launch_tc5(const RunParams& p, int M, const LaunchGeom& g, cudaStream_t s) {
+    static_assert(tc5_smem_bytes<F, MT>() + 2048 <= 228 * 1024, "shared memory budget exceeded");
+    RunParams q = p;
+    q.plan = g.plan;
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = config(g.grid, kTc5Threads, tc5_smem_bytes<F, MT>(), s, attr);
+    return cudaLaunchKernelEx(&cfg, tc5_kernel<F, MT>, q, M);
+  }
+
   static int smem_bytes(int M) {
     if (M == 1) return gemv_smem_bytes<F, 1>();
     if (M >= 2 && M <= 8) return F::mma_par(1) ? mma_smem_bytes<F, 1, true>() : mma_smem_bytes<F, 1>();
@@ -124,12 +138,23 @@ struct LaunchTable {
         e = cudaFuncSetAttribute(rowgroup_stream_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  rg_smem_bytes<F>());
     }
+    if constexpr (Tc5<F>::kHas) {
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(tc5_kernel<F, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize, tc5_smem_bytes<F, 8>());
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(tc5_kernel<F, 16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 tc5_smem_bytes<F, 16>());
+    }
     return e;
   }
 
   static cudaError_t launch(int M, const RunParams& p, const LaunchGeom& g, cudaStream_t s,
                             bool batch_invariant) {
     RunParams q = p;
+    if constexpr (Tc5<F>::kHas) {
+      if (!batch_invariant && g.tc5_min_m > 0 && M >= g.tc5_min_m && M <= kMaxM)
+        return M <= 8 ? launch_tc5<8>(q, M, g, s) : launch_tc5<16>(q, M, g, s);
+    }
     if (M == 1 && !batch_invariant) {
       if constexpr (F::kTileParity) {
         if (g.grid_rg > 0) return launch_rg(q, g.grid_rg, s);

@@ -113,6 +113,11 @@ bool is_device_pointer(const void* p) {
 //   QGEMV_ROWGROUP=0|1      (not a fault) forbid or force the M = 1
 //                           row-group kernel of the table formats, so that
 //                           tests cover both M = 1 kernels on any shape;
+//   QGEMV_TC5=n             (not a fault) runs with at least n activation
+//                           rows use the tensor-memory kernel of the formats
+//                           that have it (0: never, 1: every M), instead of
+//                           the measured default, so that tests and the
+//                           benchmark's crossover sweep reach both kernels;
 //   QGEMV_FAULT_SKIP_CTA=c  the handle's runs launch CTA c as a no-op, so
 //                           the CTAs that share a row tile with it never get
 //                           its partial sums: their bounded fix-up waits run
@@ -220,6 +225,7 @@ struct qgemv_ctx {
   int x_int8;           // qgemv_set_x_int8 (PQ2_0)
   int glu;              // qgemv_create_glu: gate and up interleaved, output SiLU(gate) * up
   int skip_cta;         // QGEMV_FAULT_SKIP_CTA test hook, -1 normally
+  int tc5_min_m;        // runs of at least this many rows use the tensor-memory kernel (0: never)
   qgemv_ctx* mma;       // AQLM: the tensor-core companion (format kAqlmMma), else nullptr
 };
 
@@ -313,6 +319,8 @@ static qgemv_handle create_impl(int format, int64_t N, int64_t K, const void* pa
   }
   h->magic = kMagic;
   h->skip_cta = env_int("QGEMV_FAULT_SKIP_CTA", -1);
+  h->tc5_min_m = qgemv::has_tc5(format) ? env_int("QGEMV_TC5", ops->tc5_min_m) : 0;
+  if (h->tc5_min_m < 0 || h->tc5_min_m > qgemv::kMaxM) h->tc5_min_m = 0;
   if (!nested) {
     g_alloc_count = 0;
     g_alloc_fail = env_int("QGEMV_FAULT_ALLOC", 0);
@@ -606,7 +614,7 @@ static int run_impl(qgemv_handle h, const void* x, int M, float* y, const float*
   if (h->glu) {
     if (residual) return set_error(QGEMV_ERR_ARG, "a GLU handle takes no residual");
     const qgemv::RunParams p = params_of(h, x, y, nullptr);
-    const qgemv::LaunchGeom g = {h->grid, h->plan, h->grid_m1, h->plan_m1, 0};
+    const qgemv::LaunchGeom g = {h->grid, h->plan, h->grid_m1, h->plan_m1, 0, 0};
     const cudaError_t e = h->ops->launch_glu(M, p, g, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_error(e, "launching the GEMV kernel");
     return ok();
@@ -614,7 +622,7 @@ static int run_impl(qgemv_handle h, const void* x, int M, float* y, const float*
   const bool inv = h->batch_invariant != 0;
   if (h->mma && (M >= kAqlmMmaMinM || inv)) h = h->mma;  // AQLM: the tensor-core layout
   const qgemv::RunParams p = params_of(h, x, y, residual);
-  const qgemv::LaunchGeom g = {h->grid, h->plan, h->grid_m1, h->plan_m1, h->grid_rg};
+  const qgemv::LaunchGeom g = {h->grid, h->plan, h->grid_m1, h->plan_m1, h->grid_rg, h->tc5_min_m};
   cudaError_t e = h->x_int8 ? h->ops->launch_x_int8(M, p, g, static_cast<cudaStream_t>(stream))
                             : h->ops->launch(M, p, g, static_cast<cudaStream_t>(stream), inv);
   if (e != cudaSuccess) return cuda_error(e, "launching the GEMV kernel");
@@ -678,7 +686,7 @@ int qgemv_run_xq(qgemv_handle h, const void* xq, int M, float* y, const float* r
   const uint8_t* base = static_cast<const uint8_t*>(xq);
   p.x_scale = reinterpret_cast<const float*>(base + int64_t(M) * h->K);
   p.x_qsum = reinterpret_cast<const int32_t*>(base + int64_t(M) * h->K + 4 * int64_t(M) * (h->K / 128));
-  const qgemv::LaunchGeom g = {h->grid, h->plan, h->grid_m1, h->plan_m1, h->grid_rg};
+  const qgemv::LaunchGeom g = {h->grid, h->plan, h->grid_m1, h->plan_m1, h->grid_rg, 0};
   cudaError_t e = h->ops->launch_xq(M, p, g, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_error(e, "launching the GEMV kernel");
   return ok();
