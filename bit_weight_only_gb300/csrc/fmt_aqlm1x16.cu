@@ -52,7 +52,10 @@ __device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
 }
 
 template <int MB>
-__global__ void __launch_bounds__(kThreads) aqlm1x16_kernel(const RunParams p, int M) {
+// A register cap rather than launch bounds: left to itself the compiler
+// gives the eight-row instantiation 48 registers and spills; 64 keep four
+// CTAs of 256 threads per SM resident.
+__global__ void __maxnreg__(64) aqlm1x16_kernel(const RunParams p, int M) {
   const uint4* cb = static_cast<const uint4*>(p.aux);
   const unsigned short* scales =
       reinterpret_cast<const unsigned short*>(static_cast<const uint8_t*>(p.aux) + kCodebookBytes);

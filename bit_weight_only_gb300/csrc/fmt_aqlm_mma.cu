@@ -49,6 +49,7 @@ struct FmtAQLM {
 
   static constexpr int kMmaSharedBytes = kTableAlign;
   static constexpr int kMmaRowWords = 4;  // the 16 code bytes of the thread's half of the row
+  static constexpr bool kMmaLateCodes = true;  // two activation blocks: one m-tile's codes live at a time
   static constexpr int kMmaCodebooks = 2;
   static constexpr bool kMmaRowScales = true;
   __device__ static const __half* mma_row_scales(const RunParams& p) {

@@ -48,6 +48,20 @@
 namespace qgemv {
 
 constexpr int kMmaTiles = 4;  // 16-row m-tiles per warp
+
+// Formats that, with two activation blocks, load each m-tile's code words
+// just before its MMAs (F::kMmaLateCodes) instead of all four m-tiles' at
+// the start of a slice: only one m-tile's codes are live, at the price of
+// releasing the stage after the last m-tile.  Measured: no slower for AQLM
+// (whose four code words per row would otherwise spill), 7% slower for CBK4.
+template <class F, class = void>
+struct MmaLateCodes {
+  static constexpr bool value = false;
+};
+template <class F>
+struct MmaLateCodes<F, decltype(void(F::kMmaLateCodes))> {
+  static constexpr bool value = F::kMmaLateCodes;
+};
 // Geometry.  Default: two warps per group of F::mma_spw(NB) k-slices (one
 // slice per warp: 16 warps, one CTA per SM; two slices per warp: 8 warps, two
 // CTAs per SM, F::mma_ctas(NB)).  Tile parity (PAR; one-CTA-per-SM formats):
@@ -382,8 +396,7 @@ __global__ void __launch_bounds__(mma_threads<F, NB, PAR>(), F::mma_ctas(NB)) ws
           // the warp's last slice, release the stage
           uint32_t w[kMmaTiles][2][F::kMmaRowWords];
           typename F::MmaScales d[kMmaTiles][2];  // block scales of the rows, read per block
-  #pragma unroll
-          for (int mt = 0; mt < kMmaTiles; ++mt) {
+          auto load_mtile = [&](int mt) {
             const int j = 2 * hf + (mt >> 1);
             const int l = 16 * (mt & 1) + gi;
             F::mma_load_row(stage, slice, l, j, q, w[mt][0]);
@@ -392,17 +405,23 @@ __global__ void __launch_bounds__(mma_threads<F, NB, PAR>(), F::mma_ctas(NB)) ws
               F::mma_scales(stage, slice, l, j, d[mt][0]);
               F::mma_scales(stage, slice, l + 8, j, d[mt][1]);
             }
-          }
-          if (ss == SPW - 1) {
-            release_stage(&empty[st], lane);
-          }
-
+          };
           // MG m-tiles at a time, their MMAs interleaved so that consecutive
           // MMAs are independent (all four for one activation block; one for
           // two, which need twice the accumulators)
           constexpr int MG = NB == 1 ? kMmaTiles : 1;
+          constexpr bool kLate = MG == 1 && MmaLateCodes<F>::value;
+          if constexpr (!kLate) {
+  #pragma unroll
+            for (int mt = 0; mt < kMmaTiles; ++mt) load_mtile(mt);
+            if (ss == SPW - 1) release_stage(&empty[st], lane);
+          }
   #pragma unroll
           for (int mg = 0; mg < kMmaTiles; mg += MG) {
+            if constexpr (kLate) {
+              load_mtile(mg);
+              if (ss == SPW - 1 && mg == kMmaTiles - 1) release_stage(&empty[st], lane);
+            }
   #pragma unroll
             for (int blk = 0; blk < NBLK; ++blk) {
               float tmp[MG][NB][4];  // block sums (block formats); the first MMA writes them
