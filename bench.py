@@ -511,11 +511,11 @@ def run_ours(args, rank, world, device):
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": K_e2e},
         # one launch per GEMV (AQLM: one table pass for M <= 2, else the
-        # tensor-core kernel); the INT8 path launches once per 4, 2 or 1
-        # rows, CBK4_ROW once per 2 or 1
+        # tensor-core kernel; the fused SiLU(gate)*up one for every M); the
+        # INT8 path launches once per 4, 2 or 1 rows, CBK4_ROW once per 2 or 1
         "gpu_launches": sum((x_int8_launches(M) + (1 if "xq" in o else 0)) if o.get("x_int8") else
                             (M + 1) // 2 if o["fmt"] == "cbk4_row" else
-                            M if o["fmt"] == "pq2_0_glu" else 1 for o in ops) * K,
+                            1 for o in ops) * K,
         "clocks": clocks,
     }
     if not args.no_cpu_baseline and world == 1:

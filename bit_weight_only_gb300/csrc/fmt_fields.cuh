@@ -81,6 +81,7 @@ struct FmtQ4_0 {
   static constexpr int kMmaRowWords = 2;   // words q of the two 16-byte halves
   static constexpr int kMmaCodebooks = 1;
   static constexpr bool kMmaRowScales = false;
+  static constexpr bool kMmaGlu = true;    // the GLU form of the tensor-core kernel
   __device__ static const __half* mma_row_scales(const RunParams&) { return nullptr; }
   static constexpr int kMmaBlockSteps = 2;
   static constexpr int kMmaXWords = 8;  // x[m][32b + 8q .. +7], b = 0, 1
@@ -255,6 +256,7 @@ struct FmtPQ2 {
   static constexpr int kMmaRowWords = 2;   // words q of the two 16-byte halves
   static constexpr int kMmaCodebooks = 1;
   static constexpr bool kMmaRowScales = false;
+  static constexpr bool kMmaGlu = true;    // the GLU form of the tensor-core kernel
   __device__ static const __half* mma_row_scales(const RunParams&) { return nullptr; }
   static constexpr int kMmaBlockSteps = 8;
   static constexpr int kMmaXWords = 16;  // x[m][64h + 16q .. +15], h = 0, 1

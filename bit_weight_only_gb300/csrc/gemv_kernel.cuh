@@ -363,7 +363,7 @@ __device__ __forceinline__ float take_slot(const RunParams& p, float* slot, bool
 // gate and up sums over the S contributors in order, then SiLU(gate) * up.
 template <int M, int NT>
 __device__ __noinline__ void finish_rows_glu(const RunParams& p, const CtaPlan& pl, int sg, float out_scale,
-                                             int tid) {
+                                             int tid, int mrows = M) {
   const int64_t rt = pl.seg_rt[sg];
   const int64_t cf = pl.seg_cf[sg];
   const int S = pl.seg_S[sg];
@@ -373,7 +373,7 @@ __device__ __noinline__ void finish_rows_glu(const RunParams& p, const CtaPlan& 
   float* first_slot = p.partials + (cf * 2 + (pl.seg_side1[sg] ? 1 : 0)) * kPartialStride;
   float* base = p.partials + cf * 2 * kPartialStride;
   bool gave_up = false;
-  for (int t = tid; t < nr * M; t += NT) {
+  for (int t = tid; t < nr * mrows; t += NT) {
     const int m = t / nr;
     const int r = r0 + (t - m * nr);
     float g = 0.f, u = 0.f;

@@ -78,15 +78,40 @@ struct LaunchTable {
     return cudaLaunchKernelEx(&cfg, rowgroup_stream_kernel<F>, p);
   }
 
-  // GLU handles (gate and up interleaved; wstream_kernel's GLU epilogue): the
-  // M = 1 CUDA-core kernel once per activation row, on the M = 1 grid and
-  // its plan (made with 64-row halves).
+  // GLU handles (gate and up interleaved; the GLU epilogues): M = 1 on the
+  // CUDA-core kernel, on the M = 1 grid and its plan (made with 64-row
+  // halves); M >= 2 in one launch of the tensor-core kernel for formats that
+  // have its GLU form (F::kMmaGlu), else the CUDA-core kernel once per
+  // activation row.
+  static constexpr bool kMmaGlu = MmaGluOf<F>::value;
   static cudaError_t setup_glu() {
-    return cudaFuncSetAttribute(wstream_kernel<F, 1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                gemv_smem_bytes<F, 1>());
+    cudaError_t e = cudaFuncSetAttribute(wstream_kernel<F, 1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         gemv_smem_bytes<F, 1>());
+    if constexpr (kMmaGlu) {
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(wstream_mma_kernel<F, 1, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 mma_smem_bytes<F, 1>());
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(wstream_mma_kernel<F, 2, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 mma_smem_bytes<F, 2>());
+    }
+    return e;
+  }
+  template <int NB>
+  static cudaError_t launch_mma_glu(const RunParams& p, int M, const LaunchGeom& g, cudaStream_t s) {
+    RunParams q = p;
+    q.residual = nullptr;
+    q.plan = F::mma_ctas(NB) == 1 ? g.plan : g.plan_m1;
+    const int grid = F::mma_ctas(NB) == 1 ? g.grid : g.grid_m1;
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = config(grid, mma_threads<F, NB>(), mma_smem_bytes<F, NB>(), s, attr);
+    return cudaLaunchKernelEx(&cfg, wstream_mma_kernel<F, NB, false, true>, q, M);
   }
   static cudaError_t launch_glu(int M, const RunParams& p, const LaunchGeom& g, cudaStream_t s) {
     if (M < 1 || M > kMaxM) return cudaErrorInvalidValue;
+    if constexpr (kMmaGlu) {
+      if (M >= 2) return M <= 8 ? launch_mma_glu<1>(p, M, g, s) : launch_mma_glu<2>(p, M, g, s);
+    }
     for (int m = 0; m < M; ++m) {
       RunParams q = p;
       q.x = p.x + m * p.K;

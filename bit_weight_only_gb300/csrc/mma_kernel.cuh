@@ -54,6 +54,16 @@ constexpr int kMmaTiles = 4;  // 16-row m-tiles per warp
 // the start of a slice: only one m-tile's codes are live, at the price of
 // releasing the stage after the last m-tile.  Measured: no slower for AQLM
 // (whose four code words per row would otherwise spill), 7% slower for CBK4.
+// Formats whose tensor-core kernel has the GLU form (F::kMmaGlu).
+template <class F, class = void>
+struct MmaGluOf {
+  static constexpr bool value = false;
+};
+template <class F>
+struct MmaGluOf<F, decltype(void(F::kMmaGlu))> {
+  static constexpr bool value = F::kMmaGlu;
+};
+
 template <class F, class = void>
 struct MmaLateCodes {
   static constexpr bool value = false;
@@ -217,7 +227,13 @@ __device__ __noinline__ void mma_rebuild_table(uint8_t* lut, const uint16_t* cb,
   F::template mma_init_shared<NT>(lut, cb, warp, lane);
 }
 
-template <class F, int NB, bool PAR = false>
+// GLU: the handle's rows are a gate and an up projection interleaved in
+// 64-row halves of every row tile (as for wstream_kernel's GLU form), and
+// the stores are y[m][64t + r] = SiLU(gate) * up.  A thread's m-tiles 2a and
+// 2a + 1 hold the same rows of the two halves (l and l + 16, the same j), so
+// each gate sum meets its up sum in one thread; split row tiles go through
+// the pair finisher.
+template <class F, int NB, bool PAR = false, bool GLU = false>
 __global__ void __launch_bounds__(mma_threads<F, NB, PAR>(), F::mma_ctas(NB)) wstream_mma_kernel(const RunParams p, int M) {
   constexpr int NS = mma_stages_of<F, NB, PAR>();
   constexpr int TB = F::kTileBytes;
@@ -522,7 +538,12 @@ __global__ void __launch_bounds__(mma_threads<F, NB, PAR>(), F::mma_ctas(NB)) ws
               const int l = 16 * (mt & 1) + gi + (e >> 1) * 8;
               const int r = 4 * l + 2 * hf + (mt >> 1);
               if (m < M) {
-                if (owner) {
+                if (GLU && owner) {
+                  // gate row r (m-tile mt, l < 16) with up row r + 64 (m-tile mt + 1)
+                  if constexpr (GLU) {
+                    if ((mt & 1) == 0) glu_store(p, m, cur_rt * (kTileRows / 2) + r, acc[mt][nb][e], acc[mt + 1][nb][e]);
+                  }
+                } else if (owner) {
                   const int64_t n = cur_rt * kTileRows + r;
                   if (n < p.N) {
                     if constexpr (F::kMmaRowScales)
@@ -630,7 +651,12 @@ __global__ void __launch_bounds__(mma_threads<F, NB, PAR>(), F::mma_ctas(NB)) ws
   wait_plan();
   const __half* row_scales = nullptr;  // per-row output scales (F::kMmaRowScales), applied at the finish
   if constexpr (F::kMmaRowScales) row_scales = F::mma_row_scales(p);
-  finish_all<kTileRows, 8 * NB, NT>(p, kPartialStride, s_plan, row_scales, 1.0f, s_sub, tid, M);
+  if constexpr (GLU) {
+    for (int sg = 0; sg < 2; ++sg)
+      if (s_plan.seg_rt[sg] >= 0) finish_rows_glu<8 * NB, NT>(p, s_plan, sg, 1.0f, tid, M);
+  } else {
+    finish_all<kTileRows, 8 * NB, NT>(p, kPartialStride, s_plan, row_scales, 1.0f, s_sub, tid, M);
+  }
 }
 
 }  // namespace qgemv

@@ -139,7 +139,9 @@ qgemv_handle qgemv_create_stacked(int format, int nseg, const int64_t* seg_rows,
  * runs store the fused activation y[m][n] = SiLU(x . G^T)[m][n] * (x . U^T)
  * [m][n], SiLU(v) = v / (1 + e^-v): the gate/up GEMV with "SiLU(gate) * up
  * in the reduce" of "Trapetum benchmarks" ("Short-context decode, step by
- * step"), one launch per activation row and no separate activation kernel.
+ * step"), with no separate activation kernel.  Q4_0 and PQ2_0 run every M in
+ * one launch (M >= 2 on the tensor-core kernel, the weights read once per
+ * call); CBK4_ROW launches once per activation row.
  *   format: QGEMV_Q4_0, QGEMV_PQ2_0 or QGEMV_CBK4_ROW (the gate and up rows
  *     share the prepared tiles, so formats with one codebook per matrix are
  *     refused; per-row codebooks travel with their rows).

@@ -1,6 +1,7 @@
 """GPU parity of the fused MLP gate/up projection (qgemv_create_glu):
-y = SiLU(x . G^T) * (x . U^T) in one launch per activation row, against the
-oracle's ``gemv_glu`` with the bound of ``within_tolerance_glu`` (each GEMV
+y = SiLU(x . G^T) * (x . U^T) -- Q4_0 and PQ2_0 in one launch for every M
+(the tensor-core kernel from M = 2), CBK4_ROW once per activation row --
+against the oracle's ``gemv_glu`` with the bound of ``within_tolerance_glu`` (each GEMV
 sum within its own 1e-3 * sum |x w| + 1e-6, propagated through SiLU and the
 product, plus a few fp32 roundings).
 
@@ -8,7 +9,8 @@ Covered: Q4_0, PQ2_0 and CBK4_ROW (per-row codebooks interleaved with their
 rows); shapes whose row tiles are split between CTAs
 (the pair finisher) and owned whole (the epilogue); the 7B MLP's gate/up
 11008 x 4096 and the 5120/17408 model's 17408 x 5120 at full size on
-sampled outputs; M = 1 and 3; the dequant of the interleaved rows; and the
+sampled outputs; M = 1, 3, 9 and 16 (both activation blocks of the
+tensor-core kernel); the dequant of the interleaved rows; and the
 refusals (codebook formats, N not a multiple of 64, residual, INT8 mode).
 """
 import numpy as np
@@ -47,7 +49,7 @@ def _codebooks(fmt, N, K, tag):
 
 @pytest.mark.parametrize("fmt", ["q4_0", "pq2_0", "cbk4_row"])
 @pytest.mark.parametrize("N,K", [(192, 1024), (704, 2048), (4096, 4096)])
-@pytest.mark.parametrize("M", [1, 3])
+@pytest.mark.parametrize("M", [1, 3, 9, 16])
 def test_glu_matches_oracle(fmt, N, K, M):
     tag = f"glu/{fmt}/{N}x{K}"
     pg, pu = _pair(fmt, N, K, tag)
