@@ -304,10 +304,14 @@ class ClockSampler:
 
 # ----------------------------------------------------------- our arm ------
 
-def x_int8_launches(M):
-    """Launches of one PQ2_0 INT8-path call: rows go four, then two, then one
-    at a time."""
-    return M // 4 + (M % 4) // 2 + M % 2
+def x_int8_launches(M, prepared=False):
+    """Launches of one PQ2_0 INT8-path call: up to three rows, the CUDA-core
+    kernel (four, two, then one rows per launch); four or more, the
+    activation prologue then the tensor-core kernel (on prepared activations
+    the tensor-core kernel alone)."""
+    if M < 4:
+        return M // 2 + M % 2
+    return 1 if prepared else 2
 
 
 def max_over_ranks(values, world, device):
@@ -489,7 +493,9 @@ def run_ours(args, rank, world, device):
                    "parallelism": f"replicas{world}", "peak_hbm_gbs": peak,
                    "frac_of_peak": round(value / world / peak, 4)},
         "roofline": {"bound": "hbm",
-                     "kernel": ("wstream_kernel<FmtPQ2I8, MB>, MB = 4, 2, 1 activation rows per launch" if args.x_int8
+                     "kernel": (("wstream_kernel<FmtPQ2I8, MB>, MB = 2, 1 rows per launch" if M < 4 else
+                                 f"wstream_mma_kernel<FmtPQ2Q8, NB={1 if M <= 8 else 2}> (f16 MMA on INT8 codes)")
+                                if args.x_int8
                                 else "aqlm1x16_kernel (codebook entries gathered from L2: a 32-byte sector "
                                      "per group of 8 weights bounds it before HBM does)" if dominant == "aqlm_1x16"
                                 else "wstream_kernel<FmtCBK4R, MB>, MB = 2, 1 activation rows per launch"
@@ -512,8 +518,9 @@ def run_ours(args, rank, world, device):
                 "d2h_bytes_per_step": d2h, "steps": K_e2e},
         # one launch per GEMV (AQLM: one table pass for M <= 2, else the
         # tensor-core kernel; the fused SiLU(gate)*up one for every M); the
-        # INT8 path launches once per 4, 2 or 1 rows, CBK4_ROW once per 2 or 1
-        "gpu_launches": sum((x_int8_launches(M) + (1 if "xq" in o else 0)) if o.get("x_int8") else
+        # INT8 path with several rows adds its activation prologue; CBK4_ROW
+        # launches once per 2 or 1 rows
+        "gpu_launches": sum((x_int8_launches(M, "xq" in o) + (1 if "xq" in o else 0)) if o.get("x_int8") else
                             (M + 1) // 2 if o["fmt"] == "cbk4_row" else
                             1 for o in ops) * K,
         "clocks": clocks,

@@ -601,4 +601,72 @@ struct FmtPQ2I8P : FmtPQ2I8 {
   }
 };
 
+// ------------------------------- PQ2_0 integer path on the tensor cores --
+//
+// The integer path for several activation rows: PQ2_0 tiles and decode as
+// FmtPQ2 (A = code - 1, exact fp16), and as B the prepared INT8 activations
+// (qgemv_prepare_x_int8's layout) converted to fp16 in registers -- every
+// INT8 value is an exact fp16 -- so the f16 MMA's fp32 block sum is the
+// exact integer sum of (code - 1) times the INT8 codes (at most 2 * 127 *
+// 128 in magnitude, far below 2^24).  The block (one slice, one INT8 group)
+// then adds d * (a * inner) in fp32, the CUDA-core integer path's
+// operations.  The f16 MMA rather than the INT8 one: this part's INT8
+// tensor rate is far below its f16 rate.
+//   Activations: thread q's k16 step 4h + sub needs, of its column's
+//   inputs, k0 + {2sub, 2sub + 8} and k0 + {2sub + 1, 2sub + 9} with
+//   k0 = 64h + 16q (FmtPQ2's fragment order).  The prepared group holds
+//   input 16i + s + 4b at byte 16i + 4s + b, so the 16 bytes of word
+//   i = 4h + q of the slice hold all of them: byte pairs (0, 2) and (4, 6)
+//   for sub = 0, (8, 10) and (12, 14) for 1, (1, 3) and (5, 7) for 2,
+//   (9, 11) and (13, 15) for 3.  A pair becomes fp16 with one PRMT (the
+//   bytes, xor 0x80, under an exponent byte 0x64: 1024 + 128 + q) and one
+//   HADD2 (- 1152).
+struct FmtPQ2Q8 : FmtPQ2 {
+  static constexpr bool kMmaXCodes = true;  // B from INT8 codes, a per-group column scale
+  static constexpr int kMmaXWords = 10;     // the two 16-byte words of the halves, then a of the two D columns
+  __host__ __device__ static constexpr bool mma_prefetch_x(int nb) { return nb == 1; }
+  // Codes of prepared row mb (B column gi of the block) for the slice at kb
+  // (words q and 4 + q of the group, 16 bytes each), and the group's scale
+  // for D columns md and md + 1; zeros past M and K.
+  __device__ static void mma_load_x_q(uint32_t (&xw)[kMmaXWords], const RunParams& p, int M, int mb, int md,
+                                      int64_t kb, int q, bool vec) {
+    const uint8_t* xq = reinterpret_cast<const uint8_t*>(p.x);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      if (mb < M && kb < p.K) {
+        const uint8_t* src = xq + mb * p.K + kb + 64 * h + 16 * q;
+        if (vec) {
+          const uint4 v = __ldg(reinterpret_cast<const uint4*>(src));
+          xw[4 * h] = v.x; xw[4 * h + 1] = v.y; xw[4 * h + 2] = v.z; xw[4 * h + 3] = v.w;
+        } else {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) xw[4 * h + i] = __ldg(reinterpret_cast<const uint32_t*>(src) + i);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) xw[4 * h + i] = 0u;
+      }
+    }
+    const int64_t G = p.K / 128, g = kb / 128;
+#pragma unroll
+    for (int c = 0; c < 2; ++c)
+      xw[8 + c] = (md + c < M && kb < p.K) ? __float_as_uint(__ldg(p.x_scale + (md + c) * G + g)) : 0u;
+  }
+  // the fp16 pair of signed bytes lo, hi of w (PRMT selector sel)
+  __device__ static uint32_t i8_pair(uint32_t w, uint32_t sel) {
+    const uint32_t t = prmt(w ^ 0x80808080u, 0x64646464u, sel);
+    uint32_t r;
+    asm("add.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(t), "r"(0xE480E480u));  // - 1152
+    return r;
+  }
+  __device__ static uint2 mma_bfrag(const uint32_t (&xw)[kMmaXWords], int ks) {
+    const uint32_t* W = xw + 4 * (ks >> 2);
+    const int sub = ks & 3;
+    const uint32_t sel = (sub & 2) ? 0x4341u : 0x4240u;  // bytes (1, 3) or (0, 2)
+    const int w0 = (sub & 1) ? 2 : 0;                     // words (0, 1) or (2, 3)
+    return make_uint2(i8_pair(W[w0], sel), i8_pair(W[w0 + 1], sel));
+  }
+  __device__ static float mma_col_scale(const uint32_t (&xw)[kMmaXWords], int c) { return __uint_as_float(xw[8 + c]); }
+};
+
 }  // namespace qgemv

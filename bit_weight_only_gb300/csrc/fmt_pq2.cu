@@ -142,8 +142,18 @@ cudaError_t set_i8_smem_of() {
                               gemv_smem_bytes<FI, MB>());
 }
 
+// The INT8 tensor-core kernel (FmtPQ2Q8): one or two activation blocks.
+template <int NB>
+cudaError_t set_q8_smem() {
+  static_assert(mma_smem_bytes<FmtPQ2Q8, NB>() + 2048 <= 228 * 1024, "shared memory budget exceeded");
+  return cudaFuncSetAttribute(wstream_mma_kernel<FmtPQ2Q8, NB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              mma_smem_bytes<FmtPQ2Q8, NB>());
+}
+
 cudaError_t setup() {
   cudaError_t e = LaunchTable<F>::setup();
+  if (e == cudaSuccess) e = set_q8_smem<1>();
+  if (e == cudaSuccess) e = set_q8_smem<2>();
   if (e == cudaSuccess) e = set_i8_smem<1>();
   if (e == cudaSuccess) e = set_i8_smem<2>();
   if (e == cudaSuccess) e = set_i8_smem<4>();
@@ -169,13 +179,44 @@ cudaError_t launch_i8_rows(const RunParams& p, int m0, const LaunchGeom& g, cuda
   return cudaLaunchKernelEx(&cfg, wstream_kernel<FmtPQ2I8, MB>, q);
 }
 
-// Up to four activation rows per launch (the weights are read once per
-// launch); rows are computed independently of each other with the same
-// instructions and summation order in every instantiation, so a row's bits
-// do not depend on M or on its place in the batch.  Consecutive launches on
-// the stream are ordered by the kernel's grid-dependency wait.
-cudaError_t launch_x_int8(int M, const RunParams& p, const LaunchGeom& g, cudaStream_t s) {
+// Calls with at least this many activation rows run the integer path on the
+// tensor cores (measured: the two-row CUDA-core kernel, one launch, is
+// faster at M = 2; from M = 4 the tensor-core kernel, flat in M, is).
+constexpr int kQ8MinM = 4;
+
+// All M rows of a call on prepared activations (p.x: the codes, p.x_scale)
+// in one launch of the tensor-core kernel (FmtPQ2Q8, the handle's
+// one-CTA-per-SM grid and plan): every code read once per call.
+cudaError_t launch_q8(int M, const RunParams& p, const LaunchGeom& g, cudaStream_t s) {
+  RunParams q = p;
+  q.plan = g.plan;
+  cudaLaunchAttribute attr[1];
+  if (M <= 8) {
+    const cudaLaunchConfig_t cfg =
+        I8::config(g.grid, mma_threads<FmtPQ2Q8, 1>(), mma_smem_bytes<FmtPQ2Q8, 1>(), s, attr);
+    return cudaLaunchKernelEx(&cfg, wstream_mma_kernel<FmtPQ2Q8, 1>, q, M);
+  }
+  const cudaLaunchConfig_t cfg = I8::config(g.grid, mma_threads<FmtPQ2Q8, 2>(), mma_smem_bytes<FmtPQ2Q8, 2>(), s, attr);
+  return cudaLaunchKernelEx(&cfg, wstream_mma_kernel<FmtPQ2Q8, 2>, q, M);
+}
+
+// M < kQ8MinM: the CUDA-core kernel, up to four rows per launch (each row
+// with the same instructions and order in every instantiation).  From
+// kQ8MinM rows (or in batch-invariant mode): the activation prologue into the
+// handle's workspace, then the integer path on the tensor cores -- two
+// launches, the weights read once.  Consecutive launches on the stream are
+// ordered by the kernels' grid-dependency waits.
+cudaError_t launch_x_int8(int M, const RunParams& p, const LaunchGeom& g, cudaStream_t s, bool batch_invariant) {
   if (M < 1 || M > kMaxM) return cudaErrorInvalidValue;
+  if ((M >= kQ8MinM || batch_invariant) && p.xq_ws != nullptr) {
+    cudaError_t e = prepare_x_int8(p.x, M, p.K, nullptr, 0, p.xq_ws, s);
+    if (e != cudaSuccess) return e;
+    RunParams q = p;
+    q.x = reinterpret_cast<const __half*>(p.xq_ws);
+    q.x_scale = reinterpret_cast<const float*>(p.xq_ws + int64_t(M) * p.K);
+    q.x_qsum = reinterpret_cast<const int32_t*>(p.xq_ws + int64_t(M) * p.K + 4 * int64_t(M) * (p.K / 128));
+    return launch_q8(M, q, g, s);
+  }
   int m0 = 0;
   while (m0 < M) {
     const int rem = M - m0;
@@ -208,9 +249,11 @@ cudaError_t launch_xq_rows(const RunParams& p, int m0, const LaunchGeom& g, cuda
   return cudaLaunchKernelEx(&cfg, wstream_kernel<FmtPQ2I8P, MB>, q);
 }
 
-// As launch_x_int8: four, two, then one activation rows per launch.
-cudaError_t launch_xq(int M, const RunParams& p, const LaunchGeom& g, cudaStream_t s) {
+// As launch_x_int8: fewer than kQ8MinM rows on the CUDA-core kernel, more
+// (or batch-invariant mode) in one launch of the tensor-core kernel.
+cudaError_t launch_xq(int M, const RunParams& p, const LaunchGeom& g, cudaStream_t s, bool batch_invariant) {
   if (M < 1 || M > kMaxM) return cudaErrorInvalidValue;
+  if (M >= kQ8MinM || batch_invariant) return launch_q8(M, p, g, s);
   int m0 = 0;
   while (m0 < M) {
     const int rem = M - m0;

@@ -57,12 +57,14 @@ struct FormatOps {
   int m1_ctas_per_sm = 1;           // CTAs per SM of the M = 1 kernel (LaunchGeom::grid_m1)
   int rowgroup = 0;                 // has the M = 1 row-group kernel (rowgroup_kernel.cuh)
   // PQ2_0 only: the run with INT8 activations (qgemv_set_x_int8), else nullptr
-  cudaError_t (*launch_x_int8)(int M, const RunParams& p, const LaunchGeom& g, cudaStream_t s) = nullptr;
+  cudaError_t (*launch_x_int8)(int M, const RunParams& p, const LaunchGeom& g, cudaStream_t s,
+                               bool batch_invariant) = nullptr;
   // one codebook table per row tile, built from per-row codebooks (CBK4_ROW):
   // aux holds cb_entries fp16-sized units per row tile and seg_of_rt[rt] = rt
   int row_tables = 0;
   // PQ2_0 only: the run on prepared INT8 activations (qgemv_run_xq), else nullptr
-  cudaError_t (*launch_xq)(int M, const RunParams& p, const LaunchGeom& g, cudaStream_t s) = nullptr;
+  cudaError_t (*launch_xq)(int M, const RunParams& p, const LaunchGeom& g, cudaStream_t s,
+                           bool batch_invariant) = nullptr;
   // Q4_0, PQ2_0: the fused SiLU(gate) * up run of a GLU handle (qgemv_create_glu), else nullptr
   cudaError_t (*launch_glu)(int M, const RunParams& p, const LaunchGeom& g, cudaStream_t s) = nullptr;
   // formats with the tensor-memory kernel (tc5_kernel.cuh): the smallest M

@@ -84,6 +84,9 @@ struct RunParams {
   // group scales and group code sums, [M][K/128]; null otherwise
   const float* x_scale;
   const int32_t* x_qsum;
+  // PQ2_0 handles in INT8 mode: device workspace for the activation prologue
+  // of runs with several rows (qgemv_xq_bytes(16, K) bytes), or null
+  uint8_t* xq_ws;
 };
 
 // y[idx] = v, plus the residual in one fp32 add (never fused with the

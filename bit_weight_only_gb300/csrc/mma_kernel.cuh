@@ -54,6 +54,20 @@ constexpr int kMmaTiles = 4;  // 16-row m-tiles per warp
 // the start of a slice: only one m-tile's codes are live, at the price of
 // releasing the stage after the last m-tile.  Measured: no slower for AQLM
 // (whose four code words per row would otherwise spill), 7% slower for CBK4.
+// Formats whose activations are INT8 codes with a per-group scale
+// (F::kMmaXCodes: the PQ2_0 integer path on prepared activations): the
+// loader reads the codes and the D columns' scales (F::mma_load_x_q), and a
+// block's sum is multiplied by its column's scale (F::mma_col_scale) before
+// the row's block scale.
+template <class F, class = void>
+struct MmaXCodes {
+  static constexpr bool value = false;
+};
+template <class F>
+struct MmaXCodes<F, decltype(void(F::kMmaXCodes))> {
+  static constexpr bool value = F::kMmaXCodes;
+};
+
 // Formats whose tensor-core kernel has the GLU form (F::kMmaGlu).
 template <class F, class = void>
 struct MmaGluOf {
@@ -338,6 +352,7 @@ __global__ void __launch_bounds__(mma_threads<F, NB, PAR>(), F::mma_ctas(NB)) ws
   int64_t rt = rt_first;
   int kt = static_cast<int>(t0 - rt * p.nKT);
   const bool xvec = (reinterpret_cast<uintptr_t>(p.x) & 15) == 0 && (p.K & 7) == 0;
+  const bool xq_vec = (reinterpret_cast<uintptr_t>(p.x) & 15) == 0;  // INT8: prepared rows of K bytes, K % 128 == 0
   // activation fragments of the thread's B rows m = gi + 8 nb for each of
   // its slices (a tile ahead when PF, else loaded at the top of each tile)
   uint32_t xw[SPW][NB][XW];
@@ -350,7 +365,12 @@ __global__ void __launch_bounds__(mma_threads<F, NB, PAR>(), F::mma_ctas(NB)) ws
     for (int ss = 0; ss < SPW; ++ss) {
       const int64_t kb = static_cast<int64_t>(ktile) * F::kKT + (sgrp * SPW + ss) * F::kKW;
 #pragma unroll
-      for (int nb = 0; nb < NB; ++nb) F::mma_load_x(dst[ss][nb], xrow[nb], p.K, kb, q, xvec);
+      for (int nb = 0; nb < NB; ++nb) {
+        if constexpr (MmaXCodes<F>::value)
+          F::mma_load_x_q(dst[ss][nb], p, M, gi + 8 * nb, 8 * nb + 2 * q, kb, q, xq_vec);
+        else
+          F::mma_load_x(dst[ss][nb], xrow[nb], p.K, kb, q, xvec);
+      }
     }
   };
   const int nKT = static_cast<int>(p.nKT);
@@ -475,6 +495,12 @@ __global__ void __launch_bounds__(mma_threads<F, NB, PAR>(), F::mma_ctas(NB)) ws
                   for (int nb = 0; nb < NB; ++nb) {
                     const int mt = mg + mi;
                     const float d0 = F::mma_scale(d[mt][0], blk), d1 = F::mma_scale(d[mt][1], blk);
+                    if constexpr (MmaXCodes<F>::value) {
+                      // the exact integer sum times the activation column's group scale
+  #pragma unroll
+                      for (int e = 0; e < 4; ++e)
+                        tmp[mi][nb][e] = __fmul_rn(F::mma_col_scale(xw[ss][nb], e & 1), tmp[mi][nb][e]);
+                    }
                     acc[mt][nb][0] = fmaf(d0, tmp[mi][nb][0], acc[mt][nb][0]);
                     acc[mt][nb][1] = fmaf(d0, tmp[mi][nb][1], acc[mt][nb][1]);
                     acc[mt][nb][2] = fmaf(d1, tmp[mi][nb][2], acc[mt][nb][2]);

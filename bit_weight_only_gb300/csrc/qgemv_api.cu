@@ -226,6 +226,7 @@ struct qgemv_ctx {
   int glu;              // qgemv_create_glu: gate and up interleaved, output SiLU(gate) * up
   int skip_cta;         // QGEMV_FAULT_SKIP_CTA test hook, -1 normally
   int tc5_min_m;        // runs of at least this many rows use the tensor-memory kernel (0: never)
+  uint8_t* xq_ws;       // INT8 mode: the activation prologue's workspace (16 rows), allocated when turned on
   qgemv_ctx* mma;       // AQLM: the tensor-core companion (format kAqlmMma), else nullptr
 };
 
@@ -594,6 +595,7 @@ static qgemv::RunParams params_of(const qgemv_ctx* h, const void* x, float* y, c
   p.residual = residual;
   p.x_scale = nullptr;
   p.x_qsum = nullptr;
+  p.xq_ws = h->xq_ws;
   return p;
 }
 
@@ -623,7 +625,7 @@ static int run_impl(qgemv_handle h, const void* x, int M, float* y, const float*
   if (h->mma && (M >= kAqlmMmaMinM || inv)) h = h->mma;  // AQLM: the tensor-core layout
   const qgemv::RunParams p = params_of(h, x, y, residual);
   const qgemv::LaunchGeom g = {h->grid, h->plan, h->grid_m1, h->plan_m1, h->grid_rg, h->tc5_min_m};
-  cudaError_t e = h->x_int8 ? h->ops->launch_x_int8(M, p, g, static_cast<cudaStream_t>(stream))
+  cudaError_t e = h->x_int8 ? h->ops->launch_x_int8(M, p, g, static_cast<cudaStream_t>(stream), inv)
                             : h->ops->launch(M, p, g, static_cast<cudaStream_t>(stream), inv);
   if (e != cudaSuccess) return cuda_error(e, "launching the GEMV kernel");
   return ok();
@@ -650,6 +652,15 @@ int qgemv_set_x_int8(qgemv_handle h, int on) {
   if (!valid(h)) return set_error(QGEMV_ERR_ARG, "invalid handle");
   if (h->ops->launch_x_int8 == nullptr || h->glu)
     return set_error(QGEMV_ERR_ARG, "INT8 activations need a PQ2_0 handle without GLU (format %d)", h->format);
+  if (on && h->xq_ws == nullptr) {  // the prologue's workspace for runs of several rows
+    void* ws = nullptr;
+    const cudaError_t e = cudaMalloc(&ws, static_cast<size_t>(qgemv_xq_bytes(qgemv::kMaxM, h->K)));
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return set_error(QGEMV_ERR_NOMEM, "INT8 activation workspace: %s", cudaGetErrorString(e));
+    }
+    h->xq_ws = static_cast<uint8_t*>(ws);
+  }
   h->x_int8 = on ? 1 : 0;
   return ok();
 }
@@ -687,7 +698,7 @@ int qgemv_run_xq(qgemv_handle h, const void* xq, int M, float* y, const float* r
   p.x_scale = reinterpret_cast<const float*>(base + int64_t(M) * h->K);
   p.x_qsum = reinterpret_cast<const int32_t*>(base + int64_t(M) * h->K + 4 * int64_t(M) * (h->K / 128));
   const qgemv::LaunchGeom g = {h->grid, h->plan, h->grid_m1, h->plan_m1, h->grid_rg, 0};
-  cudaError_t e = h->ops->launch_xq(M, p, g, static_cast<cudaStream_t>(stream));
+  cudaError_t e = h->ops->launch_xq(M, p, g, static_cast<cudaStream_t>(stream), h->batch_invariant != 0);
   if (e != cudaSuccess) return cuda_error(e, "launching the GEMV kernel");
   return ok();
 }
@@ -785,6 +796,7 @@ static void free_handle(qgemv_ctx* h) {
   cudaFree(h->partials);
   cudaFree(h->plan);
   cudaFree(h->err);
+  cudaFree(h->xq_ws);
   h->magic = 0;
   delete h;
 }

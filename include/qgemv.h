@@ -203,13 +203,20 @@ int qgemv_set_batch_invariant(qgemv_handle h, int on);
  * the quantized activations: lossy against qgemv_run with the mode off (the
  * quantization error is a property of the method, at most half a step of
  * each group's scale per nonzero weight), and accurate to the usual fp32
- * bound against the exact integer-path value.  Up to four activation rows
- * share a launch (the weights are read once per launch); every row is
- * computed with the same instructions and summation order whatever M, so a
- * row's bits never depend on M or on its place in the batch.  Works with
- * qgemv_run and qgemv_run_residual; takes effect for runs issued after the
- * call.  Returns QGEMV_ERR_ARG for an invalid handle or a handle that is not
- * PQ2_0 (stacked PQ2_0 handles are accepted).                               */
+ * bound against the exact integer-path value.  Up to three activation rows
+ * run the CUDA-core kernel (DP4A inner sums, up to four rows per launch);
+ * four or more run, in one call, the quantizer of qgemv_prepare_x_int8 into
+ * a handle-owned workspace and one launch of the tensor-core kernel (the
+ * INT8 codes as exact fp16 operands, exact integer block sums), so the
+ * weights are read once per call.  A row's bits are the same in every call
+ * of up to three rows and in every call of four or more; the two kernels
+ * may differ in the last places (same bound) unless batch-invariant mode is
+ * on, which puts every M on the tensor-core kernel.  Works with qgemv_run and qgemv_run_residual; takes
+ * effect for runs issued after the call.  The first call that turns the mode
+ * on allocates the workspace (qgemv_xq_bytes(16, K) bytes, freed with the
+ * handle): QGEMV_ERR_NOMEM if that fails.  Returns QGEMV_ERR_ARG for an
+ * invalid handle or a handle that is not PQ2_0 (stacked PQ2_0 handles are
+ * accepted).                                                                */
 int qgemv_set_x_int8(qgemv_handle h, int on);
 
 /* The INT8 activation quantizer of the PQ2_0 integer path, on the device:
@@ -256,8 +263,10 @@ int qgemv_prepare_x_int8(const void* x, int M, int64_t K, const int8_t* signs, i
 
 /* y = residual + (prepared INT8 activations) . dequant(W)^T for a PQ2_0
  * handle: the integer path of qgemv_set_x_int8 on codes from
- * qgemv_prepare_x_int8 (with the same M and the handle's K).  With
- * hadamard_block = 0 the result equals qgemv_run in INT8 mode bit for bit.
+ * qgemv_prepare_x_int8 (with the same M and the handle's K): up to three
+ * rows on the CUDA-core kernel, four or more in one launch of the
+ * tensor-core kernel (as for qgemv_set_x_int8).  With hadamard_block = 0 the result equals qgemv_run in INT8 mode
+ * bit for bit.
  * residual may be NULL (plain store) or y itself.  The handle's INT8 mode
  * setting does not matter here.  Asynchronous; as qgemv_run otherwise.     */
 int qgemv_run_xq(qgemv_handle h, const void* xq, int M, float* y, const float* residual, void* stream);

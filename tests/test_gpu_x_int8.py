@@ -98,22 +98,68 @@ def test_int8_on_grid_activations_reach_the_exact_gemv():
     assert oracle.within_tolerance(y.cpu().numpy(), y_ref, bound).all()
 
 
-@pytest.mark.parametrize("M", [2, 5, 16])
-def test_int8_rows_do_not_depend_on_M(M):
+@pytest.mark.parametrize("M", [2, 3, 5, 16])
+@pytest.mark.parametrize("inv", [False, True])
+def test_int8_rows_do_not_depend_on_M(M, inv):
+    """Up to three rows run the CUDA-core kernel (every row alone, the same
+    instructions in every instantiation); four or more the tensor-core
+    kernel, which computes every row as its own MMA column in one order.  So
+    a row's bits are the same in every call on the same kernel; across the
+    two they may differ within the bound, unless batch-invariant mode puts
+    every M on the tensor-core kernel."""
     N, K = 700, 2304
     packed, _, _ = make_case("pq2_0", N, K, tag="i8m")
     x_np = make_x(M, K, tag="i8m")
     h = qgemv.QGemv("pq2_0", N, K, packed)
     h.set_x_int8(True)
+    if inv:
+        h.set_batch_invariant(True)
     x = torch.from_numpy(x_np).cuda()
     y = h.gemv(x)
     torch.cuda.synchronize()
+    assert h.status() == qgemv.QGEMV_OK
     y_ref, bound = oracle.gemv_pq2_int8(N, K, packed, x_np)
     assert oracle.within_tolerance(y.cpu().numpy(), y_ref, bound).all()
     for m in sorted({0, M // 2, M - 1}):
-        y1 = h.gemv(x[m:m + 1])
+        y4 = h.gemv(x[[m, m, m, m]])  # the tensor-core kernel
+        y1 = h.gemv(x[m:m + 1])       # the CUDA-core kernel (tensor-core in batch-invariant mode)
         torch.cuda.synchronize()
-        assert torch.equal(y1[0], y[m]), f"row {m} of M={M} differs from its one-row call"
+        y1_ref, b1 = oracle.gemv_pq2_int8(N, K, packed, x_np[m:m + 1])
+        assert oracle.within_tolerance(y1.cpu().numpy(), y1_ref, b1).all()
+        assert oracle.within_tolerance(y4.cpu().numpy(), np.repeat(y1_ref, 4, axis=0), np.repeat(b1, 4, axis=0)).all()
+        same = y4 if (M >= 4 or inv) else y1
+        assert torch.equal(same[0], y[m]), f"row {m} of M={M} differs from the same kernel's other call"
+        if inv:
+            assert torch.equal(y1[0], y[m]) and torch.equal(y4[0], y[m])
+
+
+@pytest.mark.parametrize("N,K", [(300, 1280), (5120, 17408), (34816, 5120)])
+@pytest.mark.parametrize("M", [3, 8, 9, 16])
+def test_int8_tensor_core_rows_match_oracle(N, K, M):
+    """Several activation rows: the prologue and the INT8 tensor-core kernel,
+    at ragged and full sizes, against the exact integer-path value."""
+    if N * K > (1 << 24):
+        packed_dev = inputs.pq2_packed_cuda(f"i8tc/{N}x{K}", N, K)
+        packed = packed_dev.cpu().numpy()
+        h = qgemv.QGemv("pq2_0", N, K, packed_dev)
+        del packed_dev
+        rows = np.unique(np.concatenate([[0, 1, 127, 128, N // 2, N - 1],
+                                         np.random.default_rng(3).integers(0, N, 40)]))
+    else:
+        packed, _, _ = make_case("pq2_0", N, K, tag="i8tc")
+        h = qgemv.QGemv("pq2_0", N, K, packed)
+        rows = None
+    x_np = _special_x(M, K, tag="i8tc")
+    h.set_x_int8(True)
+    y = h.gemv(torch.from_numpy(x_np).cuda()).cpu().numpy()
+    assert h.status() == qgemv.QGEMV_OK
+    if rows is not None:
+        y = y[:, rows]
+        y_ref, bound = oracle.gemv_pq2_int8(rows.size, K, packed.reshape(N, -1)[rows], x_np)
+    else:
+        y_ref, bound = oracle.gemv_pq2_int8(N, K, packed, x_np)
+    ok = oracle.within_tolerance(y, y_ref, bound)
+    assert ok.all(), f"{N}x{K} M={M}: {np.count_nonzero(~ok)} outputs out of tolerance"
 
 
 def test_int8_residual_is_plain_plus_residual():
@@ -209,7 +255,8 @@ def test_prepared_activations_match_oracle(B, M, K):
 
 
 @pytest.mark.parametrize("B", [0, 1024])
-@pytest.mark.parametrize("N,K,M", [(700, 2048, 1), (5120, 17408, 1), (34816, 5120, 2), (700, 3072, 5)])
+@pytest.mark.parametrize("N,K,M", [(700, 2048, 1), (5120, 17408, 1), (34816, 5120, 2), (700, 3072, 5),
+                                   (700, 3072, 16)])
 def test_run_xq_matches_oracle(B, N, K, M):
     h, packed = _pq2_handle(N, K, "i8xq")
     x_np = make_x(M, K, tag="i8xq")
