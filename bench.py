@@ -498,7 +498,7 @@ def run_ours(args, rank, world, device):
                                 if args.x_int8
                                 else "aqlm1x16_kernel (codebook entries gathered from L2: a 32-byte sector "
                                      "per group of 8 weights bounds it before HBM does)" if dominant == "aqlm_1x16"
-                                else "wstream_kernel<FmtCBK4R, MB>, MB = 2, 1 activation rows per launch"
+                                else "wstream_kernel<FmtCBK4R, MB>, MB = 8, 2, 1 activation rows per launch"
                                 if dominant == "cbk4_row"
                                 else "rowcb8_kernel<MB> (one warp per row, its codebook in shared memory)"
                                 if dominant == "cbk8_row"
@@ -519,9 +519,9 @@ def run_ours(args, rank, world, device):
         # one launch per GEMV (AQLM: one table pass for M <= 2, else the
         # tensor-core kernel; the fused SiLU(gate)*up one for every M); the
         # INT8 path with several rows adds its activation prologue; CBK4_ROW
-        # launches once per 2 or 1 rows
+        # launches once per 8, 2 or 1 rows
         "gpu_launches": sum((x_int8_launches(M, "xq" in o) + (1 if "xq" in o else 0)) if o.get("x_int8") else
-                            (M + 1) // 2 if o["fmt"] == "cbk4_row" else
+                            (M // 8 + (M % 8) // 2 + M % 2) if o["fmt"] == "cbk4_row" else
                             1 for o in ops) * K,
         "clocks": clocks,
     }

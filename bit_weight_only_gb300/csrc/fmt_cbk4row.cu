@@ -8,10 +8,11 @@
 // so the CUDA-core kernel rebuilds its shared table at every row tile.
 //
 // The weights are fp32 centroids, which the f16 tensor-core path cannot
-// take exactly, so every M runs the CUDA-core kernel: one or two activation
-// rows per launch (the weights are read once per launch).  Each row's
-// arithmetic is the same in both instantiations, so a row's bits do not
-// depend on M.
+// take exactly, so every M runs the CUDA-core kernel: eight, two or one
+// activation rows per launch (the weights are read once per launch).  A
+// row's arithmetic is the same in the one- and two-row instantiations;
+// the eight-row one adds the slices in another order (batch-invariant mode
+// does not use it).
 #include "fmt_cbk.cuh"
 #include "formats.h"
 #include "launch_table.cuh"
@@ -70,11 +71,14 @@ cudaError_t set_smem() {
 cudaError_t setup() {
   cudaError_t e = set_smem<1>();
   if (e == cudaSuccess) e = set_smem<2>();
+  if (e == cudaSuccess) e = set_smem<8>();
   if (e == cudaSuccess) e = LaunchTable<F>::setup_glu();
   return e;
 }
 
-int smem_bytes(int M) { return M == 1 ? gemv_smem_bytes<F, 1>() : gemv_smem_bytes<F, 2>(); }
+int smem_bytes(int M) {
+  return M == 1 ? gemv_smem_bytes<F, 1>() : (M < 8 ? gemv_smem_bytes<F, 2>() : gemv_smem_bytes<F, 8>());
+}
 
 template <int MB>
 cudaError_t launch_rows(const RunParams& p, int m0, const LaunchGeom& g, cudaStream_t s) {
@@ -89,12 +93,18 @@ cudaError_t launch_rows(const RunParams& p, int m0, const LaunchGeom& g, cudaStr
   return cudaLaunchKernelEx(&cfg, wstream_kernel<F, MB>, q);
 }
 
-// Two activation rows per launch, one for an odd last row.
-cudaError_t launch(int M, const RunParams& p, const LaunchGeom& g, cudaStream_t s, bool) {
+// Eight activation rows per launch while eight remain (eight warps, one per
+// slice, 248 registers), then two, then one for an odd last row (sixteen
+// warps in tile parity).  The two geometries add a row's slices in
+// different orders; batch-invariant mode keeps to the second, so that a
+// row's bits never depend on M.
+cudaError_t launch(int M, const RunParams& p, const LaunchGeom& g, cudaStream_t s, bool batch_invariant) {
   if (M < 1 || M > kMaxM) return cudaErrorInvalidValue;
   for (int m0 = 0; m0 < M;) {
-    const int mb = M - m0 >= 2 ? 2 : 1;
-    const cudaError_t e = mb == 2 ? launch_rows<2>(p, m0, g, s) : launch_rows<1>(p, m0, g, s);
+    const int mb = (M - m0 >= 8 && !batch_invariant) ? 8 : (M - m0 >= 2 ? 2 : 1);
+    const cudaError_t e = mb == 8   ? launch_rows<8>(p, m0, g, s)
+                          : mb == 2 ? launch_rows<2>(p, m0, g, s)
+                                    : launch_rows<1>(p, m0, g, s);
     if (e != cudaSuccess) return e;
     m0 += mb;
   }

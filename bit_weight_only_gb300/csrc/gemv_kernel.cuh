@@ -191,17 +191,30 @@ constexpr int kTableAlign = 65536;
 constexpr int kTablePreSlack = 4096;  // room left for the window offset of the dynamic area
 
 template <class F, int M>
+__host__ __device__ constexpr int gemv_red_bytes() { return red_slots<F, M>() * kTileRows * acc_stride(M) * 4; }
+
+// Table formats whose pre-table part would not fit with the reduction slots
+// (several activation rows) place the slots after the last stage instead.
+template <class F, int M>
+__host__ __device__ constexpr bool gemv_red_post() {
+  return F::kSharedBytes != 0 && F::kTileBytes + kSlices * wps_for<F>(M) * (F::kKW / 2) * mpad(M) * 8 +
+                                         gemv_red_bytes<F, M>() + (2 * F::stages(M) * 8 + 127) / 128 * 128 +
+                                         kTablePreSlack > kTableAlign;
+}
+
+template <class F, int M>
 __host__ __device__ constexpr int gemv_pre_bytes() {
   return F::kTileBytes                                             // stage 0
          + kSlices * wps_for<F>(M) * (F::kKW / 2) * mpad(M) * 8   // x pairs, per warp
-         + red_slots<F, M>() * kTileRows * acc_stride(M) * 4       // cross-slice reduction
+         + (gemv_red_post<F, M>() ? 0 : gemv_red_bytes<F, M>())   // cross-slice reduction
          + (2 * F::stages(M) * 8 + 127) / 128 * 128;               // mbarriers (stage 1 stays 128-aligned)
 }
 
 template <class F, int M>
 __host__ __device__ constexpr int gemv_smem_bytes() {
   return F::kSharedBytes == 0 ? gemv_pre_bytes<F, M>() + (F::stages(M) - 1) * F::kTileBytes
-                              : kTableAlign + F::kSharedBytes + (F::stages(M) - 1) * F::kTileBytes;
+                              : kTableAlign + F::kSharedBytes + (F::stages(M) - 1) * F::kTileBytes +
+                                    (gemv_red_post<F, M>() ? gemv_red_bytes<F, M>() : 0);
 }
 
 template <class F, int M>
@@ -454,8 +467,8 @@ __global__ void __launch_bounds__(gemv_threads<F, M>(), F::kCtasPerSm) wstream_k
   // stage s at ring0 (s = 0) or ringN + (s - 1) TB
   uint8_t* ring0 = smem;
   float* xs_all = reinterpret_cast<float*>(smem + TB);
-  float* red = xs_all + kSlices * WPS * XS_FLOATS;
-  uint64_t* full = reinterpret_cast<uint64_t*>(red + red_slots<F, M>() * kTileRows * RS);
+  float* red = xs_all + kSlices * WPS * XS_FLOATS;  // or after the last stage (gemv_red_post)
+  uint64_t* full = reinterpret_cast<uint64_t*>(gemv_red_post<F, M>() ? red : red + red_slots<F, M>() * kTileRows * RS);
   uint8_t* ringN;
   uint8_t* fsh;
   __shared__ volatile int s_abort;
@@ -474,12 +487,13 @@ __global__ void __launch_bounds__(gemv_threads<F, M>(), F::kCtasPerSm) wstream_k
     asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
     const uint32_t R0 = (base + (kTableAlign - 1)) & ~uint32_t(kTableAlign - 1);
     if (R0 - base < uint32_t(gemv_pre_bytes<F, M>()) ||
-        R0 + kTableAlign + (NS - 1) * TB > base + dyn) {
+        R0 + kTableAlign + (NS - 1) * TB + (gemv_red_post<F, M>() ? gemv_red_bytes<F, M>() : 0) > base + dyn) {
       if (threadIdx.x == 0) atomicOr(p.err, kErrSmemLayout);
       return;
     }
     fsh = smem + (R0 - base);
     ringN = fsh + kTableAlign;
+    if constexpr (gemv_red_post<F, M>()) red = reinterpret_cast<float*>(ringN + (NS - 1) * TB);
   }
   uint64_t* empty = full + NS;
   auto stage_ptr = [&](int st) { return st == 0 ? ring0 : ringN + (st - 1) * TB; };

@@ -74,8 +74,11 @@ typedef enum {
    * codebook per output channel, stored in fp32): packed = uint8 [N][K/2]
    * as QGEMV_CBK4; codebooks = fp32 [N][16], row n's centroids together
    * (64 bytes per row); K % 2 == 0; scales = NULL.  Every M runs the
-   * CUDA-core kernel (fp32 centroids), at most two activation rows per
-   * launch; a row's bits do not depend on M.                               */
+   * CUDA-core kernel (fp32 centroids), eight activation rows per launch
+   * while eight remain, then two, then one; a row's bits do not depend on M
+   * in batch-invariant mode (which keeps to the two- and one-row launches),
+   * and otherwise differ at most in the last places between calls below and
+   * above eight rows.                                                      */
   QGEMV_CBK4_ROW = 8,
   /* CBK8 with one codebook per output row, the 8-bit LM head of the same
    * files (256 fp32 centroids per row): packed = uint8 [N][K]; codebooks =

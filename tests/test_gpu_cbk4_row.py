@@ -52,7 +52,7 @@ def test_dequant_bit_exact(N, K):
 
 
 @pytest.mark.parametrize("N,K", [(300, 2050), (129, 2), (700, 4096), (1000, 1024)])
-@pytest.mark.parametrize("M", [1, 2, 3, 16])
+@pytest.mark.parametrize("M", [1, 2, 3, 8, 11, 16])
 def test_gemv_matches_oracle(N, K, M):
     packed, _, cb = make_case(FMT, N, K, tag="c4r")
     h = qgemv.QGemv(FMT, N, K, packed, None, cb)
@@ -83,11 +83,28 @@ def test_full_size_sampled_rows(N, K):
         assert ok.all(), f"{N}x{K} M={M}: {np.count_nonzero(~ok)} sampled outputs out of tolerance"
 
 
-def test_rows_do_not_depend_on_M():
+@pytest.mark.parametrize("inv", [True, False])
+def test_rows_do_not_depend_on_M(inv):
+    """Batch-invariant mode: a row's bits never depend on M.  Otherwise calls
+    of eight or more rows run the eight-row launches (another slice order):
+    their rows agree among themselves, and with fewer-row calls within the
+    bound."""
     N, K = 700, 4096
     packed, _, cb = make_case(FMT, N, K, tag="c4rinv")
     h = qgemv.QGemv(FMT, N, K, packed, None, cb)
-    x = torch.from_numpy(make_x(16, K, tag="c4rinv")).cuda()
+    x_np = make_x(16, K, tag="c4rinv")
+    x = torch.from_numpy(x_np).cuda()
+    if not inv:
+        y16 = h.gemv(x)
+        y8 = h.gemv(x[8:])
+        y3 = h.gemv(x[:3])
+        torch.cuda.synchronize()
+        assert torch.equal(y8, y16[8:])
+        y_ref, bound = oracle.gemv(FMT, N, K, packed, None, cb, x_np)
+        assert oracle.within_tolerance(y16.cpu().numpy(), y_ref, bound).all()
+        assert oracle.within_tolerance(y3.cpu().numpy(), y_ref[:3], bound[:3]).all()
+        return
+    h.set_batch_invariant(True)
     y16 = h.gemv(x)
     for M in (1, 2, 3, 5):
         yM = h.gemv(x[:M])
