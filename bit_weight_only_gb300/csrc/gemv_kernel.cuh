@@ -62,7 +62,8 @@ struct CtaPlan {
   int32_t seg_S[2];      // number of contributors
   int32_t seg_r0[2];     // this CTA's slice of the rows: [r0, r0 + nr)
   int32_t seg_nr[2];
-  int32_t seg_side1[2];  // 1: the first contributor's run began earlier (its side-1 slot)
+  int32_t seg_flags[2];  // bit 0: the first contributor's run began earlier (its side-1 slot);
+                         // bit 1: this CTA finishes the whole row tile (kWholeFinishItems)
 };
 static_assert(sizeof(CtaPlan) == 64, "CtaPlan is copied in 16-byte pieces");
 
@@ -220,6 +221,25 @@ __host__ __device__ constexpr int gemv_smem_bytes() {
 template <class F, int M>
 __host__ __device__ constexpr int gemv_threads() { return 32 * kSlices * wps_for<F>(M); }
 
+// Rows of shared row tile sg (of `rows`) that this CTA finishes.  When the
+// whole tile is at most kWholeFinishItems items (rows x activation rows),
+// one contributor finishes it alone: the one whose part of the row tile
+// closes its run last (its plan flag), so that no CTA waits for a partial
+// written at the end of another CTA's run except that one -- a contributor
+// whose part opens its run stored it long before.  Larger tiles are split
+// into the plan's even row slices over all contributors.  Every contributor
+// of a segment decides alike (the rule depends on rows and mrows only).
+constexpr int kWholeFinishItems = 256;
+__device__ __forceinline__ void finish_slice(const CtaPlan& pl, int sg, int rows, int mrows, int& r0, int& nr) {
+  if (rows * mrows <= kWholeFinishItems) {
+    r0 = 0;
+    nr = (pl.seg_flags[sg] & 2) ? rows : 0;
+  } else {
+    r0 = pl.seg_r0[sg];
+    nr = pl.seg_nr[sg];
+  }
+}
+
 // Finish one shared row tile (ROWS output rows) as described by a CtaPlan
 // segment: sum rows [r0, r0 + nr) of each activation row over the S
 // contributors starting at CTA cf.  A partial slot holds the empty mark (all
@@ -238,15 +258,15 @@ __device__ __forceinline__ void finish_rows(const RunParams& p, int64_t stride, 
   const int64_t rt = pl.seg_rt[sg];
   const int64_t cf = pl.seg_cf[sg];
   const int S = pl.seg_S[sg];
-  const int r0 = pl.seg_r0[sg];
-  const int nr = pl.seg_nr[sg];
-  if (nr <= 0) return;  // more contributors than rows: this one has no slice
+  int r0, nr;
+  finish_slice(pl, sg, ROWS, mrows, r0, nr);
+  if (nr <= 0) return;  // another contributor finishes these rows
   constexpr int B = M > 8 ? 8 : 16;  // slots polled at once (registers)
   const int items = nr * mrows;
   const int H = (S <= 16 || items >= NT) ? 1 : NT / items;
   const int cpt = H == 1 ? S : (S + H - 1) / H;
   // slot of contributor cf + i: side 1 only for the first one, if its run began earlier
-  const float* first_slot = p.partials + (cf * 2 + (pl.seg_side1[sg] ? 1 : 0)) * stride;
+  const float* first_slot = p.partials + (cf * 2 + (pl.seg_flags[sg] & 1)) * stride;
   const float* base = p.partials + cf * 2 * stride;
   for (int t = tid; t < items * H; t += NT) {
     const int item = H == 1 ? t : t / H;
@@ -330,15 +350,18 @@ __device__ __forceinline__ void finish_segment(const RunParams& p, int64_t strid
     finish_rows<ROWS, M, NT>(p, stride, pl, sg, row_scales, out_scale, s_sub, tid, mrows);
 }
 
-// Finish the CTA's shared row tiles (the two plan segments).  When it has
-// two and neither needs the split-contributor sums (S <= 16), half the
-// threads take each, so that the two waits for other CTAs' partials overlap
-// instead of adding up.
+// Finish the CTA's shared row tiles (the two plan segments) that it has
+// rows of.  When it has two and neither needs the split-contributor sums
+// (S <= 16), half the threads take each, so that the two waits for other
+// CTAs' partials overlap instead of adding up.
 template <int ROWS, int M, int NT>
 __device__ __forceinline__ void finish_all(const RunParams& p, int64_t stride, const CtaPlan& pl,
                                            const __half* row_scales, float out_scale, float* s_sub, int tid,
                                            int mrows = M) {
-  const bool s0 = pl.seg_rt[0] >= 0, s1 = pl.seg_rt[1] >= 0;
+  int r0, nr0, nr1;
+  finish_slice(pl, 0, ROWS, mrows, r0, nr0);
+  finish_slice(pl, 1, ROWS, mrows, r0, nr1);
+  const bool s0 = pl.seg_rt[0] >= 0 && nr0 > 0, s1 = pl.seg_rt[1] >= 0 && nr1 > 0;
   if (s0 && s1 && pl.seg_S[0] <= 16 && pl.seg_S[1] <= 16) {
     const int sg = tid < NT / 2 ? 0 : 1;
     finish_segment<ROWS, M, NT / 2>(p, stride, pl, sg, row_scales, out_scale, s_sub, tid - sg * (NT / 2), mrows);
@@ -383,10 +406,10 @@ __device__ __noinline__ void finish_rows_glu(const RunParams& p, const CtaPlan& 
   const int64_t rt = pl.seg_rt[sg];
   const int64_t cf = pl.seg_cf[sg];
   const int S = pl.seg_S[sg];
-  const int r0 = pl.seg_r0[sg];
-  const int nr = pl.seg_nr[sg];
+  int r0, nr;
+  finish_slice(pl, sg, kTileRows / 2, mrows, r0, nr);
   if (nr <= 0) return;
-  float* first_slot = p.partials + (cf * 2 + (pl.seg_side1[sg] ? 1 : 0)) * kPartialStride;
+  float* first_slot = p.partials + (cf * 2 + (pl.seg_flags[sg] & 1)) * kPartialStride;
   float* base = p.partials + cf * 2 * kPartialStride;
   bool gave_up = false;
   for (int t = tid; t < nr * mrows; t += NT) {
@@ -440,6 +463,63 @@ __device__ __forceinline__ const uint16_t* table_of(const RunParams& p, int64_t 
   return static_cast<const uint16_t*>(p.aux) + (p.seg_of_rt != nullptr ? rt * F::kCbEntries : 0);
 }
 
+// Stacked table handles: the segment of the table built in shared memory
+// (seg[0]), and the segment and codebook of the row tile after it (seg[1],
+// cb), staged with cp.async ahead of time.  A global load at a row-tile
+// change would stall the CTA for a loaded-memory round trip (over a
+// microsecond while the weight stream saturates HBM), and the launch lasts
+// as long as its latest CTA.  Codebooks of up to 256 entries are staged;
+// larger ones (the per-row codebooks of a row tile, 8 KB) are read from
+// global memory by the rebuild.
+template <class F>
+constexpr bool kStagedCb = F::kCbEntries > 0 && F::kCbEntries <= 256;
+
+template <class F>
+struct alignas(16) NextTable {
+  int seg[2];
+  int pad[2];
+  uint16_t cb[kStagedCb<F> ? F::kCbEntries : 8];
+};
+
+// Stage the segment and codebook of row tile rt + 1 (rt itself if it is the
+// last), and with first also rt's segment.  Threads 0 .. E/8 - 1 copy the
+// codebook in 16-byte pieces, thread E/8 the segment numbers; every thread
+// runs cp.async.wait_all and a barrier (advance_table) before any read.
+template <class F>
+__device__ __forceinline__ void prefetch_next_table(NextTable<F>* s, const RunParams& p, int64_t rt,
+                                                    int64_t nRT, bool first, int tid) {
+  constexpr int kPieces = kStagedCb<F> ? F::kCbEntries * 2 / 16 : 0;
+  static_assert(kPieces * 16 == (kStagedCb<F> ? F::kCbEntries * 2 : 0), "codebook in 16-byte pieces");
+  const int64_t rn = rt + 1 < nRT ? rt + 1 : rt;
+  if (tid < kPieces) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n\tcp.async.commit_group;"
+                 ::"r"(smem_u32(s->cb + 8 * tid)), "l"(table_of<F>(p, rn) + 8 * tid) : "memory");
+  } else if (tid == kPieces) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(&s->seg[1])), "l"(p.seg_of_rt + rn)
+                 : "memory");
+    if (first)
+      asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(&s->seg[0])), "l"(p.seg_of_rt + rt)
+                   : "memory");
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  }
+}
+
+// At a row-tile change of a stacked handle (every thread; rt = the new row
+// tile): rebuild the table from the staged codebook if the segment changes,
+// then stage the next one.  Starts with a barrier (every warp is done with
+// the old table) and leaves the staged data consumed.
+template <class F, int NT, class Rebuild>
+__device__ __forceinline__ void advance_table(NextTable<F>* s, const RunParams& p, int64_t rt, int tid,
+                                              Rebuild&& rebuild) {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  __syncthreads();
+  const int cur = s->seg[0], nxt = s->seg[1];
+  if (nxt != cur) rebuild(kStagedCb<F> ? s->cb : table_of<F>(p, rt));
+  __syncthreads();  // every thread has read s
+  if (tid == 0) s->seg[0] = nxt;
+  prefetch_next_table<F>(s, p, rt, div_fast(p.T, p.nKT), false, tid);
+}
+
 // Table rebuild at a segment change of a stacked handle: rare, so out of
 // line, keeping the main loop's register allocation as without stacking.
 template <class F, int NT>
@@ -472,7 +552,7 @@ __global__ void __launch_bounds__(gemv_threads<F, M>(), F::kCtasPerSm) wstream_k
   uint8_t* ringN;
   uint8_t* fsh;
   __shared__ volatile int s_abort;
-  __shared__ int s_seg[2];
+  __shared__ NextTable<F> s_next;
   __shared__ __align__(16) CtaPlan s_plan;
 
   if (static_cast<int>(blockIdx.x) == p.skip_cta) return;  // test hook (QGEMV_FAULT_SKIP_CTA)
@@ -510,8 +590,14 @@ __global__ void __launch_bounds__(gemv_threads<F, M>(), F::kCtasPerSm) wstream_k
   const int64_t rt_first = div_fast(t0, p.nKT);
 
   // The elected thread initializes the barriers and at once starts filling
-  // the ring NS - 1 tiles ahead of the math, so the first tiles are in
-  // flight while the CTA builds the format's tables.
+  // the ring NS - 1 tiles ahead of the math (with tile parity: the first
+  // tile of each half), so the first tiles are in flight while the CTA
+  // builds the format's tables.  With tile parity the stages after those
+  // two are filled from the main loop: every tile issued before the grid
+  // dependency resolves queues in HBM ahead of the first copies of the CTAs
+  // that start last (those on the SMs the previous launch left last), and
+  // the launch lasts as long as its latest CTA.
+  constexpr int kPre = PAR ? 2 : NS - 1;
   const int64_t ntiles = t1 - t0;
   const bool elected = (tid == 0);
   uint64_t pol = 0;
@@ -524,7 +610,7 @@ __global__ void __launch_bounds__(gemv_threads<F, M>(), F::kCtasPerSm) wstream_k
     s_abort = 0;
     fence_mbarrier_init();
     pol = l2_policy_evict_first();
-    for (; n_issued < (PAR ? NS : NS - 1) && n_issued < ntiles; ++n_issued) {
+    for (; n_issued < kPre && n_issued < ntiles; ++n_issued) {
       mbar_arrive_expect_tx(&full[n_issued], TB);
       bulk_g2s(stage_ptr(static_cast<int>(n_issued)), p.tiles + (t0 + n_issued) * TB, TB, &full[n_issued], pol);
     }
@@ -532,14 +618,10 @@ __global__ void __launch_bounds__(gemv_threads<F, M>(), F::kCtasPerSm) wstream_k
   fetch_plan(&s_plan, p.plan, c, tid);
   // Table formats keep one codebook copy per row tile in aux (stacked
   // handles hold several codebooks); the first row tile's needs no lookup.
-  // Stacked handles (several codebooks): s_seg = segment of the table in
-  // shared memory and of the row tile after it, kept by thread 0.
+  // Stacked handles stage the next row tile's segment and codebook.
   if constexpr (F::kCbEntries > 0) {
-    if (p.seg_of_rt != nullptr && tid == 0 && ntiles > 0) {
-      const int64_t nRT = div_fast(p.T, p.nKT);
-      s_seg[0] = __ldg(p.seg_of_rt + rt_first);
-      s_seg[1] = rt_first + 1 < nRT ? __ldg(p.seg_of_rt + rt_first + 1) : s_seg[0];
-    }
+    if (p.seg_of_rt != nullptr && ntiles > 0)
+      prefetch_next_table<F>(&s_next, p, rt_first, div_fast(p.T, p.nKT), true, tid);
   }
   F::template init_shared<NT>(fsh, table_of<F>(p, rt_first), warp, lane);
   __syncthreads();
@@ -581,14 +663,9 @@ __global__ void __launch_bounds__(gemv_threads<F, M>(), F::kCtasPerSm) wstream_k
   // A new row tile of a stacked handle may use another codebook: rebuild
   // the table once every warp is done with the old one.
   auto next_table = [&]() {
-    __syncthreads();  // every warp is done with the old table and has read s_seg
-    if (s_seg[1] != s_seg[0]) rebuild_table<F, NT>(fsh, table_of<F>(p, rt), warp, lane);
-    __syncthreads();
-    if (tid == 0) {
-      const int64_t nRT = div_fast(p.T, p.nKT);
-      s_seg[0] = s_seg[1];
-      s_seg[1] = rt + 1 < nRT ? __ldg(p.seg_of_rt + rt + 1) : s_seg[0];
-    }
+    if constexpr (F::kCbEntries > 0)
+      advance_table<F, NT>(&s_next, p, rt, tid,
+                           [&](const uint16_t* cb) { rebuild_table<F, NT>(fsh, cb, warp, lane); });
   };
 
   // The warp's part of tile j (stage st, fill parity par): stage its x,
@@ -663,14 +740,16 @@ __global__ void __launch_bounds__(gemv_threads<F, M>(), F::kCtasPerSm) wstream_k
     // Tile parity: tile j lives in stage j % NS and is computed by half
     // j % 2, so (NS even) each half owns every second stage.  Each half runs
     // its own pipeline over its own tiles: at its tile j its first thread
-    // refills the stage of its tile j - 2 (released one tile ago) with tile
-    // j + NS - 2.  The prologue issued tiles 0 .. NS - 1.  Both halves walk
-    // the run row tile by row tile and meet at each row-tile end.
+    // fills the stage of its tile j - 2 (released one tile ago; for j < 2 a
+    // stage not used yet) with tile j + NS - 2.  The prologue issued tiles
+    // 0 and 1.  Both halves walk the run row tile by row tile and meet at
+    // each row-tile end.
     static_assert(NS % 2 == 0 && NS >= 4, "tile parity: each half owns every second stage");
+    static_assert(kPre == 2, "the main loop fills stages 2 .. NS - 1 first");
     const bool leader = (lane == 0) && (slice == 0);
     const uint64_t lpol = leader ? l2_policy_evict_first() : 0;
     int u_last = -1;  // leader: last tile of its parity issued (by the prologue or by itself)
-    for (int u = half; u < NS && u < nt; u += 2) u_last = u;
+    for (int u = half; u < kPre && u < nt; u += 2) u_last = u;
     int i = 0;  // first tile of the current row tile segment
     while (i < nt) {
       if (stacked && i > 0) next_table();
@@ -679,9 +758,9 @@ __global__ void __launch_bounds__(gemv_threads<F, M>(), F::kCtasPerSm) wstream_k
       for (int j = i + ((i ^ half) & 1); j < iend; j += 2) {
         bool abort = s_abort != 0;
         const int u = j + NS - 2;
-        if (leader && !abort && j >= 2 && u < nt) {
+        if (leader && !abort && u < nt) {
           const int su = u % NS;
-          if (!mbar_wait_bounded(&empty[su], static_cast<uint32_t>(((u - NS) / NS) & 1))) {
+          if (u >= NS && !mbar_wait_bounded(&empty[su], static_cast<uint32_t>(((u - NS) / NS) & 1))) {
             atomicOr(p.err, kErrTimeoutEmpty);
             s_abort = 1;
             abort = true;

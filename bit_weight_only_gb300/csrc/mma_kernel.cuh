@@ -297,7 +297,7 @@ __global__ void __launch_bounds__(mma_threads<F, NB, PAR>(), F::mma_ctas(NB)) ws
   uint64_t* empty = full + NS;
   auto stage_ptr = [&](int64_t s) { return s == 0 ? ring0 : ringN + (s - 1) * TB; };
   __shared__ volatile int s_abort;
-  __shared__ int s_seg[2];
+  __shared__ NextTable<F> s_next;
   __shared__ __align__(16) CtaPlan s_plan;
 
   const int tid = threadIdx.x;
@@ -328,18 +328,18 @@ __global__ void __launch_bounds__(mma_threads<F, NB, PAR>(), F::mma_ctas(NB)) ws
     s_abort = 0;
     fence_mbarrier_init();
     pol = l2_policy_evict_first();
-    for (; n_issued < (PAR ? NS : NS - 1) && n_issued < ntiles; ++n_issued) {
+    // with tile parity the first tile of each half only: the other stages
+    // are filled from the main loop, after the grid dependency (as in
+    // wstream_kernel, so that the CTAs that start last find a short queue)
+    for (; n_issued < (PAR ? 2 : NS - 1) && n_issued < ntiles; ++n_issued) {
       mbar_arrive_expect_tx(&full[n_issued], TB);
       bulk_g2s(stage_ptr(n_issued), p.tiles + (t0 + n_issued) * TB, TB, &full[n_issued], pol);
     }
   }
   fetch_plan(&s_plan, p.plan, c, tid);
   if constexpr (F::kCbEntries > 0) {
-    if (p.seg_of_rt != nullptr && tid == 0 && ntiles > 0) {
-      const int64_t nRT = div_fast(p.T, p.nKT);
-      s_seg[0] = __ldg(p.seg_of_rt + rt_first);
-      s_seg[1] = rt_first + 1 < nRT ? __ldg(p.seg_of_rt + rt_first + 1) : s_seg[0];
-    }
+    if (p.seg_of_rt != nullptr && ntiles > 0)
+      prefetch_next_table<F>(&s_next, p, rt_first, div_fast(p.T, p.nKT), true, tid);
   }
   F::template mma_init_shared<NT>(fsh, table_of<F>(p, rt_first), warp, lane);
   __syncthreads();
@@ -398,14 +398,9 @@ __global__ void __launch_bounds__(mma_threads<F, NB, PAR>(), F::mma_ctas(NB)) ws
   // A new row tile of a stacked handle may use another codebook: rebuild the
   // table once every warp is done with the old one.
   auto next_table = [&]() {
-    __syncthreads();
-    if (s_seg[1] != s_seg[0]) mma_rebuild_table<F, NT>(fsh, table_of<F>(p, rt), warp, lane);
-    __syncthreads();
-    if (tid == 0) {
-      const int64_t nRT = div_fast(p.T, p.nKT);
-      s_seg[0] = s_seg[1];
-      s_seg[1] = rt + 1 < nRT ? __ldg(p.seg_of_rt + rt + 1) : s_seg[0];
-    }
+    if constexpr (F::kCbEntries > 0)
+      advance_table<F, NT>(&s_next, p, rt, tid,
+                           [&](const uint16_t* cb) { mma_rebuild_table<F, NT>(fsh, cb, warp, lane); });
   };
 
   // The warp's part of the tile in stage st (fill parity fp), k-tile kt_cur:
@@ -594,14 +589,15 @@ __global__ void __launch_bounds__(mma_threads<F, NB, PAR>(), F::mma_ctas(NB)) ws
   if constexpr (PAR) {
     // Tile parity: tile j sits in stage j % NS and is computed by half j % 2,
     // so each half owns every second stage and runs its own pipeline: at its
-    // tile j its first thread refills the stage of its tile j - 2 (released
-    // one tile ago) with tile j + NS - 2.  The prologue issued tiles
-    // 0 .. NS - 1.  Both halves walk the run row tile by row tile and meet at
-    // each row-tile end.
+    // tile j its first thread fills the stage of its tile j - 2 (released
+    // one tile ago; for j < 2 a stage not used yet) with tile j + NS - 2.
+    // The prologue issued tiles 0 and 1.  Both halves walk the run row tile
+    // by row tile and meet at each row-tile end.
+    static_assert(!PAR || NS >= 4, "tile parity: two stages per half");
     const bool leader = (lane == 0) && ((warp & 7) == 0);
     const uint64_t lpol = leader ? l2_policy_evict_first() : 0;
     int u_last = -1;  // leader: last tile of its parity issued (by the prologue or by itself)
-    for (int u = par; u < NS && u < nt; u += 2) u_last = u;
+    for (int u = par; u < 2 && u < nt; u += 2) u_last = u;
     int i = 0;  // first tile of the current row tile segment
     while (i < nt) {
       if (stacked && i > 0) next_table();
@@ -610,9 +606,9 @@ __global__ void __launch_bounds__(mma_threads<F, NB, PAR>(), F::mma_ctas(NB)) ws
       for (int j = i + ((i ^ par) & 1); j < iend; j += 2) {
         bool abort = s_abort != 0;
         const int u = j + NS - 2;
-        if (leader && !abort && j >= 2 && u < nt) {
+        if (leader && !abort && u < nt) {
           const int sn = u % NS;
-          if (!mbar_wait_bounded(&empty[sn], static_cast<uint32_t>(((u - NS) / NS) & 1))) {
+          if (u >= NS && !mbar_wait_bounded(&empty[sn], static_cast<uint32_t>(((u - NS) / NS) & 1))) {
             atomicOr(p.err, kErrTimeoutEmpty);
             s_abort = 1;
             abort = true;

@@ -154,9 +154,12 @@ cudaError_t to_device(const void* src, size_t bytes, void** dst) {
 
 // The stream-K split of T tiles over G CTAs: CTA c runs [c*T/G, (c+1)*T/G).
 // A row tile (nKT consecutive tiles) that no single CTA covers is "shared";
-// its contributors are the CTAs whose runs touch it, and each later sums one
-// slice of its rows.  Computed once per handle so the kernels do no 64-bit
-// divisions.
+// its contributors are the CTAs whose runs touch it.  Each gets an even
+// slice of its rows to finish, and one of them the finisher flag (the
+// kernels' finish_slice picks between the two by the tile's item count):
+// the last contributor, unless the row tile opens that CTA's run (its part
+// is then done early), in which case the one before it.  Computed once per
+// handle so the kernels do no 64-bit divisions.
 int64_t split_point(int64_t c, int64_t T, int64_t G) { return c * T / G; }
 int64_t cta_of(int64_t t, int64_t T, int64_t G) { return ((t + 1) * G - 1) / T; }
 
@@ -184,7 +187,8 @@ std::vector<qgemv::CtaPlan> plan_stream_k(int64_t T, int64_t G, int64_t nKT, int
       pl.seg_S[sg] = static_cast<int32_t>(S);
       pl.seg_r0[sg] = static_cast<int32_t>(k * rows / S);
       pl.seg_nr[sg] = static_cast<int32_t>((k + 1) * rows / S - k * rows / S);
-      pl.seg_side1[sg] = split_point(cf, T, G) < r * nKT ? 1 : 0;
+      const int64_t fin = split_point(cl + 1, T, G) > (r + 1) * nKT ? cl - 1 : cl;
+      pl.seg_flags[sg] = (split_point(cf, T, G) < r * nKT ? 1 : 0) | (c == fin ? 2 : 0);
       ++sg;
     }
   }
@@ -776,7 +780,7 @@ int qgemv_stream_k_plan(int64_t units, int grid, int64_t units_per_row_tile, int
       o[4 + s] = pl.seg_S[s];
       o[6 + s] = pl.seg_r0[s];
       o[8 + s] = pl.seg_nr[s];
-      o[10 + s] = pl.seg_side1[s];
+      o[10 + s] = pl.seg_flags[s];
     }
   }
   return ok();

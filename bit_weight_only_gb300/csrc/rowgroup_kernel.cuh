@@ -115,8 +115,10 @@ __global__ void __launch_bounds__(kRgThreads, 1) rowgroup_stream_kernel(const Ru
     mbar_init(spare, 1);
     s_abort = 0;
     fence_mbarrier_init();
+    // the first stage of each half only; the main loop fills the others
+    // after the grid dependency (see wstream_kernel)
     const uint64_t pol = l2_policy_evict_first();
-    for (int q = 0; q < NS && q < nq; ++q) issue(q, pol);
+    for (int q = 0; q < 2 && q < nq; ++q) issue(q, pol);
   }
   const int64_t rt_first = u0 >> 2;
   F::template init_shared<NT>(fsh, table_of<F>(p, rt_first), warp, lane);
@@ -143,13 +145,13 @@ __global__ void __launch_bounds__(kRgThreads, 1) rowgroup_stream_kernel(const Ru
   };
   if (half < nq) load_stage_x(half);
 
-  // Each half's first thread refills, at its stage q, the stage of its stage
-  // q - 2 (released one stage ago) with stage q + NS - 2; the prologue issued
-  // stages 0 .. NS - 1.
+  // Each half's first thread fills, at its stage q, the stage of its stage
+  // q - 2 (released one stage ago; for q < 2 one not used yet) with stage
+  // q + NS - 2; the prologue issued stages 0 and 1.
   const bool leader = (lane == 0) && (slice == 0);
   const uint64_t lpol = leader ? l2_policy_evict_first() : 0;
   int q_last = -1;  // leader: last stage of its parity issued
-  for (int q = half; q < NS && q < nq; q += 2) q_last = q;
+  for (int q = half; q < 2 && q < nq; q += 2) q_last = q;
   int64_t rt_prev = rt_first;
   for (int64_t u = u0; u < u1; ++u) {
     const int64_t rt = u >> 2;
@@ -166,8 +168,8 @@ __global__ void __launch_bounds__(kRgThreads, 1) rowgroup_stream_kernel(const Ru
     for (int q = qb + ((qb ^ half) & 1); q < qb + nch; q += 2) {
       bool abort = s_abort != 0;
       const int qn = q + NS - 2;
-      if (leader && !abort && q >= 2 && qn < nq) {
-        if (!mbar_wait_bounded(&empty[qn % NS], static_cast<uint32_t>(((qn - NS) / NS) & 1))) {
+      if (leader && !abort && qn < nq) {
+        if (qn >= NS && !mbar_wait_bounded(&empty[qn % NS], static_cast<uint32_t>(((qn - NS) / NS) & 1))) {
           atomicOr(p.err, kErrTimeoutEmpty);
           s_abort = 1;
           abort = true;

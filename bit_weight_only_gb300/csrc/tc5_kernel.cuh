@@ -371,7 +371,7 @@ __global__ void __launch_bounds__(kTc5Threads, 1) tc5_kernel(const RunParams p, 
   uint32_t* s_tbase = reinterpret_cast<uint32_t*>(bars + NS + 16);
   auto stage_ptr = [&](int s) { return s == 0 ? ring0 : ringN + (s - 1) * TB; };
   __shared__ volatile int s_abort;
-  __shared__ int s_seg[2];
+  __shared__ NextTable<F> s_next;
   __shared__ int s_rel[4];      // warps done with the tile in each stage
   __shared__ int s_nissued;     // tiles whose copies were issued
   __shared__ __align__(16) CtaPlan s_plan;
@@ -410,11 +410,8 @@ __global__ void __launch_bounds__(kTc5Threads, 1) tc5_kernel(const RunParams p, 
   }
   fetch_plan(&s_plan, p.plan, c, tid);
   if constexpr (T::kTable) {
-    if (p.seg_of_rt != nullptr && tid == 0 && ntiles > 0) {
-      const int64_t nRT = div_fast(p.T, p.nKT);
-      s_seg[0] = __ldg(p.seg_of_rt + rt_first);
-      s_seg[1] = rt_first + 1 < nRT ? __ldg(p.seg_of_rt + rt_first + 1) : s_seg[0];
-    }
+    if (p.seg_of_rt != nullptr && ntiles > 0)
+      prefetch_next_table<F>(&s_next, p, rt_first, div_fast(p.T, p.nKT), true, tid);
     F::template mma_init_shared<kTc5Threads>(fsh, table_of<F>(p, rt_first), warp, lane);
   }
   if (warp == 0) tmem_alloc_512(s_tbase);
@@ -518,14 +515,10 @@ __global__ void __launch_bounds__(kTc5Threads, 1) tc5_kernel(const RunParams p, 
 
   const bool stacked = T::kTable && p.seg_of_rt != nullptr;
   auto next_table = [&]() {
-    __syncthreads();
-    if (s_seg[1] != s_seg[0]) mma_rebuild_table<F, kTc5Threads>(fsh, table_of<F>(p, rt), warp, lane);
-    __syncthreads();
-    if (tid == 0) {
-      const int64_t nRT = div_fast(p.T, p.nKT);
-      s_seg[0] = s_seg[1];
-      s_seg[1] = rt + 1 < nRT ? __ldg(p.seg_of_rt + rt + 1) : s_seg[0];
-    }
+    if constexpr (T::kTable)
+      advance_table<F, kTc5Threads>(&s_next, p, rt, tid, [&](const uint16_t* cb) {
+        mma_rebuild_table<F, kTc5Threads>(fsh, cb, warp, lane);
+      });
   };
 
   // The warp is done with the codes of tile i (stage st): the sixteenth warp

@@ -190,12 +190,18 @@ def qgemv_status(h: int) -> int:
 
 def qgemv_stream_k_plan(units: int, grid: int, units_per_row_tile: int, rows: int) -> list:
     """The stream-K split the handles use (host only): per CTA a dict of its
-    two shared-row-tile segments, each field a pair (first, last row tile)."""
+    two shared-row-tile segments, each field a pair (first, last row tile);
+    "side1" and "fin" are the two flag bits."""
     out = (ctypes.c_int64 * (12 * grid))()
     _check(load().qgemv_stream_k_plan(units, grid, units_per_row_tile, rows, out))
-    keys = ("rt", "cf", "S", "r0", "nr", "side1")
-    return [{k: (out[12 * c + 2 * i], out[12 * c + 2 * i + 1]) for i, k in enumerate(keys)}
+    keys = ("rt", "cf", "S", "r0", "nr", "flags")
+    plan = [{k: (out[12 * c + 2 * i], out[12 * c + 2 * i + 1]) for i, k in enumerate(keys)}
             for c in range(grid)]
+    for d in plan:
+        f = d.pop("flags")
+        d["side1"] = (f[0] & 1, f[1] & 1)
+        d["fin"] = ((f[0] >> 1) & 1, (f[1] >> 1) & 1)
+    return plan
 
 
 def qgemv_destroy(h: int) -> None:

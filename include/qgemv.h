@@ -331,8 +331,10 @@ int qgemv_run_q4_0_noalloc(const void* packed, int64_t N, int64_t K, const void*
  * shared-row-tile segments s = 0 (first row tile of its run), 1 (last):
  * out[c*12 + 0 + s] row tile (-1: none), [2 + s] first contributing CTA,
  * [4 + s] number of contributors, [6 + s] first row of this CTA's slice of
- * the rows to finish, [8 + s] rows in that slice, [10 + s] 1 if the first
- * contributor's run began before the row tile.  Returns QGEMV_ERR_ARG if a
+ * the rows to finish, [8 + s] rows in that slice, [10 + s] flags: bit 0 set
+ * if the first contributor's run began before the row tile, bit 1 set if
+ * this CTA finishes the whole row tile when it has at most 256 items (rows x
+ * activation rows; then the others finish nothing).  Returns QGEMV_ERR_ARG if a
  * size is not positive, units % units_per_row_tile != 0 or grid > units.   */
 int qgemv_stream_k_plan(int64_t units, int grid, int64_t units_per_row_tile, int rows, int64_t* out);
 

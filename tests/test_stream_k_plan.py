@@ -6,7 +6,9 @@ outputs itself when its run covers the whole row tile, else it stores its
 partial sums in one of its two slots: side 0 for the first row tile of its
 run (the one that began at or before its first unit), side 1 for the last.
 The host plan tells every contributor of a shared row tile where the other
-contributors' slots are and which rows it finishes.  These tests replay the
+contributors' slots are and which rows it finishes: an even slice each, or,
+for small tiles, all of them by the one contributor that holds the finisher
+flag.  These tests replay the
 kernels' owner/side rule against the plan that the library computes and
 check that every output row is produced exactly once from every unit."""
 import pytest
@@ -91,6 +93,16 @@ def test_plan_matches_the_kernels_split(lib, U, G, upr, rows):
                 assert side == 0
             rows_done.extend(range(plan[c]["r0"][s], plan[c]["r0"][s] + plan[c]["nr"][s]))
         assert sorted(rows_done) == list(range(rows))
+        # one finisher for the whole-tile mode: a contributor whose part closes
+        # its run (the last one, unless its part opens a run that goes on)
+        fins = [c for c, _, _, _ in parts
+                if plan[c]["fin"][[s for s in range(2) if plan[c]["rt"][s] == rt][0]]]
+        assert len(fins) == 1, (rt, fins)
+        fc = fins[0]
+        hi_of = {c: hi for c, _, _, hi in parts}
+        assert hi_of[fc] == split(fc + 1, U, G)
+        cl = ctas[-1]
+        assert fc == (cl - 1 if split(cl + 1, U, G) > (rt + 1) * upr else cl)
     # a CTA's plan names no row tile that it does not share
     for c in range(G):
         for s in range(2):
