@@ -84,12 +84,31 @@ def _code_only(text: str) -> str:
     return " ".join("".join(out).split())
 
 
-def kernel_source_hash() -> str:
-    """Hash of the kernel sources' code (comments and layout ignored), which
+# The sources of the kernels that stream each format at M = 1 (the kernel,
+# its format's decode, the shared device helpers and launch code), whose
+# code keys the stored DRAM-traffic captures: a change to any other kernel
+# leaves them valid.  M > 1 adds the tensor-core kernels' sources.
+KERNEL_SOURCES = {
+    "cbk4": ["gemv_kernel.cuh", "rowgroup_kernel.cuh", "fmt_cbk.cuh", "device_common.cuh", "launch_table.cuh",
+             "formats.h", "fmt_cbk4.cu", "fmt_cbk8.cu"],
+    "cbk8": ["gemv_kernel.cuh", "rowgroup_kernel.cuh", "fmt_cbk.cuh", "device_common.cuh", "launch_table.cuh",
+             "formats.h", "fmt_cbk8.cu"],
+    "q4_0": ["gemv_kernel.cuh", "fmt_fields.cuh", "device_common.cuh", "launch_table.cuh", "formats.h", "fmt_q4_0.cu"],
+    "pq2_0": ["gemv_kernel.cuh", "fmt_fields.cuh", "device_common.cuh", "launch_table.cuh", "formats.h", "fmt_pq2.cu"],
+    "aqlm_2x8": ["gemv_kernel.cuh", "device_common.cuh", "formats.h", "fmt_aqlm.cu"],
+}
+KERNEL_SOURCES_MMA = ["mma_kernel.cuh", "tc5_kernel.cuh", "fmt_aqlm_mma.cu"]
+
+
+def kernel_source_hash(fmt: str | None = None, M: int = 1) -> str:
+    """Hash of the code (comments and layout ignored) of the sources behind
+    format fmt's kernels at M rows (all of csrc when fmt has no list), which
     keys the stored DRAM-traffic captures."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "bit_weight_only_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    files = KERNEL_SOURCES.get(fmt)
+    files = (files + (KERNEL_SOURCES_MMA if M > 1 else [])) if files else sorted(os.listdir(csrc))
+    for f in files:
         h.update(f.encode())
         h.update(_code_only(open(os.path.join(csrc, f), encoding="utf-8").read()).encode())
     return h.hexdigest()[:16]
@@ -105,7 +124,7 @@ LLAMA70B_AQLM = [("gate", 28672, 8192), ("up", 28672, 8192), ("down", 8192, 2867
                  ("q", 8192, 8192), ("o", 8192, 8192)]
 
 
-def cbk4_stack_specs(layers=32, stacked=True):
+def cbk4_stack_specs(layers=32, stacked=True, head=True):
     """The 7B projection stack.  stacked: q|k|v and gate|up, which share
     their input, run as one stacked handle each (4 GEMV calls per layer)."""
     specs = []
@@ -118,7 +137,8 @@ def cbk4_stack_specs(layers=32, stacked=True):
         else:
             for name, N, K in LLAMA7B:
                 specs.append(("cbk4", f"L{layer}.{name}", N, K))
-    specs.append(("cbk8", "lm_head", 32000, 4096))
+    if head:
+        specs.append(("cbk8", "lm_head", 32000, 4096))
     return specs
 
 
@@ -131,6 +151,10 @@ WORKLOADS = {
     "cbk4_7b_stack": (lambda: cbk4_stack_specs(), "cbk4",
                       "7B decoder projection stack, 224 CBK4 projections (q|k|v and gate|up stacked: "
                       "128 calls) + CBK8 LM head 32000x4096"),
+    "cbk4_7b_layer": (lambda: cbk4_stack_specs(layers=1, head=False), "cbk4",
+                      "one layer of the 7B CBK4 projection stack: q|k|v 12288x4096, o 4096x4096, gate|up "
+                      "22016x4096, down 4096x11008 (the stack's four call shapes; the small case for "
+                      "DRAM-traffic captures)"),
     "cbk4_7b_stack_unfused": (lambda: cbk4_stack_specs(stacked=False), "cbk4",
                               "7B decoder projection stack, 224 CBK4 calls + CBK8 LM head 32000x4096"),
     "q4_0_4096": (lambda: [("q4_0", "q4_0", 4096, 4096)], "q4_0", "Q4_0 GEMV 4096x4096"),
@@ -464,7 +488,7 @@ def run_ours(args, rank, world, device):
             pj = json.load(open(prof))
             entry = pj.get((args.workload if M == 1 else f"{args.workload}/M={M}")
                            + ("/x_int8" if args.x_int8 else ""))
-            if entry and entry.get("kernel_source_hash") == kernel_source_hash():
+            if entry and entry.get("kernel_source_hash") == kernel_source_hash(entry.get("format"), M):
                 traffic = entry.get("dram_bytes_per_launch")
         except Exception:
             traffic = None
