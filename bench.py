@@ -124,14 +124,16 @@ LLAMA70B_AQLM = [("gate", 28672, 8192), ("up", 28672, 8192), ("down", 8192, 2867
                  ("q", 8192, 8192), ("o", 8192, 8192)]
 
 
-def cbk4_stack_specs(layers=32, stacked=True, head=True):
+def cbk4_stack_specs(layers=32, stacked=True, head=True, glu=False):
     """The 7B projection stack.  stacked: q|k|v and gate|up, which share
-    their input, run as one stacked handle each (4 GEMV calls per layer)."""
+    their input, run as one stacked handle each (4 GEMV calls per layer);
+    glu: gate|up as a fused SiLU(gate)*up handle instead (output 11008)."""
     specs = []
     for layer in range(layers):
         if stacked:
             specs += [("cbk4", f"L{layer}.qkv", [4096, 4096, 4096], 4096),
                       ("cbk4", f"L{layer}.o", 4096, 4096),
+                      ("cbk4_glu", f"L{layer}.gate_up", 11008, 4096) if glu else
                       ("cbk4", f"L{layer}.gate_up", [11008, 11008], 4096),
                       ("cbk4", f"L{layer}.down", 4096, 11008)]
         else:
@@ -155,6 +157,9 @@ WORKLOADS = {
                       "one layer of the 7B CBK4 projection stack: q|k|v 12288x4096, o 4096x4096, gate|up "
                       "22016x4096, down 4096x11008 (the stack's four call shapes; the small case for "
                       "DRAM-traffic captures)"),
+    "cbk4_7b_stack_glu": (lambda: cbk4_stack_specs(glu=True), "cbk4",
+                          "7B decoder projection stack, 224 CBK4 projections as 128 calls (q|k|v stacked, "
+                          "gate|up fused: SiLU(gate)*up stored) + CBK8 LM head 32000x4096"),
     "cbk4_7b_stack_unfused": (lambda: cbk4_stack_specs(stacked=False), "cbk4",
                               "7B decoder projection stack, 224 CBK4 calls + CBK8 LM head 32000x4096"),
     "q4_0_4096": (lambda: [("q4_0", "q4_0", 4096, 4096)], "q4_0", "Q4_0 GEMV 4096x4096"),
@@ -221,6 +226,19 @@ def build_handles(specs, M, device, seed=0):
             y = y_all[yo:yo + M * N].view(M, N)
             xo += M * K
             yo += M * N
+            ops.append({"fmt": fmt, "name": name, "N": N, "K": K, "h": h, "x": x, "y": y, "bytes": nbytes})
+            continue
+        if fmt == "cbk4_glu":  # gate and up in one handle (a codebook each), output SiLU(gate) * up
+            pg = inputs.cbk_packed_cuda(f"{tag}/gate", N, K, 4, p16, device, seed)
+            pu = inputs.cbk_packed_cuda(f"{tag}/up", N, K, 4, p16, device, seed)
+            h = qgemv.QGemv.glu("cbk4", N, K, pg, pu, c16, c16)
+            del pg, pu
+            x = x_all[xo:xo + M * K].view(M, K)
+            x.copy_(inputs.x_fp16_cuda(f"{tag}/x", M, K, device=device, seed=seed))
+            y = y_all[yo:yo + M * N].view(M, N)
+            xo += M * K
+            yo += M * N
+            nbytes = 2 * (qgemv.qgemv_packed_bytes("cbk4", N, K) + canonical_extra_bytes("cbk4", N)) + 2 * M * K + 4 * M * N
             ops.append({"fmt": fmt, "name": name, "N": N, "K": K, "h": h, "x": x, "y": y, "bytes": nbytes})
             continue
         if fmt == "pq2_0_glu":  # gate and up in one handle, output SiLU(gate) * up
@@ -363,8 +381,8 @@ def run_ours(args, rank, world, device):
     # runs all of them back to back, so no copy is still in L2 when its turn
     # comes round again.
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
-    one_copy = sum(qgemv.qgemv_packed_bytes(f if f != "pq2_0_glu" else "pq2_0", total_rows(N), K)
-                   * (2 if f == "pq2_0_glu" else 1) for f, _, N, K in specs)
+    one_copy = sum(qgemv.qgemv_packed_bytes(f[:-4] if f.endswith("_glu") else f, total_rows(N), K)
+                   * (2 if f.endswith("_glu") else 1) for f, _, N, K in specs)
     R = 1 if one_copy >= 3 * l2 else -(-3 * l2 // one_copy)
     copies = [build_handles(specs, M, device, seed=r) for r in range(R)]
     ops = [o for c_ops, _, _ in copies for o in c_ops]
@@ -381,8 +399,10 @@ def run_ours(args, rank, world, device):
     log(f"[bench] rank {rank}: {len(specs)} GEMVs x {R} copies ready in {time.time() - t_setup:.1f}s")
 
     step_bytes = sum(o["bytes"] for o in ops)
-    dom = [o for o in ops if o["fmt"] == dominant]
-    rest = [o for o in ops if o["fmt"] != dominant]
+    # the dominant format's calls (with its fused gate|up handles, if any)
+    in_dom = lambda o: o["fmt"] in (dominant, dominant + "_glu")
+    dom = [o for o in ops if in_dom(o)]
+    rest = [o for o in ops if not in_dom(o)]
     dom_bytes = sum(o["bytes"] for o in dom)
 
     stream = torch.cuda.Stream(device=device)

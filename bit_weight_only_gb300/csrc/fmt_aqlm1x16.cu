@@ -162,7 +162,7 @@ cudaError_t prepare(const PrepareArgs& a, cudaStream_t s) {
 }
 
 cudaError_t dequant(const uint8_t* tiles, const void* aux, const int32_t*, int64_t N, int64_t K, int nKT,
-                    float* w_out, cudaStream_t s) {
+                    float* w_out, int, cudaStream_t s) {
   dequant_kernel<<<grid_for(N * (K / 8)), 256, 0, s>>>(reinterpret_cast<const uint16_t*>(tiles),
                                                        static_cast<const uint8_t*>(aux), N, K, nKT, w_out);
   return cudaGetLastError();

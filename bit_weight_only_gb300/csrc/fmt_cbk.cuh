@@ -57,6 +57,8 @@ struct FmtCBK4 {
   __host__ __device__ static constexpr int stages(int M) { return M <= 4 ? 4 : 2; }
   static constexpr int kSharedBytes = kLutBytes;
   static constexpr int kCbEntries = 16;
+  static constexpr bool kGluTables = true;  // GLU: the up table in each entry row's second half
+  static constexpr bool kMmaGlu = true;     // the GLU form of the tensor-core kernel
   static constexpr float kOutScale = 1.0f;
   static constexpr int kSumGroups = 1;  // unused: codebook values carry no offset
   using XRegs = XRegsT<2>;
@@ -223,6 +225,8 @@ struct FmtCBK8 {
   static constexpr bool kTileParity = true;  // so the two warps of a slice take alternate tiles
   __host__ __device__ static constexpr int stages(int M) { return M <= 4 ? 4 : 2; }
   static constexpr int kCbEntries = 256;
+  static constexpr bool kGluTables = true;  // GLU: the up table in each entry row's second half
+  static constexpr bool kMmaGlu = true;     // the GLU form of the tensor-core kernel
   static constexpr int kSharedBytes = kLutBytes;
   static constexpr float kOutScale = 1.0f;
   static constexpr int kSumGroups = 1;  // unused
@@ -516,10 +520,12 @@ __global__ void prepare_kernel(const uint8_t* __restrict__ canon, int64_t N, int
 
 // Exact decode (codebook entry of each index) from the prepared tiles; cb
 // holds one codebook (cb_stride 0) or one copy per row tile (cb_stride =
-// entries, stacked handles).
+// entries, stacked handles); up_off: offset of the codebook of rows 64..127
+// of every tile (the up rows of a GLU handle), else 0.
 template <class F, int kBitsPerIndex>
 __global__ void dequant_kernel(const uint8_t* __restrict__ tiles, const uint16_t* __restrict__ cb,
-                               int64_t cb_stride, int64_t N, int64_t K, int nKT, float* __restrict__ w) {
+                               int64_t cb_stride, int64_t up_off, int64_t N, int64_t K, int nKT,
+                               float* __restrict__ w) {
   const int64_t total = N * K;
   for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
        e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -534,7 +540,7 @@ __global__ void dequant_kernel(const uint8_t* __restrict__ tiles, const uint16_t
     const uint8_t byte = tiles[tile * F::kTileBytes + ((j * 2 + h) * kLaneSlots + cw * 32 + lane) * 16 +
                                byte_in_row % 16];
     const int idx = kBitsPerIndex == 8 ? byte : ((el & 1) ? (byte >> 4) : (byte & 15));
-    w[e] = h2f(cb[(n / kTileRows) * cb_stride + idx]);
+    w[e] = h2f(cb[(n / kTileRows) * cb_stride + (r >= kTileRows / 2 ? up_off : 0) + idx]);
   }
 }
 

@@ -55,7 +55,7 @@ __global__ void dequant_kernel(const uint8_t* __restrict__ tiles, const float* _
 }
 
 cudaError_t dequant(const uint8_t* tiles, const void* aux, const int32_t*, int64_t N, int64_t K, int nKT,
-                    float* w, cudaStream_t s) {
+                    float* w, int, cudaStream_t s) {
   dequant_kernel<<<cbk::grid_for(N * K, 256), 256, 0, s>>>(tiles, static_cast<const float*>(aux), N, K, nKT,
                                                            w);
   return cudaGetLastError();

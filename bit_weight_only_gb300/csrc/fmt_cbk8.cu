@@ -15,18 +15,25 @@ cudaError_t prepare(const PrepareArgs& a, cudaStream_t s) {
                                                                        nchunks, a.tiles);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if (a.seg_of_rt == nullptr)  // one codebook
-    return cudaMemcpyAsync(a.aux, a.codebooks, 256 * sizeof(uint16_t), cudaMemcpyDeviceToDevice, s);
+  if (a.seg_of_rt == nullptr)  // one codebook (a GLU handle: the gate's, then the up's)
+    return cudaMemcpyAsync(a.aux, a.codebooks, (a.glu ? 2 : 1) * 256 * sizeof(uint16_t), cudaMemcpyDeviceToDevice, s);
   cbk::expand_codebooks_kernel<256><<<cbk::grid_for(a.nRT * 256, 256), 256, 0, s>>>(
       a.codebooks, a.seg_of_rt, a.nRT, static_cast<uint16_t*>(a.aux));
   return cudaGetLastError();
 }
 
 cudaError_t dequant(const uint8_t* tiles, const void* aux, const int32_t* seg_of_rt, int64_t N, int64_t K,
-                    int nKT, float* w, cudaStream_t s) {
+                    int nKT, float* w, int glu, cudaStream_t s) {
   cbk::dequant_kernel<F, 8><<<cbk::grid_for(N * K, 256), 256, 0, s>>>(
-      tiles, static_cast<const uint16_t*>(aux), seg_of_rt ? 256 : 0, N, K, nKT, w);
+      tiles, static_cast<const uint16_t*>(aux), seg_of_rt ? 256 : 0, glu ? 256 : 0, N, K, nKT, w);
   return cudaGetLastError();
+}
+
+// the regular launches and the GLU handles' kernels
+cudaError_t setup_all() {
+  cudaError_t e = LaunchTable<F>::setup();
+  if (e == cudaSuccess) e = LaunchTable<F>::setup_glu();
+  return e;
 }
 
 }  // namespace
@@ -34,11 +41,11 @@ cudaError_t dequant(const uint8_t* tiles, const void* aux, const int32_t* seg_of
 const FormatOps* ops_cbk8() {
   static const FormatOps ops = {
       /*format=*/3, F::kKT, F::kTileBytes, /*aux_bytes=*/0,
-      &LaunchTable<F>::smem_bytes, &LaunchTable<F>::setup, &LaunchTable<F>::launch,
+      &LaunchTable<F>::smem_bytes, &setup_all, &LaunchTable<F>::launch,
       &prepare, &dequant, /*cb_entries=*/256, /*tile_rows=*/128, /*partial_stride=*/128 * 16,
       /*aux_per_row=*/0, /*m1_ctas_per_sm=*/LaunchTable<F>::kM1CtasPerSm,
       /*rowgroup=*/1, /*launch_x_int8=*/nullptr, /*row_tables=*/0, /*launch_xq=*/nullptr,
-      /*launch_glu=*/nullptr, /*tc5_min_m=*/kTc5DefaultMinM};
+      /*launch_glu=*/&LaunchTable<F>::launch_glu, /*tc5_min_m=*/kTc5DefaultMinM};
   return &ops;
 }
 

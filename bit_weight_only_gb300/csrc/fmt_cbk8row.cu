@@ -164,7 +164,7 @@ cudaError_t prepare(const PrepareArgs& a, cudaStream_t s) {
 }
 
 cudaError_t dequant(const uint8_t* tiles, const void* aux, const int32_t*, int64_t N, int64_t K, int nKT,
-                    float* w, cudaStream_t s) {
+                    float* w, int, cudaStream_t s) {
   dequant_kernel<<<grid_for(N * K), 256, 0, s>>>(tiles, static_cast<const float*>(aux), N, K, int64_t(nKT) * kKC,
                                                  w);
   return cudaGetLastError();

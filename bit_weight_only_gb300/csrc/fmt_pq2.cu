@@ -118,7 +118,7 @@ cudaError_t prepare(const PrepareArgs& a, cudaStream_t s) {
 }
 
 cudaError_t dequant(const uint8_t* tiles, const void*, const int32_t*, int64_t N, int64_t K, int nKT,
-                    float* w, cudaStream_t s) {
+                    float* w, int, cudaStream_t s) {
   dequant_kernel<<<grid_for(N * K, 256), 256, 0, s>>>(tiles, N, K, nKT, w);
   return cudaGetLastError();
 }

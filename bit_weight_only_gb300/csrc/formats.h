@@ -22,6 +22,7 @@ struct PrepareArgs {
   void* aux;                 // out: format data (aux_bytes), may be nullptr
   int nseg;                  // codebooks (stacked handles; 1 otherwise)
   const int32_t* seg_of_rt;  // device [nRT] codebook of each row tile, or nullptr
+  int glu = 0;               // GLU handle of a one-codebook format: codebooks = gate's, then up's
 };
 
 // Grids and stream-K plans of a handle: `grid`/`plan` for the tensor-core and
@@ -48,8 +49,10 @@ struct FormatOps {
   cudaError_t (*launch)(int M, const RunParams& p, const LaunchGeom& g, cudaStream_t s, bool batch_invariant);
   cudaError_t (*prepare)(const PrepareArgs& a, cudaStream_t s);
   // w_out[n*K + k] = exact decoded weight, read back from the prepared tiles
+  // glu: a GLU handle of a one-codebook format (aux holds the gate then the
+  // up codebook; rows 64..127 of every tile use the second)
   cudaError_t (*dequant)(const uint8_t* tiles, const void* aux, const int32_t* seg_of_rt, int64_t N,
-                         int64_t K, int nKT, float* w_out, cudaStream_t s);
+                         int64_t K, int nKT, float* w_out, int glu, cudaStream_t s);
   int cb_entries = 0;               // fp16 entries per codebook (CBK4 16, CBK8 256)
   int tile_rows = 128;              // output rows per prepared tile
   int64_t partial_stride = 128 * 16;  // floats per stream-K partial slot

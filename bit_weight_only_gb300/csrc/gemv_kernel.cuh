@@ -378,28 +378,13 @@ __device__ __forceinline__ void glu_store(const RunParams& p, int m, int64_t n, 
   if (n < nout) p.y[m * nout + n] = __fmul_rn(g / (1.0f + expf(-g)), u);
 }
 
-// Read one partial slot with a bounded poll and mark it empty again.  After
-// a wait of this thread has given up (gave_up), later slots are not waited
-// for, so a run whose partials never come ends after one time limit.
-__device__ __forceinline__ float take_slot(const RunParams& p, float* slot, bool& gave_up) {
-  unsigned long long t_start = 0;
-  uint32_t bits;
-  while ((bits = ld_relaxed_u32(slot)) == kEmptySlot) {
-    const unsigned long long now = global_timer_ns();
-    if (t_start == 0) t_start = now;
-    else if (gave_up || now - t_start > kWaitLimitNs) {
-      atomicOr(p.err, kErrTimeoutFixup);
-      gave_up = true;
-      return 0.f;
-    }
-  }
-  st_relaxed_u32(slot, kEmptySlot);
-  return __uint_as_float(bits);
-}
-
 // Finish a shared row tile of a GLU handle (plan segment sg, whose row slice
 // counts gate/up row pairs, 0..63): for each pair and activation row, the
 // gate and up sums over the S contributors in order, then SiLU(gate) * up.
+// The gate and up slots of up to 8 contributors are polled at once (one L2
+// round trip when they are there), each with a bounded wait; after a wait
+// has given up, the rest of the thread's slots count as 0 and are not waited
+// for, so a run whose partials never come ends after one time limit.
 template <int M, int NT>
 __device__ __noinline__ void finish_rows_glu(const RunParams& p, const CtaPlan& pl, int sg, float out_scale,
                                              int tid, int mrows = M) {
@@ -409,6 +394,7 @@ __device__ __noinline__ void finish_rows_glu(const RunParams& p, const CtaPlan& 
   int r0, nr;
   finish_slice(pl, sg, kTileRows / 2, mrows, r0, nr);
   if (nr <= 0) return;
+  constexpr int B = 8;  // contributors polled at once
   float* first_slot = p.partials + (cf * 2 + (pl.seg_flags[sg] & 1)) * kPartialStride;
   float* base = p.partials + cf * 2 * kPartialStride;
   bool gave_up = false;
@@ -416,10 +402,48 @@ __device__ __noinline__ void finish_rows_glu(const RunParams& p, const CtaPlan& 
     const int m = t / nr;
     const int r = r0 + (t - m * nr);
     float g = 0.f, u = 0.f;
-    for (int i = 0; i < S; ++i) {
-      float* sl = (i == 0 ? first_slot : base + int64_t(i) * 2 * kPartialStride) + m * kTileRows;
-      g += take_slot(p, sl + r, gave_up);
-      u += take_slot(p, sl + kTileRows / 2 + r, gave_up);
+    for (int i0 = 0; i0 < S; i0 += B) {
+      const int cnt = min(B, S - i0);
+      // slot word 2j: gate row r of contributor i0 + j, 2j + 1: its up row
+      auto slot = [&](int w) {
+        const int i = i0 + (w >> 1);
+        return (i == 0 ? first_slot : base + int64_t(i) * 2 * kPartialStride) + m * kTileRows + r +
+               ((w & 1) ? kTileRows / 2 : 0);
+      };
+      uint32_t bits[2 * B];
+      uint32_t pending = gave_up ? 0u : (1u << (2 * cnt)) - 1u;
+#pragma unroll
+      for (int w = 0; w < 2 * B; ++w) bits[w] = 0u;  // +0.0 for a slot given up on
+      unsigned long long t_start = 0;
+      while (pending) {
+#pragma unroll
+        for (int w = 0; w < 2 * B; ++w)
+          if (pending & (1u << w)) bits[w] = ld_relaxed_u32(slot(w));
+#pragma unroll
+        for (int w = 0; w < 2 * B; ++w)
+          if ((pending & (1u << w)) && bits[w] != kEmptySlot) pending &= ~(1u << w);
+        if (!pending) break;
+        const unsigned long long now = global_timer_ns();
+        if (t_start == 0) {
+          t_start = now;
+        } else if (now - t_start > kWaitLimitNs) {
+          atomicOr(p.err, kErrTimeoutFixup);
+          gave_up = true;
+#pragma unroll
+          for (int w = 0; w < 2 * B; ++w)
+            if (pending & (1u << w)) bits[w] = 0u;
+          break;
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < B; ++j) {
+        if (j < cnt) {
+          g += __uint_as_float(bits[2 * j]);
+          u += __uint_as_float(bits[2 * j + 1]);
+          st_relaxed_u32(slot(2 * j), kEmptySlot);
+          st_relaxed_u32(slot(2 * j + 1), kEmptySlot);
+        }
+      }
     }
     glu_store(p, m, rt * (kTileRows / 2) + r, __fmul_rn(g, out_scale), __fmul_rn(u, out_scale));
   }
@@ -462,6 +486,23 @@ template <class F>
 __device__ __forceinline__ const uint16_t* table_of(const RunParams& p, int64_t rt) {
   return static_cast<const uint16_t*>(p.aux) + (p.seg_of_rt != nullptr ? rt * F::kCbEntries : 0);
 }
+
+// GLU handles of the one-codebook table formats (F::kGluTables): the gate
+// and up projections have a codebook each.  Their tables share the 64 KB
+// region: a lane-replicated entry row is 256 bytes of which lanes use the
+// first 128 (lane * 4), so the up table sits in the second 128 (a key with
+// bit 7 set) and every lookup stays one conflict-free LDS.  The up rows of a
+// tile (64..127) are those of lanes 16..31, or the odd m-tiles of the
+// tensor-core kernel.
+template <class F, class = void>
+struct GluTables {
+  static constexpr bool value = false;
+};
+template <class F>
+struct GluTables<F, decltype(void(F::kGluTables))> {
+  static constexpr bool value = F::kGluTables;
+};
+constexpr int kGluUpTable = 128;  // byte offset of the up table in each entry row
 
 // Stacked table handles: the segment of the table built in shared memory
 // (seg[0]), and the segment and codebook of the row tile after it (seg[1],
@@ -624,7 +665,11 @@ __global__ void __launch_bounds__(gemv_threads<F, M>(), F::kCtasPerSm) wstream_k
       prefetch_next_table<F>(&s_next, p, rt_first, div_fast(p.T, p.nKT), true, tid);
   }
   F::template init_shared<NT>(fsh, table_of<F>(p, rt_first), warp, lane);
+  if constexpr (GLU && GluTables<F>::value)
+    F::template init_shared<NT>(fsh + kGluUpTable, table_of<F>(p, rt_first) + F::kCbEntries, warp, lane);
   __syncthreads();
+  // the table of the lane's rows (GLU: lanes 16..31 hold the up rows)
+  uint8_t* const lane_table = fsh + (GLU && GluTables<F>::value && lane >= 16 ? kGluUpTable : 0);
 
   float* xs = xs_all + warp * XS_FLOATS;
   RowAcc<M, RPW> acc;
@@ -682,7 +727,7 @@ __global__ void __launch_bounds__(gemv_threads<F, M>(), F::kCtasPerSm) wstream_k
       if (!abort && lane == 0) atomicOr(p.err, kErrTimeoutFull);
       s_abort = 1;
     } else {
-      F::template tile_math<M, RPW>(stage_ptr(st), xs, xsum, acc, fsh, slice, rhalf, lane, &empty[st]);
+      F::template tile_math<M, RPW>(stage_ptr(st), xs, xsum, acc, lane_table, slice, rhalf, lane, &empty[st]);
     }
   };
 

@@ -342,6 +342,8 @@ __global__ void __launch_bounds__(mma_threads<F, NB, PAR>(), F::mma_ctas(NB)) ws
       prefetch_next_table<F>(&s_next, p, rt_first, div_fast(p.T, p.nKT), true, tid);
   }
   F::template mma_init_shared<NT>(fsh, table_of<F>(p, rt_first), warp, lane);
+  if constexpr (GLU && GluTables<F>::value)
+    F::template mma_init_shared<NT>(fsh + kGluUpTable, table_of<F>(p, rt_first) + F::kCbEntries, warp, lane);
   __syncthreads();
 
   // The prologue touches nothing a previous kernel writes; x and the outputs
@@ -466,8 +468,10 @@ __global__ void __launch_bounds__(mma_threads<F, NB, PAR>(), F::mma_ctas(NB)) ws
   #pragma unroll
                   for (int mi = 0; mi < MG; ++mi) {
                     const int mt = mg + mi;
-                    const uint2 r0 = F::mma_frag(w[mt][0], ks, lut_key, cb);  // row gi: (k lo pair, k hi pair)
-                    const uint2 r1 = F::mma_frag(w[mt][1], ks, lut_key, cb);  // row gi + 8
+                    // GLU with two tables: the odd m-tiles hold the up rows
+                    const uint32_t key = lut_key | (GLU && GluTables<F>::value && (mt & 1) ? kGluUpTable : 0);
+                    const uint2 r0 = F::mma_frag(w[mt][0], ks, key, cb);  // row gi: (k lo pair, k hi pair)
+                    const uint2 r1 = F::mma_frag(w[mt][1], ks, key, cb);  // row gi + 8
   #pragma unroll
                     for (int nb = 0; nb < NB; ++nb) {
                       const uint2 bf = F::mma_bfrag(xw[ss][nb], ks);

@@ -401,8 +401,10 @@ static qgemv_handle create_impl(int format, int64_t N, int64_t K, const void* pa
   e = to_device(packed, static_cast<size_t>(canonical_bytes(format, N, K)), &d_packed);
   if (e == cudaSuccess) e = to_device(scales, 2 * scales_count(format, N), &d_scales);
   const bool per_row_cb = format == QGEMV_CBK4_ROW || format == QGEMV_CBK8_ROW;
+  // a GLU handle of a one-codebook format holds two codebooks (gate, up)
+  const bool glu_tables = glu && ops->cb_entries > 0 && !ops->row_tables;
   const int64_t cb_bytes = per_row_cb ? 4 * codebook_count(format) * N  // fp32 per row
-                                      : 2 * codebook_count(format) * nseg;
+                                      : 2 * codebook_count(format) * nseg * (glu_tables ? 2 : 1);
   if (e == cudaSuccess) e = to_device(codebooks, static_cast<size_t>(cb_bytes), &d_cb);
   if (e != cudaSuccess) return cleanup(QGEMV_ERR_CUDA, "copying the canonical inputs", e);
 
@@ -410,7 +412,7 @@ static qgemv_handle create_impl(int format, int64_t N, int64_t K, const void* pa
   // table formats: one codebook, or (stacked) one copy per row tile followed
   // by the row tiles' segments
   const bool stacked = ops->cb_entries > 0 && (nseg > 1 || ops->row_tables);
-  const int64_t table_bytes = int64_t(2) * ops->cb_entries * (stacked ? h->nRT : 1);
+  const int64_t table_bytes = int64_t(2) * ops->cb_entries * (stacked ? h->nRT : 1) * (glu_tables ? 2 : 1);
   const int64_t aux_bytes = ops->cb_entries > 0 ? table_bytes + (stacked ? 4 * h->nRT : 0)
                                                 : ops->aux_bytes + ops->aux_per_row * N;
   if (e == cudaSuccess && aux_bytes > 0) e = dev_alloc(&h->aux, static_cast<size_t>(aux_bytes));
@@ -452,6 +454,7 @@ static qgemv_handle create_impl(int format, int64_t N, int64_t K, const void* pa
   a.aux = h->aux;
   a.nseg = nseg;
   a.seg_of_rt = h->seg_of_rt;
+  a.glu = glu_tables ? 1 : 0;
   e = ops->prepare(a, 0);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return cleanup(QGEMV_ERR_CUDA, "preparing the tiles", e);
@@ -514,7 +517,8 @@ qgemv_handle qgemv_create_glu(int format, int64_t N, int64_t K, const void* pack
                               const void* codebooks_gate, const void* codebooks_up) {
   const qgemv::FormatOps* ops = ops_for(format);
   if (!ops || format == kAqlmMma || ops->launch_glu == nullptr) {
-    set_error(QGEMV_ERR_ARG, "format %d has no fused SiLU(gate) * up (Q4_0, PQ2_0 and CBK4_ROW have)", format);
+    set_error(QGEMV_ERR_ARG,
+              "format %d has no fused SiLU(gate) * up (Q4_0, PQ2_0, CBK4, CBK8 and CBK4_ROW have)", format);
     return nullptr;
   }
   if (!packed_gate || !packed_up) {
@@ -522,9 +526,10 @@ qgemv_handle qgemv_create_glu(int format, int64_t N, int64_t K, const void* pack
     return nullptr;
   }
   const bool row_cb = format == QGEMV_CBK4_ROW;  // per-row codebooks travel with their rows
-  if (row_cb != (codebooks_gate != nullptr && codebooks_up != nullptr) ||
-      (!row_cb && (codebooks_gate != nullptr || codebooks_up != nullptr))) {
-    set_error(QGEMV_ERR_ARG, row_cb ? "CBK4_ROW needs both codebook arrays" : "format %d takes no codebooks",
+  const bool has_cb = row_cb || ops->cb_entries > 0;
+  if (has_cb != (codebooks_gate != nullptr && codebooks_up != nullptr) ||
+      (!has_cb && (codebooks_gate != nullptr || codebooks_up != nullptr))) {
+    set_error(QGEMV_ERR_ARG, has_cb ? "format %d needs both codebook arrays" : "format %d takes no codebooks",
               format);
     return nullptr;
   }
@@ -558,6 +563,12 @@ qgemv_handle qgemv_create_glu(int format, int64_t N, int64_t K, const void* pack
   if (e == cudaSuccess) e = interleave(inter, packed_gate, packed_up, row_bytes);
   if (e == cudaSuccess && row_cb) e = dev_alloc(&inter_cb, static_cast<size_t>(2 * N * 16 * 4));
   if (e == cudaSuccess && row_cb) e = interleave(inter_cb, codebooks_gate, codebooks_up, 16 * 4);
+  // one codebook per matrix: the gate's, then the up's (the kernels' two tables)
+  const size_t cb1 = 2 * static_cast<size_t>(ops->cb_entries);
+  if (e == cudaSuccess && !row_cb && has_cb) e = dev_alloc(&inter_cb, 2 * cb1);
+  if (e == cudaSuccess && !row_cb && has_cb) e = cudaMemcpy(inter_cb, codebooks_gate, cb1, cudaMemcpyDefault);
+  if (e == cudaSuccess && !row_cb && has_cb)
+    e = cudaMemcpy(static_cast<uint8_t*>(inter_cb) + cb1, codebooks_up, cb1, cudaMemcpyDefault);
   if (e != cudaSuccess) {
     cudaFree(inter);
     cudaFree(inter_cb);
@@ -721,6 +732,7 @@ int qgemv_dequant(qgemv_handle h, float* w_out, void* stream) {
   if (!valid(h)) return set_error(QGEMV_ERR_ARG, "invalid handle");
   if (!w_out) return set_error(QGEMV_ERR_ARG, "w_out is NULL");
   cudaError_t e = h->ops->dequant(h->tiles, h->aux, h->seg_of_rt, h->N, h->K, h->nKT, w_out,
+                                  h->glu && h->ops->cb_entries > 0 && !h->ops->row_tables,
                                   static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_error(e, "launching the decode kernel");
   return ok();

@@ -272,7 +272,8 @@ class QGemv:
     @classmethod
     def glu(cls, fmt, N: int, K: int, packed_gate, packed_up, codebooks_gate=None, codebooks_up=None):
         """Fused MLP gate/up: ``gemv(x)`` returns SiLU(x . G^T) * (x . U^T),
-        fp32 [M, N] (codebooks: CBK4_ROW's per-row fp32 [N, 16] arrays)."""
+        fp32 [M, N] (codebooks: each matrix's fp16 codebook for CBK4 / CBK8,
+        CBK4_ROW's per-row fp32 [N, 16] arrays)."""
         self = cls.__new__(cls)
         self.fmt, self.N, self.K = _fmt(fmt), int(N), int(K)
         g, kg = _addr(packed_gate)

@@ -142,18 +142,19 @@ qgemv_handle qgemv_create_stacked(int format, int nseg, const int64_t* seg_rows,
  * runs store the fused activation y[m][n] = SiLU(x . G^T)[m][n] * (x . U^T)
  * [m][n], SiLU(v) = v / (1 + e^-v): the gate/up GEMV with "SiLU(gate) * up
  * in the reduce" of "Trapetum benchmarks" ("Short-context decode, step by
- * step"), with no separate activation kernel.  Q4_0 and PQ2_0 run every M in
- * one launch (M >= 2 on the tensor-core kernel, the weights read once per
- * call); CBK4_ROW launches once per activation row.
- *   format: QGEMV_Q4_0, QGEMV_PQ2_0 or QGEMV_CBK4_ROW (the gate and up rows
- *     share the prepared tiles, so formats with one codebook per matrix are
- *     refused; per-row codebooks travel with their rows).
+ * step"), with no separate activation kernel.  Q4_0, PQ2_0, CBK4 and CBK8
+ * run every M in one launch (M >= 2 on the tensor-core kernel, the weights
+ * read once per call); CBK4_ROW launches once per activation row.
+ *   format: QGEMV_Q4_0, QGEMV_PQ2_0, QGEMV_CBK4, QGEMV_CBK8 or QGEMV_CBK4_ROW
+ *     (CBK4 / CBK8: the gate and up tables share the kernels' table region,
+ *     each lookup still one shared-memory read; per-row codebooks travel
+ *     with their rows).
  *   N: rows of each projection (the output width), a positive multiple of
  *     64; K as for qgemv_create.
  *   packed_gate, packed_up: each projection's canonical bytes (host or
  *     device), copied.  The handle holds them interleaved in 64-row blocks.
- *   codebooks_gate, codebooks_up: CBK4_ROW's fp32 [N][16] codebooks of each
- *     projection; NULL for the other formats.
+ *   codebooks_gate, codebooks_up: each projection's codebook -- CBK4 fp16
+ *     [16], CBK8 fp16 [256], CBK4_ROW fp32 [N][16]; NULL for Q4_0 and PQ2_0.
  * Runs: qgemv_run with y fp32 [M][N]; the residual form is refused, and so
  * are qgemv_set_x_int8 and qgemv_run_xq.  qgemv_dequant of such a handle
  * writes the 2N interleaved rows (64 gate rows, then the 64 up rows of the

@@ -120,8 +120,10 @@ def test_stacked_create_rejects_bad_arguments_on_host(lib):
 
 
 def test_glu_create_rejects_bad_arguments_on_host(lib):
-    assert not lib.qgemv_create_glu(qgemv.CBK4, 128, 256, 1, 1, 1, 1)
+    assert not lib.qgemv_create_glu(qgemv.AQLM_2X8, 128, 256, 1, 1, None, None)
     assert "no fused" in qgemv.qgemv_last_error()
+    assert not lib.qgemv_create_glu(qgemv.CBK4, 128, 256, 1, 1, 1, None)
+    assert "needs both codebook" in qgemv.qgemv_last_error()
     assert not lib.qgemv_create_glu(qgemv.PQ2_0, 100, 256, 1, 1, None, None)
     assert "multiple of 64" in qgemv.qgemv_last_error()
     assert not lib.qgemv_create_glu(qgemv.Q4_0, 128, 48, 1, 1, None, None)

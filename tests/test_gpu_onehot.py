@@ -221,7 +221,7 @@ def test_one_hot_columns_stacked_m1(monkeypatch):
     check_columns(y, z, W, cols, "stacked cbk4 M=1")
 
 
-@pytest.mark.parametrize("fmt", ["q4_0", "pq2_0", "cbk4_row"])
+@pytest.mark.parametrize("fmt", ["q4_0", "pq2_0", "cbk4", "cbk8", "cbk4_row"])
 @pytest.mark.parametrize("M", [1, 2])
 def test_one_hot_glu_pairs(fmt, M):
     """The fused SiLU(gate) * up handle: with x = e_k its two sums are the
@@ -232,8 +232,10 @@ def test_one_hot_glu_pairs(fmt, M):
     device's expf may differ from a correctly rounded one in the last place)."""
     N, K = 704, 2048
     tag = f"onehot/glu/{fmt}"
-    pg, _, cg = make_case(fmt, N, K, tag=f"{tag}/gate")  # codebooks: CBK4_ROW only, else None
+    pg, _, cg = make_case(fmt, N, K, tag=f"{tag}/gate")  # codebooks: CBK4, CBK8, CBK4_ROW, else None
     pu, _, cu = make_case(fmt, N, K, tag=f"{tag}/up")
+    if fmt in ("cbk4", "cbk8"):  # one codebook per matrix: make the up one differ from the gate one
+        cu = (cg.astype(np.float32) * np.float32(-0.75)).astype(np.float16)
     G = oracle.dequant(fmt, N, K, pg, None, cg)
     U = oracle.dequant(fmt, N, K, pu, None, cu)
     h = qgemv.QGemv.glu(fmt, N, K, pg, pu, cg, cu)
