@@ -96,6 +96,9 @@ KERNEL_SOURCES = {
     "q4_0": ["gemv_kernel.cuh", "fmt_fields.cuh", "device_common.cuh", "launch_table.cuh", "formats.h", "fmt_q4_0.cu"],
     "pq2_0": ["gemv_kernel.cuh", "fmt_fields.cuh", "device_common.cuh", "launch_table.cuh", "formats.h", "fmt_pq2.cu"],
     "aqlm_2x8": ["gemv_kernel.cuh", "device_common.cuh", "formats.h", "fmt_aqlm.cu"],
+    "cbk4_row": ["gemv_kernel.cuh", "fmt_cbk.cuh", "device_common.cuh", "launch_table.cuh", "formats.h",
+                 "fmt_cbk4row.cu"],
+    "aqlm_1x16": ["gemv_kernel.cuh", "device_common.cuh", "formats.h", "fmt_aqlm1x16.cu"],
 }
 KERNEL_SOURCES_MMA = ["mma_kernel.cuh", "tc5_kernel.cuh", "fmt_aqlm_mma.cu"]
 
