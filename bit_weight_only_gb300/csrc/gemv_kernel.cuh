@@ -79,6 +79,7 @@ struct RunParams {
   int64_t N, K;
   int64_t T;             // tiles in the stream = nRT * nKT
   int nKT;               // k tiles per row tile
+  int split_unit;        // the stream-K split's mode (stream_split: 0 spread, 1 or 2 chunked)
   int skip_cta;          // test hook: this CTA does nothing (-1: none)
   const float* residual; // [M][N] fp32 added to y in the store (may be y itself), or null
   // PQ2_0 on prepared INT8 activations (x then points to their codes):
@@ -449,13 +450,31 @@ __device__ __noinline__ void finish_rows_glu(const RunParams& p, const CtaPlan& 
   }
 }
 
-// CTA c's share of the stream: [c * T / G, (c + 1) * T / G), with 32-bit
-// divisions when the products fit (the common case).
-__device__ __forceinline__ int64_t stream_split(int64_t c, int64_t T, int64_t G) {
-  const int64_t prod = c * T;
-  if (prod < (int64_t(1) << 31) && G < (int64_t(1) << 31))
-    return static_cast<int64_t>(static_cast<uint32_t>(prod) / static_cast<uint32_t>(G));
-  return prod / G;
+// CTA c's share of a stream of T work units.  U = 0: [c T / G, (c + 1) T / G)
+// (the larger runs spread evenly over the grid).  U = 1 or 2: chunks of U
+// consecutive units (the last chunk may be short); with n = ceil(T / U)
+// chunks, q = n / G and r = n % G, CTA c runs chunks [c q + min(c, r),
+// (c + 1) q + min(c + 1, r)) -- the first r CTAs take one chunk more.  CTAs
+// are placed in index order as SMs free up, so those with the extra chunk
+// start first and the last-placed ones carry less; with U = 2 the two halves
+// of a tile-parity kernel (alternate tiles) stay busy to the run's end.
+// 32-bit divisions when the sizes fit.
+__device__ __forceinline__ int64_t stream_split(int64_t c, int64_t T, int64_t G, int U = 0) {
+  if (U == 0) {
+    const int64_t prod = c * T;
+    if (prod < (int64_t(1) << 31) && G < (int64_t(1) << 31))
+      return static_cast<int64_t>(static_cast<uint32_t>(prod) / static_cast<uint32_t>(G));
+    return prod / G;
+  }
+  const int64_t n = U == 1 ? T : (T + U - 1) / U;
+  int64_t q;
+  if (n < (int64_t(1) << 31) && G < (int64_t(1) << 31))
+    q = static_cast<int64_t>(static_cast<uint32_t>(n) / static_cast<uint32_t>(G));
+  else
+    q = n / G;
+  const int64_t r = n - q * G;
+  const int64_t t = (c * q + (c < r ? c : r)) * U;
+  return t < T ? t : T;
 }
 
 __device__ __forceinline__ int64_t div_fast(int64_t a, int64_t b) {
@@ -625,8 +644,8 @@ __global__ void __launch_bounds__(gemv_threads<F, M>(), F::kCtasPerSm) wstream_k
   const int tid = threadIdx.x;
   const int64_t G = gridDim.x;
   const int64_t c = blockIdx.x;
-  const int64_t t0 = stream_split(c, p.T, G);
-  const int64_t t1 = stream_split(c + 1, p.T, G);
+  const int64_t t0 = stream_split(c, p.T, G, p.split_unit);
+  const int64_t t1 = stream_split(c + 1, p.T, G, p.split_unit);
 
   const int64_t rt_first = div_fast(t0, p.nKT);
 

@@ -118,6 +118,9 @@ bool is_device_pointer(const void* p) {
 //                           that have it (0: never, 1: every M), instead of
 //                           the measured default, so that tests and the
 //                           benchmark's crossover sweep reach both kernels;
+//   QGEMV_SPLIT=0|1|2       (not a fault) the stream-K split's mode
+//                           (stream_split) instead of the format's
+//                           measured choice, so that tests cover every mode;
 //   QGEMV_FAULT_SKIP_CTA=c  the handle's runs launch CTA c as a no-op, so
 //                           the CTAs that share a row tile with it never get
 //                           its partial sums: their bounded fix-up waits run
@@ -160,16 +163,26 @@ cudaError_t to_device(const void* src, size_t bytes, void** dst) {
 // the last contributor, unless the row tile opens that CTA's run (its part
 // is then done early), in which case the one before it.  Computed once per
 // handle so the kernels do no 64-bit divisions.
-int64_t split_point(int64_t c, int64_t T, int64_t G) { return c * T / G; }
-int64_t cta_of(int64_t t, int64_t T, int64_t G) { return ((t + 1) * G - 1) / T; }
+int64_t split_point(int64_t c, int64_t T, int64_t G, int64_t U) {
+  if (U == 0) return c * T / G;
+  const int64_t n = (T + U - 1) / U, q = n / G, r = n % G;
+  const int64_t t = (c * q + (c < r ? c : r)) * U;
+  return t < T ? t : T;
+}
+// the CTA whose run holds unit t
+int64_t cta_of(int64_t t, int64_t T, int64_t G, int64_t U) {
+  if (U == 0) return ((t + 1) * G - 1) / T;
+  const int64_t n = (T + U - 1) / U, q = n / G, r = n % G, u = t / U;
+  return u < r * (q + 1) ? u / (q + 1) : r + (u - r * (q + 1)) / q;
+}
 
-std::vector<qgemv::CtaPlan> plan_stream_k(int64_t T, int64_t G, int64_t nKT, int64_t rows) {
+std::vector<qgemv::CtaPlan> plan_stream_k(int64_t T, int64_t G, int64_t nKT, int64_t rows, int64_t U) {
   std::vector<qgemv::CtaPlan> plan(static_cast<size_t>(G));
   for (int64_t c = 0; c < G; ++c) {
     qgemv::CtaPlan& pl = plan[static_cast<size_t>(c)];
     std::memset(&pl, 0, sizeof(pl));
     pl.seg_rt[0] = pl.seg_rt[1] = -1;
-    const int64_t t0 = split_point(c, T, G), t1 = split_point(c + 1, T, G);
+    const int64_t t0 = split_point(c, T, G, U), t1 = split_point(c + 1, T, G, U);
     if (t1 <= t0) continue;
     auto owned = [&](int64_t r) { return r * nKT >= t0 && (r + 1) * nKT <= t1; };
     const int64_t first = t0 / nKT, last = (t1 - 1) / nKT;
@@ -179,16 +192,16 @@ std::vector<qgemv::CtaPlan> plan_stream_k(int64_t T, int64_t G, int64_t nKT, int
         ++sg;
         continue;
       }
-      const int64_t cf = cta_of(r * nKT, T, G);
-      const int64_t cl = cta_of((r + 1) * nKT - 1, T, G);
+      const int64_t cf = cta_of(r * nKT, T, G, U);
+      const int64_t cl = cta_of((r + 1) * nKT - 1, T, G, U);
       pl.seg_rt[sg] = r;
       pl.seg_cf[sg] = cf;
       const int64_t S = cl - cf + 1, k = c - cf;
       pl.seg_S[sg] = static_cast<int32_t>(S);
       pl.seg_r0[sg] = static_cast<int32_t>(k * rows / S);
       pl.seg_nr[sg] = static_cast<int32_t>((k + 1) * rows / S - k * rows / S);
-      const int64_t fin = split_point(cl + 1, T, G) > (r + 1) * nKT ? cl - 1 : cl;
-      pl.seg_flags[sg] = (split_point(cf, T, G) < r * nKT ? 1 : 0) | (c == fin ? 2 : 0);
+      const int64_t fin = split_point(cl + 1, T, G, U) > (r + 1) * nKT ? cl - 1 : cl;
+      pl.seg_flags[sg] = (split_point(cf, T, G, U) < r * nKT ? 1 : 0) | (c == fin ? 2 : 0);
       ++sg;
     }
   }
@@ -230,6 +243,7 @@ struct qgemv_ctx {
   int glu;              // qgemv_create_glu: gate and up interleaved, output SiLU(gate) * up
   int skip_cta;         // QGEMV_FAULT_SKIP_CTA test hook, -1 normally
   int tc5_min_m;        // runs of at least this many rows use the tensor-memory kernel (0: never)
+  int split_unit;       // the stream-K split's mode (0 spread, 1 or 2 front-loaded chunks)
   uint8_t* xq_ws;       // INT8 mode: the activation prologue's workspace (16 rows), allocated when turned on
   qgemv_ctx* mma;       // AQLM: the tensor-core companion (format kAqlmMma), else nullptr
 };
@@ -325,6 +339,8 @@ static qgemv_handle create_impl(int format, int64_t N, int64_t K, const void* pa
   h->magic = kMagic;
   h->skip_cta = env_int("QGEMV_FAULT_SKIP_CTA", -1);
   h->tc5_min_m = qgemv::has_tc5(format) ? env_int("QGEMV_TC5", ops->tc5_min_m) : 0;
+  h->split_unit = env_int("QGEMV_SPLIT", ops->split_unit);
+  if (h->split_unit < 0 || h->split_unit > 2) h->split_unit = ops->split_unit;
   if (h->tc5_min_m < 0 || h->tc5_min_m > qgemv::kMaxM) h->tc5_min_m = 0;
   if (!nested) {
     g_alloc_count = 0;
@@ -428,9 +444,9 @@ static qgemv_handle create_impl(int format, int64_t N, int64_t K, const void* pa
   if (e == cudaSuccess) {
     // a GLU handle's shared row tiles are finished in gate/up row pairs
     const int plan_rows = glu ? ops->tile_rows / 2 : ops->tile_rows;
-    std::vector<qgemv::CtaPlan> plan = plan_stream_k(h->T, h->grid, h->nKT, plan_rows);
+    std::vector<qgemv::CtaPlan> plan = plan_stream_k(h->T, h->grid, h->nKT, plan_rows, h->split_unit);
     if (h->grid_m1 != h->grid) {
-      const std::vector<qgemv::CtaPlan> plan1 = plan_stream_k(h->T, h->grid_m1, h->nKT, plan_rows);
+      const std::vector<qgemv::CtaPlan> plan1 = plan_stream_k(h->T, h->grid_m1, h->nKT, plan_rows, h->split_unit);
       plan.insert(plan.end(), plan1.begin(), plan1.end());
     }
     e = cudaMemcpy(h->plan, plan.data(), sizeof(qgemv::CtaPlan) * plan.size(), cudaMemcpyHostToDevice);
@@ -606,6 +622,7 @@ static qgemv::RunParams params_of(const qgemv_ctx* h, const void* x, float* y, c
   p.K = h->K;
   p.T = h->T;
   p.nKT = h->nKT;
+  p.split_unit = h->split_unit;
   p.skip_cta = h->skip_cta;
   p.residual = residual;
   p.x_scale = nullptr;
@@ -778,11 +795,12 @@ void qgemv_destroy(qgemv_handle h) {
   free_handle(h);
 }
 
-int qgemv_stream_k_plan(int64_t units, int grid, int64_t units_per_row_tile, int rows, int64_t* out) {
+int qgemv_stream_k_plan(int64_t units, int grid, int64_t units_per_row_tile, int rows, int split_unit,
+                        int64_t* out) {
   if (units <= 0 || grid <= 0 || units_per_row_tile <= 0 || rows <= 0 || out == nullptr ||
-      units % units_per_row_tile != 0 || grid > units)
+      units % units_per_row_tile != 0 || grid > units || split_unit < 0 || split_unit > 2)
     return set_error(QGEMV_ERR_ARG, "qgemv_stream_k_plan: bad sizes");
-  const std::vector<qgemv::CtaPlan> plan = plan_stream_k(units, grid, units_per_row_tile, rows);
+  const std::vector<qgemv::CtaPlan> plan = plan_stream_k(units, grid, units_per_row_tile, rows, split_unit);
   for (int c = 0; c < grid; ++c) {
     const qgemv::CtaPlan& pl = plan[static_cast<size_t>(c)];
     int64_t* o = out + static_cast<int64_t>(c) * 12;

@@ -53,7 +53,7 @@ _SIGNATURES = {
                                               ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
                                               ctypes.c_void_p]),
     "qgemv_stream_k_plan": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int, ctypes.c_int64, ctypes.c_int,
-                                           ctypes.POINTER(ctypes.c_int64)]),
+                                           ctypes.c_int, ctypes.POINTER(ctypes.c_int64)]),
     "qgemv_destroy": (None, [ctypes.c_void_p]),
     "qgemv_last_error": (ctypes.c_char_p, []),
     "qgemv_last_error_code": (ctypes.c_int, []),
@@ -188,12 +188,12 @@ def qgemv_status(h: int) -> int:
     return _check(load().qgemv_status(h))
 
 
-def qgemv_stream_k_plan(units: int, grid: int, units_per_row_tile: int, rows: int) -> list:
+def qgemv_stream_k_plan(units: int, grid: int, units_per_row_tile: int, rows: int, split_unit: int = 1) -> list:
     """The stream-K split the handles use (host only): per CTA a dict of its
     two shared-row-tile segments, each field a pair (first, last row tile);
     "side1" and "fin" are the two flag bits."""
     out = (ctypes.c_int64 * (12 * grid))()
-    _check(load().qgemv_stream_k_plan(units, grid, units_per_row_tile, rows, out))
+    _check(load().qgemv_stream_k_plan(units, grid, units_per_row_tile, rows, split_unit, out))
     keys = ("rt", "cf", "S", "r0", "nr", "flags")
     plan = [{k: (out[12 * c + 2 * i], out[12 * c + 2 * i + 1]) for i, k in enumerate(keys)}
             for c in range(grid)]

@@ -326,8 +326,12 @@ int qgemv_run_q4_0_noalloc(const void* packed, int64_t N, int64_t K, const void*
 /* The stream-K work split (host only, no GPU needed), as the handles use it:
  * `units` work units (prepared tiles; for AQLM_2X8 blocks of 2048 rows x 128
  * inputs) in row-major order, `units_per_row_tile` of them per row tile of
- * `rows` output rows, split over `grid` CTAs, CTA c running units
- * [c*units/grid, (c+1)*units/grid).  Writes 12
+ * `rows` output rows, split over `grid` CTAs: split_unit 0, CTA c runs
+ * units [c*units/grid, (c+1)*units/grid); split_unit 1 or 2, in chunks of
+ * that many consecutive units, n = ceil(units / split_unit) chunks, q = n /
+ * grid, r = n % grid, CTA c runs chunks [c*q + min(c, r), (c+1)*q + min(c+1,
+ * r)) (the last chunk may be short).  A handle uses its format's mode.
+ * Writes 12
  * int64 per CTA into `out` (caller-owned, grid*12 entries): for its two
  * shared-row-tile segments s = 0 (first row tile of its run), 1 (last):
  * out[c*12 + 0 + s] row tile (-1: none), [2 + s] first contributing CTA,
@@ -336,8 +340,10 @@ int qgemv_run_q4_0_noalloc(const void* packed, int64_t N, int64_t K, const void*
  * if the first contributor's run began before the row tile, bit 1 set if
  * this CTA finishes the whole row tile when it has at most 256 items (rows x
  * activation rows; then the others finish nothing).  Returns QGEMV_ERR_ARG if a
- * size is not positive, units % units_per_row_tile != 0 or grid > units.   */
-int qgemv_stream_k_plan(int64_t units, int grid, int64_t units_per_row_tile, int rows, int64_t* out);
+ * size is not positive, units % units_per_row_tile != 0, grid > units or
+ * split_unit is not 0, 1 or 2.                                               */
+int qgemv_stream_k_plan(int64_t units, int grid, int64_t units_per_row_tile, int rows, int split_unit,
+                        int64_t* out);
 
 /* Message and code of the last error on the calling thread ("" / 0 if none). */
 const char* qgemv_last_error(void);

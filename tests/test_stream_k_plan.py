@@ -1,7 +1,8 @@
 """Host-side checks of the stream-K work split (no GPU needed).
 
 The kernels split the stream of work units (prepared tiles, row tile after
-row tile) evenly over the CTAs.  A CTA writes a row tile's
+row tile) over the CTAs in chunks of one or two units, as evenly as the
+chunks allow, the first CTAs taking one chunk more.  A CTA writes a row tile's
 outputs itself when its run covers the whole row tile, else it stores its
 partial sums in one of its two slots: side 0 for the first row tile of its
 run (the one that began at or before its first unit), side 1 for the last.
@@ -22,16 +23,21 @@ def lib():
     return qgemv.load()
 
 
-def split(c, U, G):
-    return c * U // G
+def split(c, U, G, unit=1):
+    """Start of CTA c's run: the kernels' stream_split, restated."""
+    if unit == 0:
+        return c * U // G
+    n = -(-U // unit)
+    q, r = divmod(n, G)
+    return min((c * q + min(c, r)) * unit, U)
 
 
-def kernel_view(U, G, upr):
+def kernel_view(U, G, upr, unit=1):
     """What each CTA's kernel does: per row tile, the CTAs that store a
     partial (with the slot side they use) and the CTA that writes y."""
     writers, partials = {}, {}
     for c in range(G):
-        u0, u1 = split(c, U, G), split(c + 1, U, G)
+        u0, u1 = split(c, U, G, unit), split(c + 1, U, G, unit)
         for rt in range(u0 // upr, (u1 - 1) // upr + 1):
             owner = rt * upr >= u0 and (rt + 1) * upr <= u1
             if owner:
@@ -60,11 +66,12 @@ CASES = [
 ]
 
 
+@pytest.mark.parametrize("unit", [0, 1, 2])
 @pytest.mark.parametrize("U, G, upr, rows", CASES)
-def test_plan_matches_the_kernels_split(lib, U, G, upr, rows):
+def test_plan_matches_the_kernels_split(lib, U, G, upr, rows, unit):
     G = min(G, U)
-    plan = qgemv.qgemv_stream_k_plan(U, G, upr, rows)
-    writers, partials = kernel_view(U, G, upr)
+    plan = qgemv.qgemv_stream_k_plan(U, G, upr, rows, unit)
+    writers, partials = kernel_view(U, G, upr, unit)
     n_rt = U // upr
     for rt in range(n_rt):
         w, parts = writers.get(rt, []), partials.get(rt, [])
@@ -100,9 +107,9 @@ def test_plan_matches_the_kernels_split(lib, U, G, upr, rows):
         assert len(fins) == 1, (rt, fins)
         fc = fins[0]
         hi_of = {c: hi for c, _, _, hi in parts}
-        assert hi_of[fc] == split(fc + 1, U, G)
+        assert hi_of[fc] == split(fc + 1, U, G, unit)
         cl = ctas[-1]
-        assert fc == (cl - 1 if split(cl + 1, U, G) > (rt + 1) * upr else cl)
+        assert fc == (cl - 1 if split(cl + 1, U, G, unit) > (rt + 1) * upr else cl)
     # a CTA's plan names no row tile that it does not share
     for c in range(G):
         for s in range(2):
@@ -111,10 +118,17 @@ def test_plan_matches_the_kernels_split(lib, U, G, upr, rows):
                 assert any(cc == c for cc, _, _, _ in partials.get(rt, []))
 
 
-def test_plan_is_balanced_to_one_unit(lib):
-    U, G = 258 * 8, 152
-    sizes = [split(c + 1, U, G) - split(c, U, G) for c in range(G)]
-    assert max(sizes) - min(sizes) <= 1
+@pytest.mark.parametrize("unit", [1, 2])
+def test_plan_is_balanced_to_one_chunk_first_ctas_first(lib, unit):
+    for U, G in [(258 * 8, 152), (96 * 8, 152), (172 * 8, 152), (32 * 22, 152), (1001, 152)]:
+        sizes = [split(c + 1, U, G, unit) - split(c, U, G, unit) for c in range(G)]
+        assert sum(sizes) == U and split(G, U, G, unit) == U
+        # one chunk apart, and the stream's last chunk may be short
+        assert max(sizes) - min(sizes) <= 2 * unit - 1
+        # the larger runs come first (the CTAs placed first)
+        assert sizes == sorted(sizes, reverse=True) or sizes[-1] < unit
+        # chunks of two start on even units
+        assert all(split(c, U, G, unit) % unit == 0 or split(c, U, G, unit) == U for c in range(G))
 
 
 @pytest.mark.parametrize("args", [(0, 1, 1, 128), (10, 11, 10, 128), (12, 2, 5, 128), (10, 2, 5, 0)])
