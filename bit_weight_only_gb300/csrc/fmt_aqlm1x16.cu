@@ -9,8 +9,10 @@
 // kernel does, every looked-up entry is gathered from L2 (where the whole
 // codebook stays resident) and the products are taken in fp32:
 //   * one warp per output row at a time (rows grid-strided over the CTAs);
-//     lane l takes the 128-bit vectors l, l + 32, ... of the row's codes
-//     (8 codes each, 16 B, coalesced across the warp);
+//     per chunk of 256 groups, lane l takes groups l, l + 32, ..., l + 224,
+//     whose 8 codes the prepared layout keeps in the lane's 128-bit vector
+//     (16 B, coalesced across the warp), so that a warp's activation loads
+//     for one step are 32 consecutive groups' inputs (coalesced too);
 //   * for each code the 16-byte entry is one 128-bit load, reused for every
 //     activation row of the call, so each code and entry is read once per
 //     call whatever M is;
@@ -22,9 +24,10 @@
 // The bound is L2: each group costs a 32-byte sector for 16 useful bytes,
 // against 2 bytes of codes from HBM.
 //
-// Prepared layout: the codes as given, each row padded with zero codes to a
-// whole number of 256-code chunks (so every row starts 16-byte aligned);
-// aux = the codebook [65536][8] fp16, then the scales [N] fp16.
+// Prepared layout: each row padded with zero codes to a whole number of
+// 256-code chunks (so every row starts 16-byte aligned), and inside a chunk
+// the code of group 32e + l at position 8l + e (code_pos); aux = the
+// codebook [65536][8] fp16, then the scales [N] fp16.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -44,6 +47,13 @@ constexpr int64_t kCodebookBytes = 65536LL * 8 * 2;  // 1 MiB
 constexpr int kWarps = 8;
 constexpr int kThreads = 32 * kWarps;
 
+// Position in the prepared row of the code of group g (lane l = g % 32 of
+// its chunk's step e = (g % 256) / 32 holds it as element e of its vector).
+__host__ __device__ __forceinline__ int64_t code_pos(int64_t g) {
+  const int64_t gi = g % kChunkCodes;
+  return g - gi + (gi % 32) * 8 + gi / 32;
+}
+
 __device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
   f[0] = h2f(v.x & 0xffffu), f[1] = h2f(v.x >> 16);
   f[2] = h2f(v.y & 0xffffu), f[3] = h2f(v.y >> 16);
@@ -60,11 +70,17 @@ __global__ void __maxnreg__(64) aqlm1x16_kernel(const RunParams p, int M) {
   const unsigned short* scales =
       reinterpret_cast<const unsigned short*>(static_cast<const uint8_t*>(p.aux) + kCodebookBytes);
   const unsigned int* xw = reinterpret_cast<const unsigned int*>(p.x);  // fp16 pairs (x is 4-byte aligned)
+  // x 16-byte aligned (then every group's 8 inputs are, K being a multiple
+  // of 8): one 128-bit load per group and activation row instead of four
+  // 32-bit ones -- the loads, not the FMAs, fill the memory pipeline here
+  // (8192 x 28672 at M = 1: 122 -> 291 GB/s).  Staging x in shared memory
+  // instead measured slower (the lanes' 128-byte-apart reads conflict).
+  const bool xvec = (reinterpret_cast<uintptr_t>(p.x) & 15u) == 0;
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int64_t G = p.K / 8;                        // groups (codes) per row
   const int64_t pitch = int64_t(p.nKT) * kChunkCodes;  // codes per prepared row
-  const int nvec = static_cast<int>((G + 7) / 8);   // 128-bit code vectors holding real codes
+  const int nchunk = static_cast<int>((G + kChunkCodes - 1) / kChunkCodes);  // chunks holding real codes
 
   // Nothing above reads what an earlier kernel in the stream writes.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -75,15 +91,15 @@ __global__ void __maxnreg__(64) aqlm1x16_kernel(const RunParams p, int M) {
     float acc[MB];
 #pragma unroll
     for (int m = 0; m < MB; ++m) acc[m] = 0.f;
-    for (int v = lane; v < nvec; v += 32) {
-      const uint4 cv = __ldg(crow + v);
+    for (int ch = 0; ch < nchunk; ++ch) {
+      const uint4 cv = __ldg(crow + ch * 32 + lane);
       const uint32_t cw[4] = {cv.x, cv.y, cv.z, cv.w};
       uint4 ent[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) ent[e] = __ldg(cb + ((cw[e >> 1] >> (16 * (e & 1))) & 0xffffu));
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        const int64_t g = int64_t(v) * 8 + e;
+        const int64_t g = int64_t(ch) * kChunkCodes + 32 * e + lane;
         if (g < G) {  // padding codes (0) past the row's end are not used
           float c[8];
           unpack8(ent[e], c);
@@ -91,12 +107,14 @@ __global__ void __maxnreg__(64) aqlm1x16_kernel(const RunParams p, int M) {
           for (int m = 0; m < MB; ++m) {
             if (m < M) {
               const unsigned int* xr = xw + (m * p.K + g * 8) / 2;
+              const uint4 x8 = xvec ? __ldg(reinterpret_cast<const uint4*>(xr))
+                                    : make_uint4(__ldg(xr), __ldg(xr + 1), __ldg(xr + 2), __ldg(xr + 3));
+              const uint32_t x2[4] = {x8.x, x8.y, x8.z, x8.w};
               float d = 0.f;
 #pragma unroll
               for (int q = 0; q < 4; ++q) {
-                const unsigned int x2 = __ldg(xr + q);
-                d = fmaf(c[2 * q], h2f(x2 & 0xffffu), d);
-                d = fmaf(c[2 * q + 1], h2f(x2 >> 16), d);
+                d = fmaf(c[2 * q], h2f(x2[q] & 0xffffu), d);
+                d = fmaf(c[2 * q + 1], h2f(x2[q] >> 16), d);
               }
               acc[m] += d;
             }
@@ -123,7 +141,7 @@ __global__ void prepare_kernel(const uint16_t* __restrict__ canon, int64_t N, in
   for (int64_t e = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; e < total;
        e += int64_t(gridDim.x) * blockDim.x) {
     const int64_t n = e / pitch, g = e % pitch;
-    tiles[e] = g < G ? canon[n * G + g] : static_cast<uint16_t>(0);
+    tiles[n * pitch + code_pos(g)] = g < G ? canon[n * G + g] : static_cast<uint16_t>(0);
   }
 }
 
@@ -137,7 +155,7 @@ __global__ void dequant_kernel(const uint16_t* __restrict__ tiles, const uint8_t
   for (int64_t e = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; e < N * G;
        e += int64_t(gridDim.x) * blockDim.x) {
     const int64_t n = e / G, g = e % G;
-    const uint32_t code = tiles[n * pitch + g];
+    const uint32_t code = tiles[n * pitch + code_pos(g)];
     const float s = h2f(sc[n]);
 #pragma unroll
     for (int j = 0; j < 8; ++j) w_out[n * K + 8 * g + j] = __fmul_rn(s, h2f(cb[code * 8 + j]));
