@@ -155,8 +155,8 @@ __global__ void __launch_bounds__(kThreads, 1) aqlm_table_kernel(const RunParams
   const int hi = q >> 1;
   const int64_t G = gridDim.x;
   const int64_t c = blockIdx.x;
-  const int64_t u0 = stream_split(c, p.T, G, p.split_unit);
-  const int64_t u1 = stream_split(c + 1, p.T, G, p.split_unit);
+  const int64_t u0 = stream_split<0>(c, p.T, G);
+  const int64_t u1 = stream_split<0>(c + 1, p.T, G);
   const int64_t nunits = u1 - u0;
   const int nKC = p.nKT;
 

@@ -57,6 +57,7 @@ struct FmtCBK4 {
   __host__ __device__ static constexpr int stages(int M) { return M <= 4 ? 4 : 2; }
   static constexpr int kSharedBytes = kLutBytes;
   static constexpr int kCbEntries = 16;
+  static constexpr int kSplitMode = 1;      // front-loaded stream-K split
   static constexpr bool kGluTables = true;  // GLU: the up table in each entry row's second half
   static constexpr bool kMmaGlu = true;     // the GLU form of the tensor-core kernel
   static constexpr float kOutScale = 1.0f;
@@ -225,6 +226,7 @@ struct FmtCBK8 {
   static constexpr bool kTileParity = true;  // so the two warps of a slice take alternate tiles
   __host__ __device__ static constexpr int stages(int M) { return M <= 4 ? 4 : 2; }
   static constexpr int kCbEntries = 256;
+  static constexpr int kSplitMode = 1;      // front-loaded stream-K split
   static constexpr bool kGluTables = true;  // GLU: the up table in each entry row's second half
   static constexpr bool kMmaGlu = true;     // the GLU form of the tensor-core kernel
   static constexpr int kSharedBytes = kLutBytes;
@@ -389,6 +391,7 @@ struct FmtCBK4R {
   __host__ __device__ static constexpr int stages(int M) { return M <= 4 ? 4 : 2; }
   static constexpr int kSharedBytes = kLutBytes;    // the table region (8 KB of it used)
   static constexpr int kCbEntries = kTileRows * 16 * 2;  // fp16-sized units of a row tile's codebooks (8 KB)
+  static constexpr int kSplitMode = 1;                   // front-loaded stream-K split
   static constexpr float kOutScale = 1.0f;
   static constexpr int kSumGroups = 1;  // unused
   using XRegs = XRegsT<2>;

@@ -119,7 +119,7 @@ const FormatOps* ops_cbk4_row() {
       &smem_bytes, &setup, &launch, &prepare, &dequant, /*cb_entries=*/F::kCbEntries, /*tile_rows=*/128,
       /*partial_stride=*/128 * 16, /*aux_per_row=*/0, /*m1_ctas_per_sm=*/F::kCtasPerSm, /*rowgroup=*/0,
       /*launch_x_int8=*/nullptr, /*row_tables=*/1, /*launch_xq=*/nullptr,
-      /*launch_glu=*/&LaunchTable<F>::launch_glu, /*tc5_min_m=*/0, /*split_unit=*/1};
+      /*launch_glu=*/&LaunchTable<F>::launch_glu, /*tc5_min_m=*/0, /*split_unit=*/SplitModeOf<F>::value};
   return &ops;
 }
 

@@ -45,7 +45,7 @@ const FormatOps* ops_cbk8() {
       &prepare, &dequant, /*cb_entries=*/256, /*tile_rows=*/128, /*partial_stride=*/128 * 16,
       /*aux_per_row=*/0, /*m1_ctas_per_sm=*/LaunchTable<F>::kM1CtasPerSm,
       /*rowgroup=*/1, /*launch_x_int8=*/nullptr, /*row_tables=*/0, /*launch_xq=*/nullptr,
-      /*launch_glu=*/&LaunchTable<F>::launch_glu, /*tc5_min_m=*/kTc5DefaultMinM, /*split_unit=*/1};
+      /*launch_glu=*/&LaunchTable<F>::launch_glu, /*tc5_min_m=*/kTc5DefaultMinM, /*split_unit=*/SplitModeOf<F>::value};
   return &ops;
 }
 

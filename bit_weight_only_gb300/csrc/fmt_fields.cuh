@@ -232,6 +232,7 @@ struct FmtQ4_0 {
 //   scales [t][j = 0..3] fp16: d of row 4l+j, block s.
 struct FmtPQ2 {
   static constexpr int kKW = 128;
+  static constexpr int kSplitMode = 1;  // front-loaded stream-K split
   static constexpr int kKT = kKW * kSlices;                       // 1024
   static constexpr int kCodeBytes = kCodeBytes32;
   static constexpr int kTileBytes = kCodeBytes + kLaneSlots * 8;  // 34816
@@ -446,6 +447,7 @@ __device__ __forceinline__ void quant_i8_group(const float (&f)[4], float& a, in
 __host__ __device__ constexpr int i8_pos(int lane, int b) { return 16 * (lane >> 2) + 4 * b + (lane & 3); }
 
 struct FmtPQ2I8 {
+  static constexpr int kSplitMode = 1;  // the PQ2_0 handle's split (same plan)
   static constexpr int kKW = FmtPQ2::kKW;  // 128: one block, one INT8 group
   static constexpr int kKT = FmtPQ2::kKT;
   static constexpr int kCodeBytes = FmtPQ2::kCodeBytes;

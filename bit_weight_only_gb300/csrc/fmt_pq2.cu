@@ -406,7 +406,7 @@ const FormatOps* ops_pq2() {
       &prepare, &dequant, /*cb_entries=*/0, /*tile_rows=*/128, /*partial_stride=*/128 * 16,
       /*aux_per_row=*/0, /*m1_ctas_per_sm=*/LaunchTable<F>::kM1CtasPerSm, /*rowgroup=*/0,
       /*launch_x_int8=*/&launch_x_int8, /*row_tables=*/0, /*launch_xq=*/&launch_xq,
-      /*launch_glu=*/&LaunchTable<F>::launch_glu, /*tc5_min_m=*/kTc5DefaultMinM, /*split_unit=*/1};
+      /*launch_glu=*/&LaunchTable<F>::launch_glu, /*tc5_min_m=*/kTc5DefaultMinM, /*split_unit=*/SplitModeOf<F>::value};
   static_assert(I8::kM1CtasPerSm == LaunchTable<F>::kM1CtasPerSm && FmtPQ2I8::kKT == F::kKT &&
                     FmtPQ2I8::kTileBytes == F::kTileBytes,
                 "the INT8 path runs on the PQ2_0 handle's tiles, grid and plan");

@@ -185,7 +185,7 @@ const FormatOps* ops_q4_0() {
       &prepare, &dequant, /*cb_entries=*/0, /*tile_rows=*/128, /*partial_stride=*/128 * 16,
       /*aux_per_row=*/0, /*m1_ctas_per_sm=*/LaunchTable<F>::kM1CtasPerSm, /*rowgroup=*/0,
       /*launch_x_int8=*/nullptr, /*row_tables=*/0, /*launch_xq=*/nullptr,
-      /*launch_glu=*/&LaunchTable<F>::launch_glu, /*tc5_min_m=*/kTc5DefaultMinM, /*split_unit=*/0};
+      /*launch_glu=*/&LaunchTable<F>::launch_glu, /*tc5_min_m=*/kTc5DefaultMinM, /*split_unit=*/SplitModeOf<F>::value};
   return &ops;
 }
 

@@ -73,7 +73,8 @@ struct FormatOps {
   // formats with the tensor-memory kernel (tc5_kernel.cuh): the smallest M
   // that runs it by default (0: not by default)
   int tc5_min_m = 0;
-  // the stream-K split (stream_split): 0 spread, 1 or 2 front-loaded chunks.
+  // the stream-K split (stream_split): 0 spread, 1 or 2 front-loaded chunks;
+  // the kernels' formula is the format's compile-time F::kSplitMode.
   // Measured (same box): front-loaded single tiles gain 2.5% on the 7B CBK4
   // stack (3% at M = 8), 7.5% on CBK4 11008x4096 and 11% on the PQ2_0
   // 5120/17408 model's projections at M = 1; Q4_0 is even at M = 1 and 2.7%

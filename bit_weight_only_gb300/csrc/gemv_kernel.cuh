@@ -79,7 +79,6 @@ struct RunParams {
   int64_t N, K;
   int64_t T;             // tiles in the stream = nRT * nKT
   int nKT;               // k tiles per row tile
-  int split_unit;        // the stream-K split's mode (stream_split: 0 spread, 1 or 2 chunked)
   int skip_cta;          // test hook: this CTA does nothing (-1: none)
   const float* residual; // [M][N] fp32 added to y in the store (may be y itself), or null
   // PQ2_0 on prepared INT8 activations (x then points to their codes):
@@ -450,17 +449,18 @@ __device__ __noinline__ void finish_rows_glu(const RunParams& p, const CtaPlan& 
   }
 }
 
-// CTA c's share of a stream of T work units.  U = 0: [c T / G, (c + 1) T / G)
-// (the larger runs spread evenly over the grid).  U = 1 or 2: chunks of U
-// consecutive units (the last chunk may be short); with n = ceil(T / U)
-// chunks, q = n / G and r = n % G, CTA c runs chunks [c q + min(c, r),
-// (c + 1) q + min(c + 1, r)) -- the first r CTAs take one chunk more.  CTAs
-// are placed in index order as SMs free up, so those with the extra chunk
-// start first and the last-placed ones carry less; with U = 2 the two halves
-// of a tile-parity kernel (alternate tiles) stay busy to the run's end.
-// 32-bit divisions when the sizes fit.
-__device__ __forceinline__ int64_t stream_split(int64_t c, int64_t T, int64_t G, int U = 0) {
-  if (U == 0) {
+// CTA c's share of a stream of T work units, in the split mode U of the
+// format (a compile-time constant, so a kernel carries one formula).
+// U = 0: [c T / G, (c + 1) T / G) (the larger runs spread evenly over the
+// grid).  U = 1 or 2: chunks of U consecutive units (the last chunk may be
+// short); with n = ceil(T / U) chunks, q = n / G and r = n % G, CTA c runs
+// chunks [c q + min(c, r), (c + 1) q + min(c + 1, r)) -- the first r CTAs
+// take one chunk more.  CTAs are placed in index order as SMs free up, so
+// those with the extra chunk start first and the last-placed ones carry
+// less.  32-bit divisions when the sizes fit.
+template <int U>
+__device__ __forceinline__ int64_t stream_split(int64_t c, int64_t T, int64_t G) {
+  if constexpr (U == 0) {
     const int64_t prod = c * T;
     if (prod < (int64_t(1) << 31) && G < (int64_t(1) << 31))
       return static_cast<int64_t>(static_cast<uint32_t>(prod) / static_cast<uint32_t>(G));
@@ -533,6 +533,16 @@ constexpr int kGluUpTable = 128;  // byte offset of the up table in each entry r
 // global memory by the rebuild.
 template <class F>
 constexpr bool kStagedCb = F::kCbEntries > 0 && F::kCbEntries <= 256;
+
+// The format's stream-K split mode (F::kSplitMode; 0 when absent).
+template <class F, class = void>
+struct SplitModeOf {
+  static constexpr int value = 0;
+};
+template <class F>
+struct SplitModeOf<F, decltype(void(F::kSplitMode))> {
+  static constexpr int value = F::kSplitMode;
+};
 
 template <class F>
 struct alignas(16) NextTable {
@@ -644,8 +654,8 @@ __global__ void __launch_bounds__(gemv_threads<F, M>(), F::kCtasPerSm) wstream_k
   const int tid = threadIdx.x;
   const int64_t G = gridDim.x;
   const int64_t c = blockIdx.x;
-  const int64_t t0 = stream_split(c, p.T, G, p.split_unit);
-  const int64_t t1 = stream_split(c + 1, p.T, G, p.split_unit);
+  const int64_t t0 = stream_split<SplitModeOf<F>::value>(c, p.T, G);
+  const int64_t t1 = stream_split<SplitModeOf<F>::value>(c + 1, p.T, G);
 
   const int64_t rt_first = div_fast(t0, p.nKT);
 
@@ -822,7 +832,8 @@ __global__ void __launch_bounds__(gemv_threads<F, M>(), F::kCtasPerSm) wstream_k
       for (int j = i + ((i ^ half) & 1); j < iend; j += 2) {
         bool abort = s_abort != 0;
         const int u = j + NS - 2;
-        if (leader && !abort && u < nt) {
+        // tiles below kPre came from the prologue: never fill a stage twice
+        if (leader && !abort && u >= kPre && u < nt) {
           const int su = u % NS;
           if (u >= NS && !mbar_wait_bounded(&empty[su], static_cast<uint32_t>(((u - NS) / NS) & 1))) {
             atomicOr(p.err, kErrTimeoutEmpty);

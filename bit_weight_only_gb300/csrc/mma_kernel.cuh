@@ -312,8 +312,8 @@ __global__ void __launch_bounds__(mma_threads<F, NB, PAR>(), F::mma_ctas(NB)) ws
   const int ti = par * SG + sgrp;  // index of the warp's partial sums in the row-tile tree
   const int64_t G = gridDim.x;
   const int64_t c = blockIdx.x;
-  const int64_t t0 = stream_split(c, p.T, G, p.split_unit);
-  const int64_t t1 = stream_split(c + 1, p.T, G, p.split_unit);
+  const int64_t t0 = stream_split<SplitModeOf<F>::value>(c, p.T, G);
+  const int64_t t1 = stream_split<SplitModeOf<F>::value>(c + 1, p.T, G);
   const int ntiles = static_cast<int>(t1 - t0);
   const int64_t rt_first = div_fast(t0, p.nKT);
 
@@ -610,7 +610,8 @@ __global__ void __launch_bounds__(mma_threads<F, NB, PAR>(), F::mma_ctas(NB)) ws
       for (int j = i + ((i ^ par) & 1); j < iend; j += 2) {
         bool abort = s_abort != 0;
         const int u = j + NS - 2;
-        if (leader && !abort && u < nt) {
+        // tiles 0 and 1 came from the prologue: never fill a stage twice
+        if (leader && !abort && u >= 2 && u < nt) {
           const int sn = u % NS;
           if (u >= NS && !mbar_wait_bounded(&empty[sn], static_cast<uint32_t>(((u - NS) / NS) & 1))) {
             atomicOr(p.err, kErrTimeoutEmpty);

@@ -118,9 +118,6 @@ bool is_device_pointer(const void* p) {
 //                           that have it (0: never, 1: every M), instead of
 //                           the measured default, so that tests and the
 //                           benchmark's crossover sweep reach both kernels;
-//   QGEMV_SPLIT=0|1|2       (not a fault) the stream-K split's mode
-//                           (stream_split) instead of the format's
-//                           measured choice, so that tests cover every mode;
 //   QGEMV_FAULT_SKIP_CTA=c  the handle's runs launch CTA c as a no-op, so
 //                           the CTAs that share a row tile with it never get
 //                           its partial sums: their bounded fix-up waits run
@@ -243,7 +240,6 @@ struct qgemv_ctx {
   int glu;              // qgemv_create_glu: gate and up interleaved, output SiLU(gate) * up
   int skip_cta;         // QGEMV_FAULT_SKIP_CTA test hook, -1 normally
   int tc5_min_m;        // runs of at least this many rows use the tensor-memory kernel (0: never)
-  int split_unit;       // the stream-K split's mode (0 spread, 1 or 2 front-loaded chunks)
   uint8_t* xq_ws;       // INT8 mode: the activation prologue's workspace (16 rows), allocated when turned on
   qgemv_ctx* mma;       // AQLM: the tensor-core companion (format kAqlmMma), else nullptr
 };
@@ -339,8 +335,6 @@ static qgemv_handle create_impl(int format, int64_t N, int64_t K, const void* pa
   h->magic = kMagic;
   h->skip_cta = env_int("QGEMV_FAULT_SKIP_CTA", -1);
   h->tc5_min_m = qgemv::has_tc5(format) ? env_int("QGEMV_TC5", ops->tc5_min_m) : 0;
-  h->split_unit = env_int("QGEMV_SPLIT", ops->split_unit);
-  if (h->split_unit < 0 || h->split_unit > 2) h->split_unit = ops->split_unit;
   if (h->tc5_min_m < 0 || h->tc5_min_m > qgemv::kMaxM) h->tc5_min_m = 0;
   if (!nested) {
     g_alloc_count = 0;
@@ -444,9 +438,9 @@ static qgemv_handle create_impl(int format, int64_t N, int64_t K, const void* pa
   if (e == cudaSuccess) {
     // a GLU handle's shared row tiles are finished in gate/up row pairs
     const int plan_rows = glu ? ops->tile_rows / 2 : ops->tile_rows;
-    std::vector<qgemv::CtaPlan> plan = plan_stream_k(h->T, h->grid, h->nKT, plan_rows, h->split_unit);
+    std::vector<qgemv::CtaPlan> plan = plan_stream_k(h->T, h->grid, h->nKT, plan_rows, ops->split_unit);
     if (h->grid_m1 != h->grid) {
-      const std::vector<qgemv::CtaPlan> plan1 = plan_stream_k(h->T, h->grid_m1, h->nKT, plan_rows, h->split_unit);
+      const std::vector<qgemv::CtaPlan> plan1 = plan_stream_k(h->T, h->grid_m1, h->nKT, plan_rows, ops->split_unit);
       plan.insert(plan.end(), plan1.begin(), plan1.end());
     }
     e = cudaMemcpy(h->plan, plan.data(), sizeof(qgemv::CtaPlan) * plan.size(), cudaMemcpyHostToDevice);
@@ -622,7 +616,6 @@ static qgemv::RunParams params_of(const qgemv_ctx* h, const void* x, float* y, c
   p.K = h->K;
   p.T = h->T;
   p.nKT = h->nKT;
-  p.split_unit = h->split_unit;
   p.skip_cta = h->skip_cta;
   p.residual = residual;
   p.x_scale = nullptr;

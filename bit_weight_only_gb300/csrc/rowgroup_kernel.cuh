@@ -86,8 +86,8 @@ __global__ void __launch_bounds__(kRgThreads, 1) rowgroup_stream_kernel(const Ru
   const int nKT = static_cast<int>(p.nKT);
   const int64_t U = div_fast(p.T, p.nKT) * kRowsPerLane;  // units
   const int64_t G = gridDim.x;
-  const int64_t u0 = stream_split(blockIdx.x, U, G);
-  const int64_t u1 = stream_split(blockIdx.x + 1, U, G);
+  const int64_t u0 = stream_split<0>(blockIdx.x, U, G);
+  const int64_t u1 = stream_split<0>(blockIdx.x + 1, U, G);
   const int nch = (nKT + kRgSub - 1) / kRgSub;  // stages per unit
   const int nq = static_cast<int>(u1 - u0) * nch;
 
@@ -168,7 +168,8 @@ __global__ void __launch_bounds__(kRgThreads, 1) rowgroup_stream_kernel(const Ru
     for (int q = qb + ((qb ^ half) & 1); q < qb + nch; q += 2) {
       bool abort = s_abort != 0;
       const int qn = q + NS - 2;
-      if (leader && !abort && qn < nq) {
+      // stages 0 and 1 came from the prologue: never fill a stage twice
+      if (leader && !abort && qn >= 2 && qn < nq) {
         if (qn >= NS && !mbar_wait_bounded(&empty[qn % NS], static_cast<uint32_t>(((qn - NS) / NS) & 1))) {
           atomicOr(p.err, kErrTimeoutEmpty);
           s_abort = 1;

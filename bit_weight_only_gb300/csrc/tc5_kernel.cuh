@@ -386,8 +386,8 @@ __global__ void __launch_bounds__(kTc5Threads, 1) tc5_kernel(const RunParams p, 
   const int jr = lane >> 3;
   const int64_t Gd = gridDim.x;
   const int64_t c = blockIdx.x;
-  const int64_t t0 = stream_split(c, p.T, Gd, p.split_unit);
-  const int64_t t1 = stream_split(c + 1, p.T, Gd, p.split_unit);
+  const int64_t t0 = stream_split<SplitModeOf<F>::value>(c, p.T, Gd);
+  const int64_t t1 = stream_split<SplitModeOf<F>::value>(c + 1, p.T, Gd);
   const int ntiles = static_cast<int>(t1 - t0);
   const int64_t rt_first = div_fast(t0, p.nKT);
   const uint64_t pol = l2_policy_evict_first();

@@ -105,25 +105,22 @@ def test_gemv_many_tiles_per_cta(fmt, M):
 
 
 @pytest.mark.parametrize("fmt", FORMATS)
-@pytest.mark.parametrize("split", [0, 1, 2])
 @pytest.mark.parametrize("shape", ["multi", "stack_qkv"])
-def test_every_split_mode_matches_oracle(fmt, split, shape, monkeypatch):
-    """The stream-K split's three modes (QGEMV_SPLIT: spread, front-loaded
-    single tiles or tile pairs) on the M = 1 CUDA-core kernel, the M = 2 and
-    the two-block tensor-core kernels: the plan made on the host and the runs
-    the kernels take agree, and every output is within the bound.  stack_qkv:
-    a 7B q|k|v-sized shape whose tile count is not a multiple of the grid."""
+def test_split_runs_match_oracle(fmt, shape, monkeypatch):
+    """Each format's stream-K split (spread for Q4_0 and AQLM 2x8, front-loaded
+    for the others) on the M = 1 CUDA-core kernel, the M = 2 and the
+    two-block tensor-core kernels: the plan made on the host and the runs the
+    kernels take agree, and every output is within the bound.  stack_qkv: a
+    7B q|k|v-sized shape whose tile count is not a multiple of the grid."""
     N, K = MULTI[fmt] if shape == "multi" else (12288 if fmt != "aqlm_2x8" else 10240, 4096)
     packed, scales, cb = make_case(fmt, N, K, tag=f"split/{shape}")
-    monkeypatch.setenv("QGEMV_SPLIT", str(split))
     monkeypatch.setenv("QGEMV_ROWGROUP", "0")
     h = qgemv.QGemv(fmt, N, K, packed, scales, cb)
-    monkeypatch.delenv("QGEMV_SPLIT")
     monkeypatch.delenv("QGEMV_ROWGROUP")
     for M in (1, 2, 11):
         x = make_x(M, K, tag="split")
         y_ref, bound = oracle.gemv(fmt, N, K, packed, scales, cb, x)
-        assert_within(gpu_gemv(h, x), y_ref, bound, f"{fmt} split={split} {N}x{K} M={M}")
+        assert_within(gpu_gemv(h, x), y_ref, bound, f"{fmt} {N}x{K} M={M}")
 
 
 @pytest.mark.parametrize("fmt", FORMATS)
