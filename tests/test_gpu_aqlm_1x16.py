@@ -8,8 +8,9 @@ Bars:
     once for all rows, and each row's arithmetic is the same for every M);
   * the residual form is fl32(plain + residual), bit for bit;
   * stacking is refused.
-Shapes: ragged code vectors (K/8 not a multiple of 8), a single group, and
-the 70B layer at full size (gate/up 28672 x 8192, down 8192 x 28672, q/o
+Shapes: ragged code vectors (K/8 not a multiple of 8), a single group, x
+only 4-byte aligned, more rows than one pass of the grid, and the 70B layer
+at full size (gate/up 28672 x 8192, down 8192 x 28672, q/o
 8192 x 8192) on sampled rows, at M = 1 and the verify batch M = 16.
 """
 import numpy as np
@@ -51,7 +52,7 @@ def test_dequant_bit_exact(N, K):
 
 
 @pytest.mark.parametrize("N,K", [(300, 1032), (129, 8), (700, 2056)])
-@pytest.mark.parametrize("M", [1, 2, 3, 16])
+@pytest.mark.parametrize("M", [1, 2, 3, 8, 16])
 def test_gemv_matches_oracle(N, K, M):
     codes, scales, cb = make_case(FMT, N, K, tag="a16")
     h = qgemv.QGemv(FMT, N, K, codes, scales, cb)
@@ -60,6 +61,43 @@ def test_gemv_matches_oracle(N, K, M):
     y_ref, bound = oracle.gemv(FMT, N, K, codes, scales, cb, x_np)
     ok = oracle.within_tolerance(y, y_ref, bound)
     assert ok.all(), f"{N}x{K} M={M}: {np.count_nonzero(~ok)} outputs out of tolerance"
+
+
+@pytest.mark.parametrize("M", [1, 3, 8, 16])
+def test_x_only_4_byte_aligned(M):
+    """x 4 bytes past a 16-byte boundary (the API's minimum): the activation
+    loads (M = 1) and the shared-memory copies (M > 1) take 4-byte pieces."""
+    N, K = 300, 2056
+    codes, scales, cb = make_case(FMT, N, K, tag="a16al")
+    x_np = make_x(M, K, tag="a16al")
+    buf = torch.zeros(M * K + 8, dtype=torch.float16, device="cuda")
+    x = buf[2:2 + M * K].view(M, K)
+    assert x.data_ptr() % 16 == 4
+    x.copy_(torch.from_numpy(x_np).cuda())
+    h = qgemv.QGemv(FMT, N, K, codes, scales, cb)
+    y = h.gemv(x)
+    torch.cuda.synchronize()
+    assert h.status() == qgemv.QGEMV_OK
+    y_ref, bound = oracle.gemv(FMT, N, K, codes, scales, cb, x_np)
+    ok = oracle.within_tolerance(y.cpu().numpy(), y_ref, bound)
+    assert ok.all(), f"M={M}: {np.count_nonzero(~ok)} outputs out of tolerance"
+
+
+@pytest.mark.parametrize("M", [1, 3, 8])
+def test_rows_beyond_one_pass_of_the_grid(M):
+    """More rows than one pass of the largest grid (65,535 CTAs of eight
+    warps): CTAs take a second row each, and with M > 1 they copy the next
+    rows' first activations while finishing the current ones."""
+    N, K = 65535 * 8 + 301, 2064
+    codes, scales, cb = make_case(FMT, N, K, tag="a16pass")
+    h = qgemv.QGemv(FMT, N, K, codes, scales, cb)
+    x_np = make_x(M, K, tag="a16pass")
+    y = _gemv(h, x_np)
+    rows = np.array(sorted(set([0, 7, 65535 * 8 - 1, 65535 * 8, 65535 * 8 + 7, N - 1] +
+                               np.random.default_rng(3).integers(0, N, size=64).tolist())), dtype=np.int64)
+    y_ref, bound = oracle.gemv(FMT, N, K, codes, scales, cb, x_np, rows=rows)
+    ok = oracle.within_tolerance(y[:, rows], y_ref, bound)
+    assert ok.all(), f"M={M}: {np.count_nonzero(~ok)} sampled outputs out of tolerance"
 
 
 def _sample_rows(N, n=48, seed=0):
