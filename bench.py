@@ -176,6 +176,10 @@ WORKLOADS = {
     "cbk4_gate": (lambda: [("cbk4", "gate", 11008, 4096)], "cbk4", "CBK4 7B gate projection 11008x4096"),
     "aqlm_70b_layer": (lambda: [("aqlm_2x8", n, N, K) for n, N, K in LLAMA70B_AQLM], "aqlm_2x8",
                        "70B-shaped AQLM 2x8 layer: gate, up 28672x8192, down 8192x28672, q, o 8192x8192"),
+    "aqlm_70b_layer_stacked": (lambda: [("aqlm_2x8", "gate_up", [28672, 28672], 8192)] +
+                               [("aqlm_2x8", n, N, K) for n, N, K in LLAMA70B_AQLM[2:]], "aqlm_2x8",
+                               "70B-shaped AQLM 2x8 layer with gate|up stacked (one call, a codebook pair "
+                               "each): gate|up 57344x8192, down 8192x28672, q, o 8192x8192"),
     "aqlm_down": (lambda: [("aqlm_2x8", "down", 8192, 28672)], "aqlm_2x8", "AQLM 2x8 down 8192x28672"),
     "aqlm1x16_70b_layer": (lambda: [("aqlm_1x16", n, N, K) for n, N, K in LLAMA70B_AQLM], "aqlm_1x16",
                            "70B-shaped AQLM 1x16 layer: gate, up 28672x8192, down 8192x28672, q, o 8192x8192"),
@@ -215,14 +219,24 @@ def build_handles(specs, M, device, seed=0):
         tag = f"bench/{name}"
         scales = cb = None
         if isinstance(N, (list, tuple)):   # stacked projections, one codebook each
-            assert fmt == "cbk4"
             segs = list(N)
-            packed = torch.cat([inputs.cbk_packed_cuda(f"{tag}/{s}", n, K, 4, p16, device, seed)
-                                for s, n in enumerate(segs)])
-            h = qgemv.QGemv.stacked(fmt, segs, K, packed, None, np.concatenate([c16] * len(segs)))
+            if fmt == "cbk4":
+                packed = torch.cat([inputs.cbk_packed_cuda(f"{tag}/{s}", n, K, 4, p16, device, seed)
+                                    for s, n in enumerate(segs)])
+                h = qgemv.QGemv.stacked(fmt, segs, K, packed, None, np.concatenate([c16] * len(segs)))
+                extra = canonical_extra_bytes(fmt, sum(segs)) * len(segs)
+            elif fmt == "aqlm_2x8":  # codes, scales and a codebook pair per segment
+                parts = [inputs.aqlm_inputs_cuda(f"{tag}/{s}", n, K, device=device, seed=seed)
+                         for s, n in enumerate(segs)]
+                packed = torch.cat([q[0] for q in parts])
+                h = qgemv.QGemv.stacked(fmt, segs, K, packed, torch.cat([q[1] for q in parts]),
+                                        torch.cat([q[2] for q in parts]))
+                extra = 2 * sum(segs) + 8192 * len(segs)
+                del parts
+            else:
+                raise ValueError(fmt)
             N = sum(segs)
-            nbytes = (qgemv.qgemv_packed_bytes(fmt, N, K) + canonical_extra_bytes(fmt, N) * len(segs)
-                      + 2 * M * K + 4 * M * N)
+            nbytes = qgemv.qgemv_packed_bytes(fmt, N, K) + extra + 2 * M * K + 4 * M * N
             del packed
             x = x_all[xo:xo + M * K].view(M, K)
             x.copy_(inputs.x_fp16_cuda(f"{tag}/x", M, K, device=device, seed=seed))

@@ -45,6 +45,13 @@
 //
 // M > 1: a pass handles MB <= 2 activation rows (one 64 KB table slab each)
 // and a call with M rows makes ceil(M / 2) passes over the codes.
+//
+// Stacked handles (several projections sharing K, e.g. gate|up): segment s
+// has its own codebook pair; segments start on 2048-row blocks, so every
+// row block has one pair.  aux = the nseg codebook pairs, the row scales,
+// then the segment of every row block (seg_of_rt).  The warps load the B
+// fragments of a row block's pair when the tables of its first unit are
+// built (only when the segment changes).
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -140,6 +147,12 @@ __device__ __forceinline__ void lookup_row(const uint4 (&cr)[2], const uint32_t 
   }
 }
 
+// Codebook pairs before the row scales in aux: one, or (stacked handles)
+// one per segment, the last row block's segment being the last segment.
+__device__ __forceinline__ int codebook_pairs(const int32_t* seg_of_rb, int64_t nRB) {
+  return seg_of_rb != nullptr ? seg_of_rb[nRB - 1] + 1 : 1;
+}
+
 template <int MB>
 __global__ void __launch_bounds__(kThreads, 1) aqlm_table_kernel(const RunParams p) {
   if (static_cast<int>(blockIdx.x) == p.skip_cta) return;  // test hook (QGEMV_FAULT_SKIP_CTA)
@@ -184,16 +197,27 @@ __global__ void __launch_bounds__(kThreads, 1) aqlm_table_kernel(const RunParams
 
   // B fragments of this warp's entry tiles nt = 4 * warp + j.  Column n of a
   // tile is codebook (n >> 1) & 1, entry 4 * nt + 2 * (n >> 2) + (n & 1).
-  const uint16_t* cb = static_cast<const uint16_t*>(p.aux);
+  // Stacked handles: the pair of segment seg (loaded by load_bf).
+  const int32_t* seg_of_rb = p.seg_of_rt;
+  const uint8_t* aux = static_cast<const uint8_t*>(p.aux);
   uint32_t bf[4];
+  int bseg = -1;  // segment whose pair bf holds
+  auto load_bf = [&](int seg) {
+    const uint16_t* cb = reinterpret_cast<const uint16_t*>(aux + int64_t(seg) * kCodebookBytes);
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int nt = 4 * warp + j;
-    const int cbi = (gi >> 1) & 1;
-    const int e = 4 * nt + 2 * (gi >> 2) + (gi & 1);
-    bf[j] = ldg_u32(cb + (cbi * 256 + e) * 8 + 2 * q);
-  }
-  const __half* scales = reinterpret_cast<const __half*>(static_cast<const uint8_t*>(p.aux) + kCodebookBytes);
+    for (int j = 0; j < 4; ++j) {
+      const int nt = 4 * warp + j;
+      const int cbi = (gi >> 1) & 1;
+      const int e = 4 * nt + 2 * (gi >> 2) + (gi & 1);
+      bf[j] = ldg_u32(cb + (cbi * 256 + e) * 8 + 2 * q);
+    }
+    bseg = seg;
+  };
+  const int64_t nRB = p.T / nKC;
+  const __half* scales =
+      reinterpret_cast<const __half*>(aux + int64_t(codebook_pairs(seg_of_rb, nRB)) * kCodebookBytes);
+  auto seg_of = [&](int64_t r) { return seg_of_rb != nullptr ? seg_of_rb[r] : 0; };
+  load_bf(nunits > 0 ? seg_of(div_fast(u0, nKC)) : 0);
 
   // Table store addresses: D values of this lane are slots 2 * gi + (q & 1)
   // (rows gi) and that + 16 (rows gi + 8), entries eA and eA + 1.
@@ -307,6 +331,10 @@ __global__ void __launch_bounds__(kThreads, 1) aqlm_table_kernel(const RunParams
     constexpr int BUF = decltype(buf_tag)::value;
     const int k1 = next_kc(kc);
     if (i + 1 < nunits) {
+      if (seg_of_rb != nullptr && k1 == 0) {  // the next unit opens row block rb + 1
+        const int sn = seg_of_rb[rb + 1];
+        if (sn != bseg) load_bf(sn);
+      }
       build(xf, (1 - BUF) * 128);
       if (i + 2 < nunits) load_xf(xf, next_kc(k1));
     }
@@ -372,15 +400,18 @@ __global__ void prepare_kernel(const uint8_t* __restrict__ canon, int64_t N, int
 // sum and product are exact in fp64 (fp16 operands), so the one rounding to
 // fp32 gives the correctly rounded weight.
 __global__ void dequant_kernel(const uint8_t* __restrict__ tiles, const uint8_t* __restrict__ aux,
-                               int64_t N, int64_t K, int nKC, float* __restrict__ w_out) {
+                               const int32_t* __restrict__ seg_of_rb, int64_t N, int64_t K, int nKC,
+                               float* __restrict__ w_out) {
   const int64_t ng = K / 8;
-  const __half* cbk = reinterpret_cast<const __half*>(aux);
-  const __half* sc = reinterpret_cast<const __half*>(aux + kCodebookBytes);
+  const int64_t nRB = (N + kRows - 1) / kRows;
+  const __half* sc = reinterpret_cast<const __half*>(aux + int64_t(codebook_pairs(seg_of_rb, nRB)) * kCodebookBytes);
   for (int64_t t = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; t < N * ng;
        t += int64_t(gridDim.x) * blockDim.x) {
     const int64_t n = t / ng;
     const int64_t g = t % ng;
     const int64_t rb = n / kRows;
+    const __half* cbk =
+        reinterpret_cast<const __half*>(aux + int64_t(seg_of_rb != nullptr ? seg_of_rb[rb] : 0) * kCodebookBytes);
     const int nl = static_cast<int>(n % kRows);
     const int r = nl >> 9, warp = (nl >> 5) & 15, lane = nl & 31;
     const int64_t kc = g / 16;
@@ -413,16 +444,16 @@ cudaError_t prepare(const PrepareArgs& a, cudaStream_t s) {
   prepare_kernel<<<grid_for(nvec), 256, 0, s>>>(a.packed, a.N, a.K, a.nKT, nvec, a.tiles);
   cudaError_t e = cudaGetLastError();
   uint8_t* aux = static_cast<uint8_t*>(a.aux);
-  if (e == cudaSuccess)
-    e = cudaMemcpyAsync(aux, a.codebooks, kCodebookBytes, cudaMemcpyDeviceToDevice, s);
-  if (e == cudaSuccess)
-    e = cudaMemcpyAsync(aux + kCodebookBytes, a.scales, 2 * a.N, cudaMemcpyDeviceToDevice, s);
+  // the codebook pairs (one per segment), then the row scales
+  const int64_t cb_bytes = int64_t(kCodebookBytes) * (a.seg_of_rt != nullptr ? a.nseg : 1);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(aux, a.codebooks, cb_bytes, cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(aux + cb_bytes, a.scales, 2 * a.N, cudaMemcpyDeviceToDevice, s);
   return e;
 }
 
-cudaError_t dequant(const uint8_t* tiles, const void* aux, const int32_t*, int64_t N, int64_t K, int nKT,
+cudaError_t dequant(const uint8_t* tiles, const void* aux, const int32_t* seg_of_rb, int64_t N, int64_t K, int nKT,
                     float* w_out, int, cudaStream_t s) {
-  dequant_kernel<<<grid_for(N * (K / 8)), 256, 0, s>>>(tiles, static_cast<const uint8_t*>(aux), N, K,
+  dequant_kernel<<<grid_for(N * (K / 8)), 256, 0, s>>>(tiles, static_cast<const uint8_t*>(aux), seg_of_rb, N, K,
                                                        nKT, w_out);
   return cudaGetLastError();
 }

@@ -73,7 +73,7 @@ struct RunParams {
   float* y;              // [M][N] fp32
   float* partials;       // [gridDim.x][2][partial stride], all ones between calls
   const CtaPlan* plan;   // [gridDim.x]
-  const int32_t* seg_of_rt;  // stacked table formats: [row tiles] segment of each; else null
+  const int32_t* seg_of_rt;  // stacked table formats and AQLM 2x8: [row tiles] segment of each; else null
   int* err;              // error word (kErr* bits)
   const void* aux;       // format data (codebooks ...)
   int64_t N, K;

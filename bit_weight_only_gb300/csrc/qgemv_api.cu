@@ -233,7 +233,7 @@ struct qgemv_ctx {
   float* partials;
   qgemv::CtaPlan* plan;     // [grid], then [grid_m1] for the M = 1 kernel if that grid differs
   qgemv::CtaPlan* plan_m1;
-  int32_t* seg_of_rt;  // inside aux (table formats), else nullptr
+  int32_t* seg_of_rt;  // inside aux (stacked table formats and AQLM 2x8), else nullptr
   int* err;
   int batch_invariant;  // qgemv_set_batch_invariant
   int x_int8;           // qgemv_set_x_int8 (PQ2_0)
@@ -423,16 +423,21 @@ static qgemv_handle create_impl(int format, int64_t N, int64_t K, const void* pa
   // by the row tiles' segments
   const bool stacked = ops->cb_entries > 0 && (nseg > 1 || ops->row_tables);
   const int64_t table_bytes = int64_t(2) * ops->cb_entries * (stacked ? h->nRT : 1) * (glu_tables ? 2 : 1);
+  // a stacked AQLM 2x8 handle: its segments' codebook pairs, the row scales,
+  // then the segment of every 2048-row block (aligned to 4 bytes)
+  const bool aqlm_stacked = format == QGEMV_AQLM_2X8 && nseg > 1;
+  const int64_t aux_fixed = ops->aux_bytes * (aqlm_stacked ? nseg : 1) + ops->aux_per_row * N;
+  const int64_t seg_map_off = (aux_fixed + 3) / 4 * 4;
   const int64_t aux_bytes = ops->cb_entries > 0 ? table_bytes + (stacked ? 4 * h->nRT : 0)
-                                                : ops->aux_bytes + ops->aux_per_row * N;
+                                                : (aqlm_stacked ? seg_map_off + 4 * h->nRT : aux_fixed);
   if (e == cudaSuccess && aux_bytes > 0) e = dev_alloc(&h->aux, static_cast<size_t>(aux_bytes));
   if (e == cudaSuccess)
     e = dev_alloc(reinterpret_cast<void**>(&h->partials),
                   sizeof(float) * 2 * ops->partial_stride * static_cast<size_t>(slots_grid));
   if (e == cudaSuccess) e = dev_alloc(reinterpret_cast<void**>(&h->plan), sizeof(qgemv::CtaPlan) * n_plans);
   if (e == cudaSuccess) e = dev_alloc(reinterpret_cast<void**>(&h->err), sizeof(int));
-  if (e == cudaSuccess && stacked) {
-    h->seg_of_rt = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(h->aux) + table_bytes);
+  if (e == cudaSuccess && (stacked || aqlm_stacked)) {
+    h->seg_of_rt = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(h->aux) + (stacked ? table_bytes : seg_map_off));
     e = cudaMemcpy(h->seg_of_rt, seg_of_rt.data(), 4 * seg_of_rt.size(), cudaMemcpyHostToDevice);
   }
   if (e == cudaSuccess) {
@@ -472,7 +477,9 @@ static qgemv_handle create_impl(int format, int64_t N, int64_t K, const void* pa
   cudaFree(d_packed);
   cudaFree(d_scales);
   cudaFree(d_cb);
-  if (format == QGEMV_AQLM_2X8) {
+  // The tensor-core companion has one codebook pair; a stacked handle runs
+  // the table kernel at every M instead (passes of two rows).
+  if (format == QGEMV_AQLM_2X8 && !aqlm_stacked) {
     h->mma = create_impl(kAqlmMma, N, K, packed, scales, codebooks, 1, seg_rows, true);
     if (!h->mma) {  // the error is set
       free_handle(h);
@@ -502,8 +509,7 @@ qgemv_handle qgemv_create_stacked(int format, int nseg, const int64_t* seg_rows,
     set_error(QGEMV_ERR_ARG, "unknown format %d", format);
     return nullptr;
   }
-  if (format == QGEMV_AQLM_2X8 || format == kAqlmMma || format == QGEMV_AQLM_1X16 || format == QGEMV_CBK4_ROW ||
-      format == QGEMV_CBK8_ROW) {
+  if (format == kAqlmMma || format == QGEMV_AQLM_1X16 || format == QGEMV_CBK4_ROW || format == QGEMV_CBK8_ROW) {
     set_error(QGEMV_ERR_ARG, "format %d cannot be stacked", format);
     return nullptr;
   }
@@ -520,7 +526,9 @@ qgemv_handle qgemv_create_stacked(int format, int nseg, const int64_t* seg_rows,
     }
     N += seg_rows[s];
   }
-  return create_impl(format, N, K, packed, scales, codebooks, ops->cb_entries > 0 ? nseg : 1, seg_rows);
+  // codebook formats keep a codebook (AQLM 2x8: a codebook pair) per segment
+  const bool per_seg_cb = ops->cb_entries > 0 || format == QGEMV_AQLM_2X8;
+  return create_impl(format, N, K, packed, scales, codebooks, per_seg_cb ? nseg : 1, seg_rows);
 }
 
 qgemv_handle qgemv_create_glu(int format, int64_t N, int64_t K, const void* packed_gate, const void* packed_up,

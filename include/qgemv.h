@@ -123,17 +123,24 @@ qgemv_handle qgemv_create(int format, int64_t N, int64_t K, const void* packed,
  * projection.  The pages fuse such projections in their runtimes; this call
  * has no further counterpart there.
  *   nseg >= 1 segments; segment s has seg_rows[s] > 0 output rows, and every
- *     segment but the last must have a multiple of 128 rows (the prepared
- *     tile height), so that no tile mixes two codebooks.
+ *     segment but the last must have a multiple of the prepared tile height
+ *     (128 rows; AQLM 2x8: 2048, its row block), so that no tile mixes two
+ *     codebooks.
  *   packed: the segments' canonical bytes one after the other, which is the
  *     canonical layout of the stacked matrix (rows of all formats are
  *     independent).
- *   codebooks (CBK4, CBK8): nseg codebooks one after the other (16 or 256
- *     fp16 each); segment s decodes with codebook s.  NULL for Q4_0 and
- *     PQ2_0, whose stacked handle is the plain concatenation.
- *   AQLM 2x8, AQLM 1x16, CBK4_ROW and CBK8_ROW are not accepted
- *   (QGEMV_ERR_ARG; the rows of a per-row-codebook matrix carry their own
- *   codebooks, so one handle over the concatenated rows does the same).
+ *   codebooks (CBK4, CBK8, AQLM 2x8): nseg codebooks one after the other
+ *     (16 or 256 fp16 each; AQLM 2x8: a [2][256][8] fp16 pair each); segment
+ *     s decodes with codebook s.  NULL for Q4_0 and PQ2_0, whose stacked
+ *     handle is the plain concatenation.
+ *   scales (AQLM 2x8): the N row scales of all segments in order.
+ *   A stacked AQLM 2x8 handle runs its per-group-table kernel at every M (a
+ *     pass per two activation rows), without the tensor-core form that a
+ *     single-matrix handle uses from M = 3.
+ *   AQLM 1x16, CBK4_ROW and CBK8_ROW are not accepted (QGEMV_ERR_ARG; 1x16
+ *   keeps one 1 MiB codebook per handle, and the rows of a per-row-codebook
+ *   matrix carry their own codebooks, so one handle over the concatenated
+ *   rows does the same).
  * Host or device pointers, copying, errors: as for qgemv_create.             */
 qgemv_handle qgemv_create_stacked(int format, int nseg, const int64_t* seg_rows, int64_t K,
                                   const void* packed, const void* scales, const void* codebooks);

@@ -109,8 +109,9 @@ def test_stacked_create_rejects_bad_arguments_on_host(lib):
     assert not lib.qgemv_create_stacked(qgemv.CBK4, 0, rows, 256, 1, None, 1)
     assert qgemv.qgemv_last_error_code() == qgemv.QGEMV_ERR_ARG
     ok_rows = (ctypes.c_int64 * 2)(2048, 2048)
-    assert not lib.qgemv_create_stacked(qgemv.AQLM_2X8, 2, ok_rows, 256, 1, 1, 1)
-    assert "cannot be stacked" in qgemv.qgemv_last_error()
+    aqlm_rows = (ctypes.c_int64 * 2)(1024, 2048)  # AQLM 2x8 segments start on 2048-row blocks
+    assert not lib.qgemv_create_stacked(qgemv.AQLM_2X8, 2, aqlm_rows, 256, 1, 1, 1)
+    assert "multiple of 2048" in qgemv.qgemv_last_error()
     assert not lib.qgemv_create_stacked(99, 1, ok_rows, 256, 1, None, None)
     assert "unknown format" in qgemv.qgemv_last_error()
     assert not lib.qgemv_create_stacked(qgemv.AQLM_1X16, 2, ok_rows, 256, 1, 1, 1)

@@ -109,3 +109,107 @@ def test_stacked_rejects_bad_segments():
     cb = np.concatenate([inputs.cbk_centroids(16)] * 2)
     with pytest.raises(qgemv.QgemvError, match="multiple of 128"):
         qgemv.QGemv.stacked("cbk4", [100, 200], K, packed, None, cb)
+
+
+# ------------------------------------------------------------- AQLM 2x8 --
+# Segments start on the table kernel's 2048-row blocks; each has its own
+# codebook pair and its rows their own scales.
+
+def aqlm_segment_case(seg_rows, K, tag):
+    codes, scales, cbs = [], [], []
+    for s, rows in enumerate(seg_rows):
+        c, sc, cb = inputs.aqlm_inputs(inputs.rng(f"{tag}/aqlm/{s}/{rows}x{K}"), rows, K)
+        codes.append(c)
+        scales.append(sc)
+        cbs.append(cb)
+    return codes, scales, cbs
+
+
+def aqlm_handle(seg_rows, K, codes, scales, cbs):
+    return qgemv.QGemv.stacked("aqlm_2x8", seg_rows, K, np.concatenate(codes), np.concatenate(scales),
+                               np.concatenate(cbs))
+
+
+def aqlm_oracle(seg_rows, K, codes, scales, cbs, x):
+    ys, bs = [], []
+    for s, rows in enumerate(seg_rows):
+        y, b = oracle.gemv("aqlm_2x8", rows, K, codes[s], scales[s], cbs[s], x)
+        ys.append(y)
+        bs.append(b)
+    return np.concatenate(ys, axis=1), np.concatenate(bs, axis=1)
+
+
+def aqlm_dequant_ref(seg_rows, K, codes, scales, cbs):
+    return np.concatenate([oracle.dequant("aqlm_2x8", r, K, codes[s], scales[s], cbs[s])
+                           for s, r in enumerate(seg_rows)], axis=0)
+
+
+AQLM_CASES = [
+    ([2048, 2048, 700], 1032),       # ragged last segment and last chunk
+    ([2048] * 5 + [300], 4096),      # CTA runs cross row blocks of different segments
+    ([4096, 2048], 256),             # a segment of two row blocks
+]
+
+
+@pytest.mark.parametrize("seg_rows, K", AQLM_CASES)
+@pytest.mark.parametrize("M", [1, 2, 3, 5])
+def test_stacked_aqlm_matches_oracle_per_segment(seg_rows, K, M):
+    codes, scales, cbs = aqlm_segment_case(seg_rows, K, "stka")
+    h = aqlm_handle(seg_rows, K, codes, scales, cbs)
+    x = make_x(M, K, tag="stka")
+    y = h.gemv(torch.from_numpy(x).cuda())
+    torch.cuda.synchronize()
+    assert h.status() == qgemv.QGEMV_OK
+    y_ref, bound = aqlm_oracle(seg_rows, K, codes, scales, cbs, x)
+    ok = oracle.within_tolerance(y.cpu().numpy(), y_ref, bound)
+    assert ok.all(), f"M={M}: {np.count_nonzero(~ok)} outputs out of tolerance"
+
+
+@pytest.mark.parametrize("seg_rows, K", AQLM_CASES)
+def test_stacked_aqlm_dequant_bit_exact(seg_rows, K):
+    codes, scales, cbs = aqlm_segment_case(seg_rows, K, "stkadq")
+    h = aqlm_handle(seg_rows, K, codes, scales, cbs)
+    w = h.dequant().cpu().numpy()
+    ref = aqlm_dequant_ref(seg_rows, K, codes, scales, cbs)
+    assert np.array_equal(w, ref.astype(np.float32))  # the exact value rounded once
+
+
+@pytest.mark.parametrize("per_call", [1, 7])
+def test_stacked_aqlm_one_hot_columns_bit_exact(per_call):
+    """x = e_k returns column k of the stacked matrix, rounded once to fp32,
+    from one-row calls and from calls of several rows (passes of two)."""
+    seg_rows, K = [2048, 2048, 513], 1032
+    codes, scales, cbs = aqlm_segment_case(seg_rows, K, "stkaoh")
+    h = aqlm_handle(seg_rows, K, codes, scales, cbs)
+    W = aqlm_dequant_ref(seg_rows, K, codes, scales, cbs)
+    cols = [0, 7, 8, 127, 128, 1023, 1024, 1031]
+    for i0 in range(0, len(cols), per_call):
+        chunk = cols[i0:i0 + per_call]
+        x = np.zeros((len(chunk), K), dtype=np.float16)
+        for i, k in enumerate(chunk):
+            x[i, k] = 1.0
+        y = h.gemv(torch.from_numpy(x).cuda()).cpu().numpy()
+        for i, k in enumerate(chunk):
+            assert np.array_equal(y[i], W[:, k].astype(np.float32)), f"column {k}"
+
+
+def test_stacked_aqlm_batch_invariant_rows():
+    seg_rows, K = [2048, 1000], 1032
+    codes, scales, cbs = aqlm_segment_case(seg_rows, K, "stkainv")
+    h = aqlm_handle(seg_rows, K, codes, scales, cbs)
+    h.set_batch_invariant(True)
+    x = torch.from_numpy(make_x(9, K, tag="stkainv")).cuda()
+    y9 = h.gemv(x)
+    for M in (1, 2, 3):
+        yM = h.gemv(x[:M])
+        torch.cuda.synchronize()
+        assert torch.equal(yM, y9[:M]), f"M={M} rows differ from the M=9 call"
+    y_ref, bound = aqlm_oracle(seg_rows, K, codes, scales, cbs, x.cpu().numpy())
+    assert oracle.within_tolerance(y9.cpu().numpy(), y_ref, bound).all()
+
+
+def test_stacked_aqlm_rejects_unaligned_segments():
+    seg_rows, K = [1024, 1024], 256
+    codes, scales, cbs = aqlm_segment_case(seg_rows, K, "stkabad")
+    with pytest.raises(qgemv.QgemvError, match="multiple of 2048"):
+        aqlm_handle(seg_rows, K, codes, scales, cbs)
