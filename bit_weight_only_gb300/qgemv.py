@@ -259,7 +259,9 @@ class QGemv:
     @classmethod
     def stacked(cls, fmt, seg_rows, K: int, packed, scales=None, codebooks=None):
         """One handle over projections with the same K (rows stacked in
-        order, codebook s for segment s): one run computes them all."""
+        order, codebook s for segment s; AQLM 2x8: a codebook pair per
+        segment, the N row scales in order, segments on 2048-row blocks):
+        one run computes them all."""
         self = cls.__new__(cls)
         self.fmt, self.N, self.K = _fmt(fmt), int(sum(seg_rows)), int(K)
         p, kp = _addr(packed)
