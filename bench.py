@@ -202,6 +202,13 @@ def canonical_extra_bytes(fmt, N):
             "aqlm_1x16": 2 * N + 65536 * 8 * 2, "cbk4_row": 64 * N, "cbk8_row": 1024 * N}[fmt]
 
 
+def stacked_extra_bytes(fmt, segs):
+    """Codebooks and scales of a stacked handle's canonical inputs: those of
+    its segments as separate matrices (a codebook, or AQLM's pair, per
+    segment; one scale per row)."""
+    return sum(canonical_extra_bytes(fmt, n) for n in segs)
+
+
 def build_handles(specs, M, device, seed=0):
     """Create one handle per projection from device-drawn canonical inputs."""
     import torch
@@ -224,19 +231,17 @@ def build_handles(specs, M, device, seed=0):
                 packed = torch.cat([inputs.cbk_packed_cuda(f"{tag}/{s}", n, K, 4, p16, device, seed)
                                     for s, n in enumerate(segs)])
                 h = qgemv.QGemv.stacked(fmt, segs, K, packed, None, np.concatenate([c16] * len(segs)))
-                extra = canonical_extra_bytes(fmt, sum(segs)) * len(segs)
             elif fmt == "aqlm_2x8":  # codes, scales and a codebook pair per segment
                 parts = [inputs.aqlm_inputs_cuda(f"{tag}/{s}", n, K, device=device, seed=seed)
                          for s, n in enumerate(segs)]
                 packed = torch.cat([q[0] for q in parts])
                 h = qgemv.QGemv.stacked(fmt, segs, K, packed, torch.cat([q[1] for q in parts]),
                                         torch.cat([q[2] for q in parts]))
-                extra = 2 * sum(segs) + 8192 * len(segs)
                 del parts
             else:
                 raise ValueError(fmt)
             N = sum(segs)
-            nbytes = qgemv.qgemv_packed_bytes(fmt, N, K) + extra + 2 * M * K + 4 * M * N
+            nbytes = qgemv.qgemv_packed_bytes(fmt, N, K) + stacked_extra_bytes(fmt, segs) + 2 * M * K + 4 * M * N
             del packed
             x = x_all[xo:xo + M * K].view(M, K)
             x.copy_(inputs.x_fp16_cuda(f"{tag}/x", M, K, device=device, seed=seed))
