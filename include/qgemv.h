@@ -201,8 +201,11 @@ int qgemv_run_residual(qgemv_handle h, const void* x, int M, float* y, const flo
  * M = 2..8 run faster kernel geometries (and AQLM 2x8 with M <= 2 its
  * per-group table path), whose bits may differ in the last places (all
  * within the accuracy bound).  On, every M runs the tensor-core kernel's
- * default geometry (AQLM 2x8: its tensor-core layout).  Takes effect for
- * runs issued after the call; returns QGEMV_ERR_ARG for an invalid handle. */
+ * default geometry (AQLM 2x8: its tensor-core layout; a stacked AQLM 2x8
+ * handle: a one-row pass of its table kernel per row; CBK4_ROW: launches of
+ * at most two rows; AQLM 1x16 and CBK8_ROW are batch invariant in either
+ * mode).  Takes effect for runs issued after the call; returns
+ * QGEMV_ERR_ARG for an invalid handle. */
 int qgemv_set_batch_invariant(qgemv_handle h, int on);
 
 /* INT8 activations for a PQ2_0 handle (off by default): the integer path of
